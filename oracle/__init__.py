@@ -1,0 +1,151 @@
+"""CPU oracle for the int4 weight-only hot path (TEST INFRASTRUCTURE ONLY).
+
+Only tests/, the package smoke check and bench.py's CPU-baseline leg may
+import this package.  The product library never imports, links or calls it,
+and it shares no code with the CUDA path.  The arithmetic lives in
+w4_oracle.c (plain C, fp64 products); this module only marshals numpy
+arrays through ctypes.
+
+Every function is pinned against facts the source pages fix, in
+tests/test_oracle_pins.py.
+"""
+import ctypes
+import numpy as np
+
+from .build import build_oracle
+
+_lib = None
+
+F32, BF16 = 0, 1
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build_oracle())
+        P = ctypes.c_void_p
+        L = ctypes.c_long
+        lib.w4o_gemv.argtypes = [P, P, P, P, ctypes.c_int, L, L, L, L, L, P, P]
+        lib.w4o_gemv.restype = None
+        lib.w4o_gemm_at.argtypes = [P, P, P, P, L, L, L, P, P, L, P, P]
+        lib.w4o_gemm_at.restype = None
+        lib.w4o_quantize_pack.argtypes = [P, L, L, P, P]
+        lib.w4o_quantize_pack.restype = None
+        lib.w4o_permute.argtypes = [P, L, L, P]
+        lib.w4o_permute.restype = ctypes.c_int
+        _lib = lib
+    return _lib
+
+
+def _ptr(a):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _act(a, dtype):
+    """Return a C-contiguous array of the raw element type for `dtype`."""
+    if dtype == BF16:
+        a = np.ascontiguousarray(a)
+        if a.dtype != np.uint16:
+            raise TypeError("bf16 operands are passed as raw uint16 bit patterns")
+        return a
+    return np.ascontiguousarray(a, dtype=np.float32)
+
+
+def gemv(packed_weights, scales, zeros, x, act_dtype, rows=None):
+    """d[c, r] = sum_k x[c, k] * (q[r, k] - zero[r]) * scale[r], in fp64.
+
+    packed_weights: uint32 [N, K/8] (nibble j of word i is k = 8i + j).
+    scales, zeros: [N]; x: [C, K]; fp32 arrays, or uint16 bf16 bit patterns
+    when act_dtype == BF16.  rows: optional (begin, end) row range; rows
+    outside it are left as NaN.  Returns (d, ref_abs), both float64 [C, N].
+    """
+    lib = _load()
+    qw = np.ascontiguousarray(packed_weights, dtype=np.uint32)
+    N, kb = qw.shape
+    K = kb * 8
+    x = _act(x, act_dtype)
+    if x.ndim == 1:
+        x = x.reshape(1, -1)
+    C = x.shape[0]
+    if x.shape[1] != K:
+        raise ValueError("x has %d columns, weights imply K=%d" % (x.shape[1], K))
+    s = _act(scales, act_dtype)
+    z = _act(zeros, act_dtype)
+    if s.shape != (N,) or z.shape != (N,):
+        raise ValueError("scales/zeros must be [N]")
+    r0, r1 = (0, N) if rows is None else rows
+    d = np.full((C, N), np.nan)
+    ref = np.full((C, N), np.nan)
+    lib.w4o_gemv(_ptr(qw), _ptr(s), _ptr(z), _ptr(x), act_dtype, N, K, C, r0, r1,
+                 _ptr(d), _ptr(ref))
+    return d, ref
+
+
+def gemm_at(A_bits, B_packed, scale_bits, zero_bits, m_idx, n_idx):
+    """C[m, n] = sum_k A[m, k] * (u[k, n] - zero[n]) * scale[n] at the given
+    coordinates, in fp64.
+
+    A_bits: uint16 bf16 patterns [M, K]; B_packed: uint8 [K/2, N] (low nibble
+    = even k, unsigned); scale_bits, zero_bits: uint16 bf16 patterns [N].
+    Returns (c, ref_abs) float64 arrays shaped like m_idx.
+    """
+    lib = _load()
+    A = np.ascontiguousarray(A_bits, dtype=np.uint16)
+    B = np.ascontiguousarray(B_packed, dtype=np.uint8)
+    M, K = A.shape
+    if B.shape[0] * 2 != K:
+        raise ValueError("B must be [K/2, N]")
+    N = B.shape[1]
+    s = np.ascontiguousarray(scale_bits, dtype=np.uint16)
+    z = np.ascontiguousarray(zero_bits, dtype=np.uint16)
+    mi = np.ascontiguousarray(m_idx, dtype=np.int64).ravel()
+    ni = np.ascontiguousarray(n_idx, dtype=np.int64).ravel()
+    if mi.shape != ni.shape:
+        raise ValueError("m_idx and n_idx differ in size")
+    if mi.size and (mi.min() < 0 or mi.max() >= M or ni.min() < 0 or ni.max() >= N):
+        raise IndexError("coordinate out of range")
+    c = np.empty(mi.shape, np.float64)
+    ref = np.empty(mi.shape, np.float64)
+    lib.w4o_gemm_at(_ptr(A), _ptr(B), _ptr(s), _ptr(z), M, N, K, _ptr(mi), _ptr(ni),
+                    mi.size, _ptr(c), _ptr(ref))
+    shape = np.shape(m_idx)
+    return c.reshape(shape), ref.reshape(shape)
+
+
+def gemm_full(A_bits, B_packed, scale_bits, zero_bits):
+    """Every element of C (small shapes only)."""
+    M = np.shape(A_bits)[0]
+    N = np.shape(B_packed)[1]
+    mm, nn = np.meshgrid(np.arange(M), np.arange(N), indexing="ij")
+    return gemm_at(A_bits, B_packed, scale_bits, zero_bits, mm, nn)
+
+
+def quantize_pack(W_bits):
+    """Symmetric per-column int4 quantisation + column pack.
+
+    W_bits: uint16 bf16 patterns [K, N], K even.  Returns (scale float32 [N],
+    packed uint8 [K/2, N]).
+    """
+    lib = _load()
+    W = np.ascontiguousarray(W_bits, dtype=np.uint16)
+    K, N = W.shape
+    if K % 2:
+        raise ValueError("K must be even")
+    scale = np.empty(N, np.float32)
+    packed = np.empty((K // 2, N), np.uint8)
+    lib.w4o_quantize_pack(_ptr(W), K, N, _ptr(scale), _ptr(packed))
+    return scale, packed
+
+
+def permute(packed, K, N):
+    """Page-1 int4 permute of packed [K/2, N] into N*K/2 interleaved bytes."""
+    lib = _load()
+    p = np.ascontiguousarray(packed, dtype=np.uint8)
+    if p.shape != (K // 2, N):
+        raise ValueError("packed must be [K/2, N]")
+    if K % 64 or N % 4:
+        raise ValueError("permute needs K % 64 == 0 and N % 4 == 0")
+    out = np.zeros(N * K // 2, np.uint8)
+    if lib.w4o_permute(_ptr(p), K, N, _ptr(out)) != 0:
+        raise MemoryError("oracle permute could not allocate its stream")
+    return out

@@ -1,0 +1,224 @@
+/*
+ * w4_oracle.c -- plain, slow, obviously-correct CPU oracle for the int4
+ * weight-only hot path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product library may include,
+ * link or call this file; only the tests, the package smoke check and the
+ * benchmark's CPU-baseline leg use it.  It shares no code, table, constant
+ * or helper with the CUDA path.
+ *
+ * Every product is computed in IEEE double from the exact values of its
+ * inputs (bf16 and fp32 convert to double exactly), so the only rounding
+ * is the double accumulation itself.  The quantizer is the one place where
+ * fp32 arithmetic is part of the definition (it decides an integer), and
+ * there it is done in fp32, exactly as the reading below states.
+ *
+ * Sources (web pages on int4 weight-only quantisation, cited by page title
+ * and section):
+ *   [P1] "[PHI] add int4 weight only quant kernel, add int4 weight only
+ *        permute kernel" (Paddle PR #64091): sections "int4量化kernel",
+ *        "int4 permute kernel", "如何从int8 permute转换为int4 permute",
+ *        "简单的位运算", "int4 row interval".
+ *   [P2] "怎样在安卓端利用 Vulkan 编写 4-bit 专用算子" (Vulkan 4-bit GEMV blog):
+ *        section 1 "数据打包策略", section 2 "核心 GLSL 算子实现".
+ *   [P3] "int4 gemm kernel" (pytorch/helion issue #508): the
+ *        matmul_bf16_int4 example.
+ *   [P4] "三值量化模型的无损压缩" (ternary compression blog): section 3 "MMVQ",
+ *        the batched GEMV definition d[r,c] = sum_k W[r,k] x[c,k].
+ *
+ * Parity pins for every function live in tests/test_oracle_pins.py.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* Element type codes for activations/scales/zeros. */
+#define W4O_F32 0
+#define W4O_BF16 1
+
+int w4o_abi_version(void) { return 1; }
+
+/* bf16 is the upper half of an IEEE binary32: widen by appending 16 zero
+ * bits.  Exact. */
+static float bf16_bits_to_float(uint16_t h) {
+    uint32_t u = ((uint32_t)h) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+static double load_elem(const void* base, int dtype, long i) {
+    if (dtype == W4O_BF16) return (double)bf16_bits_to_float(((const uint16_t*)base)[i]);
+    return (double)((const float*)base)[i];
+}
+
+/*
+ * Fused dequant GEMV, batched.
+ *
+ * [P2 section 2]: one output per row; the row's K weights are stored as K/8
+ * uint32 words, word i of row r at packed_weights[r*K/8 + i]; nibble j of a
+ * word is (word >> 4j) & 0xF and holds weight k = 8i + j ([P2 section 1]:
+ * packed = (w7<<28)|...|(w1<<4)|w0); the weight is dequantised as
+ * (q - zero[r]) * scale[r] and multiplied by vec_in[8i + j].
+ * [P4 section 3]: the batched form d[r,c] = sum_k W[r,k] x[c,k]; here x is
+ * [C][K] row-major and the result is stored d[c*N + r].
+ *
+ * Rows [row_begin, row_end) are computed.  ref_abs (may be NULL) receives
+ * sum_k |w * x| for each output, the denominator of the parity tolerance.
+ */
+void w4o_gemv(const uint32_t* packed_weights, const void* scales, const void* zeros,
+              const void* x, int act_dtype, long N, long K, long C,
+              long row_begin, long row_end, double* d, double* ref_abs) {
+    long k_blocks = K / 8;
+    for (long c = 0; c < C; ++c) {
+        for (long row = row_begin; row < row_end; ++row) {
+            double scale = load_elem(scales, act_dtype, row);
+            double zero = load_elem(zeros, act_dtype, row);
+            double sum = 0.0, abs_sum = 0.0;
+            for (long i = 0; i < k_blocks; ++i) {
+                uint32_t packed_val = packed_weights[row * k_blocks + i];
+                for (int j = 0; j < 8; ++j) {
+                    uint32_t val = (packed_val >> (j * 4)) & 0x0Fu;
+                    double w = ((double)val - zero) * scale;
+                    double xv = load_elem(x, act_dtype, c * K + i * 8 + j);
+                    sum += xv * w;
+                    abs_sum += fabs(xv * w);
+                }
+            }
+            d[c * N + row] = sum;
+            if (ref_abs) ref_abs[c * N + row] = abs_sum;
+        }
+    }
+}
+
+/*
+ * Large-M dequant GEMM, evaluated at a list of output coordinates.
+ *
+ * [P3]: A is (M, K) bf16 row-major; B is the packed (K/2, N) int8 matrix
+ * whose byte (kp, n) holds two int4 values along K: the low nibble
+ * (b & 0x0F) is k = 2kp and the high nibble ((b >> 4) & 0x0F) is
+ * k = 2kp + 1, both read as unsigned 0..15.  C[m, n] = sum_k A[m,k] *
+ * B[k,n].  The per-column zero and scale dequantise each unpacked value as
+ * (u - zero[n]) * scale[n] (the page's sketch has neither; the workload
+ * definition supplies both, bf16).
+ *
+ * For t in [0, count): c[t] = C[m_idx[t], n_idx[t]], ref_abs[t] (may be
+ * NULL) = sum_k |A * w|.
+ */
+void w4o_gemm_at(const uint16_t* A, const uint8_t* B, const uint16_t* scale,
+                 const uint16_t* zero, long M, long N, long K, const long* m_idx,
+                 const long* n_idx, long count, double* c, double* ref_abs) {
+    (void)M;
+    for (long t = 0; t < count; ++t) {
+        long m = m_idx[t], n = n_idx[t];
+        double s = (double)bf16_bits_to_float(scale[n]);
+        double z = (double)bf16_bits_to_float(zero[n]);
+        double acc = 0.0, abs_acc = 0.0;
+        for (long kp = 0; kp < K / 2; ++kp) {
+            uint8_t b = B[kp * N + n];
+            uint32_t b_lo = b & 0x0Fu;         /* k = 2kp     */
+            uint32_t b_hi = (b >> 4) & 0x0Fu;  /* k = 2kp + 1 */
+            double a0 = (double)bf16_bits_to_float(A[m * K + 2 * kp]);
+            double a1 = (double)bf16_bits_to_float(A[m * K + 2 * kp + 1]);
+            double w0 = ((double)b_lo - z) * s;
+            double w1 = ((double)b_hi - z) * s;
+            acc += a0 * w0 + a1 * w1;
+            abs_acc += fabs(a0 * w0) + fabs(a1 * w1);
+        }
+        c[t] = acc;
+        if (ref_abs) ref_abs[t] = abs_acc;
+    }
+}
+
+/*
+ * Weight-only int4 quantisation and column pack.
+ *
+ * Workload definition (symmetric, per output column n of W[K][N]):
+ *   scale[n] = max_k |W[k][n]| / 7           (fp32, IEEE division)
+ *   q[k][n]  = clamp(round(W[k][n] / scale[n]), -8, 7)
+ * with round = round half away from zero (C roundf) and the quotient an
+ * IEEE fp32 division; a column of zeros has scale 0 and q = 0.
+ * [P1 section "int4量化kernel"]: two int4 values are packed into one int8 by
+ * taking an upper and a lower row, i.e. the pack runs along columns:
+ * byte (k/2, n) holds rows k and k+1 of column n; the even row goes in the
+ * low nibble.  Nibbles are two's complement (q & 0xF).
+ */
+void w4o_quantize_pack(const uint16_t* W, long K, long N, float* scale, uint8_t* packed) {
+    for (long n = 0; n < N; ++n) {
+        float amax = 0.0f;
+        for (long k = 0; k < K; ++k) {
+            float a = fabsf(bf16_bits_to_float(W[k * N + n]));
+            if (a > amax) amax = a;
+        }
+        float s = amax / 7.0f;
+        scale[n] = s;
+        for (long k = 0; k < K; k += 2) {
+            int q[2];
+            for (int h = 0; h < 2; ++h) {
+                float w = bf16_bits_to_float(W[(k + h) * N + n]);
+                float r = (s == 0.0f) ? 0.0f : roundf(w / s);
+                if (r < -8.0f) r = -8.0f;
+                if (r > 7.0f) r = 7.0f;
+                q[h] = (int)r;
+            }
+            packed[(k / 2) * N + n] =
+                (uint8_t)(((unsigned)q[0] & 0x0Fu) | (((unsigned)q[1] & 0x0Fu) << 4));
+        }
+    }
+}
+
+/*
+ * [P1 section "int4 permute kernel"]: destination of source byte t inside
+ * each 16-byte group of a column's byte stream (the "coordinates" of the
+ * mapping 0..15 -> 0 8 4 12 1 9 5 13 2 10 6 14 3 11 7 15).  Copied from the
+ * page; tests/test_oracle_pins.py re-derives it from the int8 permute_kk by
+ * the page's "% 8 * 2, add 1" steps.
+ */
+static const int k_permute_kk16[16] = {0, 4, 8, 12, 2, 6, 10, 14, 1, 5, 9, 13, 3, 7, 11, 15};
+
+/*
+ * int4 weight-only permute, [P1] steps in the page's order:
+ *   1. byte permute: source byte kk of column n's stream moves to
+ *      permute_kk = 16*(kk/16) + permute_kk16[kk%16]
+ *      (section "int4 permute kernel");
+ *   2. nibble swap: in each 4-byte group of the permuted stream, bytes 0/2
+ *      and 1/3 exchange low and high nibbles (section "简单的位运算");
+ *   3. row interleave: byte permute_kk of column n_id lands at
+ *      permute_kk % 32 + permute_kk / 32 * 128 + 32 * (n_id % 4)
+ *        + total_k * 4 * (n_id / 4)
+ *      (section "int4 row interval"), with total_k = K/2 counted in packed
+ *      bytes.
+ * Input: packed[K/2][N] (the quantizer's output).  Output: N*K/2 bytes.
+ * Requires K % 32 == 0 so that every 16-byte group is full; the
+ * interleave assumes N % 4 == 0 and K/2 % 32 == 0.  Returns 0, or -1 if
+ * the scratch stream cannot be allocated.
+ */
+int w4o_permute(const uint8_t* packed, long K, long N, uint8_t* out) {
+    long total_k = K / 2;
+    uint8_t* stream = (uint8_t*)malloc((size_t)(total_k > 0 ? total_k : 1));
+    if (!stream) return -1;
+    for (long n_id = 0; n_id < N; ++n_id) {
+        /* step 1 */
+        for (long kk = 0; kk < total_k; ++kk) {
+            long permute_kk = (kk / 16) * 16 + k_permute_kk16[kk % 16];
+            stream[permute_kk] = packed[kk * N + n_id];
+        }
+        /* step 2 */
+        for (long g = 0; g < total_k; g += 4) {
+            uint8_t b0 = stream[g], b1 = stream[g + 1], b2 = stream[g + 2], b3 = stream[g + 3];
+            stream[g + 0] = (uint8_t)((b0 & 0x0F) | ((b2 & 0x0F) << 4));
+            stream[g + 2] = (uint8_t)(((b0 >> 4) & 0x0F) | (b2 & 0xF0));
+            stream[g + 1] = (uint8_t)((b1 & 0x0F) | ((b3 & 0x0F) << 4));
+            stream[g + 3] = (uint8_t)(((b1 >> 4) & 0x0F) | (b3 & 0xF0));
+        }
+        /* step 3 */
+        for (long permute_kk = 0; permute_kk < total_k; ++permute_kk) {
+            long permute_index = permute_kk % 32 + permute_kk / 32 * 128 + 32 * (n_id % 4) +
+                                 total_k * 4 * (n_id / 4);
+            out[permute_index] = stream[permute_kk];
+        }
+    }
+    free(stream);
+    return 0;
+}

@@ -1,0 +1,111 @@
+"""Seeded synthetic inputs for the int4 weight-only workloads.
+
+Shared by the tests, the package smoke check and the benchmark.  This module
+holds none of the method's arithmetic: it only draws random bits and values
+with torch's CPU generator and casts dtypes.  Packed int4 operands are drawn
+directly as uniform random bytes, which is the same distribution as eight (or
+two) independent uniform 0..15 nibbles, so no packing code is needed here.
+
+Draw order for every workload is fixed (weights, scale, zero, activations)
+so the same seed gives the same bytes on every machine.
+"""
+from dataclasses import dataclass
+
+import numpy as np
+import torch
+
+# Workload shapes (synthetic stand-ins shaped like the pages' workloads: the
+# Qwen K values 5120, 6144 and 17280 of the MMVQ section, and the 8192^3
+# bf16 x int4 example of the Helion issue).
+TINY = dict(N=256, K=512, C=1, act="f32")
+DECODE = dict(N=17280, K=5120, C=1, act="bf16")
+SMALL_BATCH = [dict(N=5120, K=17280, C=4, act="bf16"), dict(N=5120, K=17280, C=8, act="bf16"),
+               dict(N=6144, K=5120, C=4, act="bf16"), dict(N=6144, K=5120, C=8, act="bf16")]
+QUANT = dict(K=8192, N=8192)
+GEMM = dict(M=8192, N=8192, K=8192)
+
+
+def _gen(seed):
+    return torch.Generator(device="cpu").manual_seed(int(seed))
+
+
+@dataclass
+class GemvInputs:
+    qweight: torch.Tensor  # int32 [N, K/8]: bit patterns of the packed uint32 words
+    scale: torch.Tensor    # [N] float32 or bfloat16
+    zero: torch.Tensor     # [N] same dtype as scale
+    x: torch.Tensor        # [C, K] same dtype as scale
+    N: int
+    K: int
+    C: int
+    act: str
+
+
+def gemv_inputs(N, K, C, act="bf16", seed=0, scale_range=None, zero_value=8.0):
+    """Packed uint4 weights uniform 0..15, per-row scale, constant zero, x ~ N(0,1).
+
+    act="bf16": scale U[0.001, 0.01], zero 8, x N(0,1), all bf16.
+    act="f32":  scale U[0.5, 2]/16, zero 8.0, x N(0,1), all fp32.
+    """
+    if K % 8:
+        raise ValueError("K must be a multiple of 8")
+    g = _gen(seed)
+    qbytes = torch.randint(0, 256, (N, K // 2), dtype=torch.uint8, generator=g)
+    qweight = qbytes.view(torch.int32)
+    if act == "f32":
+        lo, hi = scale_range or (0.5 / 16, 2.0 / 16)
+        dt = torch.float32
+    elif act == "bf16":
+        lo, hi = scale_range or (0.001, 0.01)
+        dt = torch.bfloat16
+    else:
+        raise ValueError(act)
+    scale = (torch.rand(N, generator=g, dtype=torch.float32) * (hi - lo) + lo).to(dt)
+    zero = torch.full((N,), float(zero_value), dtype=dt)
+    x = torch.randn(C, K, generator=g, dtype=torch.float32).to(dt)
+    return GemvInputs(qweight, scale, zero, x, N, K, C, act)
+
+
+def quant_inputs(K, N, seed=0, std=0.02):
+    """W bf16 [K, N] ~ N(0, std)."""
+    g = _gen(seed)
+    return (torch.randn(K, N, generator=g, dtype=torch.float32) * std).to(torch.bfloat16)
+
+
+@dataclass
+class GemmInputs:
+    A: torch.Tensor      # bf16 [M, K]
+    B: torch.Tensor      # uint8 [K/2, N]: two unsigned nibbles per byte along K
+    scale: torch.Tensor  # bf16 [N]
+    zero: torch.Tensor   # bf16 [N]
+    M: int
+    N: int
+    K: int
+
+
+def gemm_inputs(M, N, K, seed=0, scale_value=0.01, zero_value=8.0, random_scale=False):
+    """A ~ N(0,1) bf16; B uniform bytes; zero 8; scale 0.01 (or U[0.005,0.02])."""
+    if K % 2:
+        raise ValueError("K must be even")
+    g = _gen(seed)
+    A = torch.randn(M, K, generator=g, dtype=torch.float32).to(torch.bfloat16)
+    B = torch.randint(0, 256, (K // 2, N), dtype=torch.uint8, generator=g)
+    if random_scale:
+        scale = (torch.rand(N, generator=g) * 0.015 + 0.005).to(torch.bfloat16)
+    else:
+        scale = torch.full((N,), float(scale_value), dtype=torch.bfloat16)
+    zero = torch.full((N,), float(zero_value), dtype=torch.bfloat16)
+    return GemmInputs(A, B, scale, zero, M, N, K)
+
+
+def np_bits(t):
+    """numpy view of a CPU tensor's raw bits: bf16 -> uint16, int32 -> uint32,
+    uint8 -> uint8, float32 -> float32."""
+    t = t.detach().contiguous().cpu()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view(np.uint16)
+    if t.dtype == torch.int32:
+        return t.numpy().view(np.uint32)
+    if t.dtype == torch.int8:
+        return t.numpy().view(np.uint8)
+    return t.numpy()

@@ -1,0 +1,325 @@
+"""Pins of the CPU oracle against what the source pages and mathematics fix.
+
+Every oracle function is checked here against something other than itself:
+the worked sequences printed on the Paddle permute page (tests/golden), the
+packing order stated on the Vulkan GEMV page, closed forms, special cases
+that reduce to a library matmul, and invariants.  A plausible mistake in the
+oracle (a swapped nibble, a transposed operand, a dropped zero or scale, a
+wrong rounding mode) fails at least one of these.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from helpers import bf16_bits, bf16_values, load_golden
+
+G = load_golden("p1_permute_sequences.txt")
+
+
+# ---------------------------------------------------------------------------
+# Page-internal consistency of the permute derivation (these fix our reading
+# of the page before the oracle is trusted with it).
+# ---------------------------------------------------------------------------
+
+def test_page_permute_kk_derivation_from_int8():
+    """int8 permute_kk -> regroup -> %8*2 -> +1 on the second half = int4 permute_kk."""
+    int8 = G["permute_kk_int8"]
+    regrouped = G["permute_kk_int8_regrouped"]
+    # the regrouping exchanges the second and third quarters
+    assert regrouped == int8[0:4] + int8[8:12] + int8[4:8] + int8[12:16]
+    mod = [(v % 8) * 2 for v in regrouped]
+    assert mod == G["permute_kk_mod8x2"]
+    int4 = [v + (1 if t >= 8 else 0) for t, v in enumerate(mod)]
+    assert int4 == G["permute_kk_int4"]
+
+
+def test_page_permute_kk_is_scatter_of_byte_order():
+    """Moving source byte t to permute_kk[t] lays the bytes out in byte_order."""
+    dst = G["permute_kk_int4"]
+    assert sorted(dst) == list(range(16))
+    laid = [None] * 16
+    for t, d in enumerate(dst):
+        laid[d] = t
+    assert laid == G["byte_order"]
+
+
+def test_page_byte_order_matches_pair_order():
+    pairs = G["byte_pair_order"]
+    assert [pairs[2 * i] // 2 for i in range(16)] == G["byte_order"]
+    assert all(pairs[2 * i + 1] == pairs[2 * i] + 1 for i in range(16))
+
+
+def test_page_fast_dequant_maps_pre_order_to_fragment_order():
+    slots = G["fast_dequant_slots"]          # slot i holds element slots[i]
+    pre = G["pre_dequant_order"]
+    out = []
+    for w in range(4):
+        word = pre[8 * w:8 * w + 8]
+        elem = [None] * 8
+        for i in range(8):
+            elem[slots[i]] = word[i]
+        out += elem
+    assert out == G["fragment_order"]
+
+
+# ---------------------------------------------------------------------------
+# Oracle permute, traced with nibble labels.
+# ---------------------------------------------------------------------------
+
+def _pack_rows(vals):
+    """Two rows per byte along K, even row in the low nibble (the pack the
+    quantiser page describes and the workload definition fixes)."""
+    vals = np.asarray(vals, dtype=np.int64)
+    return ((vals[0::2] & 0xF) | ((vals[1::2] & 0xF) << 4)).astype(np.uint8)
+
+
+def _trace_permute(K, N):
+    """Run the oracle permute on 4-bit planes of unique nibble ids.
+
+    Returns src[pos] = id of the input nibble found at output nibble
+    position pos (pos = 2*byte + (0 for low, 1 for high)); id = k*N + n.
+    Valid because the permute only moves nibbles and never looks at them.
+    """
+    ids = np.arange(K * N, dtype=np.int64).reshape(K, N)
+    planes = max(1, int(np.ceil(np.log2(K * N) / 4)))
+    src = np.zeros(N * K, dtype=np.int64)
+    for p in range(planes):
+        out = oracle.permute(_pack_rows((ids >> (4 * p)) & 0xF), K, N)
+        nib = np.empty(N * K, dtype=np.int64)
+        nib[0::2] = out & 0xF
+        nib[1::2] = out >> 4
+        src |= nib << (4 * p)
+    return src
+
+
+@pytest.mark.parametrize("K,N", [(64, 4), (128, 8), (256, 12)])
+def test_oracle_permute_matches_page_sequences(K, N):
+    src = _trace_permute(K, N)
+    assert np.array_equal(np.sort(src), np.arange(K * N)), "not a bijection"
+    k_of, n_of = src // N, src % N
+    runs_per_col = (K // 2) // 32          # 32-byte runs per column stream
+    pre = np.array(G["pre_dequant_order"])
+    frag = G["fragment_order"]
+    slots = G["fast_dequant_slots"]
+    for rho in range(N * K // 64):          # every 32-byte run of the output
+        seg = slice(64 * rho, 64 * rho + 64)  # its 64 nibbles
+        cols = set(n_of[seg].tolist())
+        # "in four adjacent rows, every 32 elements are interleaved":
+        # runs cycle through the four columns of a group, chunk by chunk
+        group, rem = divmod(rho, 4 * runs_per_col)
+        chunk, lane = divmod(rem, 4)
+        assert cols == {4 * group + lane}
+        ks = k_of[seg]
+        for h in range(2):                  # two 16-byte groups per run
+            g_k = ks[32 * h:32 * h + 32]
+            base = 64 * chunk + 32 * h
+            assert np.array_equal(g_k - base, pre), (rho, h)
+            # the consumer's fast dequant then yields the fragment order
+            out = []
+            for w in range(4):
+                word = (g_k - base)[8 * w:8 * w + 8].tolist()
+                elem = [None] * 8
+                for i in range(8):
+                    elem[slots[i]] = word[i]
+                out += elem
+            assert out == frag
+
+
+def test_oracle_permute_preserves_nibble_multiset():
+    """The permute only moves nibbles: the multiset of nibble values of any
+    input survives unchanged."""
+    K, N = 64, 4
+    rng = np.random.default_rng(1)
+    packed = rng.integers(0, 256, (K // 2, N), dtype=np.uint8)
+    out = oracle.permute(packed, K, N)
+    # nibble multiset is preserved
+    nib_in = np.concatenate([packed.ravel() & 0xF, packed.ravel() >> 4])
+    nib_out = np.concatenate([out & 0xF, out >> 4])
+    assert np.array_equal(np.bincount(nib_in, minlength=16), np.bincount(nib_out, minlength=16))
+
+
+# ---------------------------------------------------------------------------
+# Quantise + pack.
+# ---------------------------------------------------------------------------
+
+def _unpack_rows(packed):
+    """Inverse of the pack along K (even row = low nibble), sign-extended."""
+    lo = (packed & 0xF).astype(np.int64)
+    hi = (packed >> 4).astype(np.int64)
+    K2, N = packed.shape
+    q = np.empty((2 * K2, N), np.int64)
+    q[0::2], q[1::2] = lo, hi
+    return np.where(q >= 8, q - 16, q)
+
+
+def test_quantize_exact_grid():
+    """W = (k-7)/16: absmax 7/16 gives scale exactly 1/16 and q = k - 7."""
+    K = 16
+    col = np.array([(k - 7) / 16.0 for k in range(15)] + [0.0])
+    W = np.stack([col, -col, np.zeros(K), col * 2], axis=1)
+    scale, packed = oracle.quantize_pack(bf16_bits(W))
+    assert scale[0] == np.float32(1 / 16) and scale[1] == np.float32(1 / 16)
+    assert scale[2] == 0.0 and scale[3] == np.float32(1 / 8)
+    q = _unpack_rows(packed)
+    expect = np.array([k - 7 for k in range(15)] + [0])
+    assert np.array_equal(q[:, 0], expect)
+    assert np.array_equal(q[:, 1], -expect)
+    assert np.array_equal(q[:, 2], np.zeros(K))
+    assert np.array_equal(q[:, 3], expect)
+
+
+def test_quantize_rounds_half_away_from_zero():
+    # scale 1/16; w/s = 0.5, 1.5, 2.5, -0.5, -2.5 exactly
+    col = np.array([7, 0.5, 1.5, 2.5, -0.5, -2.5, 0, 0]) / 16.0
+    scale, packed = oracle.quantize_pack(bf16_bits(col.reshape(-1, 1)))
+    assert scale[0] == np.float32(1 / 16)
+    assert _unpack_rows(packed)[:, 0].tolist() == [7, 1, 2, 3, -1, -3, 0, 0]
+
+
+def test_quantize_pack_puts_even_row_in_low_nibble():
+    col = np.array([7, 1, -7, 2]) / 16.0        # q = 7, 1, -7, 2
+    _, packed = oracle.quantize_pack(bf16_bits(col.reshape(-1, 1)))
+    assert packed[:, 0].tolist() == [0x17, 0x29]   # -7 & 0xF = 9
+
+
+def test_quantize_invariants_random():
+    rng = np.random.default_rng(0)
+    K, N = 256, 48
+    W = bf16_bits(rng.normal(0, 0.02, (K, N)))
+    Wv = bf16_values(W)
+    scale, packed = oracle.quantize_pack(W)
+    amax = np.abs(Wv).max(axis=0)
+    assert np.array_equal(scale, (amax.astype(np.float32) / np.float32(7)))
+    q = _unpack_rows(packed)
+    assert q.min() >= -7 and q.max() <= 7           # symmetric absmax never hits -8
+    # each column's extreme maps to +-7
+    assert np.all(np.abs(q).max(axis=0) == 7)
+    err = np.abs(Wv - q * scale.astype(np.float64))
+    assert np.all(err <= scale.astype(np.float64) * (0.5 + 1e-6))
+    # sign symmetry of round-half-away
+    _, packed_neg = oracle.quantize_pack(W ^ np.uint16(0x8000))
+    assert np.array_equal(_unpack_rows(packed_neg), -q)
+
+
+# ---------------------------------------------------------------------------
+# GEMV.
+# ---------------------------------------------------------------------------
+
+def _pack_words(Q):
+    """packed = (w7<<28)|...|(w1<<4)|w0 along K, eight weights per uint32."""
+    N, K = Q.shape
+    Q = Q.astype(np.uint64).reshape(N, K // 8, 8)
+    words = np.zeros((N, K // 8), np.uint64)
+    for j in range(8):
+        words |= Q[:, :, j] << np.uint64(4 * j)
+    return words.astype(np.uint32)
+
+
+@pytest.mark.parametrize("act", [oracle.F32, oracle.BF16])
+def test_gemv_matches_dense_matmul(act):
+    rng = np.random.default_rng(2)
+    N, K, C = 24, 64, 3
+    Q = rng.integers(0, 16, (N, K))
+    s = rng.uniform(0.5, 2.0, N)
+    z = rng.uniform(6.0, 9.0, N)
+    x = rng.normal(0, 1, (C, K))
+    if act == oracle.BF16:
+        s, z, x = bf16_bits(s), bf16_bits(z), bf16_bits(x)
+        sv, zv, xv = bf16_values(s), bf16_values(z), bf16_values(x)
+    else:
+        s, z, x = s.astype(np.float32), z.astype(np.float32), x.astype(np.float32)
+        sv, zv, xv = s.astype(np.float64), z.astype(np.float64), x.astype(np.float64)
+    d, ref = oracle.gemv(_pack_words(Q), s, z, x, act)
+    W = (Q - zv[:, None]) * sv[:, None]
+    np.testing.assert_allclose(d, xv @ W.T, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(ref, np.abs(xv) @ np.abs(W).T, rtol=1e-12, atol=1e-12)
+
+
+def test_gemv_one_hot_picks_single_nibble():
+    N, K = 4, 16
+    Q = np.arange(N * K).reshape(N, K) % 16
+    s = np.full(N, 1.0, np.float32)
+    z = np.full(N, 8.0, np.float32)
+    for k in range(K):
+        x = np.zeros((1, K), np.float32)
+        x[0, k] = 1.0
+        d, _ = oracle.gemv(_pack_words(Q), s, z, x, oracle.F32)
+        assert np.array_equal(d[0], Q[:, k] - 8.0)
+
+
+def test_gemv_page_word_example():
+    """Word 0x76543210 holds weights 0..7 at k = 0..7 (w0 in the low bits)."""
+    qw = np.array([[0x76543210]], np.uint32)
+    x = np.eye(8, dtype=np.float32)
+    d, _ = oracle.gemv(qw, np.ones(1, np.float32), np.zeros(1, np.float32), x, oracle.F32)
+    assert d[:, 0].tolist() == list(range(8))
+
+
+def test_gemv_q_equal_zero_point_gives_zero_and_integers_exact():
+    rng = np.random.default_rng(3)
+    N, K = 8, 128
+    Q = np.full((N, K), 8)
+    x = rng.normal(0, 1, (2, K)).astype(np.float32)
+    d, _ = oracle.gemv(_pack_words(Q), np.ones(N, np.float32), np.full(N, 8.0, np.float32), x, oracle.F32)
+    assert np.all(d == 0.0)
+    Q = rng.integers(0, 16, (N, K))
+    xi = rng.integers(-5, 6, (2, K)).astype(np.float32)
+    d, _ = oracle.gemv(_pack_words(Q), np.ones(N, np.float32), np.zeros(N, np.float32), xi, oracle.F32)
+    assert np.array_equal(d, xi.astype(np.int64) @ Q.T)
+
+
+def test_gemv_row_range_and_linearity():
+    rng = np.random.default_rng(4)
+    N, K = 16, 64
+    qw = rng.integers(0, 2**32, (N, K // 8), dtype=np.uint64).astype(np.uint32)
+    s = rng.uniform(0.1, 1, N).astype(np.float32)
+    z = np.full(N, 8, np.float32)
+    x1 = rng.normal(size=(1, K)).astype(np.float32)
+    x2 = rng.normal(size=(1, K)).astype(np.float32)
+    d1, _ = oracle.gemv(qw, s, z, x1, oracle.F32)
+    d2, _ = oracle.gemv(qw, s, z, x2, oracle.F32)
+    d12, _ = oracle.gemv(qw, s, z, np.concatenate([x1, x2]), oracle.F32)
+    assert np.array_equal(d12, np.concatenate([d1, d2]))
+    d3, _ = oracle.gemv(qw, s, z, (x1.astype(np.float64) * 2).astype(np.float32), oracle.F32)
+    np.testing.assert_allclose(d3, 2 * d1, rtol=1e-12)
+    part, _ = oracle.gemv(qw, s, z, x1, oracle.F32, rows=(3, 9))
+    assert np.array_equal(part[0, 3:9], d1[0, 3:9]) and np.isnan(part[0, :3]).all()
+
+
+# ---------------------------------------------------------------------------
+# GEMM.
+# ---------------------------------------------------------------------------
+
+def test_gemm_matches_dense_matmul():
+    rng = np.random.default_rng(5)
+    M, N, K = 12, 20, 32
+    Q = rng.integers(0, 16, (K, N))
+    A = bf16_bits(rng.normal(0, 1, (M, K)))
+    s = bf16_bits(rng.uniform(0.005, 0.02, N))
+    z = bf16_bits(rng.uniform(6, 9, N))
+    c, ref = oracle.gemm_full(A, _pack_rows(Q), s, z)
+    W = (Q - bf16_values(z)[None, :]) * bf16_values(s)[None, :]
+    np.testing.assert_allclose(c, bf16_values(A) @ W, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(ref, np.abs(bf16_values(A)) @ np.abs(W), rtol=1e-12, atol=1e-12)
+
+
+def test_gemm_identity_A_returns_dequantised_weights():
+    K, N = 16, 8
+    rng = np.random.default_rng(6)
+    Q = rng.integers(0, 16, (K, N))
+    A = bf16_bits(np.eye(K))
+    c, _ = oracle.gemm_full(A, _pack_rows(Q), bf16_bits(np.full(N, 0.25)), bf16_bits(np.full(N, 8.0)))
+    assert np.array_equal(c, (Q - 8) * 0.25)
+
+
+def test_gemm_sampled_equals_full():
+    rng = np.random.default_rng(7)
+    M, N, K = 9, 7, 20
+    A = bf16_bits(rng.normal(size=(M, K)))
+    B = rng.integers(0, 256, (K // 2, N), dtype=np.uint8)
+    s, z = bf16_bits(np.full(N, 0.01)), bf16_bits(np.full(N, 8.0))
+    full, _ = oracle.gemm_full(A, B, s, z)
+    mi = rng.integers(0, M, 30)
+    ni = rng.integers(0, N, 30)
+    part, _ = oracle.gemm_at(A, B, s, z, mi, ni)
+    assert np.array_equal(part, full[mi, ni])

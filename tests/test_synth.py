@@ -1,0 +1,36 @@
+"""The seeded input generators are deterministic and have the stated shapes."""
+import numpy as np
+import torch
+
+import synth
+
+
+def test_gemv_inputs_deterministic_and_shaped():
+    a = synth.gemv_inputs(64, 256, 2, act="bf16", seed=0)
+    b = synth.gemv_inputs(64, 256, 2, act="bf16", seed=0)
+    c = synth.gemv_inputs(64, 256, 2, act="bf16", seed=1)
+    assert torch.equal(a.qweight, b.qweight) and torch.equal(a.x, b.x)
+    assert not torch.equal(a.qweight, c.qweight)
+    assert a.qweight.shape == (64, 32) and a.qweight.dtype == torch.int32
+    assert a.x.shape == (2, 256) and a.x.dtype == torch.bfloat16
+    s = a.scale.float()
+    assert s.min() >= 0.001 - 1e-5 and s.max() <= 0.01 + 1e-4
+    assert torch.all(a.zero.float() == 8.0)
+
+
+def test_gemv_inputs_nibbles_uniform():
+    t = synth.gemv_inputs(512, 1024, 1, act="f32", seed=0)
+    words = synth.np_bits(t.qweight)
+    nib = np.concatenate([(words >> (4 * j)) & 0xF for j in range(8)]).ravel()
+    counts = np.bincount(nib, minlength=16)
+    assert counts.min() > 0.9 * counts.mean() and counts.max() < 1.1 * counts.mean()
+    assert t.scale.dtype == torch.float32 and float(t.scale.max()) <= 2.0 / 16
+
+
+def test_gemm_and_quant_inputs():
+    g = synth.gemm_inputs(16, 32, 64, seed=0)
+    assert g.A.shape == (16, 64) and g.B.shape == (32, 32) and g.B.dtype == torch.uint8
+    assert torch.all(g.zero.float() == 8.0) and torch.all(g.scale.float() == torch.tensor(0.01).bfloat16().float())
+    w = synth.quant_inputs(64, 32, seed=0)
+    assert w.dtype == torch.bfloat16 and w.shape == (64, 32)
+    assert torch.equal(w, synth.quant_inputs(64, 32, seed=0))
