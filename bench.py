@@ -1,0 +1,596 @@
+"""Benchmark of the int4 weight-only hot path on GB300.
+
+Default workload: the decode GEMV, N=17280 rows, K=5120, C=1 (bf16 x,
+scale, zero and output; uint4 weights packed eight per uint32), the
+configuration the headline metric "int4 W-only GEMV HBM GB/s" is quoted
+on.  One step = one gemv_w4 call on one batch.  The line also carries the
+other kernels of the hot path as components: the small-batch GEMVs (C = 4,
+8), quantise+pack+permute of an 8192x8192 bf16 weight, and the 8192^3
+bf16 x int4 dequant GEMM (TFLOP/s).
+
+Timing: inputs resident in HBM; weights rotate through enough copies that
+the working set is more than twice the L2 (no step reads a weight copy the
+L2 still holds); the K timed steps are one CUDA-graph replay bracketed by a
+barrier and a device synchronise, timed with CUDA events on the launching
+stream; max over ranks.  `e2e` repeats the measurement through the public
+Python API with x copied from pinned host memory and d copied back every
+step (weights stay resident, as in a decode loop).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload decode|c4|c8|gemm|quant] [--no-components]
+"""
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "int4 W-only GEMV HBM GB/s (% of GB300 peak); dequant-GEMM TFLOP/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+WORKLOADS = {
+    "decode": dict(kind="gemv", N=17280, K=5120, C=1),
+    "c4": dict(kind="gemv", N=5120, K=17280, C=4),
+    "c8": dict(kind="gemv", N=5120, K=17280, C=8),
+    "c4s": dict(kind="gemv", N=6144, K=5120, C=4),
+    "c8s": dict(kind="gemv", N=6144, K=5120, C=8),
+    "quant": dict(kind="quant", K=8192, N=8192),
+    "gemm": dict(kind="gemm", M=8192, N=8192, K=8192),
+}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ---------------------------------------------------------------------------
+# algorithmic bytes / flops per unit of work
+# ---------------------------------------------------------------------------
+
+def gemv_bytes(N, K, C, esz=2):
+    # packed weights + scale + zero + x + d
+    return N * K // 2 + 2 * N * esz + C * K * esz + C * N * esz
+
+
+def quant_bytes(K, N):
+    # quantize_pack: read W, write packed + scale; permute: read + write packed
+    return (K * N * 2 + K * N // 2 + 4 * N) + 2 * (K * N // 2)
+
+
+def gemm_bytes(M, N, K):
+    return M * K * 2 + K * N // 2 + M * N * 2 + 4 * N
+
+
+def gemm_flops(M, N, K):
+    return 2 * M * N * K
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing
+# ---------------------------------------------------------------------------
+
+def dist_setup(gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    return world, rank
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v, world):
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# clocks during load
+# ---------------------------------------------------------------------------
+
+CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + CLOCK_QUERY, "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        rows = []
+        for line in (self.out or "").splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(f[1]), smax=float(f[2]), power=float(f[3]), hw=f[5], hwt=f[6], swt=f[7],
+                                 pcap=f[8]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        reasons = set()
+        for r in rows:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"), ("swt", "sw_thermal_slowdown"),
+                              ("pcap", "sw_power_cap")):
+                if r[key].lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in rows), "sm_max_mhz": max(r["smax"] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows),
+                "power_w_max": max(r["power"] for r in rows)}
+
+
+# ---------------------------------------------------------------------------
+# ncu traffic recorded in profiles/ (valid only while the kernel source is unchanged)
+# ---------------------------------------------------------------------------
+
+def source_hash(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+KERNEL_SOURCES = {
+    "gemv": ["gemm_int4_dequant_gb300/csrc/gemv.cu", "gemm_int4_dequant_gb300/csrc/common.cuh"],
+    "gemm": ["gemm_int4_dequant_gb300/csrc/gemm_tc.cu", "gemm_int4_dequant_gb300/csrc/common.cuh"],
+    "quant": ["gemm_int4_dequant_gb300/csrc/quant_permute.cu", "gemm_int4_dequant_gb300/csrc/common.cuh"],
+}
+
+
+def recorded_traffic(kind, workload):
+    """dram bytes per launch from profiles/<kind>_<workload>_ncu.md, if its
+    recorded source hash matches the current kernel source."""
+    p = os.path.join(ROOT, "profiles", "%s_%s_ncu.md" % (kind, workload))
+    if not os.path.exists(p):
+        return None
+    text = open(p).read()
+    m1 = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    m2 = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
+    if not m1 or not m2 or m2.group(1) != source_hash(KERNEL_SOURCES[kind]):
+        return None
+    return float(m1.group(1))
+
+
+# ---------------------------------------------------------------------------
+# workloads (our implementation)
+# ---------------------------------------------------------------------------
+
+def l2_bytes():
+    try:
+        return int(torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size)
+    except Exception:
+        return 128 * 2**20
+
+
+def copies_for(bytes_per_copy):
+    return max(2, int(np.ceil(2.0 * l2_bytes() / bytes_per_copy)) + 1)
+
+
+class GemvWork:
+    def __init__(self, w4, N, K, C, seed=0):
+        g = synth.gemv_inputs(N, K, C, act="bf16", seed=seed)
+        self.g = g
+        dev = torch.device("cuda")
+        self.R = copies_for(N * K // 2)
+        self.q = [g.qweight.to(dev) for _ in range(self.R)]
+        self.s, self.z, self.x = g.scale.to(dev), g.zero.to(dev), g.x.to(dev)
+        self.d = torch.empty((C, N), dtype=torch.bfloat16, device=dev)
+        self.w4 = w4
+        self.i = 0
+        self.N, self.K, self.C = N, K, C
+        self.bytes = gemv_bytes(N, K, C)
+        self.flops = 2 * N * K * C
+        self.launches_per_step = 1
+
+    def step(self):
+        self.w4.gemv_w4(self.q[self.i % self.R], self.s, self.z, self.x, out=self.d)
+        self.i += 1
+
+    def l2_note(self):
+        return "rotating %d weight copies (%.0f MB > 2x L2)" % (self.R, self.R * self.N * self.K / 2 / 1e6)
+
+
+class QuantWork:
+    def __init__(self, w4, K, N, seed=0):
+        dev = torch.device("cuda")
+        W = synth.quant_inputs(K, N, seed=seed).to(dev)
+        self.W = W
+        self.packed = torch.empty((K // 2, N), dtype=torch.int8, device=dev)
+        self.scale = torch.empty((N,), dtype=torch.float32, device=dev)
+        self.out = torch.empty((N * K // 2,), dtype=torch.int8, device=dev)
+        self.w4 = w4
+        self.K, self.N = K, N
+        self.bytes = quant_bytes(K, N)
+        self.flops = 0
+        self.launches_per_step = 2
+
+    def step(self):
+        self.w4.quantize_pack_int4(self.W, packed=self.packed, scale=self.scale)
+        self.w4.permute_int4(self.packed, out=self.out)
+
+    def l2_note(self):
+        return "W is %.0f MB > L2" % (self.K * self.N * 2 / 1e6)
+
+
+class GemmWork:
+    def __init__(self, w4, M, N, K, seed=0):
+        dev = torch.device("cuda")
+        gi = synth.gemm_inputs(M, N, K, seed=seed)
+        self.A, self.B = gi.A.to(dev), gi.B.to(dev)
+        self.s, self.z = gi.scale.to(dev), gi.zero.to(dev)
+        self.C = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        self.w4 = w4
+        self.M, self.N, self.K = M, N, K
+        self.bytes = gemm_bytes(M, N, K)
+        self.flops = gemm_flops(M, N, K)
+        self.launches_per_step = 1
+
+    def step(self):
+        self.w4.gemm_w4(self.A, self.B, self.s, self.z, out=self.C)
+
+    def l2_note(self):
+        return "A+C are %.0f MB > L2" % ((self.M * self.K + self.M * self.N) * 2 / 1e6)
+
+
+def make_work(w4, name):
+    cfg = dict(WORKLOADS[name])
+    kind = cfg.pop("kind")
+    if kind == "gemv":
+        return GemvWork(w4, **cfg)
+    if kind == "quant":
+        return QuantWork(w4, **cfg)
+    return GemmWork(w4, **cfg)
+
+
+def time_graph(work, steps, warmup, world):
+    """Warm up eagerly, capture `steps` steps into one CUDA graph, replay it
+    once untimed and once timed.  Returns seconds for the timed replay
+    (max over ranks)."""
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, warmup)):
+            work.step()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
+        for _ in range(steps):
+            work.step()
+    g.replay()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        g.replay()
+        end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    sec = start.elapsed_time(end) / 1e3
+    return max_over_ranks(sec, world), g, stream
+
+
+def soak(g, stream, seconds):
+    t0 = time.time()
+    with torch.cuda.stream(stream):
+        while time.time() - t0 < seconds:
+            g.replay()
+            torch.cuda.synchronize()
+
+
+def e2e_gemv(w4, work, steps, world):
+    """Public API, host buffers: x from pinned host memory in, d back out."""
+    x_host = work.g.x.clone().pin_memory()
+    d_host = torch.empty((work.C, work.N), dtype=torch.bfloat16).pin_memory()
+    x_dev = torch.empty_like(work.x)
+    q = work.q[0]
+    stream = torch.cuda.current_stream()
+    for _ in range(3):
+        x_dev.copy_(x_host, non_blocking=True)
+        w4.gemv_w4(q, work.s, work.z, x_dev, out=work.d)
+        d_host.copy_(work.d, non_blocking=True)
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for i in range(steps):
+        x_dev.copy_(x_host, non_blocking=True)
+        w4.gemv_w4(work.q[i % work.R], work.s, work.z, x_dev, out=work.d)
+        d_host.copy_(work.d, non_blocking=True)
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    sec = max_over_ranks(start.elapsed_time(end) / 1e3, world)
+    return sec, x_host.numel() * 2, d_host.numel() * 2
+
+
+def e2e_generic(work, steps, world):
+    """GEMM / quant: every input copied in from pinned host memory and the
+    result copied back, each step."""
+    if isinstance(work, GemmWork):
+        hosts = [work.A.cpu().pin_memory(), work.B.cpu().pin_memory()]
+        devs = [work.A, work.B]
+        outs = [(work.C, torch.empty_like(work.C, device="cpu").pin_memory())]
+    else:
+        hosts = [work.W.cpu().pin_memory()]
+        devs = [work.W]
+        outs = [(work.out, torch.empty_like(work.out, device="cpu").pin_memory()),
+                (work.scale, torch.empty_like(work.scale, device="cpu").pin_memory())]
+    stream = torch.cuda.current_stream()
+
+    def one():
+        for h, d in zip(hosts, devs):
+            d.copy_(h, non_blocking=True)
+        work.step()
+        for d, h in outs:
+            h.copy_(d, non_blocking=True)
+
+    for _ in range(2):
+        one()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for _ in range(steps):
+        one()
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    sec = max_over_ranks(start.elapsed_time(end) / 1e3, world)
+    hb = sum(h.numel() * h.element_size() for h in hosts)
+    ob = sum(h.numel() * h.element_size() for _, h in outs)
+    return sec, hb, ob
+
+
+# ---------------------------------------------------------------------------
+# CPU baseline: the oracle as it stands, on a bounded sample
+# ---------------------------------------------------------------------------
+
+def cpu_baseline(name, budget_s=10.0):
+    import oracle
+    from synth import np_bits
+    cfg = WORKLOADS[name]
+    if cfg["kind"] == "gemv":
+        g = synth.gemv_inputs(cfg["N"], cfg["K"], cfg["C"], act="bf16", seed=0)
+        args = (np_bits(g.qweight), np_bits(g.scale), np_bits(g.zero), np_bits(g.x), oracle.BF16)
+        N = cfg["N"]
+        # rows per call sized to ~1 s; repeat until the budget is used
+        t0 = time.perf_counter()
+        oracle.gemv(*args, rows=(0, min(N, 512)))
+        per_row = (time.perf_counter() - t0) / min(N, 512)
+        rows = int(max(1, min(N, 1.0 / max(per_row, 1e-9))))
+        done_rows, t_total, r0 = 0, 0.0, 0
+        while t_total < budget_s:
+            r1 = min(N, r0 + rows)
+            t0 = time.perf_counter()
+            oracle.gemv(*args, rows=(r0, r1))
+            t_total += time.perf_counter() - t0
+            done_rows += r1 - r0
+            r0 = 0 if r1 >= N else r1
+        bytes_done = gemv_bytes(cfg["N"], cfg["K"], cfg["C"]) * done_rows / N
+        return {"value": bytes_done / t_total / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                "sample": "%d rows of the %dx%d C=%d GEMV (fp64 C oracle, single thread), %.1f s" %
+                          (done_rows, cfg["N"], cfg["K"], cfg["C"], t_total)}
+    if cfg["kind"] == "gemm":
+        gi = synth.gemm_inputs(cfg["M"], cfg["N"], cfg["K"], seed=0)
+        A, B, s, z = np_bits(gi.A), gi.B.numpy(), np_bits(gi.scale), np_bits(gi.zero)
+        n_out, t_total = 0, 0.0
+        rng = np.random.default_rng(0)
+        while t_total < budget_s:
+            mi = rng.integers(0, cfg["M"], 4096)
+            ni = rng.integers(0, cfg["N"], 4096)
+            t0 = time.perf_counter()
+            oracle.gemm_at(A, B, s, z, mi, ni)
+            t_total += time.perf_counter() - t0
+            n_out += 4096
+        flops = 2 * cfg["K"] * n_out
+        return {"value": flops / t_total / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+                "sample": "%d sampled outputs of the 8192^3 GEMM (fp64 C oracle, single thread), %.1f s" %
+                          (n_out, t_total)}
+    K, N = cfg["K"], cfg["N"]
+    W = np_bits(synth.quant_inputs(K, N, seed=0))
+    n_done, t_total = 0, 0.0
+    while t_total < budget_s:
+        t0 = time.perf_counter()
+        s_ref, p_ref = oracle.quantize_pack(W)
+        oracle.permute(p_ref, K, N)
+        t_total += time.perf_counter() - t0
+        n_done += 1
+    return {"value": quant_bytes(K, N) * n_done / t_total / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": "%d full quantize+pack+permute of %dx%d (C oracle, single thread), %.1f s" %
+                      (n_done, K, N, t_total)}
+
+
+# ---------------------------------------------------------------------------
+# main
+# ---------------------------------------------------------------------------
+
+def unit_of(work):
+    return "TFLOP/s" if isinstance(work, GemmWork) else "GB/s"
+
+
+def rate(work, sec_per_step):
+    if isinstance(work, GemmWork):
+        return work.flops / sec_per_step / 1e12
+    return work.bytes / sec_per_step / 1e9
+
+
+def roofline(work, sec_per_launch, peaks, peak_src, kind_name, workload):
+    if isinstance(work, GemmWork):
+        achieved = work.flops / sec_per_launch / 1e12
+        peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+        return {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "peak_source": "%s bf16 burst" % peak_src,
+                "traffic": recorded_traffic("gemm", workload)}
+    achieved = work.bytes / work.launches_per_step / sec_per_launch / 1e9 if not isinstance(work, QuantWork) else \
+        work.bytes / sec_per_launch / 1e9
+    peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    return {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+            "peak_source": "%s HBM copy" % peak_src, "traffic": recorded_traffic(kind_name, workload)}
+
+
+def run_ours(args, world, rank):
+    import gemm_int4_dequant_gb300 as w4
+    peaks, peak_src = load_peaks()
+    work = make_work(w4, args.workload)
+    kind = WORKLOADS[args.workload]["kind"]
+    sec, g, stream = time_graph(work, args.steps, args.warmup, world)
+    sec_step = sec / args.steps
+    value = rate(work, sec_step) * world
+    with ClockSampler(int(os.environ.get("LOCAL_RANK", "0"))) as cs:
+        soak(g, stream, 2.0)
+        sec2, _, _ = time_graph(work, args.steps, 0, world)
+    clocks = cs.summary()
+    if kind == "gemv":
+        e2e_sec, hb, ob = e2e_gemv(w4, work, args.steps, world)
+    else:
+        e2e_sec, hb, ob = e2e_generic(work, max(2, min(args.steps, 10)), world)
+        e2e_sec = e2e_sec * args.steps / max(2, min(args.steps, 10))
+    e2e_val = rate(work, e2e_sec / args.steps) * world
+    line = {
+        "metric": METRIC, "value": value, "unit": unit_of(work), "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": sec_step * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16 x / uint4 weights, fp32 accumulate",
+        "data": "synthetic (seeded; shapes of the pages' workloads)",
+        "config": {"workload": args.workload, **{k: v for k, v in WORKLOADS[args.workload].items() if k != "kind"},
+                   "l2": work.l2_note(), "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": roofline(work, sec_step / work.launches_per_step, peaks, peak_src, kind, args.workload),
+        "gpu_launches": args.steps * work.launches_per_step,
+        "clocks": clocks,
+        "e2e": {"value": e2e_val, "unit": unit_of(work), "h2d_bytes_per_step": hb, "d2h_bytes_per_step": ob},
+    }
+    if kind == "quant":
+        line["roofline"]["note"] = "two kernels per step (quantize_pack_int4 + permute_int4); achieved = step bytes / step time"
+    if rank == 0 and world == 1:
+        line["cpu_baseline"] = cpu_baseline(args.workload, budget_s=args.cpu_seconds)
+    if args.components and world == 1:
+        comps = {}
+        for name in [n for n in ("c4", "c8", "c4s", "c8s", "quant", "gemm") if n != args.workload]:
+            wk = make_work(w4, name)
+            s, _, _ = time_graph(wk, max(10, args.steps // 4), 3, world)
+            per = s / max(10, args.steps // 4)
+            rl = roofline(wk, per / wk.launches_per_step, peaks, peak_src, WORKLOADS[name]["kind"], name)
+            comps[name] = {"value": rate(wk, per), "unit": unit_of(wk), "ms_per_step": per * 1e3,
+                           "frac": rl["frac"], "bound": rl["bound"], "traffic": rl["traffic"],
+                           "config": {k: v for k, v in WORKLOADS[name].items() if k != "kind"}}
+            del wk
+            torch.cuda.empty_cache()
+        line["components"] = comps
+    return line
+
+
+def run_reference(args, world, rank):
+    """The oracle (the plain CPU reference) on the host cores, rank 0 only."""
+    if rank != 0:
+        return None
+    cfg = WORKLOADS[args.workload]
+    t_budget = max(1.0, args.cpu_seconds / max(1, args.steps))
+    vals = []
+    last = None
+    for _ in range(args.warmup and 1):
+        cpu_baseline(args.workload, budget_s=0.5)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        last = cpu_baseline(args.workload, budget_s=t_budget)
+        vals.append(last["value"])
+    elapsed = time.perf_counter() - t0
+    value = statistics.median(vals)
+    unit = last["unit"]
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": elapsed / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic (seeded)",
+        "config": {"workload": args.workload, **{k: v for k, v in cfg.items() if k != "kind"}},
+        "cpu_baseline": {"value": value, "unit": unit, "cores": 1, "kind": "oracle",
+                         "sample": "%d steps, each: %s" % (args.steps, last["sample"])},
+        "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="decode")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-components", dest="components", action="store_false")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    if args.impl == "reference":
+        rank = int(os.environ.get("RANK", "0"))
+        world = int(os.environ.get("WORLD_SIZE", "1"))
+        line = run_reference(args, world, rank)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    world, rank = dist_setup(args.gpus)
+    line = run_ours(args, world, rank)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

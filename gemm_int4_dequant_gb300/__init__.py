@@ -1,0 +1,133 @@
+"""int4 weight-only GEMV / GEMM with fused dequantisation for GB300 (sm_103a).
+
+Thin PyTorch-facing binding over the C ABI in include/w4.h.  Tensors are
+only used as device memory: each function checks dtypes, shapes and
+devices, allocates missing outputs with torch, and passes raw pointers and
+the current CUDA stream to libw4.so.  The computation itself runs entirely
+in the library's CUDA kernels; there is no CPU or eager fallback.
+
+    quantize_pack_int4(W)               -> (packed [K/2, N] int8, scale [N] fp32)
+    permute_int4(packed)                -> out [N*K/2] int8 (interleaved)
+    gemv_w4(qweight, scale, zero, x)    -> d [C, N]
+    gemm_w4(A, B, scale, zero)          -> C [M, N] bf16
+"""
+import torch
+
+from . import _lib
+from ._lib import W4Error, W4_BF16, W4_F32
+
+__all__ = ["quantize_pack_int4", "permute_int4", "gemv_w4", "gemm_w4", "device_error", "W4Error"]
+
+_lib.load()  # fail loudly at import if the CUDA library is missing
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes_ptr(stream.cuda_stream)
+
+
+def ctypes_ptr(v):
+    return int(v) if v else None
+
+
+def _need(t, name, dtypes, ndim=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % name)
+    if t.device.type != "cuda":
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if t.dtype not in dtypes:
+        raise TypeError("%s has dtype %s, expected one of %s" % (name, t.dtype, dtypes))
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError("%s must have %d dims" % (name, ndim))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+
+
+def quantize_pack_int4(W, packed=None, scale=None, stream=None):
+    """Symmetric per-column int4 quantisation of W [K, N] bf16 plus the
+    column pack (two rows per byte, even row in the low nibble)."""
+    _need(W, "W", (torch.bfloat16,), 2)
+    K, N = W.shape
+    if packed is None:
+        packed = torch.empty((K // 2, N), dtype=torch.int8, device=W.device)
+    if scale is None:
+        scale = torch.empty((N,), dtype=torch.float32, device=W.device)
+    _need(packed, "packed", (torch.int8, torch.uint8))
+    _need(scale, "scale", (torch.float32,))
+    if packed.numel() != (K // 2) * N or scale.numel() != N:
+        raise ValueError("output shapes do not match W")
+    st = _lib.load().quantize_pack_int4(W.data_ptr(), packed.data_ptr(), scale.data_ptr(), K, N, _stream(stream))
+    _lib.check("quantize_pack_int4", st)
+    return packed, scale
+
+
+def permute_int4(packed, out=None, stream=None):
+    """Page-1 int4 interleave permute of packed [K/2, N] into N*K/2 bytes."""
+    _need(packed, "packed", (torch.int8, torch.uint8), 2)
+    Kp, N = packed.shape
+    K = 2 * Kp
+    if out is None:
+        out = torch.empty((N * Kp,), dtype=packed.dtype, device=packed.device)
+    _need(out, "out", (torch.int8, torch.uint8))
+    if out.numel() != N * Kp:
+        raise ValueError("out must hold N*K/2 bytes")
+    st = _lib.load().permute_int4(packed.data_ptr(), out.data_ptr(), K, N, _stream(stream))
+    _lib.check("permute_int4", st)
+    return out
+
+
+def gemv_w4(qweight, scale, zero, x, out=None, stream=None):
+    """d[c, r] = sum_k (q[r, k] - zero[r]) * scale[r] * x[c, k].
+
+    qweight: int32/uint32 [N, K/8] packed words; scale, zero: [N]; x: [C, K]
+    (C <= 8) -- scale, zero, x and the output share one dtype, fp32 or bf16.
+    """
+    _need(qweight, "qweight", (torch.int32, torch.uint32) if hasattr(torch, "uint32") else (torch.int32,), 2)
+    _need(x, "x", (torch.float32, torch.bfloat16))
+    dt = x.dtype
+    _need(scale, "scale", (dt,), 1)
+    _need(zero, "zero", (dt,), 1)
+    xx = x if x.dim() == 2 else x.reshape(1, -1)
+    N, K = qweight.shape[0], qweight.shape[1] * 8
+    C = xx.shape[0]
+    if xx.shape[1] != K or scale.numel() != N or zero.numel() != N:
+        raise ValueError("shape mismatch: qweight %s, x %s, scale %s" % (tuple(qweight.shape), tuple(x.shape), tuple(scale.shape)))
+    if out is None:
+        out = torch.empty((C, N), dtype=dt, device=x.device)
+    _need(out, "out", (dt,))
+    if out.numel() != C * N:
+        raise ValueError("out must hold C*N elements")
+    st = _lib.load().gemv_w4(qweight.data_ptr(), scale.data_ptr(), zero.data_ptr(), xx.data_ptr(), out.data_ptr(),
+                             N, K, C, W4_F32 if dt == torch.float32 else W4_BF16, _stream(stream))
+    _lib.check("gemv_w4", st)
+    return out
+
+
+def gemm_w4(A, B, scale, zero, out=None, stream=None):
+    """C[m, n] = scale[n] * sum_k A[m, k] * (u[k, n] - zero[n]); A bf16 [M, K],
+    B int8/uint8 [K/2, N] (low nibble = even k, unsigned), scale/zero bf16 [N]."""
+    _need(A, "A", (torch.bfloat16,), 2)
+    _need(B, "B", (torch.int8, torch.uint8), 2)
+    _need(scale, "scale", (torch.bfloat16,), 1)
+    _need(zero, "zero", (torch.bfloat16,), 1)
+    M, K = A.shape
+    if B.shape[0] * 2 != K:
+        raise ValueError("B must be [K/2, N]")
+    N = B.shape[1]
+    if scale.numel() != N or zero.numel() != N:
+        raise ValueError("scale/zero must be [N]")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    _need(out, "out", (torch.bfloat16,))
+    if out.numel() != M * N:
+        raise ValueError("out must hold M*N elements")
+    st = _lib.load().gemm_w4(A.data_ptr(), B.data_ptr(), scale.data_ptr(), zero.data_ptr(), out.data_ptr(),
+                             M, N, K, _stream(stream))
+    _lib.check("gemm_w4", st)
+    return out
+
+
+def device_error(stream=None):
+    """Synchronise and return/clear the library's device-side error code."""
+    return _lib.load().w4_device_error(_stream(stream))

@@ -1,0 +1,432 @@
+// gemm_tc.cu -- large-M bf16 x int4 dequant GEMM on the 5th-generation
+// (tcgen05) tensor cores of sm_103a.
+//
+//   C[m][n] = scale[n] * sum_k A[m][k] * (u[k][n] - zero[n])
+//
+// (page "int4 gemm kernel", the matmul_bf16_int4 example: A (M,K) bf16 and B
+// packed (K/2, N) int8 with the low nibble for even k; one packed k-tile of B
+// feeds an A k-tile twice as long.)
+//
+// CTA = one 128 x 256 output tile, 6 warps:
+//   warp 0      TMA producer: A tile [128 x 64] bf16 (128B-swizzled, K-major)
+//               and the packed B tile [32 x 256] bytes, one mbarrier per stage;
+//   warp 1      TMEM allocator and MMA issuer (one thread): 4 x
+//               tcgen05.mma.cta_group::1.kind::f16 (M128 N256 K16) per k-tile,
+//               fp32 accumulator in TMEM, tcgen05.commit frees the stage;
+//   warps 2..5  dequant: packed bytes -> (u - zero) bf16, written straight into
+//               the canonical 128B-swizzled MN-major operand layout, then the
+//               epilogue: tcgen05.ld of the accumulator, * scale, -> bf16.
+// Every wait is bounded; on timeout the kernel records an error code in a
+// device word (w4_device_error), stops issuing work, drains and frees TMEM.
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+
+namespace w4 {
+
+__device__ int g_device_error;  // first error code recorded by any kernel (0 = none)
+
+namespace gemm {
+
+constexpr int BM = 128, BN = 256, BK = 64;
+constexpr int STAGES = 4;
+constexpr int THREADS = 192;
+constexpr int A_BYTES = BM * BK * 2;         // 16 KB
+constexpr int BP_BYTES = (BK / 2) * BN;      // 8 KB packed
+constexpr int BD_BYTES = BK * BN * 2;        // 32 KB dequantised
+constexpr int OFF_A = 0;
+constexpr int OFF_BD = OFF_A + STAGES * A_BYTES;
+constexpr int OFF_BP = OFF_BD + STAGES * BD_BYTES;
+constexpr int OFF_BAR = OFF_BP + STAGES * BP_BYTES;
+constexpr int NUM_BARS = 3 * STAGES + 1;
+constexpr int OFF_TMEM_SLOT = OFF_BAR + NUM_BARS * 8;
+constexpr int OFF_ABORT = OFF_TMEM_SLOT + 4;
+constexpr int SMEM_USED = OFF_ABORT + 4;
+constexpr int SMEM_BYTES = SMEM_USED + 1024;  // slack to align the base to 1 KB
+constexpr uint32_t TMEM_COLS = 256;
+constexpr int DEQ_THREADS = 128;
+
+constexpr int ERR_TIMEOUT = 1;
+
+// ---- PTX wrappers ---------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait: about two seconds of SM clock, or until another role of this
+// CTA has aborted.  Returns false on timeout/abort.
+__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (clock64() - t0 > (1ll << 32)) {
+            *abort_flag = 1;
+            atomicCAS(&g_device_error, 0, ERR_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+// Bounded wait used only while draining (ignores the abort flag): waits for
+// work this CTA already issued (TMA copies, MMAs) before it frees resources.
+__device__ __noinline__ void mbar_drain(uint32_t bar, uint32_t parity) {
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if (clock64() - t0 > (1ll << 32)) {
+            atomicCAS(&g_device_error, 0, ERR_TIMEOUT);
+            return;
+        }
+    }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            dst),
+        "l"(map), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_alloc(uint32_t slot_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_smem), "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+// 32 lanes x 32 consecutive fp32 columns: thread i gets row (lane base + i).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor (sm_100 format): start address, leading and
+// stride byte offsets (all >> 4), descriptor version 1, 128-byte swizzle.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+    d |= static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
+    d |= 1ull << 46;  // version
+    d |= 2ull << 61;  // SWIZZLE_128B
+    return d;
+}
+
+// Instruction descriptor, kind::f16: D fp32, A bf16 K-major, B bf16 MN-major,
+// N = 256, M = 128.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (0u << 15) | (1u << 16) |
+                            (static_cast<uint32_t>(BN >> 3) << 17) | (static_cast<uint32_t>(BM >> 4) << 24);
+
+// Byte offset of element (k, n) of the dequantised B tile: atoms of 8 k-rows
+// x 64 n (1 KB, 16-byte chunks XOR-swizzled by k % 8), atom (n/64, k/8) at
+// ((n/64) * (BK/8) + k/8) KB.  n is a multiple of 8 (one 16-byte chunk).
+__device__ __forceinline__ uint32_t bd_offset(int k, int n) {
+    const int atom = (n >> 6) * (BK / 8) + (k >> 3);
+    const int r = k & 7, chunk = (n & 63) >> 3;
+    return static_cast<uint32_t>(atom * 1024 + r * 128 + ((chunk ^ r) << 4));
+}
+
+__device__ __forceinline__ uint32_t bsub2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// Two packed bytes (columns n, n+1, in the low 16 bits of `pair`) -> bf16x2
+// for even k (low nibbles) and odd k (high nibbles), minus the zero points.
+__device__ __forceinline__ void dequant_pair(uint32_t pair16, uint32_t zz, uint32_t& even, uint32_t& odd) {
+    const uint32_t spread = __byte_perm(pair16, 0u, 0x4140);  // byte0 -> bits 0..7, byte1 -> bits 16..23
+    const uint32_t k128 = 0x43004300u;                        // bf16x2 (128, 128)
+    const uint32_t lo = (spread & 0x000F000Fu) | k128;        // 128 + u_even
+    const uint32_t hi = ((spread >> 4) & 0x000F000Fu) | k128; // 128 + u_odd
+    even = bsub2(bsub2(lo, k128), zz);
+    odd = bsub2(bsub2(hi, k128), zz);
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+gemm_w4_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                  const __nv_bfloat16* __restrict__ scale, const __nv_bfloat16* __restrict__ zero,
+                  __nv_bfloat16* __restrict__ C, int M, int N, int K) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* sbase = smem_raw + (base - raw);
+    const uint32_t bar0 = base + OFF_BAR;
+    auto full_tma = [&](int s) { return bar0 + 8u * s; };
+    auto full_deq = [&](int s) { return bar0 + 8u * (STAGES + s); };
+    auto empty = [&](int s) { return bar0 + 8u * (2 * STAGES + s); };
+    const uint32_t tmem_full = bar0 + 8u * (3 * STAGES);
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(sbase + OFF_TMEM_SLOT);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sbase + OFF_ABORT);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
+    const int num_kt = K / BK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_tma(s), 1);
+            mbar_init(full_deq(s), DEQ_THREADS);
+            mbar_init(empty(s), 1);
+        }
+        mbar_init(tmem_full, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        // ---------------- TMA producer ----------------
+        if (lane == 0) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"(&tmap_a) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(&tmap_b) : "memory");
+            int issued = 0;
+            for (int kt = 0; kt < num_kt; ++kt) {
+                const int s = kt % STAGES, round = kt / STAGES;
+                if (round > 0 && !mbar_wait(empty(s), (round - 1) & 1, abort_flag)) break;
+                mbar_arrive_expect_tx(full_tma(s), A_BYTES + BP_BYTES);
+                tma_load_2d(base + OFF_A + s * A_BYTES, &tmap_a, kt * BK, m0, full_tma(s));
+                tma_load_2d(base + OFF_BP + s * BP_BYTES, &tmap_b, n0, kt * (BK / 2), full_tma(s));
+                issued = kt + 1;
+            }
+            // the last copies may still be landing if a consumer aborted
+            for (int kt = max(0, issued - STAGES); kt < issued; ++kt)
+                mbar_drain(full_tma(kt % STAGES), (kt / STAGES) & 1);
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer ----------------
+        if (lane == 0) {
+            bool ok = true;
+            for (int kt = 0; kt < num_kt && ok; ++kt) {
+                const int s = kt % STAGES, round = kt / STAGES;
+                ok = mbar_wait(full_tma(s), round & 1, abort_flag) && mbar_wait(full_deq(s), round & 1, abort_flag);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t a_addr = base + OFF_A + s * A_BYTES;
+                const uint32_t b_addr = base + OFF_BD + s * BD_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < BK / 16; ++kk) {
+                    // A: K-major SW128, +32 B per 16-element k step; SBO = 8 rows * 128 B.
+                    const uint64_t adesc = sw128_desc(a_addr + kk * 32, 16, 1024);
+                    // B: MN-major SW128, k-groups of 8 rows 1 KB apart (SBO),
+                    // 64-column atoms (BK/8) KB apart (LBO).
+                    const uint64_t bdesc = sw128_desc(b_addr + kk * 2 * 1024, (BK / 8) * 1024, 1024);
+                    umma_bf16(tmem_base, adesc, bdesc, kIdesc, (kt > 0 || kk > 0) ? 1u : 0u);
+                }
+                umma_commit(empty(s));
+            }
+            umma_commit(tmem_full);
+            mbar_drain(tmem_full, 0);  // all MMAs done before TMEM can be freed
+        }
+    } else {
+        // ---------------- dequant (warps 2..5) ----------------
+        const int t = threadIdx.x - 64;          // 0..127
+        const int nl = (t & 31) * 8;             // 8 columns per thread
+        const int kp_lane = t >> 5;              // 0..3
+        uint32_t zz[4];
+        {
+            uint16_t zb[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int n = n0 + nl + j;
+                zb[j] = n < N ? __bfloat16_as_ushort(zero[n]) : 0;
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) zz[j] = static_cast<uint32_t>(zb[2 * j]) | (static_cast<uint32_t>(zb[2 * j + 1]) << 16);
+        }
+        bool ok = true;
+        for (int kt = 0; kt < num_kt && ok; ++kt) {
+            const int s = kt % STAGES, round = kt / STAGES;
+            if (round > 0 && !mbar_wait(empty(s), (round - 1) & 1, abort_flag)) { ok = false; break; }
+            if (!mbar_wait(full_tma(s), round & 1, abort_flag)) { ok = false; break; }
+            const uint8_t* bp = sbase + OFF_BP + s * BP_BYTES;
+            uint8_t* bd = sbase + OFF_BD + s * BD_BYTES;
+#pragma unroll
+            for (int i = 0; i < (BK / 2) / 4; ++i) {
+                const int kp = kp_lane + 4 * i;
+                const uint2 v = *reinterpret_cast<const uint2*>(bp + kp * BN + nl);
+                uint32_t ev[4], od[4];
+                dequant_pair(v.x & 0xFFFFu, zz[0], ev[0], od[0]);
+                dequant_pair(v.x >> 16, zz[1], ev[1], od[1]);
+                dequant_pair(v.y & 0xFFFFu, zz[2], ev[2], od[2]);
+                dequant_pair(v.y >> 16, zz[3], ev[3], od[3]);
+                *reinterpret_cast<uint4*>(bd + bd_offset(2 * kp, nl)) = make_uint4(ev[0], ev[1], ev[2], ev[3]);
+                *reinterpret_cast<uint4*>(bd + bd_offset(2 * kp + 1, nl)) = make_uint4(od[0], od[1], od[2], od[3]);
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(full_deq(s));
+        }
+
+        // ---------------- epilogue ----------------
+        if (ok && mbar_wait(tmem_full, 0, abort_flag)) {
+            tc_fence_after();
+            const int quarter = warp & 3;           // TMEM lanes 32*quarter .. +31
+            const int m = m0 + quarter * 32 + lane;
+            for (int cb = 0; cb < BN / 32; ++cb) {
+                uint32_t r[32];
+                tmem_ld32(tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + cb * 32, r);
+                const int nb = n0 + cb * 32;
+                if (m < M && nb < N) {
+                    uint32_t packed[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int na = nb + 2 * j;
+                        const float s0 = na < N ? __bfloat162float(scale[na]) : 0.f;
+                        const float s1 = na + 1 < N ? __bfloat162float(scale[na + 1]) : 0.f;
+                        const __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(r[2 * j]) * s0,
+                                                                       __uint_as_float(r[2 * j + 1]) * s1);
+                        packed[j] = *reinterpret_cast<const uint32_t*>(&h);
+                    }
+                    __nv_bfloat16* dst = C + static_cast<int64_t>(m) * N + nb;
+                    if (nb + 32 <= N) {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            reinterpret_cast<uint4*>(dst)[q] =
+                                make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+                    } else {
+                        for (int q = 0; q < (N - nb) / 8; ++q)
+                            reinterpret_cast<uint4*>(dst)[q] =
+                                make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+// ---- host side --------------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+}  // namespace gemm
+
+w4_status run_gemm(const void* A, const void* B, const void* scale, const void* zero, void* C, int64_t M,
+                   int64_t N, int64_t K, cudaStream_t stream) {
+    using namespace gemm;
+    if (M > 0x7FFFFFFF || N > 0x7FFFFFFF || K > 0x7FFFFFFF) return W4_ERR_SHAPE;
+    const int64_t tiles_m = (M + BM - 1) / BM, tiles_n = (N + BN - 1) / BN;
+    if (tiles_m > 65535 || tiles_n > 0x7FFFFFFF) return W4_ERR_SHAPE;
+    auto encode = get_encode_fn();
+    if (!encode) return W4_ERR_CUDA;
+
+    CUtensorMap ta, tb;
+    {
+        cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
+        cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+        cuuint32_t box[2] = {BK, BM};
+        cuuint32_t estr[2] = {1, 1};
+        if (encode(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(A), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return W4_ERR_CUDA;
+    }
+    {
+        cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(K / 2)};
+        cuuint64_t strides[1] = {static_cast<cuuint64_t>(N)};
+        cuuint32_t box[2] = {BN, BK / 2};
+        cuuint32_t estr[2] = {1, 1};
+        if (encode(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(B), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return W4_ERR_CUDA;
+    }
+    static int smem_set[64];
+    cudaError_t e = ensure_smem_limit(gemm_w4_tc_kernel, SMEM_BYTES, smem_set);
+    if (e != cudaSuccess) return W4_ERR_CUDA;
+    dim3 grid(static_cast<unsigned>(tiles_n), static_cast<unsigned>(tiles_m));
+    gemm_w4_tc_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(
+        ta, tb, static_cast<const __nv_bfloat16*>(scale), static_cast<const __nv_bfloat16*>(zero),
+        static_cast<__nv_bfloat16*>(C), static_cast<int>(M), static_cast<int>(N), static_cast<int>(K));
+    return launch_status(cudaGetLastError());
+}
+
+}  // namespace w4
+
+extern "C" int w4_device_error(void* stream) {
+    // Reads (and clears) the first error code any kernel recorded on the
+    // current device; synchronises `stream` first.  0 = no error.
+    int v = 0;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return -1;
+    if (cudaMemcpyFromSymbol(&v, w4::g_device_error, sizeof(int)) != cudaSuccess) return -1;
+    const int zero = 0;
+    if (v != 0 && cudaMemcpyToSymbol(w4::g_device_error, &zero, sizeof(int)) != cudaSuccess) return -1;
+    return v;
+}

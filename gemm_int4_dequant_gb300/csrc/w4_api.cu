@@ -1,0 +1,115 @@
+// w4_api.cu -- the extern "C" boundary (declared in include/w4.h).
+//
+// Every entry point validates its arguments on the host, before anything is
+// enqueued, and then launches its kernel(s) on the caller's stream.  No entry
+// point allocates, synchronises or keeps state between calls.
+
+#include "common.cuh"
+
+namespace w4 {
+
+w4_status run_quantize_pack(const void* W, void* packed, float* scale, int64_t K, int64_t N, cudaStream_t s);
+w4_status run_permute(const void* packed, void* out, int64_t K, int64_t N, cudaStream_t s);
+w4_status run_gemv(const void* qw, const void* scale, const void* zero, const void* x, void* d, int64_t N,
+                   int64_t K, int64_t C, w4_dtype dtype, cudaStream_t s);
+w4_status run_gemm(const void* A, const void* B, const void* scale, const void* zero, void* C, int64_t M,
+                   int64_t N, int64_t K, cudaStream_t s);
+
+namespace {
+constexpr int kMaxDevices = 64;
+int g_sm_count[kMaxDevices];
+int g_is_sm103[kMaxDevices];  // 0 unknown, 1 yes, -1 no
+}  // namespace
+
+int sm_count() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+    if (g_sm_count[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        g_sm_count[dev] = n;
+    }
+    return g_sm_count[dev];
+}
+
+bool device_is_sm103() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+    if (g_is_sm103[dev] == 0) {
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+            return false;
+        g_is_sm103[dev] = (major == 10 && minor == 3) ? 1 : -1;
+    }
+    return g_is_sm103[dev] == 1;
+}
+
+}  // namespace w4
+
+using namespace w4;
+
+extern "C" {
+
+int w4_abi_version(void) { return 1; }
+
+const char* w4_status_string(w4_status status) {
+    switch (status) {
+        case W4_OK: return "ok";
+        case W4_ERR_NULL: return "null pointer argument";
+        case W4_ERR_SHAPE: return "illegal size or shape";
+        case W4_ERR_ALIGN: return "pointer not 16-byte aligned";
+        case W4_ERR_DTYPE: return "unsupported dtype";
+        case W4_ERR_CUDA: return "CUDA launch error";
+        case W4_ERR_DEVICE: return "current device is not an sm_103 (GB300) GPU";
+    }
+    return "unknown status";
+}
+
+w4_status quantize_pack_int4(const void* W, void* packed, float* scale, int64_t K, int64_t N, void* stream) {
+    if (K < 0 || N < 0 || (K % 2) != 0) return W4_ERR_SHAPE;
+    if (N == 0) return W4_OK;
+    if (!scale || (K > 0 && (!W || !packed))) return W4_ERR_NULL;
+    if (!aligned16(scale) || (K > 0 && (!aligned16(W) || !aligned16(packed)))) return W4_ERR_ALIGN;
+    if (!device_is_sm103()) return W4_ERR_DEVICE;
+    if (K == 0) return launch_status(cudaMemsetAsync(scale, 0, N * sizeof(float), (cudaStream_t)stream));
+    return run_quantize_pack(W, packed, scale, K, N, (cudaStream_t)stream);
+}
+
+w4_status permute_int4(const void* packed, void* out, int64_t K, int64_t N, void* stream) {
+    if (K < 0 || N < 0 || (K % 64) != 0 || (N % 4) != 0) return W4_ERR_SHAPE;
+    if (K == 0 || N == 0) return W4_OK;
+    if (!packed || !out) return W4_ERR_NULL;
+    if (!aligned16(packed) || !aligned16(out)) return W4_ERR_ALIGN;
+    if (!device_is_sm103()) return W4_ERR_DEVICE;
+    return run_permute(packed, out, K, N, (cudaStream_t)stream);
+}
+
+w4_status gemv_w4(const void* qweight, const void* scale, const void* zero, const void* x, void* d, int64_t N,
+                  int64_t K, int64_t C, w4_dtype dtype, void* stream) {
+    if (dtype != W4_F32 && dtype != W4_BF16) return W4_ERR_DTYPE;
+    if (N < 0 || K < 0 || (K % 8) != 0 || C < 1 || C > 8) return W4_ERR_SHAPE;
+    if (N == 0) return W4_OK;
+    if (!d || !scale || !zero || (K > 0 && (!qweight || !x))) return W4_ERR_NULL;
+    if (!aligned16(d) || !aligned16(scale) || !aligned16(zero) ||
+        (K > 0 && (!aligned16(qweight) || !aligned16(x))))
+        return W4_ERR_ALIGN;
+    if (!device_is_sm103()) return W4_ERR_DEVICE;
+    const size_t esz = dtype == W4_F32 ? 4 : 2;
+    if (K == 0) return launch_status(cudaMemsetAsync(d, 0, C * N * esz, (cudaStream_t)stream));
+    return run_gemv(qweight, scale, zero, x, d, N, K, C, dtype, (cudaStream_t)stream);
+}
+
+w4_status gemm_w4(const void* A, const void* B, const void* scale, const void* zero, void* C, int64_t M, int64_t N,
+                  int64_t K, void* stream) {
+    if (M < 0 || N < 0 || K < 0 || (K % 64) != 0 || (N % 8) != 0) return W4_ERR_SHAPE;
+    if (M == 0 || N == 0) return W4_OK;
+    if (!C || !scale || !zero || (K > 0 && (!A || !B))) return W4_ERR_NULL;
+    if (!aligned16(C) || !aligned16(scale) || !aligned16(zero) || (K > 0 && (!aligned16(A) || !aligned16(B))))
+        return W4_ERR_ALIGN;
+    if (!device_is_sm103()) return W4_ERR_DEVICE;
+    if (K == 0) return launch_status(cudaMemsetAsync(C, 0, M * N * 2, (cudaStream_t)stream));
+    return run_gemm(A, B, scale, zero, C, M, N, K, (cudaStream_t)stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,163 @@
+/*
+ * w4.h -- C ABI of the int4 weight-only GEMV/GEMM library for GB300 (sm_103a).
+ *
+ * Operations (sources are the web pages on int4 weight-only quantisation,
+ * cited by page title and section):
+ *   quantize_pack_int4  per-column symmetric int4 quantisation of W[K][N] and
+ *                       the column pack of two rows per byte
+ *                       ("[PHI] add int4 weight only quant kernel, add int4
+ *                       weight only permute kernel", section "int4量化kernel").
+ *   permute_int4        the int4 interleave permute of the packed matrix
+ *                       (same page, sections "int4 permute kernel",
+ *                       "简单的位运算", "int4 row interval").
+ *   gemv_w4             fused dequant GEMV / small-batch multiply,
+ *                       d[c][r] = sum_k (q[r][k] - zero[r]) * scale[r] * x[c][k]
+ *                       ("怎样在安卓端利用 Vulkan 编写 4-bit 专用算子", sections 1
+ *                       and 2; batched form from "三值量化模型的无损压缩", section 3).
+ *   gemm_w4             large-M bf16 x int4 dequant GEMM
+ *                       ("int4 gemm kernel", the matmul_bf16_int4 example).
+ *
+ * Conventions shared by every entry point:
+ *   - All data pointers are DEVICE pointers owned by the caller.  The library
+ *     never allocates, frees or retains them, and keeps no per-call state.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Every call only enqueues work on that stream and returns; the
+ *     results are ready when the stream reaches that point.
+ *   - Arguments are validated on the host before anything is enqueued: a
+ *     NULL pointer gives W4_ERR_NULL, an illegal size W4_ERR_SHAPE, a pointer
+ *     that is not 16-byte aligned W4_ERR_ALIGN, an unknown dtype W4_ERR_DTYPE;
+ *     in all those cases nothing is launched and no output is touched.  A
+ *     CUDA error while launching gives W4_ERR_CUDA (the CUDA error itself is
+ *     left for cudaGetLastError of the caller's runtime to report) and
+ *     W4_ERR_DEVICE means the current device is not an sm_103 GPU.
+ *   - Sizes are int64_t; every size must be >= 0.  Outputs are fully
+ *     overwritten (their prior contents never matter).  Inputs and outputs
+ *     must not overlap.
+ *   - Calls are re-entrant and may run concurrently on different streams.
+ */
+#ifndef W4_H_
+#define W4_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    W4_OK = 0,
+    W4_ERR_NULL = -1,
+    W4_ERR_SHAPE = -2,
+    W4_ERR_ALIGN = -3,
+    W4_ERR_DTYPE = -4,
+    W4_ERR_CUDA = -5,
+    W4_ERR_DEVICE = -6
+} w4_status;
+
+/* Element type of gemv_w4's x, scale, zero and d (all four share it). */
+typedef enum { W4_F32 = 0, W4_BF16 = 1 } w4_dtype;
+
+/* Version of this ABI (bumped on any signature change). */
+int w4_abi_version(void);
+
+/* Static text for a status code. */
+const char* w4_status_string(w4_status status);
+
+/*
+ * Device-side error word.  Kernels never trap: a wait that exceeds its
+ * iteration/time limit (about two seconds) records a nonzero code here,
+ * drains the work it already issued, frees its tensor memory and returns.
+ * This call synchronises `stream`, then returns and clears the first code
+ * recorded on the current device (0 = none, 1 = a pipeline wait timed out),
+ * or -1 if the synchronisation or the read failed.
+ */
+int w4_device_error(void* stream);
+
+/*
+ * quantize_pack_int4 -- symmetric per-column int4 quantisation + column pack.
+ *
+ *   scale[n]  = max_k |W[k][n]| / 7                (IEEE fp32 division)
+ *   q[k][n]   = clamp(round(W[k][n] / scale[n]), -8, 7)
+ *               (IEEE fp32 division; round half away from zero; a column
+ *               whose maximum is 0 gets scale 0 and q = 0)
+ *   packed[k/2][n] = (q[k][n] & 0xF) | ((q[k+1][n] & 0xF) << 4)
+ *               (two rows per byte along K, even row in the low nibble)
+ *
+ * W       bf16 [K][N] row-major (N contiguous), 16-byte aligned.
+ * packed  int8 [K/2][N] row-major, 16-byte aligned (output).
+ * scale   fp32 [N], 16-byte aligned (output).
+ * K must be even; K == 0 writes scale = 0 and nothing else; N == 0 is a no-op.
+ * NaN or Inf in W is undefined.  Results are bit-exact with the
+ * definition above.
+ */
+w4_status quantize_pack_int4(const void* W, void* packed, float* scale, int64_t K, int64_t N,
+                             void* stream);
+
+/*
+ * permute_int4 -- the int4 interleave permute for a fast-dequant consumer.
+ *
+ * For each column n, with b[j] = packed[j][n] (j < K/2, "total_k" = K/2):
+ *   1. byte permute inside every 16-byte group: source byte t goes to
+ *      position (0 4 8 12 2 6 10 14 1 5 9 13 3 7 11 15)[t];
+ *   2. nibble swap inside every 4-byte group p0..p3 of the result:
+ *      p0' = lo(p0)|lo(p2)<<4, p1' = lo(p1)|lo(p3)<<4,
+ *      p2' = hi(p0)|hi(p2)<<4, p3' = hi(p1)|hi(p3)<<4;
+ *   3. row interleave: byte j of the column's stream is stored at
+ *      out[j%32 + (j/32)*128 + 32*(n%4) + (K/2)*4*(n/4)].
+ * The result is N/4 runs of 2K bytes; every 32-byte chunk of four adjacent
+ * columns is interleaved.  In each 32-bit word the nibble slots hold the
+ * k-indices 0 8 16 24 1 9 17 25 (+2 per further word, +32 per 16-byte group),
+ * the order a fast dequant reading slots 0 2 4 6 1 3 5 7 turns into
+ * 0 1 8 9 16 17 24 25 ...
+ *
+ * packed  int8 [K/2][N] (the output of quantize_pack_int4), 16-byte aligned.
+ * out     int8 [N*K/2], 16-byte aligned (output).
+ * Requires K % 64 == 0 and N % 4 == 0 (else W4_ERR_SHAPE); K == 0 or N == 0
+ * is a no-op.  Bit-exact.
+ */
+w4_status permute_int4(const void* packed, void* out, int64_t K, int64_t N, void* stream);
+
+/*
+ * gemv_w4 -- fused dequant GEMV / small-batch multiply.
+ *
+ *   d[c][r] = sum_k (q[r][k] - zero[r]) * scale[r] * x[c][k],  0 <= c < C
+ *
+ * qweight  uint32 [N][K/8] row-major: word i of row r holds q[r][8i+j] in
+ *          bits 4j..4j+3 (packed = (w7<<28)|...|(w1<<4)|w0), unsigned 0..15.
+ * scale, zero  [N] of `dtype`.
+ * x        [C][K] of `dtype`, row-major.
+ * d        [C][N] of `dtype`, row-major (output).
+ * All pointers 16-byte aligned.  K % 8 == 0 (the caller pads K), 1 <= C <= 8,
+ * N >= 0.  K == 0 gives d = 0.  Accumulation is fp32; with dtype W4_BF16 the
+ * result is rounded once to bf16.  The difference from the exact value is
+ * bounded by the parity tolerance of the test suite (2e-3 * sum_k |w*x|
+ * for bf16, 1e-5 * sum_k |w*x| for fp32).
+ */
+w4_status gemv_w4(const void* qweight, const void* scale, const void* zero, const void* x, void* d,
+                  int64_t N, int64_t K, int64_t C, w4_dtype dtype, void* stream);
+
+/*
+ * gemm_w4 -- large-M bf16 x int4 dequant GEMM on the tcgen05 tensor cores.
+ *
+ *   C[m][n] = scale[n] * sum_k A[m][k] * (u[k][n] - zero[n])
+ *
+ * A      bf16 [M][K] row-major.
+ * B      int8 [K/2][N] row-major; byte (kp, n) holds u[2kp][n] in its low
+ *        nibble and u[2kp+1][n] in its high nibble, both unsigned 0..15.
+ * scale, zero  bf16 [N].
+ * C      bf16 [M][N] row-major (output).
+ * All pointers 16-byte aligned.  Requires M, N, K >= 0 with K % 64 == 0 and
+ * N % 8 == 0 (so that every row of A, B and C starts on a 16-byte
+ * boundary); any M.  K == 0 gives C = 0.  Products are bf16 x bf16 on the
+ * tensor cores with fp32 accumulation; the dequantised weight (u - zero[n])
+ * is formed in bf16 (exact whenever it is representable, e.g. for integer
+ * zero points) and the result is rounded once to bf16.
+ */
+w4_status gemm_w4(const void* A, const void* B, const void* scale, const void* zero, void* C,
+                  int64_t M, int64_t N, int64_t K, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* W4_H_ */

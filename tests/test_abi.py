@@ -1,0 +1,100 @@
+"""Host-only checks of the C ABI: the library builds, loads without a GPU,
+exports every symbol include/w4.h declares, and rejects bad arguments on the
+host before touching the device (no compute is launched here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from helpers import ROOT
+
+
+def _lib():
+    from gemm_int4_dequant_gb300.build import build_library
+    build_library()
+    from gemm_int4_dequant_gb300 import _lib as L
+    return L.load(), L
+
+
+def _declared_functions():
+    src = open(os.path.join(ROOT, "include", "w4.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w]*\s*\**\s+\**(\w+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_hot_path():
+    names = _declared_functions()
+    for fn in ("quantize_pack_int4", "permute_int4", "gemv_w4", "gemm_w4", "w4_status_string",
+               "w4_abi_version", "w4_device_error"):
+        assert fn in names
+
+
+def test_library_exports_every_declared_symbol():
+    lib, _ = _lib()
+    for fn in _declared_functions():
+        assert hasattr(lib, fn), "libw4.so does not export %s" % fn
+    assert lib.w4_abi_version() == 1
+    assert lib.w4_status_string(-2) == b"illegal size or shape"
+
+
+def test_library_has_no_oracle_dependency():
+    from gemm_int4_dequant_gb300._lib import LIB_PATH
+    data = open(LIB_PATH, "rb").read()
+    assert b"w4o_" not in data, "product library references the oracle"
+    pkg = os.path.join(ROOT, "gemm_int4_dequant_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f), errors="ignore").read()
+                assert "import oracle" not in text and "from oracle" not in text and "w4_oracle" not in text, f
+
+
+def test_argument_validation_happens_on_host():
+    lib, L = _lib()
+    A = 0x10000  # 16-byte aligned dummy addresses, never dereferenced
+    odd = 0x10008
+    # quantize_pack_int4
+    assert lib.quantize_pack_int4(A, A, A, 3, 8, None) == L.W4_ERR_SHAPE
+    assert lib.quantize_pack_int4(A, A, A, -2, 8, None) == L.W4_ERR_SHAPE
+    assert lib.quantize_pack_int4(A, A, A, 4, 0, None) == L.W4_OK  # N == 0: no-op
+    assert lib.quantize_pack_int4(None, A, A, 4, 8, None) == L.W4_ERR_NULL
+    assert lib.quantize_pack_int4(odd, A, A, 4, 8, None) == L.W4_ERR_ALIGN
+    # permute_int4
+    assert lib.permute_int4(A, A, 96, 8, None) == L.W4_ERR_SHAPE
+    assert lib.permute_int4(A, A, 64, 6, None) == L.W4_ERR_SHAPE
+    assert lib.permute_int4(A, A, 0, 8, None) == L.W4_OK
+    assert lib.permute_int4(A, None, 64, 8, None) == L.W4_ERR_NULL
+    assert lib.permute_int4(A, odd, 64, 8, None) == L.W4_ERR_ALIGN
+    # gemv_w4
+    assert lib.gemv_w4(A, A, A, A, A, 16, 12, 1, L.W4_BF16, None) == L.W4_ERR_SHAPE
+    assert lib.gemv_w4(A, A, A, A, A, 16, 16, 0, L.W4_BF16, None) == L.W4_ERR_SHAPE
+    assert lib.gemv_w4(A, A, A, A, A, 16, 16, 9, L.W4_BF16, None) == L.W4_ERR_SHAPE
+    assert lib.gemv_w4(A, A, A, A, A, 16, 16, 1, 7, None) == L.W4_ERR_DTYPE
+    assert lib.gemv_w4(A, A, None, A, A, 16, 16, 1, L.W4_F32, None) == L.W4_ERR_NULL
+    assert lib.gemv_w4(A, A, A, odd, A, 16, 16, 1, L.W4_F32, None) == L.W4_ERR_ALIGN
+    assert lib.gemv_w4(A, A, A, A, A, 0, 16, 1, L.W4_F32, None) == L.W4_OK
+    # gemm_w4
+    assert lib.gemm_w4(A, A, A, A, A, 128, 256, 100, None) == L.W4_ERR_SHAPE
+    assert lib.gemm_w4(A, A, A, A, A, 128, 250, 128, None) == L.W4_ERR_SHAPE
+    assert lib.gemm_w4(A, None, A, A, A, 128, 256, 128, None) == L.W4_ERR_NULL
+    assert lib.gemm_w4(A, A, A, odd, A, 128, 256, 128, None) == L.W4_ERR_ALIGN
+    assert lib.gemm_w4(A, A, A, A, A, 0, 256, 128, None) == L.W4_OK
+
+
+def test_valid_call_without_gpu_reports_device_error():
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    lib, L = _lib()
+    A = 0x10000
+    assert lib.gemv_w4(A, A, A, A, A, 16, 16, 1, L.W4_F32, None) == L.W4_ERR_DEVICE
+
+
+def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
+    from gemm_int4_dequant_gb300 import _lib as L
+    monkeypatch.setattr(L, "_lib", None)
+    monkeypatch.setattr(L, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(ImportError):
+        L.load()

@@ -1,0 +1,225 @@
+"""GPU parity: every CUDA entry point against the CPU oracle.
+
+Pack and permute must match bit-exactly; products must satisfy
+|gpu - exact| <= tol * sum_k |w * x| per output, with tol = 2e-3 for bf16
+inputs and 1e-5 for the fp32-input GEMV.  Inputs come from the seeded
+generators in synth/, shaped like the pages' workloads, at full size and at
+small sizes with ragged tails and degenerate cases.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from synth import np_bits
+
+pytestmark = pytest.mark.gpu
+
+BF16_TOL = 2e-3
+F32_TOL = 1e-5
+
+
+@pytest.fixture(scope="module")
+def w4():
+    import gemm_int4_dequant_gb300 as m
+    return m
+
+
+def _dev():
+    return torch.device("cuda:0")
+
+
+def _guarded(n_elems, dtype, fill):
+    """A contiguous view of n_elems with 64-byte guard bands on both sides."""
+    esz = torch.tensor([], dtype=dtype).element_size()
+    pad = 64 // esz
+    buf = torch.full((n_elems + 2 * pad,), fill, dtype=dtype, device=_dev())
+    return buf, buf[pad:pad + n_elems], pad
+
+
+def _guards_intact(buf, pad, n_elems, fill):
+    return bool(torch.all(buf[:pad] == fill)) and bool(torch.all(buf[pad + n_elems:] == fill))
+
+
+# ---------------------------------------------------------------------------
+# quantize_pack_int4 + permute_int4 (bit-exact)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("K,N", [(2, 8), (128, 64), (130, 37), (64, 1), (1024, 1000), (8192, 8192)])
+def test_quantize_pack_bit_exact(w4, K, N):
+    W = synth.quant_inputs(K, N, seed=K + N)
+    if N > 3:
+        W[:, 3] = 0  # a column of zeros: scale 0, q 0
+    buf, packed, pad = _guarded((K // 2) * N, torch.uint8, 0xA5)
+    packed, scale = w4.quantize_pack_int4(W.to(_dev()), packed=packed)
+    s_ref, p_ref = oracle.quantize_pack(np_bits(W))
+    assert np.array_equal(scale.cpu().numpy().view(np.uint32), s_ref.view(np.uint32))
+    assert np.array_equal(packed.cpu().numpy().reshape(K // 2, N), p_ref)
+    assert _guards_intact(buf, pad, (K // 2) * N, 0xA5)
+
+
+def test_quantize_pack_k_zero(w4):
+    scale = torch.full((16,), 3.0, device=_dev())
+    w4.quantize_pack_int4(torch.empty((0, 16), dtype=torch.bfloat16, device=_dev()), scale=scale)
+    assert torch.all(scale == 0)
+
+
+@pytest.mark.parametrize("K,N", [(64, 4), (128, 132), (1024, 4096), (8192, 8192)])
+def test_permute_bit_exact(w4, K, N):
+    g = torch.Generator().manual_seed(K * 7 + N)
+    packed = torch.randint(0, 256, (K // 2, N), dtype=torch.uint8, generator=g)
+    buf, out, pad = _guarded(N * K // 2, torch.uint8, 0x5A)
+    w4.permute_int4(packed.to(_dev()), out=out)
+    ref = oracle.permute(packed.numpy(), K, N)
+    assert np.array_equal(out.cpu().numpy(), ref)
+    assert _guards_intact(buf, pad, N * K // 2, 0x5A)
+
+
+def test_quantize_pack_permute_chain_full_size(w4):
+    cfg = synth.QUANT
+    W = synth.quant_inputs(cfg["K"], cfg["N"], seed=0)
+    packed, scale = w4.quantize_pack_int4(W.to(_dev()))
+    out = w4.permute_int4(packed)
+    s_ref, p_ref = oracle.quantize_pack(np_bits(W))
+    assert np.array_equal(scale.cpu().numpy(), s_ref)
+    assert np.array_equal(np_bits(out.cpu()), oracle.permute(p_ref, cfg["K"], cfg["N"]))
+
+
+# ---------------------------------------------------------------------------
+# gemv_w4
+# ---------------------------------------------------------------------------
+
+def _check_gemv(w4, N, K, C, act, seed=0, **kw):
+    g = synth.gemv_inputs(N, K, C, act=act, seed=seed, **kw)
+    dt = torch.float32 if act == "f32" else torch.bfloat16
+    buf, out, pad = _guarded(C * N, dt, -7.0)
+    w4.gemv_w4(g.qweight.to(_dev()), g.scale.to(_dev()), g.zero.to(_dev()), g.x.to(_dev()), out=out)
+    code = oracle.F32 if act == "f32" else oracle.BF16
+    ref, ref_abs = oracle.gemv(np_bits(g.qweight), np_bits(g.scale), np_bits(g.zero), np_bits(g.x), code)
+    got = out.float().cpu().numpy().astype(np.float64).reshape(C, N)
+    tol = F32_TOL if act == "f32" else BF16_TOL
+    err = np.abs(got - ref)
+    bad = err > tol * ref_abs
+    assert not bad.any(), "max err/ref_abs = %g at %s" % ((err / ref_abs).max(), np.argwhere(bad)[:5])
+    assert _guards_intact(buf, pad, C * N, -7.0)
+
+
+def test_gemv_tiny_f32(w4):
+    _check_gemv(w4, **synth.TINY)
+
+
+def test_gemv_decode_full_size(w4):
+    _check_gemv(w4, **synth.DECODE)
+
+
+@pytest.mark.parametrize("cfg", synth.SMALL_BATCH, ids=lambda c: "N%dK%dC%d" % (c["N"], c["K"], c["C"]))
+def test_gemv_small_batch_full_size(w4, cfg):
+    _check_gemv(w4, **cfg)
+
+
+@pytest.mark.parametrize("N,K,C,act", [
+    (1, 8, 1, "bf16"),          # smallest legal problem
+    (77, 520, 3, "bf16"),       # K % 32 != 0: single-word loads
+    (130, 1000, 8, "f32"),      # K % 32 == 8
+    (300, 4096, 2, "bf16"),
+    (65, 2048, 5, "f32"),
+    (63, 64, 6, "bf16"),        # fewer rows than one CTA tile
+    (1000, 40000, 2, "bf16"),   # long K: split across a cluster
+    (333, 24008, 7, "bf16"),    # long ragged K, cluster split, word loads
+    (257, 12288, 8, "f32"),     # fp32 x split across a cluster
+])
+def test_gemv_ragged_and_edge(w4, N, K, C, act):
+    _check_gemv(w4, N, K, C, act, seed=N + K + C)
+
+
+def test_gemv_non_integer_zero_and_wide_scales(w4):
+    _check_gemv(w4, 500, 2048, 4, "bf16", seed=3, zero_value=7.3, scale_range=(0.5, 4.0))
+    _check_gemv(w4, 500, 2048, 2, "f32", seed=4, zero_value=0.013, scale_range=(1e-3, 1.0))
+
+
+def test_gemv_k_zero_gives_zero(w4):
+    x = torch.empty((2, 0), dtype=torch.bfloat16, device=_dev())
+    q = torch.empty((16, 0), dtype=torch.int32, device=_dev())
+    s = torch.ones(16, dtype=torch.bfloat16, device=_dev())
+    out = torch.full((2, 16), 5.0, dtype=torch.bfloat16, device=_dev())
+    w4.gemv_w4(q, s, s, x, out=out)
+    assert torch.all(out == 0)
+
+
+def test_gemv_through_raw_c_abi(w4):
+    from gemm_int4_dequant_gb300 import _lib as L
+    g = synth.gemv_inputs(96, 256, 2, act="bf16", seed=9)
+    q, s, z, x = (t.to(_dev()) for t in (g.qweight, g.scale, g.zero, g.x))
+    d = torch.empty((2, 96), dtype=torch.bfloat16, device=_dev())
+    st = L.load().gemv_w4(q.data_ptr(), s.data_ptr(), z.data_ptr(), x.data_ptr(), d.data_ptr(), 96, 256, 2,
+                          L.W4_BF16, torch.cuda.current_stream().cuda_stream)
+    assert st == 0
+    ref, ref_abs = oracle.gemv(np_bits(g.qweight), np_bits(g.scale), np_bits(g.zero), np_bits(g.x), oracle.BF16)
+    assert np.all(np.abs(d.float().cpu().numpy() - ref) <= BF16_TOL * ref_abs)
+
+
+# ---------------------------------------------------------------------------
+# gemm_w4
+# ---------------------------------------------------------------------------
+
+def _check_gemm_full(w4, M, N, K, seed=0, **kw):
+    gi = synth.gemm_inputs(M, N, K, seed=seed, **kw)
+    buf, out, pad = _guarded(M * N, torch.bfloat16, -3.0)
+    w4.gemm_w4(gi.A.to(_dev()), gi.B.to(_dev()), gi.scale.to(_dev()), gi.zero.to(_dev()), out=out)
+    ref, ref_abs = oracle.gemm_full(np_bits(gi.A), gi.B.numpy(), np_bits(gi.scale), np_bits(gi.zero))
+    got = out.float().cpu().numpy().astype(np.float64).reshape(M, N)
+    err = np.abs(got - ref)
+    bad = err > BF16_TOL * ref_abs
+    assert not bad.any(), "max err/ref_abs = %g at %s" % ((err / ref_abs).max(), np.argwhere(bad)[:5])
+    assert _guards_intact(buf, pad, M * N, -3.0)
+    assert w4.device_error() == 0
+
+
+@pytest.mark.parametrize("M,N,K", [
+    (128, 256, 64),     # one tile, one k-tile
+    (256, 512, 256),
+    (200, 264, 128),    # ragged M and N
+    (1, 8, 64),         # degenerate
+    (300, 1000, 1024),
+    (129, 520, 512),
+])
+def test_gemm_small(w4, M, N, K):
+    _check_gemm_full(w4, M, N, K, seed=M + N + K)
+
+
+def test_gemm_non_integer_zero_random_scale(w4):
+    _check_gemm_full(w4, 256, 512, 512, seed=11, zero_value=7.5, random_scale=True)
+    _check_gemm_full(w4, 256, 256, 256, seed=12, zero_value=0.013, random_scale=True)
+
+
+def test_gemm_full_size_sampled(w4):
+    cfg = synth.GEMM
+    M, N, K = cfg["M"], cfg["N"], cfg["K"]
+    gi = synth.gemm_inputs(M, N, K, seed=0)
+    C = w4.gemm_w4(gi.A.to(_dev()), gi.B.to(_dev()), gi.scale.to(_dev()), gi.zero.to(_dev()))
+    assert w4.device_error() == 0
+    Cn = C.float().cpu().numpy().astype(np.float64)
+    rng = np.random.default_rng(0)
+    mi = list(rng.integers(0, M, 65536))
+    ni = list(rng.integers(0, N, 65536))
+    # full rows and columns at tile edges
+    for m in (0, 127, 128, M - 1):
+        mi += [m] * N
+        ni += list(range(N))
+    for n in (0, 255, 256, N - 1):
+        mi += list(range(M))
+        ni += [n] * M
+    mi, ni = np.array(mi), np.array(ni)
+    ref, ref_abs = oracle.gemm_at(np_bits(gi.A), gi.B.numpy(), np_bits(gi.scale), np_bits(gi.zero), mi, ni)
+    err = np.abs(Cn[mi, ni] - ref)
+    assert np.all(err <= BF16_TOL * ref_abs), "max err/ref_abs %g" % (err / ref_abs).max()
+
+
+def test_gemm_k_zero(w4):
+    A = torch.empty((4, 0), dtype=torch.bfloat16, device=_dev())
+    B = torch.empty((0, 16), dtype=torch.uint8, device=_dev())
+    s = torch.ones(16, dtype=torch.bfloat16, device=_dev())
+    out = torch.full((4, 16), 2.0, dtype=torch.bfloat16, device=_dev())
+    w4.gemm_w4(A, B, s, s, out=out)
+    assert torch.all(out == 0)
