@@ -30,3 +30,23 @@ def bf16_values(bits):
     """float64 values of uint16 bf16 bit patterns, converted by torch."""
     t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
     return t.double().numpy()
+
+
+def bf16_half_ulp(ref):
+    """Half a bf16 ulp at |ref|: the largest error of rounding the exact value
+    to the bf16 output (bf16 carries 8 significant bits)."""
+    ref = np.abs(np.asarray(ref, dtype=np.float64))
+    _, e = np.frexp(ref)           # ref = m * 2**e, 0.5 <= m < 1
+    h = np.ldexp(1.0, e - 9)
+    return np.where(ref > 0, h, 0.0)
+
+
+def parity_violations(got, ref, ref_abs, tol, bf16_out):
+    """Boolean mask of outputs outside |got - ref| <= tol * ref_abs (+ the
+    half-ulp rounding of a bf16 output).  The accumulation tolerance bounds
+    the value before it is stored; storing it as bf16 adds at most half an
+    ulp, which alone can exceed tol * ref_abs when |ref| is close to ref_abs
+    (short K)."""
+    err = np.abs(np.asarray(got, dtype=np.float64) - ref)
+    bound = tol * ref_abs + (bf16_half_ulp(ref) if bf16_out else 0.0)
+    return err > bound

@@ -11,8 +11,8 @@ from helpers import ROOT
 
 
 def _lib():
-    from gemm_int4_dequant_gb300.build import build_library
-    build_library()
+    import __graft_entry__
+    __graft_entry__._load_builder().build_library()
     from gemm_int4_dequant_gb300 import _lib as L
     return L.load(), L
 

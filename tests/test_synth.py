@@ -34,3 +34,13 @@ def test_gemm_and_quant_inputs():
     w = synth.quant_inputs(64, 32, seed=0)
     assert w.dtype == torch.bfloat16 and w.shape == (64, 32)
     assert torch.equal(w, synth.quant_inputs(64, 32, seed=0))
+
+
+def test_bf16_half_ulp_helper():
+    import sys
+    from helpers import bf16_half_ulp, parity_violations
+    assert list(bf16_half_ulp([1.0, 1.5, 255.0, 256.0, 0.0, -3.0])) == [2**-8, 2**-8, 0.5, 1.0, 0.0, 2**-7]
+    # a correctly rounded bf16 value of 1 + 2**-8 + tiny passes, a value two ulps off fails
+    ref = np.array([1.0 + 2**-8 + 1e-6])
+    assert not parity_violations(np.array([1.0]), ref, np.array([1.0]), 2e-3, True).any()
+    assert parity_violations(np.array([1.0 - 2**-6]), ref, np.array([1.0]), 2e-3, True).any()
