@@ -102,7 +102,7 @@ w4_status gemv_w4(const void* qweight, const void* scale, const void* zero, cons
 
 w4_status gemm_w4(const void* A, const void* B, const void* scale, const void* zero, void* C, int64_t M, int64_t N,
                   int64_t K, void* stream) {
-    if (M < 0 || N < 0 || K < 0 || (K % 64) != 0 || (N % 8) != 0) return W4_ERR_SHAPE;
+    if (M < 0 || N < 0 || K < 0 || (K % 64) != 0 || (N % 16) != 0) return W4_ERR_SHAPE;
     if (M == 0 || N == 0) return W4_OK;
     if (!C || !scale || !zero || (K > 0 && (!A || !B))) return W4_ERR_NULL;
     if (!aligned16(C) || !aligned16(scale) || !aligned16(zero) || (K > 0 && (!aligned16(A) || !aligned16(B))))

@@ -147,8 +147,8 @@ w4_status gemv_w4(const void* qweight, const void* scale, const void* zero, cons
  * scale, zero  bf16 [N].
  * C      bf16 [M][N] row-major (output).
  * All pointers 16-byte aligned.  Requires M, N, K >= 0 with K % 64 == 0 and
- * N % 8 == 0 (so that every row of A, B and C starts on a 16-byte
- * boundary); any M.  K == 0 gives C = 0.  Products are bf16 x bf16 on the
+ * N % 16 == 0 (so that every row of A, B and C starts on a 16-byte
+ * boundary, as the tensor-memory-access copies need); any M.  K == 0 gives C = 0.  Products are bf16 x bf16 on the
  * tensor cores with fp32 accumulation; the dequantised weight (u - zero[n])
  * is formed in bf16 (exact whenever it is representable, e.g. for integer
  * zero points) and the result is rounded once to bf16.

@@ -78,6 +78,7 @@ def test_argument_validation_happens_on_host():
     # gemm_w4
     assert lib.gemm_w4(A, A, A, A, A, 128, 256, 100, None) == L.W4_ERR_SHAPE
     assert lib.gemm_w4(A, A, A, A, A, 128, 250, 128, None) == L.W4_ERR_SHAPE
+    assert lib.gemm_w4(A, A, A, A, A, 128, 264, 128, None) == L.W4_ERR_SHAPE
     assert lib.gemm_w4(A, None, A, A, A, 128, 256, 128, None) == L.W4_ERR_NULL
     assert lib.gemm_w4(A, A, A, odd, A, 128, 256, 128, None) == L.W4_ERR_ALIGN
     assert lib.gemm_w4(A, A, A, A, A, 0, 256, 128, None) == L.W4_OK

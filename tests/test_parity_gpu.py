@@ -180,10 +180,10 @@ def _check_gemm_full(w4, M, N, K, seed=0, **kw):
 @pytest.mark.parametrize("M,N,K", [
     (128, 256, 64),     # one tile, one k-tile
     (256, 512, 256),
-    (200, 264, 128),    # ragged M and N
-    (1, 8, 64),         # degenerate
+    (200, 272, 128),    # ragged M and N (N % 256 != 0)
+    (1, 16, 64),        # degenerate
     (300, 1000, 1024),
-    (129, 520, 512),
+    (129, 528, 512),
 ])
 def test_gemm_small(w4, M, N, K):
     _check_gemm_full(w4, M, N, K, seed=M + N + K)
