@@ -274,11 +274,17 @@ w4_status dispatch_c(const void* qw, const void* scale, const void* zero, const 
 
 }  // namespace
 
+w4_status run_gemv_mma(const void* qw, const void* scale, const void* zero, const void* x, void* d, int N, int K,
+                       int C, cudaStream_t stream);
+
 w4_status run_gemv(const void* qw, const void* scale, const void* zero, const void* x, void* d, int64_t N,
                    int64_t K, int64_t C, w4_dtype dtype, cudaStream_t stream) {
     if (N > (1 << 30) || K > (1 << 30) || (N + GV_ROWS - 1) / GV_ROWS > 65535) return W4_ERR_SHAPE;
     const bool vec = (K % 32) == 0;
     const int n = static_cast<int>(N), k = static_cast<int>(K), c = static_cast<int>(C);
+    // bf16 with 16-byte aligned rows: tensor-core MMA path; otherwise the
+    // CUDA-core path (fp32 inputs need fp32 products; odd K needs word loads)
+    if (dtype == W4_BF16 && vec) return run_gemv_mma(qw, scale, zero, x, d, n, k, c, stream);
     if (dtype == W4_F32)
         return vec ? dispatch_c<float, true>(qw, scale, zero, x, d, n, k, c, stream)
                    : dispatch_c<float, false>(qw, scale, zero, x, d, n, k, c, stream);
