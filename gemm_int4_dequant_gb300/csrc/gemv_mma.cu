@@ -91,9 +91,12 @@ gemv_mma_kernel(const uint32_t* __restrict__ qw, const __nv_bfloat16* __restrict
     const int nkb = (klen + KB - 1) / KB;
     const int ntiles = (nrows + 15) / 16;
 
+    // The layout must be identical in every CTA of a cluster (peers read
+    // part/xsum at this CTA's offsets), so it is sized for the longest slice.
     uint4* xf = reinterpret_cast<uint4*>(smem);
     const int xf_entries = nkb * 4 * C * 4;
-    float* part = reinterpret_cast<float*>(smem + static_cast<size_t>(xf_entries) * 16);
+    const int xf_cap = ((kslice + KB - 1) / KB) * 4 * C * 4;
+    float* part = reinterpret_cast<float*>(smem + static_cast<size_t>(xf_cap) * 16);
     float* slot = part + rows_cap * C;
     float* xsum = slot + slot_floats(C);
     int* tspan = reinterpret_cast<int*>(xsum + C);  // [WARPS][2]: first, last tile
