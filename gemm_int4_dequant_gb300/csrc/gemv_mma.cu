@@ -44,20 +44,31 @@ constexpr int THREADS = WARPS * 32;
 constexpr int PF = 4;            // units of loads in flight per warp
 constexpr int KB = 128;          // k per unit
 
-__device__ __forceinline__ uint32_t bsub2(uint32_t a, uint32_t b) {
+// Word of 8 nibbles -> 4 bf16x2 of (q - 8): pair h = (nibble h, nibble h+4).
+// Each pair is one mask-and-OR into the mantissa of 128.0 (exact 128 + q)
+// and one bf16x2 FMA (x * 1 - 136, exact).  The right shifts by 4, 8, 12 are
+// done as multiply-high by 2^28, 2^24, 2^20 passed in at run time (m[0..2]),
+// which keeps them on the FMA pipe and off the integer ALU pipe that the
+// mask-and-ORs already load.
+__device__ __forceinline__ uint32_t bfma2(uint32_t a, uint32_t b, uint32_t c) {
     uint32_t d;
-    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
     return d;
 }
 
-// Word of 8 nibbles -> 4 bf16x2 of (q - 8): pair h = (nibble h, nibble h+4).
-__device__ __forceinline__ void dequant_word(uint32_t w, uint32_t (&p)[4]) {
-    const uint32_t magic = 0x43004300u;   // (128, 128)
-    const uint32_t off = 0x43084308u;     // (136, 136)
-    p[0] = bsub2((w & 0x000F000Fu) | magic, off);
-    p[1] = bsub2(((w >> 4) & 0x000F000Fu) | magic, off);
-    p[2] = bsub2(((w >> 8) & 0x000F000Fu) | magic, off);
-    p[3] = bsub2(((w >> 12) & 0x000F000Fu) | magic, off);
+struct DequantConsts {
+    uint32_t m4, m8, m12;  // 2^28, 2^24, 2^20
+};
+
+__device__ __forceinline__ void dequant_word(uint32_t w, const DequantConsts& k, uint32_t (&p)[4]) {
+    const uint32_t mask = 0x000F000Fu, magic = 0x43004300u;  // bf16x2 (128, 128)
+    const uint32_t one = 0x3F803F80u;                          // bf16x2 (1, 1)
+    const uint32_t neg136 = 0xC308C308u;                       // bf16x2 (-136, -136)
+    const uint32_t w4 = __umulhi(w, k.m4), w8 = __umulhi(w, k.m8), w12 = __umulhi(w, k.m12);
+    p[0] = bfma2((w & mask) | magic, one, neg136);
+    p[1] = bfma2((w4 & mask) | magic, one, neg136);
+    p[2] = bfma2((w8 & mask) | magic, one, neg136);
+    p[3] = bfma2((w12 & mask) | magic, one, neg136);
 }
 
 __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
@@ -78,7 +89,8 @@ template <int C>
 __global__ void __launch_bounds__(THREADS, 1)
 gemv_mma_kernel(const uint32_t* __restrict__ qw, const __nv_bfloat16* __restrict__ scale,
                 const __nv_bfloat16* __restrict__ zero, const __nv_bfloat16* __restrict__ x,
-                __nv_bfloat16* __restrict__ d, int N, int K, int kslice, int groups, int rows_cap, int S) {
+                __nv_bfloat16* __restrict__ d, int N, int K, int kslice, int groups, int rows_cap, int S,
+                DequantConsts dqk) {
     extern __shared__ __align__(16) uint8_t smem[];
     const int ks = blockIdx.x % S;           // K-slice = rank in the cluster
     const int grp = blockIdx.x / S;          // row group
@@ -96,7 +108,8 @@ gemv_mma_kernel(const uint32_t* __restrict__ qw, const __nv_bfloat16* __restrict
     uint4* xf = reinterpret_cast<uint4*>(smem);
     const int xf_entries = nkb * 4 * C * 4;
     const int xf_cap = ((kslice + KB - 1) / KB) * 4 * C * 4;
-    float* part = reinterpret_cast<float*>(smem + static_cast<size_t>(xf_cap) * 16);
+    uint4* xzero = xf + xf_cap;                     // 16 zero entries for padding lanes
+    float* part = reinterpret_cast<float*>(smem + static_cast<size_t>(xf_cap + 16) * 16);
     float* slot = part + rows_cap * C;
     float* xsum = slot + slot_floats(C);
     int* tspan = reinterpret_cast<int*>(xsum + C);  // [WARPS][2]: first, last tile
@@ -110,27 +123,35 @@ gemv_mma_kernel(const uint32_t* __restrict__ qw, const __nv_bfloat16* __restrict
     const int u_begin = static_cast<int>((static_cast<int64_t>(warp) * units) / WARPS);
     const int u_end = static_cast<int>((static_cast<int64_t>(warp + 1) * units) / WARPS);
 
-    // issue the first PF units of weight loads before staging x (they do not
-    // depend on it), so HBM traffic starts at once
+    // Load cursor.  Rows past the end of the CTA's range and k past the end
+    // of the slice are clamped to the last valid row / 16-byte group instead
+    // of being predicated off: their weights then multiply zero x fragments
+    // (k) or are never flushed (rows), so no select is needed per load.
+    const int kw_last = klen / 8 - 4;              // last valid 16-byte group (words)
+    const uint32_t* qslice = qw + k0 / 8 + 4 * t4;
     uint4 buf[PF][2];
-    auto load_unit = [&](int tile, int kb, uint4 (&b)[2]) {
-        const int kofs = kb * KB + 32 * t4;           // within the slice
-        const int ra = tile * 16 + g, rb = ra + 8;
-        const bool kin = kofs < klen;
-        const uint32_t* base = qw + (k0 + kofs) / 8;
-        b[0] = (kin && ra < nrows) ? ldg_stream_u4(base + static_cast<int64_t>(r0 + ra) * kw) : make_uint4(0, 0, 0, 0);
-        b[1] = (kin && rb < nrows) ? ldg_stream_u4(base + static_cast<int64_t>(r0 + rb) * kw) : make_uint4(0, 0, 0, 0);
-    };
-    // (ltile, lkb): next unit to load; advanced without divisions
     int ltile = nkb > 0 ? u_begin / nkb : 0;
     int lkb = u_begin - ltile * nkb;
-#pragma unroll
-    for (int p = 0; p < PF; ++p) {
-        if (u_begin + p < u_end) {
-            load_unit(ltile, lkb, buf[p]);
-            if (++lkb == nkb) { lkb = 0; ++ltile; }
+    const uint32_t* la = nullptr;
+    const uint32_t* lb = nullptr;
+    auto set_rows = [&](int tile) {
+        const int ra = min(tile * 16 + g, nrows - 1), rb = min(tile * 16 + g + 8, nrows - 1);
+        la = qslice + static_cast<int64_t>(r0 + ra) * kw;
+        lb = qslice + static_cast<int64_t>(r0 + rb) * kw;
+    };
+    auto load_next = [&](uint4 (&b)[2]) {
+        const int wofs = min(lkb * 16, kw_last - 4 * t4);
+        b[0] = ldg_stream_u4(la + wofs);
+        b[1] = ldg_stream_u4(lb + wofs);
+        if (++lkb == nkb) {
+            lkb = 0;
+            set_rows(++ltile);
         }
-    }
+    };
+    if (u_begin < u_end) set_rows(ltile);
+#pragma unroll
+    for (int p = 0; p < PF; ++p)
+        if (u_begin + p < u_end) load_next(buf[p]);
 
     // ---- stage x as B fragments, and its per-row sums ----
     for (int e = tid; e < xf_entries; e += THREADS) {
@@ -147,6 +168,7 @@ gemv_mma_kernel(const uint32_t* __restrict__ qw, const __nv_bfloat16* __restrict
         }
         xf[e] = make_uint4(r[0], r[1], r[2], r[3]);
     }
+    if (tid < 16) xzero[tid] = make_uint4(0, 0, 0, 0);
     if (lane == 0) {
         tspan[2 * warp] = u_begin < u_end ? u_begin / nkb : -1;
         tspan[2 * warp + 1] = u_begin < u_end ? (u_end - 1) / nkb : -2;
@@ -182,6 +204,11 @@ gemv_mma_kernel(const uint32_t* __restrict__ qw, const __nv_bfloat16* __restrict
         acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
     };
 
+    // B fragments: lanes whose column is a real batch row read x, the others
+    // read the zero block
+    const uint4* xlane = bl ? xf + g * 4 + t4 : xzero + t4;
+    const int xw_stride = bl ? C * 4 : 4;          // entries between words
+    const int xkb_stride = bl ? 4 * C * 4 : 0;     // entries between k-blocks
     for (int ub = u_begin; ub < u_end; ub += PF) {
 #pragma unroll
         for (int p = 0; p < PF; ++p) {
@@ -192,20 +219,16 @@ gemv_mma_kernel(const uint32_t* __restrict__ qw, const __nv_bfloat16* __restrict
                     cur_tile = ctile;
                 }
                 const uint4 wa = buf[p][0], wb = buf[p][1];
-                if (u + PF < u_end) {
-                    load_unit(ltile, lkb, buf[p]);
-                    if (++lkb == nkb) { lkb = 0; ++ltile; }
-                }
-                const uint4* xb = xf + static_cast<size_t>(ckb) * 4 * C * 4;
+                if (u + PF < u_end) load_next(buf[p]);
+                const uint4* xb = xlane + ckb * xkb_stride;
                 const uint32_t wav[4] = {wa.x, wa.y, wa.z, wa.w};
                 const uint32_t wbv[4] = {wb.x, wb.y, wb.z, wb.w};
 #pragma unroll
                 for (int w = 0; w < 4; ++w) {
-                    uint4 bx = make_uint4(0, 0, 0, 0);
-                    if (bl) bx = xb[(w * C + g) * 4 + t4];
+                    const uint4 bx = xb[w * xw_stride];
                     uint32_t pa[4], pb[4];
-                    dequant_word(wav[w], pa);
-                    dequant_word(wbv[w], pb);
+                    dequant_word(wav[w], dqk, pa);
+                    dequant_word(wbv[w], dqk, pb);
                     const uint32_t a0[4] = {pa[0], pb[0], pa[1], pb[1]};
                     const uint32_t a1[4] = {pa[2], pb[2], pa[3], pb[3]};
                     mma_bf16(acc, a0, bx.x, bx.y);
@@ -278,7 +301,7 @@ w4_status launch_gemv_mma_t(const void* qw, const void* scale, const void* zero,
     // no more row groups than 16-row tiles
     groups = static_cast<int>(std::min<int64_t>(groups, (static_cast<int64_t>(N) + 15) / 16));
     const int rows_cap = (N + groups - 1) / groups;
-    const size_t smem = xf_bytes(S) + (static_cast<size_t>(rows_cap) * C + slot_floats(C) + C) * 4 + WARPS * 2 * 4;
+    const size_t smem = xf_bytes(S) + 256 + (static_cast<size_t>(rows_cap) * C + slot_floats(C) + C) * 4 + WARPS * 2 * 4;
     if (smem > 220 * 1024) return W4_ERR_SHAPE;
     auto kern = gemv_mma_kernel<C>;
     static int smem_set[64];
@@ -313,7 +336,7 @@ w4_status launch_gemv_mma_t(const void* qw, const void* scale, const void* zero,
     const int rows_cap2 = (N + groups - 1) / groups;
     if (rows_cap2 != rows_cap) {
         // fewer groups than planned: recompute the per-CTA row capacity
-        const size_t smem2 = xf_bytes(S) + (static_cast<size_t>(rows_cap2) * C + slot_floats(C) + C) * 4 + WARPS * 2 * 4;
+        const size_t smem2 = xf_bytes(S) + 256 + (static_cast<size_t>(rows_cap2) * C + slot_floats(C) + C) * 4 + WARPS * 2 * 4;
         if (smem2 > 220 * 1024) return W4_ERR_SHAPE;
         e = ensure_smem_limit(kern, static_cast<int>(smem2), smem_set);
         if (e != cudaSuccess) return W4_ERR_CUDA;
@@ -322,7 +345,8 @@ w4_status launch_gemv_mma_t(const void* qw, const void* scale, const void* zero,
     cfg.gridDim = dim3(S * groups, 1, 1);
     e = cudaLaunchKernelEx(&cfg, kern, static_cast<const uint32_t*>(qw), static_cast<const __nv_bfloat16*>(scale),
                            static_cast<const __nv_bfloat16*>(zero), static_cast<const __nv_bfloat16*>(x),
-                           static_cast<__nv_bfloat16*>(d), N, K, kslice, groups, rows_cap2, S);
+                           static_cast<__nv_bfloat16*>(d), N, K, kslice, groups, rows_cap2, S,
+                           DequantConsts{1u << 28, 1u << 24, 1u << 20});
     return launch_status(e);
 }
 
