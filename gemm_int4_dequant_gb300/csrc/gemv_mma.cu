@@ -154,34 +154,35 @@ gemv_mma_kernel(const uint32_t* __restrict__ qw, const __nv_bfloat16* __restrict
         if (u_begin + p < u_end) load_next(buf[p]);
 
     // ---- stage x as B fragments, and its per-row sums ----
-    for (int e = tid; e < xf_entries; e += THREADS) {
-        const int t = e & 3, n = (e >> 2) % C, rest = (e >> 2) / C, p = rest & 3, kb = rest >> 2;
-        const int kk = kb * KB + 32 * t + 8 * p;        // within the slice
-        uint32_t r[4] = {0, 0, 0, 0};
-        if (kk < klen) {
-            const uint4 raw = *reinterpret_cast<const uint4*>(x + static_cast<int64_t>(n) * K + k0 + kk);
-            // raw holds x[kk + 0..7] as bf16 pairs (0,1) (2,3) (4,5) (6,7)
-            r[0] = __byte_perm(raw.x, raw.z, 0x5410);  // (x0, x4)
-            r[1] = __byte_perm(raw.x, raw.z, 0x7632);  // (x1, x5)
-            r[2] = __byte_perm(raw.y, raw.w, 0x5410);  // (x2, x6)
-            r[3] = __byte_perm(raw.y, raw.w, 0x7632);  // (x3, x7)
-        }
-        xf[e] = make_uint4(r[0], r[1], r[2], r[3]);
-    }
-    if (tid < 16) xzero[tid] = make_uint4(0, 0, 0, 0);
-    if (lane == 0) {
-        tspan[2 * warp] = u_begin < u_end ? u_begin / nkb : -1;
-        tspan[2 * warp + 1] = u_begin < u_end ? (u_end - 1) / nkb : -2;
-    }
-    if (warp < C) {
-        float s = 0.f;
-        for (int i = lane; i < klen; i += 32) s += __bfloat162float(x[static_cast<int64_t>(warp) * K + k0 + i]);
+    // Entries are visited batch row by batch row so every thread's partial
+    // sum belongs to one row n; partials are reduced in a fixed order (lanes
+    // by shuffle tree, then warps in index order), so xsum is deterministic.
+    float* xsw = slot;  // [WARPS][C] warp partials (slots are free until the main loop ends)
+    const int per_n = nkb * 16;                    // entries per batch row
+    for (int n = 0; n < C; ++n) {
+        float xs_part = 0.f;
+        for (int j = tid; j < per_n; j += THREADS) {
+            const int t = j & 3, p = (j >> 2) & 3, kb = j >> 4;
+            const int kk = kb * KB + 32 * t + 8 * p;        // within the slice
+            uint32_t r[4] = {0, 0, 0, 0};
+            if (kk < klen) {
+                const uint4 raw = *reinterpret_cast<const uint4*>(x + static_cast<int64_t>(n) * K + k0 + kk);
+                // raw holds x[kk + 0..7] as bf16 pairs (0,1) (2,3) (4,5) (6,7)
+                r[0] = __byte_perm(raw.x, raw.z, 0x5410);  // (x0, x4)
+                r[1] = __byte_perm(raw.x, raw.z, 0x7632);  // (x1, x5)
+                r[2] = __byte_perm(raw.y, raw.w, 0x5410);  // (x2, x6)
+                r[3] = __byte_perm(raw.y, raw.w, 0x7632);  // (x3, x7)
+                const uint32_t v[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-        if (lane == 0) xsum[warp] = s;
+                for (int q = 0; q < 4; ++q)
+                    xs_part += bf16_bits_to_f32(v[q] & 0xFFFFu) + bf16_bits_to_f32(v[q] >> 16);
+            }
+            xf[((kb * 4 + p) * C + n) * 4 + t] = make_uint4(r[0], r[1], r[2], r[3]);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) xs_part += __shfl_xor_sync(0xffffffffu, xs_part, o);
+        if (lane == 0) xsw[warp * C + n] = xs_part;
     }
-    __syncthreads();
-
     // ---- main loop ----
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     int ctile = nkb > 0 ? u_begin / nkb : 0;      // unit being computed
