@@ -183,6 +183,19 @@ gemv_mma_kernel(const uint32_t* __restrict__ qw, const __nv_bfloat16* __restrict
         for (int o = 16; o > 0; o >>= 1) xs_part += __shfl_xor_sync(0xffffffffu, xs_part, o);
         if (lane == 0) xsw[warp * C + n] = xs_part;
     }
+    if (tid < 16) xzero[tid] = make_uint4(0, 0, 0, 0);
+    if (lane == 0) {
+        tspan[2 * warp] = u_begin < u_end ? u_begin / nkb : -1;
+        tspan[2 * warp + 1] = u_begin < u_end ? (u_end - 1) / nkb : -2;
+    }
+    __syncthreads();
+    if (tid < C) {
+        float s = 0.f;
+        for (int w = 0; w < WARPS; ++w) s += xsw[w * C + tid];
+        xsum[tid] = s;
+    }
+    __syncthreads();  // xsw lives in the slots, which the main loop reuses
+
     // ---- main loop ----
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     int ctile = nkb > 0 ? u_begin / nkb : 0;      // unit being computed
