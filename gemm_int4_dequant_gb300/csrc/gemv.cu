@@ -274,7 +274,7 @@ w4_status dispatch_c(const void* qw, const void* scale, const void* zero, const 
 
 }  // namespace
 
-w4_status run_gemv_mma(const void* qw, const void* scale, const void* zero, const void* x, void* d, int N, int K,
+w4_status run_gemv_tma(const void* qw, const void* scale, const void* zero, const void* x, void* d, int N, int K,
                        int C, cudaStream_t stream);
 
 w4_status run_gemv(const void* qw, const void* scale, const void* zero, const void* x, void* d, int64_t N,
@@ -284,7 +284,7 @@ w4_status run_gemv(const void* qw, const void* scale, const void* zero, const vo
     const int n = static_cast<int>(N), k = static_cast<int>(K), c = static_cast<int>(C);
     // bf16 with 16-byte aligned rows: tensor-core MMA path; otherwise the
     // CUDA-core path (fp32 inputs need fp32 products; odd K needs word loads)
-    if (dtype == W4_BF16 && vec) return run_gemv_mma(qw, scale, zero, x, d, n, k, c, stream);
+    if (dtype == W4_BF16 && vec) return run_gemv_tma(qw, scale, zero, x, d, n, k, c, stream);
     if (dtype == W4_F32)
         return vec ? dispatch_c<float, true>(qw, scale, zero, x, d, n, k, c, stream)
                    : dispatch_c<float, false>(qw, scale, zero, x, d, n, k, c, stream);

@@ -39,9 +39,19 @@ namespace w4 {
 
 namespace gmma {
 
-constexpr int WARPS = 16;
+// Tuning knobs (compile-time).
+#ifndef W4_GEMV_WARPS
+#define W4_GEMV_WARPS 16
+#endif
+#ifndef W4_GEMV_PF
+#define W4_GEMV_PF 4
+#endif
+#ifndef W4_GEMV_MINB
+#define W4_GEMV_MINB 1
+#endif
+constexpr int WARPS = W4_GEMV_WARPS;
 constexpr int THREADS = WARPS * 32;
-constexpr int PF = 4;            // units of loads in flight per warp
+constexpr int PF = W4_GEMV_PF;   // units of loads in flight per warp
 constexpr int KB = 128;          // k per unit
 
 // Word of 8 nibbles -> 4 bf16x2 of (q - 8): pair h = (nibble h, nibble h+4).
@@ -86,7 +96,7 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], 
 __host__ __device__ constexpr size_t slot_floats(int C) { return static_cast<size_t>(WARPS) * 2 * 16 * C; }
 
 template <int C>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(THREADS, W4_GEMV_MINB)
 gemv_mma_kernel(const uint32_t* __restrict__ qw, const __nv_bfloat16* __restrict__ scale,
                 const __nv_bfloat16* __restrict__ zero, const __nv_bfloat16* __restrict__ x,
                 __nv_bfloat16* __restrict__ d, int N, int K, int kslice, int groups, int rows_cap, int S,
@@ -197,7 +207,10 @@ gemv_mma_kernel(const uint32_t* __restrict__ qw, const __nv_bfloat16* __restrict
     __syncthreads();  // xsw lives in the slots, which the main loop reuses
 
     // ---- main loop ----
+    // two independent accumulator chains (even / odd MMA of each word) halve
+    // the dependent-MMA chain per unit; they are added at flush
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    float acc2[4] = {0.f, 0.f, 0.f, 0.f};
     int ctile = nkb > 0 ? u_begin / nkb : 0;      // unit being computed
     int ckb = u_begin - ctile * nkb;
     int cur_tile = ctile;
@@ -210,6 +223,8 @@ gemv_mma_kernel(const uint32_t* __restrict__ qw, const __nv_bfloat16* __restrict
     // order so the rounding never depends on timing.
     auto flush = [&](int tile) {
         const int c0 = 2 * t4, c1 = 2 * t4 + 1;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) { acc[i] += acc2[i]; acc2[i] = 0.f; }
         float* dst = (tile == t_first || tile == t_last)
                          ? slot + (static_cast<size_t>(warp) * 2 + (tile == t_first ? 0 : 1)) * 16 * C
                          : part + static_cast<size_t>(tile) * 16 * C;
@@ -246,7 +261,7 @@ gemv_mma_kernel(const uint32_t* __restrict__ qw, const __nv_bfloat16* __restrict
                     const uint32_t a0[4] = {pa[0], pb[0], pa[1], pb[1]};
                     const uint32_t a1[4] = {pa[2], pb[2], pa[3], pb[3]};
                     mma_bf16(acc, a0, bx.x, bx.y);
-                    mma_bf16(acc, a1, bx.z, bx.w);
+                    mma_bf16(acc2, a1, bx.z, bx.w);
                 }
                 if (++ckb == nkb) { ckb = 0; ++ctile; }
             }

@@ -1,0 +1,411 @@
+// gemv_tma.cu -- fused dequant GEMV / small-batch multiply for bf16 x (C <= 8),
+// weights streamed by the tensor memory accelerator (TMA) into a shared-memory
+// ring and multiplied on the warp-level tensor-core MMA.
+//
+//   d[c][r] = sum_k (q[r][k] - zero[r]) * scale[r] * x[c][k]
+//
+// (page "怎样在安卓端利用 Vulkan 编写 4-bit 专用算子", sections 1-2: uint32 words
+// of eight nibbles, w0 in the low bits, dequant (q - zero) * scale in the dot
+// loop; batched form from "三值量化模型的无损压缩", section 3 "MMVQ".)
+//
+// GB300 design.  The op reads 0.5 B of weight per multiply-add, so HBM
+// bandwidth is the roofline.  One CTA per SM owns a contiguous, balanced row
+// range (and, when x does not fit, one K-slice of a thread-block cluster):
+//   * warp NC (producer) issues 2-D TMA copies of 16-row x 128-k boxes
+//     (1 KB each) into an NST-deep ring of 16-row x 2048-k stages, so about
+//     128 KB of loads are in flight per SM without spending registers;
+//   * warps 0..NC-1 (consumers) each take one 128-k block of every stage:
+//     two 16-byte shared loads give a lane its rows g and g+8, each uint32
+//     word becomes four bf16x2 pairs (nibbles j, j+4) with one mask-and-OR
+//     into the mantissa of 128.0 (exactly 128 + q), and two
+//     mma.sync.m16n8k16 per word accumulate in fp32 against x, which was
+//     staged once per CTA in B-fragment order;
+//   * per 16-row tile the NC partial sums are added in warp order (named
+//     barrier, double-buffered), so results never depend on timing;
+//   * the offset is folded out exactly at the end:
+//       sum_k (q - z) x = sum_k (128 + q) x - (128 + z) sum_k x,
+//     and K-slices are combined through distributed shared memory.
+// Every mbarrier wait is bounded (about two seconds); on timeout the kernel
+// records an error code (w4_device_error), stops issuing copies, drains the
+// ones in flight and returns.
+
+#include <cooperative_groups.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace cg = cooperative_groups;
+
+namespace w4 {
+
+namespace gtma {
+
+using namespace ptx;
+
+constexpr int NC = 16;                        // consumer warps
+constexpr int THREADS = (NC + 1) * 32;        // + one producer warp
+constexpr int CT = NC * 32;                   // consumer threads
+constexpr int KB = 128;                       // k per unit (one consumer warp per unit)
+constexpr int KC = NC * KB;                   // k per stage
+constexpr int NST = 8;                        // stages in the ring
+constexpr int BOX_BYTES = 16 * KB / 2;        // 16 rows x 64 B
+constexpr int BOX4_BYTES = 4 * KB / 2;        // 4 rows x 64 B
+constexpr int STAGE_BYTES = NC * BOX_BYTES;   // 16 KB
+
+struct Layout {
+    // byte offsets into dynamic shared memory (base aligned to 1 KB)
+    int xf, xzero, red, part, xsw, xsum, sz, bars, abort, total;
+};
+
+__host__ __device__ inline Layout make_layout(int C, int kslice, int rows_cap) {
+    Layout L;
+    const int nkb_cap = (kslice + KB - 1) / KB;
+    int o = NST * STAGE_BYTES;
+    L.xf = o;        o += nkb_cap * 16 * C * 16;
+    L.xzero = o;     o += 16 * 16;
+    L.red = o;       o += 2 * NC * 16 * C * 4;
+    L.part = o;      o += rows_cap * C * 4;
+    L.xsw = o;       o += NC * C * 4;
+    L.xsum = o;      o += 8 * 4;
+    L.sz = o;        o += rows_cap * 8;           // (scale, zero) per row as fp32
+    o = (o + 7) & ~7;
+    L.bars = o;      o += 2 * NST * 8;
+    L.abort = o;     o += 16;
+    L.total = o;
+    return L;
+}
+
+template <int C>
+__global__ void __launch_bounds__(THREADS, 1)
+gemv_tma_kernel(const __grid_constant__ CUtensorMap map16, const __grid_constant__ CUtensorMap map4,
+                const __nv_bfloat16* __restrict__ scale, const __nv_bfloat16* __restrict__ zero,
+                const __nv_bfloat16* __restrict__ x, __nv_bfloat16* __restrict__ d, int N, int K, int kslice,
+                int groups, int rows_cap, int S) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    uint8_t* sm = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+    const uint32_t sm_addr = smem_u32(sm);
+    const Layout L = make_layout(C, kslice, rows_cap);
+
+    const int ks = blockIdx.x % S;        // K-slice = rank in the cluster
+    const int grp = blockIdx.x / S;       // row group
+    const int64_t quads = (static_cast<int64_t>(N) + 3) / 4;
+    const int r0 = static_cast<int>(4 * ((grp * quads) / groups));
+    const int r1 = static_cast<int>((N < 4 * (((grp + 1) * quads) / groups) ? static_cast<int64_t>(N) : 4 * (((grp + 1) * quads) / groups)));
+    const int nrows = max(0, r1 - r0);
+    const int k0 = min(K, ks * kslice);
+    const int klen = min(K, k0 + kslice) - k0;   // multiple of 32
+    const int nkb = (klen + KB - 1) / KB;
+    const int nch = (klen + KC - 1) / KC;
+    const int ntiles = (nrows + 15) / 16;
+    const int nstages = ntiles * nch;
+
+    uint4* xf = reinterpret_cast<uint4*>(sm + L.xf);
+    uint4* xzero = reinterpret_cast<uint4*>(sm + L.xzero);
+    float* red = reinterpret_cast<float*>(sm + L.red);
+    float* part = reinterpret_cast<float*>(sm + L.part);
+    float* xsw = reinterpret_cast<float*>(sm + L.xsw);
+    float* xsum = reinterpret_cast<float*>(sm + L.xsum);
+    float2* sz = reinterpret_cast<float2*>(sm + L.sz);
+    const uint32_t bar_full = sm_addr + L.bars;
+    const uint32_t bar_empty = bar_full + NST * 8;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L.abort);
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+    if (tid == 0) {
+        for (int s = 0; s < NST; ++s) {
+            mbar_init(bar_full + 8 * s, 1);
+            mbar_init(bar_empty + 8 * s, NC);
+        }
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+
+    if (warp == NC) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0 && nstages > 0) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"(&map16) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(&map4) : "memory");
+            const uint64_t policy = l2_evict_first_policy();
+            int tile = 0, ch = 0, issued = 0;
+            for (int s = 0; s < nstages; ++s) {
+                const int slot = s % NST, round = s / NST;
+                if (round > 0 && !mbar_wait(bar_empty + 8 * slot, (round - 1) & 1, abort_flag)) break;
+                const int rows_here = min(16, nrows - tile * 16);
+                const int nvalid = min(NC, (klen - ch * KC + KB - 1) / KB);
+                const int xw = (k0 + ch * KC) / 8;          // word coordinate of the stage
+                const int y = r0 + tile * 16;
+                const uint32_t dst = sm_addr + slot * STAGE_BYTES;
+                if (rows_here == 16) {
+                    mbar_arrive_expect_tx(bar_full + 8 * slot, nvalid * BOX_BYTES);
+                    for (int kb = 0; kb < nvalid; ++kb)
+                        tma_load_2d_hint(dst + kb * BOX_BYTES, &map16, xw + kb * (KB / 8), y, bar_full + 8 * slot,
+                                         policy);
+                } else {
+                    const int nq = (rows_here + 3) / 4;
+                    mbar_arrive_expect_tx(bar_full + 8 * slot, nvalid * nq * BOX4_BYTES);
+                    for (int kb = 0; kb < nvalid; ++kb)
+                        for (int qd = 0; qd < nq; ++qd)
+                            tma_load_2d_hint(dst + kb * BOX_BYTES + qd * BOX4_BYTES, &map4, xw + kb * (KB / 8),
+                                             y + 4 * qd, bar_full + 8 * slot, policy);
+                }
+                issued = s + 1;
+                if (++ch == nch) { ch = 0; ++tile; }
+            }
+            // copies still landing if a consumer aborted
+            for (int s = max(0, issued - NST); s < issued; ++s) mbar_drain(bar_full + 8 * (s % NST), (s / NST) & 1);
+        }
+    } else {
+        // ------------------------------------------------------------ consumers
+        // scale / zero of this CTA's rows, early so their latency overlaps
+        for (int i = tid; i < nrows; i += CT)
+            sz[i] = make_float2(__bfloat162float(scale[r0 + i]), __bfloat162float(zero[r0 + i]));
+        // x as B fragments: entry (kb, word p, n, t4) holds, for kk = kb*128 +
+        // 32*t4 + 8*p, the bf16 pairs (x[kk], x[kk+4]) (x[kk+1], x[kk+5])
+        // (x[kk+2], x[kk+6]) (x[kk+3], x[kk+7]) -- the b0b1/b2b3 registers of
+        // the two MMAs that consume word p.  Loads are issued four at a time.
+        const int per_n = nkb * 16;
+        const int total = C * per_n;
+        float xs_part[C];
+#pragma unroll
+        for (int c = 0; c < C; ++c) xs_part[c] = 0.f;
+        for (int e0 = tid; e0 < total; e0 += 4 * CT) {
+            uint4 raw[4];
+            int ent[4];
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+                const int e = e0 + b * CT;
+                ent[b] = -1;
+                raw[b] = make_uint4(0, 0, 0, 0);
+                if (e < total) {
+                    const int n = e / per_n, j = e - n * per_n;
+                    const int t = j & 3, p = (j >> 2) & 3, kb = j >> 4;
+                    const int kk = kb * KB + 32 * t + 8 * p;
+                    ent[b] = e;
+                    if (kk < klen)
+                        raw[b] = *reinterpret_cast<const uint4*>(x + static_cast<int64_t>(n) * K + k0 + kk);
+                }
+            }
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+                if (ent[b] < 0) continue;
+                const int e = ent[b];
+                const int n = e / per_n, j = e - n * per_n;
+                const int t = j & 3, p = (j >> 2) & 3, kb = j >> 4;
+                const uint4 r = raw[b];
+                xf[((kb * 4 + p) * C + n) * 4 + t] =
+                    make_uint4(__byte_perm(r.x, r.z, 0x5410), __byte_perm(r.x, r.z, 0x7632),
+                               __byte_perm(r.y, r.w, 0x5410), __byte_perm(r.y, r.w, 0x7632));
+                const float v = bf16_bits_to_f32(r.x & 0xFFFFu) + bf16_bits_to_f32(r.x >> 16) +
+                                bf16_bits_to_f32(r.y & 0xFFFFu) + bf16_bits_to_f32(r.y >> 16) +
+                                bf16_bits_to_f32(r.z & 0xFFFFu) + bf16_bits_to_f32(r.z >> 16) +
+                                bf16_bits_to_f32(r.w & 0xFFFFu) + bf16_bits_to_f32(r.w >> 16);
+#pragma unroll
+                for (int c = 0; c < C; ++c)
+                    if (c == n) xs_part[c] += v;
+            }
+        }
+#pragma unroll
+        for (int c = 0; c < C; ++c) {
+            float v = xs_part[c];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+            if (lane == 0) xsw[warp * C + c] = v;
+        }
+        if (tid < 16) xzero[tid] = make_uint4(0, 0, 0, 0);
+        named_barrier(1, CT);
+        if (tid < C) {
+            float v = 0.f;
+            for (int w = 0; w < NC; ++w) v += xsw[w * C + tid];
+            xsum[tid] = v;
+        }
+
+        // main loop
+        const int g = lane >> 2, t4 = lane & 3;
+        const bool bl = g < C;
+        const uint4* xlane = bl ? xf + g * 4 + t4 : xzero + t4;
+        const int xw_stride = bl ? C * 4 : 4;
+        const int xkb_stride = bl ? 4 * C * 4 : 0;
+        const uint32_t mask = 0x000F000Fu, magic = 0x43004300u;  // bf16x2 (128, 128)
+        int s = 0;
+        for (int tile = 0; tile < ntiles; ++tile) {
+            float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int ch = 0; ch < nch; ++ch, ++s) {
+                const int slot = s % NST;
+                const bool ok = mbar_wait(bar_full + 8 * slot, (s / NST) & 1, abort_flag);
+                const int kk = ch * KC + warp * KB;
+                if (ok && kk < klen) {
+                    const uint8_t* st = sm + slot * STAGE_BYTES + warp * BOX_BYTES;
+                    const uint4 wa = *reinterpret_cast<const uint4*>(st + g * 64 + 16 * t4);
+                    const uint4 wb = *reinterpret_cast<const uint4*>(st + (g + 8) * 64 + 16 * t4);
+                    const uint4* xb = xlane + (kk / KB) * xkb_stride;
+                    const uint32_t wav[4] = {wa.x, wa.y, wa.z, wa.w};
+                    const uint32_t wbv[4] = {wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) {
+                        const uint4 bx = xb[w * xw_stride];
+                        const uint32_t va = wav[w], vb = wbv[w];
+                        const uint32_t a0[4] = {(va & mask) | magic, (vb & mask) | magic,
+                                                ((va >> 4) & mask) | magic, ((vb >> 4) & mask) | magic};
+                        const uint32_t a1[4] = {((va >> 8) & mask) | magic, ((vb >> 8) & mask) | magic,
+                                                ((va >> 12) & mask) | magic, ((vb >> 12) & mask) | magic};
+                        mma_bf16(acc, a0, bx.x, bx.y);
+                        mma_bf16(acc2, a1, bx.z, bx.w);
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
+            }
+            // tile partials, added in warp order
+            float* rb = red + ((tile & 1) * NC + warp) * 16 * C;
+            const int c0 = 2 * t4, c1 = 2 * t4 + 1;
+            if (c0 < C) { rb[g * C + c0] = acc[0] + acc2[0]; rb[(g + 8) * C + c0] = acc[2] + acc2[2]; }
+            if (c1 < C) { rb[g * C + c1] = acc[1] + acc2[1]; rb[(g + 8) * C + c1] = acc[3] + acc2[3]; }
+            named_barrier(1, CT);
+            for (int i = tid; i < 16 * C; i += CT) {
+                const int r = i / C;
+                if (tile * 16 + r < nrows) {
+                    float v = 0.f;
+                    for (int w = 0; w < NC; ++w) v += red[((tile & 1) * NC + w) * 16 * C + i];
+                    part[(tile * 16) * C + i] = v;
+                }
+            }
+        }
+    }
+    __syncthreads();
+
+    // combine the K-slices of the cluster, fold the offset, scale, store
+    cg::cluster_group cluster = cg::this_cluster();
+    if (S > 1) cluster.sync();
+    for (int i = ks + S * tid; i < nrows; i += S * THREADS) {
+        const float2 s_z = sz[i];
+        const float off = 128.0f + s_z.y;
+#pragma unroll
+        for (int c = 0; c < C; ++c) {
+            float sum = 0.f, xs = 0.f;
+            for (int r = 0; r < S; ++r) {
+                const float* pp = (S > 1) ? cluster.map_shared_rank(part, r) : part;
+                const float* xx = (S > 1) ? cluster.map_shared_rank(xsum, r) : xsum;
+                sum += pp[i * C + c];
+                xs += xx[c];
+            }
+            d[static_cast<int64_t>(c) * N + r0 + i] = __float2bfloat16_rn(s_z.x * fmaf(-off, xs, sum));
+        }
+    }
+    if (S > 1) cluster.sync();
+}
+
+}  // namespace gtma
+
+namespace {
+
+using namespace gtma;
+
+constexpr size_t kXfBudget = 48 * 1024;
+constexpr size_t kSmemMax = 227 * 1024;
+
+bool encode_qmap(CUtensorMap* m, const void* qw, int N, int K, int rows) {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return false;
+        fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 8), static_cast<cuuint64_t>(N)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 8) * 4};
+    cuuint32_t box[2] = {KB / 8, static_cast<cuuint32_t>(rows)};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(qw), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int C>
+w4_status launch_gemv_tma_t(const void* qw, const void* scale, const void* zero, const void* x, void* d, int N,
+                            int K, cudaStream_t stream) {
+    const int sms = sm_count();
+    if (sms <= 0) return W4_ERR_CUDA;
+    auto slice_of = [&](int s) { return ((K + s - 1) / s + 31) / 32 * 32; };
+    auto xf_bytes = [&](int s) { return static_cast<size_t>((slice_of(s) + KB - 1) / KB) * 16 * C * 16; };
+    int S = 1;
+    while (S < 8 && xf_bytes(S) > kXfBudget) S *= 2;
+    const int kslice = slice_of(S);
+    auto kern = gemv_tma_kernel<C>;
+    static int smem_set[64];
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(THREADS, 1, 1);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = S;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+
+    const int64_t quads = (static_cast<int64_t>(N) + 3) / 4;
+    int groups = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(sms / S, quads)));
+    auto rows_cap_of = [&](int gr) { return static_cast<int>(4 * ((quads + gr - 1) / gr)); };
+    auto smem_of = [&](int gr) { return static_cast<size_t>(make_layout(C, kslice, rows_cap_of(gr)).total) + 1024; };
+    if (smem_of(groups) > kSmemMax) return W4_ERR_SHAPE;
+    cudaError_t e = ensure_smem_limit(kern, static_cast<int>(smem_of(groups)), smem_set);
+    if (e != cudaSuccess) return W4_ERR_CUDA;
+    if (S > 1) {
+        // every cluster must be resident at once: cap the row groups by the
+        // number of clusters the GPCs can hold together
+        static int max_clusters[64][4];
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return W4_ERR_CUDA;
+        const int si = S == 2 ? 0 : S == 4 ? 1 : 2;
+        if (max_clusters[dev][si] == 0) {
+            cfg.gridDim = dim3(S * groups, 1, 1);
+            cfg.dynamicSmemBytes = smem_of(groups);
+            int n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) return W4_ERR_CUDA;
+            max_clusters[dev][si] = n;
+        }
+        groups = std::min(groups, max_clusters[dev][si]);
+        if (smem_of(groups) > kSmemMax) return W4_ERR_SHAPE;
+        e = ensure_smem_limit(kern, static_cast<int>(smem_of(groups)), smem_set);
+        if (e != cudaSuccess) return W4_ERR_CUDA;
+    }
+    CUtensorMap m16, m4;
+    if (!encode_qmap(&m16, qw, N, K, 16) || !encode_qmap(&m4, qw, N, K, 4)) return W4_ERR_CUDA;
+    cfg.gridDim = dim3(S * groups, 1, 1);
+    cfg.dynamicSmemBytes = smem_of(groups);
+    e = cudaLaunchKernelEx(&cfg, kern, m16, m4, static_cast<const __nv_bfloat16*>(scale),
+                           static_cast<const __nv_bfloat16*>(zero), static_cast<const __nv_bfloat16*>(x),
+                           static_cast<__nv_bfloat16*>(d), N, K, kslice, groups, rows_cap_of(groups), S);
+    return launch_status(e);
+}
+
+}  // namespace
+
+// bf16 GEMV, TMA-fed tensor-core path; requires K % 32 == 0 (16-byte rows).
+w4_status run_gemv_tma(const void* qw, const void* scale, const void* zero, const void* x, void* d, int N, int K,
+                       int C, cudaStream_t stream) {
+    switch (C) {
+        case 1: return launch_gemv_tma_t<1>(qw, scale, zero, x, d, N, K, stream);
+        case 2: return launch_gemv_tma_t<2>(qw, scale, zero, x, d, N, K, stream);
+        case 3: return launch_gemv_tma_t<3>(qw, scale, zero, x, d, N, K, stream);
+        case 4: return launch_gemv_tma_t<4>(qw, scale, zero, x, d, N, K, stream);
+        case 5: return launch_gemv_tma_t<5>(qw, scale, zero, x, d, N, K, stream);
+        case 6: return launch_gemv_tma_t<6>(qw, scale, zero, x, d, N, K, stream);
+        case 7: return launch_gemv_tma_t<7>(qw, scale, zero, x, d, N, K, stream);
+        case 8: return launch_gemv_tma_t<8>(qw, scale, zero, x, d, N, K, stream);
+        default: return W4_ERR_SHAPE;
+    }
+}
+
+int take_device_error_gemv() { return take_unit_device_error(); }
+
+}  // namespace w4

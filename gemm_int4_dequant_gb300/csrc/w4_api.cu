@@ -14,6 +14,8 @@ w4_status run_gemv(const void* qw, const void* scale, const void* zero, const vo
                    int64_t K, int64_t C, w4_dtype dtype, cudaStream_t s);
 w4_status run_gemm(const void* A, const void* B, const void* scale, const void* zero, void* C, int64_t M,
                    int64_t N, int64_t K, cudaStream_t s);
+int take_device_error_gemm();
+int take_device_error_gemv();
 
 namespace {
 constexpr int kMaxDevices = 64;
@@ -52,6 +54,14 @@ using namespace w4;
 extern "C" {
 
 int w4_abi_version(void) { return 1; }
+
+int w4_device_error(void* stream) {
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return -1;
+    const int a = take_device_error_gemm();
+    const int b = take_device_error_gemv();
+    if (a < 0 || b < 0) return -1;
+    return a != 0 ? a : b;
+}
 
 const char* w4_status_string(w4_status status) {
     switch (status) {
