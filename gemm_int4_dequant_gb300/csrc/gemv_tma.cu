@@ -11,9 +11,10 @@
 // GB300 design.  The op reads 0.5 B of weight per multiply-add, so HBM
 // bandwidth is the roofline.  One CTA per SM owns a contiguous, balanced row
 // range (and, when x does not fit, one K-slice of a thread-block cluster):
-//   * warp NC (producer) issues 2-D TMA copies of 16-row x 128-k boxes
-//     (1 KB each) into an NST-deep ring of 16-row x 2048-k stages, so about
-//     128 KB of loads are in flight per SM without spending registers;
+//   * warp NC (producer) issues 1-D bulk copies (TMA) of each row's 1 KB
+//     segment into an NST-deep ring of 16-row x 2048-k stages (rows padded
+//     to 1088 B so the consumers' fragment loads hit distinct banks), so
+//     about 136 KB of loads are in flight per SM without spending registers;
 //   * warps 0..NC-1 (consumers) each take one 128-k block of every stage:
 //     two 16-byte shared loads give a lane its rows g and g+8, each uint32
 //     word becomes four bf16x2 pairs (nibbles j, j+4) with one mask-and-OR
@@ -51,9 +52,15 @@ constexpr int CT = NC * 32;                   // consumer threads
 constexpr int KB = 128;                       // k per unit (one consumer warp per unit)
 constexpr int KC = NC * KB;                   // k per stage
 constexpr int NST = 8;                        // stages in the ring
-constexpr int BOX_BYTES = 16 * KB / 2;        // 16 rows x 64 B
-constexpr int BOX4_BYTES = 4 * KB / 2;        // 4 rows x 64 B
-constexpr int STAGE_BYTES = NC * BOX_BYTES;   // 16 KB
+constexpr int SEG = KC / 2;                   // bytes of one row per stage (1 KB)
+constexpr int ROWP = SEG + 64;                // padded row pitch in shared memory
+constexpr int STAGE_BYTES = 16 * ROWP;        // 16 rows
+
+// Nibble mask and bf16 magic passed at run time so they stay in registers and
+// each mask-and-OR is a single three-input logic op.
+struct MaskMagic {
+    uint32_t mask, magic;
+};
 
 struct Layout {
     // byte offsets into dynamic shared memory (base aligned to 1 KB)
@@ -80,10 +87,9 @@ __host__ __device__ inline Layout make_layout(int C, int kslice, int rows_cap) {
 
 template <int C>
 __global__ void __launch_bounds__(THREADS, 1)
-gemv_tma_kernel(const __grid_constant__ CUtensorMap map16, const __grid_constant__ CUtensorMap map4,
-                const __nv_bfloat16* __restrict__ scale, const __nv_bfloat16* __restrict__ zero,
+gemv_tma_kernel(const uint8_t* __restrict__ qw, const __nv_bfloat16* __restrict__ scale, const __nv_bfloat16* __restrict__ zero,
                 const __nv_bfloat16* __restrict__ x, __nv_bfloat16* __restrict__ d, int N, int K, int kslice,
-                int groups, int rows_cap, int S) {
+                int groups, int rows_cap, int S, MaskMagic dq) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t* sm = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -129,31 +135,20 @@ gemv_tma_kernel(const __grid_constant__ CUtensorMap map16, const __grid_constant
     if (warp == NC) {
         // ------------------------------------------------------------ producer
         if (lane == 0 && nstages > 0) {
-            asm volatile("prefetch.tensormap [%0];" ::"l"(&map16) : "memory");
-            asm volatile("prefetch.tensormap [%0];" ::"l"(&map4) : "memory");
             const uint64_t policy = l2_evict_first_policy();
+            const int64_t row_bytes = K / 2;
+            const uint8_t* src0 = qw + static_cast<int64_t>(r0) * row_bytes + k0 / 2;
             int tile = 0, ch = 0, issued = 0;
             for (int s = 0; s < nstages; ++s) {
                 const int slot = s % NST, round = s / NST;
-                if (round > 0 && !mbar_wait(bar_empty + 8 * slot, (round - 1) & 1, abort_flag)) break;
+                if (round > 0 && !mbar_wait_fast(bar_empty + 8 * slot, (round - 1) & 1, abort_flag)) break;
                 const int rows_here = min(16, nrows - tile * 16);
-                const int nvalid = min(NC, (klen - ch * KC + KB - 1) / KB);
-                const int xw = (k0 + ch * KC) / 8;          // word coordinate of the stage
-                const int y = r0 + tile * 16;
+                const int seg = min(SEG, (klen - ch * KC) / 2);     // bytes of each row (multiple of 16)
                 const uint32_t dst = sm_addr + slot * STAGE_BYTES;
-                if (rows_here == 16) {
-                    mbar_arrive_expect_tx(bar_full + 8 * slot, nvalid * BOX_BYTES);
-                    for (int kb = 0; kb < nvalid; ++kb)
-                        tma_load_2d_hint(dst + kb * BOX_BYTES, &map16, xw + kb * (KB / 8), y, bar_full + 8 * slot,
-                                         policy);
-                } else {
-                    const int nq = (rows_here + 3) / 4;
-                    mbar_arrive_expect_tx(bar_full + 8 * slot, nvalid * nq * BOX4_BYTES);
-                    for (int kb = 0; kb < nvalid; ++kb)
-                        for (int qd = 0; qd < nq; ++qd)
-                            tma_load_2d_hint(dst + kb * BOX_BYTES + qd * BOX4_BYTES, &map4, xw + kb * (KB / 8),
-                                             y + 4 * qd, bar_full + 8 * slot, policy);
-                }
+                const uint8_t* src = src0 + static_cast<int64_t>(tile) * 16 * row_bytes + ch * SEG;
+                mbar_arrive_expect_tx(bar_full + 8 * slot, rows_here * seg);
+                for (int r = 0; r < rows_here; ++r)
+                    bulk_load_hint(dst + r * ROWP, src + r * row_bytes, seg, bar_full + 8 * slot, policy);
                 issued = s + 1;
                 if (++ch == nch) { ch = 0; ++tile; }
             }
@@ -231,18 +226,18 @@ gemv_tma_kernel(const __grid_constant__ CUtensorMap map16, const __grid_constant
         const uint4* xlane = bl ? xf + g * 4 + t4 : xzero + t4;
         const int xw_stride = bl ? C * 4 : 4;
         const int xkb_stride = bl ? 4 * C * 4 : 0;
-        const uint32_t mask = 0x000F000Fu, magic = 0x43004300u;  // bf16x2 (128, 128)
+        const uint32_t mask = dq.mask, magic = dq.magic;  // 0x000F000F, bf16x2 (128, 128)
         int s = 0;
         for (int tile = 0; tile < ntiles; ++tile) {
             float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};
             for (int ch = 0; ch < nch; ++ch, ++s) {
                 const int slot = s % NST;
-                const bool ok = mbar_wait(bar_full + 8 * slot, (s / NST) & 1, abort_flag);
+                const bool ok = mbar_wait_fast(bar_full + 8 * slot, (s / NST) & 1, abort_flag);
                 const int kk = ch * KC + warp * KB;
                 if (ok && kk < klen) {
-                    const uint8_t* st = sm + slot * STAGE_BYTES + warp * BOX_BYTES;
-                    const uint4 wa = *reinterpret_cast<const uint4*>(st + g * 64 + 16 * t4);
-                    const uint4 wb = *reinterpret_cast<const uint4*>(st + (g + 8) * 64 + 16 * t4);
+                    const uint8_t* st = sm + slot * STAGE_BYTES + warp * 64 + 16 * t4;
+                    const uint4 wa = *reinterpret_cast<const uint4*>(st + g * ROWP);
+                    const uint4 wb = *reinterpret_cast<const uint4*>(st + (g + 8) * ROWP);
                     const uint4* xb = xlane + (kk / KB) * xkb_stride;
                     const uint32_t wav[4] = {wa.x, wa.y, wa.z, wa.w};
                     const uint32_t wbv[4] = {wb.x, wb.y, wb.z, wb.w};
@@ -250,10 +245,10 @@ gemv_tma_kernel(const __grid_constant__ CUtensorMap map16, const __grid_constant
                     for (int w = 0; w < 4; ++w) {
                         const uint4 bx = xb[w * xw_stride];
                         const uint32_t va = wav[w], vb = wbv[w];
-                        const uint32_t a0[4] = {(va & mask) | magic, (vb & mask) | magic,
-                                                ((va >> 4) & mask) | magic, ((vb >> 4) & mask) | magic};
-                        const uint32_t a1[4] = {((va >> 8) & mask) | magic, ((vb >> 8) & mask) | magic,
-                                                ((va >> 12) & mask) | magic, ((vb >> 12) & mask) | magic};
+                        const uint32_t a0[4] = {and_or(va, mask, magic), and_or(vb, mask, magic),
+                                                and_or(va >> 4, mask, magic), and_or(vb >> 4, mask, magic)};
+                        const uint32_t a1[4] = {and_or(va >> 8, mask, magic), and_or(vb >> 8, mask, magic),
+                                                and_or(va >> 12, mask, magic), and_or(vb >> 12, mask, magic)};
                         mma_bf16(acc, a0, bx.x, bx.y);
                         mma_bf16(acc2, a1, bx.z, bx.w);
                     }
@@ -309,26 +304,6 @@ using namespace gtma;
 constexpr size_t kXfBudget = 48 * 1024;
 constexpr size_t kSmemMax = 227 * 1024;
 
-bool encode_qmap(CUtensorMap* m, const void* qw, int N, int K, int rows) {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
-                cudaSuccess ||
-            q != cudaDriverEntryPointSuccess)
-            return false;
-        fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 8), static_cast<cuuint64_t>(N)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 8) * 4};
-    cuuint32_t box[2] = {KB / 8, static_cast<cuuint32_t>(rows)};
-    cuuint32_t estr[2] = {1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(qw), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int C>
 w4_status launch_gemv_tma_t(const void* qw, const void* scale, const void* zero, const void* x, void* d, int N,
                             int K, cudaStream_t stream) {
@@ -378,13 +353,12 @@ w4_status launch_gemv_tma_t(const void* qw, const void* scale, const void* zero,
         e = ensure_smem_limit(kern, static_cast<int>(smem_of(groups)), smem_set);
         if (e != cudaSuccess) return W4_ERR_CUDA;
     }
-    CUtensorMap m16, m4;
-    if (!encode_qmap(&m16, qw, N, K, 16) || !encode_qmap(&m4, qw, N, K, 4)) return W4_ERR_CUDA;
     cfg.gridDim = dim3(S * groups, 1, 1);
     cfg.dynamicSmemBytes = smem_of(groups);
-    e = cudaLaunchKernelEx(&cfg, kern, m16, m4, static_cast<const __nv_bfloat16*>(scale),
+    e = cudaLaunchKernelEx(&cfg, kern, static_cast<const uint8_t*>(qw), static_cast<const __nv_bfloat16*>(scale),
                            static_cast<const __nv_bfloat16*>(zero), static_cast<const __nv_bfloat16*>(x),
-                           static_cast<__nv_bfloat16*>(d), N, K, kslice, groups, rows_cap_of(groups), S);
+                           static_cast<__nv_bfloat16*>(d), N, K, kslice, groups, rows_cap_of(groups), S,
+                           MaskMagic{0x000F000Fu, 0x43004300u});
     return launch_status(e);
 }
 

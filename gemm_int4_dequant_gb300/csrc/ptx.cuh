@@ -148,6 +148,30 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy() {
     return p;
 }
 
+// 1-D bulk copy global -> shared (both 16-byte aligned, size a multiple of
+// 16), completing on an mbarrier, with an L2 cache-policy hint.
+__device__ __forceinline__ void bulk_load_hint(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
+                                               uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+            dst),
+        "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+// (a & b) | c in one LOP3 with all three operands in registers.
+__device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+// Wait with the common case (already complete) inline and the bounded
+// polling loop out of line.
+__device__ __forceinline__ bool mbar_wait_fast(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+    return mbar_try_wait(bar, parity) || mbar_wait(bar, parity, abort_flag);
+}
+
 // Named barrier over `count` threads (id 1..15; 0 is __syncthreads).
 __device__ __forceinline__ void named_barrier(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
