@@ -11,11 +11,15 @@
 // GB300 design.  The op reads 0.5 B of weight per multiply-add, so HBM
 // bandwidth is the roofline.  One CTA per SM owns a contiguous, balanced row
 // range (and, when x does not fit, one K-slice of a thread-block cluster):
-//   * warp NC (producer) issues 1-D bulk copies (TMA) of each row's 1 KB
-//     segment into an NST-deep ring of 16-row x 2048-k stages (rows padded
-//     to 1088 B so the consumers' fragment loads hit distinct banks), so
-//     about 136 KB of loads are in flight per SM without spending registers;
-//   * warps 0..NC-1 (consumers) each take one 128-k block of every stage:
+//   * warp NC (producer) streams 16-row tiles with 1-D bulk copies (TMA).
+//     The copy engine has a fixed cost per copy, so copies are large: a tile
+//     whose rows are contiguous in memory (no K split) is one copy of 16 full
+//     rows; otherwise each row's K-chunk is one copy (>= 2 KB) into a row
+//     pitch padded to 64 mod 128 bytes, which keeps the consumers' fragment
+//     loads on distinct banks.  The ring holds as many stages as shared
+//     memory allows (about 200 KB in flight per SM, no registers spent);
+//   * warps 0..NC-1 (consumers) share out the 128-k blocks of every stage
+//     round-robin (continuing across stages, so the split stays balanced):
 //     two 16-byte shared loads give a lane its rows g and g+8, each uint32
 //     word becomes four bf16x2 pairs (nibbles j, j+4) with one mask-and-OR
 //     into the mantissa of 128.0 (exactly 128 + q), and two
@@ -50,11 +54,8 @@ constexpr int NC = 16;                        // consumer warps
 constexpr int THREADS = (NC + 1) * 32;        // + one producer warp
 constexpr int CT = NC * 32;                   // consumer threads
 constexpr int KB = 128;                       // k per unit (one consumer warp per unit)
-constexpr int KC = NC * KB;                   // k per stage
-constexpr int NST = 8;                        // stages in the ring
-constexpr int SEG = KC / 2;                   // bytes of one row per stage (1 KB)
-constexpr int ROWP = SEG + 64;                // padded row pitch in shared memory
-constexpr int STAGE_BYTES = 16 * ROWP;        // 16 rows
+constexpr int MAX_NST = 8;                    // stages in the ring (at most)
+constexpr int KCHUNK_MAX = 8192;              // k per stage at most (4 KB per row)
 
 // Nibble mask and bf16 magic passed at run time so they stay in registers and
 // each mask-and-OR is a single three-input logic op.
@@ -62,24 +63,38 @@ struct MaskMagic {
     uint32_t mask, magic;
 };
 
-struct Layout {
-    // byte offsets into dynamic shared memory (base aligned to 1 KB)
-    int xf, xzero, red, part, xsw, xsum, sz, bars, abort, total;
+// Run-time shape of the pipeline, identical for every CTA of a launch (peers
+// in a cluster read each other's shared memory at the same offsets).
+struct Plan {
+    int S;          // K-slices (cluster size)
+    int kslice;     // k per slice (multiple of 32)
+    int kchunk;     // k per stage (multiple of 128, <= kslice rounded up)
+    int dense;      // 1: a stage is one copy of 16 contiguous full rows
+    int pitch;      // bytes between rows of a stage in shared memory
+    int nst;        // stages in the ring
+    int groups;     // row groups
+    int rows_cap;   // rows per CTA at most
 };
 
-__host__ __device__ inline Layout make_layout(int C, int kslice, int rows_cap) {
+struct Layout {
+    int stage_bytes, xf, xzero, red, part, xsw, xsum, sz, bars, abort, total;
+};
+
+__host__ __device__ inline Layout make_layout(int C, const Plan& P) {
     Layout L;
-    const int nkb_cap = (kslice + KB - 1) / KB;
-    int o = NST * STAGE_BYTES;
+    L.stage_bytes = 16 * P.pitch;
+    const int nkb_cap = (P.kslice + KB - 1) / KB;
+    int o = P.nst * L.stage_bytes;
+    o = (o + 127) & ~127;
     L.xf = o;        o += nkb_cap * 16 * C * 16;
     L.xzero = o;     o += 16 * 16;
     L.red = o;       o += 2 * NC * 16 * C * 4;
-    L.part = o;      o += rows_cap * C * 4;
+    L.part = o;      o += P.rows_cap * C * 4;
     L.xsw = o;       o += NC * C * 4;
     L.xsum = o;      o += 8 * 4;
-    L.sz = o;        o += rows_cap * 8;           // (scale, zero) per row as fp32
+    L.sz = o;        o += P.rows_cap * 8;          // (scale, zero) per row as fp32
     o = (o + 7) & ~7;
-    L.bars = o;      o += 2 * NST * 8;
+    L.bars = o;      o += 2 * MAX_NST * 8;
     L.abort = o;     o += 16;
     L.total = o;
     return L;
@@ -87,25 +102,26 @@ __host__ __device__ inline Layout make_layout(int C, int kslice, int rows_cap) {
 
 template <int C>
 __global__ void __launch_bounds__(THREADS, 1)
-gemv_tma_kernel(const uint8_t* __restrict__ qw, const __nv_bfloat16* __restrict__ scale, const __nv_bfloat16* __restrict__ zero,
-                const __nv_bfloat16* __restrict__ x, __nv_bfloat16* __restrict__ d, int N, int K, int kslice,
-                int groups, int rows_cap, int S, MaskMagic dq) {
+gemv_tma_kernel(const uint8_t* __restrict__ qw, const __nv_bfloat16* __restrict__ scale,
+                const __nv_bfloat16* __restrict__ zero, const __nv_bfloat16* __restrict__ x,
+                __nv_bfloat16* __restrict__ d, int N, int K, Plan P, MaskMagic dq) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t* sm = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
     const uint32_t sm_addr = smem_u32(sm);
-    const Layout L = make_layout(C, kslice, rows_cap);
+    const Layout L = make_layout(C, P);
+    const int S = P.S, NST = P.nst, pitch = P.pitch;
 
     const int ks = blockIdx.x % S;        // K-slice = rank in the cluster
     const int grp = blockIdx.x / S;       // row group
     const int64_t quads = (static_cast<int64_t>(N) + 3) / 4;
-    const int r0 = static_cast<int>(4 * ((grp * quads) / groups));
-    const int r1 = static_cast<int>((N < 4 * (((grp + 1) * quads) / groups) ? static_cast<int64_t>(N) : 4 * (((grp + 1) * quads) / groups)));
+    const int64_t r1q = 4 * (((grp + 1) * quads) / P.groups);
+    const int r0 = static_cast<int>(4 * ((grp * quads) / P.groups));
+    const int r1 = static_cast<int>(N < r1q ? static_cast<int64_t>(N) : r1q);
     const int nrows = max(0, r1 - r0);
-    const int k0 = min(K, ks * kslice);
-    const int klen = min(K, k0 + kslice) - k0;   // multiple of 32
-    const int nkb = (klen + KB - 1) / KB;
-    const int nch = (klen + KC - 1) / KC;
+    const int k0 = min(K, ks * P.kslice);
+    const int klen = min(K, k0 + P.kslice) - k0;      // multiple of 32
+    const int nch = (klen + P.kchunk - 1) / P.kchunk;
     const int ntiles = (nrows + 15) / 16;
     const int nstages = ntiles * nch;
 
@@ -117,7 +133,7 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const __nv_bfloat16* __restrict_
     float* xsum = reinterpret_cast<float*>(sm + L.xsum);
     float2* sz = reinterpret_cast<float2*>(sm + L.sz);
     const uint32_t bar_full = sm_addr + L.bars;
-    const uint32_t bar_empty = bar_full + NST * 8;
+    const uint32_t bar_empty = bar_full + MAX_NST * 8;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L.abort);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -143,12 +159,16 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const __nv_bfloat16* __restrict_
                 const int slot = s % NST, round = s / NST;
                 if (round > 0 && !mbar_wait_fast(bar_empty + 8 * slot, (round - 1) & 1, abort_flag)) break;
                 const int rows_here = min(16, nrows - tile * 16);
-                const int seg = min(SEG, (klen - ch * KC) / 2);     // bytes of each row (multiple of 16)
-                const uint32_t dst = sm_addr + slot * STAGE_BYTES;
-                const uint8_t* src = src0 + static_cast<int64_t>(tile) * 16 * row_bytes + ch * SEG;
+                const int seg = min(P.kchunk, klen - ch * P.kchunk) / 2;   // bytes per row (multiple of 16)
+                const uint32_t dst = sm_addr + slot * L.stage_bytes;
+                const uint8_t* src = src0 + static_cast<int64_t>(tile) * 16 * row_bytes + ch * (P.kchunk / 2);
                 mbar_arrive_expect_tx(bar_full + 8 * slot, rows_here * seg);
-                for (int r = 0; r < rows_here; ++r)
-                    bulk_load_hint(dst + r * ROWP, src + r * row_bytes, seg, bar_full + 8 * slot, policy);
+                if (P.dense) {
+                    bulk_load_hint(dst, src, rows_here * seg, bar_full + 8 * slot, policy);
+                } else {
+                    for (int r = 0; r < rows_here; ++r)
+                        bulk_load_hint(dst + r * pitch, src + r * row_bytes, seg, bar_full + 8 * slot, policy);
+                }
                 issued = s + 1;
                 if (++ch == nch) { ch = 0; ++tile; }
             }
@@ -164,6 +184,7 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const __nv_bfloat16* __restrict_
         // 32*t4 + 8*p, the bf16 pairs (x[kk], x[kk+4]) (x[kk+1], x[kk+5])
         // (x[kk+2], x[kk+6]) (x[kk+3], x[kk+7]) -- the b0b1/b2b3 registers of
         // the two MMAs that consume word p.  Loads are issued four at a time.
+        const int nkb = (klen + KB - 1) / KB;
         const int per_n = nkb * 16;
         const int total = C * per_n;
         float xs_part[C];
@@ -220,39 +241,45 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const __nv_bfloat16* __restrict_
             xsum[tid] = v;
         }
 
-        // main loop
+        // main loop: units of each stage go round-robin to the warps, the
+        // rotation carrying over from stage to stage
         const int g = lane >> 2, t4 = lane & 3;
         const bool bl = g < C;
         const uint4* xlane = bl ? xf + g * 4 + t4 : xzero + t4;
         const int xw_stride = bl ? C * 4 : 4;
         const int xkb_stride = bl ? 4 * C * 4 : 0;
-        const uint32_t mask = dq.mask, magic = dq.magic;  // 0x000F000F, bf16x2 (128, 128)
-        int s = 0;
+        const uint32_t mask = dq.mask, magic = dq.magic;
+        const int row_off_a = g * pitch + 16 * t4, row_off_b = (g + 8) * pitch + 16 * t4;
+        int s = 0, first = warp;      // first unit of this warp in the current stage
         for (int tile = 0; tile < ntiles; ++tile) {
             float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};
             for (int ch = 0; ch < nch; ++ch, ++s) {
                 const int slot = s % NST;
+                const int units = (min(P.kchunk, klen - ch * P.kchunk) + KB - 1) / KB;
                 const bool ok = mbar_wait_fast(bar_full + 8 * slot, (s / NST) & 1, abort_flag);
-                const int kk = ch * KC + warp * KB;
-                if (ok && kk < klen) {
-                    const uint8_t* st = sm + slot * STAGE_BYTES + warp * 64 + 16 * t4;
-                    const uint4 wa = *reinterpret_cast<const uint4*>(st + g * ROWP);
-                    const uint4 wb = *reinterpret_cast<const uint4*>(st + (g + 8) * ROWP);
-                    const uint4* xb = xlane + (kk / KB) * xkb_stride;
-                    const uint32_t wav[4] = {wa.x, wa.y, wa.z, wa.w};
-                    const uint32_t wbv[4] = {wb.x, wb.y, wb.z, wb.w};
+                if (ok) {
+                    const uint8_t* st = sm + slot * L.stage_bytes;
+                    for (int u = first; u < units; u += NC) {
+                        const uint4 wa = *reinterpret_cast<const uint4*>(st + row_off_a + u * 64);
+                        const uint4 wb = *reinterpret_cast<const uint4*>(st + row_off_b + u * 64);
+                        const uint4* xb = xlane + (ch * (P.kchunk / KB) + u) * xkb_stride;
+                        const uint32_t wav[4] = {wa.x, wa.y, wa.z, wa.w};
+                        const uint32_t wbv[4] = {wb.x, wb.y, wb.z, wb.w};
 #pragma unroll
-                    for (int w = 0; w < 4; ++w) {
-                        const uint4 bx = xb[w * xw_stride];
-                        const uint32_t va = wav[w], vb = wbv[w];
-                        const uint32_t a0[4] = {and_or(va, mask, magic), and_or(vb, mask, magic),
-                                                and_or(va >> 4, mask, magic), and_or(vb >> 4, mask, magic)};
-                        const uint32_t a1[4] = {and_or(va >> 8, mask, magic), and_or(vb >> 8, mask, magic),
-                                                and_or(va >> 12, mask, magic), and_or(vb >> 12, mask, magic)};
-                        mma_bf16(acc, a0, bx.x, bx.y);
-                        mma_bf16(acc2, a1, bx.z, bx.w);
+                        for (int w = 0; w < 4; ++w) {
+                            const uint4 bx = xb[w * xw_stride];
+                            const uint32_t va = wav[w], vb = wbv[w];
+                            const uint32_t a0[4] = {and_or(va, mask, magic), and_or(vb, mask, magic),
+                                                    and_or(va >> 4, mask, magic), and_or(vb >> 4, mask, magic)};
+                            const uint32_t a1[4] = {and_or(va >> 8, mask, magic), and_or(vb >> 8, mask, magic),
+                                                    and_or(va >> 12, mask, magic), and_or(vb >> 12, mask, magic)};
+                            mma_bf16(acc, a0, bx.x, bx.y);
+                            mma_bf16(acc2, a1, bx.z, bx.w);
+                        }
                     }
                 }
+                // rotate: the next stage's first unit for this warp
+                first = ((first - units) % NC + NC) % NC;
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
             }
@@ -301,19 +328,50 @@ namespace {
 
 using namespace gtma;
 
-constexpr size_t kXfBudget = 48 * 1024;
-constexpr size_t kSmemMax = 227 * 1024;
+constexpr int kSmemMax = 227 * 1024;
+constexpr size_t kXfBudget = 80 * 1024;
+
+// Pipeline shape for (N, K, C) on `sms` SMs; nst == 0 if nothing fits.
+template <int C>
+Plan make_plan(int N, int K, int sms, int max_clusters_for_S /* 0: unknown */, int S_forced) {
+    Plan P{};
+    auto slice_of = [&](int s) { return ((K + s - 1) / s + 31) / 32 * 32; };
+    auto xf_bytes = [&](int s) { return static_cast<size_t>((slice_of(s) + KB - 1) / KB) * 16 * C * 16; };
+    int S = 1;
+    if (S_forced) S = S_forced;
+    else while (S < 8 && xf_bytes(S) > kXfBudget) S *= 2;
+    P.S = S;
+    P.kslice = slice_of(S);
+    const int64_t quads = (static_cast<int64_t>(N) + 3) / 4;
+    int groups = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(sms / S, quads)));
+    if (max_clusters_for_S > 0) groups = std::min(groups, max_clusters_for_S);
+    P.groups = groups;
+    P.rows_cap = static_cast<int>(4 * ((quads + groups - 1) / groups));
+    // stage: one 16-row tile over a K-chunk
+    {
+        const int nch0 = (P.kslice + KCHUNK_MAX - 1) / KCHUNK_MAX;  // chunks of about equal size
+        P.kchunk = ((P.kslice + nch0 - 1) / nch0 + KB - 1) / KB * KB;
+    }
+    P.dense = (S == 1 && P.kchunk >= K) ? 1 : 0;
+    if (P.dense) {
+        P.pitch = K / 2;
+    } else {
+        const int seg = P.kchunk / 2;
+        P.pitch = (seg + 127) / 128 * 128 + 64;   // 64 mod 128: conflict-free fragment loads
+    }
+    P.nst = MAX_NST;
+    while (P.nst >= 2 && make_layout(C, P).total + 1024 > kSmemMax) --P.nst;
+    if (P.nst < 2) P.nst = 0;
+    return P;
+}
 
 template <int C>
 w4_status launch_gemv_tma_t(const void* qw, const void* scale, const void* zero, const void* x, void* d, int N,
                             int K, cudaStream_t stream) {
     const int sms = sm_count();
     if (sms <= 0) return W4_ERR_CUDA;
-    auto slice_of = [&](int s) { return ((K + s - 1) / s + 31) / 32 * 32; };
-    auto xf_bytes = [&](int s) { return static_cast<size_t>((slice_of(s) + KB - 1) / KB) * 16 * C * 16; };
-    int S = 1;
-    while (S < 8 && xf_bytes(S) > kXfBudget) S *= 2;
-    const int kslice = slice_of(S);
+    Plan P = make_plan<C>(N, K, sms, 0, 0);
+    if (P.nst == 0) return W4_ERR_SHAPE;
     auto kern = gemv_tma_kernel<C>;
     static int smem_set[64];
     cudaLaunchConfig_t cfg = {};
@@ -321,44 +379,37 @@ w4_status launch_gemv_tma_t(const void* qw, const void* scale, const void* zero,
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = S;
+    attr[0].val.clusterDim.x = P.S;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-
-    const int64_t quads = (static_cast<int64_t>(N) + 3) / 4;
-    int groups = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(sms / S, quads)));
-    auto rows_cap_of = [&](int gr) { return static_cast<int>(4 * ((quads + gr - 1) / gr)); };
-    auto smem_of = [&](int gr) { return static_cast<size_t>(make_layout(C, kslice, rows_cap_of(gr)).total) + 1024; };
-    if (smem_of(groups) > kSmemMax) return W4_ERR_SHAPE;
-    cudaError_t e = ensure_smem_limit(kern, static_cast<int>(smem_of(groups)), smem_set);
+    cudaError_t e = ensure_smem_limit(kern, make_layout(C, P).total + 1024, smem_set);
     if (e != cudaSuccess) return W4_ERR_CUDA;
-    if (S > 1) {
+    if (P.S > 1) {
         // every cluster must be resident at once: cap the row groups by the
         // number of clusters the GPCs can hold together
         static int max_clusters[64][4];
         int dev = 0;
         if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return W4_ERR_CUDA;
-        const int si = S == 2 ? 0 : S == 4 ? 1 : 2;
+        const int si = P.S == 2 ? 0 : P.S == 4 ? 1 : 2;
         if (max_clusters[dev][si] == 0) {
-            cfg.gridDim = dim3(S * groups, 1, 1);
-            cfg.dynamicSmemBytes = smem_of(groups);
+            cfg.gridDim = dim3(P.S * P.groups, 1, 1);
+            cfg.dynamicSmemBytes = make_layout(C, P).total + 1024;
             int n = 0;
             if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) return W4_ERR_CUDA;
             max_clusters[dev][si] = n;
         }
-        groups = std::min(groups, max_clusters[dev][si]);
-        if (smem_of(groups) > kSmemMax) return W4_ERR_SHAPE;
-        e = ensure_smem_limit(kern, static_cast<int>(smem_of(groups)), smem_set);
+        P = make_plan<C>(N, K, sms, max_clusters[dev][si], P.S);
+        if (P.nst == 0) return W4_ERR_SHAPE;
+        e = ensure_smem_limit(kern, make_layout(C, P).total + 1024, smem_set);
         if (e != cudaSuccess) return W4_ERR_CUDA;
     }
-    cfg.gridDim = dim3(S * groups, 1, 1);
-    cfg.dynamicSmemBytes = smem_of(groups);
+    cfg.gridDim = dim3(P.S * P.groups, 1, 1);
+    cfg.dynamicSmemBytes = make_layout(C, P).total + 1024;
     e = cudaLaunchKernelEx(&cfg, kern, static_cast<const uint8_t*>(qw), static_cast<const __nv_bfloat16*>(scale),
                            static_cast<const __nv_bfloat16*>(zero), static_cast<const __nv_bfloat16*>(x),
-                           static_cast<__nv_bfloat16*>(d), N, K, kslice, groups, rows_cap_of(groups), S,
-                           MaskMagic{0x000F000Fu, 0x43004300u});
+                           static_cast<__nv_bfloat16*>(d), N, K, P, MaskMagic{0x000F000Fu, 0x43004300u});
     return launch_status(e);
 }
 
