@@ -74,10 +74,11 @@ struct Plan {
     int nst;        // stages in the ring
     int groups;     // row groups
     int rows_cap;   // rows per CTA at most
+    int perwarp;    // 1: every warp keeps its own row partials (no per-tile barrier)
 };
 
 struct Layout {
-    int stage_bytes, xf, xzero, red, part, xsw, xsum, sz, bars, abort, total;
+    int stage_bytes, xf, xzero, red, part, partw, xsw, xsum, sz, bars, abort, total;
 };
 
 __host__ __device__ inline Layout make_layout(int C, const Plan& P) {
@@ -88,8 +89,9 @@ __host__ __device__ inline Layout make_layout(int C, const Plan& P) {
     o = (o + 127) & ~127;
     L.xf = o;        o += nkb_cap * 16 * C * 16;
     L.xzero = o;     o += 16 * 16;
-    L.red = o;       o += 2 * NC * 16 * C * 4;
+    L.red = o;       o += P.perwarp ? 0 : 2 * NC * 16 * C * 4;
     L.part = o;      o += P.rows_cap * C * 4;
+    L.partw = o;     o += P.perwarp ? NC * ((P.rows_cap + 15) / 16 * 16) * C * 4 : 0;
     L.xsw = o;       o += NC * C * 4;
     L.xsum = o;      o += 8 * 4;
     L.sz = o;        o += P.rows_cap * 8;          // (scale, zero) per row as fp32
@@ -129,6 +131,7 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const __nv_bfloat16* __restrict_
     uint4* xzero = reinterpret_cast<uint4*>(sm + L.xzero);
     float* red = reinterpret_cast<float*>(sm + L.red);
     float* part = reinterpret_cast<float*>(sm + L.part);
+    float* partw = reinterpret_cast<float*>(sm + L.partw);
     float* xsw = reinterpret_cast<float*>(sm + L.xsw);
     float* xsum = reinterpret_cast<float*>(sm + L.xsum);
     float2* sz = reinterpret_cast<float2*>(sm + L.sz);
@@ -154,9 +157,8 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const __nv_bfloat16* __restrict_
             const uint64_t policy = l2_evict_first_policy();
             const int64_t row_bytes = K / 2;
             const uint8_t* src0 = qw + static_cast<int64_t>(r0) * row_bytes + k0 / 2;
-            int tile = 0, ch = 0, issued = 0;
+            int tile = 0, ch = 0, issued = 0, slot = 0, round = 0;
             for (int s = 0; s < nstages; ++s) {
-                const int slot = s % NST, round = s / NST;
                 if (round > 0 && !mbar_wait_fast(bar_empty + 8 * slot, (round - 1) & 1, abort_flag)) break;
                 const int rows_here = min(16, nrows - tile * 16);
                 const int seg = min(P.kchunk, klen - ch * P.kchunk) / 2;   // bytes per row (multiple of 16)
@@ -171,6 +173,7 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const __nv_bfloat16* __restrict_
                 }
                 issued = s + 1;
                 if (++ch == nch) { ch = 0; ++tile; }
+                if (++slot == NST) { slot = 0; ++round; }
             }
             // copies still landing if a consumer aborted
             for (int s = max(0, issued - NST); s < issued; ++s) mbar_drain(bar_full + 8 * (s % NST), (s / NST) & 1);
@@ -250,13 +253,13 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const __nv_bfloat16* __restrict_
         const int xkb_stride = bl ? 4 * C * 4 : 0;
         const uint32_t mask = dq.mask, magic = dq.magic;
         const int row_off_a = g * pitch + 16 * t4, row_off_b = (g + 8) * pitch + 16 * t4;
-        int s = 0, first = warp;      // first unit of this warp in the current stage
+        int slot = 0, round = 0, first = warp;   // first unit of this warp in the current stage
+        const int rows16 = (P.rows_cap + 15) / 16 * 16;
         for (int tile = 0; tile < ntiles; ++tile) {
             float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};
-            for (int ch = 0; ch < nch; ++ch, ++s) {
-                const int slot = s % NST;
+            for (int ch = 0; ch < nch; ++ch) {
                 const int units = (min(P.kchunk, klen - ch * P.kchunk) + KB - 1) / KB;
-                const bool ok = mbar_wait_fast(bar_full + 8 * slot, (s / NST) & 1, abort_flag);
+                const bool ok = mbar_wait_fast(bar_full + 8 * slot, round & 1, abort_flag);
                 if (ok) {
                     const uint8_t* st = sm + slot * L.stage_bytes;
                     for (int u = first; u < units; u += NC) {
@@ -278,24 +281,41 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const __nv_bfloat16* __restrict_
                         }
                     }
                 }
-                // rotate: the next stage's first unit for this warp
-                first = ((first - units) % NC + NC) % NC;
+                // rotate: this warp's first unit of the next stage
+                first -= units % NC;
+                if (first < 0) first += NC;
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
+                if (++slot == NST) { slot = 0; ++round; }
             }
-            // tile partials, added in warp order
-            float* rb = red + ((tile & 1) * NC + warp) * 16 * C;
             const int c0 = 2 * t4, c1 = 2 * t4 + 1;
-            if (c0 < C) { rb[g * C + c0] = acc[0] + acc2[0]; rb[(g + 8) * C + c0] = acc[2] + acc2[2]; }
-            if (c1 < C) { rb[g * C + c1] = acc[1] + acc2[1]; rb[(g + 8) * C + c1] = acc[3] + acc2[3]; }
-            named_barrier(1, CT);
-            for (int i = tid; i < 16 * C; i += CT) {
-                const int r = i / C;
-                if (tile * 16 + r < nrows) {
-                    float v = 0.f;
-                    for (int w = 0; w < NC; ++w) v += red[((tile & 1) * NC + w) * 16 * C + i];
-                    part[(tile * 16) * C + i] = v;
+            if (P.perwarp) {
+                // this warp's partial of the tile; warps are added at the end
+                float* pw = partw + (static_cast<size_t>(warp) * rows16 + tile * 16) * C;
+                if (c0 < C) { pw[g * C + c0] = acc[0] + acc2[0]; pw[(g + 8) * C + c0] = acc[2] + acc2[2]; }
+                if (c1 < C) { pw[g * C + c1] = acc[1] + acc2[1]; pw[(g + 8) * C + c1] = acc[3] + acc2[3]; }
+            } else {
+                // tile partials, added in warp order now (bounded shared memory)
+                float* rb = red + ((tile & 1) * NC + warp) * 16 * C;
+                if (c0 < C) { rb[g * C + c0] = acc[0] + acc2[0]; rb[(g + 8) * C + c0] = acc[2] + acc2[2]; }
+                if (c1 < C) { rb[g * C + c1] = acc[1] + acc2[1]; rb[(g + 8) * C + c1] = acc[3] + acc2[3]; }
+                named_barrier(1, CT);
+                for (int i = tid; i < 16 * C; i += CT) {
+                    const int r = i / C;
+                    if (tile * 16 + r < nrows) {
+                        float v = 0.f;
+                        for (int w = 0; w < NC; ++w) v += red[((tile & 1) * NC + w) * 16 * C + i];
+                        part[(tile * 16) * C + i] = v;
+                    }
                 }
+            }
+        }
+        if (P.perwarp) {
+            named_barrier(1, CT);
+            for (int i = tid; i < nrows * C; i += CT) {
+                float v = 0.f;
+                for (int w = 0; w < NC; ++w) v += partw[static_cast<size_t>(w) * rows16 * C + i];
+                part[i] = v;
             }
         }
     }
@@ -359,9 +379,15 @@ Plan make_plan(int N, int K, int sms, int max_clusters_for_S /* 0: unknown */, i
         const int seg = P.kchunk / 2;
         P.pitch = (seg + 127) / 128 * 128 + 64;   // 64 mod 128: conflict-free fragment loads
     }
-    P.nst = MAX_NST;
-    while (P.nst >= 2 && make_layout(C, P).total + 1024 > kSmemMax) --P.nst;
-    if (P.nst < 2) P.nst = 0;
+    // prefer per-warp partials (no per-tile barrier) when they leave room
+    // for at least 3 stages; otherwise reduce each tile across warps at once
+    for (int pw = 1; pw >= 0; --pw) {
+        P.perwarp = pw;
+        P.nst = MAX_NST;
+        while (P.nst >= 2 && make_layout(C, P).total + 1024 > kSmemMax) --P.nst;
+        if (P.nst >= (pw ? 3 : 2)) return P;
+    }
+    P.nst = 0;
     return P;
 }
 
