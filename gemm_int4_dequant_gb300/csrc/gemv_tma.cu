@@ -50,7 +50,10 @@ namespace gtma {
 
 using namespace ptx;
 
-constexpr int NC = 16;                        // consumer warps
+#ifndef W4_GEMV_NC
+#define W4_GEMV_NC 16
+#endif
+constexpr int NC = W4_GEMV_NC;                // consumer warps
 constexpr int THREADS = (NC + 1) * 32;        // + one producer warp
 constexpr int CT = NC * 32;                   // consumer threads
 constexpr int KB = 128;                       // k per unit (one consumer warp per unit)
@@ -88,7 +91,7 @@ __host__ __device__ inline Layout make_layout(int C, const Plan& P) {
     int o = P.nst * L.stage_bytes;
     o = (o + 127) & ~127;
     L.xf = o;        o += nkb_cap * 16 * C * 16;
-    L.xzero = o;     o += 16 * 16;
+    L.xzero = o;     o += 16 * C * 16;
     L.red = o;       o += P.perwarp ? 0 : 2 * NC * 16 * C * 4;
     L.part = o;      o += P.rows_cap * C * 4;
     L.partw = o;     o += P.perwarp ? NC * ((P.rows_cap + 15) / 16 * 16) * C * 4 : 0;
@@ -236,7 +239,7 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const __nv_bfloat16* __restrict_
             for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
             if (lane == 0) xsw[warp * C + c] = v;
         }
-        if (tid < 16) xzero[tid] = make_uint4(0, 0, 0, 0);
+        for (int i = tid; i < 16 * C; i += CT) xzero[i] = make_uint4(0, 0, 0, 0);
         named_barrier(1, CT);
         if (tid < C) {
             float v = 0.f;
@@ -249,7 +252,7 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const __nv_bfloat16* __restrict_
         const int g = lane >> 2, t4 = lane & 3;
         const bool bl = g < C;
         const uint4* xlane = bl ? xf + g * 4 + t4 : xzero + t4;
-        const int xw_stride = bl ? C * 4 : 4;
+        constexpr int xw_stride = C * 4;
         const int xkb_stride = bl ? 4 * C * 4 : 0;
         const uint32_t mask = dq.mask, magic = dq.magic;
         const int row_off_a = g * pitch + 16 * t4, row_off_b = (g + 8) * pitch + 16 * t4;
@@ -273,9 +276,12 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const __nv_bfloat16* __restrict_
                             const uint4 bx = xb[w * xw_stride];
                             const uint32_t va = wav[w], vb = wbv[w];
                             const uint32_t a0[4] = {and_or(va, mask, magic), and_or(vb, mask, magic),
-                                                    and_or(va >> 4, mask, magic), and_or(vb >> 4, mask, magic)};
-                            const uint32_t a1[4] = {and_or(va >> 8, mask, magic), and_or(vb >> 8, mask, magic),
-                                                    and_or(va >> 12, mask, magic), and_or(vb >> 12, mask, magic)};
+                                                    and_or((va >> 4), mask, magic),
+                                                    and_or((vb >> 4), mask, magic)};
+                            const uint32_t a1[4] = {and_or((va >> 8), mask, magic),
+                                                    and_or((vb >> 8), mask, magic),
+                                                    and_or((va >> 12), mask, magic),
+                                                    and_or((vb >> 12), mask, magic)};
                             mma_bf16(acc, a0, bx.x, bx.y);
                             mma_bf16(acc2, a1, bx.z, bx.w);
                         }
