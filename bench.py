@@ -184,16 +184,24 @@ def source_hash(files):
 
 
 KERNEL_SOURCES = {
-    "gemv": ["gemm_int4_dequant_gb300/csrc/gemv.cu", "gemm_int4_dequant_gb300/csrc/common.cuh"],
-    "gemm": ["gemm_int4_dequant_gb300/csrc/gemm_tc.cu", "gemm_int4_dequant_gb300/csrc/common.cuh"],
+    "gemv": ["gemm_int4_dequant_gb300/csrc/gemv_tma.cu", "gemm_int4_dequant_gb300/csrc/ptx.cuh",
+             "gemm_int4_dequant_gb300/csrc/common.cuh"],
+    "gemm": ["gemm_int4_dequant_gb300/csrc/gemm_tc.cu", "gemm_int4_dequant_gb300/csrc/ptx.cuh",
+             "gemm_int4_dequant_gb300/csrc/common.cuh"],
     "quant": ["gemm_int4_dequant_gb300/csrc/quant_permute.cu", "gemm_int4_dequant_gb300/csrc/common.cuh"],
 }
 
 
+PROFILE_FILES = {"decode": "gemv_decode_ncu.md", "gemm": "gemm_8192_ncu.md", "quant": "quant_8192_ncu.md"}
+
+
 def recorded_traffic(kind, workload):
-    """dram bytes per launch from profiles/<kind>_<workload>_ncu.md, if its
-    recorded source hash matches the current kernel source."""
-    p = os.path.join(ROOT, "profiles", "%s_%s_ncu.md" % (kind, workload))
+    """dram bytes per launch (per step for the two-kernel quant step) from the
+    ncu summary in profiles/, if its recorded source hash matches the current
+    kernel source; None otherwise."""
+    if workload not in PROFILE_FILES:
+        return None
+    p = os.path.join(ROOT, "profiles", PROFILE_FILES[workload])
     if not os.path.exists(p):
         return None
     text = open(p).read()
