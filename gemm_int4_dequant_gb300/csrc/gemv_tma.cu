@@ -96,7 +96,7 @@ __host__ __device__ inline Layout make_layout(int C, const Plan& P) {
     L.part = o;      o += P.rows_cap * C * 4;
     L.partw = o;     o += P.perwarp ? NC * ((P.rows_cap + 15) / 16 * 16) * C * 4 : 0;
     L.xsw = o;       o += NC * C * 4;
-    L.xsum = o;      o += 8 * 4;
+    L.xsum = o;      o += 16 * 4;                 // [0, 8): this CTA's sums, [8, 16): cluster totals
     L.sz = o;        o += P.rows_cap * 8;          // (scale, zero) per row as fp32
     o = (o + 7) & ~7;
     L.bars = o;      o += 2 * MAX_NST * 8;
@@ -183,9 +183,15 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const __nv_bfloat16* __restrict_
         }
     } else {
         // ------------------------------------------------------------ consumers
-        // scale / zero of this CTA's rows, early so their latency overlaps
-        for (int i = tid; i < nrows; i += CT)
-            sz[i] = make_float2(__bfloat162float(scale[r0 + i]), __bfloat162float(zero[r0 + i]));
+        // scale / zero of this CTA's rows: the first two per thread are loaded
+        // now into registers (nothing waits on them) and stored after the
+        // main loop, so their latency never delays the start
+        __nv_bfloat16 sc_pf[2], zr_pf[2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int i = tid + j * CT;
+            if (i < nrows) { sc_pf[j] = scale[r0 + i]; zr_pf[j] = zero[r0 + i]; }
+        }
         // x as B fragments: entry (kb, word p, n, t4) holds, for kk = kb*128 +
         // 32*t4 + 8*p, the bf16 pairs (x[kk], x[kk+4]) (x[kk+1], x[kk+5])
         // (x[kk+2], x[kk+6]) (x[kk+3], x[kk+7]) -- the b0b1/b2b3 registers of
@@ -196,27 +202,24 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const __nv_bfloat16* __restrict_
         float xs_part[C];
 #pragma unroll
         for (int c = 0; c < C; ++c) xs_part[c] = 0.f;
-        for (int e0 = tid; e0 < total; e0 += 4 * CT) {
-            uint4 raw[4];
-            int ent[4];
+        constexpr int XB = 8;  // loads in flight per thread while staging x
+        for (int e0 = tid; e0 < total; e0 += XB * CT) {
+            uint4 raw[XB];
 #pragma unroll
-            for (int b = 0; b < 4; ++b) {
+            for (int b = 0; b < XB; ++b) {
                 const int e = e0 + b * CT;
-                ent[b] = -1;
                 raw[b] = make_uint4(0, 0, 0, 0);
                 if (e < total) {
                     const int n = e / per_n, j = e - n * per_n;
-                    const int t = j & 3, p = (j >> 2) & 3, kb = j >> 4;
-                    const int kk = kb * KB + 32 * t + 8 * p;
-                    ent[b] = e;
+                    const int kk = (j >> 4) * KB + 32 * (j & 3) + 8 * ((j >> 2) & 3);
                     if (kk < klen)
                         raw[b] = *reinterpret_cast<const uint4*>(x + static_cast<int64_t>(n) * K + k0 + kk);
                 }
             }
 #pragma unroll
-            for (int b = 0; b < 4; ++b) {
-                if (ent[b] < 0) continue;
-                const int e = ent[b];
+            for (int b = 0; b < XB; ++b) {
+                const int e = e0 + b * CT;
+                if (e >= total) break;
                 const int n = e / per_n, j = e - n * per_n;
                 const int t = j & 3, p = (j >> 2) & 3, kb = j >> 4;
                 const uint4 r = raw[b];
@@ -316,6 +319,13 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const __nv_bfloat16* __restrict_
                 }
             }
         }
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int i = tid + j * CT;
+            if (i < nrows) sz[i] = make_float2(__bfloat162float(sc_pf[j]), __bfloat162float(zr_pf[j]));
+        }
+        for (int i = tid + 2 * CT; i < nrows; i += CT)
+            sz[i] = make_float2(__bfloat162float(scale[r0 + i]), __bfloat162float(zero[r0 + i]));
         if (P.perwarp) {
             named_barrier(1, CT);
             for (int i = tid; i < nrows * C; i += CT) {
@@ -327,23 +337,35 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const __nv_bfloat16* __restrict_
     }
     __syncthreads();
 
-    // combine the K-slices of the cluster, fold the offset, scale, store
+    // combine the K-slices of the cluster, fold the offset, scale, store.
+    // Rank ks writes rows ks, ks+S, ...; every (row, c) is one thread, so the
+    // remote (distributed shared memory) loads of all ranks are in flight at once.
     cg::cluster_group cluster = cg::this_cluster();
+    float* xs_tot = xsum + 8;
     if (S > 1) cluster.sync();
-    for (int i = ks + S * tid; i < nrows; i += S * THREADS) {
-        const float2 s_z = sz[i];
-        const float off = 128.0f + s_z.y;
+    if (tid < C) {
+        float v = 0.f;
+        for (int r = 0; r < S; ++r) v += (S > 1 ? cluster.map_shared_rank(xsum, r) : xsum)[tid];
+        xs_tot[tid] = v;
+    }
+    __syncthreads();
+    const int my_rows = nrows > ks ? (nrows - ks + S - 1) / S : 0;
+    for (int j = tid; j < my_rows * C; j += THREADS) {
+        const int i = ks + S * (j / C), c = j - (j / C) * C;
+        float sum = 0.f;
+        if (S > 1) {
+            float v[8];
 #pragma unroll
-        for (int c = 0; c < C; ++c) {
-            float sum = 0.f, xs = 0.f;
-            for (int r = 0; r < S; ++r) {
-                const float* pp = (S > 1) ? cluster.map_shared_rank(part, r) : part;
-                const float* xx = (S > 1) ? cluster.map_shared_rank(xsum, r) : xsum;
-                sum += pp[i * C + c];
-                xs += xx[c];
-            }
-            d[static_cast<int64_t>(c) * N + r0 + i] = __float2bfloat16_rn(s_z.x * fmaf(-off, xs, sum));
+            for (int r = 0; r < 8; ++r)
+                if (r < S) v[r] = cluster.map_shared_rank(part, r)[i * C + c];
+#pragma unroll
+            for (int r = 0; r < 8; ++r)
+                if (r < S) sum += v[r];
+        } else {
+            sum = part[i * C + c];
         }
+        const float2 s_z = sz[i];
+        d[static_cast<int64_t>(c) * N + r0 + i] = __float2bfloat16_rn(s_z.x * fmaf(-(128.0f + s_z.y), xs_tot[c], sum));
     }
     if (S > 1) cluster.sync();
 }
