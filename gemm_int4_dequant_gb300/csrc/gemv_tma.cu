@@ -152,6 +152,10 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const __nv_bfloat16* __restrict_
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    // Launched with programmatic stream serialisation: everything above
+    // overlapped the previous kernel's tail; no global memory is read before
+    // the previous grid has completed.
+    pdl_wait();
     __syncthreads();
 
     if (warp == NC) {
@@ -336,6 +340,7 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const __nv_bfloat16* __restrict_
         }
     }
     __syncthreads();
+    pdl_launch_dependents();
 
     // combine the K-slices of the cluster, fold the offset, scale, store.
     // Rank ks writes rows ks, ks+S, ...; every (row, c) is one thread, so the
@@ -431,13 +436,15 @@ w4_status launch_gemv_tma_t(const void* qw, const void* scale, const void* zero,
     cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3(THREADS, 1, 1);
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = P.S;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     cudaError_t e = ensure_smem_limit(kern, make_layout(C, P).total + 1024, smem_set);
     if (e != cudaSuccess) return W4_ERR_CUDA;
     if (P.S > 1) {

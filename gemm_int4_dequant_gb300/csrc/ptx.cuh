@@ -172,6 +172,14 @@ __device__ __forceinline__ bool mbar_wait_fast(uint32_t bar, uint32_t parity, vo
     return mbar_try_wait(bar, parity) || mbar_wait(bar, parity, abort_flag);
 }
 
+// Programmatic dependent launch.  wait: block until the preceding grid in
+// the stream has completed and its memory is visible (a no-op when the
+// launch had no programmatic dependency).  launch_dependents: allow the next
+// grid in the stream to begin launching (its own wait still orders it after
+// this grid's completion).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+
 // Named barrier over `count` threads (id 1..15; 0 is __syncthreads).
 __device__ __forceinline__ void named_barrier(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
