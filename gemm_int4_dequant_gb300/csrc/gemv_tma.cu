@@ -272,26 +272,15 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const __nv_bfloat16* __restrict_
                 const bool ok = mbar_wait_fast(bar_full + 8 * slot, round & 1, abort_flag);
                 if (ok) {
                     const uint8_t* st = sm + slot * L.stage_bytes;
-                    // two-deep software pipeline over this warp's units of the
-                    // stage: the shared loads of the next unit are in flight
-                    // while the current one is dequantised and multiplied
-                    const uint4* xst = xlane + ch * (P.kchunk / KB) * xkb_stride;
-                    uint4 wa, wb, bx[4];
-                    auto load = [&](int u) {
-                        wa = *reinterpret_cast<const uint4*>(st + row_off_a + u * 64);
-                        wb = *reinterpret_cast<const uint4*>(st + row_off_b + u * 64);
-                        const uint4* xb = xst + u * xkb_stride;
-#pragma unroll
-                        for (int w = 0; w < 4; ++w) bx[w] = xb[w * xw_stride];
-                    };
-                    if (first < units) load(first);
                     for (int u = first; u < units; u += NC) {
+                        const uint4 wa = *reinterpret_cast<const uint4*>(st + row_off_a + u * 64);
+                        const uint4 wb = *reinterpret_cast<const uint4*>(st + row_off_b + u * 64);
+                        const uint4* xb = xlane + (ch * (P.kchunk / KB) + u) * xkb_stride;
                         const uint32_t wav[4] = {wa.x, wa.y, wa.z, wa.w};
                         const uint32_t wbv[4] = {wb.x, wb.y, wb.z, wb.w};
-                        const uint4 bxc[4] = {bx[0], bx[1], bx[2], bx[3]};
-                        if (u + NC < units) load(u + NC);
 #pragma unroll
                         for (int w = 0; w < 4; ++w) {
+                            const uint4 bx = xb[w * xw_stride];
                             const uint32_t va = wav[w], vb = wbv[w];
                             const uint32_t a0[4] = {and_or(va, mask, magic), and_or(vb, mask, magic),
                                                     and_or((va >> 4), mask, magic),
@@ -300,8 +289,8 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const __nv_bfloat16* __restrict_
                                                     and_or((vb >> 8), mask, magic),
                                                     and_or((va >> 12), mask, magic),
                                                     and_or((vb >> 12), mask, magic)};
-                            mma_bf16(acc, a0, bxc[w].x, bxc[w].y);
-                            mma_bf16(acc2, a1, bxc[w].z, bxc[w].w);
+                            mma_bf16(acc, a0, bx.x, bx.y);
+                            mma_bf16(acc2, a1, bx.z, bx.w);
                         }
                     }
                 }
