@@ -13,9 +13,14 @@
 //   warp 1      TMEM allocator and MMA issuer (one thread): 4 x
 //               tcgen05.mma.cta_group::1.kind::f16 (M128 N256 K16) per k-tile,
 //               fp32 accumulator in TMEM, tcgen05.commit frees the stage;
-//   warps 2..5  dequant: packed bytes -> (u - zero) bf16, written straight into
+//   warps 2..9  dequant: packed bytes -> (u - zero) bf16, written straight into
 //               the canonical 128B-swizzled MN-major operand layout, then the
 //               epilogue: tcgen05.ld of the accumulator, * scale, -> bf16.
+// Inside every group of four columns the shared-memory (and so TMEM) column
+// order is n0 n2 n1 n3: one mask of a packed 32-bit word then yields the
+// nibbles of bytes 0 and 2 (or 1 and 3) as a bf16 pair, so unpacking eight
+// weights costs three shifts and four three-input logic ops.  The epilogue
+// puts the columns back in order.
 // Every wait is bounded; on timeout the kernel records an error code in a
 // device word (w4_device_error), stops issuing work, drains and frees TMEM.
 
@@ -33,7 +38,7 @@ using namespace ptx;
 
 constexpr int BM = 128, BN = 256, BK = 64;
 constexpr int STAGES = 4;
-constexpr int THREADS = 192;
+constexpr int THREADS = 320;
 constexpr int A_BYTES = BM * BK * 2;         // 16 KB
 constexpr int BP_BYTES = (BK / 2) * BN;      // 8 KB packed
 constexpr int BD_BYTES = BK * BN * 2;        // 32 KB dequantised
@@ -47,7 +52,7 @@ constexpr int OFF_ABORT = OFF_TMEM_SLOT + 4;
 constexpr int SMEM_USED = OFF_ABORT + 4;
 constexpr int SMEM_BYTES = SMEM_USED + 1024;  // slack to align the base to 1 KB
 constexpr uint32_t TMEM_COLS = 256;
-constexpr int DEQ_THREADS = 128;
+constexpr int DEQ_THREADS = 256;
 
 
 // Shared-memory matrix descriptor (sm_100 format): start address, leading and
@@ -82,15 +87,15 @@ __device__ __forceinline__ uint32_t bsub2(uint32_t a, uint32_t b) {
     return d;
 }
 
-// Two packed bytes (columns n, n+1, in the low 16 bits of `pair`) -> bf16x2
-// for even k (low nibbles) and odd k (high nibbles), minus the zero points.
-__device__ __forceinline__ void dequant_pair(uint32_t pair16, uint32_t zz, uint32_t& even, uint32_t& odd) {
-    const uint32_t spread = __byte_perm(pair16, 0u, 0x4140);  // byte0 -> bits 0..7, byte1 -> bits 16..23
-    const uint32_t k128 = 0x43004300u;                        // bf16x2 (128, 128)
-    const uint32_t lo = (spread & 0x000F000Fu) | k128;        // 128 + u_even
-    const uint32_t hi = ((spread >> 4) & 0x000F000Fu) | k128; // 128 + u_odd
-    even = bsub2(bsub2(lo, k128), zz);
-    odd = bsub2(bsub2(hi, k128), zz);
+// One packed word (bytes b0..b3 = columns c0..c3; low nibble = even k) ->
+// bf16 pairs in shared-memory column order (c0, c2) and (c1, c3):
+// e0/e1 for the even k, o0/o1 for the odd k, each 128 + u.
+__device__ __forceinline__ void unpack_word(uint32_t w, uint32_t& e0, uint32_t& e1, uint32_t& o0, uint32_t& o1) {
+    const uint32_t mask = 0x000F000Fu, magic = 0x43004300u;  // bf16x2 (128, 128)
+    e0 = and_or(w, mask, magic);
+    e1 = and_or(w >> 8, mask, magic);
+    o0 = and_or(w >> 4, mask, magic);
+    o1 = and_or(w >> 12, mask, magic);
 }
 
 __global__ void __launch_bounds__(THREADS, 1)
@@ -173,21 +178,33 @@ gemm_w4_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
             mbar_drain(tmem_full, 0);  // all MMAs done before TMEM can be freed
         }
     } else {
-        // ---------------- dequant (warps 2..5) ----------------
-        const int t = threadIdx.x - 64;          // 0..127
+        // ---------------- dequant (warps 2..9) ----------------
+        const int t = threadIdx.x - 64;          // 0..255
         const int nl = (t & 31) * 8;             // 8 columns per thread
-        const int kp_lane = t >> 5;              // 0..3
-        uint32_t zz[4];
+        const int kp_lane = t >> 5;              // 0..7
+        // zero-point pairs in shared-memory column order: (z0,z2) (z1,z3) (z4,z6) (z5,z7).
+        // Fast path: 128 + z exact in bf16 (integer zero points) -> one subtract.
+        uint32_t zz[4], zraw[4];
+        bool fast = true;
         {
-            uint16_t zb[8];
+            float zf[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 const int n = n0 + nl + j;
-                zb[j] = n < N ? __bfloat16_as_ushort(zero[n]) : 0;
+                zf[j] = n < N ? __bfloat162float(zero[n]) : 0.f;
             }
+            const int pa[4] = {0, 1, 4, 5}, pb[4] = {2, 3, 6, 7};
 #pragma unroll
-            for (int j = 0; j < 4; ++j) zz[j] = static_cast<uint32_t>(zb[2 * j]) | (static_cast<uint32_t>(zb[2 * j + 1]) << 16);
+            for (int j = 0; j < 4; ++j) {
+                const float a = 128.0f + zf[pa[j]], b = 128.0f + zf[pb[j]];
+                const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+                fast = fast && __low2float(h) == a && __high2float(h) == b;
+                zz[j] = *reinterpret_cast<const uint32_t*>(&h);
+                const __nv_bfloat162 r = __floats2bfloat162_rn(zf[pa[j]], zf[pb[j]]);
+                zraw[j] = *reinterpret_cast<const uint32_t*>(&r);
+            }
         }
+        const uint32_t k128 = 0x43004300u;
         bool ok = true;
         for (int kt = 0; kt < num_kt && ok; ++kt) {
             const int s = kt % STAGES, round = kt / STAGES;
@@ -196,40 +213,57 @@ gemm_w4_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
             const uint8_t* bp = sbase + OFF_BP + s * BP_BYTES;
             uint8_t* bd = sbase + OFF_BD + s * BD_BYTES;
 #pragma unroll
-            for (int i = 0; i < (BK / 2) / 4; ++i) {
-                const int kp = kp_lane + 4 * i;
+            for (int i = 0; i < (BK / 2) / 8; ++i) {
+                const int kp = kp_lane + 8 * i;
                 const uint2 v = *reinterpret_cast<const uint2*>(bp + kp * BN + nl);
-                uint32_t ev[4], od[4];
-                dequant_pair(v.x & 0xFFFFu, zz[0], ev[0], od[0]);
-                dequant_pair(v.x >> 16, zz[1], ev[1], od[1]);
-                dequant_pair(v.y & 0xFFFFu, zz[2], ev[2], od[2]);
-                dequant_pair(v.y >> 16, zz[3], ev[3], od[3]);
-                *reinterpret_cast<uint4*>(bd + bd_offset(2 * kp, nl)) = make_uint4(ev[0], ev[1], ev[2], ev[3]);
-                *reinterpret_cast<uint4*>(bd + bd_offset(2 * kp + 1, nl)) = make_uint4(od[0], od[1], od[2], od[3]);
+                uint32_t e[4], o[4];
+                unpack_word(v.x, e[0], e[1], o[0], o[1]);
+                unpack_word(v.y, e[2], e[3], o[2], o[3]);
+                if (fast) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) { e[j] = bsub2(e[j], zz[j]); o[j] = bsub2(o[j], zz[j]); }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        e[j] = bsub2(bsub2(e[j], k128), zraw[j]);
+                        o[j] = bsub2(bsub2(o[j], k128), zraw[j]);
+                    }
+                }
+                *reinterpret_cast<uint4*>(bd + bd_offset(2 * kp, nl)) = make_uint4(e[0], e[1], e[2], e[3]);
+                *reinterpret_cast<uint4*>(bd + bd_offset(2 * kp + 1, nl)) = make_uint4(o[0], o[1], o[2], o[3]);
             }
             fence_proxy_async_smem();
             mbar_arrive(full_deq(s));
         }
 
         // ---------------- epilogue ----------------
+        // warps 2..9: TMEM lane quarter (warp % 4), column half ((warp-2) / 4)
         if (ok && mbar_wait(tmem_full, 0, abort_flag)) {
             tc_fence_after();
             const int quarter = warp & 3;           // TMEM lanes 32*quarter .. +31
+            const int half = (warp - 2) >> 2;
             const int m = m0 + quarter * 32 + lane;
-            for (int cb = 0; cb < BN / 32; ++cb) {
+            for (int cb = half * (BN / 64); cb < (half + 1) * (BN / 64); ++cb) {
                 uint32_t r[32];
                 tmem_ld32(tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + cb * 32, r);
                 const int nb = n0 + cb * 32;
                 if (m < M && nb < N) {
+                    // TMEM column order inside each group of 4 is n0 n2 n1 n3
                     uint32_t packed[16];
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const int na = nb + 2 * j;
-                        const float s0 = na < N ? __bfloat162float(scale[na]) : 0.f;
-                        const float s1 = na + 1 < N ? __bfloat162float(scale[na + 1]) : 0.f;
-                        const __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(r[2 * j]) * s0,
-                                                                       __uint_as_float(r[2 * j + 1]) * s1);
-                        packed[j] = *reinterpret_cast<const uint32_t*>(&h);
+                    for (int g4 = 0; g4 < 8; ++g4) {
+                        const int na = nb + 4 * g4;
+                        float sc[4];
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) sc[q] = na + q < N ? __bfloat162float(scale[na + q]) : 0.f;
+                        const float v0 = __uint_as_float(r[4 * g4 + 0]) * sc[0];
+                        const float v1 = __uint_as_float(r[4 * g4 + 2]) * sc[1];
+                        const float v2 = __uint_as_float(r[4 * g4 + 1]) * sc[2];
+                        const float v3 = __uint_as_float(r[4 * g4 + 3]) * sc[3];
+                        const __nv_bfloat162 h01 = __floats2bfloat162_rn(v0, v1);
+                        const __nv_bfloat162 h23 = __floats2bfloat162_rn(v2, v3);
+                        packed[2 * g4] = *reinterpret_cast<const uint32_t*>(&h01);
+                        packed[2 * g4 + 1] = *reinterpret_cast<const uint32_t*>(&h23);
                     }
                     __nv_bfloat16* dst = C + static_cast<int64_t>(m) * N + nb;
                     if (nb + 32 <= N) {
