@@ -55,13 +55,28 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// try_wait that lets the hardware suspend the thread until the phase
+// completes (or a time hint of about a millisecond passes), instead of
+// returning at once: a waiting warp then stops taking issue slots.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(1000000u)
+        : "memory");
+    return ok != 0;
+}
+
 // Bounded wait: about two seconds of SM clock, or until another role of this
 // CTA has aborted.  Returns false on timeout/abort.
 static __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_sleep(bar, parity)) return true;
         if (*abort_flag) return false;
         if (clock64() - t0 > (1ll << 32)) {
             *abort_flag = 1;
@@ -75,7 +90,7 @@ static __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, vol
 // work this CTA already issued (TMA copies, MMAs) before it frees resources.
 static __device__ __noinline__ void mbar_drain(uint32_t bar, uint32_t parity) {
     const long long t0 = clock64();
-    while (!mbar_try_wait(bar, parity)) {
+    while (!mbar_try_wait_sleep(bar, parity)) {
         if (clock64() - t0 > (1ll << 32)) {
             atomicCAS(&g_device_error, 0, ERR_TIMEOUT);
             return;
