@@ -55,18 +55,6 @@ constexpr uint32_t TMEM_COLS = 256;
 constexpr int DEQ_THREADS = 256;
 
 
-// Shared-memory matrix descriptor (sm_100 format): start address, leading and
-// stride byte offsets (all >> 4), descriptor version 1, 128-byte swizzle.
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
-    uint64_t d = 0;
-    d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
-    d |= static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16;
-    d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
-    d |= 1ull << 46;  // version
-    d |= 2ull << 61;  // SWIZZLE_128B
-    return d;
-}
-
 // Instruction descriptor, kind::f16: D fp32, A bf16 K-major, B bf16 MN-major,
 // N = 256, M = 128.
 constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (0u << 15) | (1u << 16) |
@@ -237,8 +225,9 @@ gemm_w4_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
         }
 
         // ---------------- epilogue ----------------
-        // warps 2..9: TMEM lane quarter (warp % 4), column half ((warp-2) / 4)
-        if (ok && mbar_wait(tmem_full, 0, abort_flag)) {
+        // warps 2..9: TMEM lane quarter (warp % 4), column half ((warp-2) / 4);
+        // the decision is warp-uniform (tcgen05.ld is warp-collective)
+        if (__all_sync(0xffffffffu, ok && mbar_wait(tmem_full, 0, abort_flag))) {
             tc_fence_after();
             const int quarter = warp & 3;           // TMEM lanes 32*quarter .. +31
             const int half = (warp - 2) >> 2;

@@ -59,6 +59,9 @@ constexpr int CT = NC * 32;                   // consumer threads
 constexpr int KB = 128;                       // k per unit (one consumer warp per unit)
 constexpr int MAX_NST = 8;                    // stages in the ring (at most)
 constexpr int KCHUNK_MAX = 8192;              // k per stage at most (4 KB per row)
+#ifndef W4_GEMV_PREFETCH_STAGES
+#define W4_GEMV_PREFETCH_STAGES 1               // stages warmed in L2 before the wait
+#endif
 
 // Nibble mask and bf16 magic passed at run time so they stay in registers and
 // each mask-and-OR is a single three-input logic op.
@@ -152,9 +155,27 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const __nv_bfloat16* __restrict_
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    // Launched with programmatic stream serialisation: everything above
-    // overlapped the previous kernel's tail; no global memory is read before
-    // the previous grid has completed.
+    // Launched with programmatic stream serialisation.  Before waiting for
+    // the previous kernel, warm L2 with this CTA's first stage(s): L2 is the
+    // device's point of coherence, so a prefetch cannot yield stale data even
+    // if the previous kernel writes these bytes; every load into shared
+    // memory or registers is issued only after the wait.
+    if (warp == NC && lane == 0) {
+        const int64_t row_bytes = K / 2;
+        const uint8_t* src0 = qw + static_cast<int64_t>(r0) * row_bytes + k0 / 2;
+        int tile = 0, ch = 0;
+        for (int s = 0; s < min(nstages, W4_GEMV_PREFETCH_STAGES); ++s) {
+            const int rows_here = min(16, nrows - tile * 16);
+            const int seg = min(P.kchunk, klen - ch * P.kchunk) / 2;
+            const uint8_t* src = src0 + static_cast<int64_t>(tile) * 16 * row_bytes + ch * (P.kchunk / 2);
+            if (P.dense) {
+                bulk_prefetch_l2(src, rows_here * seg);
+            } else {
+                for (int r = 0; r < rows_here; ++r) bulk_prefetch_l2(src + r * row_bytes, seg);
+            }
+            if (++ch == nch) { ch = 0; ++tile; }
+        }
+    }
     pdl_wait();
     __syncthreads();
 
@@ -340,6 +361,8 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const __nv_bfloat16* __restrict_
         }
     }
     __syncthreads();
+    // the next kernel in the stream may begin launching (its own wait still
+    // orders its reads after this grid has completed)
     pdl_launch_dependents();
 
     // combine the K-slices of the cluster, fold the offset, scale, store.

@@ -147,6 +147,18 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// Shared-memory matrix descriptor (sm_100 format): start address, leading and
+// stride byte offsets (all >> 4), descriptor version 1, 128-byte swizzle.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+    d |= static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
+    d |= 1ull << 46;  // version
+    d |= 2ull << 61;  // SWIZZLE_128B
+    return d;
+}
+
 __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar,
                                                  uint64_t policy) {
     asm volatile(
@@ -172,6 +184,12 @@ __device__ __forceinline__ void bulk_load_hint(uint32_t dst, const void* src, ui
             dst),
         "l"(src), "r"(bytes), "r"(bar), "l"(policy)
         : "memory");
+}
+
+// Prefetch `bytes` (a multiple of 16) at a 16-byte aligned global address
+// into L2; no shared-memory destination, no completion tracking.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 // (a & b) | c in one LOP3 with all three operands in registers.

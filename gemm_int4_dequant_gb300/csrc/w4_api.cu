@@ -98,7 +98,7 @@ w4_status permute_int4(const void* packed, void* out, int64_t K, int64_t N, void
 w4_status gemv_w4(const void* qweight, const void* scale, const void* zero, const void* x, void* d, int64_t N,
                   int64_t K, int64_t C, w4_dtype dtype, void* stream) {
     if (dtype != W4_F32 && dtype != W4_BF16) return W4_ERR_DTYPE;
-    if (N < 0 || K < 0 || (K % 8) != 0 || C < 1 || C > 8) return W4_ERR_SHAPE;
+    if (N < 0 || K < 0 || (K % 8) != 0 || K > W4_GEMV_MAX_K || C < 1 || C > 8) return W4_ERR_SHAPE;
     if (N == 0) return W4_OK;
     if (!d || !scale || !zero || (K > 0 && (!qweight || !x))) return W4_ERR_NULL;
     if (!aligned16(d) || !aligned16(scale) || !aligned16(zero) ||

@@ -54,6 +54,9 @@ typedef enum {
     W4_ERR_DEVICE = -6
 } w4_status;
 
+/* Largest K that gemv_w4 accepts. */
+#define W4_GEMV_MAX_K 40960
+
 /* Element type of gemv_w4's x, scale, zero and d (all four share it). */
 typedef enum { W4_F32 = 0, W4_BF16 = 1 } w4_dtype;
 
@@ -127,8 +130,9 @@ w4_status permute_int4(const void* packed, void* out, int64_t K, int64_t N, void
  * scale, zero  [N] of `dtype`.
  * x        [C][K] of `dtype`, row-major.
  * d        [C][N] of `dtype`, row-major (output).
- * All pointers 16-byte aligned.  K % 8 == 0 (the caller pads K), 1 <= C <= 8,
- * N >= 0.  K == 0 gives d = 0.  Accumulation is fp32; with dtype W4_BF16 the
+ * All pointers 16-byte aligned.  K % 8 == 0 (the caller pads K),
+ * K <= W4_GEMV_MAX_K (x is held in the shared memory of at most eight SMs),
+ * 1 <= C <= 8, N >= 0.  K == 0 gives d = 0.  Accumulation is fp32; with dtype W4_BF16 the
  * result is rounded once to bf16.  The difference from the exact value is
  * bounded by the parity tolerance of the test suite (2e-3 * sum_k |w*x|
  * for bf16, 1e-5 * sum_k |w*x| for fp32).

@@ -71,6 +71,7 @@ def test_argument_validation_happens_on_host():
     assert lib.gemv_w4(A, A, A, A, A, 16, 12, 1, L.W4_BF16, None) == L.W4_ERR_SHAPE
     assert lib.gemv_w4(A, A, A, A, A, 16, 16, 0, L.W4_BF16, None) == L.W4_ERR_SHAPE
     assert lib.gemv_w4(A, A, A, A, A, 16, 16, 9, L.W4_BF16, None) == L.W4_ERR_SHAPE
+    assert lib.gemv_w4(A, A, A, A, A, 16, 40960 + 8, 1, L.W4_BF16, None) == L.W4_ERR_SHAPE  # K limit
     assert lib.gemv_w4(A, A, A, A, A, 16, 16, 1, 7, None) == L.W4_ERR_DTYPE
     assert lib.gemv_w4(A, A, None, A, A, 16, 16, 1, L.W4_F32, None) == L.W4_ERR_NULL
     assert lib.gemv_w4(A, A, A, odd, A, 16, 16, 1, L.W4_F32, None) == L.W4_ERR_ALIGN

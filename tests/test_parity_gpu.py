@@ -129,6 +129,12 @@ def test_gemv_small_batch_full_size(w4, cfg):
     (1000, 40000, 2, "bf16"),   # long K: split across a cluster
     (333, 24008, 7, "bf16"),    # long ragged K, cluster split, word loads
     (257, 12288, 8, "f32"),     # fp32 x split across a cluster
+    (1, 256, 1, "bf16"),        # one row, one band
+    (3, 288, 8, "bf16"),        # partial band (x zero-padded), rows < one lane quarter
+    (40000, 512, 3, "bf16"),    # several row tiles per CTA
+    (1001, 17312, 8, "bf16"),   # cluster split with a partial last band per slice
+    (5, 40960, 8, "bf16"),      # longest K accepted
+    (400000, 256, 1, "bf16"),   # more row tiles than one wave holds
 ])
 def test_gemv_ragged_and_edge(w4, N, K, C, act):
     _check_gemv(w4, N, K, C, act, seed=N + K + C)
