@@ -1,6 +1,8 @@
 // common.cuh -- small device/host helpers shared by the library's kernels.
 #pragma once
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -17,6 +19,10 @@ namespace w4 {
 int sm_count();
 // True if the current device is compute capability 10.3 (GB300).
 bool device_is_sm103();
+
+// cuTensorMapEncodeTiled, reached through the runtime's driver entry-point
+// query (the library does not link the driver API); nullptr if unavailable.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 

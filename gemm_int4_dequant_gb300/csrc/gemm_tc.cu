@@ -278,22 +278,6 @@ gemm_w4_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
     }
 }
 
-// ---- host side --------------------------------------------------------------
-
-PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
-                cudaSuccess ||
-            q != cudaDriverEntryPointSuccess)
-            return nullptr;
-        fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }
-    return fn;
-}
-
 }  // namespace gemm
 
 w4_status run_gemm(const void* A, const void* B, const void* scale, const void* zero, void* C, int64_t M,
@@ -302,7 +286,7 @@ w4_status run_gemm(const void* A, const void* B, const void* scale, const void* 
     if (M > 0x7FFFFFFF || N > 0x7FFFFFFF || K > 0x7FFFFFFF) return W4_ERR_SHAPE;
     const int64_t tiles_m = (M + BM - 1) / BM, tiles_n = (N + BN - 1) / BN;
     if (tiles_m > 65535 || tiles_n > 0x7FFFFFFF) return W4_ERR_SHAPE;
-    auto encode = get_encode_fn();
+    auto encode = tensor_map_encoder();
     if (!encode) return W4_ERR_CUDA;
 
     CUtensorMap ta, tb;

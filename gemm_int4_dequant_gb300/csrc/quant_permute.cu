@@ -6,12 +6,201 @@
 // Both kernels are HBM-bound byte movers.  Roofline bytes per element are
 // stated next to each kernel.
 
+#include <cooperative_groups.h>
+
+#include <algorithm>
+
 #include "common.cuh"
+#include "ptx.cuh"
+
+namespace cg = cooperative_groups;
 
 namespace w4 {
 
 // ---------------------------------------------------------------------------
-// quantize_pack_int4
+// quantize_pack_int4, single HBM read (N % 8 == 0, K <= QC_MAX_K)
+//
+// A thread-block cluster of cs CTAs owns a strip of 32 columns over all K;
+// CTA r holds rows [r*R, r*R + R) of the strip in shared memory, loaded once
+// with 2-D TMA boxes (64 bytes x up to 256 rows).  Each CTA reduces its rows
+// to a per-column max |W| (bf16 bit patterns with the sign cleared order
+// non-negative values exactly), the CTAs read each other's partial maxima
+// through distributed shared memory, and every CTA then quantises the rows it
+// already holds.  W is read from HBM exactly once.  Algorithmic bytes: 2 B
+// read per weight + 0.5 B written.  64 KB per CTA for K = 8192, so three
+// CTAs share an SM and one's copy overlaps another's arithmetic.
+// ---------------------------------------------------------------------------
+
+constexpr int QC_COLS = 32;                      // columns per strip (64-byte rows)
+constexpr int QC_THREADS = 256;
+constexpr int QC_RL = QC_THREADS / 4;            // row lanes (4 threads of 8 columns per row)
+constexpr int QC_CS = 8;                         // CTAs per cluster at most (K-slices)
+constexpr int QC_BOXR = 256;                     // rows per TMA box
+constexpr int QC_SMEM = 208 * 1024;              // strip rows per CTA at most (bytes)
+constexpr int QC_MAX_R = QC_SMEM / (QC_COLS * 2) / QC_BOXR * QC_BOXR;
+constexpr int64_t QC_MAX_K = static_cast<int64_t>(QC_CS) * QC_MAX_R;
+
+// q = clamp(round_half_away(w / s), -8, 7) as a nibble; s == 0 gives 0.
+__device__ __forceinline__ uint32_t quant_nibble(uint32_t wbits, float s) {
+    float w = bf16_bits_to_f32(wbits & 0xFFFFu);
+    float r = (s == 0.0f) ? 0.0f : roundf(__fdiv_rn(w, s));
+    r = fminf(fmaxf(r, -8.0f), 7.0f);
+    return static_cast<uint32_t>(static_cast<int>(r)) & 0xFu;
+}
+
+// The same nibble from one FMA, for all but near-ties.
+//   u = fl(w * inv + C),  inv = fl(1/s) (0 when s = 0),  C = 192.5 + 2^-15.
+// |w| <= max|w| = 7 s, so u lies in [128, 256) where the fp32 ulp is 2^-16:
+// mantissa bits 16..19 hold floor(w*inv + 0.5) mod 16 (192 = 0 mod 16) and
+// the low 16 bits its fraction, lifted by 2^-15.  Unless those low bits are
+// < 4 (the fraction is within 2^-14 of an integer), the exact product
+// w * inv -- within 1e-6 of the IEEE quotient fl(w / s) -- is clear of every
+// half-integer by more than that error, so floor(w*inv + 0.5) equals
+// round-half-away(fl(w / s)); |q| <= 7, so no clamp.  Near-ties (exact ties
+// such as w = max|w| / 2 recur in real columns) are flagged for the exact
+// division.
+__device__ __forceinline__ uint32_t quant_u(uint32_t wbits16_hi, float inv) {
+    return __float_as_uint(__fmaf_rn(__uint_as_float(wbits16_hi), inv, 192.50003051757812f));
+}
+__device__ __forceinline__ bool quant_near(uint32_t u) { return (u & 0xFFFCu) == 0; }
+
+__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// R = rows per CTA (a multiple of box); box = TMA box height;
+// grid = strips * cs with clusters of cs CTAs.
+__global__ void __launch_bounds__(QC_THREADS)
+quantize_pack_cluster_kernel(const __grid_constant__ CUtensorMap tmap, uint8_t* __restrict__ packed,
+                             float* __restrict__ scale, int K, int N, int R, int box) {
+    extern __shared__ __align__(128) uint8_t qtile[];   // [R][32] bf16
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ uint32_t pmax[QC_COLS];
+    __shared__ uint32_t wmax[QC_THREADS / 32][QC_COLS];
+    __shared__ float s_scale[QC_COLS], s_inv[QC_COLS];
+    __shared__ int abort_word;
+    cg::cluster_group cluster = cg::this_cluster();
+    const int cs = static_cast<int>(cluster.num_blocks());
+    const int rank = static_cast<int>(cluster.block_rank());
+    const int n0 = (blockIdx.x / cs) * QC_COLS;
+    const int k0 = rank * R;
+    const int rows = max(0, min(R, K - k0));      // even
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int g = tid & 3, rl = tid >> 2;          // 8-column group, row lane
+    const uint32_t b = ptx::smem_u32(&bar);
+
+    if (tid == 0) {
+        ptx::mbar_init(b, 1);
+        abort_word = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    const int nbox = (rows + box - 1) / box;
+    if (tid == 0 && nbox > 0) {
+        ptx::mbar_arrive_expect_tx(b, static_cast<uint32_t>(nbox) * box * QC_COLS * 2);
+        for (int i = 0; i < nbox; ++i)
+            ptx::tma_load_2d(ptx::smem_u32(qtile + static_cast<size_t>(i) * box * QC_COLS * 2), &tmap, n0,
+                             k0 + i * box, b);
+    }
+
+    // column max of |W| over this CTA's rows; word j of a 16-byte group holds
+    // columns 2j (low half) and 2j+1 (high half), reduced packed
+    uint32_t amax[4] = {0, 0, 0, 0};
+    bool ok = nbox == 0 || ptx::mbar_wait(b, 0, &abort_word);
+    if (!ok && tid == 0) ptx::mbar_drain(b, 0);   // copies still landing
+    if (ok) {
+#pragma unroll 4
+        for (int r = rl; r < rows; r += QC_RL) {
+            const uint4 v = *reinterpret_cast<const uint4*>(qtile + r * (QC_COLS * 2) + g * 16);
+            amax[0] = max_u16x2(amax[0], v.x & 0x7FFF7FFFu);
+            amax[1] = max_u16x2(amax[1], v.y & 0x7FFF7FFFu);
+            amax[2] = max_u16x2(amax[2], v.z & 0x7FFF7FFFu);
+            amax[3] = max_u16x2(amax[3], v.w & 0x7FFF7FFFu);
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) amax[j] = max_u16x2(amax[j], __shfl_xor_sync(0xffffffffu, amax[j], o));
+    }
+    if (lane < 4) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            wmax[warp][lane * 8 + 2 * j] = amax[j] & 0xFFFFu;
+            wmax[warp][lane * 8 + 2 * j + 1] = amax[j] >> 16;
+        }
+    }
+    __syncthreads();
+    if (tid < QC_COLS) {
+        uint32_t m = 0;
+        for (int w = 0; w < QC_THREADS / 32; ++w) m = max(m, wmax[w][tid]);
+        pmax[tid] = m;
+    }
+    cluster.sync();
+    if (tid < QC_COLS) {
+        uint32_t m = 0;
+        for (int r = 0; r < cs; ++r) m = max(m, cluster.map_shared_rank(pmax, r)[tid]);
+        const float sc = __fdiv_rn(bf16_bits_to_f32(m), 7.0f);
+        s_scale[tid] = sc;
+        s_inv[tid] = sc == 0.0f ? 0.0f : __frcp_rn(sc);
+        if (rank == 0 && n0 + tid < N) scale[n0 + tid] = sc;
+    }
+    __syncthreads();
+
+    // quantise the resident rows two at a time (low nibble = even row).
+    // Control flow is warp-uniform: the trip count is the warp's, lanes past
+    // the last pair redo a valid pair without storing, and the exact fix-up
+    // of near-ties runs under a warp vote.
+    if (__all_sync(0xffffffffu, ok)) {
+        const bool col_ok = n0 + 8 * g < N;
+        float inv[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) inv[j] = s_inv[8 * g + j];
+        const int pairs = rows / 2;
+        for (int p0 = rl & ~7; p0 < pairs; p0 += QC_RL) {   // rl & ~7: the warp's first row lane
+            const int p = p0 + (rl & 7);
+            const int pc = min(p, pairs - 1);
+            const uint8_t* ra = qtile + (2 * pc) * (QC_COLS * 2) + g * 16;
+            const uint4 a = *reinterpret_cast<const uint4*>(ra);
+            const uint4 c = *reinterpret_cast<const uint4*>(ra + QC_COLS * 2);
+            const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, wb[4] = {c.x, c.y, c.z, c.w};
+            // nibble of (row, column j) goes to bit 8*(j%4) + 4*row of word j/4
+            uint32_t out[2] = {0, 0}, nearmask = 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const uint32_t ha = (j & 1) ? (wa[j / 2] & 0xFFFF0000u) : (wa[j / 2] << 16);
+                const uint32_t hb = (j & 1) ? (wb[j / 2] & 0xFFFF0000u) : (wb[j / 2] << 16);
+                const uint32_t ua = quant_u(ha, inv[j]), ub = quant_u(hb, inv[j]);
+                const int pa = 8 * (j % 4), pb = pa + 4;
+                out[j / 4] |= ((ua >> 16) & 0xFu) << pa;
+                out[j / 4] |= ((ub >> 16) & 0xFu) << pb;
+                nearmask |= (quant_near(ua) ? 1u : 0u) << (2 * j);
+                nearmask |= (quant_near(ub) ? 1u : 0u) << (2 * j + 1);
+            }
+            if (__any_sync(0xffffffffu, nearmask != 0)) {
+                while (nearmask != 0) {
+                    const int bit = __ffs(nearmask) - 1;
+                    nearmask &= nearmask - 1;
+                    const int j = bit >> 1, row = bit & 1;
+                    const uint32_t e = reinterpret_cast<const uint16_t*>(ra + row * (QC_COLS * 2))[j];
+                    const int pos = 8 * (j & 3) + 4 * row;
+                    const uint32_t nib = quant_nibble(e, s_scale[8 * g + j]) << pos;
+                    if (j < 4) out[0] = (out[0] & ~(0xFu << pos)) | nib;
+                    else out[1] = (out[1] & ~(0xFu << pos)) | nib;
+                }
+            }
+            if (col_ok && p < pairs)
+                *reinterpret_cast<uint2*>(packed + (static_cast<int64_t>(k0 / 2) + p) * N + n0 + 8 * g) =
+                    make_uint2(out[0], out[1]);
+        }
+    }
+    cluster.sync();  // peers have read pmax
+}
+
+// ---------------------------------------------------------------------------
+// quantize_pack_int4, two passes (fallback: N % 8 != 0 or K > QC_MAX_K)
 //
 // One CTA owns a strip of QP_COLS columns over all K.  Pass 1 finds each
 // column's max |W| (compared as bf16 bit patterns with the sign cleared,
@@ -25,12 +214,6 @@ constexpr int QP_THREADS = 256;
 constexpr int QP_CG = QP_COLS / 8;             // 16-byte column groups per strip
 constexpr int QP_RL = QP_THREADS / QP_CG;      // row lanes
 
-__device__ __forceinline__ uint32_t quant_nibble(uint32_t wbits, float s) {
-    float w = bf16_bits_to_f32(wbits & 0xFFFFu);
-    float r = (s == 0.0f) ? 0.0f : roundf(__fdiv_rn(w, s));
-    r = fminf(fmaxf(r, -8.0f), 7.0f);
-    return static_cast<uint32_t>(static_cast<int>(r)) & 0xFu;
-}
 
 template <bool VEC>
 __global__ void __launch_bounds__(QP_THREADS)
@@ -113,8 +296,65 @@ quantize_pack_kernel(const uint16_t* __restrict__ W, uint8_t* __restrict__ packe
     }
 }
 
+namespace {
+
+// Single-read path; W4_ERR_SHAPE means "use the two-pass kernel".
+w4_status launch_quantize_cluster(const void* W, void* packed, float* scale, int64_t K, int64_t N,
+                                  cudaStream_t stream) {
+    if ((N % 8) != 0 || K > QC_MAX_K || N > 0x7FFFFFFF) return W4_ERR_SHAPE;
+    const int64_t strips = (N + QC_COLS - 1) / QC_COLS;
+    // rows per CTA: whole TMA boxes, 1024 rows (64 KB) per CTA while the
+    // cluster has room, more rows per CTA beyond that
+    int cs = 1, R = 0, box = 0;
+    const int64_t Keven = (K + 1) / 2 * 2;
+    if (Keven <= QC_BOXR) {
+        R = static_cast<int>(Keven);
+        box = R;
+    } else {
+        const int64_t boxes = (K + QC_BOXR - 1) / QC_BOXR;
+        cs = static_cast<int>(std::min<int64_t>(QC_CS, (boxes + 3) / 4));
+        const int64_t bpc = (boxes + cs - 1) / cs;
+        R = static_cast<int>(bpc * QC_BOXR);
+        box = QC_BOXR;
+    }
+    if (R * QC_COLS * 2 > QC_SMEM || strips * cs > 0x7FFFFFFF) return W4_ERR_SHAPE;
+    auto encode = tensor_map_encoder();
+    if (!encode) return W4_ERR_CUDA;
+    CUtensorMap tmap;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(K)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(N) * 2};
+    cuuint32_t boxd[2] = {QC_COLS, static_cast<cuuint32_t>(box)};
+    cuuint32_t estr[2] = {1, 1};
+    if (encode(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(W), dims, strides, boxd, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return W4_ERR_CUDA;
+    const int smem = R * QC_COLS * 2;
+    static int smem_set[64];
+    if (ensure_smem_limit(quantize_pack_cluster_kernel, smem, smem_set) != cudaSuccess) return W4_ERR_CUDA;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(strips * cs), 1, 1);
+    cfg.blockDim = dim3(QC_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cs;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return launch_status(cudaLaunchKernelEx(&cfg, quantize_pack_cluster_kernel, tmap,
+                                            static_cast<uint8_t*>(packed), scale, static_cast<int>(K),
+                                            static_cast<int>(N), R, box));
+}
+
+}  // namespace
+
 w4_status run_quantize_pack(const void* W, void* packed, float* scale, int64_t K, int64_t N,
                             cudaStream_t stream) {
+    const w4_status st = launch_quantize_cluster(W, packed, scale, K, N, stream);
+    if (st != W4_ERR_SHAPE) return st;
     const int64_t strips = (N + QP_COLS - 1) / QP_COLS;
     if (strips > 0x7FFFFFFF) return W4_ERR_SHAPE;
     const bool vec = (N % 8) == 0;
@@ -217,5 +457,7 @@ w4_status run_permute(const void* packed, void* out, int64_t K, int64_t N, cudaS
                                                                static_cast<uint8_t*>(out), K, N);
     return launch_status(cudaGetLastError());
 }
+
+int take_device_error_quant() { return take_unit_device_error(); }
 
 }  // namespace w4

@@ -16,6 +16,7 @@ w4_status run_gemm(const void* A, const void* B, const void* scale, const void* 
                    int64_t N, int64_t K, cudaStream_t s);
 int take_device_error_gemm();
 int take_device_error_gemv();
+int take_device_error_quant();
 
 namespace {
 constexpr int kMaxDevices = 64;
@@ -47,6 +48,20 @@ bool device_is_sm103() {
     return g_is_sm103[dev] == 1;
 }
 
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
 }  // namespace w4
 
 using namespace w4;
@@ -59,8 +74,9 @@ int w4_device_error(void* stream) {
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return -1;
     const int a = take_device_error_gemm();
     const int b = take_device_error_gemv();
-    if (a < 0 || b < 0) return -1;
-    return a != 0 ? a : b;
+    const int c = take_device_error_quant();
+    if (a < 0 || b < 0 || c < 0) return -1;
+    return a != 0 ? a : b != 0 ? b : c;
 }
 
 const char* w4_status_string(w4_status status) {

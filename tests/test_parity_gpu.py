@@ -47,7 +47,14 @@ def _guards_intact(buf, pad, n_elems, fill):
 # quantize_pack_int4 + permute_int4 (bit-exact)
 # ---------------------------------------------------------------------------
 
-@pytest.mark.parametrize("K,N", [(2, 8), (128, 64), (130, 37), (64, 1), (1024, 1000), (8192, 8192)])
+@pytest.mark.parametrize("K,N", [
+    (2, 8), (128, 64), (130, 37), (64, 1), (1024, 1000), (8192, 8192),
+    (1000, 64),      # rows per CTA not a whole number of TMA boxes
+    (4098, 8),       # five CTAs per cluster, the last holding two rows
+    (20000, 40),     # eight CTAs of 2560 rows; a strip past the last column
+    (26624, 16),     # longest K of the single-read kernel
+    (26626, 16),     # first K of the two-pass kernel
+])
 def test_quantize_pack_bit_exact(w4, K, N):
     W = synth.quant_inputs(K, N, seed=K + N)
     if N > 3:
