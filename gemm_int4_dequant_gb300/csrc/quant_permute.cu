@@ -371,16 +371,21 @@ w4_status run_quantize_pack(const void* W, void* packed, float* scale, int64_t K
 // ---------------------------------------------------------------------------
 // permute_int4
 //
-// Tile = one 32-byte chunk j of the k-byte stream (rows 32j..32j+31 of the
-// packed matrix) x PM_COLS columns.  The tile is staged in shared memory;
-// each thread then owns one column's 32-byte chunk, applies the byte permute
-// and nibble swap to its two 16-byte groups in registers and writes the
-// chunk to its interleaved position, so a warp writes 8 runs of 128
-// contiguous bytes.  Algorithmic bytes: 1 B read + 1 B written per byte.
+// A thread owns four adjacent columns (one group of the interleave) over one
+// 32-byte chunk of the k-byte stream (rows 32j..32j+31 of the packed matrix):
+// it loads the 32 rows x 4 bytes, transposes 4x4 byte blocks in registers so
+// that each column's bytes are contiguous, applies the byte permute and
+// nibble swap to each 16-byte group and writes the group's four 32-byte
+// chunks, which are adjacent in the output (128 contiguous bytes).  A warp
+// covers 8 groups x 4 chunks, so each row load is 4 whole 32-byte sectors,
+// and a CTA (8 warps) covers 32 consecutive chunks of 8 groups, so each
+// output run receives 4 KB of contiguous writes.  No shared memory.
+// Algorithmic bytes: 1 B read + 1 B written per byte.
 // ---------------------------------------------------------------------------
 
-constexpr int PM_COLS = 128;
-constexpr int PM_THREADS = PM_COLS;
+constexpr int PM_THREADS = 256;   // 8 warps x (8 groups x 4 chunks)
+constexpr int PM_GROUPS = 8;      // column groups per CTA
+constexpr int PM_CHUNKS = 32;     // 32-byte chunks per CTA
 
 // One 16-byte group, words w[0..3] = bytes 0-3, 4-7, 8-11, 12-15.
 // Byte permute: output word i holds bytes (i, 8+i, 4+i, 12+i), i.e. the
@@ -405,56 +410,151 @@ __device__ __forceinline__ void permute_group16(const uint32_t (&w)[4], uint32_t
     }
 }
 
-template <bool VEC>
+// 4x4 byte transpose: r[i] holds bytes (row i, columns 0..3); c[j] gets
+// (column j, rows 0..3).
+__device__ __forceinline__ void transpose4x4(const uint32_t (&r)[4], uint32_t (&c)[4]) {
+    const uint32_t t01 = __byte_perm(r[0], r[1], 0x5140);  // r0b0 r1b0 r0b1 r1b1
+    const uint32_t t23 = __byte_perm(r[2], r[3], 0x5140);
+    const uint32_t u01 = __byte_perm(r[0], r[1], 0x7362);  // r0b2 r1b2 r0b3 r1b3
+    const uint32_t u23 = __byte_perm(r[2], r[3], 0x7362);
+    c[0] = __byte_perm(t01, t23, 0x5410);
+    c[1] = __byte_perm(t01, t23, 0x7632);
+    c[2] = __byte_perm(u01, u23, 0x5410);
+    c[3] = __byte_perm(u01, u23, 0x7632);
+}
+
+// grid = (ceil(N/4 / PM_GROUPS), ceil(K/64 / PM_CHUNKS)); lane = group (lane % 8)
+// of chunk 4*warp + lane / 8.
 __global__ void __launch_bounds__(PM_THREADS)
 permute_kernel(const uint8_t* __restrict__ packed, uint8_t* __restrict__ out, int64_t K, int64_t N) {
-    __shared__ __align__(16) uint8_t tile[32][PM_COLS + 4];
-    const int64_t total_k = K / 2;
-    const int64_t chunk = blockIdx.x;                          // 32-byte chunk of the k stream
-    const int64_t n_base = static_cast<int64_t>(blockIdx.y) * PM_COLS;
-    const int64_t rem = N - n_base;
-    const int ncols = rem < PM_COLS ? static_cast<int>(rem) : PM_COLS;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t grp = static_cast<int64_t>(blockIdx.x) * PM_GROUPS + (lane & 7);          // columns 4grp..+3
+    const int64_t chunk = static_cast<int64_t>(blockIdx.y) * PM_CHUNKS + 4 * warp + (lane >> 3);
+    if (grp >= N / 4 || chunk >= K / 64) return;
+    const uint8_t* src = packed + chunk * 32 * N + 4 * grp;
+    uint32_t rw[32];
+#pragma unroll
+    for (int r = 0; r < 32; ++r) rw[r] = ldg_stream_u32(src + r * N);
+    // col[c][i] = bytes of column c, rows 4i..4i+3
+    uint32_t col[4][8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint32_t rr[4] = {rw[4 * i], rw[4 * i + 1], rw[4 * i + 2], rw[4 * i + 3]};
+        uint32_t cc[4];
+        transpose4x4(rr, cc);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) col[c][i] = cc[c];
+    }
+    uint4* dst = reinterpret_cast<uint4*>(out + (K / 2) * 4 * grp + 128 * chunk);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const uint32_t w[4] = {col[c][4 * h], col[c][4 * h + 1], col[c][4 * h + 2], col[c][4 * h + 3]};
+            uint32_t o[4];
+            permute_group16(w, o);
+            dst[2 * c + h] = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+    }
+}
 
-    // stage 32 rows x ncols bytes (ncols is a multiple of 4)
-    for (int i = threadIdx.x; i < 32 * (PM_COLS / 4); i += PM_THREADS) {
-        int r = i / (PM_COLS / 4), c4 = (i % (PM_COLS / 4)) * 4;
-        if (c4 < ncols) {
-            const uint8_t* src = packed + (chunk * 32 + r) * N + n_base + c4;
-            uint32_t v = VEC ? *reinterpret_cast<const uint32_t*>(src)
-                             : (uint32_t)src[0] | ((uint32_t)src[1] << 8) | ((uint32_t)src[2] << 16) |
-                                   ((uint32_t)src[3] << 24);
-            *reinterpret_cast<uint32_t*>(&tile[r][c4]) = v;
+// The same tile (8 groups x 32 chunks) with its 32 KB of input brought in by
+// four 2-D TMA boxes (32 columns x 256 rows) instead of 32 four-byte loads
+// per thread (which kept the load/store unit's queue full), and its 32 KB of
+// output staged in shared memory so that every warp store writes 512
+// contiguous bytes (whole 128-byte lines) instead of sixteen bytes into each
+// of 32 lines.  The 16-byte pieces of a group's 128-byte unit are stored at
+// position piece ^ group, which keeps both the per-thread writes and the
+// per-warp reads of the staging buffer free of bank conflicts.  Requires
+// N % 16 == 0 (16-byte row stride of the tensor map).
+constexpr int PM_SMEM = PM_CHUNKS * 32 * PM_GROUPS * 4 * 2 + 16;   // in + out + barrier
+
+__global__ void __launch_bounds__(PM_THREADS)
+permute_tma_kernel(const __grid_constant__ CUtensorMap tmap, uint8_t* __restrict__ out, int64_t K, int64_t N) {
+    extern __shared__ __align__(128) uint8_t pm_smem[];
+    uint8_t (*tile)[PM_GROUPS * 4] = reinterpret_cast<uint8_t (*)[PM_GROUPS * 4]>(pm_smem);   // [1024][32]
+    uint4* staged = reinterpret_cast<uint4*>(pm_smem + PM_CHUNKS * 32 * PM_GROUPS * 4);       // [8][32][8]
+    uint64_t* bar_p = reinterpret_cast<uint64_t*>(pm_smem + 2 * PM_CHUNKS * 32 * PM_GROUPS * 4);
+    __shared__ int abort_word;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int gl = lane & 7, cl = 4 * warp + (lane >> 3);                   // local group, local chunk
+    const int64_t g0 = static_cast<int64_t>(blockIdx.x) * PM_GROUPS;
+    const int64_t c0 = static_cast<int64_t>(blockIdx.y) * PM_CHUNKS;
+    const uint32_t b = ptx::smem_u32(bar_p);
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(b, 1);
+        abort_word = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    constexpr int BOX_ROWS = 256, NBOX = PM_CHUNKS * 32 / BOX_ROWS;
+    if (threadIdx.x == 0) {
+        ptx::mbar_arrive_expect_tx(b, PM_CHUNKS * 32 * PM_GROUPS * 4);
+        for (int i = 0; i < NBOX; ++i)
+            ptx::tma_load_2d(ptx::smem_u32(&tile[i * BOX_ROWS][0]), &tmap, blockIdx.x * PM_GROUPS * 4,
+                             blockIdx.y * PM_CHUNKS * 32 + i * BOX_ROWS, b);
+    }
+    const bool ok = ptx::mbar_wait(b, 0, &abort_word);
+    if (!__syncthreads_and(ok)) {
+        if (threadIdx.x == 0) ptx::mbar_drain(b, 0);
+        return;
+    }
+    // this thread's unit: group gl, chunk cl -> 8 pieces of 16 bytes
+    uint32_t col[4][8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        uint32_t rr[4], cc[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) rr[k] = *reinterpret_cast<const uint32_t*>(&tile[32 * cl + 4 * i + k][4 * gl]);
+        transpose4x4(rr, cc);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) col[c][i] = cc[c];
+    }
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const uint32_t w[4] = {col[c][4 * h], col[c][4 * h + 1], col[c][4 * h + 2], col[c][4 * h + 3]};
+            uint32_t o[4];
+            permute_group16(w, o);
+            staged[(gl * PM_CHUNKS + cl) * 8 + ((2 * c + h) ^ gl)] = make_uint4(o[0], o[1], o[2], o[3]);
         }
     }
     __syncthreads();
-    const int c = threadIdx.x;
-    if (c >= ncols) return;
-    const int64_t n = n_base + c;
-    uint8_t* dst = out + total_k * 4 * (n / 4) + 128 * chunk + 32 * (n % 4);
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        uint32_t w[4], o[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-            w[i] = (uint32_t)tile[16 * h + 4 * i][c] | ((uint32_t)tile[16 * h + 4 * i + 1][c] << 8) |
-                   ((uint32_t)tile[16 * h + 4 * i + 2][c] << 16) | ((uint32_t)tile[16 * h + 4 * i + 3][c] << 24);
-        permute_group16(w, o);
-        *reinterpret_cast<uint4*>(dst + 16 * h) = make_uint4(o[0], o[1], o[2], o[3]);
+    // a warp writes 4 chunks x 8 pieces of one group: 512 contiguous bytes
+    const int64_t ngroups = N / 4, nchunks = K / 64;
+    for (int e = threadIdx.x; e < PM_GROUPS * PM_CHUNKS * 8; e += PM_THREADS) {
+        const int g = e / (PM_CHUNKS * 8), rest = e % (PM_CHUNKS * 8), c = rest >> 3, p = rest & 7;
+        if (g0 + g < ngroups && c0 + c < nchunks)
+            *reinterpret_cast<uint4*>(out + (K / 2) * 4 * (g0 + g) + 128 * (c0 + c) + 16 * p) =
+                staged[(g * PM_CHUNKS + c) * 8 + (p ^ g)];
     }
 }
 
 w4_status run_permute(const void* packed, void* out, int64_t K, int64_t N, cudaStream_t stream) {
-    const int64_t chunks = (K / 2) / 32;
-    const int64_t col_tiles = (N + PM_COLS - 1) / PM_COLS;
-    if (chunks > 0x7FFFFFFF || col_tiles > 65535) return W4_ERR_SHAPE;
-    dim3 grid(static_cast<unsigned>(chunks), static_cast<unsigned>(col_tiles));
-    const bool vec = (N % 4) == 0;  // always true given the shape rules; rows are 4-byte aligned
-    if (vec)
-        permute_kernel<true><<<grid, PM_THREADS, 0, stream>>>(static_cast<const uint8_t*>(packed),
-                                                              static_cast<uint8_t*>(out), K, N);
-    else
-        permute_kernel<false><<<grid, PM_THREADS, 0, stream>>>(static_cast<const uint8_t*>(packed),
-                                                               static_cast<uint8_t*>(out), K, N);
+    const int64_t cblocks = ((K / 2) / 32 + PM_CHUNKS - 1) / PM_CHUNKS;
+    const int64_t gblocks = (N / 4 + PM_GROUPS - 1) / PM_GROUPS;
+    if (cblocks > 65535 || gblocks > 0x7FFFFFFF) return W4_ERR_SHAPE;
+    dim3 grid(static_cast<unsigned>(gblocks), static_cast<unsigned>(cblocks));
+    if ((N % 16) == 0) {
+        auto encode = tensor_map_encoder();
+        if (!encode) return W4_ERR_CUDA;
+        CUtensorMap tmap;
+        cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(K / 2)};
+        cuuint64_t strides[1] = {static_cast<cuuint64_t>(N)};
+        cuuint32_t boxd[2] = {PM_GROUPS * 4, 256};
+        cuuint32_t estr[2] = {1, 1};
+        if (encode(&tmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(packed), dims, strides, boxd, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return W4_ERR_CUDA;
+        static int smem_set[64];
+        if (ensure_smem_limit(permute_tma_kernel, PM_SMEM, smem_set) != cudaSuccess) return W4_ERR_CUDA;
+        permute_tma_kernel<<<grid, PM_THREADS, PM_SMEM, stream>>>(tmap, static_cast<uint8_t*>(out), K, N);
+        return launch_status(cudaGetLastError());
+    }
+    permute_kernel<<<grid, PM_THREADS, 0, stream>>>(static_cast<const uint8_t*>(packed), static_cast<uint8_t*>(out),
+                                                    K, N);
     return launch_status(cudaGetLastError());
 }
 

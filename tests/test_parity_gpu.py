@@ -73,7 +73,12 @@ def test_quantize_pack_k_zero(w4):
     assert torch.all(scale == 0)
 
 
-@pytest.mark.parametrize("K,N", [(64, 4), (128, 132), (1024, 4096), (8192, 8192)])
+@pytest.mark.parametrize("K,N", [
+    (64, 4), (128, 132), (1024, 4096), (8192, 8192),
+    (64, 16),        # one chunk, two column groups: TMA tile mostly outside the matrix
+    (192, 48),       # partial tile in both directions
+    (4160, 1040),    # 65 chunks and 260 groups: ragged last tiles
+])
 def test_permute_bit_exact(w4, K, N):
     g = torch.Generator().manual_seed(K * 7 + N)
     packed = torch.randint(0, 256, (K // 2, N), dtype=torch.uint8, generator=g)
