@@ -7,28 +7,30 @@
 // packed (K/2, N) int8 with the low nibble for even k; one packed k-tile of B
 // feeds an A k-tile twice as long.)
 //
-// CTA = one 128 x 256 output tile, 6 warps:
+// A thread-block cluster of two CTAs (a CTA pair on two SMs) computes one
+// 256 x 256 output tile with tcgen05.mma.cta_group::2 (M256 N256 K16): CTA r
+// holds A rows [128r, 128r+128) and B columns [128r, 128r+128) of the tile
+// in its shared memory, and the pair's MMA reads both halves, so each SM
+// loads, dequantises and serves only half of B per FLOP.  Per CTA, 10 warps:
 //   warp 0      TMA producer: A tile [128 x 64] bf16 (128B-swizzled, K-major)
-//               and the packed B tile [32 x 256] bytes, one mbarrier per stage;
-//   warp 1      TMEM allocator and MMA issuer (one thread): 4 x
-//               tcgen05.mma.cta_group::1.kind::f16 (M128 N256 K16) per k-tile,
-//               fp32 accumulator in TMEM, tcgen05.commit frees the stage;
+//               and its packed B half [32 x 128] bytes, one mbarrier per stage;
+//   warp 1      TMEM allocator (both CTAs) and, in the even CTA, the MMA
+//               issuer (one thread): 4 MMAs per k-tile into an fp32
+//               accumulator in TMEM; the commit frees the stage in both CTAs;
 //   warps 2..9  dequant: packed bytes -> (u - zero) bf16, written straight into
-//               the canonical 128B-swizzled MN-major operand layout, then the
-//               epilogue: tcgen05.ld of the accumulator, * scale, -> bf16.
-// Inside every group of four columns the shared-memory (and so TMEM) column
-// order is n0 n2 n1 n3: one mask of a packed 32-bit word then yields the
-// nibbles of bytes 0 and 2 (or 1 and 3) as a bf16 pair, so unpacking eight
-// weights costs three shifts and four three-input logic ops.  The epilogue
-// puts the columns back in order.
-// Every wait is bounded; on timeout the kernel records an error code in a
-// device word (w4_device_error), stops issuing work, drains and frees TMEM.
-
+//               the canonical 128B-swizzled MN-major operand layout; a warp
+//               then tells the even CTA's barrier (remotely from the odd CTA)
+//               that its part of the stage is ready; afterwards the epilogue:
+//               tcgen05.ld of this CTA's 128 accumulator rows, * scale, -> bf16.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <cooperative_groups.h>
+
 #include "common.cuh"
 #include "ptx.cuh"
+
+namespace cg = cooperative_groups;
 
 namespace w4 {
 
@@ -36,33 +38,36 @@ namespace gemm {
 
 using namespace ptx;
 
-constexpr int BM = 128, BN = 256, BK = 64;
-constexpr int STAGES = 4;
+constexpr int BM = 128;                      // A rows per CTA (the pair covers 256)
+constexpr int BN = 256;                      // tile columns (the pair's MMA N)
+constexpr int BNH = BN / 2;                  // B columns held by each CTA
+constexpr int BK = 64;
+constexpr int STAGES = 6;
 constexpr int THREADS = 320;
 constexpr int A_BYTES = BM * BK * 2;         // 16 KB
-constexpr int BP_BYTES = (BK / 2) * BN;      // 8 KB packed
-constexpr int BD_BYTES = BK * BN * 2;        // 32 KB dequantised
+constexpr int BP_BYTES = (BK / 2) * BNH;     // 4 KB packed
+constexpr int BD_BYTES = BK * BNH * 2;       // 16 KB dequantised
 constexpr int OFF_A = 0;
 constexpr int OFF_BD = OFF_A + STAGES * A_BYTES;
 constexpr int OFF_BP = OFF_BD + STAGES * BD_BYTES;
 constexpr int OFF_BAR = OFF_BP + STAGES * BP_BYTES;
-constexpr int NUM_BARS = 3 * STAGES + 1;
+constexpr int NUM_BARS = 4 * STAGES + 1;
 constexpr int OFF_TMEM_SLOT = OFF_BAR + NUM_BARS * 8;
 constexpr int OFF_ABORT = OFF_TMEM_SLOT + 4;
 constexpr int SMEM_USED = OFF_ABORT + 4;
 constexpr int SMEM_BYTES = SMEM_USED + 1024;  // slack to align the base to 1 KB
 constexpr uint32_t TMEM_COLS = 256;
-constexpr int DEQ_THREADS = 256;
-
+constexpr int DEQ_WARPS = 8;
+constexpr int DEQ_THREADS = DEQ_WARPS * 32;
 
 // Instruction descriptor, kind::f16: D fp32, A bf16 K-major, B bf16 MN-major,
-// N = 256, M = 128.
+// N = 256, M = 256 (CTA pair).
 constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (0u << 15) | (1u << 16) |
-                            (static_cast<uint32_t>(BN >> 3) << 17) | (static_cast<uint32_t>(BM >> 4) << 24);
+                            (static_cast<uint32_t>(BN >> 3) << 17) | (static_cast<uint32_t>((2 * BM) >> 4) << 24);
 
-// Byte offset of element (k, n) of the dequantised B tile: atoms of 8 k-rows
-// x 64 n (1 KB, 16-byte chunks XOR-swizzled by k % 8), atom (n/64, k/8) at
-// ((n/64) * (BK/8) + k/8) KB.  n is a multiple of 8 (one 16-byte chunk).
+// Byte offset of element (k, n) of this CTA's dequantised B half: atoms of 8
+// k-rows x 64 n (1 KB, 16-byte chunks XOR-swizzled by k % 8), atom (n/64,
+// k/8) at ((n/64) * (BK/8) + k/8) KB.  n is a multiple of 8 (one 16-byte chunk).
 __device__ __forceinline__ uint32_t bd_offset(int k, int n) {
     const int atom = (n >> 6) * (BK / 8) + (k >> 3);
     const int r = k & 7, chunk = (n & 63) >> 3;
@@ -96,29 +101,35 @@ gemm_w4_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
     uint8_t* sbase = smem_raw + (base - raw);
     const uint32_t bar0 = base + OFF_BAR;
     auto full_tma = [&](int s) { return bar0 + 8u * s; };
-    auto full_deq = [&](int s) { return bar0 + 8u * (STAGES + s); };
+    auto full_deq = [&](int s) { return bar0 + 8u * (STAGES + s); };   // this CTA's dequant warps
     auto empty = [&](int s) { return bar0 + 8u * (2 * STAGES + s); };
-    const uint32_t tmem_full = bar0 + 8u * (3 * STAGES);
+    auto peer_deq = [&](int s) { return bar0 + 8u * (3 * STAGES + s); };  // even CTA: the odd CTA's stage is ready
+    const uint32_t tmem_full = bar0 + 8u * (4 * STAGES);
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(sbase + OFF_TMEM_SLOT);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sbase + OFF_ABORT);
 
+    cg::cluster_group cluster = cg::this_cluster();
+    const int rank = static_cast<int>(cluster.block_rank());     // 0: issues the pair's MMAs
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
+    const int n0 = (blockIdx.x >> 1) * BN, m0 = blockIdx.y * (2 * BM);
+    const int mr = m0 + rank * BM;          // this CTA's first A row / accumulator row
+    const int nh = n0 + rank * BNH;         // this CTA's first B column
     const int num_kt = K / BK;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full_tma(s), 1);
-            mbar_init(full_deq(s), DEQ_THREADS);
+            mbar_init(full_deq(s), DEQ_WARPS);
             mbar_init(empty(s), 1);
+            mbar_init(peer_deq(s), 1);
         }
         mbar_init(tmem_full, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (warp == 1) tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), TMEM_COLS);
+    if (warp == 1) tmem_alloc_pair(smem_u32(const_cast<uint32_t*>(tmem_slot)), TMEM_COLS);
     tc_fence_before();
-    __syncthreads();
+    cluster.sync();   // both CTAs' barriers initialised, TMEM allocated
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
@@ -127,26 +138,48 @@ gemm_w4_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
         if (lane == 0) {
             asm volatile("prefetch.tensormap [%0];" ::"l"(&tmap_a) : "memory");
             asm volatile("prefetch.tensormap [%0];" ::"l"(&tmap_b) : "memory");
+            // an A or B half lying wholly outside the matrix (ragged M or N)
+            // is not copied: its rows / columns of the tile are never stored
+            const bool load_a = mr < M, load_b = nh < N;
+            const uint32_t bytes = (load_a ? A_BYTES : 0) + (load_b ? BP_BYTES : 0);
             int issued = 0;
             for (int kt = 0; kt < num_kt; ++kt) {
                 const int s = kt % STAGES, round = kt / STAGES;
-                if (round > 0 && !mbar_wait(empty(s), (round - 1) & 1, abort_flag)) break;
-                mbar_arrive_expect_tx(full_tma(s), A_BYTES + BP_BYTES);
-                tma_load_2d(base + OFF_A + s * A_BYTES, &tmap_a, kt * BK, m0, full_tma(s));
-                tma_load_2d(base + OFF_BP + s * BP_BYTES, &tmap_b, n0, kt * (BK / 2), full_tma(s));
+                if (round > 0 && !mbar_wait_fast(empty(s), (round - 1) & 1, abort_flag)) break;
+                mbar_arrive_expect_tx(full_tma(s), bytes);
+                if (load_a) tma_load_2d(base + OFF_A + s * A_BYTES, &tmap_a, kt * BK, mr, full_tma(s));
+                if (load_b) tma_load_2d(base + OFF_BP + s * BP_BYTES, &tmap_b, nh, kt * (BK / 2), full_tma(s));
                 issued = kt + 1;
             }
             // the last copies may still be landing if a consumer aborted
             for (int kt = max(0, issued - STAGES); kt < issued; ++kt)
                 mbar_drain(full_tma(kt % STAGES), (kt / STAGES) & 1);
         }
+    } else if (warp == 1 && rank == 1) {
+        // ---------------- odd CTA: forward "stage ready" to the even CTA ----------------
+        // A cluster-scope release costs far more than one stage's MMAs, so
+        // the stages that became ready meanwhile share one fence: wait for
+        // stage kt, take every later stage already complete, then one
+        // fence.acq_rel.cluster and a relaxed remote arrive per stage.
+        if (lane == 0) {
+            const uint32_t remote0 = map_cluster(peer_deq(0), 0);
+            int kt = 0;
+            while (kt < num_kt) {
+                if (!mbar_wait_fast(full_deq(kt % STAGES), (kt / STAGES) & 1, abort_flag)) break;
+                int end = kt + 1;
+                while (end < num_kt && mbar_try_wait(full_deq(end % STAGES), (end / STAGES) & 1)) ++end;
+                fence_acq_rel_cluster();
+                for (; kt < end; ++kt) mbar_arrive_cluster_relaxed(remote0 + 8u * (kt % STAGES));
+            }
+        }
     } else if (warp == 1) {
-        // ---------------- MMA issuer ----------------
+        // ---------------- MMA issuer (even CTA) ----------------
         if (lane == 0) {
             bool ok = true;
             for (int kt = 0; kt < num_kt && ok; ++kt) {
                 const int s = kt % STAGES, round = kt / STAGES;
-                ok = mbar_wait(full_tma(s), round & 1, abort_flag) && mbar_wait(full_deq(s), round & 1, abort_flag);
+                ok = mbar_wait_fast(full_deq(s), round & 1, abort_flag) &&
+                     mbar_wait_cluster(peer_deq(s), round & 1, abort_flag);
                 if (!ok) break;
                 tc_fence_after();
                 const uint32_t a_addr = base + OFF_A + s * A_BYTES;
@@ -158,18 +191,17 @@ gemm_w4_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
                     // B: MN-major SW128, k-groups of 8 rows 1 KB apart (SBO),
                     // 64-column atoms (BK/8) KB apart (LBO).
                     const uint64_t bdesc = sw128_desc(b_addr + kk * 2 * 1024, (BK / 8) * 1024, 1024);
-                    umma_bf16(tmem_base, adesc, bdesc, kIdesc, (kt > 0 || kk > 0) ? 1u : 0u);
+                    umma_bf16_pair(tmem_base, adesc, bdesc, kIdesc, (kt > 0 || kk > 0) ? 1u : 0u);
                 }
-                umma_commit(empty(s));
+                umma_commit_pair(empty(s), 0x3);
             }
-            umma_commit(tmem_full);
-            mbar_drain(tmem_full, 0);  // all MMAs done before TMEM can be freed
+            umma_commit_pair(tmem_full, 0x3);
         }
     } else {
         // ---------------- dequant (warps 2..9) ----------------
         const int t = threadIdx.x - 64;          // 0..255
-        const int nl = (t & 31) * 8;             // 8 columns per thread
-        const int kp_lane = t >> 5;              // 0..7
+        const int nl = (t & 15) * 8;             // 8 of this CTA's 128 columns
+        const int kp_lane = t >> 4;              // 0..15
         // zero-point pairs in shared-memory column order: (z0,z2) (z1,z3) (z4,z6) (z5,z7).
         // Fast path: 128 + z exact in bf16 (integer zero points) -> one subtract.
         uint32_t zz[4], zraw[4];
@@ -178,7 +210,7 @@ gemm_w4_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
             float zf[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-                const int n = n0 + nl + j;
+                const int n = nh + nl + j;
                 zf[j] = n < N ? __bfloat162float(zero[n]) : 0.f;
             }
             const int pa[4] = {0, 1, 4, 5}, pb[4] = {2, 3, 6, 7};
@@ -196,14 +228,14 @@ gemm_w4_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
         bool ok = true;
         for (int kt = 0; kt < num_kt && ok; ++kt) {
             const int s = kt % STAGES, round = kt / STAGES;
-            if (round > 0 && !mbar_wait(empty(s), (round - 1) & 1, abort_flag)) { ok = false; break; }
-            if (!mbar_wait(full_tma(s), round & 1, abort_flag)) { ok = false; break; }
+            if (round > 0 && !mbar_wait_fast(empty(s), (round - 1) & 1, abort_flag)) { ok = false; break; }
+            if (!mbar_wait_fast(full_tma(s), round & 1, abort_flag)) { ok = false; break; }
             const uint8_t* bp = sbase + OFF_BP + s * BP_BYTES;
             uint8_t* bd = sbase + OFF_BD + s * BD_BYTES;
 #pragma unroll
-            for (int i = 0; i < (BK / 2) / 8; ++i) {
-                const int kp = kp_lane + 8 * i;
-                const uint2 v = *reinterpret_cast<const uint2*>(bp + kp * BN + nl);
+            for (int i = 0; i < (BK / 2) / 16; ++i) {
+                const int kp = kp_lane + 16 * i;
+                const uint2 v = *reinterpret_cast<const uint2*>(bp + kp * BNH + nl);
                 uint32_t e[4], o[4];
                 unpack_word(v.x, e[0], e[1], o[0], o[1]);
                 unpack_word(v.y, e[2], e[3], o[2], o[3]);
@@ -221,17 +253,18 @@ gemm_w4_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
                 *reinterpret_cast<uint4*>(bd + bd_offset(2 * kp + 1, nl)) = make_uint4(o[0], o[1], o[2], o[3]);
             }
             fence_proxy_async_smem();
-            mbar_arrive(full_deq(s));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(full_deq(s));
         }
 
         // ---------------- epilogue ----------------
         // warps 2..9: TMEM lane quarter (warp % 4), column half ((warp-2) / 4);
         // the decision is warp-uniform (tcgen05.ld is warp-collective)
-        if (__all_sync(0xffffffffu, ok && mbar_wait(tmem_full, 0, abort_flag))) {
+        if (__all_sync(0xffffffffu, ok && mbar_wait_fast(tmem_full, 0, abort_flag))) {
             tc_fence_after();
             const int quarter = warp & 3;           // TMEM lanes 32*quarter .. +31
             const int half = (warp - 2) >> 2;
-            const int m = m0 + quarter * 32 + lane;
+            const int m = mr + quarter * 32 + lane;
             for (int cb = half * (BN / 64); cb < (half + 1) * (BN / 64); ++cb) {
                 uint32_t r[32];
                 tmem_ld32(tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + cb * 32, r);
@@ -270,11 +303,14 @@ gemm_w4_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
         }
     }
 
+    // every MMA of the pair is complete (both CTAs waited on tmem_full, or
+    // timed out) before either CTA frees its TMEM
+    if (warp == 1 && rank == 0 && lane == 0) mbar_drain(tmem_full, 0);
     tc_fence_before();
-    __syncthreads();
+    cluster.sync();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, TMEM_COLS);
+        tmem_dealloc_pair(tmem_base, TMEM_COLS);
     }
 }
 
@@ -284,8 +320,8 @@ w4_status run_gemm(const void* A, const void* B, const void* scale, const void* 
                    int64_t N, int64_t K, cudaStream_t stream) {
     using namespace gemm;
     if (M > 0x7FFFFFFF || N > 0x7FFFFFFF || K > 0x7FFFFFFF) return W4_ERR_SHAPE;
-    const int64_t tiles_m = (M + BM - 1) / BM, tiles_n = (N + BN - 1) / BN;
-    if (tiles_m > 65535 || tiles_n > 0x7FFFFFFF) return W4_ERR_SHAPE;
+    const int64_t tiles_m = (M + 2 * BM - 1) / (2 * BM), tiles_n = (N + BN - 1) / BN;
+    if (tiles_m > 65535 || 2 * tiles_n > 0x7FFFFFFF) return W4_ERR_SHAPE;
     auto encode = tensor_map_encoder();
     if (!encode) return W4_ERR_CUDA;
 
@@ -303,7 +339,7 @@ w4_status run_gemm(const void* A, const void* B, const void* scale, const void* 
     {
         cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(K / 2)};
         cuuint64_t strides[1] = {static_cast<cuuint64_t>(N)};
-        cuuint32_t box[2] = {BN, BK / 2};
+        cuuint32_t box[2] = {BNH, BK / 2};
         cuuint32_t estr[2] = {1, 1};
         if (encode(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(B), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -313,11 +349,21 @@ w4_status run_gemm(const void* A, const void* B, const void* scale, const void* 
     static int smem_set[64];
     cudaError_t e = ensure_smem_limit(gemm_w4_tc_kernel, SMEM_BYTES, smem_set);
     if (e != cudaSuccess) return W4_ERR_CUDA;
-    dim3 grid(static_cast<unsigned>(tiles_n), static_cast<unsigned>(tiles_m));
-    gemm_w4_tc_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(
-        ta, tb, static_cast<const __nv_bfloat16*>(scale), static_cast<const __nv_bfloat16*>(zero),
-        static_cast<__nv_bfloat16*>(C), static_cast<int>(M), static_cast<int>(N), static_cast<int>(K));
-    return launch_status(cudaGetLastError());
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * tiles_n), static_cast<unsigned>(tiles_m), 1);
+    cfg.blockDim = dim3(THREADS, 1, 1);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return launch_status(cudaLaunchKernelEx(&cfg, gemm_w4_tc_kernel, ta, tb, static_cast<const __nv_bfloat16*>(scale),
+                                            static_cast<const __nv_bfloat16*>(zero), static_cast<__nv_bfloat16*>(C),
+                                            static_cast<int>(M), static_cast<int>(N), static_cast<int>(K)));
 }
 
 int take_device_error_gemm() { return take_unit_device_error(); }

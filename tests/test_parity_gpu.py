@@ -202,6 +202,8 @@ def _check_gemm_full(w4, M, N, K, seed=0, **kw):
     (1, 16, 64),        # degenerate
     (300, 1008, 1024),
     (129, 528, 512),
+    (257, 256, 128),    # second 256-row tile holds one row; its odd CTA has no rows
+    (384, 784, 192),    # ragged M tile pair and a last column tile of 16 columns
 ])
 def test_gemm_small(w4, M, N, K):
     _check_gemm_full(w4, M, N, K, seed=M + N + K)
