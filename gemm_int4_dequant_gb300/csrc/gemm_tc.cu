@@ -157,10 +157,10 @@ gemm_w4_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
         }
     } else if (warp == 1 && rank == 1) {
         // ---------------- odd CTA: forward "stage ready" to the even CTA ----------------
-        // A cluster-scope release costs far more than one stage's MMAs, so
-        // the stages that became ready meanwhile share one fence: wait for
-        // stage kt, take every later stage already complete, then one
-        // fence.acq_rel.cluster and a relaxed remote arrive per stage.
+        // The stage data are this CTA's shared memory (TMA-written A, the
+        // dequant warps' B half): a release fence restricted to shared::cta
+        // at cluster scope, then a relaxed remote arrive per stage.  Stages
+        // that became ready meanwhile share one fence.
         if (lane == 0) {
             const uint32_t remote0 = map_cluster(peer_deq(0), 0);
             int kt = 0;
@@ -168,7 +168,7 @@ gemm_w4_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
                 if (!mbar_wait_fast(full_deq(kt % STAGES), (kt / STAGES) & 1, abort_flag)) break;
                 int end = kt + 1;
                 while (end < num_kt && mbar_try_wait(full_deq(end % STAGES), (end / STAGES) & 1)) ++end;
-                fence_acq_rel_cluster();
+                fence_release_smem_cluster();
                 for (; kt < end; ++kt) mbar_arrive_cluster_relaxed(remote0 + 8u * (kt % STAGES));
             }
         }

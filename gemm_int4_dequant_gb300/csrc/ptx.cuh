@@ -190,11 +190,17 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 // Relaxed arrive on an mbarrier of another CTA; ordering comes from a
-// preceding fence_acq_rel_cluster (release pattern: fence, then relaxed arrive).
+// preceding release fence (release pattern: fence, then relaxed arrive).
 __device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
-__device__ __forceinline__ void fence_acq_rel_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
+// Release fence at cluster scope restricted to this CTA's shared memory:
+// orders the shared-memory writes this thread performed or observed (for
+// example through an mbarrier it waited on) before its later operations at
+// cluster scope, without draining global-memory traffic.
+__device__ __forceinline__ void fence_release_smem_cluster() {
+    asm volatile("fence.release.sync_restrict::shared::cta.cluster;" ::: "memory");
+}
 
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
     uint32_t ok;
