@@ -188,7 +188,8 @@ KERNEL_SOURCES = {
              "gemm_int4_dequant_gb300/csrc/common.cuh"],
     "gemm": ["gemm_int4_dequant_gb300/csrc/gemm_tc.cu", "gemm_int4_dequant_gb300/csrc/ptx.cuh",
              "gemm_int4_dequant_gb300/csrc/common.cuh"],
-    "quant": ["gemm_int4_dequant_gb300/csrc/quant_permute.cu", "gemm_int4_dequant_gb300/csrc/common.cuh"],
+    "quant": ["gemm_int4_dequant_gb300/csrc/quant_permute.cu", "gemm_int4_dequant_gb300/csrc/ptx.cuh",
+              "gemm_int4_dequant_gb300/csrc/common.cuh"],
 }
 
 
@@ -486,8 +487,8 @@ def roofline(work, sec_per_launch, peaks, peak_src, kind_name, workload):
         return {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "peak_source": "%s bf16 burst" % peak_src,
                 "traffic": recorded_traffic("gemm", workload)}
-    achieved = work.bytes / work.launches_per_step / sec_per_launch / 1e9 if not isinstance(work, QuantWork) else \
-        work.bytes / sec_per_launch / 1e9
+    # quant: the two kernels of a step together (bytes of the step / time of the step)
+    achieved = work.bytes / work.launches_per_step / sec_per_launch / 1e9
     peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     return {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
             "peak_source": "%s HBM copy" % peak_src, "traffic": recorded_traffic(kind_name, workload)}
