@@ -7,25 +7,39 @@
 // packed (K/2, N) int8 with the low nibble for even k; one packed k-tile of B
 // feeds an A k-tile twice as long.)
 //
-// A thread-block cluster of two CTAs (a CTA pair on two SMs) computes one
-// 256 x 256 output tile with tcgen05.mma.cta_group::2 (M256 N256 K16): CTA r
-// holds A rows [128r, 128r+128) and B columns [128r, 128r+128) of the tile
-// in its shared memory, and the pair's MMA reads both halves, so each SM
-// loads, dequantises and serves only half of B per FLOP.  Per CTA, 10 warps:
-//   warp 0      TMA producer: A tile [128 x 64] bf16 (128B-swizzled, K-major)
-//               and its packed B half [32 x 128] bytes, one mbarrier per stage;
-//   warp 1      TMEM allocator (both CTAs) and, in the even CTA, the MMA
-//               issuer (one thread): 4 MMAs per k-tile into an fp32
-//               accumulator in TMEM; the commit frees the stage in both CTAs;
-//   warps 2..9  dequant: packed bytes -> (u - zero) bf16, written straight into
-//               the canonical 128B-swizzled MN-major operand layout; a warp
-//               then tells the even CTA's barrier (remotely from the odd CTA)
-//               that its part of the stage is ready; afterwards the epilogue:
-//               tcgen05.ld of this CTA's 128 accumulator rows, * scale, -> bf16.
+// Persistent CTA pairs: each thread-block cluster of two CTAs (two SMs)
+// computes 256 x 256 output tiles (tile, tile + pairs, ...) with
+// tcgen05.mma.cta_group::2 (M256 N256 K16).  CTA r holds A rows
+// [128r, 128r+128) and B columns [128r, 128r+128) of a tile in its shared
+// memory and the pair's MMA reads both halves, so each SM loads, dequantises
+// and serves only half of B per FLOP.  Per CTA, 14 warps:
+//   warp 0       TMA producer: A tile [128 x 64] bf16 (128B-swizzled, K-major)
+//                and the packed B half [32 x 128] bytes, one mbarrier per stage,
+//                running across tile boundaries;
+//   warp 1       TMEM allocator (both CTAs); in the even CTA the MMA issuer (one
+//                thread): 4 MMAs per k-tile into one of two fp32 accumulators in
+//                TMEM (tiles alternate), the commit frees the stage in both CTAs;
+//                in the odd CTA the forwarder of "stage ready" to the even CTA;
+//   warps 2..9   dequant: packed bytes -> (u - zero) bf16, written straight into
+//                the canonical 128B-swizzled MN-major operand layout;
+//   warps 10..13 epilogue, one per TMEM lane quarter: tcgen05.ld of the
+//                finished accumulator's 128 rows, * scale, -> bf16, then the
+//                accumulator is handed back to the MMA issuer; the epilogue of
+//                one tile overlaps the main loop of the next.
+// Inside every group of four columns the shared-memory (and so TMEM) column
+// order is n0 n2 n1 n3: one mask of a packed 32-bit word then yields the
+// nibbles of bytes 0 and 2 (or 1 and 3) as a bf16 pair, so unpacking eight
+// weights costs three shifts and four three-input logic ops.  The epilogue
+// puts the columns back in order.
+// Every wait is bounded; on timeout the kernel records an error code in a
+// device word (w4_device_error), stops issuing work, drains and frees TMEM.
+
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
 #include <cooperative_groups.h>
+
+#include <algorithm>
 
 #include "common.cuh"
 #include "ptx.cuh"
@@ -43,7 +57,7 @@ constexpr int BN = 256;                      // tile columns (the pair's MMA N)
 constexpr int BNH = BN / 2;                  // B columns held by each CTA
 constexpr int BK = 64;
 constexpr int STAGES = 6;
-constexpr int THREADS = 320;
+constexpr int THREADS = 448;
 constexpr int A_BYTES = BM * BK * 2;         // 16 KB
 constexpr int BP_BYTES = (BK / 2) * BNH;     // 4 KB packed
 constexpr int BD_BYTES = BK * BNH * 2;       // 16 KB dequantised
@@ -51,12 +65,13 @@ constexpr int OFF_A = 0;
 constexpr int OFF_BD = OFF_A + STAGES * A_BYTES;
 constexpr int OFF_BP = OFF_BD + STAGES * BD_BYTES;
 constexpr int OFF_BAR = OFF_BP + STAGES * BP_BYTES;
-constexpr int NUM_BARS = 4 * STAGES + 1;
+constexpr int NUM_BARS = 4 * STAGES + 4;
 constexpr int OFF_TMEM_SLOT = OFF_BAR + NUM_BARS * 8;
 constexpr int OFF_ABORT = OFF_TMEM_SLOT + 4;
 constexpr int SMEM_USED = OFF_ABORT + 4;
 constexpr int SMEM_BYTES = SMEM_USED + 1024;  // slack to align the base to 1 KB
-constexpr uint32_t TMEM_COLS = 256;
+constexpr uint32_t TMEM_COLS = 512;            // two accumulators of 256 columns
+constexpr int EPI_WARP0 = 10;                   // warps 10..13
 constexpr int DEQ_WARPS = 8;
 constexpr int DEQ_THREADS = DEQ_WARPS * 32;
 
@@ -94,27 +109,32 @@ __device__ __forceinline__ void unpack_word(uint32_t w, uint32_t& e0, uint32_t& 
 __global__ void __launch_bounds__(THREADS, 1)
 gemm_w4_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                   const __nv_bfloat16* __restrict__ scale, const __nv_bfloat16* __restrict__ zero,
-                  __nv_bfloat16* __restrict__ C, int M, int N, int K) {
+                  __nv_bfloat16* __restrict__ C, int M, int N, int K, int tiles_n, int num_tiles) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* sbase = smem_raw + (base - raw);
     const uint32_t bar0 = base + OFF_BAR;
     auto full_tma = [&](int s) { return bar0 + 8u * s; };
-    auto full_deq = [&](int s) { return bar0 + 8u * (STAGES + s); };   // this CTA's dequant warps
+    auto full_deq = [&](int s) { return bar0 + 8u * (STAGES + s); };     // this CTA's dequant warps
     auto empty = [&](int s) { return bar0 + 8u * (2 * STAGES + s); };
     auto peer_deq = [&](int s) { return bar0 + 8u * (3 * STAGES + s); };  // even CTA: the odd CTA's stage is ready
-    const uint32_t tmem_full = bar0 + 8u * (4 * STAGES);
+    auto acc_full = [&](int b) { return bar0 + 8u * (4 * STAGES + b); };  // accumulator b finished
+    auto acc_empty = [&](int b) { return bar0 + 8u * (4 * STAGES + 2 + b); };   // even CTA: b read out by both
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(sbase + OFF_TMEM_SLOT);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sbase + OFF_ABORT);
 
     cg::cluster_group cluster = cg::this_cluster();
     const int rank = static_cast<int>(cluster.block_rank());     // 0: issues the pair's MMAs
+    const int pair = blockIdx.x >> 1, pairs = gridDim.x >> 1;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n0 = (blockIdx.x >> 1) * BN, m0 = blockIdx.y * (2 * BM);
-    const int mr = m0 + rank * BM;          // this CTA's first A row / accumulator row
-    const int nh = n0 + rank * BNH;         // this CTA's first B column
     const int num_kt = K / BK;
+    const int my_tiles = pair < num_tiles ? (num_tiles - pair + pairs - 1) / pairs : 0;
+    const int total_kt = my_tiles * num_kt;   // k-tiles this pair works through (stage ring position)
+    // tile it of this pair: row block, column block (column blocks fastest, so
+    // concurrently running pairs share rows of A)
+    auto tile_m = [&](int it) { return (pair + it * pairs) / tiles_n; };
+    auto tile_n = [&](int it) { return (pair + it * pairs) % tiles_n; };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -123,7 +143,10 @@ gemm_w4_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
             mbar_init(empty(s), 1);
             mbar_init(peer_deq(s), 1);
         }
-        mbar_init(tmem_full, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(acc_full(b), 1);
+            mbar_init(acc_empty(b), 2 * 4);   // four epilogue warps in each CTA
+        }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -138,22 +161,27 @@ gemm_w4_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
         if (lane == 0) {
             asm volatile("prefetch.tensormap [%0];" ::"l"(&tmap_a) : "memory");
             asm volatile("prefetch.tensormap [%0];" ::"l"(&tmap_b) : "memory");
-            // an A or B half lying wholly outside the matrix (ragged M or N)
-            // is not copied: its rows / columns of the tile are never stored
-            const bool load_a = mr < M, load_b = nh < N;
-            const uint32_t bytes = (load_a ? A_BYTES : 0) + (load_b ? BP_BYTES : 0);
             int issued = 0;
-            for (int kt = 0; kt < num_kt; ++kt) {
-                const int s = kt % STAGES, round = kt / STAGES;
-                if (round > 0 && !mbar_wait_fast(empty(s), (round - 1) & 1, abort_flag)) break;
-                mbar_arrive_expect_tx(full_tma(s), bytes);
-                if (load_a) tma_load_2d(base + OFF_A + s * A_BYTES, &tmap_a, kt * BK, mr, full_tma(s));
-                if (load_b) tma_load_2d(base + OFF_BP + s * BP_BYTES, &tmap_b, nh, kt * (BK / 2), full_tma(s));
-                issued = kt + 1;
+            bool ok = true;
+            for (int it = 0; it < my_tiles && ok; ++it) {
+                const int mr = tile_m(it) * (2 * BM) + rank * BM;   // this CTA's first A row
+                const int nh = tile_n(it) * BN + rank * BNH;        // this CTA's first B column
+                // an A or B half wholly outside the matrix (ragged M or N) is not
+                // copied: its rows / columns of the tile are never stored
+                const bool load_a = mr < M, load_b = nh < N;
+                const uint32_t bytes = (load_a ? A_BYTES : 0) + (load_b ? BP_BYTES : 0);
+                for (int kt = 0; kt < num_kt; ++kt) {
+                    const int g = it * num_kt + kt, s = g % STAGES, round = g / STAGES;
+                    if (round > 0 && !mbar_wait_fast(empty(s), (round - 1) & 1, abort_flag)) { ok = false; break; }
+                    mbar_arrive_expect_tx(full_tma(s), bytes);
+                    if (load_a) tma_load_2d(base + OFF_A + s * A_BYTES, &tmap_a, kt * BK, mr, full_tma(s));
+                    if (load_b) tma_load_2d(base + OFF_BP + s * BP_BYTES, &tmap_b, nh, kt * (BK / 2), full_tma(s));
+                    issued = g + 1;
+                }
             }
             // the last copies may still be landing if a consumer aborted
-            for (int kt = max(0, issued - STAGES); kt < issued; ++kt)
-                mbar_drain(full_tma(kt % STAGES), (kt / STAGES) & 1);
+            for (int g = max(0, issued - STAGES); g < issued; ++g)
+                mbar_drain(full_tma(g % STAGES), (g / STAGES) & 1);
         }
     } else if (warp == 1 && rank == 1) {
         // ---------------- odd CTA: forward "stage ready" to the even CTA ----------------
@@ -163,111 +191,125 @@ gemm_w4_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
         // that became ready meanwhile share one fence.
         if (lane == 0) {
             const uint32_t remote0 = map_cluster(peer_deq(0), 0);
-            int kt = 0;
-            while (kt < num_kt) {
-                if (!mbar_wait_fast(full_deq(kt % STAGES), (kt / STAGES) & 1, abort_flag)) break;
-                int end = kt + 1;
-                while (end < num_kt && mbar_try_wait(full_deq(end % STAGES), (end / STAGES) & 1)) ++end;
+            int g = 0;
+            while (g < total_kt) {
+                if (!mbar_wait_fast(full_deq(g % STAGES), (g / STAGES) & 1, abort_flag)) break;
+                int end = g + 1;
+                while (end < total_kt && mbar_try_wait(full_deq(end % STAGES), (end / STAGES) & 1)) ++end;
                 fence_release_smem_cluster();
-                for (; kt < end; ++kt) mbar_arrive_cluster_relaxed(remote0 + 8u * (kt % STAGES));
+                for (; g < end; ++g) mbar_arrive_cluster_relaxed(remote0 + 8u * (g % STAGES));
             }
         }
     } else if (warp == 1) {
         // ---------------- MMA issuer (even CTA) ----------------
         if (lane == 0) {
             bool ok = true;
-            for (int kt = 0; kt < num_kt && ok; ++kt) {
-                const int s = kt % STAGES, round = kt / STAGES;
-                ok = mbar_wait_fast(full_deq(s), round & 1, abort_flag) &&
-                     mbar_wait_cluster(peer_deq(s), round & 1, abort_flag);
-                if (!ok) break;
+            for (int it = 0; it < my_tiles && ok; ++it) {
+                const int b = it & 1;
+                // accumulator b was read out by both CTAs' epilogues (tile it - 2)
+                if (it >= 2 && !mbar_wait_cluster(acc_empty(b), ((it >> 1) - 1) & 1, abort_flag)) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t a_addr = base + OFF_A + s * A_BYTES;
-                const uint32_t b_addr = base + OFF_BD + s * BD_BYTES;
+                const uint32_t d_tmem = tmem_base + b * BN;
+                for (int kt = 0; kt < num_kt; ++kt) {
+                    const int g = it * num_kt + kt, s = g % STAGES, round = g / STAGES;
+                    ok = mbar_wait_fast(full_deq(s), round & 1, abort_flag) &&
+                         mbar_wait_cluster(peer_deq(s), round & 1, abort_flag);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t a_addr = base + OFF_A + s * A_BYTES;
+                    const uint32_t b_addr = base + OFF_BD + s * BD_BYTES;
 #pragma unroll
-                for (int kk = 0; kk < BK / 16; ++kk) {
-                    // A: K-major SW128, +32 B per 16-element k step; SBO = 8 rows * 128 B.
-                    const uint64_t adesc = sw128_desc(a_addr + kk * 32, 16, 1024);
-                    // B: MN-major SW128, k-groups of 8 rows 1 KB apart (SBO),
-                    // 64-column atoms (BK/8) KB apart (LBO).
-                    const uint64_t bdesc = sw128_desc(b_addr + kk * 2 * 1024, (BK / 8) * 1024, 1024);
-                    umma_bf16_pair(tmem_base, adesc, bdesc, kIdesc, (kt > 0 || kk > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < BK / 16; ++kk) {
+                        // A: K-major SW128, +32 B per 16-element k step; SBO = 8 rows * 128 B.
+                        const uint64_t adesc = sw128_desc(a_addr + kk * 32, 16, 1024);
+                        // B: MN-major SW128, k-groups of 8 rows 1 KB apart (SBO),
+                        // 64-column atoms (BK/8) KB apart (LBO).
+                        const uint64_t bdesc = sw128_desc(b_addr + kk * 2 * 1024, (BK / 8) * 1024, 1024);
+                        umma_bf16_pair(d_tmem, adesc, bdesc, kIdesc, (kt > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    umma_commit_pair(empty(s), 0x3);
                 }
-                umma_commit_pair(empty(s), 0x3);
+                if (ok) umma_commit_pair(acc_full(b), 0x3);
             }
-            umma_commit_pair(tmem_full, 0x3);
         }
-    } else {
+    } else if (warp < EPI_WARP0) {
         // ---------------- dequant (warps 2..9) ----------------
         const int t = threadIdx.x - 64;          // 0..255
         const int nl = (t & 15) * 8;             // 8 of this CTA's 128 columns
         const int kp_lane = t >> 4;              // 0..15
-        // zero-point pairs in shared-memory column order: (z0,z2) (z1,z3) (z4,z6) (z5,z7).
-        // Fast path: 128 + z exact in bf16 (integer zero points) -> one subtract.
-        uint32_t zz[4], zraw[4];
-        bool fast = true;
-        {
-            float zf[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int n = nh + nl + j;
-                zf[j] = n < N ? __bfloat162float(zero[n]) : 0.f;
-            }
-            const int pa[4] = {0, 1, 4, 5}, pb[4] = {2, 3, 6, 7};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float a = 128.0f + zf[pa[j]], b = 128.0f + zf[pb[j]];
-                const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-                fast = fast && __low2float(h) == a && __high2float(h) == b;
-                zz[j] = *reinterpret_cast<const uint32_t*>(&h);
-                const __nv_bfloat162 r = __floats2bfloat162_rn(zf[pa[j]], zf[pb[j]]);
-                zraw[j] = *reinterpret_cast<const uint32_t*>(&r);
-            }
-        }
         const uint32_t k128 = 0x43004300u;
         bool ok = true;
-        for (int kt = 0; kt < num_kt && ok; ++kt) {
-            const int s = kt % STAGES, round = kt / STAGES;
-            if (round > 0 && !mbar_wait_fast(empty(s), (round - 1) & 1, abort_flag)) { ok = false; break; }
-            if (!mbar_wait_fast(full_tma(s), round & 1, abort_flag)) { ok = false; break; }
-            const uint8_t* bp = sbase + OFF_BP + s * BP_BYTES;
-            uint8_t* bd = sbase + OFF_BD + s * BD_BYTES;
+        for (int it = 0; it < my_tiles && ok; ++it) {
+            const int nh = tile_n(it) * BN + rank * BNH;
+            // zero-point pairs in shared-memory column order: (z0,z2) (z1,z3) (z4,z6) (z5,z7).
+            // Fast path: 128 + z exact in bf16 (integer zero points) -> one subtract.
+            uint32_t zz[4], zraw[4];
+            bool fast = true;
+            {
+                float zf[8];
 #pragma unroll
-            for (int i = 0; i < (BK / 2) / 16; ++i) {
-                const int kp = kp_lane + 16 * i;
-                const uint2 v = *reinterpret_cast<const uint2*>(bp + kp * BNH + nl);
-                uint32_t e[4], o[4];
-                unpack_word(v.x, e[0], e[1], o[0], o[1]);
-                unpack_word(v.y, e[2], e[3], o[2], o[3]);
-                if (fast) {
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) { e[j] = bsub2(e[j], zz[j]); o[j] = bsub2(o[j], zz[j]); }
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        e[j] = bsub2(bsub2(e[j], k128), zraw[j]);
-                        o[j] = bsub2(bsub2(o[j], k128), zraw[j]);
-                    }
+                for (int j = 0; j < 8; ++j) {
+                    const int n = nh + nl + j;
+                    zf[j] = n < N ? __bfloat162float(zero[n]) : 0.f;
                 }
-                *reinterpret_cast<uint4*>(bd + bd_offset(2 * kp, nl)) = make_uint4(e[0], e[1], e[2], e[3]);
-                *reinterpret_cast<uint4*>(bd + bd_offset(2 * kp + 1, nl)) = make_uint4(o[0], o[1], o[2], o[3]);
+                const int pa[4] = {0, 1, 4, 5}, pb[4] = {2, 3, 6, 7};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float a = 128.0f + zf[pa[j]], c = 128.0f + zf[pb[j]];
+                    const __nv_bfloat162 h = __floats2bfloat162_rn(a, c);
+                    fast = fast && __low2float(h) == a && __high2float(h) == c;
+                    zz[j] = *reinterpret_cast<const uint32_t*>(&h);
+                    const __nv_bfloat162 r = __floats2bfloat162_rn(zf[pa[j]], zf[pb[j]]);
+                    zraw[j] = *reinterpret_cast<const uint32_t*>(&r);
+                }
             }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(full_deq(s));
+            for (int kt = 0; kt < num_kt; ++kt) {
+                const int g = it * num_kt + kt, s = g % STAGES, round = g / STAGES;
+                if (round > 0 && !mbar_wait_fast(empty(s), (round - 1) & 1, abort_flag)) { ok = false; break; }
+                if (!mbar_wait_fast(full_tma(s), round & 1, abort_flag)) { ok = false; break; }
+                const uint8_t* bp = sbase + OFF_BP + s * BP_BYTES;
+                uint8_t* bd = sbase + OFF_BD + s * BD_BYTES;
+#pragma unroll
+                for (int i = 0; i < (BK / 2) / 16; ++i) {
+                    const int kp = kp_lane + 16 * i;
+                    const uint2 v = *reinterpret_cast<const uint2*>(bp + kp * BNH + nl);
+                    uint32_t e[4], o[4];
+                    unpack_word(v.x, e[0], e[1], o[0], o[1]);
+                    unpack_word(v.y, e[2], e[3], o[2], o[3]);
+                    if (fast) {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) { e[j] = bsub2(e[j], zz[j]); o[j] = bsub2(o[j], zz[j]); }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            e[j] = bsub2(bsub2(e[j], k128), zraw[j]);
+                            o[j] = bsub2(bsub2(o[j], k128), zraw[j]);
+                        }
+                    }
+                    *reinterpret_cast<uint4*>(bd + bd_offset(2 * kp, nl)) = make_uint4(e[0], e[1], e[2], e[3]);
+                    *reinterpret_cast<uint4*>(bd + bd_offset(2 * kp + 1, nl)) = make_uint4(o[0], o[1], o[2], o[3]);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(full_deq(s));
+            }
         }
-
-        // ---------------- epilogue ----------------
-        // warps 2..9: TMEM lane quarter (warp % 4), column half ((warp-2) / 4);
-        // the decision is warp-uniform (tcgen05.ld is warp-collective)
-        if (__all_sync(0xffffffffu, ok && mbar_wait_fast(tmem_full, 0, abort_flag))) {
+    } else {
+        // ---------------- epilogue (warps 10..13) ----------------
+        // TMEM lane quarter = warp % 4; each warp stores its 32 rows x 256
+        // columns of the tile.  Decisions are warp-uniform (tcgen05.ld is
+        // warp-collective).
+        const int quarter = warp & 3;
+        const uint32_t release = map_cluster(acc_empty(0), 0);
+        for (int it = 0; it < my_tiles; ++it) {
+            const int b = it & 1;
+            if (!__all_sync(0xffffffffu, mbar_wait_cluster(acc_full(b), (it >> 1) & 1, abort_flag))) break;
             tc_fence_after();
-            const int quarter = warp & 3;           // TMEM lanes 32*quarter .. +31
-            const int half = (warp - 2) >> 2;
-            const int m = mr + quarter * 32 + lane;
-            for (int cb = half * (BN / 64); cb < (half + 1) * (BN / 64); ++cb) {
+            const int n0 = tile_n(it) * BN;
+            const int m = tile_m(it) * (2 * BM) + rank * BM + quarter * 32 + lane;
+            for (int cb = 0; cb < BN / 32; ++cb) {
                 uint32_t r[32];
-                tmem_ld32(tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + cb * 32, r);
+                tmem_ld32(tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + b * BN + cb * 32, r);
                 const int nb = n0 + cb * 32;
                 if (m < M && nb < N) {
                     // TMEM column order inside each group of 4 is n0 n2 n1 n3
@@ -300,12 +342,17 @@ gemm_w4_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
                     }
                 }
             }
+            // accumulator b is read out (tcgen05.ld waited): hand it back to the even CTA
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(release + 8u * b);
         }
     }
 
-    // every MMA of the pair is complete (both CTAs waited on tmem_full, or
-    // timed out) before either CTA frees its TMEM
-    if (warp == 1 && rank == 0 && lane == 0) mbar_drain(tmem_full, 0);
+    // every MMA of the pair is complete (the epilogues waited for the last
+    // accumulator, or everything timed out) before either CTA frees its TMEM
+    if (warp == 1 && rank == 0 && lane == 0 && my_tiles > 0)
+        mbar_drain(acc_full((my_tiles - 1) & 1), ((my_tiles - 1) >> 1) & 1);
     tc_fence_before();
     cluster.sync();
     if (warp == 1) {
@@ -321,7 +368,7 @@ w4_status run_gemm(const void* A, const void* B, const void* scale, const void* 
     using namespace gemm;
     if (M > 0x7FFFFFFF || N > 0x7FFFFFFF || K > 0x7FFFFFFF) return W4_ERR_SHAPE;
     const int64_t tiles_m = (M + 2 * BM - 1) / (2 * BM), tiles_n = (N + BN - 1) / BN;
-    if (tiles_m > 65535 || 2 * tiles_n > 0x7FFFFFFF) return W4_ERR_SHAPE;
+    if (tiles_m * tiles_n > 0x7FFFFFFF) return W4_ERR_SHAPE;
     auto encode = tensor_map_encoder();
     if (!encode) return W4_ERR_CUDA;
 
@@ -350,7 +397,6 @@ w4_status run_gemm(const void* A, const void* B, const void* scale, const void* 
     cudaError_t e = ensure_smem_limit(gemm_w4_tc_kernel, SMEM_BYTES, smem_set);
     if (e != cudaSuccess) return W4_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(2 * tiles_n), static_cast<unsigned>(tiles_m), 1);
     cfg.blockDim = dim3(THREADS, 1, 1);
     cfg.dynamicSmemBytes = SMEM_BYTES;
     cfg.stream = stream;
@@ -361,9 +407,23 @@ w4_status run_gemm(const void* A, const void* B, const void* scale, const void* 
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    // persistent: as many CTA pairs as can be resident at once
+    static int max_pairs[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return W4_ERR_CUDA;
+    if (max_pairs[dev] == 0) {
+        cfg.gridDim = dim3(static_cast<unsigned>(2 * std::max(1, sm_count() / 2)), 1, 1);
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, gemm_w4_tc_kernel, &cfg) != cudaSuccess || n <= 0) return W4_ERR_CUDA;
+        max_pairs[dev] = n;
+    }
+    const int64_t num_tiles = tiles_m * tiles_n;
+    const int pairs = static_cast<int>(std::min<int64_t>(num_tiles, max_pairs[dev]));
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs), 1, 1);
     return launch_status(cudaLaunchKernelEx(&cfg, gemm_w4_tc_kernel, ta, tb, static_cast<const __nv_bfloat16*>(scale),
                                             static_cast<const __nv_bfloat16*>(zero), static_cast<__nv_bfloat16*>(C),
-                                            static_cast<int>(M), static_cast<int>(N), static_cast<int>(K)));
+                                            static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
+                                            static_cast<int>(tiles_n), static_cast<int>(num_tiles)));
 }
 
 int take_device_error_gemm() { return take_unit_device_error(); }
