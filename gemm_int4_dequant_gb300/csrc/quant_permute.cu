@@ -77,7 +77,8 @@ quantize_pack_cluster_kernel(const __grid_constant__ CUtensorMap tmap, uint8_t* 
                              float* __restrict__ scale, int K, int N, int R, int box) {
     extern __shared__ __align__(128) uint8_t qtile[];   // [R][32] bf16
     __shared__ __align__(8) uint64_t bar;
-    __shared__ uint32_t pmax[QC_COLS];
+    __shared__ __align__(8) uint64_t pm_bar;          // every rank's partial maxima have landed
+    __shared__ uint32_t pm_all[QC_CS][QC_COLS];       // partial maxima, one row per rank
     __shared__ uint32_t wmax[QC_THREADS / 32][QC_COLS];
     __shared__ float s_scale[QC_COLS], s_inv[QC_COLS];
     __shared__ int abort_word;
@@ -90,13 +91,20 @@ quantize_pack_cluster_kernel(const __grid_constant__ CUtensorMap tmap, uint8_t* 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = tid & 3, rl = tid >> 2;          // 8-column group, row lane
     const uint32_t b = ptx::smem_u32(&bar);
+    const uint32_t pb = ptx::smem_u32(&pm_bar);
 
     if (tid == 0) {
         ptx::mbar_init(b, 1);
+        ptx::mbar_init(pb, 1);
         abort_word = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        // the peers' pushes (cs x 32 words) complete this phase
+        ptx::mbar_arrive_expect_tx(pb, static_cast<uint32_t>(cs) * QC_COLS * 4);
     }
     __syncthreads();
+    // first half of a cluster barrier: this CTA's barriers are initialised
+    // (the second half is waited for just before pushing to the peers)
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
     const int nbox = (rows + box - 1) / box;
     if (tid == 0 && nbox > 0) {
         ptx::mbar_arrive_expect_tx(b, static_cast<uint32_t>(nbox) * box * QC_COLS * 2);
@@ -133,15 +141,25 @@ quantize_pack_cluster_kernel(const __grid_constant__ CUtensorMap tmap, uint8_t* 
         }
     }
     __syncthreads();
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");   // every peer is initialised
     if (tid < QC_COLS) {
+        // push this CTA's partial maximum of column tid into every rank's
+        // pm_all[rank][tid]; each store completes 4 bytes on that rank's pm_bar
         uint32_t m = 0;
         for (int w = 0; w < QC_THREADS / 32; ++w) m = max(m, wmax[w][tid]);
-        pmax[tid] = m;
+        const uint32_t slot = ptx::smem_u32(&pm_all[rank][tid]);
+        for (int r = 0; r < cs; ++r)
+            asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.u32 [%0], %1, [%2];" ::"r"(
+                             ptx::map_cluster(slot, r)),
+                         "r"(m), "r"(ptx::map_cluster(pb, r))
+                         : "memory");
     }
-    cluster.sync();
+    // wait for every rank's push (bounded); afterwards no peer touches this
+    // CTA's shared memory again, so no cluster barrier is needed at exit
+    if (!ptx::mbar_wait(pb, 0, &abort_word)) ok = false;
     if (tid < QC_COLS) {
         uint32_t m = 0;
-        for (int r = 0; r < cs; ++r) m = max(m, cluster.map_shared_rank(pmax, r)[tid]);
+        for (int r = 0; r < cs; ++r) m = max(m, pm_all[r][tid]);
         const float sc = __fdiv_rn(bf16_bits_to_f32(m), 7.0f);
         s_scale[tid] = sc;
         s_inv[tid] = sc == 0.0f ? 0.0f : __frcp_rn(sc);
@@ -196,7 +214,6 @@ quantize_pack_cluster_kernel(const __grid_constant__ CUtensorMap tmap, uint8_t* 
                     make_uint2(out[0], out[1]);
         }
     }
-    cluster.sync();  // peers have read pmax
 }
 
 // ---------------------------------------------------------------------------
