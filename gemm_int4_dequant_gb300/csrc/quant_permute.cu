@@ -156,7 +156,10 @@ quantize_pack_cluster_kernel(const __grid_constant__ CUtensorMap tmap, uint8_t* 
     }
     // wait for every rank's push (bounded); afterwards no peer touches this
     // CTA's shared memory again, so no cluster barrier is needed at exit
-    if (!ptx::mbar_wait(pb, 0, &abort_word)) ok = false;
+    if (!ptx::mbar_wait(pb, 0, &abort_word)) {
+        ok = false;
+        if (tid == 0) ptx::mbar_drain(pb, 0);   // a slow peer's push may still be on its way
+    }
     if (tid < QC_COLS) {
         uint32_t m = 0;
         for (int r = 0; r < cs; ++r) m = max(m, pm_all[r][tid]);
