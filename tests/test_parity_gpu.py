@@ -204,6 +204,8 @@ def _check_gemm_full(w4, M, N, K, seed=0, **kw):
     (129, 528, 512),
     (257, 256, 128),    # second 256-row tile holds one row; its odd CTA has no rows
     (384, 784, 192),    # ragged M tile pair and a last column tile of 16 columns
+    (2048, 4096, 64),   # 256 tiles, one k-tile each: ring and accumulators wrap across tiles
+    (1280, 2320, 192),  # several tiles per CTA pair with ragged last row and column tiles
 ])
 def test_gemm_small(w4, M, N, K):
     _check_gemm_full(w4, M, N, K, seed=M + N + K)
