@@ -105,13 +105,21 @@ def barrier(world):
         dist.barrier()
 
 
-def max_over_ranks(v, world):
+def max_over_ranks(v, world, device="cuda"):
+    """The slowest rank's time (every rank gets it); device is where the
+    reduction tensor lives (cuda under NCCL, cpu under gloo)."""
     if world == 1:
         return v
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    t = torch.tensor([v], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_rate(per_rank_rate_at_max_time, world):
+    """Whole-job throughput: every rank processes the same units (replicas,
+    weak scaling), all within the slowest rank's time."""
+    return per_rank_rate_at_max_time * world
 
 
 # ---------------------------------------------------------------------------
@@ -501,7 +509,7 @@ def run_ours(args, world, rank):
     kind = WORKLOADS[args.workload]["kind"]
     sec, g, stream = time_graph(work, args.steps, args.warmup, world)
     sec_step = sec / args.steps
-    value = rate(work, sec_step) * world
+    value = job_rate(rate(work, sec_step), world)
     with ClockSampler(int(os.environ.get("LOCAL_RANK", "0"))) as cs:
         soak(g, stream, 2.0)
         sec2, _, _ = time_graph(work, args.steps, 0, world)
@@ -511,7 +519,7 @@ def run_ours(args, world, rank):
     else:
         e2e_sec, hb, ob = e2e_generic(work, max(2, min(args.steps, 10)), world)
         e2e_sec = e2e_sec * args.steps / max(2, min(args.steps, 10))
-    e2e_val = rate(work, e2e_sec / args.steps) * world
+    e2e_val = job_rate(rate(work, e2e_sec / args.steps), world)
     line = {
         "metric": METRIC, "value": value, "unit": unit_of(work), "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": sec_step * 1e3, "higher_is_better": True, "scaling": "weak",
