@@ -11,13 +11,18 @@
 // GB300 design.  The op reads 0.5 B of weight per multiply-add, so HBM
 // bandwidth is the roofline.  One CTA per SM owns a contiguous, balanced row
 // range (and, when x does not fit, one K-slice of a thread-block cluster):
-//   * warp NC (producer) streams 16-row tiles with 1-D bulk copies (TMA).
-//     The copy engine has a fixed cost per copy, so copies are large: a tile
-//     whose rows are contiguous in memory (no K split) is one copy of 16 full
-//     rows; otherwise each row's K-chunk is one copy (>= 2 KB) into a row
-//     pitch padded to 64 mod 128 bytes, which keeps the consumers' fragment
-//     loads on distinct banks.  The ring holds as many stages as shared
-//     memory allows (about 200 KB in flight per SM, no registers spent);
+//   * warp NC (producer) streams 16-row tiles with the TMA.  The copy engine
+//     has a fixed cost per copy, so a stage is one copy: the weights are
+//     viewed as a 3-D tensor (8-byte words x 64-byte chunks x rows) and a box
+//     of 16 rows x an ODD number of chunks lands at a row pitch of 64 mod
+//     128 bytes, which keeps the consumers' fragment loads on distinct banks
+//     (chunks past the end of a row are zero-filled, not fetched).  A tile
+//     with fewer rows (the end of a CTA's range) takes 4-row boxes so that no
+//     neighbour's rows are read.  Rows that are not whole 64-byte chunks
+//     (K % 128 != 0) fall back to 1-D bulk copies: one per tile when its rows
+//     are contiguous, else one per row into a padded pitch.  The ring holds
+//     as many stages as shared memory allows (about 200 KB in flight per SM,
+//     no registers spent);
 //   * warps 0..NC-1 (consumers) share out the 128-k blocks of every stage
 //     round-robin (continuing across stages, so the split stays balanced):
 //     two 16-byte shared loads give a lane its rows g and g+8, each uint32
@@ -38,6 +43,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cstring>
 
 #include "common.cuh"
 #include "ptx.cuh"
@@ -81,6 +87,8 @@ struct Plan {
     int groups;     // row groups
     int rows_cap;   // rows per CTA at most
     int perwarp;    // 1: every warp keeps its own row partials (no per-tile barrier)
+    int tmap;       // 1: a stage is one (or, for a partial tile, a few) 3-D tensor copies
+    int nbox;       // 64-byte chunks per row in a tensor box (odd: pitch = 64 mod 128)
 };
 
 struct Layout {
@@ -112,7 +120,8 @@ template <int C>
 __global__ void __launch_bounds__(THREADS, 1)
 gemv_tma_kernel(const uint8_t* __restrict__ qw, const __nv_bfloat16* __restrict__ scale,
                 const __nv_bfloat16* __restrict__ zero, const __nv_bfloat16* __restrict__ x,
-                __nv_bfloat16* __restrict__ d, int N, int K, Plan P, MaskMagic dq) {
+                __nv_bfloat16* __restrict__ d, int N, int K, Plan P, MaskMagic dq,
+                const __grid_constant__ CUtensorMap tm16, const __grid_constant__ CUtensorMap tm4) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t* sm = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -192,10 +201,23 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const __nv_bfloat16* __restrict_
                 const int seg = min(P.kchunk, klen - ch * P.kchunk) / 2;   // bytes per row (multiple of 16)
                 const uint32_t dst = sm_addr + slot * L.stage_bytes;
                 const uint8_t* src = src0 + static_cast<int64_t>(tile) * 16 * row_bytes + ch * (P.kchunk / 2);
-                mbar_arrive_expect_tx(bar_full + 8 * slot, rows_here * seg);
-                if (P.dense) {
+                if (P.tmap) {
+                    const int c0 = (k0 + ch * P.kchunk) / 128, row0 = r0 + tile * 16;
+                    if (rows_here == 16) {
+                        mbar_arrive_expect_tx(bar_full + 8 * slot, 16 * pitch);
+                        tma_load_3d_hint(dst, &tm16, 0, c0, row0, bar_full + 8 * slot, policy);
+                    } else {
+                        const int nb = (rows_here + 3) / 4;
+                        mbar_arrive_expect_tx(bar_full + 8 * slot, nb * 4 * pitch);
+                        for (int b = 0; b < nb; ++b)
+                            tma_load_3d_hint(dst + b * 4 * pitch, &tm4, 0, c0, row0 + 4 * b, bar_full + 8 * slot,
+                                             policy);
+                    }
+                } else if (P.dense) {
+                    mbar_arrive_expect_tx(bar_full + 8 * slot, rows_here * seg);
                     bulk_load_hint(dst, src, rows_here * seg, bar_full + 8 * slot, policy);
                 } else {
+                    mbar_arrive_expect_tx(bar_full + 8 * slot, rows_here * seg);
                     for (int r = 0; r < rows_here; ++r)
                         bulk_load_hint(dst + r * pitch, src + r * row_bytes, seg, bar_full + 8 * slot, policy);
                 }
@@ -411,7 +433,9 @@ constexpr size_t kXfBudget = 80 * 1024;
 template <int C>
 Plan make_plan(int N, int K, int sms, int max_clusters_for_S /* 0: unknown */, int S_forced) {
     Plan P{};
-    auto slice_of = [&](int s) { return ((K + s - 1) / s + 31) / 32 * 32; };
+    const int tm = (K % 128 == 0) ? 1 : 0;   // rows are whole 64-byte chunks
+    const int sgran = tm ? 128 : 32;
+    auto slice_of = [&](int s) { return ((K + s - 1) / s + sgran - 1) / sgran * sgran; };
     auto xf_bytes = [&](int s) { return static_cast<size_t>((slice_of(s) + KB - 1) / KB) * 16 * C * 16; };
     int S = 1;
     if (S_forced) S = S_forced;
@@ -429,7 +453,11 @@ Plan make_plan(int N, int K, int sms, int max_clusters_for_S /* 0: unknown */, i
         P.kchunk = ((P.kslice + nch0 - 1) / nch0 + KB - 1) / KB * KB;
     }
     P.dense = (S == 1 && P.kchunk >= K) ? 1 : 0;
-    if (P.dense) {
+    P.tmap = tm;
+    if (tm) {
+        P.nbox = (P.kchunk / 128) | 1;
+        P.pitch = P.nbox * 64;
+    } else if (P.dense) {
         P.pitch = K / 2;
     } else {
         const int seg = P.kchunk / 2;
@@ -491,9 +519,26 @@ w4_status launch_gemv_tma_t(const void* qw, const void* scale, const void* zero,
     }
     cfg.gridDim = dim3(P.S * P.groups, 1, 1);
     cfg.dynamicSmemBytes = make_layout(C, P).total + 1024;
+    CUtensorMap tm16, tm4;
+    memset(&tm16, 0, sizeof(tm16));
+    memset(&tm4, 0, sizeof(tm4));
+    if (P.tmap) {
+        auto encode = tensor_map_encoder();
+        if (!encode) return W4_ERR_CUDA;
+        cuuint64_t dims[3] = {8, static_cast<cuuint64_t>(K / 128), static_cast<cuuint64_t>(N)};
+        cuuint64_t strides[2] = {64, static_cast<cuuint64_t>(K / 2)};
+        cuuint32_t estr[3] = {1, 1, 1};
+        for (int b = 0; b < 2; ++b) {
+            cuuint32_t box[3] = {8, static_cast<cuuint32_t>(P.nbox), b == 0 ? 16u : 4u};
+            if (encode(b == 0 ? &tm16 : &tm4, CU_TENSOR_MAP_DATA_TYPE_UINT64, 3, const_cast<void*>(qw), dims, strides,
+                       box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+                return W4_ERR_CUDA;
+        }
+    }
     e = cudaLaunchKernelEx(&cfg, kern, static_cast<const uint8_t*>(qw), static_cast<const __nv_bfloat16*>(scale),
                            static_cast<const __nv_bfloat16*>(zero), static_cast<const __nv_bfloat16*>(x),
-                           static_cast<__nv_bfloat16*>(d), N, K, P, MaskMagic{0x000F000Fu, 0x43004300u});
+                           static_cast<__nv_bfloat16*>(d), N, K, P, MaskMagic{0x000F000Fu, 0x43004300u}, tm16, tm4);
     return launch_status(e);
 }
 

@@ -147,6 +147,9 @@ def test_gemv_small_batch_full_size(w4, cfg):
     (1001, 17312, 8, "bf16"),   # cluster split with a partial last band per slice
     (5, 40960, 8, "bf16"),      # longest K accepted
     (400000, 256, 1, "bf16"),   # more row tiles than one wave holds
+    (1001, 4096, 3, "bf16"),    # tensor boxes running past the last row (zero-filled)
+    (2000, 12800, 6, "bf16"),   # tensor boxes with a cluster split and a 12-row tile (three 4-row boxes)
+    (4099, 384, 4, "bf16"),     # box of 3 chunks over a 3-chunk row, partial last tile
 ])
 def test_gemv_ragged_and_edge(w4, N, K, C, act):
     _check_gemv(w4, N, K, C, act, seed=N + K + C)
