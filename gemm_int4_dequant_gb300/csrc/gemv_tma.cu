@@ -242,67 +242,148 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const __nv_bfloat16* __restrict_
         // x as B fragments: entry (kb, word p, n, t4) holds, for kk = kb*128 +
         // 32*t4 + 8*p, the bf16 pairs (x[kk], x[kk+4]) (x[kk+1], x[kk+5])
         // (x[kk+2], x[kk+6]) (x[kk+3], x[kk+7]) -- the b0b1/b2b3 registers of
-        // the two MMAs that consume word p.  Loads are issued four at a time.
-        const int nkb = (klen + KB - 1) / KB;
-        const int per_n = nkb * 16;
-        const int total = C * per_n;
-        float xs_part[C];
-#pragma unroll
-        for (int c = 0; c < C; ++c) xs_part[c] = 0.f;
-        constexpr int XB = 8;  // loads in flight per thread while staging x
-        for (int e0 = tid; e0 < total; e0 += XB * CT) {
-            uint4 raw[XB];
-#pragma unroll
-            for (int b = 0; b < XB; ++b) {
-                const int e = e0 + b * CT;
-                raw[b] = make_uint4(0, 0, 0, 0);
-                if (e < total) {
-                    const int n = e / per_n, j = e - n * per_n;
-                    const int kk = (j >> 4) * KB + 32 * (j & 3) + 8 * ((j >> 2) & 3);
-                    if (kk < klen)
-                        raw[b] = *reinterpret_cast<const uint4*>(x + static_cast<int64_t>(n) * K + k0 + kk);
-                }
-            }
-#pragma unroll
-            for (int b = 0; b < XB; ++b) {
-                const int e = e0 + b * CT;
-                if (e >= total) break;
-                const int n = e / per_n, j = e - n * per_n;
-                const int t = j & 3, p = (j >> 2) & 3, kb = j >> 4;
-                const uint4 r = raw[b];
-                xf[((kb * 4 + p) * C + n) * 4 + t] =
-                    make_uint4(__byte_perm(r.x, r.z, 0x5410), __byte_perm(r.x, r.z, 0x7632),
-                               __byte_perm(r.y, r.w, 0x5410), __byte_perm(r.y, r.w, 0x7632));
-                const float v = bf16_bits_to_f32(r.x & 0xFFFFu) + bf16_bits_to_f32(r.x >> 16) +
-                                bf16_bits_to_f32(r.y & 0xFFFFu) + bf16_bits_to_f32(r.y >> 16) +
-                                bf16_bits_to_f32(r.z & 0xFFFFu) + bf16_bits_to_f32(r.z >> 16) +
-                                bf16_bits_to_f32(r.w & 0xFFFFu) + bf16_bits_to_f32(r.w >> 16);
-#pragma unroll
-                for (int c = 0; c < C; ++c)
-                    if (c == n) xs_part[c] += v;
-            }
-        }
-#pragma unroll
-        for (int c = 0; c < C; ++c) {
-            float v = xs_part[c];
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-            if (lane == 0) xsw[warp * C + c] = v;
-        }
-        for (int i = tid; i < 16 * C; i += CT) xzero[i] = make_uint4(0, 0, 0, 0);
-        named_barrier(1, CT);
-        if (tid < C) {
-            float v = 0.f;
-            for (int w = 0; w < NC; ++w) v += xsw[w * C + tid];
-            xsum[tid] = v;
-        }
-
-        // main loop: units of each stage go round-robin to the warps, the
-        // rotation carrying over from stage to stage
+        // the two MMAs that consume word p.
         const int g = lane >> 2, t4 = lane & 3;
         const bool bl = g < C;
         const uint4* xlane = bl ? xf + g * 4 + t4 : xzero + t4;
         constexpr int xw_stride = C * 4;
+        if constexpr (C == 1) {
+            // one column: a thread adds the eight values of each entry it
+            // stages (a few adds per entry, against up to eight columns' worth
+            // of conversions and selects per entry in the general case)
+            const int nkb = (klen + KB - 1) / KB;
+            const int per_n = nkb * 16;
+            const int total = C * per_n;
+            float xs_part[C];
+#pragma unroll
+            for (int c = 0; c < C; ++c) xs_part[c] = 0.f;
+            constexpr int XB = 8;  // loads in flight per thread while staging x
+            for (int e0 = tid; e0 < total; e0 += XB * CT) {
+                uint4 raw[XB];
+#pragma unroll
+                for (int b = 0; b < XB; ++b) {
+                    const int e = e0 + b * CT;
+                    raw[b] = make_uint4(0, 0, 0, 0);
+                    if (e < total) {
+                        const int n = e / per_n, j = e - n * per_n;
+                        const int kk = (j >> 4) * KB + 32 * (j & 3) + 8 * ((j >> 2) & 3);
+                        if (kk < klen)
+                            raw[b] = *reinterpret_cast<const uint4*>(x + static_cast<int64_t>(n) * K + k0 + kk);
+                    }
+                }
+#pragma unroll
+                for (int b = 0; b < XB; ++b) {
+                    const int e = e0 + b * CT;
+                    if (e >= total) break;
+                    const int n = e / per_n, j = e - n * per_n;
+                    const int t = j & 3, p = (j >> 2) & 3, kb = j >> 4;
+                    const uint4 r = raw[b];
+                    xf[((kb * 4 + p) * C + n) * 4 + t] =
+                        make_uint4(__byte_perm(r.x, r.z, 0x5410), __byte_perm(r.x, r.z, 0x7632),
+                                   __byte_perm(r.y, r.w, 0x5410), __byte_perm(r.y, r.w, 0x7632));
+                    const float v = bf16_bits_to_f32(r.x & 0xFFFFu) + bf16_bits_to_f32(r.x >> 16) +
+                                    bf16_bits_to_f32(r.y & 0xFFFFu) + bf16_bits_to_f32(r.y >> 16) +
+                                    bf16_bits_to_f32(r.z & 0xFFFFu) + bf16_bits_to_f32(r.z >> 16) +
+                                    bf16_bits_to_f32(r.w & 0xFFFFu) + bf16_bits_to_f32(r.w >> 16);
+#pragma unroll
+                    for (int c = 0; c < C; ++c)
+                        if (c == n) xs_part[c] += v;
+                }
+            }
+#pragma unroll
+            for (int c = 0; c < C; ++c) {
+                float v = xs_part[c];
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+                if (lane == 0) xsw[warp * C + c] = v;
+            }
+            for (int i = tid; i < 16 * C; i += CT) xzero[i] = make_uint4(0, 0, 0, 0);
+            named_barrier(1, CT);
+            if (tid < C) {
+                float v = 0.f;
+                for (int w = 0; w < NC; ++w) v += xsw[w * C + tid];
+                xsum[tid] = v;
+            }
+        } else {
+            // up to eight columns: thread tid stages entries tid, tid + CT, ...
+            // (n-major), stepping (n, j) without dividing, XB loads in
+            // flight; the column sums are left to the tensor cores
+            const int nkb = (klen + KB - 1) / KB;
+            const int per_n = nkb * 16;
+            constexpr int XB = 8;
+            const int dn = per_n > 0 ? CT / per_n : 0, dj = CT - dn * per_n;
+            int n_cur = per_n > 0 ? tid / per_n : C, j_cur = tid - n_cur * per_n;
+            while (n_cur < C) {
+                uint4 raw[XB];
+                int n = n_cur, j = j_cur;
+#pragma unroll
+                for (int b = 0; b < XB; ++b) {
+                    raw[b] = make_uint4(0, 0, 0, 0);
+                    if (n < C) {
+                        const int kk = (j >> 4) * KB + 32 * (j & 3) + 8 * ((j >> 2) & 3);
+                        if (kk < klen)
+                            raw[b] = *reinterpret_cast<const uint4*>(x + static_cast<int64_t>(n) * K + k0 + kk);
+                    }
+                    j += dj;
+                    n += dn;
+                    if (j >= per_n) { j -= per_n; ++n; }
+                }
+                n = n_cur;
+                j = j_cur;
+#pragma unroll
+                for (int b = 0; b < XB; ++b) {
+                    if (n < C) {
+                        const int t = j & 3, p = (j >> 2) & 3, kb = j >> 4;
+                        const uint4 r = raw[b];
+                        xf[((kb * 4 + p) * C + n) * 4 + t] =
+                            make_uint4(__byte_perm(r.x, r.z, 0x5410), __byte_perm(r.x, r.z, 0x7632),
+                                       __byte_perm(r.y, r.w, 0x5410), __byte_perm(r.y, r.w, 0x7632));
+                    }
+                    j += dj;
+                    n += dn;
+                    if (j >= per_n) { j -= per_n; ++n; }
+                }
+                n_cur = n;
+                j_cur = j;
+            }
+            for (int i = tid; i < 16 * C; i += CT) xzero[i] = make_uint4(0, 0, 0, 0);
+            named_barrier(1, CT);
+
+            // sum_k x[c][k] on the tensor cores: an all-ones A operand turns each
+            // MMA over a staged fragment into column sums (fp32 accumulation, as
+            // in the main product).  Warps take the (kb, word) pairs round-robin,
+            // two at a time on independent accumulators.
+            {
+                const uint32_t ones = 0x3F803F80u;   // bf16x2 (1.0, 1.0)
+                const uint32_t a1s[4] = {ones, ones, ones, ones};
+                float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+                float s2[4] = {0.f, 0.f, 0.f, 0.f}, s3[4] = {0.f, 0.f, 0.f, 0.f};
+                const int nq = nkb * 4, qstride = bl ? xw_stride : 0;
+                for (int q = warp; q < nq; q += 2 * NC) {
+                    const uint4 b0 = xlane[q * qstride];
+                    const uint4 b1 = q + NC < nq ? xlane[(q + NC) * qstride] : make_uint4(0, 0, 0, 0);
+                    mma_bf16(s0, a1s, b0.x, b0.y);
+                    mma_bf16(s1, a1s, b0.z, b0.w);
+                    mma_bf16(s2, a1s, b1.x, b1.y);
+                    mma_bf16(s3, a1s, b1.z, b1.w);
+                }
+                // every row of the product holds the same sums: lanes of row 0
+                // own columns 2*t4 and 2*t4 + 1
+                if (g == 0) {
+                    if (2 * t4 < C) xsw[warp * C + 2 * t4] = (s0[0] + s1[0]) + (s2[0] + s3[0]);
+                    if (2 * t4 + 1 < C) xsw[warp * C + 2 * t4 + 1] = (s0[1] + s1[1]) + (s2[1] + s3[1]);
+                }
+            }
+            named_barrier(1, CT);
+            if (tid < C) {
+                float v = 0.f;
+                for (int w = 0; w < NC; ++w) v += xsw[w * C + tid];
+                xsum[tid] = v;
+            }
+        }
+
+        // main loop: units of each stage go round-robin to the warps, the
+        // rotation carrying over from stage to stage
         const int xkb_stride = bl ? 4 * C * 4 : 0;
         const uint32_t mask = dq.mask, magic = dq.magic;
         const int row_off_a = g * pitch + 16 * t4, row_off_b = (g + 8) * pitch + 16 * t4;
