@@ -33,6 +33,8 @@ def _load():
         lib.w4o_quantize_pack.restype = None
         lib.w4o_permute.argtypes = [P, L, L, P]
         lib.w4o_permute.restype = ctypes.c_int
+        lib.w4o_gemv_packed.argtypes = [P, P, P, L, L, L, L, L, P, P]
+        lib.w4o_gemv_packed.restype = None
         _lib = lib
     return _lib
 
@@ -135,6 +137,31 @@ def quantize_pack(W_bits):
     packed = np.empty((K // 2, N), np.uint8)
     lib.w4o_quantize_pack(_ptr(W), K, N, _ptr(scale), _ptr(packed))
     return scale, packed
+
+
+def gemv_packed(packed, scale, x_bits, cols=None):
+    """d[c, n] = sum_k x[c, k] * q[k, n] * scale[n], in fp64, over the
+    quantiser's packed matrix.
+
+    packed: uint8 [K/2, N] (low nibble = even k, two's complement);
+    scale: float32 [N]; x_bits: uint16 bf16 patterns [C, K].  cols: optional
+    (begin, end) column range; columns outside it are NaN.  Returns
+    (d, ref_abs), both float64 [C, N].
+    """
+    lib = _load()
+    p = np.ascontiguousarray(packed, dtype=np.uint8)
+    s = np.ascontiguousarray(scale, dtype=np.float32)
+    xb = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    Kp, N = p.shape
+    K = 2 * Kp
+    C = xb.shape[0] if xb.ndim == 2 else 1
+    if xb.size != C * K or s.size != N:
+        raise ValueError("shape mismatch")
+    b, e = (0, N) if cols is None else cols
+    d = np.full((C, N), np.nan)
+    ref = np.full((C, N), np.nan)
+    lib.w4o_gemv_packed(_ptr(p), _ptr(s), _ptr(xb), N, K, C, b, e, _ptr(d), _ptr(ref))
+    return d, ref
 
 
 def permute(packed, K, N):

@@ -169,6 +169,39 @@ void w4o_quantize_pack(const uint16_t* W, long K, long N, float* scale, uint8_t*
 }
 
 /*
+ * GEMV over the quantiser's packed matrix (the operand the permute turns
+ * into the fast-dequant layout).
+ *
+ * [P1 section "int4量化kernel"]: byte (k/2, n) of packed[K/2][N] holds rows
+ * k (low nibble) and k+1 (high nibble) of column n as two's complement int4;
+ * the column's weight is q[k][n] * scale[n] (symmetric per-column
+ * quantisation, fp32 scale).  [P4 section 3]: the batched product
+ * d[c][n] = sum_k W[k][n] x[c][k], x bf16 [C][K] row-major, stored d[c*N + n].
+ * Columns [col_begin, col_end) are computed; ref_abs (may be NULL) receives
+ * sum_k |w * x|.
+ */
+void w4o_gemv_packed(const uint8_t* packed, const float* scale, const uint16_t* x, long N, long K, long C,
+                     long col_begin, long col_end, double* d, double* ref_abs) {
+    for (long c = 0; c < C; ++c) {
+        for (long n = col_begin; n < col_end; ++n) {
+            double s = (double)scale[n];
+            double sum = 0.0, abs_sum = 0.0;
+            for (long k = 0; k < K; ++k) {
+                unsigned byte = packed[(k / 2) * N + n];
+                unsigned nib = (k % 2 == 0) ? (byte & 0x0Fu) : ((byte >> 4) & 0x0Fu);
+                int q = (nib >= 8u) ? (int)nib - 16 : (int)nib;
+                double w = (double)q * s;
+                double xv = (double)bf16_bits_to_float(x[c * K + k]);
+                sum += xv * w;
+                abs_sum += fabs(xv * w);
+            }
+            d[c * N + n] = sum;
+            if (ref_abs) ref_abs[c * N + n] = abs_sum;
+        }
+    }
+}
+
+/*
  * [P1 section "int4 permute kernel"]: destination of source byte t inside
  * each 16-byte group of a column's byte stream (the "coordinates" of the
  * mapping 0..15 -> 0 8 4 12 1 9 5 13 2 10 6 14 3 11 7 15).  Copied from the

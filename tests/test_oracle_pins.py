@@ -290,6 +290,80 @@ def test_gemv_row_range_and_linearity():
 # GEMM.
 # ---------------------------------------------------------------------------
 
+# ---------------------------------------------------------------------------
+# GEMV over the quantiser's packed matrix (the operand of the permuted path).
+# ---------------------------------------------------------------------------
+
+def _pack_cols(Q):
+    """Column pack of signed int4 Q [K, N]: byte (k/2, n) = (q[k] & 0xF) |
+    (q[k+1] & 0xF) << 4 (two rows per byte, even row low)."""
+    Q = np.asarray(Q)
+    lo = (Q[0::2] & 0xF).astype(np.uint8)
+    hi = (Q[1::2] & 0xF).astype(np.uint8)
+    return (lo | (hi << 4)).astype(np.uint8)
+
+
+def _signed_q(rng, K, N):
+    return rng.integers(-8, 8, (K, N))
+
+
+def test_gemv_packed_matches_dense_matmul():
+    rng = np.random.default_rng(21)
+    K, N, C = 64, 20, 3
+    Q = _signed_q(rng, K, N)
+    s = rng.uniform(0.01, 0.2, N).astype(np.float32)
+    x = bf16_bits(rng.normal(0, 1, (C, K)))
+    d, ref = oracle.gemv_packed(_pack_cols(Q), s, x)
+    W = Q * s.astype(np.float64)[None, :]
+    xv = bf16_values(x)
+    np.testing.assert_allclose(d, xv @ W, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(ref, np.abs(xv) @ np.abs(W), rtol=1e-12, atol=1e-12)
+
+
+def test_gemv_packed_agrees_with_row_gemv_at_zero_point_8():
+    """Two's complement q is the unsigned u = q + 8 with zero point 8: the
+    row-layout GEMV over the re-encoded words must give the same products."""
+    rng = np.random.default_rng(22)
+    K, N, C = 128, 12, 4
+    Q = _signed_q(rng, K, N)
+    s = rng.uniform(0.01, 0.2, N).astype(np.float32)
+    x = bf16_bits(rng.normal(0, 1, (C, K)))
+    d, _ = oracle.gemv_packed(_pack_cols(Q), s, x)
+    U = (Q + 8).T                     # [N, K], 0..15
+    d_row, _ = oracle.gemv(_pack_words(U), s, np.full(N, 8.0, np.float32),
+                           bf16_values(x).astype(np.float32), oracle.F32)
+    np.testing.assert_allclose(d, d_row, rtol=1e-12, atol=1e-12)
+
+
+def test_gemv_packed_one_hot_picks_signed_weight():
+    rng = np.random.default_rng(23)
+    K, N = 32, 8
+    Q = _signed_q(rng, K, N)
+    Q[5, 3], Q[6, 3] = -8, 7            # both ends of the range, both nibble positions
+    s = np.linspace(0.5, 2.0, N).astype(np.float32)
+    packed = _pack_cols(Q)
+    for k in range(K):
+        x = np.zeros((1, K), np.uint16)
+        x[0, k] = 0x3F80                # bf16 1.0
+        d, _ = oracle.gemv_packed(packed, s, x)
+        assert np.array_equal(d[0], Q[k] * s.astype(np.float64))
+
+
+def test_gemv_packed_of_quantised_matrix_is_within_half_step():
+    """d over quantize_pack's output differs from x @ W by at most
+    sum_k |x[k]| * scale[n] / 2 (each weight is off by at most half a step)."""
+    rng = np.random.default_rng(24)
+    K, N, C = 96, 10, 2
+    W = bf16_bits(rng.normal(0, 0.02, (K, N)))
+    scale, packed = oracle.quantize_pack(W)
+    x = bf16_bits(rng.normal(0, 1, (C, K)))
+    d, _ = oracle.gemv_packed(packed, scale, x)
+    xv = bf16_values(x)
+    exact = xv @ bf16_values(W)
+    bound = np.abs(xv).sum(axis=1)[:, None] * scale.astype(np.float64)[None, :] / 2
+    assert np.all(np.abs(d - exact) <= bound * (1 + 1e-9) + 1e-12)
+
+
 def test_gemm_matches_dense_matmul():
     rng = np.random.default_rng(5)
     M, N, K = 12, 20, 32
