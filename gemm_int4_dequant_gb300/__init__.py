@@ -9,6 +9,7 @@ in the library's CUDA kernels; there is no CPU or eager fallback.
     quantize_pack_int4(W)               -> (packed [K/2, N] int8, scale [N] fp32)
     permute_int4(packed)                -> out [N*K/2] int8 (interleaved)
     gemv_w4(qweight, scale, zero, x)    -> d [C, N]
+    gemv_w4_permuted(permuted, scale, x) -> d [C, N] bf16 (over permute_int4's output)
     gemm_w4(A, B, scale, zero)          -> C [M, N] bf16
 """
 import torch
@@ -16,7 +17,8 @@ import torch
 from . import _lib
 from ._lib import W4Error, W4_BF16, W4_F32
 
-__all__ = ["quantize_pack_int4", "permute_int4", "gemv_w4", "gemm_w4", "device_error", "W4Error"]
+__all__ = ["quantize_pack_int4", "permute_int4", "gemv_w4", "gemv_w4_permuted", "gemm_w4", "device_error",
+           "W4Error"]
 
 _lib.load()  # fail loudly at import if the CUDA library is missing
 
@@ -101,6 +103,31 @@ def gemv_w4(qweight, scale, zero, x, out=None, stream=None):
     st = _lib.load().gemv_w4(qweight.data_ptr(), scale.data_ptr(), zero.data_ptr(), xx.data_ptr(), out.data_ptr(),
                              N, K, C, W4_F32 if dt == torch.float32 else W4_BF16, _stream(stream))
     _lib.check("gemv_w4", st)
+    return out
+
+
+def gemv_w4_permuted(permuted, scale, x, out=None, stream=None):
+    """d[c, n] = sum_k q[k, n] * scale[n] * x[c, k] over permute_int4's output.
+
+    permuted: int8/uint8 with N*K/2 bytes; scale: fp32 [N] (quantize_pack_int4's);
+    x: bf16 [C, K] (C <= 8).  Returns bf16 [C, N].
+    """
+    _need(permuted, "permuted", (torch.int8, torch.uint8))
+    _need(scale, "scale", (torch.float32,), 1)
+    _need(x, "x", (torch.bfloat16,))
+    xx = x if x.dim() == 2 else x.reshape(1, -1)
+    C, K = xx.shape
+    N = scale.numel()
+    if permuted.numel() * 2 != N * K:
+        raise ValueError("permuted must hold N*K/2 bytes (N = scale.numel(), K = x.shape[-1])")
+    if out is None:
+        out = torch.empty((C, N), dtype=torch.bfloat16, device=x.device)
+    _need(out, "out", (torch.bfloat16,))
+    if out.numel() != C * N:
+        raise ValueError("out must hold C*N elements")
+    st = _lib.load().gemv_w4_permuted(permuted.data_ptr(), scale.data_ptr(), xx.data_ptr(), out.data_ptr(),
+                                      N, K, C, _stream(stream))
+    _lib.check("gemv_w4_permuted", st)
     return out
 
 

@@ -45,6 +45,8 @@ def load():
     lib.permute_int4.restype = I
     lib.gemv_w4.argtypes = [P, P, P, P, P, I64, I64, I64, I, P]
     lib.gemv_w4.restype = I
+    lib.gemv_w4_permuted.argtypes = [P, P, P, P, I64, I64, I64, P]
+    lib.gemv_w4_permuted.restype = I
     lib.gemm_w4.argtypes = [P, P, P, P, P, I64, I64, I64, P]
     lib.gemm_w4.restype = I
     _lib = lib

@@ -116,10 +116,14 @@ __host__ __device__ inline Layout make_layout(int C, const Plan& P) {
     return L;
 }
 
-template <int C>
+// PERM = false: weights uint32 [N][K/8] (rows of eight nibbles per word),
+// bf16 scale and zero per row.  PERM = true: weights in the permuted layout
+// of permute_int4 (column groups of 4, 128-byte lines of 64 k, two's
+// complement nibbles), fp32 scale per column and no zero point.
+template <int C, bool PERM>
 __global__ void __launch_bounds__(THREADS, 1)
-gemv_tma_kernel(const uint8_t* __restrict__ qw, const __nv_bfloat16* __restrict__ scale,
-                const __nv_bfloat16* __restrict__ zero, const __nv_bfloat16* __restrict__ x,
+gemv_tma_kernel(const uint8_t* __restrict__ qw, const void* __restrict__ scale,
+                const void* __restrict__ zero, const __nv_bfloat16* __restrict__ x,
                 __nv_bfloat16* __restrict__ d, int N, int K, Plan P, MaskMagic dq,
                 const __grid_constant__ CUtensorMap tm16, const __grid_constant__ CUtensorMap tm4) {
     extern __shared__ uint8_t smem_raw[];
@@ -155,6 +159,16 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const __nv_bfloat16* __restrict_
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L.abort);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // (scale, zero) of output row r; the permuted operand is symmetric and
+    // its nibbles are read as 8 + q, which the fold treats as zero point 8
+    auto load_sz = [&](int r) -> float2 {
+        if constexpr (PERM) {
+            return make_float2(static_cast<const float*>(scale)[r], 8.0f);
+        } else {
+            return make_float2(__bfloat162float(static_cast<const __nv_bfloat16*>(scale)[r]),
+                               __bfloat162float(static_cast<const __nv_bfloat16*>(zero)[r]));
+        }
+    };
 
     if (tid == 0) {
         for (int s = 0; s < NST; ++s) {
@@ -169,7 +183,12 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const __nv_bfloat16* __restrict_
     // device's point of coherence, so a prefetch cannot yield stale data even
     // if the previous kernel writes these bytes; every load into shared
     // memory or registers is issued only after the wait.
-    if (warp == NC && lane == 0) {
+    if (PERM && warp == NC && lane == 0 && nstages > 0) {
+        // the first stage: each column group's first lines
+        const uint32_t gbytes = (min(P.kchunk, klen) + 63) / 64 * 128;
+        for (int gi = 0; gi < min(16, nrows) / 4; ++gi)
+            bulk_prefetch_l2(qw + static_cast<int64_t>(r0 / 4 + gi) * 2 * K + (k0 / 64) * 128, gbytes);
+    } else if (warp == NC && lane == 0) {
         const int64_t row_bytes = K / 2;
         const uint8_t* src0 = qw + static_cast<int64_t>(r0) * row_bytes + k0 / 2;
         int tile = 0, ch = 0;
@@ -201,7 +220,20 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const __nv_bfloat16* __restrict_
                 const int seg = min(P.kchunk, klen - ch * P.kchunk) / 2;   // bytes per row (multiple of 16)
                 const uint32_t dst = sm_addr + slot * L.stage_bytes;
                 const uint8_t* src = src0 + static_cast<int64_t>(tile) * 16 * row_bytes + ch * (P.kchunk / 2);
-                if (P.tmap) {
+                if constexpr (PERM) {
+                    // one bulk copy per column group: its lines of this K-chunk
+                    // (128 bytes = 64 k of 4 columns each), at a group stride of
+                    // 16 mod 128 bytes so that ldmatrix rows hit distinct banks
+                    const int len = min(P.kchunk, klen - ch * P.kchunk);   // multiple of 64
+                    const uint32_t gbytes = len / 64 * 128;
+                    const int ng = rows_here / 4;
+                    const uint8_t* g0 = qw + static_cast<int64_t>(r0 / 4 + tile * 4) * 2 * K +
+                                        ((k0 + ch * P.kchunk) / 64) * 128;
+                    mbar_arrive_expect_tx(bar_full + 8 * slot, ng * gbytes);
+                    for (int gi = 0; gi < ng; ++gi)
+                        bulk_load_hint(dst + gi * 4 * pitch, g0 + static_cast<int64_t>(gi) * 2 * K, gbytes,
+                                       bar_full + 8 * slot, policy);
+                } else if (P.tmap) {
                     const int c0 = (k0 + ch * P.kchunk) / 128, row0 = r0 + tile * 16;
                     if (rows_here == 16) {
                         mbar_arrive_expect_tx(bar_full + 8 * slot, 16 * pitch);
@@ -233,11 +265,11 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const __nv_bfloat16* __restrict_
         // scale / zero of this CTA's rows: the first two per thread are loaded
         // now into registers (nothing waits on them) and stored after the
         // main loop, so their latency never delays the start
-        __nv_bfloat16 sc_pf[2], zr_pf[2];
+        float2 sz_pf[2];
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
             const int i = tid + j * CT;
-            if (i < nrows) { sc_pf[j] = scale[r0 + i]; zr_pf[j] = zero[r0 + i]; }
+            if (i < nrows) sz_pf[j] = load_sz(r0 + i);
         }
         // x as B fragments: entry (kb, word p, n, t4) holds, for kk = kb*128 +
         // 32*t4 + 8*p, the bf16 pairs (x[kk], x[kk+4]) (x[kk+1], x[kk+5])
@@ -247,7 +279,7 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const __nv_bfloat16* __restrict_
         const bool bl = g < C;
         const uint4* xlane = bl ? xf + g * 4 + t4 : xzero + t4;
         constexpr int xw_stride = C * 4;
-        if constexpr (C == 1) {
+        if constexpr (!PERM && C == 1) {
             // one column: a thread adds the eight values of each entry it
             // stages (a few adds per entry, against up to eight columns' worth
             // of conversions and selects per entry in the general case)
@@ -309,6 +341,51 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const __nv_bfloat16* __restrict_
             // (n-major), stepping (n, j) without dividing, XB loads in
             // flight; the column sums are left to the tensor cores
             const int nkb = (klen + KB - 1) / KB;
+            if constexpr (PERM) {
+                // permuted operand: the fragment of 32-k group m pairs k =
+                // 32m + 2t4 + 8i (i = 0..3), i.e. word t4 of each 16-byte piece
+                // of the group -- a 4x4 word transpose of 64 bytes of x.  Every
+                // group of every unit is written (zeros past the slice) because
+                // the last unit of a row may be half full.
+                const int per_n = nkb * 4;
+                constexpr int XB = 2;
+                const int dn = per_n > 0 ? CT / per_n : 0, dj = CT - dn * per_n;
+                int n_cur = per_n > 0 ? tid / per_n : C, j_cur = tid - n_cur * per_n;
+                while (n_cur < C) {
+                    uint4 raw[XB][4];
+                    int n = n_cur, j = j_cur;
+#pragma unroll
+                    for (int b = 0; b < XB; ++b) {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            raw[b][i] = make_uint4(0, 0, 0, 0);
+                            if (n < C && 32 * j + 8 * i < klen)
+                                raw[b][i] = *reinterpret_cast<const uint4*>(x + static_cast<int64_t>(n) * K + k0 +
+                                                                            32 * j + 8 * i);
+                        }
+                        j += dj;
+                        n += dn;
+                        if (j >= per_n) { j -= per_n; ++n; }
+                    }
+                    n = n_cur;
+                    j = j_cur;
+#pragma unroll
+                    for (int b = 0; b < XB; ++b) {
+                        if (n < C) {
+                            uint4* e = xf + (j * C + n) * 4;
+                            e[0] = make_uint4(raw[b][0].x, raw[b][1].x, raw[b][2].x, raw[b][3].x);
+                            e[1] = make_uint4(raw[b][0].y, raw[b][1].y, raw[b][2].y, raw[b][3].y);
+                            e[2] = make_uint4(raw[b][0].z, raw[b][1].z, raw[b][2].z, raw[b][3].z);
+                            e[3] = make_uint4(raw[b][0].w, raw[b][1].w, raw[b][2].w, raw[b][3].w);
+                        }
+                        j += dj;
+                        n += dn;
+                        if (j >= per_n) { j -= per_n; ++n; }
+                    }
+                    n_cur = n;
+                    j_cur = j;
+                }
+            } else {
             const int per_n = nkb * 16;
             constexpr int XB = 8;
             const int dn = per_n > 0 ? CT / per_n : 0, dj = CT - dn * per_n;
@@ -345,6 +422,7 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const __nv_bfloat16* __restrict_
                 }
                 n_cur = n;
                 j_cur = j;
+            }
             }
             for (int i = tid; i < 16 * C; i += CT) xzero[i] = make_uint4(0, 0, 0, 0);
             named_barrier(1, CT);
@@ -387,6 +465,13 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const __nv_bfloat16* __restrict_
         const int xkb_stride = bl ? 4 * C * 4 : 0;
         const uint32_t mask = dq.mask, magic = dq.magic;
         const int row_off_a = g * pitch + 16 * t4, row_off_b = (g + 8) * pitch + 16 * t4;
+        // permuted operand: this lane's ldmatrix row -- column r + 8*(i & 1)
+        // of matrix i = lane / 8 (r = lane % 8), 32-k group +(i >> 1); the
+        // column groups sit 4*pitch apart, lines of 128 bytes, 32 bytes per column
+        const int ldm_col = (lane & 7) + 8 * ((lane >> 3) & 1);
+        const uint32_t ldm_off = (ldm_col >> 2) * 4 * pitch + (ldm_col & 3) * 32 + (lane >> 4) * 16;
+        // nibble -> bf16 (128 + q, or 136 + q for two's complement nibbles)
+        auto unpack = [&](uint32_t v) { return PERM ? pass_flip_or(v, mask, magic) : and_or(v, mask, magic); };
         int slot = 0, round = 0, first = warp;   // first unit of this warp in the current stage
         const int rows16 = (P.rows_cap + 15) / 16 * 16;
         for (int tile = 0; tile < ntiles; ++tile) {
@@ -397,22 +482,26 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const __nv_bfloat16* __restrict_
                 if (ok) {
                     const uint8_t* st = sm + slot * L.stage_bytes;
                     for (int u = first; u < units; u += NC) {
-                        const uint4 wa = *reinterpret_cast<const uint4*>(st + row_off_a + u * 64);
-                        const uint4 wb = *reinterpret_cast<const uint4*>(st + row_off_b + u * 64);
                         const uint4* xb = xlane + (ch * (P.kchunk / KB) + u) * xkb_stride;
-                        const uint32_t wav[4] = {wa.x, wa.y, wa.z, wa.w};
-                        const uint32_t wbv[4] = {wb.x, wb.y, wb.z, wb.w};
+                        uint32_t wav[4], wbv[4];
+                        if constexpr (PERM) {
+                            // words of columns g and g+8 for the unit's four 32-k groups
+                            const uint32_t a = smem_u32(st) + ldm_off + u * 256;
+                            ldmatrix_x4(a, wav[0], wbv[0], wav[1], wbv[1]);
+                            ldmatrix_x4(a + 128, wav[2], wbv[2], wav[3], wbv[3]);
+                        } else {
+                            const uint4 wa = *reinterpret_cast<const uint4*>(st + row_off_a + u * 64);
+                            const uint4 wb = *reinterpret_cast<const uint4*>(st + row_off_b + u * 64);
+                            wav[0] = wa.x; wav[1] = wa.y; wav[2] = wa.z; wav[3] = wa.w;
+                            wbv[0] = wb.x; wbv[1] = wb.y; wbv[2] = wb.z; wbv[3] = wb.w;
+                        }
 #pragma unroll
                         for (int w = 0; w < 4; ++w) {
                             const uint4 bx = xb[w * xw_stride];
                             const uint32_t va = wav[w], vb = wbv[w];
-                            const uint32_t a0[4] = {and_or(va, mask, magic), and_or(vb, mask, magic),
-                                                    and_or((va >> 4), mask, magic),
-                                                    and_or((vb >> 4), mask, magic)};
-                            const uint32_t a1[4] = {and_or((va >> 8), mask, magic),
-                                                    and_or((vb >> 8), mask, magic),
-                                                    and_or((va >> 12), mask, magic),
-                                                    and_or((vb >> 12), mask, magic)};
+                            const uint32_t a0[4] = {unpack(va), unpack(vb), unpack(va >> 4), unpack(vb >> 4)};
+                            const uint32_t a1[4] = {unpack(va >> 8), unpack(vb >> 8), unpack(va >> 12),
+                                                    unpack(vb >> 12)};
                             mma_bf16(acc, a0, bx.x, bx.y);
                             mma_bf16(acc2, a1, bx.z, bx.w);
                         }
@@ -450,10 +539,9 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const __nv_bfloat16* __restrict_
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
             const int i = tid + j * CT;
-            if (i < nrows) sz[i] = make_float2(__bfloat162float(sc_pf[j]), __bfloat162float(zr_pf[j]));
+            if (i < nrows) sz[i] = sz_pf[j];
         }
-        for (int i = tid + 2 * CT; i < nrows; i += CT)
-            sz[i] = make_float2(__bfloat162float(scale[r0 + i]), __bfloat162float(zero[r0 + i]));
+        for (int i = tid + 2 * CT; i < nrows; i += CT) sz[i] = load_sz(r0 + i);
         if (P.perwarp) {
             named_barrier(1, CT);
             for (int i = tid; i < nrows * C; i += CT) {
@@ -511,11 +599,11 @@ constexpr int kSmemMax = 227 * 1024;
 constexpr size_t kXfBudget = 80 * 1024;
 
 // Pipeline shape for (N, K, C) on `sms` SMs; nst == 0 if nothing fits.
-template <int C>
+template <int C, bool PERM>
 Plan make_plan(int N, int K, int sms, int max_clusters_for_S /* 0: unknown */, int S_forced) {
     Plan P{};
-    const int tm = (K % 128 == 0) ? 1 : 0;   // rows are whole 64-byte chunks
-    const int sgran = tm ? 128 : 32;
+    const int tm = (!PERM && K % 128 == 0) ? 1 : 0;   // rows are whole 64-byte chunks
+    const int sgran = (tm || PERM) ? 128 : 32;
     auto slice_of = [&](int s) { return ((K + s - 1) / s + sgran - 1) / sgran * sgran; };
     auto xf_bytes = [&](int s) { return static_cast<size_t>((slice_of(s) + KB - 1) / KB) * 16 * C * 16; };
     int S = 1;
@@ -533,9 +621,12 @@ Plan make_plan(int N, int K, int sms, int max_clusters_for_S /* 0: unknown */, i
         const int nch0 = (P.kslice + KCHUNK_MAX - 1) / KCHUNK_MAX;  // chunks of about equal size
         P.kchunk = ((P.kslice + nch0 - 1) / nch0 + KB - 1) / KB * KB;
     }
-    P.dense = (S == 1 && P.kchunk >= K) ? 1 : 0;
+    P.dense = (!PERM && S == 1 && P.kchunk >= K) ? 1 : 0;
     P.tmap = tm;
-    if (tm) {
+    if (PERM) {
+        // four column groups of kchunk/64 lines each, 16 mod 128 bytes apart
+        P.pitch = 32 * (P.kchunk / 64) + 4;
+    } else if (tm) {
         P.nbox = (P.kchunk / 128) | 1;
         P.pitch = P.nbox * 64;
     } else if (P.dense) {
@@ -556,14 +647,14 @@ Plan make_plan(int N, int K, int sms, int max_clusters_for_S /* 0: unknown */, i
     return P;
 }
 
-template <int C>
+template <int C, bool PERM>
 w4_status launch_gemv_tma_t(const void* qw, const void* scale, const void* zero, const void* x, void* d, int N,
                             int K, cudaStream_t stream) {
     const int sms = sm_count();
     if (sms <= 0) return W4_ERR_CUDA;
-    Plan P = make_plan<C>(N, K, sms, 0, 0);
+    Plan P = make_plan<C, PERM>(N, K, sms, 0, 0);
     if (P.nst == 0) return W4_ERR_SHAPE;
-    auto kern = gemv_tma_kernel<C>;
+    auto kern = gemv_tma_kernel<C, PERM>;
     static int smem_set[64];
     cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3(THREADS, 1, 1);
@@ -593,7 +684,7 @@ w4_status launch_gemv_tma_t(const void* qw, const void* scale, const void* zero,
             if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) return W4_ERR_CUDA;
             max_clusters[dev][si] = n;
         }
-        P = make_plan<C>(N, K, sms, max_clusters[dev][si], P.S);
+        P = make_plan<C, PERM>(N, K, sms, max_clusters[dev][si], P.S);
         if (P.nst == 0) return W4_ERR_SHAPE;
         e = ensure_smem_limit(kern, make_layout(C, P).total + 1024, smem_set);
         if (e != cudaSuccess) return W4_ERR_CUDA;
@@ -617,9 +708,12 @@ w4_status launch_gemv_tma_t(const void* qw, const void* scale, const void* zero,
                 return W4_ERR_CUDA;
         }
     }
-    e = cudaLaunchKernelEx(&cfg, kern, static_cast<const uint8_t*>(qw), static_cast<const __nv_bfloat16*>(scale),
-                           static_cast<const __nv_bfloat16*>(zero), static_cast<const __nv_bfloat16*>(x),
-                           static_cast<__nv_bfloat16*>(d), N, K, P, MaskMagic{0x000F000Fu, 0x43004300u}, tm16, tm4);
+    // row layout: (v & 0x000F000F) | 0x43004300; permuted (two's complement):
+    // pass bits 0-2, invert bit 3, set the exponent of 128.0
+    const MaskMagic dq = PERM ? MaskMagic{0x43074307u, 0x43084308u} : MaskMagic{0x000F000Fu, 0x43004300u};
+    e = cudaLaunchKernelEx(&cfg, kern, static_cast<const uint8_t*>(qw), scale, zero,
+                           static_cast<const __nv_bfloat16*>(x), static_cast<__nv_bfloat16*>(d), N, K, P, dq, tm16,
+                           tm4);
     return launch_status(e);
 }
 
@@ -629,14 +723,30 @@ w4_status launch_gemv_tma_t(const void* qw, const void* scale, const void* zero,
 w4_status run_gemv_tma(const void* qw, const void* scale, const void* zero, const void* x, void* d, int N, int K,
                        int C, cudaStream_t stream) {
     switch (C) {
-        case 1: return launch_gemv_tma_t<1>(qw, scale, zero, x, d, N, K, stream);
-        case 2: return launch_gemv_tma_t<2>(qw, scale, zero, x, d, N, K, stream);
-        case 3: return launch_gemv_tma_t<3>(qw, scale, zero, x, d, N, K, stream);
-        case 4: return launch_gemv_tma_t<4>(qw, scale, zero, x, d, N, K, stream);
-        case 5: return launch_gemv_tma_t<5>(qw, scale, zero, x, d, N, K, stream);
-        case 6: return launch_gemv_tma_t<6>(qw, scale, zero, x, d, N, K, stream);
-        case 7: return launch_gemv_tma_t<7>(qw, scale, zero, x, d, N, K, stream);
-        case 8: return launch_gemv_tma_t<8>(qw, scale, zero, x, d, N, K, stream);
+        case 1: return launch_gemv_tma_t<1, false>(qw, scale, zero, x, d, N, K, stream);
+        case 2: return launch_gemv_tma_t<2, false>(qw, scale, zero, x, d, N, K, stream);
+        case 3: return launch_gemv_tma_t<3, false>(qw, scale, zero, x, d, N, K, stream);
+        case 4: return launch_gemv_tma_t<4, false>(qw, scale, zero, x, d, N, K, stream);
+        case 5: return launch_gemv_tma_t<5, false>(qw, scale, zero, x, d, N, K, stream);
+        case 6: return launch_gemv_tma_t<6, false>(qw, scale, zero, x, d, N, K, stream);
+        case 7: return launch_gemv_tma_t<7, false>(qw, scale, zero, x, d, N, K, stream);
+        case 8: return launch_gemv_tma_t<8, false>(qw, scale, zero, x, d, N, K, stream);
+        default: return W4_ERR_SHAPE;
+    }
+}
+
+// bf16 GEMV over permute_int4's output; requires K % 64 == 0, N % 4 == 0.
+w4_status run_gemv_permuted(const void* permuted, const float* scale, const void* x, void* d, int N, int K, int C,
+                            cudaStream_t stream) {
+    switch (C) {
+        case 1: return launch_gemv_tma_t<1, true>(permuted, scale, nullptr, x, d, N, K, stream);
+        case 2: return launch_gemv_tma_t<2, true>(permuted, scale, nullptr, x, d, N, K, stream);
+        case 3: return launch_gemv_tma_t<3, true>(permuted, scale, nullptr, x, d, N, K, stream);
+        case 4: return launch_gemv_tma_t<4, true>(permuted, scale, nullptr, x, d, N, K, stream);
+        case 5: return launch_gemv_tma_t<5, true>(permuted, scale, nullptr, x, d, N, K, stream);
+        case 6: return launch_gemv_tma_t<6, true>(permuted, scale, nullptr, x, d, N, K, stream);
+        case 7: return launch_gemv_tma_t<7, true>(permuted, scale, nullptr, x, d, N, K, stream);
+        case 8: return launch_gemv_tma_t<8, true>(permuted, scale, nullptr, x, d, N, K, stream);
         default: return W4_ERR_SHAPE;
     }
 }

@@ -304,6 +304,26 @@ __device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t b, uint32_t c) {
     return d;
 }
 
+// (a & b & ~c) | (~a & ~b & c) | (b & c) in one LOP3.  With b holding the
+// bits to pass plus a magic exponent and c the bit to invert plus the same
+// exponent, a two's complement nibble q in bits 0..3 of each half becomes
+// the bf16 value 136 + q (q ^ 8 = q + 8 in the mantissa of 128.0).
+__device__ __forceinline__ uint32_t pass_flip_or(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0xCA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+// Four 8x8 b16 matrices from shared memory: lanes 8i..8i+7 give the row
+// addresses of matrix i; lane 4g+t receives row g, elements 2t and 2t+1 of
+// each matrix (one 32-bit word per matrix).
+__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& d0, uint32_t& d1, uint32_t& d2, uint32_t& d3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(d0), "=r"(d1), "=r"(d2), "=r"(d3)
+                 : "r"(addr)
+                 : "memory");
+}
+
 // Wait with the common case (already complete) inline and the bounded
 // polling loop out of line.
 __device__ __forceinline__ bool mbar_wait_fast(uint32_t bar, uint32_t parity, volatile int* abort_flag) {

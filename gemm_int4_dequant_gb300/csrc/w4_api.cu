@@ -14,6 +14,8 @@ w4_status run_gemv(const void* qw, const void* scale, const void* zero, const vo
                    int64_t K, int64_t C, w4_dtype dtype, cudaStream_t s);
 w4_status run_gemm(const void* A, const void* B, const void* scale, const void* zero, void* C, int64_t M,
                    int64_t N, int64_t K, cudaStream_t s);
+w4_status run_gemv_permuted(const void* permuted, const float* scale, const void* x, void* d, int N, int K, int C,
+                            cudaStream_t s);
 int take_device_error_gemm();
 int take_device_error_gemv();
 int take_device_error_quant();
@@ -124,6 +126,20 @@ w4_status gemv_w4(const void* qweight, const void* scale, const void* zero, cons
     const size_t esz = dtype == W4_F32 ? 4 : 2;
     if (K == 0) return launch_status(cudaMemsetAsync(d, 0, C * N * esz, (cudaStream_t)stream));
     return run_gemv(qweight, scale, zero, x, d, N, K, C, dtype, (cudaStream_t)stream);
+}
+
+w4_status gemv_w4_permuted(const void* permuted, const float* scale, const void* x, void* d, int64_t N, int64_t K,
+                          int64_t C, void* stream) {
+    if (N < 0 || K < 0 || (K % 64) != 0 || (N % 4) != 0 || K > W4_GEMV_MAX_K || C < 1 || C > 8 ||
+        N > (int64_t(1) << 30))
+        return W4_ERR_SHAPE;
+    if (N == 0) return W4_OK;
+    if (!d || !scale || (K > 0 && (!permuted || !x))) return W4_ERR_NULL;
+    if (!aligned16(d) || !aligned16(scale) || (K > 0 && (!aligned16(permuted) || !aligned16(x)))) return W4_ERR_ALIGN;
+    if (!device_is_sm103()) return W4_ERR_DEVICE;
+    if (K == 0) return launch_status(cudaMemsetAsync(d, 0, C * N * 2, (cudaStream_t)stream));
+    return run_gemv_permuted(permuted, scale, x, d, static_cast<int>(N), static_cast<int>(K), static_cast<int>(C),
+                             (cudaStream_t)stream);
 }
 
 w4_status gemm_w4(const void* A, const void* B, const void* scale, const void* zero, void* C, int64_t M, int64_t N,

@@ -14,6 +14,9 @@
  *                       d[c][r] = sum_k (q[r][k] - zero[r]) * scale[r] * x[c][k]
  *                       ("怎样在安卓端利用 Vulkan 编写 4-bit 专用算子", sections 1
  *                       and 2; batched form from "三值量化模型的无损压缩", section 3).
+ *   gemv_w4_permuted    the same multiply over permute_int4's output (the
+ *                       interleaved layout the page builds for the fast
+ *                       int4 -> 16-bit dequant), symmetric per-column scale.
  *   gemm_w4             large-M bf16 x int4 dequant GEMM
  *                       ("int4 gemm kernel", the matmul_bf16_int4 example).
  *
@@ -139,6 +142,31 @@ w4_status permute_int4(const void* packed, void* out, int64_t K, int64_t N, void
  */
 w4_status gemv_w4(const void* qweight, const void* scale, const void* zero, const void* x, void* d,
                   int64_t N, int64_t K, int64_t C, w4_dtype dtype, void* stream);
+
+/*
+ * gemv_w4_permuted -- multiply by the quantiser's weights in the permuted
+ * layout, without undoing the permute.
+ *
+ *   d[c][n] = sum_k q[k][n] * scale[n] * x[c][k],  0 <= c < C
+ *
+ * ("[PHI] add int4 weight only quant kernel, add int4 weight only permute
+ * kernel", sections "int4量化kernel" and "int4 permute kernel": q is the
+ * two's complement int4 of quantize_pack_int4, permute_int4 arranges it so
+ * that one shift-and-mask per pair yields the values in the order the MMA
+ * fragments take them.)
+ *
+ * permuted  N*K/2 bytes, the output of permute_int4 for the packed
+ *           [K/2][N] matrix (column groups of 4, 128-byte lines of 64 k).
+ * scale     fp32 [N] (quantize_pack_int4's scale).
+ * x         bf16 [C][K] row-major.
+ * d         bf16 [C][N] row-major (output).
+ * All pointers 16-byte aligned.  K % 64 == 0 and N % 4 == 0 (the permute's
+ * own requirements), K <= W4_GEMV_MAX_K, 1 <= C <= 8; else W4_ERR_SHAPE.
+ * K == 0 gives d = 0.  fp32 accumulation, one bf16 rounding; the tolerance
+ * is gemv_w4's (2e-3 * sum_k |w*x|).
+ */
+w4_status gemv_w4_permuted(const void* permuted, const float* scale, const void* x, void* d, int64_t N, int64_t K,
+                           int64_t C, void* stream);
 
 /*
  * gemm_w4 -- large-M bf16 x int4 dequant GEMM on the tcgen05 tensor cores.

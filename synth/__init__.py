@@ -66,6 +66,30 @@ def gemv_inputs(N, K, C, act="bf16", seed=0, scale_range=None, zero_value=8.0):
     return GemvInputs(qweight, scale, zero, x, N, K, C, act)
 
 
+@dataclass
+class PackedGemvInputs:
+    packed: torch.Tensor  # uint8 [K/2, N]: two two's complement nibbles per byte along K
+    scale: torch.Tensor   # float32 [N]
+    x: torch.Tensor       # bf16 [C, K]
+    N: int
+    K: int
+    C: int
+
+
+def packed_gemv_inputs(N, K, C, seed=0, scale_range=(0.005, 0.02)):
+    """The quantiser's operand layout: uniform random bytes (= independent
+    uniform nibbles), fp32 per-column scale in the range the quantiser gives
+    for N(0, 0.02) weights, x ~ N(0,1) bf16."""
+    if K % 2:
+        raise ValueError("K must be even")
+    g = _gen(seed)
+    packed = torch.randint(0, 256, (K // 2, N), dtype=torch.uint8, generator=g)
+    lo, hi = scale_range
+    scale = torch.rand(N, generator=g, dtype=torch.float32) * (hi - lo) + lo
+    x = torch.randn(C, K, generator=g, dtype=torch.float32).to(torch.bfloat16)
+    return PackedGemvInputs(packed, scale, x, N, K, C)
+
+
 def quant_inputs(K, N, seed=0, std=0.02):
     """W bf16 [K, N] ~ N(0, std)."""
     g = _gen(seed)

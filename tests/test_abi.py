@@ -26,8 +26,8 @@ def _declared_functions():
 
 def test_header_declares_the_hot_path():
     names = _declared_functions()
-    for fn in ("quantize_pack_int4", "permute_int4", "gemv_w4", "gemm_w4", "w4_status_string",
-               "w4_abi_version", "w4_device_error"):
+    for fn in ("quantize_pack_int4", "permute_int4", "gemv_w4", "gemv_w4_permuted", "gemm_w4",
+               "w4_status_string", "w4_abi_version", "w4_device_error"):
         assert fn in names
 
 
@@ -76,6 +76,14 @@ def test_argument_validation_happens_on_host():
     assert lib.gemv_w4(A, A, None, A, A, 16, 16, 1, L.W4_F32, None) == L.W4_ERR_NULL
     assert lib.gemv_w4(A, A, A, odd, A, 16, 16, 1, L.W4_F32, None) == L.W4_ERR_ALIGN
     assert lib.gemv_w4(A, A, A, A, A, 0, 16, 1, L.W4_F32, None) == L.W4_OK
+    # gemv_w4_permuted: the permute's shape rules, C and the K limit
+    assert lib.gemv_w4_permuted(A, A, A, A, 16, 96, 1, None) == L.W4_ERR_SHAPE       # K % 64
+    assert lib.gemv_w4_permuted(A, A, A, A, 18, 128, 1, None) == L.W4_ERR_SHAPE      # N % 4
+    assert lib.gemv_w4_permuted(A, A, A, A, 16, 128, 9, None) == L.W4_ERR_SHAPE
+    assert lib.gemv_w4_permuted(A, A, A, A, 16, 40960 + 64, 1, None) == L.W4_ERR_SHAPE
+    assert lib.gemv_w4_permuted(A, A, A, A, 0, 128, 1, None) == L.W4_OK
+    assert lib.gemv_w4_permuted(A, None, A, A, 16, 128, 1, None) == L.W4_ERR_NULL
+    assert lib.gemv_w4_permuted(odd, A, A, A, 16, 128, 1, None) == L.W4_ERR_ALIGN
     # gemm_w4
     assert lib.gemm_w4(A, A, A, A, A, 128, 256, 100, None) == L.W4_ERR_SHAPE
     assert lib.gemm_w4(A, A, A, A, A, 128, 250, 128, None) == L.W4_ERR_SHAPE

@@ -182,6 +182,55 @@ def test_gemv_through_raw_c_abi(w4):
 
 
 # ---------------------------------------------------------------------------
+# gemv_w4_permuted (permute_int4's output consumed directly)
+# ---------------------------------------------------------------------------
+
+def _check_gemv_permuted(w4, N, K, C, seed):
+    g = synth.packed_gemv_inputs(N, K, C, seed=seed)
+    perm = w4.permute_int4(g.packed.to(_dev()))
+    buf, out, pad = _guarded(C * N, torch.bfloat16, -7.0)
+    w4.gemv_w4_permuted(perm, g.scale.to(_dev()), g.x.to(_dev()), out=out)
+    ref, ref_abs = oracle.gemv_packed(g.packed.numpy(), g.scale.numpy(), np_bits(g.x))
+    got = out.float().cpu().numpy().astype(np.float64).reshape(C, N)
+    bad = parity_violations(got, ref, ref_abs, BF16_TOL, bf16_out=True)
+    err = np.abs(got - ref)
+    assert not bad.any(), "max err/ref_abs = %g at %s" % ((err / ref_abs).max(), np.argwhere(bad)[:5])
+    assert _guards_intact(buf, pad, C * N, -7.0)
+
+
+@pytest.mark.parametrize("N,K,C", [
+    (4, 64, 1),          # one column group, one line
+    (12, 128, 3),        # three groups: a partial 16-column tile
+    (100, 192, 8),       # 6 full tiles and a 4-column one; K % 128 == 64 (half unit)
+    (1000, 512, 2),
+    (4096, 4160, 5),     # a half unit at the end of every row
+    (260, 40960, 8),     # x split over an eight-CTA cluster
+    (17280, 5120, 1),    # decode shape
+    (5120, 17280, 4),    # small-batch shapes of the pages' workloads
+    (5120, 17280, 8),
+    (6144, 5120, 4),
+    (6144, 5120, 8),
+])
+def test_gemv_permuted(w4, N, K, C):
+    _check_gemv_permuted(w4, N, K, C, seed=N + K + C)
+
+
+def test_quantize_permute_gemv_chain(w4):
+    """W -> quantize_pack_int4 -> permute_int4 -> gemv_w4_permuted against the
+    oracle GEMV over the oracle's own quantised matrix."""
+    K, N, C = 2048, 1024, 4
+    W = synth.quant_inputs(K, N, seed=7)
+    x = synth.packed_gemv_inputs(N, K, C, seed=8).x
+    packed, scale = w4.quantize_pack_int4(W.to(_dev()))
+    out = w4.gemv_w4_permuted(w4.permute_int4(packed), scale, x.to(_dev()))
+    s_ref, p_ref = oracle.quantize_pack(np_bits(W))
+    ref, ref_abs = oracle.gemv_packed(p_ref, s_ref, np_bits(x))
+    got = out.float().cpu().numpy().astype(np.float64)
+    assert not parity_violations(got, ref, ref_abs, BF16_TOL, bf16_out=True).any()
+    assert w4.device_error() == 0
+
+
+# ---------------------------------------------------------------------------
 # gemm_w4
 # ---------------------------------------------------------------------------
 
