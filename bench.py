@@ -5,8 +5,9 @@ scale, zero and output; uint4 weights packed eight per uint32), the
 configuration the headline metric "int4 W-only GEMV HBM GB/s" is quoted
 on.  One step = one gemv_w4 call on one batch.  The line also carries the
 other kernels of the hot path as components: the small-batch GEMVs (C = 4,
-8), quantise+pack+permute of an 8192x8192 bf16 weight, and the 8192^3
-bf16 x int4 dequant GEMM (TFLOP/s).
+8), the same GEMVs over permute_int4's output (gemv_w4_permuted),
+quantise+pack+permute of an 8192x8192 bf16 weight, and the 8192^3 bf16 x
+int4 dequant GEMM (TFLOP/s).
 
 Timing: inputs resident in HBM; weights rotate through enough copies that
 the working set is more than twice the L2 (no step reads a weight copy the
@@ -48,6 +49,15 @@ WORKLOADS = {
     "c8s": dict(kind="gemv", N=6144, K=5120, C=8),
     "quant": dict(kind="quant", K=8192, N=8192),
     "gemm": dict(kind="gemm", M=8192, N=8192, K=8192),
+}
+
+# Components only: the same small-batch GEMVs over permute_int4's output
+# (gemv_w4_permuted; fp32 scale per column, no zero -- the same 4N bytes).
+PERM_WORKLOADS = {
+    "c4_perm": dict(kind="gemv", N=5120, K=17280, C=4, perm=True),
+    "c8_perm": dict(kind="gemv", N=5120, K=17280, C=8, perm=True),
+    "c4s_perm": dict(kind="gemv", N=6144, K=5120, C=4, perm=True),
+    "c8s_perm": dict(kind="gemv", N=6144, K=5120, C=8, perm=True),
 }
 
 
@@ -260,6 +270,33 @@ class GemvWork:
         return "rotating %d weight copies (%.0f MB > 2x L2)" % (self.R, self.R * self.N * self.K / 2 / 1e6)
 
 
+class GemvPermWork:
+    """gemv_w4_permuted over weights permuted once at setup (untimed)."""
+
+    def __init__(self, w4, N, K, C, seed=0):
+        g = synth.packed_gemv_inputs(N, K, C, seed=seed)
+        dev = torch.device("cuda")
+        self.R = copies_for(N * K // 2)
+        packed = g.packed.to(dev)
+        self.q = [w4.permute_int4(packed) for _ in range(self.R)]
+        del packed
+        self.s, self.x = g.scale.to(dev), g.x.to(dev)
+        self.d = torch.empty((C, N), dtype=torch.bfloat16, device=dev)
+        self.w4 = w4
+        self.i = 0
+        self.N, self.K, self.C = N, K, C
+        self.bytes = gemv_bytes(N, K, C)
+        self.flops = 2 * N * K * C
+        self.launches_per_step = 1
+
+    def step(self):
+        self.w4.gemv_w4_permuted(self.q[self.i % self.R], self.s, self.x, out=self.d)
+        self.i += 1
+
+    def l2_note(self):
+        return "rotating %d permuted weight copies (%.0f MB > 2x L2)" % (self.R, self.R * self.N * self.K / 2 / 1e6)
+
+
 class QuantWork:
     def __init__(self, w4, K, N, seed=0):
         dev = torch.device("cuda")
@@ -303,8 +340,10 @@ class GemmWork:
 
 
 def make_work(w4, name):
-    cfg = dict(WORKLOADS[name])
+    cfg = dict(WORKLOADS[name]) if name in WORKLOADS else dict(PERM_WORKLOADS[name])
     kind = cfg.pop("kind")
+    if cfg.pop("perm", False):
+        return GemvPermWork(w4, **cfg)
     if kind == "gemv":
         return GemvWork(w4, **cfg)
     if kind == "quant":
@@ -538,14 +577,16 @@ def run_ours(args, world, rank):
         line["cpu_baseline"] = cpu_baseline(args.workload, budget_s=args.cpu_seconds)
     if args.components and world == 1:
         comps = {}
-        for name in [n for n in ("c4", "c8", "c4s", "c8s", "quant", "gemm") if n != args.workload]:
+        names = [n for n in ("c4", "c8", "c4s", "c8s", "quant", "gemm") if n != args.workload] + list(PERM_WORKLOADS)
+        for name in names:
+            cfg = WORKLOADS[name] if name in WORKLOADS else PERM_WORKLOADS[name]
             wk = make_work(w4, name)
             s, _, _ = time_graph(wk, max(10, args.steps // 4), 3, world)
             per = s / max(10, args.steps // 4)
-            rl = roofline(wk, per / wk.launches_per_step, peaks, peak_src, WORKLOADS[name]["kind"], name)
+            rl = roofline(wk, per / wk.launches_per_step, peaks, peak_src, cfg["kind"], name)
             comps[name] = {"value": rate(wk, per), "unit": unit_of(wk), "ms_per_step": per * 1e3,
                            "frac": rl["frac"], "bound": rl["bound"], "traffic": rl["traffic"],
-                           "config": {k: v for k, v in WORKLOADS[name].items() if k != "kind"}}
+                           "config": {k: v for k, v in cfg.items() if k != "kind"}}
             del wk
             torch.cuda.empty_cache()
         line["components"] = comps

@@ -89,6 +89,7 @@ struct Plan {
     int perwarp;    // 1: every warp keeps its own row partials (no per-tile barrier)
     int tmap;       // 1: a stage is one (or, for a partial tile, a few) 3-D tensor copies
     int nbox;       // 64-byte chunks per row in a tensor box (odd: pitch = 64 mod 128)
+    int xpitch;     // permuted layout: bytes per row of x in shared memory (16 mod 128); 0 otherwise
 };
 
 struct Layout {
@@ -101,7 +102,7 @@ __host__ __device__ inline Layout make_layout(int C, const Plan& P) {
     const int nkb_cap = (P.kslice + KB - 1) / KB;
     int o = P.nst * L.stage_bytes;
     o = (o + 127) & ~127;
-    L.xf = o;        o += nkb_cap * 16 * C * 16;
+    L.xf = o;        o += P.xpitch ? C * P.xpitch : nkb_cap * 16 * C * 16;
     L.xzero = o;     o += 16 * C * 16;
     L.red = o;       o += P.perwarp ? 0 : 2 * NC * 16 * C * 4;
     L.part = o;      o += P.rows_cap * C * 4;
@@ -110,7 +111,7 @@ __host__ __device__ inline Layout make_layout(int C, const Plan& P) {
     L.xsum = o;      o += 16 * 4;                 // [0, 8): this CTA's sums, [8, 16): cluster totals
     L.sz = o;        o += P.rows_cap * 8;          // (scale, zero) per row as fp32
     o = (o + 7) & ~7;
-    L.bars = o;      o += 2 * MAX_NST * 8;
+    L.bars = o;      o += (2 * MAX_NST + 1) * 8;   // full[], empty[], x copied
     L.abort = o;     o += 16;
     L.total = o;
     return L;
@@ -156,6 +157,7 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const void* __restrict__ scale,
     float2* sz = reinterpret_cast<float2*>(sm + L.sz);
     const uint32_t bar_full = sm_addr + L.bars;
     const uint32_t bar_empty = bar_full + MAX_NST * 8;
+    const uint32_t bar_x = bar_full + 2 * MAX_NST * 8;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L.abort);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -175,6 +177,7 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const void* __restrict__ scale,
             mbar_init(bar_full + 8 * s, 1);
             mbar_init(bar_empty + 8 * s, NC);
         }
+        mbar_init(bar_x, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -209,6 +212,14 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const void* __restrict__ scale,
 
     if (warp == NC) {
         // ------------------------------------------------------------ producer
+        if (PERM && lane == 0) {
+            // x rows of this slice, straight into rows of xpitch bytes (every
+            // CTA reads the same x: default L2 policy)
+            mbar_arrive_expect_tx(bar_x, C * klen * 2);
+            if (klen > 0)
+                for (int n = 0; n < C; ++n)
+                    bulk_load(smem_u32(xf) + n * P.xpitch, x + static_cast<int64_t>(n) * K + k0, klen * 2, bar_x);
+        }
         if (lane == 0 && nstages > 0) {
             const uint64_t policy = l2_evict_first_policy();
             const int64_t row_bytes = K / 2;
@@ -260,6 +271,7 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const void* __restrict__ scale,
             // copies still landing if a consumer aborted
             for (int s = max(0, issued - NST); s < issued; ++s) mbar_drain(bar_full + 8 * (s % NST), (s / NST) & 1);
         }
+        if (PERM && lane == 0) mbar_drain(bar_x, 0);
     } else {
         // ------------------------------------------------------------ consumers
         // scale / zero of this CTA's rows: the first two per thread are loaded
@@ -279,6 +291,12 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const void* __restrict__ scale,
         const bool bl = g < C;
         const uint4* xlane = bl ? xf + g * 4 + t4 : xzero + t4;
         constexpr int xw_stride = C * 4;
+        // permuted layout: x is kept as rows; this lane gives the ldmatrix row
+        // address for row n = lane % 8 of matrix lane / 8 (k + 8 * matrix
+        // within each 32-k group); rows past C read a zero block
+        const int xrow = lane & 7;
+        const uint32_t xa = xrow < C ? smem_u32(xf) + xrow * P.xpitch + (lane >> 3) * 16 : smem_u32(xzero);
+        const uint32_t xs = xrow < C ? 64 : 0;   // bytes per 32-k group
         if constexpr (!PERM && C == 1) {
             // one column: a thread adds the eight values of each entry it
             // stages (a few adds per entry, against up to eight columns' worth
@@ -342,49 +360,16 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const void* __restrict__ scale,
             // flight; the column sums are left to the tensor cores
             const int nkb = (klen + KB - 1) / KB;
             if constexpr (PERM) {
-                // permuted operand: the fragment of 32-k group m pairs k =
-                // 32m + 2t4 + 8i (i = 0..3), i.e. word t4 of each 16-byte piece
-                // of the group -- a 4x4 word transpose of 64 bytes of x.  Every
-                // group of every unit is written (zeros past the slice) because
-                // the last unit of a row may be half full.
-                const int per_n = nkb * 4;
-                constexpr int XB = 2;
-                const int dn = per_n > 0 ? CT / per_n : 0, dj = CT - dn * per_n;
-                int n_cur = per_n > 0 ? tid / per_n : C, j_cur = tid - n_cur * per_n;
-                while (n_cur < C) {
-                    uint4 raw[XB][4];
-                    int n = n_cur, j = j_cur;
-#pragma unroll
-                    for (int b = 0; b < XB; ++b) {
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            raw[b][i] = make_uint4(0, 0, 0, 0);
-                            if (n < C && 32 * j + 8 * i < klen)
-                                raw[b][i] = *reinterpret_cast<const uint4*>(x + static_cast<int64_t>(n) * K + k0 +
-                                                                            32 * j + 8 * i);
-                        }
-                        j += dj;
-                        n += dn;
-                        if (j >= per_n) { j -= per_n; ++n; }
-                    }
-                    n = n_cur;
-                    j = j_cur;
-#pragma unroll
-                    for (int b = 0; b < XB; ++b) {
-                        if (n < C) {
-                            uint4* e = xf + (j * C + n) * 4;
-                            e[0] = make_uint4(raw[b][0].x, raw[b][1].x, raw[b][2].x, raw[b][3].x);
-                            e[1] = make_uint4(raw[b][0].y, raw[b][1].y, raw[b][2].y, raw[b][3].y);
-                            e[2] = make_uint4(raw[b][0].z, raw[b][1].z, raw[b][2].z, raw[b][3].z);
-                            e[3] = make_uint4(raw[b][0].w, raw[b][1].w, raw[b][2].w, raw[b][3].w);
-                        }
-                        j += dj;
-                        n += dn;
-                        if (j >= per_n) { j -= per_n; ++n; }
-                    }
-                    n_cur = n;
-                    j_cur = j;
+                // permuted operand: x arrives by bulk copies (issued by the
+                // producer) as rows of xpitch bytes; ldmatrix reads it as B
+                // fragments directly.  Zero the tail of a half unit, then wait.
+                const int tail = (nkb * KB - klen) * 2;   // bytes past the slice in the last unit
+                for (int i = tid; i < C * (tail / 16); i += CT) {
+                    const int n = i / (tail / 16), q = i - n * (tail / 16);
+                    *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(xf) + n * P.xpitch + klen * 2 + q * 16) =
+                        make_uint4(0, 0, 0, 0);
                 }
+                mbar_wait_fast(bar_x, 0, abort_flag);
             } else {
             const int per_n = nkb * 16;
             constexpr int XB = 8;
@@ -438,8 +423,14 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const void* __restrict__ scale,
                 float s2[4] = {0.f, 0.f, 0.f, 0.f}, s3[4] = {0.f, 0.f, 0.f, 0.f};
                 const int nq = nkb * 4, qstride = bl ? xw_stride : 0;
                 for (int q = warp; q < nq; q += 2 * NC) {
-                    const uint4 b0 = xlane[q * qstride];
-                    const uint4 b1 = q + NC < nq ? xlane[(q + NC) * qstride] : make_uint4(0, 0, 0, 0);
+                    uint4 b0, b1 = make_uint4(0, 0, 0, 0);
+                    if constexpr (PERM) {
+                        ldmatrix_x4(xa + q * xs, b0.x, b0.y, b0.z, b0.w);
+                        if (q + NC < nq) ldmatrix_x4(xa + (q + NC) * xs, b1.x, b1.y, b1.z, b1.w);
+                    } else {
+                        b0 = xlane[q * qstride];
+                        if (q + NC < nq) b1 = xlane[(q + NC) * qstride];
+                    }
                     mma_bf16(s0, a1s, b0.x, b0.y);
                     mma_bf16(s1, a1s, b0.z, b0.w);
                     mma_bf16(s2, a1s, b1.x, b1.y);
@@ -462,7 +453,7 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const void* __restrict__ scale,
 
         // main loop: units of each stage go round-robin to the warps, the
         // rotation carrying over from stage to stage
-        const int xkb_stride = bl ? 4 * C * 4 : 0;
+        const int xkb_stride = bl ? 4 * xw_stride : 0;   // next unit
         const uint32_t mask = dq.mask, magic = dq.magic;
         const int row_off_a = g * pitch + 16 * t4, row_off_b = (g + 8) * pitch + 16 * t4;
         // permuted operand: this lane's ldmatrix row -- column r + 8*(i & 1)
@@ -497,7 +488,12 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const void* __restrict__ scale,
                         }
 #pragma unroll
                         for (int w = 0; w < 4; ++w) {
-                            const uint4 bx = xb[w * xw_stride];
+                            uint4 bx;
+                            if constexpr (PERM) {
+                                ldmatrix_x4(xa + ((ch * (P.kchunk / KB) + u) * 4 + w) * xs, bx.x, bx.y, bx.z, bx.w);
+                            } else {
+                                bx = xb[w * xw_stride];
+                            }
                             const uint32_t va = wav[w], vb = wbv[w];
                             const uint32_t a0[4] = {unpack(va), unpack(vb), unpack(va >> 4), unpack(vb >> 4)};
                             const uint32_t a1[4] = {unpack(va >> 8), unpack(vb >> 8), unpack(va >> 12),
@@ -624,8 +620,10 @@ Plan make_plan(int N, int K, int sms, int max_clusters_for_S /* 0: unknown */, i
     P.dense = (!PERM && S == 1 && P.kchunk >= K) ? 1 : 0;
     P.tmap = tm;
     if (PERM) {
-        // four column groups of kchunk/64 lines each, 16 mod 128 bytes apart
+        // four column groups of kchunk/64 lines each, 16 mod 128 bytes apart;
+        // x rows of whole units, 16 mod 128 bytes apart
         P.pitch = 32 * (P.kchunk / 64) + 4;
+        P.xpitch = (P.kslice + KB - 1) / KB * KB * 2 + 16;
     } else if (tm) {
         P.nbox = (P.kchunk / 128) | 1;
         P.pitch = P.nbox * 64;

@@ -282,6 +282,13 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy() {
 
 // 1-D bulk copy global -> shared (both 16-byte aligned, size a multiple of
 // 16), completing on an mbarrier, with an L2 cache-policy hint.
+// 1-D bulk copy global -> shared, completing on an mbarrier (default L2 policy).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
 __device__ __forceinline__ void bulk_load_hint(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
                                                uint64_t policy) {
     asm volatile(
