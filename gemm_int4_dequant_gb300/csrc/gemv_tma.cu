@@ -212,13 +212,16 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const void* __restrict__ scale,
 
     if (warp == NC) {
         // ------------------------------------------------------------ producer
-        if (PERM && lane == 0) {
-            // x rows of this slice, straight into rows of xpitch bytes (every
-            // CTA reads the same x: default L2 policy)
+        if ((PERM || C > 1) && lane == 0) {
+            // x rows of this slice, first thing (every CTA reads the same x:
+            // default L2 policy): rows of xpitch bytes for the permuted
+            // layout, dense rows of klen elements for the row layout (which
+            // the consumers then rearrange in place)
+            const int xrow = PERM ? P.xpitch : klen * 2;
             mbar_arrive_expect_tx(bar_x, C * klen * 2);
             if (klen > 0)
                 for (int n = 0; n < C; ++n)
-                    bulk_load(smem_u32(xf) + n * P.xpitch, x + static_cast<int64_t>(n) * K + k0, klen * 2, bar_x);
+                    bulk_load(smem_u32(xf) + n * xrow, x + static_cast<int64_t>(n) * K + k0, klen * 2, bar_x);
         }
         if (lane == 0 && nstages > 0) {
             const uint64_t policy = l2_evict_first_policy();
@@ -271,7 +274,7 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const void* __restrict__ scale,
             // copies still landing if a consumer aborted
             for (int s = max(0, issued - NST); s < issued; ++s) mbar_drain(bar_full + 8 * (s % NST), (s / NST) & 1);
         }
-        if (PERM && lane == 0) mbar_drain(bar_x, 0);
+        if ((PERM || C > 1) && lane == 0) mbar_drain(bar_x, 0);
     } else {
         // ------------------------------------------------------------ consumers
         // scale / zero of this CTA's rows: the first two per thread are loaded
@@ -371,42 +374,45 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const void* __restrict__ scale,
                 }
                 mbar_wait_fast(bar_x, 0, abort_flag);
             } else {
+            // x arrived by bulk copies as dense rows (row n at n*klen*2 bytes)
+            // in the fragment buffer itself: every thread reads its entries'
+            // sources into registers, then (after a barrier) writes them in
+            // fragment order.  At most XR entries per thread: the plan keeps
+            // the fragments within 80 KB = 10 entries per consumer thread.
             const int per_n = nkb * 16;
-            constexpr int XB = 8;
+            constexpr int XR = 10;
             const int dn = per_n > 0 ? CT / per_n : 0, dj = CT - dn * per_n;
-            int n_cur = per_n > 0 ? tid / per_n : C, j_cur = tid - n_cur * per_n;
-            while (n_cur < C) {
-                uint4 raw[XB];
-                int n = n_cur, j = j_cur;
+            const int n_cur = per_n > 0 ? tid / per_n : C, j_cur = tid - n_cur * per_n;
+            const uint8_t* rows = reinterpret_cast<const uint8_t*>(xf);
+            uint4 v[XR];
+            mbar_wait_fast(bar_x, 0, abort_flag);
+            int n = n_cur, j = j_cur;
 #pragma unroll
-                for (int b = 0; b < XB; ++b) {
-                    raw[b] = make_uint4(0, 0, 0, 0);
-                    if (n < C) {
-                        const int kk = (j >> 4) * KB + 32 * (j & 3) + 8 * ((j >> 2) & 3);
-                        if (kk < klen)
-                            raw[b] = *reinterpret_cast<const uint4*>(x + static_cast<int64_t>(n) * K + k0 + kk);
-                    }
-                    j += dj;
-                    n += dn;
-                    if (j >= per_n) { j -= per_n; ++n; }
+            for (int b = 0; b < XR; ++b) {
+                v[b] = make_uint4(0, 0, 0, 0);
+                if (n < C) {
+                    const int kk = (j >> 4) * KB + 32 * (j & 3) + 8 * ((j >> 2) & 3);
+                    if (kk < klen) v[b] = *reinterpret_cast<const uint4*>(rows + (n * klen + kk) * 2);
                 }
-                n = n_cur;
-                j = j_cur;
+                j += dj;
+                n += dn;
+                if (j >= per_n) { j -= per_n; ++n; }
+            }
+            named_barrier(1, CT);   // every source read before any entry is written
+            n = n_cur;
+            j = j_cur;
 #pragma unroll
-                for (int b = 0; b < XB; ++b) {
-                    if (n < C) {
-                        const int t = j & 3, p = (j >> 2) & 3, kb = j >> 4;
-                        const uint4 r = raw[b];
-                        xf[((kb * 4 + p) * C + n) * 4 + t] =
-                            make_uint4(__byte_perm(r.x, r.z, 0x5410), __byte_perm(r.x, r.z, 0x7632),
-                                       __byte_perm(r.y, r.w, 0x5410), __byte_perm(r.y, r.w, 0x7632));
-                    }
-                    j += dj;
-                    n += dn;
-                    if (j >= per_n) { j -= per_n; ++n; }
+            for (int b = 0; b < XR; ++b) {
+                if (n < C) {
+                    const int t = j & 3, p = (j >> 2) & 3, kb = j >> 4;
+                    const uint4 r = v[b];
+                    xf[((kb * 4 + p) * C + n) * 4 + t] =
+                        make_uint4(__byte_perm(r.x, r.z, 0x5410), __byte_perm(r.x, r.z, 0x7632),
+                                   __byte_perm(r.y, r.w, 0x5410), __byte_perm(r.y, r.w, 0x7632));
                 }
-                n_cur = n;
-                j_cur = j;
+                j += dj;
+                n += dn;
+                if (j >= per_n) { j -= per_n; ++n; }
             }
             }
             for (int i = tid; i < 16 * C; i += CT) xzero[i] = make_uint4(0, 0, 0, 0);
