@@ -18,7 +18,8 @@ Python API with x copied from pinned host memory and d copied back every
 step (weights stay resident, as in a decode loop).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload decode|c4|c8|gemm|quant] [--no-components]
+                    [--workload decode|c4|c8|c4s|c8s|c4_perm|c8_perm|c4s_perm|c8s_perm|gemm|quant]
+                    [--no-components]
 """
 import argparse
 import hashlib
@@ -49,16 +50,14 @@ WORKLOADS = {
     "c8s": dict(kind="gemv", N=6144, K=5120, C=8),
     "quant": dict(kind="quant", K=8192, N=8192),
     "gemm": dict(kind="gemm", M=8192, N=8192, K=8192),
-}
-
-# Components only: the same small-batch GEMVs over permute_int4's output
-# (gemv_w4_permuted; fp32 scale per column, no zero -- the same 4N bytes).
-PERM_WORKLOADS = {
+    # the small-batch GEMVs over permute_int4's output (gemv_w4_permuted;
+    # fp32 scale per column and no zero point: the same 4N bytes)
     "c4_perm": dict(kind="gemv", N=5120, K=17280, C=4, perm=True),
     "c8_perm": dict(kind="gemv", N=5120, K=17280, C=8, perm=True),
     "c4s_perm": dict(kind="gemv", N=6144, K=5120, C=4, perm=True),
     "c8s_perm": dict(kind="gemv", N=6144, K=5120, C=8, perm=True),
 }
+COMPONENTS = ["c4", "c8", "c4s", "c8s", "c4_perm", "c8_perm", "c4s_perm", "c8s_perm", "quant", "gemm"]
 
 
 def load_peaks():
@@ -211,7 +210,8 @@ KERNEL_SOURCES = {
 }
 
 
-PROFILE_FILES = {"decode": "gemv_decode_ncu.md", "gemm": "gemm_8192_ncu.md", "quant": "quant_8192_ncu.md"}
+PROFILE_FILES = {"decode": "gemv_decode_ncu.md", "gemm": "gemm_8192_ncu.md", "quant": "quant_8192_ncu.md",
+                 "c8_perm": "gemv_perm_c8_ncu.md"}
 
 
 def recorded_traffic(kind, workload):
@@ -275,6 +275,7 @@ class GemvPermWork:
 
     def __init__(self, w4, N, K, C, seed=0):
         g = synth.packed_gemv_inputs(N, K, C, seed=seed)
+        self.g = g
         dev = torch.device("cuda")
         self.R = copies_for(N * K // 2)
         packed = g.packed.to(dev)
@@ -340,7 +341,7 @@ class GemmWork:
 
 
 def make_work(w4, name):
-    cfg = dict(WORKLOADS[name]) if name in WORKLOADS else dict(PERM_WORKLOADS[name])
+    cfg = dict(WORKLOADS[name])
     kind = cfg.pop("kind")
     if cfg.pop("perm", False):
         return GemvPermWork(w4, **cfg)
@@ -393,11 +394,18 @@ def e2e_gemv(w4, work, steps, world):
     x_host = work.g.x.clone().pin_memory()
     d_host = torch.empty((work.C, work.N), dtype=torch.bfloat16).pin_memory()
     x_dev = torch.empty_like(work.x)
-    q = work.q[0]
     stream = torch.cuda.current_stream()
-    for _ in range(3):
+    perm = isinstance(work, GemvPermWork)
+
+    def call(i):
+        if perm:
+            w4.gemv_w4_permuted(work.q[i % work.R], work.s, x_dev, out=work.d)
+        else:
+            w4.gemv_w4(work.q[i % work.R], work.s, work.z, x_dev, out=work.d)
+
+    for i in range(3):
         x_dev.copy_(x_host, non_blocking=True)
-        w4.gemv_w4(q, work.s, work.z, x_dev, out=work.d)
+        call(i)
         d_host.copy_(work.d, non_blocking=True)
     torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -406,7 +414,7 @@ def e2e_gemv(w4, work, steps, world):
     start.record(stream)
     for i in range(steps):
         x_dev.copy_(x_host, non_blocking=True)
-        w4.gemv_w4(work.q[i % work.R], work.s, work.z, x_dev, out=work.d)
+        call(i)
         d_host.copy_(work.d, non_blocking=True)
     end.record(stream)
     torch.cuda.synchronize()
@@ -462,6 +470,26 @@ def cpu_baseline(name, budget_s=10.0):
     import oracle
     from synth import np_bits
     cfg = WORKLOADS[name]
+    if cfg["kind"] == "gemv" and cfg.get("perm"):
+        g = synth.packed_gemv_inputs(cfg["N"], cfg["K"], cfg["C"], seed=0)
+        packed, scale, xb = g.packed.numpy(), g.scale.numpy(), np_bits(g.x)
+        N = cfg["N"]
+        t0 = time.perf_counter()
+        oracle.gemv_packed(packed, scale, xb, cols=(0, min(N, 64)))
+        per_col = (time.perf_counter() - t0) / min(N, 64)
+        cols = int(max(1, min(N, 1.0 / max(per_col, 1e-9))))
+        done, t_total, c0 = 0, 0.0, 0
+        while t_total < budget_s:
+            c1 = min(N, c0 + cols)
+            t0 = time.perf_counter()
+            oracle.gemv_packed(packed, scale, xb, cols=(c0, c1))
+            t_total += time.perf_counter() - t0
+            done += c1 - c0
+            c0 = 0 if c1 >= N else c1
+        bytes_done = gemv_bytes(cfg["N"], cfg["K"], cfg["C"]) * done / N
+        return {"value": bytes_done / t_total / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                "sample": "%d columns of the %dx%d C=%d GEMV over the packed matrix (fp64 C oracle, single "
+                          "thread), %.1f s" % (done, cfg["N"], cfg["K"], cfg["C"], t_total)}
     if cfg["kind"] == "gemv":
         g = synth.gemv_inputs(cfg["N"], cfg["K"], cfg["C"], act="bf16", seed=0)
         args = (np_bits(g.qweight), np_bits(g.scale), np_bits(g.zero), np_bits(g.x), oracle.BF16)
@@ -577,9 +605,8 @@ def run_ours(args, world, rank):
         line["cpu_baseline"] = cpu_baseline(args.workload, budget_s=args.cpu_seconds)
     if args.components and world == 1:
         comps = {}
-        names = [n for n in ("c4", "c8", "c4s", "c8s", "quant", "gemm") if n != args.workload] + list(PERM_WORKLOADS)
-        for name in names:
-            cfg = WORKLOADS[name] if name in WORKLOADS else PERM_WORKLOADS[name]
+        for name in [n for n in COMPONENTS if n != args.workload]:
+            cfg = WORKLOADS[name]
             wk = make_work(w4, name)
             s, _, _ = time_graph(wk, max(10, args.steps // 4), 3, world)
             per = s / max(10, args.steps // 4)
