@@ -9,8 +9,10 @@
 // loop; batched form from "三值量化模型的无损压缩", section 3 "MMVQ".)
 //
 // GB300 design.  The op reads 0.5 B of weight per multiply-add, so HBM
-// bandwidth is the roofline.  One CTA per SM owns a contiguous, balanced row
-// range (and, when x does not fit, one K-slice of a thread-block cluster):
+// bandwidth is the roofline.  One CTA per SM owns a contiguous range of whole
+// 16-row tiles (and, when x does not fit, one K-slice of a thread-block
+// cluster); the grid is the smallest that keeps the busiest range as short,
+// so SMs left over take the next launch's CTAs while this one finishes:
 //   * warp NC (producer) streams 16-row tiles with the TMA.  The copy engine
 //     has a fixed cost per copy, so a stage is one copy: the weights are
 //     viewed as a 3-D tensor (8-byte words x 64-byte chunks x rows) and a box
@@ -66,7 +68,7 @@ constexpr int KB = 128;                       // k per unit (one consumer warp p
 constexpr int MAX_NST = 8;                    // stages in the ring (at most)
 constexpr int KCHUNK_MAX = 8192;              // k per stage at most (4 KB per row)
 #ifndef W4_GEMV_PREFETCH_STAGES
-#define W4_GEMV_PREFETCH_STAGES 1               // stages warmed in L2 before the wait
+#define W4_GEMV_PREFETCH_STAGES 3               // stages warmed in L2 before the wait
 #endif
 
 // Nibble mask and bf16 magic passed at run time so they stay in registers and
@@ -136,10 +138,14 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const void* __restrict__ scale,
 
     const int ks = blockIdx.x % S;        // K-slice = rank in the cluster
     const int grp = blockIdx.x / S;       // row group
-    const int64_t quads = (static_cast<int64_t>(N) + 3) / 4;
-    const int64_t r1q = 4 * (((grp + 1) * quads) / P.groups);
-    const int r0 = static_cast<int>(4 * ((grp * quads) / P.groups));
-    const int r1 = static_cast<int>(N < r1q ? static_cast<int64_t>(N) : r1q);
+    // whole 16-row tiles per row group; the first (tiles % groups) groups
+    // take one more (they are dispatched first)
+    const int64_t tiles = (static_cast<int64_t>(N) + 15) / 16;
+    const int64_t tb = tiles / P.groups, te = tiles % P.groups;
+    const int64_t t0 = grp * tb + (grp < te ? grp : te);
+    const int64_t r1t = 16 * (t0 + tb + (grp < te ? 1 : 0));
+    const int r0 = static_cast<int>(16 * t0);
+    const int r1 = static_cast<int>(N < r1t ? static_cast<int64_t>(N) : r1t);
     const int nrows = max(0, r1 - r0);
     const int k0 = min(K, ks * P.kslice);
     const int klen = min(K, k0 + P.kslice) - k0;      // multiple of 32
@@ -181,11 +187,15 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const void* __restrict__ scale,
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    // Launched with programmatic stream serialisation.  Before waiting for
-    // the previous kernel, warm L2 with this CTA's first stage(s): L2 is the
-    // device's point of coherence, so a prefetch cannot yield stale data even
-    // if the previous kernel writes these bytes; every load into shared
-    // memory or registers is issued only after the wait.
+    // Launched with programmatic stream serialisation.  The next kernel in
+    // the stream may be scheduled at once: its CTAs take SMs as they come
+    // free (idle SMs first) and prepare while this grid finishes, and its own
+    // wait still orders all of its reads after this grid has completed.
+    pdl_launch_dependents();
+    // Before waiting for the previous kernel, warm L2 with this CTA's first
+    // stage(s): L2 is the device's point of coherence, so a prefetch cannot
+    // yield stale data even if the previous kernel writes these bytes; every
+    // load into shared memory or registers is issued only after the wait.
     if (PERM && warp == NC && lane == 0 && nstages > 0) {
         // the first stage: each column group's first lines
         const uint32_t gbytes = (min(P.kchunk, klen) + 63) / 64 * 128;
@@ -554,9 +564,6 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const void* __restrict__ scale,
         }
     }
     __syncthreads();
-    // the next kernel in the stream may begin launching (its own wait still
-    // orders its reads after this grid has completed)
-    pdl_launch_dependents();
 
     // combine the K-slices of the cluster, fold the offset, scale, store.
     // Rank ks writes rows ks, ks+S, ...; every (row, c) is one thread, so the
@@ -613,11 +620,18 @@ Plan make_plan(int N, int K, int sms, int max_clusters_for_S /* 0: unknown */, i
     else while (S < 8 && xf_bytes(S) > kXfBudget) S *= 2;
     P.S = S;
     P.kslice = slice_of(S);
-    const int64_t quads = (static_cast<int64_t>(N) + 3) / 4;
-    int groups = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(sms / S, quads)));
+    // Row groups own whole 16-row tiles (a partial tile costs a full stage of
+    // consumer time, so a finer split would not shorten the busiest group).
+    // Of the row-group counts that give the busiest group the same number of
+    // tiles, take the smallest: the SMs left over hold the next launch's
+    // CTAs early (see the launch trigger in the kernel).
+    const int64_t tiles = (static_cast<int64_t>(N) + 15) / 16;
+    int groups = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(sms / S, tiles)));
     if (max_clusters_for_S > 0) groups = std::min(groups, max_clusters_for_S);
+    const int64_t per = std::max<int64_t>(1, (tiles + groups - 1) / groups);
+    groups = static_cast<int>(std::max<int64_t>(1, (tiles + per - 1) / per));
     P.groups = groups;
-    P.rows_cap = static_cast<int>(4 * ((quads + groups - 1) / groups));
+    P.rows_cap = static_cast<int>(16 * std::max<int64_t>(1, per));
     // stage: one 16-row tile over a K-chunk
     {
         const int nch0 = (P.kslice + KCHUNK_MAX - 1) / KCHUNK_MAX;  // chunks of about equal size
