@@ -28,14 +28,25 @@
 //   * warps 0..NC-1 (consumers) share out the 128-k blocks of every stage
 //     round-robin (continuing across stages, so the split stays balanced):
 //     two 16-byte shared loads give a lane its rows g and g+8, each uint32
-//     word becomes four bf16x2 pairs (nibbles j, j+4) with one mask-and-OR
-//     into the mantissa of 128.0 (exactly 128 + q), and two
+//     word becomes four 16-bit pairs (nibbles j, j+4) and two
 //     mma.sync.m16n8k16 per word accumulate in fp32 against x, which was
-//     staged once per CTA in B-fragment order;
+//     staged once per CTA in B-fragment order.  With several columns of x
+//     the pairs are bf16: one mask-and-OR per pair into the mantissa of
+//     128.0 (exactly 128 + q), after a shift by 4j.  With one column they
+//     are fp16, whose ten mantissa bits take a nibble at bits 0-3 or 4-7
+//     unshifted: one mask-and-OR gives 1024 + q (nibbles 0, 2; the second
+//     after a single shift by 8) or 1024 + 16q (nibbles 1, 3), five logic
+//     ops per word instead of seven; the two MMAs of a word then cover even
+//     and odd k, and the odd accumulator is scaled by 1/16.  x is scaled by
+//     a power of two (largest |x| in [2^14, 2^15)) before its fp16
+//     conversion, which is exact for every element within 2^32 of the
+//     largest, and the scaling is undone in fp32;
 //   * per 16-row tile the NC partial sums are added in warp order (named
 //     barrier, double-buffered), so results never depend on timing;
 //   * the offset is folded out exactly at the end:
-//       sum_k (q - z) x = sum_k (128 + q) x - (128 + z) sum_k x,
+//       sum_k (q - z) x = sum_k (128 + q) x - (128 + z) sum_k x
+//     (fp16: sum_k (q - z) x = S_even + S_odd / 16 - 1024 X_even - 64 X_odd
+//     - z X, with S the two accumulators and X the sums of x),
 //     and K-slices are combined through distributed shared memory.
 // Every mbarrier wait is bounded (about two seconds); on timeout the kernel
 // records an error code (w4_device_error), stops issuing copies, drains the
@@ -109,8 +120,11 @@ __host__ __device__ inline Layout make_layout(int C, const Plan& P) {
     L.red = o;       o += P.perwarp ? 0 : 2 * NC * 16 * C * 4;
     L.part = o;      o += P.rows_cap * C * 4;
     L.partw = o;     o += P.perwarp ? NC * ((P.rows_cap + 15) / 16 * 16) * C * 4 : 0;
-    L.xsw = o;       o += NC * C * 4;
-    L.xsum = o;      o += 16 * 4;                 // [0, 8): this CTA's sums, [8, 16): cluster totals
+    L.xsw = o;       o += NC * C * 2 * 4;
+    // per column: [0, 8) this CTA's sum of x (unscaled), [8, 16) cluster
+    // totals, [16, 24) the offset term to fold out, [24, 32) the factor that
+    // undoes the scaling of x
+    L.xsum = o;      o += 32 * 4;
     L.sz = o;        o += P.rows_cap * 8;          // (scale, zero) per row as fp32
     o = (o + 7) & ~7;
     L.bars = o;      o += (2 * MAX_NST + 1) * 8;   // full[], empty[], x copied
@@ -167,6 +181,9 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const void* __restrict__ scale,
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L.abort);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // one column of the row layout runs on fp16 MMAs (x scaled by a power of
+    // two, weights unpacked with five logic ops per word); the others on bf16
+    constexpr bool F16 = !PERM && C == 1;
     // (scale, zero) of output row r; the permuted operand is symmetric and
     // its nibbles are read as 8 + q, which the fold treats as zero point 8
     auto load_sz = [&](int r) -> float2 {
@@ -185,6 +202,7 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const void* __restrict__ scale,
         }
         mbar_init(bar_x, 1);
         *abort_flag = 0;
+        for (int c = 0; c < 8; ++c) reinterpret_cast<uint32_t*>(xsum)[16 + c] = 0;   // column maxima of |x|
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     // Launched with programmatic stream serialisation.  The next kernel in
@@ -222,7 +240,7 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const void* __restrict__ scale,
 
     if (warp == NC) {
         // ------------------------------------------------------------ producer
-        if ((PERM || C > 1) && lane == 0) {
+        if (lane == 0) {
             // x rows of this slice, first thing (every CTA reads the same x:
             // default L2 policy): rows of xpitch bytes for the permuted
             // layout, dense rows of klen elements for the row layout (which
@@ -284,7 +302,7 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const void* __restrict__ scale,
             // copies still landing if a consumer aborted
             for (int s = max(0, issued - NST); s < issued; ++s) mbar_drain(bar_full + 8 * (s % NST), (s / NST) & 1);
         }
-        if ((PERM || C > 1) && lane == 0) mbar_drain(bar_x, 0);
+        if (lane == 0) mbar_drain(bar_x, 0);
     } else {
         // ------------------------------------------------------------ consumers
         // scale / zero of this CTA's rows: the first two per thread are loaded
@@ -296,10 +314,15 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const void* __restrict__ scale,
             const int i = tid + j * CT;
             if (i < nrows) sz_pf[j] = load_sz(r0 + i);
         }
-        // x as B fragments: entry (kb, word p, n, t4) holds, for kk = kb*128 +
-        // 32*t4 + 8*p, the bf16 pairs (x[kk], x[kk+4]) (x[kk+1], x[kk+5])
-        // (x[kk+2], x[kk+6]) (x[kk+3], x[kk+7]) -- the b0b1/b2b3 registers of
-        // the two MMAs that consume word p.
+        // x as B fragments.  Row layout: entry (kb, word p, n, t4) holds, for
+        // kk = kb*128 + 32*t4 + 8*p, the pairs (x[kk], x[kk+4]) (x[kk+1],
+        // x[kk+5]) (x[kk+2], x[kk+6]) (x[kk+3], x[kk+7]) in bf16 -- the b0b1 /
+        // b2b3 registers of the two MMAs that consume word p (nibbles 0, 1 and
+        // 2, 3).  On fp16 (one column) the order is (x[kk], x[kk+4]) (x[kk+2],
+        // x[kk+6]) (x[kk+1], x[kk+5]) (x[kk+3], x[kk+7]): one MMA over the
+        // word's nibbles 0 and 2 (even k), one over 1 and 3 (odd k); x is
+        // multiplied by a power of two first (its largest |x| lands in
+        // [2^14, 2^15)).
         const int g = lane >> 2, t4 = lane & 3;
         const bool bl = g < C;
         const uint4* xlane = bl ? xf + g * 4 + t4 : xzero + t4;
@@ -310,67 +333,10 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const void* __restrict__ scale,
         const int xrow = lane & 7;
         const uint32_t xa = xrow < C ? smem_u32(xf) + xrow * P.xpitch + (lane >> 3) * 16 : smem_u32(xzero);
         const uint32_t xs = xrow < C ? 64 : 0;   // bytes per 32-k group
-        if constexpr (!PERM && C == 1) {
-            // one column: a thread adds the eight values of each entry it
-            // stages (a few adds per entry, against up to eight columns' worth
-            // of conversions and selects per entry in the general case)
-            const int nkb = (klen + KB - 1) / KB;
-            const int per_n = nkb * 16;
-            const int total = C * per_n;
-            float xs_part[C];
-#pragma unroll
-            for (int c = 0; c < C; ++c) xs_part[c] = 0.f;
-            constexpr int XB = 8;  // loads in flight per thread while staging x
-            for (int e0 = tid; e0 < total; e0 += XB * CT) {
-                uint4 raw[XB];
-#pragma unroll
-                for (int b = 0; b < XB; ++b) {
-                    const int e = e0 + b * CT;
-                    raw[b] = make_uint4(0, 0, 0, 0);
-                    if (e < total) {
-                        const int n = e / per_n, j = e - n * per_n;
-                        const int kk = (j >> 4) * KB + 32 * (j & 3) + 8 * ((j >> 2) & 3);
-                        if (kk < klen)
-                            raw[b] = *reinterpret_cast<const uint4*>(x + static_cast<int64_t>(n) * K + k0 + kk);
-                    }
-                }
-#pragma unroll
-                for (int b = 0; b < XB; ++b) {
-                    const int e = e0 + b * CT;
-                    if (e >= total) break;
-                    const int n = e / per_n, j = e - n * per_n;
-                    const int t = j & 3, p = (j >> 2) & 3, kb = j >> 4;
-                    const uint4 r = raw[b];
-                    xf[((kb * 4 + p) * C + n) * 4 + t] =
-                        make_uint4(__byte_perm(r.x, r.z, 0x5410), __byte_perm(r.x, r.z, 0x7632),
-                                   __byte_perm(r.y, r.w, 0x5410), __byte_perm(r.y, r.w, 0x7632));
-                    const float v = bf16_bits_to_f32(r.x & 0xFFFFu) + bf16_bits_to_f32(r.x >> 16) +
-                                    bf16_bits_to_f32(r.y & 0xFFFFu) + bf16_bits_to_f32(r.y >> 16) +
-                                    bf16_bits_to_f32(r.z & 0xFFFFu) + bf16_bits_to_f32(r.z >> 16) +
-                                    bf16_bits_to_f32(r.w & 0xFFFFu) + bf16_bits_to_f32(r.w >> 16);
-#pragma unroll
-                    for (int c = 0; c < C; ++c)
-                        if (c == n) xs_part[c] += v;
-                }
-            }
-#pragma unroll
-            for (int c = 0; c < C; ++c) {
-                float v = xs_part[c];
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-                if (lane == 0) xsw[warp * C + c] = v;
-            }
-            for (int i = tid; i < 16 * C; i += CT) xzero[i] = make_uint4(0, 0, 0, 0);
-            named_barrier(1, CT);
-            if (tid < C) {
-                float v = 0.f;
-                for (int w = 0; w < NC; ++w) v += xsw[w * C + tid];
-                xsum[tid] = v;
-            }
-        } else {
-            // up to eight columns: thread tid stages entries tid, tid + CT, ...
-            // (n-major), stepping (n, j) without dividing, XB loads in
-            // flight; the column sums are left to the tensor cores
+        {
+            // thread tid stages entries tid, tid + CT, ... (n-major), stepping
+            // (n, j) without dividing; the column sums are left to the tensor
+            // cores
             const int nkb = (klen + KB - 1) / KB;
             if constexpr (PERM) {
                 // permuted operand: x arrives by bulk copies (issued by the
@@ -384,55 +350,104 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const void* __restrict__ scale,
                 }
                 mbar_wait_fast(bar_x, 0, abort_flag);
             } else {
-            // x arrived by bulk copies as dense rows (row n at n*klen*2 bytes)
-            // in the fragment buffer itself: every thread reads its entries'
-            // sources into registers, then (after a barrier) writes them in
-            // fragment order.  At most XR entries per thread: the plan keeps
-            // the fragments within 80 KB = 10 entries per consumer thread.
-            const int per_n = nkb * 16;
-            constexpr int XR = 10;
-            const int dn = per_n > 0 ? CT / per_n : 0, dj = CT - dn * per_n;
-            const int n_cur = per_n > 0 ? tid / per_n : C, j_cur = tid - n_cur * per_n;
-            const uint8_t* rows = reinterpret_cast<const uint8_t*>(xf);
-            uint4 v[XR];
-            mbar_wait_fast(bar_x, 0, abort_flag);
-            int n = n_cur, j = j_cur;
+                // x arrived by bulk copies as dense rows (row n at n*klen*2
+                // bytes) in the fragment buffer itself: every thread reads its
+                // entries' sources into registers (on fp16 noting the largest
+                // |x|: warp maxima meet in shared memory); after a barrier it
+                // writes them in fragment order (on fp16 scaled and
+                // converted).  At most XR entries per thread: the plan keeps
+                // the fragments within 80 KB = 10 entries per consumer thread.
+                const int per_n = nkb * 16;
+                constexpr int XR = 10;
+                const int dn = per_n > 0 ? CT / per_n : 0, dj = CT - dn * per_n;
+                const int n_cur = per_n > 0 ? tid / per_n : C, j_cur = tid - n_cur * per_n;
+                const uint8_t* rows = reinterpret_cast<const uint8_t*>(xf);
+                uint32_t* xmax = reinterpret_cast<uint32_t*>(xsum) + 16;   // fp16: max |x| bits, zeroed at entry
+                uint4 v[XR];
+                uint32_t mx = 0;
+                mbar_wait_fast(bar_x, 0, abort_flag);
+                int n = n_cur, j = j_cur;
 #pragma unroll
-            for (int b = 0; b < XR; ++b) {
-                v[b] = make_uint4(0, 0, 0, 0);
-                if (n < C) {
-                    const int kk = (j >> 4) * KB + 32 * (j & 3) + 8 * ((j >> 2) & 3);
-                    if (kk < klen) v[b] = *reinterpret_cast<const uint4*>(rows + (n * klen + kk) * 2);
+                for (int b = 0; b < XR; ++b) {
+                    v[b] = make_uint4(0, 0, 0, 0);
+                    if (n < C) {
+                        const int kk = (j >> 4) * KB + 32 * (j & 3) + 8 * ((j >> 2) & 3);
+                        if (kk < klen) v[b] = *reinterpret_cast<const uint4*>(rows + (n * klen + kk) * 2);
+                        if constexpr (F16) {
+                            // |x| as bf16 bit patterns with the sign cleared (ordered as integers)
+                            const uint32_t m2 = __vmaxu2(__vmaxu2(v[b].x & 0x7FFF7FFFu, v[b].y & 0x7FFF7FFFu),
+                                                         __vmaxu2(v[b].z & 0x7FFF7FFFu, v[b].w & 0x7FFF7FFFu));
+                            mx = max(mx, max(m2 & 0xFFFFu, m2 >> 16));
+                        }
+                    }
+                    j += dj;
+                    n += dn;
+                    if (j >= per_n) { j -= per_n; ++n; }
                 }
-                j += dj;
-                n += dn;
-                if (j >= per_n) { j -= per_n; ++n; }
-            }
-            named_barrier(1, CT);   // every source read before any entry is written
-            n = n_cur;
-            j = j_cur;
+                if constexpr (F16) {
+                    const uint32_t wm = __reduce_max_sync(0xffffffffu, mx);
+                    if (lane == 0 && wm != 0) atomicMax(&xmax[0], wm);
+                }
+                named_barrier(1, CT);   // every source read (and the maximum of |x| final)
+                // fp16: x is scaled by 2^e, e = 141 - (biased bf16 exponent of
+                // max|x|), so that max|x| 2^e lies in [2^14, 2^15); at most 100
+                // (all-zero or tiny x).  se / so: sums of the converted x over
+                // even / odd k.
+                const float sc = F16 ? __int_as_float((127 + min(100, 141 - static_cast<int>(xmax[0] >> 7))) << 23) : 1.0f;
+                float se = 0.f, so = 0.f;
+                n = n_cur;
+                j = j_cur;
 #pragma unroll
-            for (int b = 0; b < XR; ++b) {
-                if (n < C) {
-                    const int t = j & 3, p = (j >> 2) & 3, kb = j >> 4;
-                    const uint4 r = v[b];
-                    xf[((kb * 4 + p) * C + n) * 4 + t] =
-                        make_uint4(__byte_perm(r.x, r.z, 0x5410), __byte_perm(r.x, r.z, 0x7632),
-                                   __byte_perm(r.y, r.w, 0x5410), __byte_perm(r.y, r.w, 0x7632));
+                for (int b = 0; b < XR; ++b) {
+                    if (n < C) {
+                        const int t = j & 3, p = (j >> 2) & 3, kb = j >> 4;
+                        const uint4 r = v[b];
+                        if constexpr (!F16) {
+                            xf[((kb * 4 + p) * C + n) * 4 + t] =
+                                make_uint4(__byte_perm(r.x, r.z, 0x5410), __byte_perm(r.x, r.z, 0x7632),
+                                           __byte_perm(r.y, r.w, 0x5410), __byte_perm(r.y, r.w, 0x7632));
+                        } else {
+                            auto h2 = [&](uint32_t lo_bits, uint32_t hi_bits) {
+                                return __floats2half2_rn(bf16_bits_to_f32(lo_bits) * sc,
+                                                         bf16_bits_to_f32(hi_bits) * sc);
+                            };
+                            // r holds x[kk..kk+7] as (x0,x1) (x2,x3) (x4,x5) (x6,x7)
+                            const __half2 h04 = h2(r.x & 0xFFFFu, r.z & 0xFFFFu);
+                            const __half2 h26 = h2(r.y & 0xFFFFu, r.w & 0xFFFFu);
+                            const __half2 h15 = h2(r.x >> 16, r.z >> 16), h37 = h2(r.y >> 16, r.w >> 16);
+                            xf[((kb * 4 + p) * C + n) * 4 + t] = make_uint4(
+                                *reinterpret_cast<const uint32_t*>(&h04), *reinterpret_cast<const uint32_t*>(&h26),
+                                *reinterpret_cast<const uint32_t*>(&h15), *reinterpret_cast<const uint32_t*>(&h37));
+                            const float2 f04 = __half22float2(h04), f26 = __half22float2(h26);
+                            const float2 f15 = __half22float2(h15), f37 = __half22float2(h37);
+                            se += (f04.x + f04.y) + (f26.x + f26.y);
+                            so += (f15.x + f15.y) + (f37.x + f37.y);
+                        }
+                    }
+                    j += dj;
+                    n += dn;
+                    if (j >= per_n) { j -= per_n; ++n; }
                 }
-                j += dj;
-                n += dn;
-                if (j >= per_n) { j -= per_n; ++n; }
-            }
+                if constexpr (F16) {
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) {
+                        se += __shfl_xor_sync(0xffffffffu, se, o);
+                        so += __shfl_xor_sync(0xffffffffu, so, o);
+                    }
+                    if (lane == 0) {
+                        xsw[warp * 2] = se;
+                        xsw[warp * 2 + 1] = so;
+                    }
+                }
             }
             for (int i = tid; i < 16 * C; i += CT) xzero[i] = make_uint4(0, 0, 0, 0);
             named_barrier(1, CT);
 
-            // sum_k x[c][k] on the tensor cores: an all-ones A operand turns each
-            // MMA over a staged fragment into column sums (fp32 accumulation, as
-            // in the main product).  Warps take the (kb, word) pairs round-robin,
-            // two at a time on independent accumulators.
-            {
+            // bf16: sums of x on the tensor cores -- an all-ones A operand turns
+            // each MMA over a staged fragment into column sums (fp32
+            // accumulation, as in the main product).  Warps take the (kb, word)
+            // pairs round-robin, two at a time on independent accumulators.
+            if constexpr (!F16) {
                 const uint32_t ones = 0x3F803F80u;   // bf16x2 (1.0, 1.0)
                 const uint32_t a1s[4] = {ones, ones, ones, ones};
                 float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
@@ -455,22 +470,45 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const void* __restrict__ scale,
                 // every row of the product holds the same sums: lanes of row 0
                 // own columns 2*t4 and 2*t4 + 1
                 if (g == 0) {
-                    if (2 * t4 < C) xsw[warp * C + 2 * t4] = (s0[0] + s1[0]) + (s2[0] + s3[0]);
-                    if (2 * t4 + 1 < C) xsw[warp * C + 2 * t4 + 1] = (s0[1] + s1[1]) + (s2[1] + s3[1]);
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int c = 2 * t4 + h;
+                        if (c < C) {
+                            xsw[(warp * C + c) * 2] = (s0[h] + s1[h]) + (s2[h] + s3[h]);
+                            xsw[(warp * C + c) * 2 + 1] = 0.f;
+                        }
+                    }
                 }
-            }
-            named_barrier(1, CT);
+                named_barrier(1, CT);
+            }   // (fp16: the sums were stored before the last barrier)
             if (tid < C) {
-                float v = 0.f;
-                for (int w = 0; w < NC; ++w) v += xsw[w * C + tid];
-                xsum[tid] = v;
+                float se = 0.f, so = 0.f;
+                for (int w = 0; w < NC; ++w) {
+                    se += xsw[(w * C + tid) * 2];
+                    so += xsw[(w * C + tid) * 2 + 1];
+                }
+                if constexpr (!F16) {
+                    // nibbles read as 128 + q (row layout) or 128 + (q + 8)
+                    // (permuted layout, zero point 8): offset 128
+                    xsum[16 + tid] = 128.0f * se;
+                    xsum[24 + tid] = 1.0f;
+                    xsum[tid] = se;
+                } else {
+                    // even k read as 1024 + q, odd k as 1024 + 16q (the odd
+                    // accumulator is scaled by 1/16 before the fold)
+                    const int e = min(100, 141 - static_cast<int>(reinterpret_cast<const uint32_t*>(xsum)[16 + tid] >> 7));
+                    const float inv = __int_as_float((127 - e) << 23);   // 2^-e
+                    xsum[24 + tid] = inv;
+                    xsum[16 + tid] = fmaf(64.0f, so, 1024.0f * se);
+                    xsum[tid] = (se + so) * inv;
+                }
             }
         }
 
         // main loop: units of each stage go round-robin to the warps, the
         // rotation carrying over from stage to stage
         const int xkb_stride = bl ? 4 * xw_stride : 0;   // next unit
-        const uint32_t mask = dq.mask, magic = dq.magic;
+        const uint32_t mask = dq.mask, magic = dq.magic, mask_hi = dq.mask << 4;
         const int row_off_a = g * pitch + 16 * t4, row_off_b = (g + 8) * pitch + 16 * t4;
         // permuted operand: this lane's ldmatrix row -- column r + 8*(i & 1)
         // of matrix i = lane / 8 (r = lane % 8), 32-k group +(i >> 1); the
@@ -511,11 +549,24 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const void* __restrict__ scale,
                                 bx = xb[w * xw_stride];
                             }
                             const uint32_t va = wav[w], vb = wbv[w];
-                            const uint32_t a0[4] = {unpack(va), unpack(vb), unpack(va >> 4), unpack(vb >> 4)};
-                            const uint32_t a1[4] = {unpack(va >> 8), unpack(vb >> 8), unpack(va >> 12),
-                                                    unpack(vb >> 12)};
-                            mma_bf16(acc, a0, bx.x, bx.y);
-                            mma_bf16(acc2, a1, bx.z, bx.w);
+                            if constexpr (!F16) {
+                                const uint32_t a0[4] = {unpack(va), unpack(vb), unpack(va >> 4), unpack(vb >> 4)};
+                                const uint32_t a1[4] = {unpack(va >> 8), unpack(vb >> 8), unpack(va >> 12),
+                                                        unpack(vb >> 12)};
+                                mma_bf16(acc, a0, bx.x, bx.y);
+                                mma_bf16(acc2, a1, bx.z, bx.w);
+                            } else {
+                                // fp16 1024 + q from nibbles 0 and 2 (bits 0-3 of each
+                                // half, after one shift by 8 for nibble 2), 1024 + 16q
+                                // from nibbles 1 and 3 (bits 4-7): five logic ops per word
+                                const uint32_t va8 = va >> 8, vb8 = vb >> 8;
+                                const uint32_t a0[4] = {and_or(va, mask, magic), and_or(vb, mask, magic),
+                                                        and_or(va8, mask, magic), and_or(vb8, mask, magic)};
+                                const uint32_t a1[4] = {and_or(va, mask_hi, magic), and_or(vb, mask_hi, magic),
+                                                        and_or(va8, mask_hi, magic), and_or(vb8, mask_hi, magic)};
+                                mma_f16(acc, a0, bx.x, bx.y);
+                                mma_f16(acc2, a1, bx.z, bx.w);
+                            }
                         }
                     }
                 }
@@ -527,23 +578,38 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const void* __restrict__ scale,
                 if (++slot == NST) { slot = 0; ++round; }
             }
             const int c0 = 2 * t4, c1 = 2 * t4 + 1;
+            // the odd-k accumulator holds 16x its share on the row layout
+            constexpr float kOdd = F16 ? 0.0625f : 1.0f;
             if (P.perwarp) {
                 // this warp's partial of the tile; warps are added at the end
                 float* pw = partw + (static_cast<size_t>(warp) * rows16 + tile * 16) * C;
-                if (c0 < C) { pw[g * C + c0] = acc[0] + acc2[0]; pw[(g + 8) * C + c0] = acc[2] + acc2[2]; }
-                if (c1 < C) { pw[g * C + c1] = acc[1] + acc2[1]; pw[(g + 8) * C + c1] = acc[3] + acc2[3]; }
+                if (c0 < C) {
+                    pw[g * C + c0] = fmaf(acc2[0], kOdd, acc[0]);
+                    pw[(g + 8) * C + c0] = fmaf(acc2[2], kOdd, acc[2]);
+                }
+                if (c1 < C) {
+                    pw[g * C + c1] = fmaf(acc2[1], kOdd, acc[1]);
+                    pw[(g + 8) * C + c1] = fmaf(acc2[3], kOdd, acc[3]);
+                }
             } else {
                 // tile partials, added in warp order now (bounded shared memory)
                 float* rb = red + ((tile & 1) * NC + warp) * 16 * C;
-                if (c0 < C) { rb[g * C + c0] = acc[0] + acc2[0]; rb[(g + 8) * C + c0] = acc[2] + acc2[2]; }
-                if (c1 < C) { rb[g * C + c1] = acc[1] + acc2[1]; rb[(g + 8) * C + c1] = acc[3] + acc2[3]; }
+                if (c0 < C) {
+                    rb[g * C + c0] = fmaf(acc2[0], kOdd, acc[0]);
+                    rb[(g + 8) * C + c0] = fmaf(acc2[2], kOdd, acc[2]);
+                }
+                if (c1 < C) {
+                    rb[g * C + c1] = fmaf(acc2[1], kOdd, acc[1]);
+                    rb[(g + 8) * C + c1] = fmaf(acc2[3], kOdd, acc[3]);
+                }
                 named_barrier(1, CT);
                 for (int i = tid; i < 16 * C; i += CT) {
                     const int r = i / C;
                     if (tile * 16 + r < nrows) {
                         float v = 0.f;
                         for (int w = 0; w < NC; ++w) v += red[((tile & 1) * NC + w) * 16 * C + i];
-                        part[(tile * 16) * C + i] = v;
+                        const int c = i - r * C;
+                        part[(tile * 16) * C + i] = (v - xsum[16 + c]) * xsum[24 + c];
                     }
                 }
             }
@@ -559,15 +625,19 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const void* __restrict__ scale,
             for (int i = tid; i < nrows * C; i += CT) {
                 float v = 0.f;
                 for (int w = 0; w < NC; ++w) v += partw[static_cast<size_t>(w) * rows16 * C + i];
-                part[i] = v;
+                const int c = i % C;
+                part[i] = (v - xsum[16 + c]) * xsum[24 + c];
             }
         }
     }
     __syncthreads();
 
-    // combine the K-slices of the cluster, fold the offset, scale, store.
-    // Rank ks writes rows ks, ks+S, ...; every (row, c) is one thread, so the
-    // remote (distributed shared memory) loads of all ranks are in flight at once.
+    // part[] holds sum_k q x per (row, column) over this CTA's K-slice, in
+    // the units of x (offset folded out, scaling undone); xsum[0, C) the
+    // slice's sum of x.  Combine the K-slices of the cluster, fold the zero
+    // point, scale, store.  Rank ks writes rows ks, ks+S, ...; every
+    // (row, c) is one thread, so the remote (distributed shared memory) loads
+    // of all ranks are in flight at once.
     cg::cluster_group cluster = cg::this_cluster();
     float* xs_tot = xsum + 8;
     if (S > 1) cluster.sync();
@@ -593,7 +663,7 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const void* __restrict__ scale,
             sum = part[i * C + c];
         }
         const float2 s_z = sz[i];
-        d[static_cast<int64_t>(c) * N + r0 + i] = __float2bfloat16_rn(s_z.x * fmaf(-(128.0f + s_z.y), xs_tot[c], sum));
+        d[static_cast<int64_t>(c) * N + r0 + i] = __float2bfloat16_rn(s_z.x * fmaf(-s_z.y, xs_tot[c], sum));
     }
     if (S > 1) cluster.sync();
 }
@@ -728,7 +798,9 @@ w4_status launch_gemv_tma_t(const void* qw, const void* scale, const void* zero,
     }
     // row layout: (v & 0x000F000F) | 0x43004300; permuted (two's complement):
     // pass bits 0-2, invert bit 3, set the exponent of 128.0
-    const MaskMagic dq = PERM ? MaskMagic{0x43074307u, 0x43084308u} : MaskMagic{0x000F000Fu, 0x43004300u};
+    const MaskMagic dq = PERM      ? MaskMagic{0x43074307u, 0x43084308u}
+                         : C == 1 ? MaskMagic{0x000F000Fu, 0x64006400u}   // fp16 1024 + q
+                                  : MaskMagic{0x000F000Fu, 0x43004300u};  // bf16 128 + q
     e = cudaLaunchKernelEx(&cfg, kern, static_cast<const uint8_t*>(qw), scale, zero,
                            static_cast<const __nv_bfloat16*>(x), static_cast<__nv_bfloat16*>(d), N, K, P, dq, tm16,
                            tm4);

@@ -160,6 +160,35 @@ def test_gemv_non_integer_zero_and_wide_scales(w4):
     _check_gemv(w4, 500, 2048, 2, "f32", seed=4, zero_value=0.013, scale_range=(1e-3, 1.0))
 
 
+@pytest.mark.parametrize("N,K", [(300, 4096), (200, 24576)])   # one CTA per row range; K split over a cluster
+def test_gemv_x_magnitudes(w4, N, K):
+    """x columns far outside fp16's range, tiny, spanning 2^40 within a
+    column, and all zero: the tensor-core path scales each column of x by a
+    power of two before its fp16 conversion."""
+    C = 5
+    g = synth.gemv_inputs(N, K, C, act="bf16", seed=11)
+    x = g.x.float()
+    x[0] *= 2.0 ** 40                      # beyond fp16's largest finite value
+    x[1] *= 2.0 ** -60                     # below fp16's smallest subnormal
+    span = torch.ones(K)
+    span[::3] = 2.0 ** 20
+    span[1::3] = 2.0 ** -20
+    x[2] *= span                           # 2^40 between elements of one column
+    x[3] = 0.0
+    x[4, : K // 2] = 0.0                   # half zero
+    g.x = x.to(torch.bfloat16)
+    buf, out, pad = _guarded(C * N, torch.bfloat16, -7.0)
+    w4.gemv_w4(g.qweight.to(_dev()), g.scale.to(_dev()), g.zero.to(_dev()), g.x.to(_dev()), out=out)
+    ref, ref_abs = oracle.gemv(np_bits(g.qweight), np_bits(g.scale), np_bits(g.zero), np_bits(g.x), oracle.BF16)
+    got = out.float().cpu().numpy().astype(np.float64).reshape(C, N)
+    bad = parity_violations(got, ref, ref_abs, BF16_TOL, bf16_out=True)
+    err = np.abs(got - ref)
+    assert not bad.any(), "max err/ref_abs = %g at %s" % ((err / np.maximum(ref_abs, 1e-300)).max(),
+                                                          np.argwhere(bad)[:5])
+    assert np.all(got[3] == 0)
+    assert _guards_intact(buf, pad, C * N, -7.0)
+
+
 def test_gemv_k_zero_gives_zero(w4):
     x = torch.empty((2, 0), dtype=torch.bfloat16, device=_dev())
     q = torch.empty((16, 0), dtype=torch.int32, device=_dev())
