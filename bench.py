@@ -6,8 +6,9 @@ configuration the headline metric "int4 W-only GEMV HBM GB/s" is quoted
 on.  One step = one gemv_w4 call on one batch.  The line also carries the
 other kernels of the hot path as components: the small-batch GEMVs (C = 4,
 8), the same GEMVs over permute_int4's output (gemv_w4_permuted),
-quantise+pack+permute of an 8192x8192 bf16 weight, and the 8192^3 bf16 x
-int4 dequant GEMM (TFLOP/s).
+quantise+pack+permute of an 8192x8192 bf16 weight (one pass,
+quantize_pack_permute_int4; and as the two calls quantize_pack_int4 +
+permute_int4), and the 8192^3 bf16 x int4 dequant GEMM (TFLOP/s).
 
 Timing: inputs resident in HBM; weights rotate through enough copies that
 the working set is more than twice the L2 (no step reads a weight copy the
@@ -18,7 +19,7 @@ Python API with x copied from pinned host memory and d copied back every
 step (weights stay resident, as in a decode loop).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload decode|c4|c8|c4s|c8s|c4_perm|c8_perm|c4s_perm|c8s_perm|gemm|quant]
+                    [--workload decode|c4|c8|c4s|c8s|c4_perm|c8_perm|c4s_perm|c8s_perm|gemm|quant|quant_2call]
                     [--no-components]
 """
 import argparse
@@ -48,7 +49,10 @@ WORKLOADS = {
     "c8": dict(kind="gemv", N=5120, K=17280, C=8),
     "c4s": dict(kind="gemv", N=6144, K=5120, C=4),
     "c8s": dict(kind="gemv", N=6144, K=5120, C=8),
-    "quant": dict(kind="quant", K=8192, N=8192),
+    # quantise + pack + permute of one 8192x8192 weight: the one-pass call,
+    # and the two separate calls (packed matrix stored, then permuted)
+    "quant": dict(kind="quant", K=8192, N=8192, fused=True),
+    "quant_2call": dict(kind="quant", K=8192, N=8192, fused=False),
     "gemm": dict(kind="gemm", M=8192, N=8192, K=8192),
     # the small-batch GEMVs over permute_int4's output (gemv_w4_permuted;
     # fp32 scale per column and no zero point: the same 4N bytes)
@@ -57,7 +61,7 @@ WORKLOADS = {
     "c4s_perm": dict(kind="gemv", N=6144, K=5120, C=4, perm=True),
     "c8s_perm": dict(kind="gemv", N=6144, K=5120, C=8, perm=True),
 }
-COMPONENTS = ["c4", "c8", "c4s", "c8s", "c4_perm", "c8_perm", "c4s_perm", "c8s_perm", "quant", "gemm"]
+COMPONENTS = ["c4", "c8", "c4s", "c8s", "c4_perm", "c8_perm", "c4s_perm", "c8s_perm", "quant", "quant_2call", "gemm"]
 
 
 def load_peaks():
@@ -78,9 +82,11 @@ def gemv_bytes(N, K, C, esz=2):
     return N * K // 2 + 2 * N * esz + C * K * esz + C * N * esz
 
 
-def quant_bytes(K, N):
-    # quantize_pack: read W, write packed + scale; permute: read + write packed
-    return (K * N * 2 + K * N // 2 + 4 * N) + 2 * (K * N // 2)
+def quant_bytes(K, N, fused=True):
+    # one pass: read W, write the permuted matrix + scale; two calls add the
+    # packed matrix's write and re-read
+    one_pass = K * N * 2 + K * N // 2 + 4 * N
+    return one_pass if fused else one_pass + 2 * (K * N // 2)
 
 
 def gemm_bytes(M, N, K):
@@ -299,7 +305,7 @@ class GemvPermWork:
 
 
 class QuantWork:
-    def __init__(self, w4, K, N, seed=0):
+    def __init__(self, w4, K, N, fused=True, seed=0):
         dev = torch.device("cuda")
         W = synth.quant_inputs(K, N, seed=seed).to(dev)
         self.W = W
@@ -308,13 +314,17 @@ class QuantWork:
         self.out = torch.empty((N * K // 2,), dtype=torch.int8, device=dev)
         self.w4 = w4
         self.K, self.N = K, N
-        self.bytes = quant_bytes(K, N)
+        self.fused = fused
+        self.bytes = quant_bytes(K, N, fused)
         self.flops = 0
-        self.launches_per_step = 2
+        self.launches_per_step = 1 if fused else 2
 
     def step(self):
-        self.w4.quantize_pack_int4(self.W, packed=self.packed, scale=self.scale)
-        self.w4.permute_int4(self.packed, out=self.out)
+        if self.fused:
+            self.w4.quantize_pack_permute_int4(self.W, out=self.out, scale=self.scale)
+        else:
+            self.w4.quantize_pack_int4(self.W, packed=self.packed, scale=self.scale)
+            self.w4.permute_int4(self.packed, out=self.out)
 
     def l2_note(self):
         return "W is %.0f MB > L2" % (self.K * self.N * 2 / 1e6)
@@ -536,7 +546,8 @@ def cpu_baseline(name, budget_s=10.0):
         oracle.permute(p_ref, K, N)
         t_total += time.perf_counter() - t0
         n_done += 1
-    return {"value": quant_bytes(K, N) * n_done / t_total / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+    return {"value": quant_bytes(K, N, cfg.get("fused", True)) * n_done / t_total / 1e9, "unit": "GB/s", "cores": 1,
+            "kind": "oracle",
             "sample": "%d full quantize+pack+permute of %dx%d (C oracle, single thread), %.1f s" %
                       (n_done, K, N, t_total)}
 
@@ -599,7 +610,7 @@ def run_ours(args, world, rank):
         "clocks": clocks,
         "e2e": {"value": e2e_val, "unit": unit_of(work), "h2d_bytes_per_step": hb, "d2h_bytes_per_step": ob},
     }
-    if kind == "quant":
+    if kind == "quant" and not WORKLOADS[args.workload].get("fused", True):
         line["roofline"]["note"] = "two kernels per step (quantize_pack_int4 + permute_int4); achieved = step bytes / step time"
     if rank == 0 and world == 1:
         line["cpu_baseline"] = cpu_baseline(args.workload, budget_s=args.cpu_seconds)

@@ -8,6 +8,7 @@ in the library's CUDA kernels; there is no CPU or eager fallback.
 
     quantize_pack_int4(W)               -> (packed [K/2, N] int8, scale [N] fp32)
     permute_int4(packed)                -> out [N*K/2] int8 (interleaved)
+    quantize_pack_permute_int4(W)       -> (out [N*K/2] int8, scale [N] fp32), both in one pass
     gemv_w4(qweight, scale, zero, x)    -> d [C, N]
     gemv_w4_permuted(permuted, scale, x) -> d [C, N] bf16 (over permute_int4's output)
     gemm_w4(A, B, scale, zero)          -> C [M, N] bf16
@@ -17,7 +18,7 @@ import torch
 from . import _lib
 from ._lib import W4Error, W4_BF16, W4_F32
 
-__all__ = ["quantize_pack_int4", "permute_int4", "gemv_w4", "gemv_w4_permuted", "gemm_w4", "device_error",
+__all__ = ["quantize_pack_int4", "permute_int4", "quantize_pack_permute_int4", "gemv_w4", "gemv_w4_permuted", "gemm_w4", "device_error",
            "W4Error"]
 
 _lib.load()  # fail loudly at import if the CUDA library is missing
@@ -62,6 +63,26 @@ def quantize_pack_int4(W, packed=None, scale=None, stream=None):
     st = _lib.load().quantize_pack_int4(W.data_ptr(), packed.data_ptr(), scale.data_ptr(), K, N, _stream(stream))
     _lib.check("quantize_pack_int4", st)
     return packed, scale
+
+
+def quantize_pack_permute_int4(W, out=None, scale=None, stream=None):
+    """quantize_pack_int4 then permute_int4 in one pass over W [K, N] bf16
+    (K % 64 == 0, N % 8 == 0, K <= 26624): the permuted N*K/2 bytes and the
+    fp32 scale, bit-exact with the two separate calls."""
+    _need(W, "W", (torch.bfloat16,), 2)
+    K, N = W.shape
+    if out is None:
+        out = torch.empty((N * (K // 2),), dtype=torch.int8, device=W.device)
+    if scale is None:
+        scale = torch.empty((N,), dtype=torch.float32, device=W.device)
+    _need(out, "out", (torch.int8, torch.uint8))
+    _need(scale, "scale", (torch.float32,))
+    if out.numel() != N * (K // 2) or scale.numel() != N:
+        raise ValueError("output shapes do not match W")
+    st = _lib.load().quantize_pack_permute_int4(W.data_ptr(), out.data_ptr(), scale.data_ptr(), K, N,
+                                                _stream(stream))
+    _lib.check("quantize_pack_permute_int4", st)
+    return out, scale
 
 
 def permute_int4(packed, out=None, stream=None):

@@ -43,6 +43,8 @@ def load():
     lib.quantize_pack_int4.restype = I
     lib.permute_int4.argtypes = [P, P, I64, I64, P]
     lib.permute_int4.restype = I
+    lib.quantize_pack_permute_int4.argtypes = [P, P, P, I64, I64, P]
+    lib.quantize_pack_permute_int4.restype = I
     lib.gemv_w4.argtypes = [P, P, P, P, P, I64, I64, I64, I, P]
     lib.gemv_w4.restype = I
     lib.gemv_w4_permuted.argtypes = [P, P, P, P, I64, I64, I64, P]

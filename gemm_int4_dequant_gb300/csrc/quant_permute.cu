@@ -39,6 +39,7 @@ constexpr int QC_BOXR = 256;                     // rows per TMA box
 constexpr int QC_SMEM = 208 * 1024;              // strip rows per CTA at most (bytes)
 constexpr int QC_MAX_R = QC_SMEM / (QC_COLS * 2) / QC_BOXR * QC_BOXR;
 constexpr int64_t QC_MAX_K = static_cast<int64_t>(QC_CS) * QC_MAX_R;
+static_assert(QC_MAX_K == W4_QUANT_PERMUTE_MAX_K, "the header's K limit is the single-read kernel's");
 
 // q = clamp(round_half_away(w / s), -8, 7) as a nibble; s == 0 gives 0.
 __device__ __forceinline__ uint32_t quant_nibble(uint32_t wbits, float s) {
@@ -64,6 +65,29 @@ __device__ __forceinline__ uint32_t quant_u(uint32_t wbits16_hi, float inv) {
 }
 __device__ __forceinline__ bool quant_near(uint32_t u) { return (u & 0xFFFCu) == 0; }
 
+// Bracketed variant: u_hi / u_lo = fl(w * inv + 192.5 +/- 2^-15).  If both
+// have the same integer part F, then w * inv + 192.5 lies at least 3*2^-17
+// inside (F, F + 1); the IEEE quotient fl(w / s) differs from w * inv by less
+// than 2^-21 (|w / s| <= 7), so fl(w / s) + 0.5 is not an integer and
+// round-half-away(fl(w / s)) = floor(fl(w / s) + 0.5) = F - 192, whose low
+// four bits are bits 16..19 of u (F - 128 fills bits 16..22 of the
+// mantissa; 128 and 192 are 0 mod 16).  Different integer parts flag the
+// weight for the exact division.
+constexpr float QB_HI = 192.50003051757812f;   // 192.5 + 2^-15
+constexpr float QB_LO = 192.49996948242188f;   // 192.5 - 2^-15
+
+// Byte 2 of a and byte 2 of b in bytes 0, 1 (sel 0x0062) or 2, 3 (sel 0x6200).
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) { return __byte_perm(a, b, sel); }
+
+// The nibbles (bits 16..19) of x0..x3 and y0..y3 as one word with nibble
+// order x0 y0 x1 y1 x2 y2 x3 y3 (x0 in bits 0..3).
+__device__ __forceinline__ uint32_t pack_nibbles(uint32_t x0, uint32_t x1, uint32_t x2, uint32_t x3, uint32_t y0,
+                                                 uint32_t y1, uint32_t y2, uint32_t y3) {
+    const uint32_t X = prmt(prmt(x0, x1, 0x0062), prmt(x2, x3, 0x6200), 0x7610);
+    const uint32_t Y = prmt(prmt(y0, y1, 0x0062), prmt(y2, y3, 0x6200), 0x7610);
+    return (X & 0x0F0F0F0Fu) | ((Y << 4) & 0xF0F0F0F0u);
+}
+
 __device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
     uint32_t d;
     asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
@@ -72,9 +96,16 @@ __device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
 
 // R = rows per CTA (a multiple of box); box = TMA box height;
 // grid = strips * cs with clusters of cs CTAs.
+// PERMUTED = false: `out` is the packed [K/2][N] matrix.  PERMUTED = true:
+// `out` is permute_int4's layout of it (N*K/2 bytes; K % 64 == 0), written
+// directly: for column n and 32-row group t the 16 bytes at
+// (K/2)*4*(n/4) + (t/2)*128 + 32*(n%4) + 16*(t%2), whose 32-bit word i holds
+// in nibble slots 0..7 the rows 32t + 2i + (0, 8, 16, 24, 1, 9, 17, 25).
+template <bool PERMUTED>
 __global__ void __launch_bounds__(QC_THREADS)
-quantize_pack_cluster_kernel(const __grid_constant__ CUtensorMap tmap, uint8_t* __restrict__ packed,
+quantize_pack_cluster_kernel(const __grid_constant__ CUtensorMap tmap, uint8_t* __restrict__ out,
                              float* __restrict__ scale, int K, int N, int R, int box) {
+    uint8_t* __restrict__ packed = out;
     extern __shared__ __align__(128) uint8_t qtile[];   // [R][32] bf16
     __shared__ __align__(8) uint64_t bar;
     __shared__ __align__(8) uint64_t pm_bar;          // every rank's partial maxima have landed
@@ -169,6 +200,108 @@ quantize_pack_cluster_kernel(const __grid_constant__ CUtensorMap tmap, uint8_t* 
         if (rank == 0 && n0 + tid < N) scale[n0 + tid] = sc;
     }
     __syncthreads();
+
+    if constexpr (PERMUTED) {
+        // quantise 64 rows (two 32-row groups) per warp iteration: lane
+        // (cp, par) takes columns 2cp, 2cp+1 on rows 2i + par of a group
+        // (one 32-bit shared load per row), brackets each weight with two
+        // FMAs, and packs the nibbles of its 16 rows into four half-words per
+        // column; the partner lane (par ^ 1) holds the other half of each
+        // output word.
+        if (__all_sync(0xffffffffu, ok)) {
+            const int cp = lane & 15, par = lane >> 4;
+            const float inv0 = s_inv[2 * cp], inv1 = s_inv[2 * cp + 1];
+            const int mycol = 2 * cp + par;                       // the column this lane stores
+            const bool col_ok = n0 + mycol < N;
+            // output: 128-byte lines of the column's group of four, this
+            // CTA's first line; + 16 * (t % 2) and 128 per group pair
+            uint8_t* dst = out + static_cast<int64_t>(K / 2) * 4 * ((n0 + mycol) / 4) +
+                           static_cast<int64_t>(k0 / 64) * 128 + 32 * (mycol % 4);
+            const uint32_t sel_lo = par ? 0x1054u : 0x5410u, sel_hi = par ? 0x3276u : 0x7632u;
+            const int npairs = rows / 64;
+            for (int pr = warp; pr < npairs; pr += QC_THREADS / 32) {
+                uint4 res[2];
+#pragma unroll
+                for (int tt = 0; tt < 2; ++tt) {
+                    const uint8_t* base = qtile + (64 * pr + 32 * tt + par) * (QC_COLS * 2) + 4 * cp;
+                    // z[col][h]: h = 0 holds half-words 0, 1 (rows i = 0,4,8,12 | 1,5,9,13),
+                    // h = 1 half-words 2, 3 (i + 2); zb: the same from the lower bracket
+                    uint32_t z[2][2], zb[2][2];
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        // rows i in nibble order x0 y0 x1 y1 x2 y2 x3 y3
+                        constexpr int ix[4] = {0, 8, 1, 9}, iy[4] = {4, 12, 5, 13};
+                        uint32_t wx[4], wy[4];
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            wx[k] = *reinterpret_cast<const uint32_t*>(base + (2 * (ix[k] + 2 * h)) * (QC_COLS * 2));
+                            wy[k] = *reinterpret_cast<const uint32_t*>(base + (2 * (iy[k] + 2 * h)) * (QC_COLS * 2));
+                        }
+#pragma unroll
+                        for (int col = 0; col < 2; ++col) {
+                            const float inv = col ? inv1 : inv0;
+                            uint32_t ux[4], uy[4], vx[4], vy[4];
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) {
+                                const float fx = __uint_as_float(col ? (wx[k] & 0xFFFF0000u) : (wx[k] << 16));
+                                const float fy = __uint_as_float(col ? (wy[k] & 0xFFFF0000u) : (wy[k] << 16));
+                                ux[k] = __float_as_uint(__fmaf_rn(fx, inv, QB_HI));
+                                uy[k] = __float_as_uint(__fmaf_rn(fy, inv, QB_HI));
+                                vx[k] = __float_as_uint(__fmaf_rn(fx, inv, QB_LO));
+                                vy[k] = __float_as_uint(__fmaf_rn(fy, inv, QB_LO));
+                            }
+                            z[col][h] = pack_nibbles(ux[0], ux[1], ux[2], ux[3], uy[0], uy[1], uy[2], uy[3]);
+                            zb[col][h] = pack_nibbles(vx[0], vx[1], vx[2], vx[3], vy[0], vy[1], vy[2], vy[3]);
+                        }
+                    }
+                    // weights whose brackets disagree: exact IEEE division
+                    uint32_t fl[2][2];
+                    bool any = false;
+#pragma unroll
+                    for (int col = 0; col < 2; ++col)
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            fl[col][h] = z[col][h] ^ zb[col][h];
+                            any |= fl[col][h] != 0;
+                        }
+                    if (__any_sync(0xffffffffu, any)) {
+#pragma unroll
+                        for (int col = 0; col < 2; ++col)
+#pragma unroll
+                            for (int h = 0; h < 2; ++h) {
+                                uint32_t f = fl[col][h];
+                                while (f != 0) {
+                                    const int nib = (__ffs(f) - 1) >> 2;   // nibble slot 0..7
+                                    f &= ~(0xFu << (4 * nib));
+                                    // slot -> row i: even slots ix[slot/2], odd iy[slot/2] (+ 2h)
+                                    const int k = nib >> 1;
+                                    const int i = (k >> 1) + 8 * (k & 1) + 4 * (nib & 1) + 2 * h;
+                                    const uint32_t e =
+                                        reinterpret_cast<const uint16_t*>(base + (2 * i) * (QC_COLS * 2))[col];
+                                    const uint32_t nibv = quant_nibble(e, s_scale[2 * cp + col]);
+                                    z[col][h] = (z[col][h] & ~(0xFu << (4 * nib))) | (nibv << (4 * nib));
+                                }
+                            }
+                    }
+                    // lane par = 0 keeps column 2cp, par = 1 column 2cp+1: trade the
+                    // other column's half-words with the partner lane
+                    const uint32_t send0 = par ? z[0][0] : z[1][0], send1 = par ? z[0][1] : z[1][1];
+                    const uint32_t own0 = par ? z[1][0] : z[0][0], own1 = par ? z[1][1] : z[0][1];
+                    const uint32_t r0 = __shfl_xor_sync(0xffffffffu, send0, 16);
+                    const uint32_t r1 = __shfl_xor_sync(0xffffffffu, send1, 16);
+                    // word i: half-word i of the even rows (low) and of the odd rows (high)
+                    res[tt] = make_uint4(__byte_perm(own0, r0, sel_lo), __byte_perm(own0, r0, sel_hi),
+                                         __byte_perm(own1, r1, sel_lo), __byte_perm(own1, r1, sel_hi));
+                }
+                if (col_ok) {
+                    uint4* d = reinterpret_cast<uint4*>(dst + static_cast<int64_t>(pr) * 128);
+                    d[0] = res[0];
+                    d[1] = res[1];
+                }
+            }
+        }
+        return;
+    }
 
     // quantise the resident rows two at a time (low nibble = even row).
     // Control flow is warp-uniform: the trip count is the warp's, lanes past
@@ -319,8 +452,9 @@ quantize_pack_kernel(const uint16_t* __restrict__ W, uint8_t* __restrict__ packe
 namespace {
 
 // Single-read path; W4_ERR_SHAPE means "use the two-pass kernel".
+// permuted = true writes permute_int4's layout (requires K % 64 == 0).
 w4_status launch_quantize_cluster(const void* W, void* packed, float* scale, int64_t K, int64_t N,
-                                  cudaStream_t stream) {
+                                  cudaStream_t stream, bool permuted) {
     if ((N % 8) != 0 || K > QC_MAX_K || N > 0x7FFFFFFF) return W4_ERR_SHAPE;
     const int64_t strips = (N + QC_COLS - 1) / QC_COLS;
     // rows per CTA: whole TMA boxes, 1024 rows (64 KB) per CTA while the
@@ -350,8 +484,9 @@ w4_status launch_quantize_cluster(const void* W, void* packed, float* scale, int
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return W4_ERR_CUDA;
     const int smem = R * QC_COLS * 2;
-    static int smem_set[64];
-    if (ensure_smem_limit(quantize_pack_cluster_kernel, smem, smem_set) != cudaSuccess) return W4_ERR_CUDA;
+    static int smem_set[2][64];
+    auto kern = permuted ? quantize_pack_cluster_kernel<true> : quantize_pack_cluster_kernel<false>;
+    if (ensure_smem_limit(kern, smem, smem_set[permuted ? 1 : 0]) != cudaSuccess) return W4_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(strips * cs), 1, 1);
     cfg.blockDim = dim3(QC_THREADS, 1, 1);
@@ -364,16 +499,15 @@ w4_status launch_quantize_cluster(const void* W, void* packed, float* scale, int
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return launch_status(cudaLaunchKernelEx(&cfg, quantize_pack_cluster_kernel, tmap,
-                                            static_cast<uint8_t*>(packed), scale, static_cast<int>(K),
-                                            static_cast<int>(N), R, box));
+    return launch_status(cudaLaunchKernelEx(&cfg, kern, tmap, static_cast<uint8_t*>(packed), scale,
+                                            static_cast<int>(K), static_cast<int>(N), R, box));
 }
 
 }  // namespace
 
 w4_status run_quantize_pack(const void* W, void* packed, float* scale, int64_t K, int64_t N,
                             cudaStream_t stream) {
-    const w4_status st = launch_quantize_cluster(W, packed, scale, K, N, stream);
+    const w4_status st = launch_quantize_cluster(W, packed, scale, K, N, stream, false);
     if (st != W4_ERR_SHAPE) return st;
     const int64_t strips = (N + QP_COLS - 1) / QP_COLS;
     if (strips > 0x7FFFFFFF) return W4_ERR_SHAPE;
@@ -576,6 +710,15 @@ w4_status run_permute(const void* packed, void* out, int64_t K, int64_t N, cudaS
     permute_kernel<<<grid, PM_THREADS, 0, stream>>>(static_cast<const uint8_t*>(packed), static_cast<uint8_t*>(out),
                                                     K, N);
     return launch_status(cudaGetLastError());
+}
+
+// quantize_pack_int4 followed by permute_int4 in one pass over W (the
+// single-read kernel writing the permuted layout); W4_ERR_SHAPE unless
+// N % 8 == 0, K % 64 == 0 and K <= QC_MAX_K.
+w4_status run_quantize_pack_permute(const void* W, void* out, float* scale, int64_t K, int64_t N,
+                                    cudaStream_t stream) {
+    if ((K % 64) != 0) return W4_ERR_SHAPE;
+    return launch_quantize_cluster(W, out, scale, K, N, stream, true);
 }
 
 int take_device_error_quant() { return take_unit_device_error(); }

@@ -10,6 +10,7 @@ namespace w4 {
 
 w4_status run_quantize_pack(const void* W, void* packed, float* scale, int64_t K, int64_t N, cudaStream_t s);
 w4_status run_permute(const void* packed, void* out, int64_t K, int64_t N, cudaStream_t s);
+w4_status run_quantize_pack_permute(const void* W, void* out, float* scale, int64_t K, int64_t N, cudaStream_t s);
 w4_status run_gemv(const void* qw, const void* scale, const void* zero, const void* x, void* d, int64_t N,
                    int64_t K, int64_t C, w4_dtype dtype, cudaStream_t s);
 w4_status run_gemm(const void* A, const void* B, const void* scale, const void* zero, void* C, int64_t M,
@@ -70,7 +71,7 @@ using namespace w4;
 
 extern "C" {
 
-int w4_abi_version(void) { return 1; }
+int w4_abi_version(void) { return 2; }
 
 int w4_device_error(void* stream) {
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return -1;
@@ -102,6 +103,17 @@ w4_status quantize_pack_int4(const void* W, void* packed, float* scale, int64_t 
     if (!device_is_sm103()) return W4_ERR_DEVICE;
     if (K == 0) return launch_status(cudaMemsetAsync(scale, 0, N * sizeof(float), (cudaStream_t)stream));
     return run_quantize_pack(W, packed, scale, K, N, (cudaStream_t)stream);
+}
+
+w4_status quantize_pack_permute_int4(const void* W, void* permuted, float* scale, int64_t K, int64_t N,
+                                     void* stream) {
+    if (K < 0 || N < 0 || (K % 64) != 0 || (N % 8) != 0 || K > W4_QUANT_PERMUTE_MAX_K) return W4_ERR_SHAPE;
+    if (N == 0) return W4_OK;
+    if (!scale || (K > 0 && (!W || !permuted))) return W4_ERR_NULL;
+    if (!aligned16(scale) || (K > 0 && (!aligned16(W) || !aligned16(permuted)))) return W4_ERR_ALIGN;
+    if (!device_is_sm103()) return W4_ERR_DEVICE;
+    if (K == 0) return launch_status(cudaMemsetAsync(scale, 0, N * sizeof(float), (cudaStream_t)stream));
+    return run_quantize_pack_permute(W, permuted, scale, K, N, (cudaStream_t)stream);
 }
 
 w4_status permute_int4(const void* packed, void* out, int64_t K, int64_t N, void* stream) {

@@ -123,6 +123,32 @@ w4_status quantize_pack_int4(const void* W, void* packed, float* scale, int64_t 
  */
 w4_status permute_int4(const void* packed, void* out, int64_t K, int64_t N, void* stream);
 
+/* Largest K that quantize_pack_permute_int4 accepts (eight CTAs of a
+ * cluster hold the strip of W in shared memory). */
+#define W4_QUANT_PERMUTE_MAX_K 26624
+
+/*
+ * quantize_pack_permute_int4 -- quantize_pack_int4 and permute_int4 in one
+ * pass: W is read from memory once and the packed matrix is never stored
+ * ("[PHI] add int4 weight only quant kernel, add int4 weight only permute
+ * kernel", sections "int4量化kernel", "int4 permute kernel", "简单的位运算",
+ * "int4 row interval").
+ *
+ * Writes scale exactly as quantize_pack_int4 does, and into `permuted`
+ * (N*K/2 bytes) exactly what permute_int4 would produce from
+ * quantize_pack_int4's packed matrix.  Bit-exact with both definitions.
+ *
+ * W         bf16 [K][N] row-major, 16-byte aligned.
+ * permuted  int8 [N*K/2], 16-byte aligned (output).
+ * scale     fp32 [N], 16-byte aligned (output).
+ * Requires K % 64 == 0, N % 8 == 0 and K <= W4_QUANT_PERMUTE_MAX_K (else
+ * W4_ERR_SHAPE; the two separate calls cover every other shape).  K == 0
+ * writes scale = 0 and nothing else; N == 0 is a no-op.  NaN or Inf in W is
+ * undefined.
+ */
+w4_status quantize_pack_permute_int4(const void* W, void* permuted, float* scale, int64_t K, int64_t N,
+                                     void* stream);
+
 /*
  * gemv_w4 -- fused dequant GEMV / small-batch multiply.
  *

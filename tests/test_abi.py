@@ -26,7 +26,8 @@ def _declared_functions():
 
 def test_header_declares_the_hot_path():
     names = _declared_functions()
-    for fn in ("quantize_pack_int4", "permute_int4", "gemv_w4", "gemv_w4_permuted", "gemm_w4",
+    for fn in ("quantize_pack_int4", "permute_int4", "quantize_pack_permute_int4", "gemv_w4", "gemv_w4_permuted",
+               "gemm_w4",
                "w4_status_string", "w4_abi_version", "w4_device_error"):
         assert fn in names
 
@@ -35,7 +36,7 @@ def test_library_exports_every_declared_symbol():
     lib, _ = _lib()
     for fn in _declared_functions():
         assert hasattr(lib, fn), "libw4.so does not export %s" % fn
-    assert lib.w4_abi_version() == 1
+    assert lib.w4_abi_version() == 2
     assert lib.w4_status_string(-2) == b"illegal size or shape"
 
 
@@ -67,6 +68,15 @@ def test_argument_validation_happens_on_host():
     assert lib.permute_int4(A, A, 0, 8, None) == L.W4_OK
     assert lib.permute_int4(A, None, 64, 8, None) == L.W4_ERR_NULL
     assert lib.permute_int4(A, odd, 64, 8, None) == L.W4_ERR_ALIGN
+    # quantize_pack_permute_int4: the permute's K rule, N % 8, the K limit
+    assert lib.quantize_pack_permute_int4(A, A, A, 96, 8, None) == L.W4_ERR_SHAPE         # K % 64
+    assert lib.quantize_pack_permute_int4(A, A, A, 64, 12, None) == L.W4_ERR_SHAPE        # N % 8
+    assert lib.quantize_pack_permute_int4(A, A, A, 26624 + 64, 8, None) == L.W4_ERR_SHAPE
+    assert lib.quantize_pack_permute_int4(A, A, A, -64, 8, None) == L.W4_ERR_SHAPE
+    assert lib.quantize_pack_permute_int4(A, A, A, 64, 0, None) == L.W4_OK                # N == 0
+    assert lib.quantize_pack_permute_int4(None, A, A, 64, 8, None) == L.W4_ERR_NULL
+    assert lib.quantize_pack_permute_int4(A, A, None, 64, 8, None) == L.W4_ERR_NULL
+    assert lib.quantize_pack_permute_int4(A, odd, A, 64, 8, None) == L.W4_ERR_ALIGN
     # gemv_w4
     assert lib.gemv_w4(A, A, A, A, A, 16, 12, 1, L.W4_BF16, None) == L.W4_ERR_SHAPE
     assert lib.gemv_w4(A, A, A, A, A, 16, 16, 0, L.W4_BF16, None) == L.W4_ERR_SHAPE

@@ -89,6 +89,47 @@ def test_permute_bit_exact(w4, K, N):
     assert _guards_intact(buf, pad, N * K // 2, 0x5A)
 
 
+@pytest.mark.parametrize("K,N", [
+    (64, 8), (128, 64), (256, 40),   # one TMA box per CTA; a strip past the last column
+    (8192, 8192),                    # the quantise+pack+permute workload
+    (4160, 32),                      # five CTAs per cluster, the last holding 64 rows
+    (20480, 24),                     # eight CTAs of 2560 rows, partial strip
+    (26624, 16),                     # longest K accepted
+    (1024, 4104),                    # many strips, N % 32 == 8
+])
+def test_quantize_pack_permute_bit_exact(w4, K, N):
+    """The one-pass call equals permute(quantize_pack(W)) of the oracle."""
+    W = synth.quant_inputs(K, N, seed=K + 3 * N)
+    W[:, 3] = 0                                    # a column of zeros: scale 0, q 0
+    if N > 5:
+        # exact ties of W / s: column 5 holds multiples of max / 14 (k + 1/2 for odd multiples)
+        m = float(W[:, 5].float().abs().max())
+        ties = (torch.arange(K) % 15 - 7).float() * (m / 7.0) * 0.5
+        W[:, 5] = ties.to(torch.bfloat16)
+        W[0, 5] = m
+    buf, out, pad = _guarded(N * K // 2, torch.uint8, 0x3C)
+    sbuf, scale, spad = _guarded(N, torch.float32, -1.0)
+    w4.quantize_pack_permute_int4(W.to(_dev()), out=out, scale=scale)
+    s_ref, p_ref = oracle.quantize_pack(np_bits(W))
+    assert np.array_equal(scale.cpu().numpy().view(np.uint32), s_ref.view(np.uint32))
+    ref = oracle.permute(p_ref, K, N)
+    got = out.cpu().numpy()
+    if not np.array_equal(got, ref):
+        bad = np.nonzero(got != ref)[0]
+        raise AssertionError("%d bytes differ, first at %s" % (bad.size, bad[:8]))
+    assert _guards_intact(buf, pad, N * K // 2, 0x3C)
+    assert _guards_intact(sbuf, spad, N, -1.0)
+
+
+def test_quantize_pack_permute_k_zero(w4):
+    scale = torch.full((16,), 3.0, device=_dev())
+    out = torch.full((8,), 7, dtype=torch.int8, device=_dev())
+    w4.quantize_pack_permute_int4(torch.empty((0, 16), dtype=torch.bfloat16, device=_dev()), out=out[:0],
+                                  scale=scale)
+    assert torch.all(scale == 0)
+    assert torch.all(out == 7)
+
+
 def test_quantize_pack_permute_chain_full_size(w4):
     cfg = synth.QUANT
     W = synth.quant_inputs(cfg["K"], cfg["N"], seed=0)
