@@ -32,7 +32,10 @@ namespace w4 {
 // ---------------------------------------------------------------------------
 
 constexpr int QC_COLS = 32;                      // columns per strip (64-byte rows)
-constexpr int QC_THREADS = 256;
+#ifndef W4_QC_THREADS
+#define W4_QC_THREADS 256
+#endif
+constexpr int QC_THREADS = W4_QC_THREADS;
 constexpr int QC_RL = QC_THREADS / 4;            // row lanes (4 threads of 8 columns per row)
 constexpr int QC_CS = 8;                         // CTAs per cluster at most (K-slices)
 constexpr int QC_BOXR = 256;                     // rows per TMA box
@@ -254,34 +257,37 @@ quantize_pack_cluster_kernel(const __grid_constant__ CUtensorMap tmap, uint8_t* 
                             zb[col][h] = pack_nibbles(vx[0], vx[1], vx[2], vx[3], vy[0], vy[1], vy[2], vy[3]);
                         }
                     }
-                    // weights whose brackets disagree: exact IEEE division
-                    uint32_t fl[2][2];
-                    bool any = false;
-#pragma unroll
-                    for (int col = 0; col < 2; ++col)
-#pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            fl[col][h] = z[col][h] ^ zb[col][h];
-                            any |= fl[col][h] != 0;
+                    // Weights whose brackets disagree lie within 2^-15 of a tie
+                    // m = k + 1/2 (k = integer part of the lower bracket - 192).
+                    // Exact ties (w = m s, the usual case: the FMA residual is
+                    // then exactly 0) round away from zero; the rest take the
+                    // exact IEEE division.  One weight per trip of a lane.
+                    uint32_t f0 = z[0][0] ^ zb[0][0], f1 = z[0][1] ^ zb[0][1];
+                    uint32_t f2 = z[1][0] ^ zb[1][0], f3 = z[1][1] ^ zb[1][1];
+                    if (__any_sync(0xffffffffu, (f0 | f1 | f2 | f3) != 0)) {
+                        while ((f0 | f1 | f2 | f3) != 0) {
+                            const int wsel = f0 ? 0 : f1 ? 1 : f2 ? 2 : 3;   // word: col = wsel / 2, h = wsel % 2
+                            const uint32_t f = wsel == 0 ? f0 : wsel == 1 ? f1 : wsel == 2 ? f2 : f3;
+                            const int nib = (__ffs(f) - 1) >> 2;              // nibble slot 0..7
+                            const int col = wsel >> 1, h = wsel & 1;
+                            // slot -> row i: even slots ix[slot/2], odd iy[slot/2] (+ 2h)
+                            const int kk = nib >> 1;
+                            const int i = (kk >> 1) + 8 * (kk & 1) + 4 * (nib & 1) + 2 * h;
+                            const uint32_t e = reinterpret_cast<const uint16_t*>(base + (2 * i) * (QC_COLS * 2))[col];
+                            const float wf = bf16_bits_to_f32(e);
+                            const float sc = s_scale[2 * cp + col];
+                            const uint32_t ulo = __float_as_uint(__fmaf_rn(wf, col ? inv1 : inv0, QB_LO));
+                            const int k = 128 + static_cast<int>((ulo >> 16) & 0x7Fu) - 192;
+                            const float m = static_cast<float>(k) + 0.5f;
+                            uint32_t nibv;
+                            if (__fmaf_rn(-m, sc, wf) == 0.0f) nibv = static_cast<uint32_t>(m > 0.0f ? k + 1 : k) & 0xFu;
+                            else nibv = quant_nibble(e, sc);
+                            const uint32_t keep = ~(0xFu << (4 * nib)), put = nibv << (4 * nib);
+                            if (wsel == 0) { f0 &= keep; z[0][0] = (z[0][0] & keep) | put; }
+                            else if (wsel == 1) { f1 &= keep; z[0][1] = (z[0][1] & keep) | put; }
+                            else if (wsel == 2) { f2 &= keep; z[1][0] = (z[1][0] & keep) | put; }
+                            else { f3 &= keep; z[1][1] = (z[1][1] & keep) | put; }
                         }
-                    if (__any_sync(0xffffffffu, any)) {
-#pragma unroll
-                        for (int col = 0; col < 2; ++col)
-#pragma unroll
-                            for (int h = 0; h < 2; ++h) {
-                                uint32_t f = fl[col][h];
-                                while (f != 0) {
-                                    const int nib = (__ffs(f) - 1) >> 2;   // nibble slot 0..7
-                                    f &= ~(0xFu << (4 * nib));
-                                    // slot -> row i: even slots ix[slot/2], odd iy[slot/2] (+ 2h)
-                                    const int k = nib >> 1;
-                                    const int i = (k >> 1) + 8 * (k & 1) + 4 * (nib & 1) + 2 * h;
-                                    const uint32_t e =
-                                        reinterpret_cast<const uint16_t*>(base + (2 * i) * (QC_COLS * 2))[col];
-                                    const uint32_t nibv = quant_nibble(e, s_scale[2 * cp + col]);
-                                    z[col][h] = (z[col][h] & ~(0xFu << (4 * nib))) | (nibv << (4 * nib));
-                                }
-                            }
                     }
                     // lane par = 0 keeps column 2cp, par = 1 column 2cp+1: trade the
                     // other column's half-words with the partner lane
