@@ -361,6 +361,7 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const void* __restrict__ scale,
                 constexpr int XR = 10;
                 const int dn = per_n > 0 ? CT / per_n : 0, dj = CT - dn * per_n;
                 const int n_cur = per_n > 0 ? tid / per_n : C, j_cur = tid - n_cur * per_n;
+                const int mine = (C * per_n - tid + CT - 1) / CT;   // entries of this thread (<= XR)
                 const uint8_t* rows = reinterpret_cast<const uint8_t*>(xf);
                 uint32_t* xmax = reinterpret_cast<uint32_t*>(xsum) + 16;   // fp16: max |x| bits, zeroed at entry
                 uint4 v[XR];
@@ -369,6 +370,7 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const void* __restrict__ scale,
                 int n = n_cur, j = j_cur;
 #pragma unroll
                 for (int b = 0; b < XR; ++b) {
+                    if (b >= mine) break;
                     v[b] = make_uint4(0, 0, 0, 0);
                     if (n < C) {
                         const int kk = (j >> 4) * KB + 32 * (j & 3) + 8 * ((j >> 2) & 3);
@@ -399,6 +401,7 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const void* __restrict__ scale,
                 j = j_cur;
 #pragma unroll
                 for (int b = 0; b < XR; ++b) {
+                    if (b >= mine) break;
                     if (n < C) {
                         const int t = j & 3, p = (j >> 2) & 3, kb = j >> 4;
                         const uint4 r = v[b];
