@@ -623,7 +623,24 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const void* __restrict__ scale,
             if (i < nrows) sz[i] = sz_pf[j];
         }
         for (int i = tid + 2 * CT; i < nrows; i += CT) sz[i] = load_sz(r0 + i);
-        if (P.perwarp) {
+        if (S == 1) {
+            // no K split: add the warps' partials (or take the tile sums),
+            // fold the zero point, scale and store straight away
+            named_barrier(1, CT);
+            for (int i = tid; i < nrows * C; i += CT) {
+                const int r = i / C, c = i - r * C;
+                float v;
+                if (P.perwarp) {
+                    v = 0.f;
+                    for (int w = 0; w < NC; ++w) v += partw[static_cast<size_t>(w) * rows16 * C + i];
+                    v = (v - xsum[16 + c]) * xsum[24 + c];
+                } else {
+                    v = part[i];
+                }
+                const float2 s_z = sz[r];
+                d[static_cast<int64_t>(c) * N + r0 + r] = __float2bfloat16_rn(s_z.x * fmaf(-s_z.y, xsum[c], v));
+            }
+        } else if (P.perwarp) {
             named_barrier(1, CT);
             for (int i = tid; i < nrows * C; i += CT) {
                 float v = 0.f;
@@ -633,6 +650,7 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const void* __restrict__ scale,
             }
         }
     }
+    if (S == 1) return;   // (the producer has drained its copies)
     __syncthreads();
 
     // part[] holds sum_k q x per (row, column) over this CTA's K-slice, in
