@@ -20,24 +20,26 @@ namespace w4 {
 // ---------------------------------------------------------------------------
 // quantize_pack_int4, single HBM read (N % 8 == 0, K <= QC_MAX_K)
 //
-// A thread-block cluster of cs CTAs owns a strip of 32 columns over all K;
+// A thread-block cluster of cs CTAs (up to 16, a non-portable cluster size)
+// owns a strip of 32 columns over all K;
 // CTA r holds rows [r*R, r*R + R) of the strip in shared memory, loaded once
 // with 2-D TMA boxes (64 bytes x up to 256 rows).  Each CTA reduces its rows
 // to a per-column max |W| (bf16 bit patterns with the sign cleared order
 // non-negative values exactly), the CTAs read each other's partial maxima
 // through distributed shared memory, and every CTA then quantises the rows it
 // already holds.  W is read from HBM exactly once.  Algorithmic bytes: 2 B
-// read per weight + 0.5 B written.  64 KB per CTA for K = 8192, so three
-// CTAs share an SM and one's copy overlaps another's arithmetic.
+// read per weight + 0.5 B written.  32 KB per CTA for K = 8192 (sixteen
+// CTAs of 512 rows), so several CTAs share an SM and one's copy overlaps
+// another's arithmetic (eight CTAs of 64 KB measured 3.5% slower).
 // ---------------------------------------------------------------------------
 
 constexpr int QC_COLS = 32;                      // columns per strip (64-byte rows)
-#ifndef W4_QC_THREADS
-#define W4_QC_THREADS 256
-#endif
-constexpr int QC_THREADS = W4_QC_THREADS;
+constexpr int QC_THREADS = 256;
 constexpr int QC_RL = QC_THREADS / 4;            // row lanes (4 threads of 8 columns per row)
-constexpr int QC_CS = 8;                         // CTAs per cluster at most (K-slices)
+constexpr int QC_CS = 8;                         // K limit: eight CTAs of QC_MAX_R rows
+constexpr int QC_CS_USE = 16;                    // CTAs per cluster at most (non-portable size)
+constexpr int QC_BPC = 2;                        // TMA boxes per CTA aimed for (512 rows, 32 KB)
+constexpr int QC_CS_ALLOC = QC_CS_USE > QC_CS ? QC_CS_USE : QC_CS;
 constexpr int QC_BOXR = 256;                     // rows per TMA box
 constexpr int QC_SMEM = 208 * 1024;              // strip rows per CTA at most (bytes)
 constexpr int QC_MAX_R = QC_SMEM / (QC_COLS * 2) / QC_BOXR * QC_BOXR;
@@ -112,7 +114,7 @@ quantize_pack_cluster_kernel(const __grid_constant__ CUtensorMap tmap, uint8_t* 
     extern __shared__ __align__(128) uint8_t qtile[];   // [R][32] bf16
     __shared__ __align__(8) uint64_t bar;
     __shared__ __align__(8) uint64_t pm_bar;          // every rank's partial maxima have landed
-    __shared__ uint32_t pm_all[QC_CS][QC_COLS];       // partial maxima, one row per rank
+    __shared__ uint32_t pm_all[QC_CS_ALLOC][QC_COLS]; // partial maxima, one row per rank
     __shared__ uint32_t wmax[QC_THREADS / 32][QC_COLS];
     __shared__ float s_scale[QC_COLS], s_inv[QC_COLS];
     __shared__ int abort_word;
@@ -472,7 +474,7 @@ w4_status launch_quantize_cluster(const void* W, void* packed, float* scale, int
         box = R;
     } else {
         const int64_t boxes = (K + QC_BOXR - 1) / QC_BOXR;
-        cs = static_cast<int>(std::min<int64_t>(QC_CS, (boxes + 3) / 4));
+        cs = static_cast<int>(std::min<int64_t>(QC_CS_USE, (boxes + QC_BPC - 1) / QC_BPC));
         const int64_t bpc = (boxes + cs - 1) / cs;
         R = static_cast<int>(bpc * QC_BOXR);
         box = QC_BOXR;
@@ -493,6 +495,8 @@ w4_status launch_quantize_cluster(const void* W, void* packed, float* scale, int
     static int smem_set[2][64];
     auto kern = permuted ? quantize_pack_cluster_kernel<true> : quantize_pack_cluster_kernel<false>;
     if (ensure_smem_limit(kern, smem, smem_set[permuted ? 1 : 0]) != cudaSuccess) return W4_ERR_CUDA;
+    if (cs > 8 && cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+        return W4_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(strips * cs), 1, 1);
     cfg.blockDim = dim3(QC_THREADS, 1, 1);
