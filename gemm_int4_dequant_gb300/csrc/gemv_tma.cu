@@ -106,7 +106,7 @@ struct Plan {
 };
 
 struct Layout {
-    int stage_bytes, xf, xzero, red, part, partw, xsw, xsum, sz, bars, abort, total;
+    int stage_bytes, xf, xzero, red, part, partw, xsw, xsum, sz, rcv, rxs, bars, abort, total;
 };
 
 __host__ __device__ inline Layout make_layout(int C, const Plan& P) {
@@ -126,8 +126,12 @@ __host__ __device__ inline Layout make_layout(int C, const Plan& P) {
     // undoes the scaling of x
     L.xsum = o;      o += 32 * 4;
     L.sz = o;        o += P.rows_cap * 8;          // (scale, zero) per row as fp32
+    // K split: the other slices' partials of the rows this rank owns (rows
+    // ks, ks+S, ...) and their sums of x, pushed in by the peers
+    L.rcv = o;       o += P.S > 1 ? P.S * ((P.rows_cap + P.S - 1) / P.S) * C * 4 : 0;
+    L.rxs = o;       o += P.S > 1 ? 8 * 8 * 4 : 0;
     o = (o + 7) & ~7;
-    L.bars = o;      o += (2 * MAX_NST + 1) * 8;   // full[], empty[], x copied
+    L.bars = o;      o += (2 * MAX_NST + 2) * 8;   // full[], empty[], x copied, pushes received
     L.abort = o;     o += 16;
     L.total = o;
     return L;
@@ -178,6 +182,7 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const void* __restrict__ scale,
     const uint32_t bar_full = sm_addr + L.bars;
     const uint32_t bar_empty = bar_full + MAX_NST * 8;
     const uint32_t bar_x = bar_full + 2 * MAX_NST * 8;
+    const uint32_t bar_rcv = bar_x + 8;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L.abort);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -203,8 +208,18 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const void* __restrict__ scale,
         mbar_init(bar_x, 1);
         *abort_flag = 0;
         for (int c = 0; c < 8; ++c) reinterpret_cast<uint32_t*>(xsum)[16 + c] = 0;   // column maxima of |x|
+        if (S > 1) {
+            // every peer pushes its partials of the rows this rank owns and its
+            // C sums of x; they complete bytes on this barrier
+            const int own = nrows > ks ? (nrows - ks + S - 1) / S : 0;
+            mbar_init(bar_rcv, 1);
+            mbar_arrive_expect_tx(bar_rcv, static_cast<uint32_t>((S - 1) * (own * C + C) * 4));
+        }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    // first half of a cluster barrier: this CTA's barriers are initialised
+    // (the second half is waited for just before the first push to a peer)
+    if (S > 1) asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
     // Launched with programmatic stream serialisation.  The next kernel in
     // the stream may be scheduled at once: its CTAs take SMs as they come
     // free (idle SMs first) and prepare while this grid finishes, and its own
@@ -655,38 +670,52 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const void* __restrict__ scale,
 
     // part[] holds sum_k q x per (row, column) over this CTA's K-slice, in
     // the units of x (offset folded out, scaling undone); xsum[0, C) the
-    // slice's sum of x.  Combine the K-slices of the cluster, fold the zero
-    // point, scale, store.  Rank ks writes rows ks, ks+S, ...; every
-    // (row, c) is one thread, so the remote (distributed shared memory) loads
-    // of all ranks are in flight at once.
-    cg::cluster_group cluster = cg::this_cluster();
-    float* xs_tot = xsum + 8;
-    if (S > 1) cluster.sync();
-    if (tid < C) {
-        float v = 0.f;
-        for (int r = 0; r < S; ++r) v += (S > 1 ? cluster.map_shared_rank(xsum, r) : xsum)[tid];
-        xs_tot[tid] = v;
+    // slice's sum of x.  Rank ks owns rows ks, ks+S, ...: every rank pushes
+    // its partials of the rows the others own, and its sums of x, into their
+    // shared memory (st.async, completing bytes on the owner's barrier); an
+    // owner adds the S slices in rank order, folds the zero point, scales
+    // and stores.  No CTA reads another's shared memory, so CTAs do not meet
+    // at exit; each waits (bounded) until every push into it has landed.
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");   // every peer is initialised
+    float* rcv = reinterpret_cast<float*>(sm + L.rcv);
+    float* rxs = reinterpret_cast<float*>(sm + L.rxs);
+    const int own_cap = (P.rows_cap + S - 1) / S;
+    {
+        const uint32_t rcv_l = smem_u32(rcv), rxs_l = smem_u32(rxs);
+        for (int j = tid; j < nrows * C; j += THREADS) {
+            const int i = j / C, c = j - i * C;
+            const int owner = i % S;
+            if (owner == ks) continue;
+            const uint32_t dst = map_cluster(rcv_l + ((ks * own_cap + i / S) * C + c) * 4, owner);
+            asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.u32 [%0], %1, [%2];" ::"r"(dst),
+                         "r"(__float_as_uint(part[j])), "r"(map_cluster(bar_rcv, owner))
+                         : "memory");
+        }
+        if (tid < C) {
+            for (int r = 0; r < S; ++r) {
+                if (r == ks) continue;
+                asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.u32 [%0], %1, [%2];" ::"r"(
+                                 map_cluster(rxs_l + (ks * 8 + tid) * 4, r)),
+                             "r"(__float_as_uint(xsum[tid])), "r"(map_cluster(bar_rcv, r))
+                             : "memory");
+            }
+        }
     }
-    __syncthreads();
+    if (!mbar_wait(bar_rcv, 0, abort_flag)) {
+        mbar_drain(bar_rcv, 0);   // a slow peer's push may still be on its way
+        return;
+    }
     const int my_rows = nrows > ks ? (nrows - ks + S - 1) / S : 0;
     for (int j = tid; j < my_rows * C; j += THREADS) {
-        const int i = ks + S * (j / C), c = j - (j / C) * C;
-        float sum = 0.f;
-        if (S > 1) {
-            float v[8];
-#pragma unroll
-            for (int r = 0; r < 8; ++r)
-                if (r < S) v[r] = cluster.map_shared_rank(part, r)[i * C + c];
-#pragma unroll
-            for (int r = 0; r < 8; ++r)
-                if (r < S) sum += v[r];
-        } else {
-            sum = part[i * C + c];
+        const int il = j / C, c = j - il * C, i = ks + S * il;
+        float sum = 0.f, xt = 0.f;
+        for (int r = 0; r < S; ++r) {
+            sum += r == ks ? part[i * C + c] : rcv[(r * own_cap + il) * C + c];
+            xt += r == ks ? xsum[c] : rxs[r * 8 + c];
         }
         const float2 s_z = sz[i];
-        d[static_cast<int64_t>(c) * N + r0 + i] = __float2bfloat16_rn(s_z.x * fmaf(-s_z.y, xs_tot[c], sum));
+        d[static_cast<int64_t>(c) * N + r0 + i] = __float2bfloat16_rn(s_z.x * fmaf(-s_z.y, xt, sum));
     }
-    if (S > 1) cluster.sync();
 }
 
 }  // namespace gtma
