@@ -79,7 +79,7 @@ constexpr int KB = 128;                       // k per unit (one consumer warp p
 constexpr int MAX_NST = 8;                    // stages in the ring (at most)
 constexpr int KCHUNK_MAX = 8192;              // k per stage at most (4 KB per row)
 #ifndef W4_GEMV_PREFETCH_STAGES
-#define W4_GEMV_PREFETCH_STAGES 3               // stages warmed in L2 before the wait
+#define W4_GEMV_PREFETCH_STAGES 3               // stages warmed in L2 before the wait (one column of x)
 #endif
 
 // Nibble mask and bf16 magic passed at run time so they stay in registers and
@@ -238,7 +238,10 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const void* __restrict__ scale,
         const int64_t row_bytes = K / 2;
         const uint8_t* src0 = qw + static_cast<int64_t>(r0) * row_bytes + k0 / 2;
         int tile = 0, ch = 0;
-        for (int s = 0; s < min(nstages, W4_GEMV_PREFETCH_STAGES); ++s) {
+        // one column: three stages (measured best); several columns: one, since
+        // their larger x copy follows the wait and competes with the prefetch
+        constexpr int kPrefetch = C == 1 ? W4_GEMV_PREFETCH_STAGES : 1;
+        for (int s = 0; s < min(nstages, kPrefetch); ++s) {
             const int rows_here = min(16, nrows - tile * 16);
             const int seg = min(P.kchunk, klen - ch * P.kchunk) / 2;
             const uint8_t* src = src0 + static_cast<int64_t>(tile) * 16 * row_bytes + ch * (P.kchunk / 2);
