@@ -199,10 +199,16 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 
 def source_hash(files):
+    """Hash of the kernel sources with comments and whitespace removed, so
+    that the recorded counters stay valid across comment edits and are
+    dropped when any code changes."""
     h = hashlib.sha256()
     for f in files:
-        with open(os.path.join(ROOT, f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, f), encoding="utf-8") as fh:
+            text = fh.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(re.sub(r"\s+", "", text).encode("utf-8"))
     return h.hexdigest()[:16]
 
 

@@ -41,13 +41,16 @@
 //     a power of two (largest |x| in [2^14, 2^15)) before its fp16
 //     conversion, which is exact for every element within 2^32 of the
 //     largest, and the scaling is undone in fp32;
-//   * per 16-row tile the NC partial sums are added in warp order (named
-//     barrier, double-buffered), so results never depend on timing;
+//   * the NC warps' partial sums of a row are added in warp order (each warp
+//     keeps its own row partials, or per 16-row tile through a named
+//     barrier when those do not fit), so results never depend on timing;
 //   * the offset is folded out exactly at the end:
 //       sum_k (q - z) x = sum_k (128 + q) x - (128 + z) sum_k x
 //     (fp16: sum_k (q - z) x = S_even + S_odd / 16 - 1024 X_even - 64 X_odd
-//     - z X, with S the two accumulators and X the sums of x),
-//     and K-slices are combined through distributed shared memory.
+//     - z X, with S the two accumulators and X the sums of x);
+//   * K-slices of a cluster meet at the row's owner: every rank pushes its
+//     partials of the rows the others own into their shared memory
+//     (st.async), and owners add the slices in rank order.
 // Every mbarrier wait is bounded (about two seconds); on timeout the kernel
 // records an error code (w4_device_error), stops issuing copies, drains the
 // ones in flight and returns.
