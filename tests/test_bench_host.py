@@ -1,0 +1,79 @@
+"""Host-side arithmetic of bench.py (no GPU): algorithmic byte counts, the
+roofline record and the source hash that keys the recorded ncu traffic."""
+import os
+import shutil
+
+import pytest
+
+import bench
+
+
+def test_gemv_bytes_decode():
+    # N*K/2 weights + 2N*2 scale/zero + C*K*2 x + C*N*2 d
+    assert bench.gemv_bytes(17280, 5120, 1) == 17280 * 5120 // 2 + 4 * 17280 + 2 * 5120 + 2 * 17280
+    assert bench.gemv_bytes(17280, 5120, 1) == 44350720
+
+
+def test_quant_bytes_one_pass_and_two_calls():
+    K = N = 8192
+    one = bench.quant_bytes(K, N, fused=True)
+    assert one == 2 * K * N + K * N // 2 + 4 * N == 167804928
+    # two calls also write the packed matrix and read it back
+    assert bench.quant_bytes(K, N, fused=False) == one + K * N
+
+
+def test_gemm_bytes_and_flops():
+    assert bench.gemm_flops(8192, 8192, 8192) == 2 * 8192 ** 3
+    assert bench.gemm_bytes(8192, 8192, 8192) == 302022656
+
+
+def test_workloads_name_known_kinds():
+    for name, cfg in bench.WORKLOADS.items():
+        assert cfg["kind"] in ("gemv", "quant", "gemm"), name
+    assert set(bench.COMPONENTS) <= set(bench.WORKLOADS)
+    assert bench.WORKLOADS["quant"]["fused"] and not bench.WORKLOADS["quant_2call"]["fused"]
+
+
+class _Gemv:
+    bytes = 44350720
+    launches_per_step = 1
+
+
+def test_roofline_record_hbm():
+    peaks = {"hbm_gbs": 6772.5}
+    r = bench.roofline(_Gemv(), 10e-6, peaks, "measured", "gemv", "decode")
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s"
+    assert r["achieved"] == pytest.approx(4435.072)
+    assert r["frac"] == pytest.approx(4435.072 / 6772.5)
+
+
+def test_source_hash_ignores_comments_but_not_code(tmp_path, monkeypatch):
+    src = tmp_path / "k.cu"
+    src.write_text("// header\n__global__ void k(int* p) {\n  p[0] = 1; /* one */\n}\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    h0 = bench.source_hash(["k.cu"])
+    src.write_text("// another header\n__global__ void k(int* p) {\n    p[0] = 1;   // set\n}\n")
+    assert bench.source_hash(["k.cu"]) == h0
+    src.write_text("__global__ void k(int* p) {\n  p[0] = 2;\n}\n")
+    assert bench.source_hash(["k.cu"]) != h0
+
+
+def test_recorded_traffic_matches_current_sources():
+    """Every committed ncu summary names the hash of the code it measured;
+    the bench reports its traffic only while that hash is current."""
+    for workload, kind in (("decode", "gemv"), ("c8_perm", "gemv"), ("quant", "quant"), ("gemm", "gemm")):
+        t = bench.recorded_traffic(kind, workload)
+        assert t is not None and t > 0, workload
+
+
+def test_recorded_traffic_drops_on_code_change(tmp_path, monkeypatch):
+    root = tmp_path / "repo"
+    for rel in bench.KERNEL_SOURCES["gemv"] + ["profiles/" + bench.PROFILE_FILES["decode"]]:
+        dst = root / rel
+        dst.parent.mkdir(parents=True, exist_ok=True)
+        shutil.copy(os.path.join(bench.ROOT, rel), dst)
+    monkeypatch.setattr(bench, "ROOT", str(root))
+    assert bench.recorded_traffic("gemv", "decode") is not None
+    f = root / bench.KERNEL_SOURCES["gemv"][0]
+    f.write_text(f.read_text() + "\nstatic int changed_code = 1;\n")
+    assert bench.recorded_traffic("gemv", "decode") is None
