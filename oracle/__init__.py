@@ -35,6 +35,12 @@ def _load():
         lib.w4o_permute.restype = ctypes.c_int
         lib.w4o_gemv_packed.argtypes = [P, P, P, L, L, L, L, L, P, P]
         lib.w4o_gemv_packed.restype = None
+        lib.w4o_quantize_int8.argtypes = [P, L, L, P, P]
+        lib.w4o_quantize_int8.restype = None
+        lib.w4o_permute_int8.argtypes = [P, L, L, P]
+        lib.w4o_permute_int8.restype = ctypes.c_int
+        lib.w4o_gemv_int8.argtypes = [P, P, P, L, L, L, L, L, P, P]
+        lib.w4o_gemv_int8.restype = None
         _lib = lib
     return _lib
 
@@ -176,3 +182,55 @@ def permute(packed, K, N):
     if lib.w4o_permute(_ptr(p), K, N, _ptr(out)) != 0:
         raise MemoryError("oracle permute could not allocate its stream")
     return out
+
+
+# ---------------------------------------------------------------------------
+# int8 weight-only variant
+# ---------------------------------------------------------------------------
+
+def quantize_int8(W_bits):
+    """Symmetric per-column int8 quantisation of W [K, N] (uint16 bf16
+    patterns).  Returns (scale float32 [N], q int8 [K, N])."""
+    lib = _load()
+    W = np.ascontiguousarray(W_bits, dtype=np.uint16)
+    K, N = W.shape
+    scale = np.empty(N, np.float32)
+    q = np.empty((K, N), np.int8)
+    lib.w4o_quantize_int8(_ptr(W), K, N, _ptr(scale), _ptr(q))
+    return scale, q
+
+
+def permute_int8(q, K, N):
+    """Page-1 int8 permute of q [K, N] into N*K interleaved bytes."""
+    lib = _load()
+    a = np.ascontiguousarray(q, dtype=np.int8)
+    if a.shape != (K, N):
+        raise ValueError("q must be [K, N]")
+    if K % 64 or N % 2:
+        raise ValueError("the int8 permute needs K % 64 == 0 and N % 2 == 0")
+    out = np.zeros(N * K, np.uint8)
+    if lib.w4o_permute_int8(_ptr(a), K, N, _ptr(out)) != 0:
+        raise MemoryError("oracle permute could not allocate its stream")
+    return out
+
+
+def gemv_int8(q, scale, x_bits, cols=None):
+    """d[c, n] = sum_k x[c, k] * q[k, n] * scale[n], in fp64.
+
+    q: int8 [K, N]; scale: float32 [N]; x_bits: uint16 bf16 patterns [C, K].
+    cols: optional (begin, end) column range; columns outside it are NaN.
+    Returns (d, ref_abs), both float64 [C, N].
+    """
+    lib = _load()
+    a = np.ascontiguousarray(q, dtype=np.int8)
+    s = np.ascontiguousarray(scale, dtype=np.float32)
+    xb = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    K, N = a.shape
+    C = xb.shape[0] if xb.ndim == 2 else 1
+    if xb.size != C * K or s.size != N:
+        raise ValueError("shape mismatch")
+    b, e = (0, N) if cols is None else cols
+    d = np.full((C, N), np.nan)
+    ref = np.full((C, N), np.nan)
+    lib.w4o_gemv_int8(_ptr(a), _ptr(s), _ptr(xb), N, K, C, b, e, _ptr(d), _ptr(ref))
+    return d, ref

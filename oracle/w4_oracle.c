@@ -18,7 +18,8 @@
  *   [P1] "[PHI] add int4 weight only quant kernel, add int4 weight only
  *        permute kernel" (Paddle PR #64091): sections "int4量化kernel",
  *        "int4 permute kernel", "如何从int8 permute转换为int4 permute",
- *        "简单的位运算", "int4 row interval".
+ *        "简单的位运算", "int4 row interval" (the last two also describe the
+ *        int8 permute the int4 one is derived from).
  *   [P2] "怎样在安卓端利用 Vulkan 编写 4-bit 专用算子" (Vulkan 4-bit GEMV blog):
  *        section 1 "数据打包策略", section 2 "核心 GLSL 算子实现".
  *   [P3] "int4 gemm kernel" (pytorch/helion issue #508): the
@@ -254,4 +255,105 @@ int w4o_permute(const uint8_t* packed, long K, long N, uint8_t* out) {
     }
     free(stream);
     return 0;
+}
+
+
+/* ------------------------------------------------------------------------
+ * int8 weight-only variant (the int8 counterpart of the path above).
+ * ------------------------------------------------------------------------ */
+
+/*
+ * int8 weight-only quantisation: the int4 quantiser's definition with the
+ * int8 range ([P1] quantises to int4 and describes the int8 permute its
+ * int4 permute is derived from; the quantiser formula is the same reading):
+ *   scale[n] = (float)max_k |W[k][n]| / 127.0f        (IEEE fp32 division)
+ *   q[k][n]  = clamp(roundf(W[k][n] / scale[n]), -128, 127)
+ * round half away from zero, an IEEE fp32 quotient, a column of zeros has
+ * scale 0 and q = 0.  One weight per byte: q is int8 [K][N] row-major.
+ */
+void w4o_quantize_int8(const uint16_t* W, long K, long N, float* scale, int8_t* q) {
+    for (long n = 0; n < N; ++n) {
+        float amax = 0.0f;
+        for (long k = 0; k < K; ++k) {
+            float a = fabsf(bf16_bits_to_float(W[k * N + n]));
+            if (a > amax) amax = a;
+        }
+        float s = amax / 127.0f;
+        scale[n] = s;
+        for (long k = 0; k < K; ++k) {
+            float w = bf16_bits_to_float(W[k * N + n]);
+            float r = (s == 0.0f) ? 0.0f : roundf(w / s);
+            if (r < -128.0f) r = -128.0f;
+            if (r > 127.0f) r = 127.0f;
+            q[k * N + n] = (int8_t)(int)r;
+        }
+    }
+}
+
+/*
+ * [P1 section "如何从int8 permute转换为int4 permute"]: the int8 permute_kk,
+ * the destination of source element t inside each group of 16 consecutive
+ * elements of a column's stream.  Copied from the page;
+ * tests/test_oracle_pins.py derives the int4 permute_kk from it by the
+ * page's steps.
+ */
+static const int k_permute_kk16_int8[16] = {0, 2, 4, 6, 8, 10, 12, 14, 1, 3, 5, 7, 9, 11, 13, 15};
+
+/*
+ * int8 weight-only permute, [P1] in the page's order:
+ *   1. element permute: source element kk of column n's stream (the K
+ *      weights q[0..K-1][n]) moves to 16*(kk/16) + permute_kk_int8[kk%16];
+ *   2. row interleave ([P1 section "int4 row interval"]: for int8 two
+ *      adjacent rows -- output columns -- interleave every 64 elements):
+ *      element permute_kk of column n lands at
+ *      permute_kk % 64 + permute_kk / 64 * 128 + 64 * (n % 2) + total_k * 2 * (n / 2)
+ *      with total_k = K (one element per byte).
+ * There is no nibble swap for int8.  Input: q int8 [K][N].  Output: N*K
+ * bytes.  Requires K % 64 == 0 and N % 2 == 0.  Returns 0, or -1 if the
+ * scratch stream cannot be allocated.
+ */
+int w4o_permute_int8(const int8_t* q, long K, long N, uint8_t* out) {
+    long total_k = K;
+    uint8_t* stream = (uint8_t*)malloc((size_t)(total_k > 0 ? total_k : 1));
+    if (!stream) return -1;
+    for (long n_id = 0; n_id < N; ++n_id) {
+        /* step 1 */
+        for (long kk = 0; kk < total_k; ++kk) {
+            long permute_kk = (kk / 16) * 16 + k_permute_kk16_int8[kk % 16];
+            stream[permute_kk] = (uint8_t)q[kk * N + n_id];
+        }
+        /* step 2 */
+        for (long permute_kk = 0; permute_kk < total_k; ++permute_kk) {
+            long permute_index = permute_kk % 64 + permute_kk / 64 * 128 + 64 * (n_id % 2) +
+                                 total_k * 2 * (n_id / 2);
+            out[permute_index] = stream[permute_kk];
+        }
+    }
+    free(stream);
+    return 0;
+}
+
+/*
+ * GEMV over the int8 quantised matrix ([P4 section 3] batched form, the
+ * weight q[k][n] * scale[n] of the symmetric quantiser):
+ *   d[c][n] = sum_k x[c][k] * q[k][n] * scale[n],  x bf16 [C][K], d[c*N + n].
+ * Columns [col_begin, col_end) are computed; ref_abs (may be NULL) receives
+ * sum_k |w * x|.
+ */
+void w4o_gemv_int8(const int8_t* q, const float* scale, const uint16_t* x, long N, long K, long C,
+                   long col_begin, long col_end, double* d, double* ref_abs) {
+    for (long c = 0; c < C; ++c) {
+        for (long n = col_begin; n < col_end; ++n) {
+            double s = (double)scale[n];
+            double sum = 0.0, abs_sum = 0.0;
+            for (long k = 0; k < K; ++k) {
+                double w = (double)q[k * N + n] * s;
+                double xv = (double)bf16_bits_to_float(x[c * K + k]);
+                sum += xv * w;
+                abs_sum += fabs(xv * w);
+            }
+            d[c * N + n] = sum;
+            if (ref_abs) ref_abs[c * N + n] = abs_sum;
+        }
+    }
 }

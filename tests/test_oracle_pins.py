@@ -397,3 +397,103 @@ def test_gemm_sampled_equals_full():
     ni = rng.integers(0, N, 30)
     part, _ = oracle.gemm_at(A, B, s, z, mi, ni)
     assert np.array_equal(part, full[mi, ni])
+
+
+# ---------------------------------------------------------------------------
+# int8 weight-only variant: quantiser, permute, GEMV
+# ---------------------------------------------------------------------------
+
+def test_quantize_int8_exact_grid_and_ties():
+    """Column max 127/128 gives scale exactly 2^-7 (IEEE fp32 division of a
+    value 127 * 2^-7 by 127); multiples k * 2^-7 quantise to k, and the
+    exact ties (k + 1/2) * 2^-7 round away from zero."""
+    ks = np.arange(-127, 128)
+    grid = ks * 2.0 ** -7
+    ties = (np.arange(-127, 127) + 0.5) * 2.0 ** -7       # every half step inside the range
+    K = max(grid.size, ties.size)
+    W = np.zeros((K, 2))
+    W[: grid.size, 0] = grid
+    W[: ties.size, 1] = ties
+    W[0, 1] = 127 * 2.0 ** -7                               # column 1 max |w| = 127/128 as well
+    s, q = oracle.quantize_int8(bf16_bits(W))
+    assert s[0] == np.float32(2.0 ** -7) and s[1] == np.float32(2.0 ** -7)
+    assert np.array_equal(q[: grid.size, 0], ks)
+    t = ties[1:]
+    expect = np.where(t > 0, np.floor(t * 128) + 1, np.ceil(t * 128) - 1)   # away from zero
+    assert np.array_equal(q[1: ties.size, 1], expect.astype(np.int64))
+    assert q[0, 1] == 127
+
+
+def test_quantize_int8_invariants_random():
+    rng = np.random.default_rng(7)
+    W = (rng.standard_normal((300, 24)) * 0.02).astype(np.float32)
+    W[:, 5] = 0.0
+    bits = bf16_bits(W)
+    w = bf16_values(bits)
+    s, q = oracle.quantize_int8(bits)
+    amax = np.abs(w).max(axis=0)
+    assert np.array_equal(s, (amax.astype(np.float32) / np.float32(127.0)).astype(np.float32))
+    assert s[5] == 0 and not q[:, 5].any()
+    qi = q.astype(np.int64)
+    assert np.abs(qi).max() <= 127
+    # the column maximum quantises to +-127
+    top = np.abs(w).argmax(axis=0)
+    for n in range(24):
+        if n != 5:
+            assert abs(qi[top[n], n]) == 127
+    # within half a step, plus the rounding of the fp32 quotient (|w/s| <= 127,
+    # so at most 2^-17 of a step) that decides ties
+    err = np.abs(w - qi * s.astype(np.float64))
+    assert np.all(err <= s.astype(np.float64) * (0.5 + 2.0 ** -16))
+    # sign symmetric
+    s2, q2 = oracle.quantize_int8(bf16_bits(-W))
+    assert np.array_equal(s2, s) and np.array_equal(q2, -q)
+
+
+@pytest.mark.parametrize("K,N", [(64, 2), (128, 2), (64, 4)])
+def test_permute_int8_places_elements_by_page_rules(K, N):
+    """Every element lands where the page puts it: inside each 16-element
+    group source t goes to permute_kk_int8[t]; two adjacent columns share
+    each 128-byte line, 64 elements each."""
+    dst16 = G["permute_kk_int8"]
+    ids = np.arange(K * N).reshape(K, N)
+    # label planes of 7 bits (int8 values 0..127) until every id is covered
+    planes = int(np.ceil(np.log2(K * N) / 7))
+    found = np.zeros(N * K, np.int64)
+    for p in range(planes):
+        out = oracle.permute_int8(((ids >> (7 * p)) & 0x7F).astype(np.int8), K, N)
+        found |= out.astype(np.int64) << (7 * p)
+    assert np.array_equal(np.sort(found), np.arange(K * N)), "not a bijection"
+    for k in range(K):
+        for n in range(N):
+            pk = 16 * (k // 16) + dst16[k % 16]
+            pos = pk % 64 + (pk // 64) * 128 + 64 * (n % 2) + K * 2 * (n // 2)
+            assert found[pos] == k * N + n
+
+
+def test_permute_int8_groups_pair_even_and_odd_halves():
+    """Read back in output order, each 16-element group alternates the first
+    and second halves of the source group: 0 8 1 9 2 10 ... (the inverse
+    of the page's destination list)."""
+    K, N = 64, 2
+    q = np.tile(np.arange(K, dtype=np.int8)[:, None], (1, N))
+    out = oracle.permute_int8(q, K, N)
+    first = out[:16].tolist()
+    assert first == [0, 8, 1, 9, 2, 10, 3, 11, 4, 12, 5, 13, 6, 14, 7, 15]
+
+
+def test_gemv_int8_matches_dense_matmul_and_one_hot():
+    rng = np.random.default_rng(3)
+    K, N, C = 96, 40, 3
+    q = rng.integers(-128, 128, (K, N), dtype=np.int64).astype(np.int8)
+    s = rng.uniform(1e-3, 1e-2, N).astype(np.float32)
+    x = bf16_bits(rng.standard_normal((C, K)))
+    d, ref = oracle.gemv_int8(q, s, x)
+    Wd = q.astype(np.float64) * s.astype(np.float64)[None, :]
+    xd = bf16_values(x)
+    assert np.allclose(d, xd @ Wd, rtol=1e-12, atol=1e-12)
+    assert np.allclose(ref, np.abs(xd) @ np.abs(Wd), rtol=1e-12, atol=1e-12)
+    onehot = np.zeros((1, K))
+    onehot[0, 17] = 1.0
+    d1, _ = oracle.gemv_int8(q, s, bf16_bits(onehot))
+    assert np.array_equal(d1[0], q[17].astype(np.float64) * s.astype(np.float64))
