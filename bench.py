@@ -19,7 +19,8 @@ Python API with x copied from pinned host memory and d copied back every
 step (weights stay resident, as in a decode loop).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload decode|c4|c8|c4s|c8s|c4_perm|c8_perm|c4s_perm|c8s_perm|gemm|quant|quant_2call]
+                    [--workload decode|c4|c8|c4s|c8s|c4_perm|c8_perm|c4s_perm|c8s_perm|gemm|quant|quant_2call
+                                |w8_decode|w8_quant]
                     [--no-components]
 """
 import argparse
@@ -60,8 +61,13 @@ WORKLOADS = {
     "c8_perm": dict(kind="gemv", N=5120, K=17280, C=8, perm=True),
     "c4s_perm": dict(kind="gemv", N=6144, K=5120, C=4, perm=True),
     "c8s_perm": dict(kind="gemv", N=6144, K=5120, C=8, perm=True),
+    # the int8 weight-only variant: GEMV over quantize_int8's matrix, and
+    # quantize_int8 + permute_int8 of one 8192x8192 weight
+    "w8_decode": dict(kind="gemv8", N=17280, K=5120, C=1),
+    "w8_quant": dict(kind="quant8", K=8192, N=8192),
 }
-COMPONENTS = ["c4", "c8", "c4s", "c8s", "c4_perm", "c8_perm", "c4s_perm", "c8s_perm", "quant", "quant_2call", "gemm"]
+COMPONENTS = ["c4", "c8", "c4s", "c8s", "c4_perm", "c8_perm", "c4s_perm", "c8s_perm", "quant", "quant_2call", "gemm",
+              "w8_decode", "w8_quant"]
 
 
 def load_peaks():
@@ -87,6 +93,16 @@ def quant_bytes(K, N, fused=True):
     # packed matrix's write and re-read
     one_pass = K * N * 2 + K * N // 2 + 4 * N
     return one_pass if fused else one_pass + 2 * (K * N // 2)
+
+
+def gemv8_bytes(N, K, C):
+    # int8 weights + fp32 scale + x + d
+    return N * K + 4 * N + 2 * C * K + 2 * C * N
+
+
+def quant8_bytes(K, N):
+    # quantize_int8: read W, write q + scale; permute_int8: read + write q
+    return (2 * K * N + K * N + 4 * N) + 2 * K * N
 
 
 def gemm_bytes(M, N, K):
@@ -310,6 +326,55 @@ class GemvPermWork:
         return "rotating %d permuted weight copies (%.0f MB > 2x L2)" % (self.R, self.R * self.N * self.K / 2 / 1e6)
 
 
+class Gemv8Work:
+    """gemv_w8 over rotating copies of an int8 weight."""
+
+    def __init__(self, w4, N, K, C, seed=0):
+        g = synth.int8_gemv_inputs(N, K, C, seed=seed)
+        self.g = g
+        dev = torch.device("cuda")
+        self.R = copies_for(N * K)
+        self.q = [g.q.to(dev) for _ in range(self.R)]
+        self.s, self.x = g.scale.to(dev), g.x.to(dev)
+        self.d = torch.empty((C, N), dtype=torch.bfloat16, device=dev)
+        self.w4 = w4
+        self.i = 0
+        self.N, self.K, self.C = N, K, C
+        self.bytes = gemv8_bytes(N, K, C)
+        self.flops = 2 * N * K * C
+        self.launches_per_step = 1
+
+    def step(self):
+        self.w4.gemv_w8(self.q[self.i % self.R], self.s, self.x, out=self.d)
+        self.i += 1
+
+    def l2_note(self):
+        return "rotating %d int8 weight copies (%.0f MB > 2x L2)" % (self.R, self.R * self.N * self.K / 1e6)
+
+
+class Quant8Work:
+    """quantize_int8 + permute_int8 of one weight."""
+
+    def __init__(self, w4, K, N, seed=0):
+        dev = torch.device("cuda")
+        self.W = synth.quant_inputs(K, N, seed=seed).to(dev)
+        self.q = torch.empty((K, N), dtype=torch.int8, device=dev)
+        self.scale = torch.empty((N,), dtype=torch.float32, device=dev)
+        self.out = torch.empty((N * K,), dtype=torch.int8, device=dev)
+        self.w4 = w4
+        self.K, self.N = K, N
+        self.bytes = quant8_bytes(K, N)
+        self.flops = 0
+        self.launches_per_step = 2
+
+    def step(self):
+        self.w4.quantize_int8(self.W, q=self.q, scale=self.scale)
+        self.w4.permute_int8(self.q, out=self.out)
+
+    def l2_note(self):
+        return "W is %.0f MB > L2" % (self.K * self.N * 2 / 1e6)
+
+
 class QuantWork:
     def __init__(self, w4, K, N, fused=True, seed=0):
         dev = torch.device("cuda")
@@ -365,6 +430,10 @@ def make_work(w4, name):
         return GemvWork(w4, **cfg)
     if kind == "quant":
         return QuantWork(w4, **cfg)
+    if kind == "gemv8":
+        return Gemv8Work(w4, **cfg)
+    if kind == "quant8":
+        return Quant8Work(w4, **cfg)
     return GemmWork(w4, **cfg)
 
 
@@ -412,10 +481,13 @@ def e2e_gemv(w4, work, steps, world):
     x_dev = torch.empty_like(work.x)
     stream = torch.cuda.current_stream()
     perm = isinstance(work, GemvPermWork)
+    w8 = isinstance(work, Gemv8Work)
 
     def call(i):
         if perm:
             w4.gemv_w4_permuted(work.q[i % work.R], work.s, x_dev, out=work.d)
+        elif w8:
+            w4.gemv_w8(work.q[i % work.R], work.s, x_dev, out=work.d)
         else:
             w4.gemv_w4(work.q[i % work.R], work.s, work.z, x_dev, out=work.d)
 
@@ -543,6 +615,36 @@ def cpu_baseline(name, budget_s=10.0):
         return {"value": flops / t_total / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
                 "sample": "%d sampled outputs of the 8192^3 GEMM (fp64 C oracle, single thread), %.1f s" %
                           (n_out, t_total)}
+    if cfg["kind"] == "gemv8":
+        g = synth.int8_gemv_inputs(cfg["N"], cfg["K"], cfg["C"], seed=0)
+        q, scale, xb = g.q.numpy(), g.scale.numpy(), np_bits(g.x)
+        N = cfg["N"]
+        done, t_total, c0 = 0, 0.0, 0
+        cols = 256
+        while t_total < budget_s:
+            c1 = min(N, c0 + cols)
+            t0 = time.perf_counter()
+            oracle.gemv_int8(q, scale, xb, cols=(c0, c1))
+            t_total += time.perf_counter() - t0
+            done += c1 - c0
+            c0 = 0 if c1 >= N else c1
+        return {"value": gemv8_bytes(cfg["N"], cfg["K"], cfg["C"]) * done / N / t_total / 1e9, "unit": "GB/s",
+                "cores": 1, "kind": "oracle",
+                "sample": "%d columns of the %dx%d C=%d int8 GEMV (fp64 C oracle, single thread), %.1f s" %
+                          (done, cfg["N"], cfg["K"], cfg["C"], t_total)}
+    if cfg["kind"] == "quant8":
+        K, N = cfg["K"], cfg["N"]
+        W = np_bits(synth.quant_inputs(K, N, seed=0))
+        n_done, t_total = 0, 0.0
+        while t_total < budget_s:
+            t0 = time.perf_counter()
+            s_ref, q_ref = oracle.quantize_int8(W)
+            oracle.permute_int8(q_ref, K, N)
+            t_total += time.perf_counter() - t0
+            n_done += 1
+        return {"value": quant8_bytes(K, N) * n_done / t_total / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                "sample": "%d full int8 quantize+permute of %dx%d (C oracle, single thread), %.1f s" %
+                          (n_done, K, N, t_total)}
     K, N = cfg["K"], cfg["N"]
     W = np_bits(synth.quant_inputs(K, N, seed=0))
     n_done, t_total = 0, 0.0
@@ -598,7 +700,7 @@ def run_ours(args, world, rank):
         soak(g, stream, 2.0)
         sec2, _, _ = time_graph(work, args.steps, 0, world)
     clocks = cs.summary()
-    if kind == "gemv":
+    if kind in ("gemv", "gemv8"):
         e2e_sec, hb, ob = e2e_gemv(w4, work, args.steps, world)
     else:
         e2e_sec, hb, ob = e2e_generic(work, max(2, min(args.steps, 10)), world)
@@ -616,8 +718,8 @@ def run_ours(args, world, rank):
         "clocks": clocks,
         "e2e": {"value": e2e_val, "unit": unit_of(work), "h2d_bytes_per_step": hb, "d2h_bytes_per_step": ob},
     }
-    if kind == "quant" and not WORKLOADS[args.workload].get("fused", True):
-        line["roofline"]["note"] = "two kernels per step (quantize_pack_int4 + permute_int4); achieved = step bytes / step time"
+    if kind == "quant8" or (kind == "quant" and not WORKLOADS[args.workload].get("fused", True)):
+        line["roofline"]["note"] = "two kernels per step (quantise, then permute); achieved = step bytes / step time"
     if rank == 0 and world == 1:
         line["cpu_baseline"] = cpu_baseline(args.workload, budget_s=args.cpu_seconds)
     if args.components and world == 1:

@@ -12,14 +12,17 @@ in the library's CUDA kernels; there is no CPU or eager fallback.
     gemv_w4(qweight, scale, zero, x)    -> d [C, N]
     gemv_w4_permuted(permuted, scale, x) -> d [C, N] bf16 (over permute_int4's output)
     gemm_w4(A, B, scale, zero)          -> C [M, N] bf16
+    quantize_int8(W)                    -> (q [K, N] int8, scale [N] fp32)
+    permute_int8(q)                     -> out [N*K] int8 (interleaved)
+    gemv_w8(q, scale, x)                -> d [C, N] bf16
 """
 import torch
 
 from . import _lib
 from ._lib import W4Error, W4_BF16, W4_F32
 
-__all__ = ["quantize_pack_int4", "permute_int4", "quantize_pack_permute_int4", "gemv_w4", "gemv_w4_permuted", "gemm_w4", "device_error",
-           "W4Error"]
+__all__ = ["quantize_pack_int4", "permute_int4", "quantize_pack_permute_int4", "gemv_w4", "gemv_w4_permuted", "gemm_w4",
+           "quantize_int8", "permute_int8", "gemv_w8", "device_error", "W4Error"]
 
 _lib.load()  # fail loudly at import if the CUDA library is missing
 
@@ -173,6 +176,59 @@ def gemm_w4(A, B, scale, zero, out=None, stream=None):
     st = _lib.load().gemm_w4(A.data_ptr(), B.data_ptr(), scale.data_ptr(), zero.data_ptr(), out.data_ptr(),
                              M, N, K, _stream(stream))
     _lib.check("gemm_w4", st)
+    return out
+
+
+def quantize_int8(W, q=None, scale=None, stream=None):
+    """Symmetric per-column int8 quantisation of W [K, N] bf16."""
+    _need(W, "W", (torch.bfloat16,), 2)
+    K, N = W.shape
+    if q is None:
+        q = torch.empty((K, N), dtype=torch.int8, device=W.device)
+    if scale is None:
+        scale = torch.empty((N,), dtype=torch.float32, device=W.device)
+    _need(q, "q", (torch.int8,))
+    _need(scale, "scale", (torch.float32,))
+    if q.numel() != K * N or scale.numel() != N:
+        raise ValueError("output shapes do not match W")
+    st = _lib.load().quantize_int8(W.data_ptr(), q.data_ptr(), scale.data_ptr(), K, N, _stream(stream))
+    _lib.check("quantize_int8", st)
+    return q, scale
+
+
+def permute_int8(q, out=None, stream=None):
+    """Page-1 int8 interleave permute of q [K, N] into N*K bytes."""
+    _need(q, "q", (torch.int8, torch.uint8), 2)
+    K, N = q.shape
+    if out is None:
+        out = torch.empty((N * K,), dtype=q.dtype, device=q.device)
+    _need(out, "out", (torch.int8, torch.uint8))
+    if out.numel() != N * K:
+        raise ValueError("out must hold N*K bytes")
+    st = _lib.load().permute_int8(q.data_ptr(), out.data_ptr(), K, N, _stream(stream))
+    _lib.check("permute_int8", st)
+    return out
+
+
+def gemv_w8(q, scale, x, out=None, stream=None):
+    """d[c, n] = sum_k q[k, n] * scale[n] * x[c, k]; q int8 [K, N], scale fp32 [N],
+    x bf16 [C, K] (C <= 8).  Returns bf16 [C, N]."""
+    _need(q, "q", (torch.int8,), 2)
+    _need(scale, "scale", (torch.float32,), 1)
+    _need(x, "x", (torch.bfloat16,))
+    xx = x if x.dim() == 2 else x.reshape(1, -1)
+    K, N = q.shape
+    C = xx.shape[0]
+    if xx.shape[1] != K or scale.numel() != N:
+        raise ValueError("shape mismatch")
+    if out is None:
+        out = torch.empty((C, N), dtype=torch.bfloat16, device=x.device)
+    _need(out, "out", (torch.bfloat16,))
+    if out.numel() != C * N:
+        raise ValueError("out must hold C*N elements")
+    st = _lib.load().gemv_w8(q.data_ptr(), scale.data_ptr(), xx.data_ptr(), out.data_ptr(), N, K, C,
+                             _stream(stream))
+    _lib.check("gemv_w8", st)
     return out
 
 

@@ -51,6 +51,12 @@ def load():
     lib.gemv_w4_permuted.restype = I
     lib.gemm_w4.argtypes = [P, P, P, P, P, I64, I64, I64, P]
     lib.gemm_w4.restype = I
+    lib.quantize_int8.argtypes = [P, P, P, I64, I64, P]
+    lib.quantize_int8.restype = I
+    lib.permute_int8.argtypes = [P, P, I64, I64, P]
+    lib.permute_int8.restype = I
+    lib.gemv_w8.argtypes = [P, P, P, P, I64, I64, I64, P]
+    lib.gemv_w8.restype = I
     _lib = lib
     return lib
 

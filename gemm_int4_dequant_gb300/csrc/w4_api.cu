@@ -17,6 +17,10 @@ w4_status run_gemm(const void* A, const void* B, const void* scale, const void* 
                    int64_t N, int64_t K, cudaStream_t s);
 w4_status run_gemv_permuted(const void* permuted, const float* scale, const void* x, void* d, int N, int K, int C,
                             cudaStream_t s);
+w4_status run_quantize_int8(const void* W, void* q, float* scale, int64_t K, int64_t N, cudaStream_t s);
+w4_status run_permute_int8(const void* q, void* out, int64_t K, int64_t N, cudaStream_t s);
+w4_status run_gemv_w8(const void* q, const float* scale, const void* x, void* d, int64_t N, int64_t K, int64_t C,
+                      cudaStream_t s);
 int take_device_error_gemm();
 int take_device_error_gemv();
 int take_device_error_quant();
@@ -71,7 +75,7 @@ using namespace w4;
 
 extern "C" {
 
-int w4_abi_version(void) { return 2; }
+int w4_abi_version(void) { return 3; }
 
 int w4_device_error(void* stream) {
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return -1;
@@ -152,6 +156,36 @@ w4_status gemv_w4_permuted(const void* permuted, const float* scale, const void*
     if (K == 0) return launch_status(cudaMemsetAsync(d, 0, C * N * 2, (cudaStream_t)stream));
     return run_gemv_permuted(permuted, scale, x, d, static_cast<int>(N), static_cast<int>(K), static_cast<int>(C),
                              (cudaStream_t)stream);
+}
+
+w4_status quantize_int8(const void* W, void* q, float* scale, int64_t K, int64_t N, void* stream) {
+    if (K < 0 || N < 0) return W4_ERR_SHAPE;
+    if (N == 0) return W4_OK;
+    if (!scale || (K > 0 && (!W || !q))) return W4_ERR_NULL;
+    if (!aligned16(scale) || (K > 0 && (!aligned16(W) || !aligned16(q)))) return W4_ERR_ALIGN;
+    if (!device_is_sm103()) return W4_ERR_DEVICE;
+    if (K == 0) return launch_status(cudaMemsetAsync(scale, 0, N * sizeof(float), (cudaStream_t)stream));
+    return run_quantize_int8(W, q, scale, K, N, (cudaStream_t)stream);
+}
+
+w4_status permute_int8(const void* q, void* out, int64_t K, int64_t N, void* stream) {
+    if (K < 0 || N < 0 || (K % 64) != 0 || (N % 2) != 0) return W4_ERR_SHAPE;
+    if (K == 0 || N == 0) return W4_OK;
+    if (!q || !out) return W4_ERR_NULL;
+    if (!aligned16(q) || !aligned16(out)) return W4_ERR_ALIGN;
+    if (!device_is_sm103()) return W4_ERR_DEVICE;
+    return run_permute_int8(q, out, K, N, (cudaStream_t)stream);
+}
+
+w4_status gemv_w8(const void* q, const float* scale, const void* x, void* d, int64_t N, int64_t K, int64_t C,
+                  void* stream) {
+    if (N < 0 || K < 0 || C < 1 || C > 8) return W4_ERR_SHAPE;
+    if (N == 0) return W4_OK;
+    if (!d || !scale || (K > 0 && (!q || !x))) return W4_ERR_NULL;
+    if (!aligned16(d) || !aligned16(scale) || (K > 0 && (!aligned16(q) || !aligned16(x)))) return W4_ERR_ALIGN;
+    if (!device_is_sm103()) return W4_ERR_DEVICE;
+    if (K == 0) return launch_status(cudaMemsetAsync(d, 0, C * N * 2, (cudaStream_t)stream));
+    return run_gemv_w8(q, scale, x, d, N, K, C, (cudaStream_t)stream);
 }
 
 w4_status gemm_w4(const void* A, const void* B, const void* scale, const void* zero, void* C, int64_t M, int64_t N,

@@ -19,6 +19,9 @@
  *                       int4 -> 16-bit dequant), symmetric per-column scale.
  *   gemm_w4             large-M bf16 x int4 dequant GEMM
  *                       ("int4 gemm kernel", the matmul_bf16_int4 example).
+ *   quantize_int8, permute_int8, gemv_w8
+ *                       the int8 weight-only counterparts (the first page's
+ *                       int8 permute, from which its int4 permute derives).
  *
  * Conventions shared by every entry point:
  *   - All data pointers are DEVICE pointers owned by the caller.  The library
@@ -213,6 +216,56 @@ w4_status gemv_w4_permuted(const void* permuted, const float* scale, const void*
  */
 w4_status gemm_w4(const void* A, const void* B, const void* scale, const void* zero, void* C,
                   int64_t M, int64_t N, int64_t K, void* stream);
+
+/*
+ * quantize_int8 -- symmetric per-column int8 quantisation of W[K][N] (the
+ * int4 quantiser's definition with the int8 range; "[PHI] add int4 weight
+ * only quant kernel, add int4 weight only permute kernel").
+ *
+ *   scale[n] = max_k |W[k][n]| / 127              (IEEE fp32 division)
+ *   q[k][n]  = clamp(round(W[k][n] / scale[n]), -128, 127)
+ *              (IEEE fp32 division; round half away from zero; a column
+ *              whose maximum is 0 gets scale 0 and q = 0)
+ *
+ * W      bf16 [K][N] row-major, 16-byte aligned.
+ * q      int8 [K][N] row-major, 16-byte aligned (output).
+ * scale  fp32 [N], 16-byte aligned (output).
+ * K == 0 writes scale = 0 and nothing else; N == 0 is a no-op.  NaN or Inf
+ * in W is undefined.  Bit-exact with the definition above.
+ */
+w4_status quantize_int8(const void* W, void* q, float* scale, int64_t K, int64_t N, void* stream);
+
+/*
+ * permute_int8 -- the int8 interleave permute (same page, section
+ * "如何从int8 permute转换为int4 permute" for the element order and section
+ * "int4 row interval" for the interleave of two adjacent columns every 64
+ * elements).  For each column n, with b[k] = q[k][n]:
+ *   1. element permute inside every 16-element group: source element t goes
+ *      to position (0 2 4 6 8 10 12 14 1 3 5 7 9 11 13 15)[t];
+ *   2. row interleave: element kk of the column's permuted stream is stored
+ *      at out[kk%64 + (kk/64)*128 + 64*(n%2) + K*2*(n/2)].
+ * There is no nibble swap for int8.
+ *
+ * q    int8 [K][N] (the output of quantize_int8), 16-byte aligned.
+ * out  int8 [N*K], 16-byte aligned (output).
+ * Requires K % 64 == 0 and N % 2 == 0 (else W4_ERR_SHAPE); K == 0 or
+ * N == 0 is a no-op.  Bit-exact.
+ */
+w4_status permute_int8(const void* q, void* out, int64_t K, int64_t N, void* stream);
+
+/*
+ * gemv_w8 -- GEMV / small-batch multiply by the int8 quantised matrix.
+ *
+ *   d[c][n] = sum_k q[k][n] * scale[n] * x[c][k],  0 <= c < C
+ *
+ * q      int8 [K][N] (quantize_int8's output), 16-byte aligned.
+ * scale  fp32 [N], 16-byte aligned.
+ * x      bf16 [C][K] row-major; d bf16 [C][N] row-major (output).
+ * 1 <= C <= 8 (else W4_ERR_SHAPE); K == 0 gives d = 0.  fp32 accumulation,
+ * one bf16 rounding; the tolerance is gemv_w4's (2e-3 * sum_k |w*x|).
+ */
+w4_status gemv_w8(const void* q, const float* scale, const void* x, void* d, int64_t N, int64_t K, int64_t C,
+                  void* stream);
 
 #ifdef __cplusplus
 }

@@ -90,6 +90,28 @@ def packed_gemv_inputs(N, K, C, seed=0, scale_range=(0.005, 0.02)):
     return PackedGemvInputs(packed, scale, x, N, K, C)
 
 
+@dataclass
+class Int8GemvInputs:
+    q: torch.Tensor       # int8 [K, N]
+    scale: torch.Tensor   # float32 [N]
+    x: torch.Tensor       # bf16 [C, K]
+    N: int
+    K: int
+    C: int
+
+
+def int8_gemv_inputs(N, K, C, seed=0, scale_range=(2.0e-4, 8.0e-4)):
+    """The int8 quantiser's operand: uniform int8 weights, fp32 per-column
+    scale in the range the int8 quantiser gives for N(0, 0.02) weights,
+    x ~ N(0,1) bf16."""
+    g = _gen(seed)
+    q = torch.randint(-128, 128, (K, N), dtype=torch.int16, generator=g).to(torch.int8)
+    lo, hi = scale_range
+    scale = torch.rand(N, generator=g, dtype=torch.float32) * (hi - lo) + lo
+    x = torch.randn(C, K, generator=g, dtype=torch.float32).to(torch.bfloat16)
+    return Int8GemvInputs(q, scale, x, N, K, C)
+
+
 def quant_inputs(K, N, seed=0, std=0.02):
     """W bf16 [K, N] ~ N(0, std)."""
     g = _gen(seed)

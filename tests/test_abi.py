@@ -27,7 +27,7 @@ def _declared_functions():
 def test_header_declares_the_hot_path():
     names = _declared_functions()
     for fn in ("quantize_pack_int4", "permute_int4", "quantize_pack_permute_int4", "gemv_w4", "gemv_w4_permuted",
-               "gemm_w4",
+               "gemm_w4", "quantize_int8", "permute_int8", "gemv_w8",
                "w4_status_string", "w4_abi_version", "w4_device_error"):
         assert fn in names
 
@@ -36,7 +36,7 @@ def test_library_exports_every_declared_symbol():
     lib, _ = _lib()
     for fn in _declared_functions():
         assert hasattr(lib, fn), "libw4.so does not export %s" % fn
-    assert lib.w4_abi_version() == 2
+    assert lib.w4_abi_version() == 3
     assert lib.w4_status_string(-2) == b"illegal size or shape"
 
 
@@ -94,6 +94,20 @@ def test_argument_validation_happens_on_host():
     assert lib.gemv_w4_permuted(A, A, A, A, 0, 128, 1, None) == L.W4_OK
     assert lib.gemv_w4_permuted(A, None, A, A, 16, 128, 1, None) == L.W4_ERR_NULL
     assert lib.gemv_w4_permuted(odd, A, A, A, 16, 128, 1, None) == L.W4_ERR_ALIGN
+    # int8 variant
+    assert lib.quantize_int8(A, A, A, -1, 8, None) == L.W4_ERR_SHAPE
+    assert lib.quantize_int8(A, A, A, 4, 0, None) == L.W4_OK
+    assert lib.quantize_int8(A, None, A, 4, 8, None) == L.W4_ERR_NULL
+    assert lib.quantize_int8(A, A, odd, 4, 8, None) == L.W4_ERR_ALIGN
+    assert lib.permute_int8(A, A, 96, 8, None) == L.W4_ERR_SHAPE        # K % 64
+    assert lib.permute_int8(A, A, 64, 7, None) == L.W4_ERR_SHAPE        # N % 2
+    assert lib.permute_int8(A, A, 0, 8, None) == L.W4_OK
+    assert lib.permute_int8(None, A, 64, 8, None) == L.W4_ERR_NULL
+    assert lib.gemv_w8(A, A, A, A, 16, 64, 0, None) == L.W4_ERR_SHAPE
+    assert lib.gemv_w8(A, A, A, A, 16, 64, 9, None) == L.W4_ERR_SHAPE
+    assert lib.gemv_w8(A, A, A, A, 0, 64, 1, None) == L.W4_OK
+    assert lib.gemv_w8(A, A, None, A, 16, 64, 1, None) == L.W4_ERR_NULL
+    assert lib.gemv_w8(A, A, A, odd, 16, 64, 1, None) == L.W4_ERR_ALIGN
     # gemm_w4
     assert lib.gemm_w4(A, A, A, A, A, 128, 256, 100, None) == L.W4_ERR_SHAPE
     assert lib.gemm_w4(A, A, A, A, A, 128, 250, 128, None) == L.W4_ERR_SHAPE

@@ -369,3 +369,63 @@ def test_gemm_k_zero(w4):
     out = torch.full((4, 16), 2.0, dtype=torch.bfloat16, device=_dev())
     w4.gemm_w4(A, B, s, s, out=out)
     assert torch.all(out == 0)
+
+
+# ---------------------------------------------------------------------------
+# int8 weight-only variant: quantize_int8, permute_int8 (bit-exact), gemv_w8
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("K,N", [(1, 8), (64, 2), (130, 37), (1024, 1000), (8192, 8192)])
+def test_quantize_int8_bit_exact(w4, K, N):
+    W = synth.quant_inputs(K, N, seed=K + 5 * N)
+    if N > 3:
+        W[:, 3] = 0                                  # a column of zeros: scale 0, q 0
+    if N > 5 and K > 1:
+        # exact ties of W / s: half steps of a column whose max is 127/128 (scale 2^-7)
+        t = (torch.arange(K) % 253 - 126).float() + 0.5
+        W[:, 5] = (t * 2.0 ** -7).to(torch.bfloat16)
+        W[0, 5] = 127 * 2.0 ** -7
+    buf, q, pad = _guarded(K * N, torch.int8, 91)
+    q, scale = w4.quantize_int8(W.to(_dev()), q=q)
+    s_ref, q_ref = oracle.quantize_int8(np_bits(W))
+    assert np.array_equal(scale.cpu().numpy().view(np.uint32), s_ref.view(np.uint32))
+    assert np.array_equal(q.cpu().numpy().reshape(K, N), q_ref)
+    assert _guards_intact(buf, pad, K * N, 91)
+
+
+@pytest.mark.parametrize("K,N", [(64, 2), (128, 6), (1024, 1000), (4160, 1042)])
+def test_permute_int8_bit_exact(w4, K, N):
+    g = torch.Generator().manual_seed(K * 3 + N)
+    q = torch.randint(-128, 128, (K, N), dtype=torch.int16, generator=g).to(torch.int8)
+    buf, out, pad = _guarded(N * K, torch.uint8, 0x5A)
+    w4.permute_int8(q.view(torch.uint8).to(_dev()), out=out)
+    assert np.array_equal(out.cpu().numpy(), oracle.permute_int8(q.numpy(), K, N))
+    assert _guards_intact(buf, pad, N * K, 0x5A)
+
+
+@pytest.mark.parametrize("N,K,C", [(1, 1, 1), (37, 100, 3), (300, 4096, 8), (1000, 5120, 1), (17280, 5120, 1),
+                                   (5120, 17280, 4)])
+def test_gemv_w8(w4, N, K, C):
+    gi = synth.int8_gemv_inputs(N, K, C, seed=N + K + C)
+    buf, out, pad = _guarded(C * N, torch.bfloat16, -7.0)
+    w4.gemv_w8(gi.q.to(_dev()), gi.scale.to(_dev()), gi.x.to(_dev()), out=out)
+    ref, ref_abs = oracle.gemv_int8(gi.q.numpy(), gi.scale.numpy(), np_bits(gi.x))
+    got = out.float().cpu().numpy().astype(np.float64).reshape(C, N)
+    bad = parity_violations(got, ref, ref_abs, BF16_TOL, bf16_out=True)
+    assert not bad.any(), "max err/ref_abs = %g" % (np.abs(got - ref) / np.maximum(ref_abs, 1e-300)).max()
+    assert _guards_intact(buf, pad, C * N, -7.0)
+
+
+def test_int8_quantise_permute_gemv_chain(w4):
+    """quantize_int8 -> permute_int8 and quantize_int8 -> gemv_w8 on one
+    weight, each against the oracle applied to the oracle's quantisation."""
+    K, N, C = 1024, 512, 2
+    W = synth.quant_inputs(K, N, seed=21)
+    x = synth.int8_gemv_inputs(N, K, C, seed=22).x
+    q, scale = w4.quantize_int8(W.to(_dev()))
+    s_ref, q_ref = oracle.quantize_int8(np_bits(W))
+    perm = w4.permute_int8(q)
+    assert np.array_equal(perm.cpu().numpy().view(np.uint8), oracle.permute_int8(q_ref, K, N))
+    d = w4.gemv_w8(q, scale, x.to(_dev()))
+    ref, ref_abs = oracle.gemv_int8(q_ref, s_ref, np_bits(x))
+    assert not parity_violations(d.float().cpu().numpy(), ref, ref_abs, BF16_TOL, bf16_out=True).any()
