@@ -41,6 +41,10 @@ def _load():
         lib.w4o_permute_int8.restype = ctypes.c_int
         lib.w4o_gemv_int8.argtypes = [P, P, P, L, L, L, L, L, P, P]
         lib.w4o_gemv_int8.restype = None
+        lib.w4o_quantize_q8_1_pt.argtypes = [P, L, L, P]
+        lib.w4o_quantize_q8_1_pt.restype = None
+        lib.w4o_gemv_w4a8.argtypes = [P, P, P, P, L, L, L, L, L, P, P]
+        lib.w4o_gemv_w4a8.restype = None
         _lib = lib
     return _lib
 
@@ -233,4 +237,47 @@ def gemv_int8(q, scale, x_bits, cols=None):
     d = np.full((C, N), np.nan)
     ref = np.full((C, N), np.nan)
     lib.w4o_gemv_int8(_ptr(a), _ptr(s), _ptr(xb), N, K, C, b, e, _ptr(d), _ptr(ref))
+    return d, ref
+
+
+# ---------------------------------------------------------------------------
+# W4A8: activations as block_q8_1 in the PT plane layout
+# ---------------------------------------------------------------------------
+
+def quantize_q8_1_pt(x_bits):
+    """x [C, K] (uint16 bf16 patterns, K % 128 == 0) -> uint8 [C, 144*K/128]:
+    per vector, planes 0..7 of int8 qs and plane 8 of (d, s) half pairs."""
+    lib = _load()
+    xb = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    if xb.ndim == 1:
+        xb = xb.reshape(1, -1)
+    C, K = xb.shape
+    if K % 128:
+        raise ValueError("K must be a multiple of 128")
+    pt = np.zeros((C, 144 * (K // 128)), np.uint8)
+    lib.w4o_quantize_q8_1_pt(_ptr(xb), C, K, _ptr(pt))
+    return pt
+
+
+def gemv_w4a8(packed_weights, scale_bits, zero_bits, pt, K, rows=None):
+    """W4A8 GEMV of the int4 row-layout weights (uint32 [N, K/8], bf16 scale
+    and zero [N] as uint16 patterns) against PT activations (uint8
+    [C, 144*K/128]).  Returns (d, ref_abs) float64 [C, N]."""
+    lib = _load()
+    qw = np.ascontiguousarray(packed_weights, dtype=np.uint32)
+    N = qw.shape[0]
+    if qw.shape[1] * 8 != K:
+        raise ValueError("weights imply another K")
+    s = np.ascontiguousarray(scale_bits, dtype=np.uint16)
+    z = np.ascontiguousarray(zero_bits, dtype=np.uint16)
+    p = np.ascontiguousarray(pt, dtype=np.uint8)
+    if p.ndim == 1:
+        p = p.reshape(1, -1)
+    C = p.shape[0]
+    if p.shape[1] != 144 * (K // 128):
+        raise ValueError("pt must hold 144*K/128 bytes per vector")
+    r0, r1 = (0, N) if rows is None else rows
+    d = np.full((C, N), np.nan)
+    ref = np.full((C, N), np.nan)
+    lib.w4o_gemv_w4a8(_ptr(qw), _ptr(s), _ptr(z), _ptr(p), N, K, C, r0, r1, _ptr(d), _ptr(ref))
     return d, ref

@@ -357,3 +357,141 @@ void w4o_gemv_int8(const int8_t* q, const float* scale, const uint16_t* x, long 
         }
     }
 }
+
+/* ------------------------------------------------------------------------
+ * W4A8: int4 weights with activations quantised to block_q8_1 in the PT
+ * plane layout ([P4] sections 3 and 3.1).
+ * ------------------------------------------------------------------------ */
+
+/* fp32 -> IEEE binary16 bits, round to nearest even (ggml_half). */
+static uint16_t float_to_half_bits(float f) {
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    uint32_t sign = (u >> 16) & 0x8000u;
+    uint32_t mag = u & 0x7FFFFFFFu;
+    if (mag >= 0x7F800000u) return (uint16_t)(sign | (mag > 0x7F800000u ? 0x7E00u : 0x7C00u));
+    /* |f| >= 65520 rounds to infinity */
+    if (mag >= 0x477FF000u) return (uint16_t)(sign | 0x7C00u);
+    if (mag < 0x38800000u) {
+        /* subnormal half (or zero): value = m * 2^-24, m = round(|f| * 2^24) */
+        double m = (double)f * (f < 0 ? -1.0 : 1.0) * 16777216.0;
+        double fl = floor(m);
+        double frac = m - fl;
+        uint32_t r = (uint32_t)fl;
+        if (frac > 0.5 || (frac == 0.5 && (r & 1u))) ++r;
+        return (uint16_t)(sign | r);
+    }
+    /* normal: keep 10 mantissa bits, round to nearest even on the 13 dropped */
+    uint32_t exp = ((mag >> 23) - 127 + 15);
+    uint32_t man = mag & 0x7FFFFFu;
+    uint32_t half = (exp << 10) | (man >> 13);
+    uint32_t rest = man & 0x1FFFu;
+    if (rest > 0x1000u || (rest == 0x1000u && (half & 1u))) ++half;   /* may carry into the exponent */
+    return (uint16_t)(sign | half);
+}
+
+static double half_bits_to_double(uint16_t h) {
+    int e = (h >> 10) & 0x1F;
+    int m = h & 0x3FF;
+    double v = (e == 0) ? ldexp((double)m, -24) : ldexp((double)(m | 0x400), e - 25);
+    return (h & 0x8000u) ? -v : v;
+}
+
+/*
+ * [P4 section 3.1]: x as block_q8_1 -- 32 int8 values qs and a pair of
+ * halves (d, s) per block, with s = d * sum_i qs_i.  The page gives the
+ * struct, not the quantiser; the reading is the weight quantiser's:
+ *   d  = max_i |x_i| / 127          (IEEE fp32 division)
+ *   qs = clamp(roundf(x_i / d), -127, 127)   (d == 0: qs = 0)
+ *   stored: half(d), half(d * sum_i qs_i) (fp32 product, each rounded to
+ *   the nearest half).
+ * PT layout ([P4] section 3.1, "排列方式称作 PT"): per vector of K elements
+ * (K % 128 == 0) there are K/128 blocks of 128 (four q8_1 blocks each);
+ * element e of 128-block i is the byte
+ *   o = 16 * (floor(e / 16) * K/128 + i) + e % 16
+ * (planes 0..7 of 16 bytes per block), and plane 8 holds each 128-block's
+ * four (d, s) pairs: the 16 bytes at 16 * (8 * K/128 + i), pair j at +4j
+ * (d then s, little-endian halves).  A vector takes 144 * K/128 bytes;
+ * x is [C][K] bf16, pt is C vectors back to back.
+ */
+void w4o_quantize_q8_1_pt(const uint16_t* x, long C, long K, uint8_t* pt) {
+    long bpr = K / 128;
+    long vec_bytes = 144 * bpr;
+    for (long c = 0; c < C; ++c) {
+        uint8_t* v = pt + c * vec_bytes;
+        for (long i = 0; i < bpr; ++i) {
+            for (int j = 0; j < 4; ++j) {
+                long k0 = i * 128 + 32 * j;
+                float amax = 0.0f;
+                for (int t = 0; t < 32; ++t) {
+                    float a = fabsf(bf16_bits_to_float(x[c * K + k0 + t]));
+                    if (a > amax) amax = a;
+                }
+                float d = amax / 127.0f;
+                int sum = 0;
+                for (int t = 0; t < 32; ++t) {
+                    float xv = bf16_bits_to_float(x[c * K + k0 + t]);
+                    float r = (d == 0.0f) ? 0.0f : roundf(xv / d);
+                    if (r < -127.0f) r = -127.0f;
+                    if (r > 127.0f) r = 127.0f;
+                    int q = (int)r;
+                    sum += q;
+                    int e = 32 * j + t;
+                    v[16 * ((e / 16) * bpr + i) + e % 16] = (uint8_t)(int8_t)q;
+                }
+                uint16_t dh = float_to_half_bits(d);
+                uint16_t sh = float_to_half_bits(d * (float)sum);
+                uint8_t* ds = v + 16 * (8 * bpr + i) + 4 * j;
+                ds[0] = (uint8_t)(dh & 0xFF);
+                ds[1] = (uint8_t)(dh >> 8);
+                ds[2] = (uint8_t)(sh & 0xFF);
+                ds[3] = (uint8_t)(sh >> 8);
+            }
+        }
+    }
+}
+
+/*
+ * W4A8 GEMV: the int4 weights of w4o_gemv ([P2] words, scale and zero per
+ * row, bf16) against x in block_q8_1 / PT form.  Per q8_1 block b (32
+ * elements) of row r:
+ *   contribution = d_b * sum_{k in b} q[r][k] * qs[k]  -  zero[r] * s_b
+ * ("correcting the zero through s": s_b = d_b * sum qs), and
+ *   d[c][r] = scale[r] * sum_b contribution,
+ * with d_b, s_b the stored halves; fp64 throughout (the integer dots are
+ * exact).  ref_abs (may be NULL) receives sum_k |(q - zero) scale d_b qs_k|.
+ */
+void w4o_gemv_w4a8(const uint32_t* packed_weights, const uint16_t* scales, const uint16_t* zeros,
+                   const uint8_t* pt, long N, long K, long C, long row_begin, long row_end, double* d,
+                   double* ref_abs) {
+    long bpr = K / 128;
+    long vec_bytes = 144 * bpr;
+    long k_words = K / 8;
+    for (long c = 0; c < C; ++c) {
+        const uint8_t* v = pt + c * vec_bytes;
+        for (long row = row_begin; row < row_end; ++row) {
+            double scale = (double)bf16_bits_to_float(scales[row]);
+            double zero = (double)bf16_bits_to_float(zeros[row]);
+            double total = 0.0, abs_total = 0.0;
+            for (long i = 0; i < bpr; ++i) {
+                for (int j = 0; j < 4; ++j) {
+                    const uint8_t* ds = v + 16 * (8 * bpr + i) + 4 * j;
+                    double db = half_bits_to_double((uint16_t)(ds[0] | (ds[1] << 8)));
+                    double sb = half_bits_to_double((uint16_t)(ds[2] | (ds[3] << 8)));
+                    long dot = 0;
+                    for (int t = 0; t < 32; ++t) {
+                        long k = i * 128 + 32 * j + t;
+                        int e = 32 * j + t;
+                        int qs = (int)(int8_t)v[16 * ((e / 16) * bpr + i) + e % 16];
+                        unsigned q = (packed_weights[row * k_words + k / 8] >> (4 * (k % 8))) & 0xFu;
+                        dot += (long)q * qs;
+                        abs_total += fabs(((double)q - zero) * scale * db * qs);
+                    }
+                    total += db * (double)dot - zero * sb;
+                }
+            }
+            d[c * N + row] = scale * total;
+            if (ref_abs) ref_abs[c * N + row] = abs_total;
+        }
+    }
+}

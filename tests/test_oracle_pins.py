@@ -497,3 +497,113 @@ def test_gemv_int8_matches_dense_matmul_and_one_hot():
     onehot[0, 17] = 1.0
     d1, _ = oracle.gemv_int8(q, s, bf16_bits(onehot))
     assert np.array_equal(d1[0], q[17].astype(np.float64) * s.astype(np.float64))
+
+
+# ---------------------------------------------------------------------------
+# W4A8: block_q8_1 activations in the PT plane layout
+# ---------------------------------------------------------------------------
+
+def _pt_offset(e, i, K):
+    """The page's byte of element e of 128-block i: 16(floor(e/16) K/128 + i) + e mod 16."""
+    return 16 * ((e // 16) * (K // 128) + i) + e % 16
+
+
+def _pt_ds(pt, K, i, j):
+    """(d, s) of q8_1 block j of 128-block i, from plane 8, as float64 (numpy's half)."""
+    o = 16 * (8 * (K // 128) + i) + 4 * j
+    return (float(np.frombuffer(bytes(pt[o:o + 2]), np.float16)[0]),
+            float(np.frombuffer(bytes(pt[o + 2:o + 4]), np.float16)[0]))
+
+
+def _int_activations(C, K, seed):
+    """Integer activations with a 127 in every 32-block (so d = 1 exactly),
+    the rest in -15..15 (so s = sum qs is exact in half)."""
+    rng = np.random.default_rng(seed)
+    x = rng.integers(-15, 16, (C, K)).astype(np.float64)
+    x[:, ::32] = 127
+    return x
+
+
+def test_q8_1_pt_layout_places_elements_by_page_formula():
+    K, C = 5120, 2
+    x = _int_activations(C, K, 5)
+    pt = oracle.quantize_q8_1_pt(bf16_bits(x))
+    assert pt.shape == (C, 144 * K // 128)
+    for c in range(C):
+        qs = pt[c].view(np.int8)
+        for i in range(K // 128):
+            for e in range(128):
+                assert qs[_pt_offset(e, i, K)] == x[c, 128 * i + e]
+            for j in range(4):
+                d, s = _pt_ds(pt[c], K, i, j)
+                blk = x[c, 128 * i + 32 * j:128 * i + 32 * j + 32]
+                assert d == 1.0 and s == blk.sum()
+
+
+def test_q8_1_quantiser_rounds_half_away_and_stores_halves():
+    K = 128
+    x = np.zeros((1, K))
+    x[0, :32] = np.arange(32) - 15.5          # block 0: ties (k + 1/2) around a max of 127 ...
+    x[0, 0] = 127.0                            # ... so d = 1
+    x[0, 32:64] = np.linspace(-0.3, 0.7, 32)  # block 1: a general block
+    # block 2 all zero: d = s = 0
+    x[0, 96:128] = 1e-3                        # block 3: tiny values, d a subnormal-free half
+    xb = bf16_bits(x)
+    xv = bf16_values(xb)[0]
+    pt = oracle.quantize_q8_1_pt(xb)[0]
+    qs = np.array([pt.view(np.int8)[_pt_offset(e, 0, K)] for e in range(128)], dtype=np.int64)
+    t = xv[1:32]
+    assert np.array_equal(qs[1:32], np.where(t > 0, np.floor(t) + 1, np.ceil(t) - 1))  # away from zero
+    assert qs[0] == 127
+    for j, blk in enumerate((xv[:32], xv[32:64], xv[64:96], xv[96:128])):
+        d32 = np.float32(np.abs(blk).max()) / np.float32(127.0)
+        q = qs[32 * j:32 * j + 32]
+        if d32 != 0:
+            # within half a step (plus the fp32 quotient's rounding)
+            assert np.all(np.abs(blk - q * np.float64(d32)) <= np.float64(d32) * (0.5 + 2.0 ** -16))
+        else:
+            assert not q.any()
+        d, s = _pt_ds(pt, K, 0, j)
+        assert d == float(np.float16(d32))
+        assert s == float(np.float16(np.float32(d32) * np.float32(q.sum())))
+
+
+def test_w4a8_gemv_reduces_to_exact_gemv_on_integer_activations():
+    """With d = 1 and s = sum qs exact, the W4A8 product equals the plain
+    int4 GEMV of the same weights and activations."""
+    N, K, C = 24, 256, 3
+    rng = np.random.default_rng(8)
+    qw = rng.integers(0, 2 ** 32, (N, K // 8), dtype=np.uint64).astype(np.uint32)
+    scale = bf16_bits(rng.uniform(0.01, 0.05, N))
+    zero = bf16_bits(np.full(N, 8.0))
+    x = _int_activations(C, K, 9)
+    pt = oracle.quantize_q8_1_pt(bf16_bits(x))
+    d8, _ = oracle.gemv_w4a8(qw, scale, zero, pt, K)
+    d, _ = oracle.gemv(qw, scale, zero, bf16_bits(x), oracle.BF16)
+    assert np.allclose(d8, d, rtol=1e-12, atol=1e-12)
+
+
+def test_w4a8_gemv_matches_dense_matmul_of_dequantised_operands():
+    """Zero point 0: d = W_deq @ x_hat with x_hat = d_b * qs, by a library matmul."""
+    N, K, C = 16, 384, 2
+    rng = np.random.default_rng(10)
+    qw = rng.integers(0, 2 ** 32, (N, K // 8), dtype=np.uint64).astype(np.uint32)
+    scale_v = rng.uniform(0.01, 0.05, N)
+    scale = bf16_bits(scale_v)
+    zero = bf16_bits(np.zeros(N))
+    x = rng.standard_normal((C, K))
+    pt = oracle.quantize_q8_1_pt(bf16_bits(x))
+    d8, _ = oracle.gemv_w4a8(qw, scale, zero, pt, K)
+    # dequantised weights from the page's packing: nibble j of word i is k = 8i + j
+    q = np.zeros((N, K))
+    for j in range(8):
+        q[:, j::8] = (qw >> (4 * j)) & 0xF
+    Wd = q * bf16_values(scale)[:, None]
+    xh = np.zeros((C, K))
+    for c in range(C):
+        qs = pt[c].view(np.int8)
+        for i in range(K // 128):
+            for e in range(128):
+                d, _ = _pt_ds(pt[c], K, i, e // 32)
+                xh[c, 128 * i + e] = d * qs[_pt_offset(e, i, K)]
+    assert np.allclose(d8, xh @ Wd.T, rtol=1e-12, atol=1e-12)
