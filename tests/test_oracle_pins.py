@@ -607,3 +607,27 @@ def test_w4a8_gemv_matches_dense_matmul_of_dequantised_operands():
                 d, _ = _pt_ds(pt[c], K, i, e // 32)
                 xh[c, 128 * i + e] = d * qs[_pt_offset(e, i, K)]
     assert np.allclose(d8, xh @ Wd.T, rtol=1e-12, atol=1e-12)
+
+
+def test_q8_1_pt_layout_matches_page_example():
+    """The page's K = 5120 example: 40 blocks of 128 elements, 4 (d, s) pairs
+    each, planes 0..7 of 16-byte blocks holding elements 16p..16p+15, and
+    plane 8 holding every (d, s)."""
+    P = load_golden("p4_pt_layout.txt")
+    K = P["k"][0]
+    nb = P["blocks"][0]
+    assert K // P["elements_per_block"][0] == nb
+    assert P["elements_per_block"][0] // P["q8_1_elements"][0] == P["ds_pairs_per_block"][0]
+    B = P["block_bytes_per_plane"][0]
+    rng = np.random.default_rng(4)
+    x = rng.integers(-15, 16, (1, K)).astype(np.float64)
+    x[:, ::32] = 127
+    pt = oracle.quantize_q8_1_pt(bf16_bits(x))[0]
+    assert pt.size == (P["ds_plane"][0] + 1) * nb * B
+    qs = pt.view(np.int8)
+    for p, e0 in enumerate(P["plane_first_elements"]):
+        plane = qs[p * nb * B:(p + 1) * nb * B].reshape(nb, B)
+        assert np.array_equal(plane, x[0].reshape(nb, 128)[:, e0:e0 + 16])
+    ds = pt[P["ds_plane"][0] * nb * B:].view(np.float16).reshape(nb, P["ds_pairs_per_block"][0], 2)
+    sums = x[0].reshape(nb, 4, 32).sum(axis=2)
+    assert np.all(ds[:, :, 0] == 1.0) and np.array_equal(ds[:, :, 1].astype(np.float64), sums)
