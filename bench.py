@@ -664,6 +664,24 @@ def cpu_baseline(name, budget_s=10.0):
 # main
 # ---------------------------------------------------------------------------
 
+def dtype_of(name):
+    """The arithmetic the workload's kernels compute in."""
+    cfg = WORKLOADS[name]
+    if cfg["kind"] == "gemv":
+        if cfg.get("perm"):
+            return "bf16 x / int4 weights (bf16 MMA), fp32 accumulate"
+        if cfg["C"] == 1:
+            return "fp16 MMA (bf16 x scaled by a power of two) / uint4 weights, fp32 accumulate"
+        return "bf16 x / uint4 weights (bf16 MMA), fp32 accumulate"
+    if cfg["kind"] == "gemm":
+        return "bf16 A / uint4 B (bf16 tcgen05 MMA), fp32 accumulate"
+    if cfg["kind"] == "gemv8":
+        return "bf16 x / int8 weights (fp32 FMA)"
+    if cfg["kind"] == "quant8":
+        return "bf16 in, int8 out (fp32 division)"
+    return "bf16 in, int4 out (fp32 arithmetic)"
+
+
 def unit_of(work):
     return "TFLOP/s" if isinstance(work, GemmWork) else "GB/s"
 
@@ -709,7 +727,7 @@ def run_ours(args, world, rank):
     line = {
         "metric": METRIC, "value": value, "unit": unit_of(work), "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": sec_step * 1e3, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16 x / uint4 weights, fp32 accumulate",
+        "vs_baseline": None, "dtype": dtype_of(args.workload),
         "data": "synthetic (seeded; shapes of the pages' workloads)",
         "config": {"workload": args.workload, **{k: v for k, v in WORKLOADS[args.workload].items() if k != "kind"},
                    "l2": work.l2_note(), "parallelism": "replicas" if world > 1 else "single GPU"},
