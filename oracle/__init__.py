@@ -10,6 +10,8 @@ Every function is pinned against facts the source pages fix, in
 tests/test_oracle_pins.py.
 """
 import ctypes
+import os
+
 import numpy as np
 
 from .build import build_oracle
@@ -22,7 +24,9 @@ F32, BF16 = 0, 1
 def _load():
     global _lib
     if _lib is None:
-        lib = ctypes.CDLL(build_oracle())
+        # W4_ORACLE_LIB names another build of the same source (the pin
+        # suite's mutation check loads deliberately broken copies this way).
+        lib = ctypes.CDLL(os.environ.get("W4_ORACLE_LIB") or build_oracle())
         P = ctypes.c_void_p
         L = ctypes.c_long
         lib.w4o_gemv.argtypes = [P, P, P, P, ctypes.c_int, L, L, L, L, L, P, P]
@@ -45,6 +49,10 @@ def _load():
         lib.w4o_quantize_q8_1_pt.restype = None
         lib.w4o_gemv_w4a8.argtypes = [P, P, P, P, L, L, L, L, L, P, P]
         lib.w4o_gemv_w4a8.restype = None
+        lib.w4o_float_to_half.argtypes = [P, L, P]
+        lib.w4o_float_to_half.restype = None
+        lib.w4o_half_to_double.argtypes = [P, L, P]
+        lib.w4o_half_to_double.restype = None
         _lib = lib
     return _lib
 
@@ -281,3 +289,23 @@ def gemv_w4a8(packed_weights, scale_bits, zero_bits, pt, K, rows=None):
     ref = np.full((C, N), np.nan)
     lib.w4o_gemv_w4a8(_ptr(qw), _ptr(s), _ptr(z), _ptr(p), N, K, C, r0, r1, _ptr(d), _ptr(ref))
     return d, ref
+
+
+def float_to_half(a):
+    """fp32 array -> uint16 IEEE binary16 bit patterns, the conversion the
+    block_q8_1 quantiser stores d and s with (round to nearest even)."""
+    lib = _load()
+    f = np.ascontiguousarray(a, dtype=np.float32).ravel()
+    out = np.zeros(f.size, np.uint16)
+    lib.w4o_float_to_half(_ptr(f), f.size, _ptr(out))
+    return out.reshape(np.shape(a))
+
+
+def half_to_double(h):
+    """uint16 IEEE binary16 bit patterns -> float64 values (exact), the
+    decoding the W4A8 GEMV reads d and s with."""
+    lib = _load()
+    b = np.ascontiguousarray(h, dtype=np.uint16).ravel()
+    out = np.zeros(b.size, np.float64)
+    lib.w4o_half_to_double(_ptr(b), b.size, _ptr(out))
+    return out.reshape(np.shape(h))

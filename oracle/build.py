@@ -18,11 +18,17 @@ def build_oracle(force: bool = False) -> str:
             and os.path.getmtime(LIB) >= os.path.getmtime(SRC)):
         return LIB
     tmp = LIB + ".tmp.%d" % os.getpid()
-    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fno-fast-math",
-           "-ffp-contract=off", SRC, "-o", tmp, "-lm"]
-    subprocess.run(cmd, check=True)
+    compile_oracle(SRC, tmp)
     os.replace(tmp, LIB)
     return LIB
+
+
+def compile_oracle(src: str, out: str) -> None:
+    """Compile one C source with the oracle's flags into the shared object
+    `out` (no fast-math, no FMA contraction: the source's own rounding)."""
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fno-fast-math",
+           "-ffp-contract=off", src, "-o", out, "-lm"]
+    subprocess.run(cmd, check=True)
 
 
 if __name__ == "__main__":

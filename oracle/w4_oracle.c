@@ -390,11 +390,25 @@ static uint16_t float_to_half_bits(float f) {
     return (uint16_t)(sign | half);
 }
 
+/* IEEE binary16 bits -> double (exact): exponent field 0 is m * 2^-24,
+ * 31 is infinity (m == 0) or NaN, else (1024 + m) * 2^(e - 25). */
 static double half_bits_to_double(uint16_t h) {
     int e = (h >> 10) & 0x1F;
     int m = h & 0x3FF;
-    double v = (e == 0) ? ldexp((double)m, -24) : ldexp((double)(m | 0x400), e - 25);
+    double v;
+    if (e == 31) v = (m == 0) ? HUGE_VAL : NAN;
+    else v = (e == 0) ? ldexp((double)m, -24) : ldexp((double)(m | 0x400), e - 25);
     return (h & 0x8000u) ? -v : v;
+}
+
+/* The two conversions over arrays, exported so that the pins can compare
+ * them with an IEEE library conversion on chosen values (every tie). */
+void w4o_float_to_half(const float* in, long n, uint16_t* out) {
+    for (long i = 0; i < n; ++i) out[i] = float_to_half_bits(in[i]);
+}
+
+void w4o_half_to_double(const uint16_t* in, long n, double* out) {
+    for (long i = 0; i < n; ++i) out[i] = half_bits_to_double(in[i]);
 }
 
 /*

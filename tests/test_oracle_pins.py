@@ -568,6 +568,48 @@ def test_q8_1_quantiser_rounds_half_away_and_stores_halves():
         assert s == float(np.float16(np.float32(d32) * np.float32(q.sum())))
 
 
+def test_half_conversion_rounds_ties_to_even_at_every_midpoint():
+    """d and s are stored as IEEE binary16 (ggml_half), rounded to nearest
+    even.  Checked against numpy's float16 cast on the midpoint between every
+    pair of neighbouring halves (subnormal, normal, and 65520 between the
+    largest half and the overflow), one fp32 step either side of each, every
+    half itself, both signs, and random fp32 patterns."""
+    grid = np.arange(0x7C00, dtype=np.uint16).view(np.float16).astype(np.float64)
+    mids = (grid[:-1] + grid[1:]) / 2
+    mids = np.append(mids, 65520.0)
+    m32 = mids.astype(np.float32)
+    assert np.array_equal(m32.astype(np.float64), mids)        # every midpoint is an fp32 value
+    vals = np.concatenate([m32, np.nextafter(m32, np.float32(np.inf)), np.nextafter(m32, np.float32(0)),
+                           grid.astype(np.float32), np.float32([65519.0, 65536.0, 1e30, 1e-30, np.inf])])
+    rng = np.random.default_rng(20)
+    rand = rng.integers(0, 2 ** 32, 200000, dtype=np.uint64).astype(np.uint32).view(np.float32)
+    vals = np.concatenate([vals, -vals, rand[~np.isnan(rand)]])
+    got = oracle.float_to_half(vals)
+    with np.errstate(over="ignore"):
+        want = vals.astype(np.float16).view(np.uint16)
+    assert np.array_equal(got, want)
+    # ties go to the even neighbour: 1 + 2^-11 lies between 1 and 1 + 2^-10
+    assert oracle.float_to_half(np.float32([1 + 2.0 ** -11]))[0] == 0x3C00
+    assert oracle.float_to_half(np.float32([1 + 3 * 2.0 ** -11]))[0] == 0x3C02
+    assert oracle.float_to_half(np.float32([2.0 ** -25, 3 * 2.0 ** -25]))[0] == 0x0000
+    assert oracle.float_to_half(np.float32([3 * 2.0 ** -25]))[0] == 0x0002
+
+
+def test_half_decoding_is_exact_for_every_pattern():
+    """The W4A8 GEMV reads d and s back as exact doubles: all 65536 binary16
+    patterns against numpy's float16 widening, with the closed forms of the
+    smallest subnormal, one, the largest half and infinity."""
+    h = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    got = oracle.half_to_double(h)
+    want = h.view(np.float16).astype(np.float64)
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], want[~nan])
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(want[~nan]))
+    assert got[0x0001] == 2.0 ** -24 and got[0x3C00] == 1.0 and got[0x7BFF] == 65504.0
+    assert got[0x7C00] == np.inf and got[0xFC00] == -np.inf
+
+
 def test_w4a8_gemv_reduces_to_exact_gemv_on_integer_activations():
     """With d = 1 and s = sum qs exact, the W4A8 product equals the plain
     int4 GEMV of the same weights and activations."""
