@@ -7,7 +7,7 @@ w4_oracle.c (plain C, fp64 products); this module only marshals numpy
 arrays through ctypes.
 
 Every function is pinned against facts the source pages fix, in
-tests/test_oracle_pins.py.
+tests/test_oracle_pins.py and tests/test_oracle_ternary_pins.py.
 """
 import ctypes
 import os
@@ -53,6 +53,20 @@ def _load():
         lib.w4o_float_to_half.restype = None
         lib.w4o_half_to_double.argtypes = [P, L, P]
         lib.w4o_half_to_double.restype = None
+        lib.w4o_ptq1_0_pack.argtypes = [P, P, L, L, P]
+        lib.w4o_ptq1_0_pack.restype = ctypes.c_int
+        lib.w4o_ptq1_0_unpack.argtypes = [P, L, L, P, P]
+        lib.w4o_ptq1_0_unpack.restype = None
+        lib.w4o_ptq1_1_codebook.argtypes = [P, L, L, P]
+        lib.w4o_ptq1_1_codebook.restype = L
+        lib.w4o_ptq1_1_encode.argtypes = [P, L, L, P, L, P, P, P, L]
+        lib.w4o_ptq1_1_encode.restype = L
+        lib.w4o_ptq1_1_unpack.argtypes = [P, L, L, P, L, P, P, L, P, P]
+        lib.w4o_ptq1_1_unpack.restype = ctypes.c_int
+        lib.w4o_mmvq_ptq1_0.argtypes = [P, P, L, L, L, L, L, P, P]
+        lib.w4o_mmvq_ptq1_0.restype = None
+        lib.w4o_mmvq_ptq1_1.argtypes = [P, P, L, P, P, L, P, L, L, L, L, L, P, P]
+        lib.w4o_mmvq_ptq1_1.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -309,3 +323,138 @@ def half_to_double(h):
     out = np.zeros(b.size, np.float64)
     lib.w4o_half_to_double(_ptr(b), b.size, _ptr(out))
     return out.reshape(np.shape(h))
+
+
+# ---------------------------------------------------------------------------
+# Ternary weights: PTQ1_0 blocks, PTQ1_1 superblocks, MMVQ
+# ---------------------------------------------------------------------------
+
+PTQ1_0_BYTES = 28
+PTQ1_1_BYTES = 216
+PTQ1_1_ESCAPE = 767
+
+
+def ptq1_0_pack(trits, d_bits):
+    """trits int8 [N, K] in {-1, 0, 1} (K % 128 == 0), d [N, K/128] half bit
+    patterns -> uint8 [N, K/128, 28] PTQ1_0 blocks."""
+    lib = _load()
+    t = np.ascontiguousarray(trits, dtype=np.int8)
+    N, K = t.shape
+    if K % 128:
+        raise ValueError("K must be a multiple of 128")
+    d = np.ascontiguousarray(d_bits, dtype=np.uint16)
+    if d.shape != (N, K // 128):
+        raise ValueError("d must be [N, K/128]")
+    out = np.zeros((N, K // 128, PTQ1_0_BYTES), np.uint8)
+    if lib.w4o_ptq1_0_pack(_ptr(t), _ptr(d), N, K, _ptr(out)):
+        raise ValueError("trits must lie in {-1, 0, 1}")
+    return out
+
+
+def ptq1_0_unpack(blocks):
+    """uint8 [N, K/128, 28] -> (trits int8 [N, K], d uint16 [N, K/128])."""
+    lib = _load()
+    b = np.ascontiguousarray(blocks, dtype=np.uint8)
+    N, bpr = b.shape[:2]
+    K = 128 * bpr
+    t = np.zeros((N, K), np.int8)
+    d = np.zeros((N, bpr), np.uint16)
+    lib.w4o_ptq1_0_unpack(_ptr(b), N, K, _ptr(t), _ptr(d))
+    return t, d
+
+
+class Ptq1_1:
+    """A tensor in PTQ1_1 form: superblocks uint8 [N, ceil(K/1024), 216],
+    the codebook uint8 [n_code, 8] and the escape table (esc_idx int64
+    [n_esc] ascending superblock indices, esc_patt uint8 [n_esc, 8])."""
+
+    def __init__(self, sblocks, codebook, esc_idx, esc_patt, K):
+        self.sblocks, self.codebook, self.esc_idx, self.esc_patt, self.K = sblocks, codebook, esc_idx, esc_patt, K
+
+
+def ptq1_1_encode(blocks):
+    """PTQ1_0 blocks uint8 [N, K/128, 28] -> Ptq1_1 (codebook built from
+    the tensor's own exponent patterns)."""
+    lib = _load()
+    b = np.ascontiguousarray(blocks, dtype=np.uint8)
+    N, bpr = b.shape[:2]
+    K = 128 * bpr
+    sbpr = (bpr + 7) // 8
+    code = np.zeros((PTQ1_1_ESCAPE, 8), np.uint8)
+    n_code = lib.w4o_ptq1_1_codebook(_ptr(b), N, K, _ptr(code))
+    if n_code < 0:
+        raise MemoryError("codebook")
+    out = np.zeros((N, sbpr, PTQ1_1_BYTES), np.uint8)
+    cap = max(1, N * sbpr)
+    esc_idx = np.zeros(cap, np.int64)
+    esc_patt = np.zeros((cap, 8), np.uint8)
+    n_esc = lib.w4o_ptq1_1_encode(_ptr(b), N, K, _ptr(code), n_code, _ptr(out), _ptr(esc_idx), _ptr(esc_patt), cap)
+    if n_esc == -1:
+        raise ValueError("PTQ1_1 stores no sign: every d must be non-negative")
+    if n_esc < 0:
+        raise RuntimeError("escape table overflow")
+    return Ptq1_1(out, code[:n_code].copy(), esc_idx[:n_esc].copy(), esc_patt[:n_esc].copy(), K)
+
+
+def _ptq1_1_args(w):
+    code = np.ascontiguousarray(w.codebook, dtype=np.uint8)
+    ei = np.ascontiguousarray(w.esc_idx, dtype=np.int64)
+    ep = np.ascontiguousarray(w.esc_patt, dtype=np.uint8)
+    # keep at least one element so that every pointer is valid
+    return (code if code.size else np.zeros((1, 8), np.uint8), code.shape[0],
+            ei if ei.size else np.zeros(1, np.int64), ep if ep.size else np.zeros((1, 8), np.uint8), ei.shape[0])
+
+
+def ptq1_1_unpack(w):
+    """Ptq1_1 -> (trits int8 [N, K], d uint16 [N, K/128])."""
+    lib = _load()
+    sb = np.ascontiguousarray(w.sblocks, dtype=np.uint8)
+    N, K = sb.shape[0], w.K
+    code, n_code, ei, ep, n_esc = _ptq1_1_args(w)
+    t = np.zeros((N, K), np.int8)
+    d = np.zeros((N, K // 128), np.uint16)
+    if lib.w4o_ptq1_1_unpack(_ptr(sb), N, K, _ptr(code), n_code, _ptr(ei), _ptr(ep), n_esc, _ptr(t), _ptr(d)):
+        raise ValueError("a superblock's pattern index names no codebook entry or escape")
+    return t, d
+
+
+def mmvq_ptq1_0(blocks, pt, rows=None):
+    """MMVQ of PTQ1_0 weights (uint8 [N, K/128, 28]) against x as block_q8_1
+    in the PT layout (uint8 [C, 144 K/128]).  Returns (d, ref_abs) float64
+    [C, N]; rows outside `rows` stay NaN."""
+    lib = _load()
+    b = np.ascontiguousarray(blocks, dtype=np.uint8)
+    N, bpr = b.shape[:2]
+    K = 128 * bpr
+    p = np.ascontiguousarray(pt, dtype=np.uint8)
+    if p.ndim == 1:
+        p = p.reshape(1, -1)
+    C = p.shape[0]
+    if p.shape[1] != 144 * bpr:
+        raise ValueError("pt must hold 144*K/128 bytes per vector")
+    r0, r1 = (0, N) if rows is None else rows
+    d = np.full((C, N), np.nan)
+    ref = np.full((C, N), np.nan)
+    lib.w4o_mmvq_ptq1_0(_ptr(b), _ptr(p), N, K, C, r0, r1, _ptr(d), _ptr(ref))
+    return d, ref
+
+
+def mmvq_ptq1_1(w, pt, rows=None):
+    """MMVQ of a Ptq1_1 tensor against PT activations; as mmvq_ptq1_0."""
+    lib = _load()
+    sb = np.ascontiguousarray(w.sblocks, dtype=np.uint8)
+    N, K = sb.shape[0], w.K
+    code, n_code, ei, ep, n_esc = _ptq1_1_args(w)
+    p = np.ascontiguousarray(pt, dtype=np.uint8)
+    if p.ndim == 1:
+        p = p.reshape(1, -1)
+    C = p.shape[0]
+    if p.shape[1] != 144 * (K // 128):
+        raise ValueError("pt must hold 144*K/128 bytes per vector")
+    r0, r1 = (0, N) if rows is None else rows
+    d = np.full((C, N), np.nan)
+    ref = np.full((C, N), np.nan)
+    if lib.w4o_mmvq_ptq1_1(_ptr(sb), _ptr(code), n_code, _ptr(ei), _ptr(ep), n_esc, _ptr(p), N, K, C, r0, r1,
+                           _ptr(d), _ptr(ref)):
+        raise ValueError("a superblock's pattern index names no codebook entry or escape")
+    return d, ref

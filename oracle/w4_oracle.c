@@ -27,7 +27,9 @@
  *   [P4] "三值量化模型的无损压缩" (ternary compression blog): section 3 "MMVQ",
  *        the batched GEMV definition d[r,c] = sum_k W[r,k] x[c,k].
  *
- * Parity pins for every function live in tests/test_oracle_pins.py.
+ * Parity pins for every function live in tests/test_oracle_pins.py and
+ * tests/test_oracle_ternary_pins.py; tests/test_oracle_mutants.py checks
+ * that planted mistakes in this file fail them.
  */
 #include <math.h>
 #include <stdint.h>
@@ -508,4 +510,351 @@ void w4o_gemv_w4a8(const uint32_t* packed_weights, const uint16_t* scales, const
             if (ref_abs) ref_abs[c * N + row] = abs_total;
         }
     }
+}
+
+/* ------------------------------------------------------------------------
+ * Ternary weights ([P4] sections 2, 3.1 and 3.2): PTQ1_0 blocks of 128
+ * trits, the PTQ1_1 superblock that packs eight of them into 216 bytes, and
+ * the MMVQ GEMV over either against x in block_q8_1 / PT form.
+ *
+ * Readings where the page is silent (each stated once, here):
+ *  - a trit t in {-1, 0, +1} is stored as the digit u = t + 1 in {0, 1, 2};
+ *  - a byte holding five trits is the base-3 number sum_p u_p 3^p, trit
+ *    position p being the digit of weight 3^p;
+ *  - PTQ1_0 (28 bytes): qs[24], qh[2], d (IEEE half, little-endian), in the
+ *    struct's order; weight e < 80 is position e >> 4 of qs byte e & 15,
+ *    weight 80 + e (e < 40) position e >> 3 of qs byte 16 + (e & 7) (the
+ *    page's "byte e & 7" counted from the first byte after the 80-trit
+ *    part), weight 120 + j the 2-bit field j of qh read as a little-endian
+ *    16-bit word; the weight's value is d * t;
+ *  - PTQ1_1 (216 bytes): qs[192] = the eight blocks' qs back to back (block
+ *    s at 24 s); qh[13] holds the 64 tail trits, tail trit j of block s as
+ *    digit (8 s + j) mod 5 of byte (8 s + j) / 5, and the 65th digit
+ *    (position 4 of byte 12) is the free trit f; mantissa[8] are eight
+ *    10-bit fields, field s at bits 10 s .. 10 s + 9 of the little-endian
+ *    80-bit string; exponents is one byte.  The pattern index is
+ *    exponents + 256 f, in [0, 768); an index below 767 names a codebook
+ *    entry (eight 5-bit exponents), 767 sends the decoder to the tensor's
+ *    escape table, keyed by the superblock's index r * SBPR + sb.  Block s's
+ *    d is the positive half with exponent field E_s and mantissa M_s;
+ *  - the codebook holds the tensor's most frequent exponent patterns, by
+ *    descending count, ties in ascending order of the pattern read as the
+ *    40-bit number with block 0's exponent most significant;
+ *  - a row of K/128 blocks takes ceil(K/1024) superblocks; the blocks that
+ *    pad the last one have every trit 0 and d = +0.
+ * ------------------------------------------------------------------------ */
+
+#define PTQ1_0_BYTES 28
+#define PTQ1_1_BYTES 216
+#define PTQ1_1_QH 192
+#define PTQ1_1_MANT 205
+#define PTQ1_1_EXP 215
+#define PTQ1_1_ESCAPE 767
+
+static const int k_pow3[5] = {1, 3, 9, 27, 81};
+
+/* [P4 section 3.2]: where weight e of a PTQ1_0 block sits.  Returns the qs
+ * byte and sets *pos to the trit position, or returns -1 for the tail
+ * (qh) and sets *pos to the tail index. */
+static int ptq1_0_place(int e, int* pos) {
+    if (e < 80) { *pos = e >> 4; return e & 15; }
+    if (e < 120) { *pos = (e - 80) >> 3; return 16 + ((e - 80) & 7); }
+    *pos = e - 120;
+    return -1;
+}
+
+static int trit_digit(uint8_t byte, int pos) { return (byte / k_pow3[pos]) % 3; }
+
+/*
+ * Pack ternary weights into PTQ1_0 blocks.  trits: int8 [N][K] in
+ * {-1, 0, 1}; d: [N][K/128] half bit patterns; out: N * K/128 blocks of 28
+ * bytes, row after row.  K % 128 == 0.  Returns 0, or -1 on a value
+ * outside {-1, 0, 1}.
+ */
+int w4o_ptq1_0_pack(const int8_t* trits, const uint16_t* d, long N, long K, uint8_t* out) {
+    long bpr = K / 128;
+    for (long r = 0; r < N; ++r) {
+        for (long b = 0; b < bpr; ++b) {
+            uint8_t* blk = out + (r * bpr + b) * PTQ1_0_BYTES;
+            memset(blk, 0, PTQ1_0_BYTES);
+            unsigned qh = 0;
+            for (int e = 0; e < 128; ++e) {
+                int t = trits[r * K + b * 128 + e];
+                if (t < -1 || t > 1) return -1;
+                int pos, byte = ptq1_0_place(e, &pos);
+                if (byte >= 0) blk[byte] = (uint8_t)(blk[byte] + (t + 1) * k_pow3[pos]);
+                else qh |= (unsigned)(t + 1) << (2 * pos);
+            }
+            uint16_t h = d[r * bpr + b];
+            blk[24] = (uint8_t)(qh & 0xFF);
+            blk[25] = (uint8_t)(qh >> 8);
+            blk[26] = (uint8_t)(h & 0xFF);
+            blk[27] = (uint8_t)(h >> 8);
+        }
+    }
+    return 0;
+}
+
+/* Decode one PTQ1_0 block into 128 trits and its half d. */
+static void ptq1_0_decode(const uint8_t* blk, int8_t* t, uint16_t* d) {
+    unsigned qh = (unsigned)blk[24] | ((unsigned)blk[25] << 8);
+    for (int e = 0; e < 128; ++e) {
+        int pos, byte = ptq1_0_place(e, &pos);
+        int u = (byte >= 0) ? trit_digit(blk[byte], pos) : (int)((qh >> (2 * pos)) & 3u);
+        t[e] = (int8_t)(u - 1);
+    }
+    *d = (uint16_t)(blk[26] | (blk[27] << 8));
+}
+
+/* PTQ1_0 blocks -> trits int8 [N][K] and d [N][K/128] (half bits). */
+void w4o_ptq1_0_unpack(const uint8_t* blocks, long N, long K, int8_t* trits, uint16_t* d) {
+    long bpr = K / 128;
+    for (long r = 0; r < N; ++r)
+        for (long b = 0; b < bpr; ++b)
+            ptq1_0_decode(blocks + (r * bpr + b) * PTQ1_0_BYTES, trits + r * K + b * 128, d + r * bpr + b);
+}
+
+/* The exponent field of block b of row r, 0 for the padding past the row. */
+static int block_exponent(const uint8_t* blocks, long bpr, long r, long b) {
+    if (b >= bpr) return 0;
+    const uint8_t* blk = blocks + (r * bpr + b) * PTQ1_0_BYTES;
+    return (blk[27] >> 2) & 0x1F;
+}
+
+/* Superblock (r, sb)'s pattern as a 40-bit key, block 0's exponent on top. */
+static uint64_t pattern_key(const uint8_t* blocks, long bpr, long r, long sb) {
+    uint64_t key = 0;
+    for (int s = 0; s < 8; ++s) key = (key << 5) | (uint64_t)block_exponent(blocks, bpr, r, 8 * sb + s);
+    return key;
+}
+
+static void key_to_pattern(uint64_t key, uint8_t* p) {
+    for (int s = 7; s >= 0; --s) { p[s] = (uint8_t)(key & 0x1F); key >>= 5; }
+}
+
+typedef struct { uint64_t key; long count; } pattern_count;
+
+static int cmp_u64(const void* a, const void* b) {
+    uint64_t x = *(const uint64_t*)a, y = *(const uint64_t*)b;
+    return (x > y) - (x < y);
+}
+
+static int cmp_by_count(const void* a, const void* b) {
+    const pattern_count* x = a;
+    const pattern_count* y = b;
+    if (x->count != y->count) return (x->count < y->count) - (x->count > y->count);
+    return (x->key > y->key) - (x->key < y->key);
+}
+
+/*
+ * Build the codebook of a tensor of PTQ1_0 blocks ([P4] section 2: eight
+ * consecutive blocks' exponents take fewer than 768 patterns in practice).
+ * codebook receives up to 767 patterns of eight exponents (uint8
+ * [767][8]); returns how many, or -1 if memory runs out.
+ */
+long w4o_ptq1_1_codebook(const uint8_t* blocks, long N, long K, uint8_t* codebook) {
+    long bpr = K / 128, sbpr = (bpr + 7) / 8, total = N * sbpr;
+    uint64_t* keys = malloc((size_t)(total > 0 ? total : 1) * sizeof *keys);
+    pattern_count* runs = malloc((size_t)(total > 0 ? total : 1) * sizeof *runs);
+    if (!keys || !runs) { free(keys); free(runs); return -1; }
+    for (long r = 0; r < N; ++r)
+        for (long sb = 0; sb < sbpr; ++sb) keys[r * sbpr + sb] = pattern_key(blocks, bpr, r, sb);
+    qsort(keys, (size_t)total, sizeof *keys, cmp_u64);
+    long n_runs = 0;
+    for (long i = 0; i < total; ++i) {
+        if (n_runs > 0 && runs[n_runs - 1].key == keys[i]) ++runs[n_runs - 1].count;
+        else { runs[n_runs].key = keys[i]; runs[n_runs].count = 1; ++n_runs; }
+    }
+    qsort(runs, (size_t)n_runs, sizeof *runs, cmp_by_count);
+    long n_code = n_runs < PTQ1_1_ESCAPE ? n_runs : PTQ1_1_ESCAPE;
+    for (long i = 0; i < n_code; ++i) key_to_pattern(runs[i].key, codebook + 8 * i);
+    free(keys);
+    free(runs);
+    return n_code;
+}
+
+/*
+ * PTQ1_0 blocks -> PTQ1_1 superblocks ([P4] section 2), with the codebook
+ * from w4o_ptq1_1_codebook.  out: N * ceil(K/1024) superblocks of 216
+ * bytes.  Superblocks whose pattern is not in the codebook get index 767
+ * and an entry in the escape table: esc_idx (ascending superblock indices)
+ * and esc_patt (their eight exponents), at most max_esc entries.  Returns
+ * the number of escapes, -1 if a d is negative (PTQ1_1 stores no sign), or
+ * -2 if the escape table is too small.
+ */
+long w4o_ptq1_1_encode(const uint8_t* blocks, long N, long K, const uint8_t* codebook, long n_code,
+                       uint8_t* out, long* esc_idx, uint8_t* esc_patt, long max_esc) {
+    long bpr = K / 128, sbpr = (bpr + 7) / 8, n_esc = 0;
+    for (long r = 0; r < N; ++r) {
+        for (long sb = 0; sb < sbpr; ++sb) {
+            long g = r * sbpr + sb;
+            uint8_t* o = out + g * PTQ1_1_BYTES;
+            memset(o, 0, PTQ1_1_BYTES);
+            uint8_t pattern[8];
+            for (int s = 0; s < 8; ++s) {
+                long b = 8 * sb + s;
+                int8_t t[128];
+                uint16_t h = 0;
+                if (b < bpr) ptq1_0_decode(blocks + (r * bpr + b) * PTQ1_0_BYTES, t, &h);
+                else memset(t, 0, sizeof t);
+                if (h & 0x8000u) return -1;
+                /* qs: the block's 24 bytes hold positions 0..119 exactly as in PTQ1_0 */
+                if (b < bpr) memcpy(o + 24 * s, blocks + (r * bpr + b) * PTQ1_0_BYTES, 24);
+                else memset(o + 24 * s, 1 + 3 + 9 + 27 + 81, 24);   /* every trit 0 */
+                for (int j = 0; j < 8; ++j) {
+                    int u = 8 * s + j;
+                    o[PTQ1_1_QH + u / 5] = (uint8_t)(o[PTQ1_1_QH + u / 5] + (t[120 + j] + 1) * k_pow3[u % 5]);
+                }
+                unsigned m = h & 0x3FFu;
+                for (int bit = 0; bit < 10; ++bit)
+                    if (m & (1u << bit)) o[PTQ1_1_MANT + (10 * s + bit) / 8] |= (uint8_t)(1u << ((10 * s + bit) % 8));
+                pattern[s] = (uint8_t)((h >> 10) & 0x1F);
+            }
+            long idx = PTQ1_1_ESCAPE;
+            for (long i = 0; i < n_code; ++i)
+                if (memcmp(codebook + 8 * i, pattern, 8) == 0) { idx = i; break; }
+            if (idx == PTQ1_1_ESCAPE) {
+                if (n_esc >= max_esc) return -2;
+                esc_idx[n_esc] = g;
+                memcpy(esc_patt + 8 * n_esc, pattern, 8);
+                ++n_esc;
+            }
+            o[PTQ1_1_EXP] = (uint8_t)(idx % 256);
+            o[PTQ1_1_QH + 12] = (uint8_t)(o[PTQ1_1_QH + 12] + (idx / 256) * k_pow3[4]);
+        }
+    }
+    return n_esc;
+}
+
+/* Decode superblock g into eight blocks' trits (1024) and halves.  Returns
+ * 0, or -1 if the index names no codebook entry or escape. */
+static int ptq1_1_decode(const uint8_t* o, long g, const uint8_t* codebook, long n_code, const long* esc_idx,
+                         const uint8_t* esc_patt, long n_esc, int8_t* t, uint16_t* d) {
+    long idx = o[PTQ1_1_EXP] + 256L * trit_digit(o[PTQ1_1_QH + 12], 4);
+    const uint8_t* pattern = NULL;
+    if (idx < PTQ1_1_ESCAPE) {
+        if (idx < n_code) pattern = codebook + 8 * idx;
+    } else {
+        for (long i = 0; i < n_esc; ++i)
+            if (esc_idx[i] == g) { pattern = esc_patt + 8 * i; break; }
+    }
+    if (!pattern) return -1;
+    for (int s = 0; s < 8; ++s) {
+        for (int e = 0; e < 120; ++e) {
+            int pos, byte = ptq1_0_place(e, &pos);
+            t[128 * s + e] = (int8_t)(trit_digit(o[24 * s + byte], pos) - 1);
+        }
+        for (int j = 0; j < 8; ++j) {
+            int u = 8 * s + j;
+            t[128 * s + 120 + j] = (int8_t)(trit_digit(o[PTQ1_1_QH + u / 5], u % 5) - 1);
+        }
+        unsigned m = 0;
+        for (int bit = 0; bit < 10; ++bit)
+            if (o[PTQ1_1_MANT + (10 * s + bit) / 8] & (1u << ((10 * s + bit) % 8))) m |= 1u << bit;
+        d[s] = (uint16_t)(((unsigned)pattern[s] << 10) | m);
+    }
+    return 0;
+}
+
+/* PTQ1_1 superblocks -> trits int8 [N][K] and d [N][K/128] (the padding
+ * blocks past K are dropped).  Returns 0, or -1 on an unresolvable index. */
+int w4o_ptq1_1_unpack(const uint8_t* sblocks, long N, long K, const uint8_t* codebook, long n_code,
+                      const long* esc_idx, const uint8_t* esc_patt, long n_esc, int8_t* trits, uint16_t* d) {
+    long bpr = K / 128, sbpr = (bpr + 7) / 8;
+    int8_t t[1024];
+    uint16_t h[8];
+    for (long r = 0; r < N; ++r) {
+        for (long sb = 0; sb < sbpr; ++sb) {
+            long g = r * sbpr + sb;
+            if (ptq1_1_decode(sblocks + g * PTQ1_1_BYTES, g, codebook, n_code, esc_idx, esc_patt, n_esc, t, h))
+                return -1;
+            for (int s = 0; s < 8 && 8 * sb + s < bpr; ++s) {
+                long b = 8 * sb + s;
+                memcpy(trits + r * K + b * 128, t + 128 * s, 128);
+                d[r * bpr + b] = h[s];
+            }
+        }
+    }
+    return 0;
+}
+
+/*
+ * The MMVQ product for one row given its trits and halves ([P4] section 3:
+ * d[r,c] = sum_k W[r,k] x[c,k]); x is block_q8_1 in the PT layout.  Per
+ * 32-element q8_1 block j of 128-block b:
+ *   d_w(b) * d_x(b, j) * sum_{i<32} t_i qs_i
+ * with the integer dot exact; fp64 throughout.
+ */
+static void mmvq_row(const int8_t* t, const uint16_t* dw, const uint8_t* v, long K, double* out, double* out_abs) {
+    long bpr = K / 128;
+    double total = 0.0, abs_total = 0.0;
+    for (long b = 0; b < bpr; ++b) {
+        double w = half_bits_to_double(dw[b]);
+        for (int j = 0; j < 4; ++j) {
+            const uint8_t* ds = v + 16 * (8 * bpr + b) + 4 * j;
+            double dx = half_bits_to_double((uint16_t)(ds[0] | (ds[1] << 8)));
+            long dot = 0, adot = 0;
+            for (int i = 0; i < 32; ++i) {
+                int e = 32 * j + i;
+                int qs = (int)(int8_t)v[16 * ((e / 16) * bpr + b) + e % 16];
+                dot += (long)t[128 * b + e] * qs;
+                adot += labs((long)t[128 * b + e] * qs);
+            }
+            total += w * dx * (double)dot;
+            abs_total += fabs(w * dx) * (double)adot;
+        }
+    }
+    *out = total;
+    *out_abs = abs_total;
+}
+
+/* MMVQ over PTQ1_0 blocks; pt: C vectors of 144 K/128 bytes; rows
+ * [row_begin, row_end) of d[C][N] and ref_abs (may be NULL). */
+void w4o_mmvq_ptq1_0(const uint8_t* blocks, const uint8_t* pt, long N, long K, long C, long row_begin, long row_end,
+                     double* d, double* ref_abs) {
+    long bpr = K / 128;
+    int8_t* t = malloc((size_t)(K > 0 ? K : 1));
+    uint16_t* dw = malloc((size_t)(bpr > 0 ? bpr : 1) * sizeof *dw);
+    if (!t || !dw) { free(t); free(dw); return; }
+    for (long row = row_begin; row < row_end; ++row) {
+        for (long b = 0; b < bpr; ++b) ptq1_0_decode(blocks + (row * bpr + b) * PTQ1_0_BYTES, t + 128 * b, dw + b);
+        for (long c = 0; c < C; ++c) {
+            double v, a;
+            mmvq_row(t, dw, pt + c * 144 * bpr, K, &v, &a);
+            d[c * N + row] = v;
+            if (ref_abs) ref_abs[c * N + row] = a;
+        }
+    }
+    free(t);
+    free(dw);
+}
+
+/* MMVQ over PTQ1_1 superblocks (decoded with the codebook and escape
+ * table); as w4o_mmvq_ptq1_0 otherwise.  Returns 0, or -1 on an
+ * unresolvable index. */
+int w4o_mmvq_ptq1_1(const uint8_t* sblocks, const uint8_t* codebook, long n_code, const long* esc_idx,
+                    const uint8_t* esc_patt, long n_esc, const uint8_t* pt, long N, long K, long C, long row_begin,
+                    long row_end, double* d, double* ref_abs) {
+    long bpr = K / 128, sbpr = (bpr + 7) / 8;
+    int8_t* t = malloc((size_t)(sbpr > 0 ? sbpr : 1) * 1024);
+    uint16_t* dw = malloc((size_t)(sbpr > 0 ? sbpr : 1) * 8 * sizeof *dw);
+    if (!t || !dw) { free(t); free(dw); return -1; }
+    int rc = 0;
+    for (long row = row_begin; row < row_end && rc == 0; ++row) {
+        for (long sb = 0; sb < sbpr; ++sb) {
+            long g = row * sbpr + sb;
+            if (ptq1_1_decode(sblocks + g * PTQ1_1_BYTES, g, codebook, n_code, esc_idx, esc_patt, n_esc,
+                              t + 1024 * sb, dw + 8 * sb)) { rc = -1; break; }
+        }
+        if (rc) break;
+        for (long c = 0; c < C; ++c) {
+            double v, a;
+            mmvq_row(t, dw, pt + c * 144 * bpr, K, &v, &a);
+            d[c * N + row] = v;
+            if (ref_abs) ref_abs[c * N + row] = a;
+        }
+    }
+    free(t);
+    free(dw);
+    return rc;
 }

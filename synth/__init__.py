@@ -112,6 +112,47 @@ def int8_gemv_inputs(N, K, C, seed=0, scale_range=(2.0e-4, 8.0e-4)):
     return Int8GemvInputs(q, scale, x, N, K, C)
 
 
+@dataclass
+class TernaryInputs:
+    trits: torch.Tensor   # int8 [N, K] in {-1, 0, 1}
+    d: torch.Tensor       # int16 [N, K/128]: bit patterns of positive IEEE halves, one per 128 weights
+    x: torch.Tensor       # bf16 [C, K]
+    N: int
+    K: int
+    C: int
+
+
+def ternary_inputs(N, K, C, seed=0, outlier_fraction=0.0):
+    """Ternary weights shaped like a trained model's PTQ1_0 tensors: trits
+    uniform over {-1, 0, 1}; one positive half scale per 128 weights whose
+    exponent drifts along the row (first block uniform in 8..11, each next
+    block steps -1 / 0 / +1 with probability 0.035 / 0.93 / 0.035, kept
+    within 5..14: about 0.44 bits per step, near the 0.41 bits the ternary
+    compression page measured on its model), mantissas uniform.  A fraction
+    `outlier_fraction` of rows draws every exponent uniformly in 5..14
+    instead.  x ~ N(0,1) bf16 [C, K]."""
+    if K % 128:
+        raise ValueError("K must be a multiple of 128")
+    g = _gen(seed)
+    bpr = K // 128
+    trits = (torch.randint(0, 3, (N, K), dtype=torch.int16, generator=g) - 1).to(torch.int8)
+    start = torch.randint(8, 12, (N,), dtype=torch.int32, generator=g)
+    u = torch.rand(N, max(bpr - 1, 0), generator=g)
+    steps = (u > 0.965).to(torch.int32) - (u < 0.035).to(torch.int32)
+    outlier = torch.rand(N, generator=g) < outlier_fraction
+    wild = torch.randint(5, 15, (N, bpr), dtype=torch.int32, generator=g)
+    mant = torch.randint(0, 1024, (N, bpr), dtype=torch.int32, generator=g)
+    exps = torch.empty(N, bpr, dtype=torch.int32)
+    if bpr:
+        exps[:, 0] = start
+    for b in range(1, bpr):
+        exps[:, b] = (exps[:, b - 1] + steps[:, b - 1]).clamp(5, 14)
+    exps = torch.where(outlier[:, None], wild, exps)
+    d = ((exps << 10) | mant).to(torch.int16)
+    x = torch.randn(C, K, generator=g, dtype=torch.float32).to(torch.bfloat16)
+    return TernaryInputs(trits, d, x, N, K, C)
+
+
 def quant_inputs(K, N, seed=0, std=0.02):
     """W bf16 [K, N] ~ N(0, std)."""
     g = _gen(seed)
@@ -152,6 +193,8 @@ def np_bits(t):
         return t.view(torch.int16).numpy().view(np.uint16)
     if t.dtype == torch.int32:
         return t.numpy().view(np.uint32)
+    if t.dtype == torch.int16:
+        return t.numpy().view(np.uint16)
     if t.dtype == torch.int8:
         return t.numpy().view(np.uint8)
     return t.numpy()

@@ -3,8 +3,9 @@
 Each mutant below plants one plausible mistake in oracle/w4_oracle.c -- a
 dropped term, a wrong sign, index or divisor, a transposed operand, ties
 rounded the wrong way -- builds the changed source with the oracle's own
-compiler flags into a temporary library, and runs tests/test_oracle_pins.py
-against it in a child process (the oracle loads the library that
+compiler flags into a temporary library, and runs the pin suites
+(tests/test_oracle_pins.py, tests/test_oracle_ternary_pins.py) against it in
+a child process (the oracle loads the library that
 W4_ORACLE_LIB names).  Every mutant must make at least one pin fail; the
 unchanged source, built and run the same way, must pass them all.
 
@@ -22,7 +23,7 @@ from concurrent.futures import ThreadPoolExecutor
 from oracle.build import SRC, compile_oracle
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-PINS = os.path.join(ROOT, "tests", "test_oracle_pins.py")
+PINS = [os.path.join(ROOT, "tests", name) for name in ("test_oracle_pins.py", "test_oracle_ternary_pins.py")]
 
 # (name, [(text in w4_oracle.c, replacement), ...]); each text occurs once.
 MUTANTS = [
@@ -97,6 +98,28 @@ MUTANTS = [
                                 "int qs = (int)(int8_t)v[16 * (i * 8 + e / 16) + e % 16];")]),
     ("w4a8_d_and_s_swapped", [("double db = half_bits_to_double((uint16_t)(ds[0] | (ds[1] << 8)));",
                                "double db = half_bits_to_double((uint16_t)(ds[2] | (ds[3] << 8)));")]),
+    # ternary PTQ1_0 / PTQ1_1 formats and their MMVQ
+    ("ternary_contiguous_head", [("if (e < 80) { *pos = e >> 4; return e & 15; }",
+                                  "if (e < 80) { *pos = e % 5; return e / 5; }")]),
+    ("ternary_contiguous_middle", [("if (e < 120) { *pos = (e - 80) >> 3; return 16 + ((e - 80) & 7); }",
+                                    "if (e < 120) { *pos = (e - 80) % 5; return 16 + (e - 80) / 5; }")]),
+    ("ternary_digit_weights_reversed", [("return (byte / k_pow3[pos]) % 3;", "return (byte / k_pow3[4 - pos]) % 3;"),
+                                        ("(blk[byte] + (t + 1) * k_pow3[pos])", "(blk[byte] + (t + 1) * k_pow3[4 - pos])")]),
+    ("ternary_qh_field_order", [("(int)((qh >> (2 * pos)) & 3u)", "(int)((qh >> (2 * (7 - pos))) & 3u)")]),
+    ("ternary_codebook_rarest_first", [("return (x->count < y->count) - (x->count > y->count);",
+                                        "return (x->count > y->count) - (x->count < y->count);")]),
+    ("ternary_codebook_ties_descending", [("return (x->key > y->key) - (x->key < y->key);",
+                                           "return (x->key < y->key) - (x->key > y->key);")]),
+    ("ternary_free_trit_position", [("(idx / 256) * k_pow3[4]", "(idx / 256) * k_pow3[3]")]),
+    ("ternary_mantissa_bit_order", [("m |= 1u << bit;", "m |= 1u << (9 - bit);")]),
+    ("ternary_escape_lookup", [("pattern = esc_patt + 8 * i; break;", "pattern = esc_patt; break;")]),
+    ("ternary_superblock_qs_shift", [("trit_digit(o[24 * s + byte], pos)", "trit_digit(o[24 * ((s + 1) % 8) + byte], pos)")]),
+    ("ternary_superblock_tail_order", [("int u = 8 * s + j;\n            t[128 * s + 120 + j]",
+                                        "int u = 8 * j + s;\n            t[128 * s + 120 + j]")]),
+    ("mmvq_digit_for_trit", [("dot += (long)t[128 * b + e] * qs;", "dot += (long)(t[128 * b + e] + 1) * qs;")]),
+    ("mmvq_s_for_d", [("double dx = half_bits_to_double((uint16_t)(ds[0] | (ds[1] << 8)));",
+                       "double dx = half_bits_to_double((uint16_t)(ds[2] | (ds[3] << 8)));")]),
+    ("mmvq_first_block_scale", [("double w = half_bits_to_double(dw[b]);", "double w = half_bits_to_double(dw[0]);")]),
 ]
 
 
@@ -116,7 +139,7 @@ def _run_pins(name, source, workdir):
         f.write(source)
     compile_oracle(src, lib)
     env = dict(os.environ, W4_ORACLE_LIB=lib)
-    r = subprocess.run([sys.executable, "-m", "pytest", PINS, "-x", "-q", "-p", "no:cacheprovider"],
+    r = subprocess.run([sys.executable, "-m", "pytest", *PINS, "-x", "-q", "-p", "no:cacheprovider"],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     tail = "\n".join((r.stdout + r.stderr).strip().splitlines()[-15:])
     return r.returncode, tail

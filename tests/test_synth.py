@@ -44,3 +44,20 @@ def test_bf16_half_ulp_helper():
     ref = np.array([1.0 + 2**-8 + 1e-6])
     assert not parity_violations(np.array([1.0]), ref, np.array([1.0]), 2e-3, True).any()
     assert parity_violations(np.array([1.0 - 2**-6]), ref, np.array([1.0]), 2e-3, True).any()
+
+
+def test_ternary_inputs_deterministic_and_shaped():
+    a = synth.ternary_inputs(64, 1152, 2, seed=0)
+    b = synth.ternary_inputs(64, 1152, 2, seed=0)
+    assert torch.equal(a.trits, b.trits) and torch.equal(a.d, b.d) and torch.equal(a.x, b.x)
+    assert a.trits.shape == (64, 1152) and a.trits.dtype == torch.int8
+    assert a.d.shape == (64, 9) and a.x.shape == (2, 1152) and a.x.dtype == torch.bfloat16
+    counts = np.bincount(a.trits.numpy().ravel() + 1, minlength=3)
+    assert counts.min() > 0.95 * counts.mean()
+    d = synth.np_bits(a.d)
+    e = (d >> 10) & 31
+    assert (d < 0x8000).all() and e.min() >= 5 and e.max() <= 14      # positive halves, exponents in range
+    steps = np.abs(np.diff(e.astype(int), axis=1))
+    assert steps.max() <= 1 and 0.85 < (steps == 0).mean() < 0.99
+    wild = synth.ternary_inputs(64, 1152, 1, seed=0, outlier_fraction=1.0)
+    assert (np.abs(np.diff(((synth.np_bits(wild.d) >> 10) & 31).astype(int), axis=1)) > 1).any()
