@@ -15,6 +15,7 @@ in the library's CUDA kernels; there is no CPU or eager fallback.
     quantize_int8(W)                    -> (q [K, N] int8, scale [N] fp32)
     permute_int8(q)                     -> out [N*K] int8 (interleaved)
     gemv_w8(q, scale, x)                -> d [C, N] bf16
+    ptq1_1_encode(blocks)               -> (sblocks, codebook, esc_idx, esc_patt): PTQ1_0 -> PTQ1_1 (host)
 """
 import torch
 
@@ -22,7 +23,7 @@ from . import _lib
 from ._lib import W4Error, W4_BF16, W4_F32
 
 __all__ = ["quantize_pack_int4", "permute_int4", "quantize_pack_permute_int4", "gemv_w4", "gemv_w4_permuted", "gemm_w4",
-           "quantize_int8", "permute_int8", "gemv_w8", "device_error", "W4Error"]
+           "quantize_int8", "permute_int8", "gemv_w8", "ptq1_1_encode", "device_error", "W4Error"]
 
 _lib.load()  # fail loudly at import if the CUDA library is missing
 
@@ -230,6 +231,37 @@ def gemv_w8(q, scale, x, out=None, stream=None):
                              _stream(stream))
     _lib.check("gemv_w8", st)
     return out
+
+
+def ptq1_1_encode(blocks):
+    """Convert ternary PTQ1_0 blocks (host uint8 [N, K/128, 28], numpy or a
+    CPU tensor) into PTQ1_1 superblocks with the tensor's own codebook.
+    Runs on the host.  Returns numpy (sblocks uint8 [N, ceil(K/1024), 216],
+    codebook uint8 [n_code, 8], esc_idx int64 [n_esc], esc_patt uint8
+    [n_esc, 8])."""
+    import ctypes
+    import numpy as np
+    b = blocks.numpy() if isinstance(blocks, torch.Tensor) else blocks
+    b = np.ascontiguousarray(b, dtype=np.uint8)
+    if b.ndim != 3 or b.shape[2] != 28:
+        raise ValueError("blocks must be [N, K/128, 28] bytes")
+    N, bpr = b.shape[:2]
+    K = 128 * bpr
+    sbpr = -(-bpr // 8)
+    lib = _lib.load()
+    ptr = lambda a: a.ctypes.data_as(ctypes.c_void_p)
+    code = np.zeros((767, 8), np.uint8)
+    n_code = ctypes.c_int64(0)
+    _lib.check("ptq1_1_codebook", lib.ptq1_1_codebook(ptr(b), N, K, ptr(code), ctypes.byref(n_code)))
+    sblocks = np.zeros((N, sbpr, 216), np.uint8)
+    cap = max(1, N * sbpr)
+    esc_idx = np.zeros(cap, np.int64)
+    esc_patt = np.zeros((cap, 8), np.uint8)
+    n_esc = ctypes.c_int64(0)
+    _lib.check("ptq1_1_encode", lib.ptq1_1_encode(ptr(b), N, K, ptr(code), n_code.value, ptr(sblocks), ptr(esc_idx),
+                                                  ptr(esc_patt), cap, ctypes.byref(n_esc)))
+    n = n_esc.value
+    return sblocks, code[:n_code.value].copy(), esc_idx[:n].copy(), esc_patt[:n].copy()
 
 
 def device_error(stream=None):
