@@ -65,9 +65,13 @@ WORKLOADS = {
     # quantize_int8 + permute_int8 of one 8192x8192 weight
     "w8_decode": dict(kind="gemv8", N=17280, K=5120, C=1),
     "w8_quant": dict(kind="quant8", K=8192, N=8192),
+    # W4A8: x quantised to block_q8_1 in the PT planes, then the int4 GEMV
+    # with integer dots (two kernels per step)
+    "w4a8_decode": dict(kind="w4a8", N=17280, K=5120, C=1),
+    "w4a8_c8": dict(kind="w4a8", N=5120, K=17280, C=8),
 }
 COMPONENTS = ["c4", "c8", "c4s", "c8s", "c4_perm", "c8_perm", "c4s_perm", "c8s_perm", "quant", "quant_2call", "gemm",
-              "w8_decode", "w8_quant"]
+              "w8_decode", "w8_quant", "w4a8_decode", "w4a8_c8"]
 
 
 def load_peaks():
@@ -103,6 +107,12 @@ def gemv8_bytes(N, K, C):
 def quant8_bytes(K, N):
     # quantize_int8: read W, write q + scale; permute_int8: read + write q
     return (2 * K * N + K * N + 4 * N) + 2 * K * N
+
+
+def w4a8_bytes(N, K, C):
+    # weights + bf16 scale and zero + x read by the quantiser + the PT
+    # activations written and read back + d
+    return N * K // 2 + 4 * N + 2 * C * K + 2 * C * 144 * (K // 128) + 2 * C * N
 
 
 def gemm_bytes(M, N, K):
@@ -352,6 +362,37 @@ class Gemv8Work:
         return "rotating %d int8 weight copies (%.0f MB > 2x L2)" % (self.R, self.R * self.N * self.K / 1e6)
 
 
+class W4a8Work:
+    """quantize_q8_1_pt of x, then gemv_w4a8 over rotating weight copies."""
+
+    def __init__(self, w4, N, K, C, seed=0):
+        g = synth.gemv_inputs(N, K, C, act="bf16", seed=seed)
+        self.g = g
+        dev = torch.device("cuda")
+        self.R = copies_for(N * K // 2)
+        self.q = [g.qweight.to(dev) for _ in range(self.R)]
+        self.s, self.z, self.x = g.scale.to(dev), g.zero.to(dev), g.x.to(dev)
+        self.pt = torch.empty((C, 144 * (K // 128)), dtype=torch.uint8, device=dev)
+        self.d = torch.empty((C, N), dtype=torch.bfloat16, device=dev)
+        self.w4 = w4
+        self.i = 0
+        self.N, self.K, self.C = N, K, C
+        self.bytes = w4a8_bytes(N, K, C)
+        self.flops = 2 * N * K * C
+        self.launches_per_step = 2
+
+    def run(self, x, i):
+        self.w4.quantize_q8_1_pt(x, out=self.pt)
+        self.w4.gemv_w4a8(self.q[i % self.R], self.s, self.z, self.pt, out=self.d)
+
+    def step(self):
+        self.run(self.x, self.i)
+        self.i += 1
+
+    def l2_note(self):
+        return "rotating %d weight copies (%.0f MB > 2x L2)" % (self.R, self.R * self.N * self.K / 2 / 1e6)
+
+
 class Quant8Work:
     """quantize_int8 + permute_int8 of one weight."""
 
@@ -434,6 +475,8 @@ def make_work(w4, name):
         return Gemv8Work(w4, **cfg)
     if kind == "quant8":
         return Quant8Work(w4, **cfg)
+    if kind == "w4a8":
+        return W4a8Work(w4, **cfg)
     return GemmWork(w4, **cfg)
 
 
@@ -482,9 +525,12 @@ def e2e_gemv(w4, work, steps, world):
     stream = torch.cuda.current_stream()
     perm = isinstance(work, GemvPermWork)
     w8 = isinstance(work, Gemv8Work)
+    w4a8 = isinstance(work, W4a8Work)
 
     def call(i):
-        if perm:
+        if w4a8:
+            work.run(x_dev, i)
+        elif perm:
             w4.gemv_w4_permuted(work.q[i % work.R], work.s, x_dev, out=work.d)
         elif w8:
             w4.gemv_w8(work.q[i % work.R], work.s, x_dev, out=work.d)
@@ -632,6 +678,24 @@ def cpu_baseline(name, budget_s=10.0):
                 "cores": 1, "kind": "oracle",
                 "sample": "%d columns of the %dx%d C=%d int8 GEMV (fp64 C oracle, single thread), %.1f s" %
                           (done, cfg["N"], cfg["K"], cfg["C"], t_total)}
+    if cfg["kind"] == "w4a8":
+        g = synth.gemv_inputs(cfg["N"], cfg["K"], cfg["C"], act="bf16", seed=0)
+        qw, s, z, xb = np_bits(g.qweight), np_bits(g.scale), np_bits(g.zero), np_bits(g.x)
+        N, K = cfg["N"], cfg["K"]
+        done, t_total, r0 = 0, 0.0, 0
+        rows = 256
+        while t_total < budget_s:
+            r1 = min(N, r0 + rows)
+            t0 = time.perf_counter()
+            pt = oracle.quantize_q8_1_pt(xb)
+            oracle.gemv_w4a8(qw, s, z, pt, K, rows=(r0, r1))
+            t_total += time.perf_counter() - t0
+            done += r1 - r0
+            r0 = 0 if r1 >= N else r1
+        return {"value": w4a8_bytes(N, K, cfg["C"]) * done / N / t_total / 1e9, "unit": "GB/s", "cores": 1,
+                "kind": "oracle",
+                "sample": "%d rows of the %dx%d C=%d W4A8 GEMV, x quantised each time (fp64 C oracle, single "
+                          "thread), %.1f s" % (done, N, K, cfg["C"], t_total)}
     if cfg["kind"] == "quant8":
         K, N = cfg["K"], cfg["N"]
         W = np_bits(synth.quant_inputs(K, N, seed=0))
@@ -679,6 +743,8 @@ def dtype_of(name):
         return "bf16 x / int8 weights (fp32 FMA)"
     if cfg["kind"] == "quant8":
         return "bf16 in, int8 out (fp32 division)"
+    if cfg["kind"] == "w4a8":
+        return "x quantised to int8 (block_q8_1) / uint4 weights, int32 dp4a dots, fp32 accumulate"
     return "bf16 in, int4 out (fp32 arithmetic)"
 
 
@@ -718,7 +784,7 @@ def run_ours(args, world, rank):
         soak(g, stream, 2.0)
         sec2, _, _ = time_graph(work, args.steps, 0, world)
     clocks = cs.summary()
-    if kind in ("gemv", "gemv8"):
+    if kind in ("gemv", "gemv8", "w4a8"):
         e2e_sec, hb, ob = e2e_gemv(w4, work, args.steps, world)
     else:
         e2e_sec, hb, ob = e2e_generic(work, max(2, min(args.steps, 10)), world)
@@ -738,6 +804,9 @@ def run_ours(args, world, rank):
     }
     if kind == "quant8" or (kind == "quant" and not WORKLOADS[args.workload].get("fused", True)):
         line["roofline"]["note"] = "two kernels per step (quantise, then permute); achieved = step bytes / step time"
+    if kind == "w4a8":
+        line["roofline"]["note"] = ("two kernels per step (quantise x, then the GEMV); achieved = step bytes / "
+                                    "step time")
     if rank == 0 and world == 1:
         line["cpu_baseline"] = cpu_baseline(args.workload, budget_s=args.cpu_seconds)
     if args.components and world == 1:

@@ -15,6 +15,8 @@ in the library's CUDA kernels; there is no CPU or eager fallback.
     quantize_int8(W)                    -> (q [K, N] int8, scale [N] fp32)
     permute_int8(q)                     -> out [N*K] int8 (interleaved)
     gemv_w8(q, scale, x)                -> d [C, N] bf16
+    quantize_q8_1_pt(x)                 -> pt [C, 144*K/128] uint8 (block_q8_1 in PT planes)
+    gemv_w4a8(qweight, scale, zero, pt) -> d [C, N] bf16 (int4 weights x int8 activations)
 """
 import torch
 
@@ -22,7 +24,7 @@ from . import _lib
 from ._lib import W4Error, W4_BF16, W4_F32
 
 __all__ = ["quantize_pack_int4", "permute_int4", "quantize_pack_permute_int4", "gemv_w4", "gemv_w4_permuted", "gemm_w4",
-           "quantize_int8", "permute_int8", "gemv_w8", "device_error", "W4Error"]
+           "quantize_int8", "permute_int8", "gemv_w8", "quantize_q8_1_pt", "gemv_w4a8", "device_error", "W4Error"]
 
 _lib.load()  # fail loudly at import if the CUDA library is missing
 
@@ -229,6 +231,46 @@ def gemv_w8(q, scale, x, out=None, stream=None):
     st = _lib.load().gemv_w8(q.data_ptr(), scale.data_ptr(), xx.data_ptr(), out.data_ptr(), N, K, C,
                              _stream(stream))
     _lib.check("gemv_w8", st)
+    return out
+
+
+def quantize_q8_1_pt(x, out=None, stream=None):
+    """x bf16 [C, K] (K % 128 == 0) as block_q8_1 in the PT planes: uint8
+    [C, 144*K/128] per vector (qs planes 0..7, the (d, s) halves in plane 8)."""
+    _need(x, "x", (torch.bfloat16,))
+    xx = x if x.dim() == 2 else x.reshape(1, -1)
+    C, K = xx.shape
+    if out is None:
+        out = torch.empty((C, 144 * (K // 128)), dtype=torch.uint8, device=x.device)
+    _need(out, "out", (torch.uint8, torch.int8))
+    if out.numel() != C * 144 * (K // 128):
+        raise ValueError("out must hold C*144*K/128 bytes")
+    st = _lib.load().quantize_q8_1_pt(xx.data_ptr(), out.data_ptr(), C, K, _stream(stream))
+    _lib.check("quantize_q8_1_pt", st)
+    return out
+
+
+def gemv_w4a8(qweight, scale, zero, pt, out=None, stream=None):
+    """d[c, r] = scale[r] * sum_b (d_b * sum_{k in b} q[r, k] qs[c, k] - zero[r] s_b):
+    gemv_w4's packed words (int32 [N, K/8]), bf16 scale and zero [N], and x as
+    quantize_q8_1_pt's output (uint8 [C, 144*K/128], C <= 8).  Returns bf16 [C, N]."""
+    _need(qweight, "qweight", (torch.int32, torch.uint32) if hasattr(torch, "uint32") else (torch.int32,), 2)
+    _need(scale, "scale", (torch.bfloat16,), 1)
+    _need(zero, "zero", (torch.bfloat16,), 1)
+    _need(pt, "pt", (torch.uint8, torch.int8))
+    N, K = qweight.shape[0], qweight.shape[1] * 8
+    pp = pt if pt.dim() == 2 else pt.reshape(1, -1)
+    C = pp.shape[0]
+    if K % 128 or pp.shape[1] != 144 * (K // 128) or scale.numel() != N or zero.numel() != N:
+        raise ValueError("shape mismatch")
+    if out is None:
+        out = torch.empty((C, N), dtype=torch.bfloat16, device=qweight.device)
+    _need(out, "out", (torch.bfloat16,))
+    if out.numel() != C * N:
+        raise ValueError("out must hold C*N elements")
+    st = _lib.load().gemv_w4a8(qweight.data_ptr(), scale.data_ptr(), zero.data_ptr(), pp.data_ptr(), out.data_ptr(),
+                               N, K, C, _stream(stream))
+    _lib.check("gemv_w4a8", st)
     return out
 
 

@@ -21,6 +21,10 @@ w4_status run_quantize_int8(const void* W, void* q, float* scale, int64_t K, int
 w4_status run_permute_int8(const void* q, void* out, int64_t K, int64_t N, cudaStream_t s);
 w4_status run_gemv_w8(const void* q, const float* scale, const void* x, void* d, int64_t N, int64_t K, int64_t C,
                       cudaStream_t s);
+w4_status run_quantize_q8_1_pt(const void* x, void* pt, int64_t C, int64_t K, cudaStream_t s);
+w4_status run_gemv_w4a8(const void* qw, const void* scale, const void* zero, const void* pt, void* d, int64_t N,
+                        int64_t K, int64_t C, cudaStream_t s);
+bool w4a8_fits(int64_t C, int64_t K);
 int take_device_error_gemm();
 int take_device_error_gemv();
 int take_device_error_quant();
@@ -75,7 +79,7 @@ using namespace w4;
 
 extern "C" {
 
-int w4_abi_version(void) { return 3; }
+int w4_abi_version(void) { return 4; }
 
 int w4_device_error(void* stream) {
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return -1;
@@ -186,6 +190,27 @@ w4_status gemv_w8(const void* q, const float* scale, const void* x, void* d, int
     if (!device_is_sm103()) return W4_ERR_DEVICE;
     if (K == 0) return launch_status(cudaMemsetAsync(d, 0, C * N * 2, (cudaStream_t)stream));
     return run_gemv_w8(q, scale, x, d, N, K, C, (cudaStream_t)stream);
+}
+
+w4_status quantize_q8_1_pt(const void* x, void* pt, int64_t C, int64_t K, void* stream) {
+    if (C < 0 || K < 0 || (K % 128) != 0) return W4_ERR_SHAPE;
+    if (C == 0 || K == 0) return W4_OK;
+    if (!x || !pt) return W4_ERR_NULL;
+    if (!aligned16(x) || !aligned16(pt)) return W4_ERR_ALIGN;
+    if (!device_is_sm103()) return W4_ERR_DEVICE;
+    return run_quantize_q8_1_pt(x, pt, C, K, (cudaStream_t)stream);
+}
+
+w4_status gemv_w4a8(const void* qweight, const void* scale, const void* zero, const void* pt, void* d, int64_t N,
+                    int64_t K, int64_t C, void* stream) {
+    if (N < 0 || K < 0 || (K % 128) != 0 || C < 1 || C > 8 || !w4a8_fits(C, K)) return W4_ERR_SHAPE;
+    if (N == 0) return W4_OK;
+    if (!d || !scale || !zero || (K > 0 && (!qweight || !pt))) return W4_ERR_NULL;
+    if (!aligned16(d) || !aligned16(scale) || !aligned16(zero) || (K > 0 && (!aligned16(qweight) || !aligned16(pt))))
+        return W4_ERR_ALIGN;
+    if (!device_is_sm103()) return W4_ERR_DEVICE;
+    if (K == 0) return launch_status(cudaMemsetAsync(d, 0, C * N * 2, (cudaStream_t)stream));
+    return run_gemv_w4a8(qweight, scale, zero, pt, d, N, K, C, (cudaStream_t)stream);
 }
 
 w4_status gemm_w4(const void* A, const void* B, const void* scale, const void* zero, void* C, int64_t M, int64_t N,

@@ -22,6 +22,10 @@
  *   quantize_int8, permute_int8, gemv_w8
  *                       the int8 weight-only counterparts (the first page's
  *                       int8 permute, from which its int4 permute derives).
+ *   quantize_q8_1_pt, gemv_w4a8
+ *                       x quantised to block_q8_1 in the "PT" planes, and
+ *                       gemv_w4's int4 weights against it with integer dot
+ *                       products ("三值量化模型的无损压缩", sections 3 and 3.1).
  *
  * Conventions shared by every entry point:
  *   - All data pointers are DEVICE pointers owned by the caller.  The library
@@ -266,6 +270,53 @@ w4_status permute_int8(const void* q, void* out, int64_t K, int64_t N, void* str
  */
 w4_status gemv_w8(const void* q, const float* scale, const void* x, void* d, int64_t N, int64_t K, int64_t C,
                   void* stream);
+
+/* Shared memory available to one CTA on sm_103 (227 KB); gemv_w4a8 keeps all
+ * of x there. */
+#define W4_W4A8_MAX_SMEM 232448
+
+/*
+ * quantize_q8_1_pt -- x as block_q8_1 in the PT planes (page
+ * "三值量化模型的无损压缩", section 3.1 "数据格式": 32 int8 values qs and the
+ * halves (d, s) per block, s = d * sum qs).  For every 32-element block of
+ * every vector:
+ *   d  = max |x| / 127                            (IEEE fp32 division)
+ *   qs = clamp(round(x / d), -127, 127)           (IEEE fp32 division, round
+ *        half away from zero; a block whose maximum is 0 gets d = 0, qs = 0)
+ *   stored: qs as int8, and d and the fp32 product d * sum qs as IEEE halves
+ *   rounded to nearest even.
+ * Layout of one vector (144 * K/128 bytes): element e of 128-element block i
+ * is byte 16 * ((e / 16) * K/128 + i) + e % 16 (planes 0..7), and the four
+ * (d, s) pairs of block i are the 16 bytes at 16 * (8 * K/128 + i) (plane 8;
+ * pair j at +4j, d then s, little-endian).  Vectors follow each other.
+ *
+ * x   bf16 [C][K] row-major, 16-byte aligned.
+ * pt  uint8 [C][144*K/128] (output), 16-byte aligned.
+ * Requires K % 128 == 0 (else W4_ERR_SHAPE); C == 0 or K == 0 is a no-op.
+ * NaN or Inf in x is undefined.  Bit-exact with the definition above.
+ */
+w4_status quantize_q8_1_pt(const void* x, void* pt, int64_t C, int64_t K, void* stream);
+
+/*
+ * gemv_w4a8 -- gemv_w4's int4 weights against activations in block_q8_1 /
+ * PT form (same page, sections 3 and 3.1), with exact integer dot products
+ * per 32-element block b and the zero point corrected through s:
+ *
+ *   d[c][r] = scale[r] * sum_b ( d_b * sum_{k in b} q[r][k] * qs[c][k]
+ *                                - zero[r] * s_b )
+ *
+ * qweight  uint32 [N][K/8] as for gemv_w4 (nibble j of word i is k = 8i+j,
+ *          unsigned), 16-byte aligned.
+ * scale, zero  bf16 [N], 16-byte aligned.
+ * pt       quantize_q8_1_pt's output for the C vectors, 16-byte aligned.
+ * d        bf16 [C][N] row-major (output), 16-byte aligned.
+ * Requires K % 128 == 0, 1 <= C <= 8 and C * K * 5/4 + 32 <= W4_W4A8_MAX_SMEM
+ * (x is kept in shared memory; K <= 23168 at C = 8), else W4_ERR_SHAPE;
+ * K == 0 gives d = 0.  fp32 accumulation of the exact dots; the tolerance is
+ * 2e-3 * sum_k |(q - zero) * scale * d_b * qs| plus the bf16 rounding.
+ */
+w4_status gemv_w4a8(const void* qweight, const void* scale, const void* zero, const void* pt, void* d, int64_t N,
+                    int64_t K, int64_t C, void* stream);
 
 #ifdef __cplusplus
 }

@@ -27,7 +27,7 @@ def _declared_functions():
 def test_header_declares_the_hot_path():
     names = _declared_functions()
     for fn in ("quantize_pack_int4", "permute_int4", "quantize_pack_permute_int4", "gemv_w4", "gemv_w4_permuted",
-               "gemm_w4", "quantize_int8", "permute_int8", "gemv_w8",
+               "gemm_w4", "quantize_int8", "permute_int8", "gemv_w8", "quantize_q8_1_pt", "gemv_w4a8",
                "w4_status_string", "w4_abi_version", "w4_device_error"):
         assert fn in names
 
@@ -36,7 +36,7 @@ def test_library_exports_every_declared_symbol():
     lib, _ = _lib()
     for fn in _declared_functions():
         assert hasattr(lib, fn), "libw4.so does not export %s" % fn
-    assert lib.w4_abi_version() == 3
+    assert lib.w4_abi_version() == 4
     assert lib.w4_status_string(-2) == b"illegal size or shape"
 
 
@@ -108,6 +108,20 @@ def test_argument_validation_happens_on_host():
     assert lib.gemv_w8(A, A, A, A, 0, 64, 1, None) == L.W4_OK
     assert lib.gemv_w8(A, A, None, A, 16, 64, 1, None) == L.W4_ERR_NULL
     assert lib.gemv_w8(A, A, A, odd, 16, 64, 1, None) == L.W4_ERR_ALIGN
+    # W4A8: the PT layout needs K % 128; x lives in shared memory
+    assert lib.quantize_q8_1_pt(A, A, 1, 192, None) == L.W4_ERR_SHAPE
+    assert lib.quantize_q8_1_pt(A, A, -1, 128, None) == L.W4_ERR_SHAPE
+    assert lib.quantize_q8_1_pt(A, A, 0, 128, None) == L.W4_OK
+    assert lib.quantize_q8_1_pt(A, A, 2, 0, None) == L.W4_OK
+    assert lib.quantize_q8_1_pt(None, A, 1, 128, None) == L.W4_ERR_NULL
+    assert lib.quantize_q8_1_pt(A, odd, 1, 128, None) == L.W4_ERR_ALIGN
+    assert lib.gemv_w4a8(A, A, A, A, A, 16, 192, 1, None) == L.W4_ERR_SHAPE        # K % 128
+    assert lib.gemv_w4a8(A, A, A, A, A, 16, 128, 0, None) == L.W4_ERR_SHAPE
+    assert lib.gemv_w4a8(A, A, A, A, A, 16, 128, 9, None) == L.W4_ERR_SHAPE
+    assert lib.gemv_w4a8(A, A, A, A, A, 16, 23168 + 128, 8, None) == L.W4_ERR_SHAPE  # x exceeds shared memory
+    assert lib.gemv_w4a8(A, A, A, A, A, 0, 128, 1, None) == L.W4_OK
+    assert lib.gemv_w4a8(A, A, None, A, A, 16, 128, 1, None) == L.W4_ERR_NULL
+    assert lib.gemv_w4a8(A, A, A, odd, A, 16, 128, 1, None) == L.W4_ERR_ALIGN
     # gemm_w4
     assert lib.gemm_w4(A, A, A, A, A, 128, 256, 100, None) == L.W4_ERR_SHAPE
     assert lib.gemm_w4(A, A, A, A, A, 128, 250, 128, None) == L.W4_ERR_SHAPE
