@@ -69,9 +69,13 @@ WORKLOADS = {
     # with integer dots (two kernels per step)
     "w4a8_decode": dict(kind="w4a8", N=17280, K=5120, C=1),
     "w4a8_c8": dict(kind="w4a8", N=5120, K=17280, C=8),
+    # ternary PTQ1_0 weights: x quantised to block_q8_1 / PT, then the MMVQ
+    "ptq1_decode": dict(kind="ptq1", N=17280, K=5120, C=1),
+    "ptq1_c8": dict(kind="ptq1", N=5120, K=17280, C=8),
 }
 COMPONENTS = ["c4", "c8", "c4s", "c8s", "c4_perm", "c8_perm", "c4s_perm", "c8s_perm", "quant", "quant_2call", "gemm",
-              "w8_decode", "w8_quant", "w4a8_decode", "w4a8_c8"]
+              "w8_decode", "w8_quant", "w4a8_decode", "w4a8_c8",
+              "ptq1_decode", "ptq1_c8"]
 
 
 def load_peaks():
@@ -113,6 +117,12 @@ def w4a8_bytes(N, K, C):
     # weights + bf16 scale and zero + x read by the quantiser + the PT
     # activations written and read back + d
     return N * K // 2 + 4 * N + 2 * C * K + 2 * C * 144 * (K // 128) + 2 * C * N
+
+
+def ptq1_bytes(N, K, C):
+    # PTQ1_0 blocks + x read by the quantiser + the PT activations written
+    # and read back + d (fp32)
+    return N * (K // 128) * 28 + 2 * C * K + 2 * C * 144 * (K // 128) + 4 * C * N
 
 
 def gemm_bytes(M, N, K):
@@ -393,6 +403,38 @@ class W4a8Work:
         return "rotating %d weight copies (%.0f MB > 2x L2)" % (self.R, self.R * self.N * self.K / 2 / 1e6)
 
 
+class Ptq1Work:
+    """quantize_q8_1_pt of x, then mmvq_ptq1_0 over rotating copies of a
+    PTQ1_0 tensor."""
+
+    def __init__(self, w4, N, K, C, seed=0):
+        dev = torch.device("cuda")
+        blocks = synth.ptq1_0_blocks(N, K, seed=seed)
+        self.R = copies_for(blocks.nbytes)
+        self.q = [torch.from_numpy(blocks).to(dev) for _ in range(self.R)]
+        self.x_cpu = synth.gemv_inputs(1, K, C, act="bf16", seed=seed).x
+        self.x = self.x_cpu.to(dev)
+        self.pt = torch.empty((C, 144 * (K // 128)), dtype=torch.uint8, device=dev)
+        self.d = torch.empty((C, N), dtype=torch.float32, device=dev)
+        self.w4 = w4
+        self.i = 0
+        self.N, self.K, self.C = N, K, C
+        self.bytes = ptq1_bytes(N, K, C)
+        self.flops = 2 * N * K * C
+        self.launches_per_step = 2
+
+    def run(self, x, i):
+        self.w4.quantize_q8_1_pt(x, out=self.pt)
+        self.w4.mmvq_ptq1_0(self.q[i % self.R], self.pt, out=self.d)
+
+    def step(self):
+        self.run(self.x, self.i)
+        self.i += 1
+
+    def l2_note(self):
+        return "rotating %d PTQ1_0 copies (%.0f MB > 2x L2)" % (self.R, self.R * self.N * self.K / 128 * 28 / 1e6)
+
+
 class Quant8Work:
     """quantize_int8 + permute_int8 of one weight."""
 
@@ -477,6 +519,8 @@ def make_work(w4, name):
         return Quant8Work(w4, **cfg)
     if kind == "w4a8":
         return W4a8Work(w4, **cfg)
+    if kind == "ptq1":
+        return Ptq1Work(w4, **cfg)
     return GemmWork(w4, **cfg)
 
 
@@ -519,13 +563,13 @@ def soak(g, stream, seconds):
 
 def e2e_gemv(w4, work, steps, world):
     """Public API, host buffers: x from pinned host memory in, d back out."""
-    x_host = work.g.x.clone().pin_memory()
-    d_host = torch.empty((work.C, work.N), dtype=torch.bfloat16).pin_memory()
+    x_host = (work.x_cpu if isinstance(work, Ptq1Work) else work.g.x).clone().pin_memory()
+    d_host = torch.empty((work.C, work.N), dtype=work.d.dtype).pin_memory()
     x_dev = torch.empty_like(work.x)
     stream = torch.cuda.current_stream()
     perm = isinstance(work, GemvPermWork)
     w8 = isinstance(work, Gemv8Work)
-    w4a8 = isinstance(work, W4a8Work)
+    w4a8 = isinstance(work, (W4a8Work, Ptq1Work))
 
     def call(i):
         if w4a8:
@@ -554,7 +598,7 @@ def e2e_gemv(w4, work, steps, world):
     torch.cuda.synchronize()
     barrier(world)
     sec = max_over_ranks(start.elapsed_time(end) / 1e3, world)
-    return sec, x_host.numel() * 2, d_host.numel() * 2
+    return sec, x_host.numel() * 2, d_host.numel() * d_host.element_size()
 
 
 def e2e_generic(work, steps, world):
@@ -696,6 +740,24 @@ def cpu_baseline(name, budget_s=10.0):
                 "kind": "oracle",
                 "sample": "%d rows of the %dx%d C=%d W4A8 GEMV, x quantised each time (fp64 C oracle, single "
                           "thread), %.1f s" % (done, N, K, cfg["C"], t_total)}
+    if cfg["kind"] == "ptq1":
+        N, K = cfg["N"], cfg["K"]
+        blocks = synth.ptq1_0_blocks(N, K, seed=0)
+        xb = np_bits(synth.gemv_inputs(1, K, cfg["C"], act="bf16", seed=0).x)
+        done, t_total, r0 = 0, 0.0, 0
+        rows = 256
+        while t_total < budget_s:
+            r1 = min(N, r0 + rows)
+            t0 = time.perf_counter()
+            pt = oracle.quantize_q8_1_pt(xb)
+            oracle.mmvq_ptq1_0(blocks, pt, rows=(r0, r1))
+            t_total += time.perf_counter() - t0
+            done += r1 - r0
+            r0 = 0 if r1 >= N else r1
+        return {"value": ptq1_bytes(N, K, cfg["C"]) * done / N / t_total / 1e9, "unit": "GB/s", "cores": 1,
+                "kind": "oracle",
+                "sample": "%d rows of the %dx%d C=%d ternary MMVQ, x quantised each time (fp64 C oracle, single "
+                          "thread), %.1f s" % (done, N, K, cfg["C"], t_total)}
     if cfg["kind"] == "quant8":
         K, N = cfg["K"], cfg["N"]
         W = np_bits(synth.quant_inputs(K, N, seed=0))
@@ -745,6 +807,8 @@ def dtype_of(name):
         return "bf16 in, int8 out (fp32 division)"
     if cfg["kind"] == "w4a8":
         return "x quantised to int8 (block_q8_1) / uint4 weights, int32 dp4a dots, fp32 accumulate"
+    if cfg["kind"] == "ptq1":
+        return "x quantised to int8 (block_q8_1) / ternary PTQ1_0 weights, int32 dp4a dots, fp32 accumulate"
     return "bf16 in, int4 out (fp32 arithmetic)"
 
 
@@ -784,7 +848,7 @@ def run_ours(args, world, rank):
         soak(g, stream, 2.0)
         sec2, _, _ = time_graph(work, args.steps, 0, world)
     clocks = cs.summary()
-    if kind in ("gemv", "gemv8", "w4a8"):
+    if kind in ("gemv", "gemv8", "w4a8", "ptq1"):
         e2e_sec, hb, ob = e2e_gemv(w4, work, args.steps, world)
     else:
         e2e_sec, hb, ob = e2e_generic(work, max(2, min(args.steps, 10)), world)
@@ -804,7 +868,7 @@ def run_ours(args, world, rank):
     }
     if kind == "quant8" or (kind == "quant" and not WORKLOADS[args.workload].get("fused", True)):
         line["roofline"]["note"] = "two kernels per step (quantise, then permute); achieved = step bytes / step time"
-    if kind == "w4a8":
+    if kind in ("w4a8", "ptq1"):
         line["roofline"]["note"] = ("two kernels per step (quantise x, then the GEMV); achieved = step bytes / "
                                     "step time")
     if rank == 0 and world == 1:

@@ -17,6 +17,7 @@ in the library's CUDA kernels; there is no CPU or eager fallback.
     gemv_w8(q, scale, x)                -> d [C, N] bf16
     quantize_q8_1_pt(x)                 -> pt [C, 144*K/128] uint8 (block_q8_1 in PT planes)
     gemv_w4a8(qweight, scale, zero, pt) -> d [C, N] bf16 (int4 weights x int8 activations)
+    mmvq_ptq1_0(blocks, pt)             -> d [C, N] fp32 (ternary PTQ1_0 weights x int8 activations)
 """
 import torch
 
@@ -24,7 +25,8 @@ from . import _lib
 from ._lib import W4Error, W4_BF16, W4_F32
 
 __all__ = ["quantize_pack_int4", "permute_int4", "quantize_pack_permute_int4", "gemv_w4", "gemv_w4_permuted", "gemm_w4",
-           "quantize_int8", "permute_int8", "gemv_w8", "quantize_q8_1_pt", "gemv_w4a8", "device_error", "W4Error"]
+           "quantize_int8", "permute_int8", "gemv_w8", "quantize_q8_1_pt", "gemv_w4a8", "mmvq_ptq1_0", "device_error",
+           "W4Error"]
 
 _lib.load()  # fail loudly at import if the CUDA library is missing
 
@@ -271,6 +273,31 @@ def gemv_w4a8(qweight, scale, zero, pt, out=None, stream=None):
     st = _lib.load().gemv_w4a8(qweight.data_ptr(), scale.data_ptr(), zero.data_ptr(), pp.data_ptr(), out.data_ptr(),
                                N, K, C, _stream(stream))
     _lib.check("gemv_w4a8", st)
+    return out
+
+
+def mmvq_ptq1_0(blocks, pt, out=None, stream=None):
+    """d[c, r] = sum_k W[r, k] x[c, k] for ternary W in PTQ1_0 blocks (uint8
+    [N, K/128, 28], or [N, 28*K/128]) and x as quantize_q8_1_pt's output
+    (uint8 [C, 144*K/128], C <= 8).  Returns fp32 [C, N]."""
+    _need(blocks, "blocks", (torch.uint8, torch.int8))
+    _need(pt, "pt", (torch.uint8, torch.int8))
+    N = blocks.shape[0]
+    pp = pt if pt.dim() == 2 else pt.reshape(1, -1)
+    C = pp.shape[0]
+    per_row = blocks.numel() // max(N, 1)
+    if N and (blocks.numel() % N or per_row % 28):
+        raise ValueError("blocks must hold N rows of 28-byte blocks")
+    K = 128 * (per_row // 28) if N else 128 * (pp.shape[1] // 144)
+    if pp.shape[1] != 144 * (K // 128):
+        raise ValueError("pt must hold 144*K/128 bytes per vector")
+    if out is None:
+        out = torch.empty((C, N), dtype=torch.float32, device=pt.device)
+    _need(out, "out", (torch.float32,))
+    if out.numel() != C * N:
+        raise ValueError("out must hold C*N elements")
+    st = _lib.load().mmvq_ptq1_0(blocks.data_ptr(), pp.data_ptr(), out.data_ptr(), N, K, C, _stream(stream))
+    _lib.check("mmvq_ptq1_0", st)
     return out
 
 

@@ -61,6 +61,8 @@ def load():
     lib.quantize_q8_1_pt.restype = I
     lib.gemv_w4a8.argtypes = [P, P, P, P, P, I64, I64, I64, P]
     lib.gemv_w4a8.restype = I
+    lib.mmvq_ptq1_0.argtypes = [P, P, P, I64, I64, I64, P]
+    lib.mmvq_ptq1_0.restype = I
     _lib = lib
     return lib
 

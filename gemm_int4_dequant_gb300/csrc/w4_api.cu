@@ -25,6 +25,9 @@ w4_status run_quantize_q8_1_pt(const void* x, void* pt, int64_t C, int64_t K, cu
 w4_status run_gemv_w4a8(const void* qw, const void* scale, const void* zero, const void* pt, void* d, int64_t N,
                         int64_t K, int64_t C, cudaStream_t s);
 bool w4a8_fits(int64_t C, int64_t K);
+w4_status run_mmvq_ptq1_0(const void* blocks, const void* pt, float* d, int64_t N, int64_t K, int64_t C,
+                          cudaStream_t s);
+bool ptq1_fits(int64_t C, int64_t K);
 int take_device_error_gemm();
 int take_device_error_gemv();
 int take_device_error_quant();
@@ -211,6 +214,16 @@ w4_status gemv_w4a8(const void* qweight, const void* scale, const void* zero, co
     if (!device_is_sm103()) return W4_ERR_DEVICE;
     if (K == 0) return launch_status(cudaMemsetAsync(d, 0, C * N * 2, (cudaStream_t)stream));
     return run_gemv_w4a8(qweight, scale, zero, pt, d, N, K, C, (cudaStream_t)stream);
+}
+
+w4_status mmvq_ptq1_0(const void* blocks, const void* pt, float* d, int64_t N, int64_t K, int64_t C, void* stream) {
+    if (N < 0 || K < 0 || (K % 128) != 0 || C < 1 || C > 8 || !ptq1_fits(C, K)) return W4_ERR_SHAPE;
+    if (N == 0) return W4_OK;
+    if (!d || (K > 0 && (!blocks || !pt))) return W4_ERR_NULL;
+    if (!aligned16(d) || (K > 0 && (!aligned16(blocks) || !aligned16(pt)))) return W4_ERR_ALIGN;
+    if (!device_is_sm103()) return W4_ERR_DEVICE;
+    if (K == 0) return launch_status(cudaMemsetAsync(d, 0, C * N * sizeof(float), (cudaStream_t)stream));
+    return run_mmvq_ptq1_0(blocks, pt, d, N, K, C, (cudaStream_t)stream);
 }
 
 w4_status gemm_w4(const void* A, const void* B, const void* scale, const void* zero, void* C, int64_t M, int64_t N,

@@ -26,6 +26,8 @@
  *                       x quantised to block_q8_1 in the "PT" planes, and
  *                       gemv_w4's int4 weights against it with integer dot
  *                       products ("三值量化模型的无损压缩", sections 3 and 3.1).
+ *   mmvq_ptq1_0         ternary weights in PTQ1_0 blocks against x in that
+ *                       form (same page, sections 2, 3 and 3.2).
  *
  * Conventions shared by every entry point:
  *   - All data pointers are DEVICE pointers owned by the caller.  The library
@@ -317,6 +319,32 @@ w4_status quantize_q8_1_pt(const void* x, void* pt, int64_t C, int64_t K, void* 
  */
 w4_status gemv_w4a8(const void* qweight, const void* scale, const void* zero, const void* pt, void* d, int64_t N,
                     int64_t K, int64_t C, void* stream);
+
+/*
+ * mmvq_ptq1_0 -- the MMVQ product of ternary weights stored as PTQ1_0 blocks
+ * with x in block_q8_1 / PT form (page "三值量化模型的无损压缩", section 2 for
+ * the block, 3 for the product, 3.2 for where each trit sits):
+ *
+ *   d[c][r] = sum_b d_w(r, b) * sum_{j<4} d_x(c, b, j)
+ *                             * sum_{e in q8_1 block j} t(r, 128 b + e) * qs(c, 128 b + e)
+ *
+ * A PTQ1_0 block (28 bytes) holds 128 trits and a half d_w: qs[24] with
+ * five trits a byte (byte = sum_p (t_p + 1) 3^p), weight e < 80 at trit
+ * e >> 4 of byte e & 15, weight 80 + e (e < 40) at trit e >> 3 of byte
+ * 16 + (e & 7); qh[2], a little-endian 16-bit word whose 2-bit field j is
+ * t + 1 of weight 120 + j; then d_w (little-endian half).
+ *
+ * blocks  N * K/128 blocks, row r's blocks back to back, rows back to back;
+ *         16-byte aligned.
+ * pt      quantize_q8_1_pt's output for the C vectors, 16-byte aligned.
+ * d       fp32 [C][N] row-major (output), 16-byte aligned.
+ * Requires K % 128 == 0, 1 <= C <= 8 and x within shared memory
+ * (C * K * 21/16 <= W4_W4A8_MAX_SMEM at C > 4, C * K * 11/8 at C <= 4;
+ * K <= 22016 at C = 8), else W4_ERR_SHAPE; K == 0 gives d = 0.  The integer
+ * dots are exact; fp32 products and sums, within (K/128 + 5) * 2^-24 of
+ * sum_k |w x| (2e-5 is the tested bound).
+ */
+w4_status mmvq_ptq1_0(const void* blocks, const void* pt, float* d, int64_t N, int64_t K, int64_t C, void* stream);
 
 #ifdef __cplusplus
 }
