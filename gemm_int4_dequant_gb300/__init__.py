@@ -18,6 +18,7 @@ in the library's CUDA kernels; there is no CPU or eager fallback.
     quantize_q8_1_pt(x)                 -> pt [C, 144*K/128] uint8 (block_q8_1 in PT planes)
     gemv_w4a8(qweight, scale, zero, pt) -> d [C, N] bf16 (int4 weights x int8 activations)
     mmvq_ptq1_0(blocks, pt)             -> d [C, N] fp32 (ternary PTQ1_0 weights x int8 activations)
+    mmvq_ptq1_1(sblocks, codebook, esc_idx, esc_patt, pt, K) -> d [C, N] fp32 (PTQ1_1 superblocks)
 """
 import torch
 
@@ -25,7 +26,7 @@ from . import _lib
 from ._lib import W4Error, W4_BF16, W4_F32
 
 __all__ = ["quantize_pack_int4", "permute_int4", "quantize_pack_permute_int4", "gemv_w4", "gemv_w4_permuted", "gemm_w4",
-           "quantize_int8", "permute_int8", "gemv_w8", "quantize_q8_1_pt", "gemv_w4a8", "mmvq_ptq1_0", "device_error",
+           "quantize_int8", "permute_int8", "gemv_w8", "quantize_q8_1_pt", "gemv_w4a8", "mmvq_ptq1_0", "mmvq_ptq1_1", "device_error",
            "W4Error"]
 
 _lib.load()  # fail loudly at import if the CUDA library is missing
@@ -298,6 +299,34 @@ def mmvq_ptq1_0(blocks, pt, out=None, stream=None):
         raise ValueError("out must hold C*N elements")
     st = _lib.load().mmvq_ptq1_0(blocks.data_ptr(), pp.data_ptr(), out.data_ptr(), N, K, C, _stream(stream))
     _lib.check("mmvq_ptq1_0", st)
+    return out
+
+
+def mmvq_ptq1_1(sblocks, codebook, esc_idx, esc_patt, pt, K, out=None, stream=None):
+    """mmvq_ptq1_0's product over PTQ1_1 superblocks (uint8 [N, ceil(K/1024),
+    216]) with their codebook (uint8 [n_code, 8]) and escape table (int64
+    [n_esc] ascending superblock indices, uint8 [n_esc, 8]); x as
+    quantize_q8_1_pt's output.  Returns fp32 [C, N]."""
+    for t, name in ((sblocks, "sblocks"), (codebook, "codebook"), (esc_patt, "esc_patt"), (pt, "pt")):
+        _need(t, name, (torch.uint8, torch.int8))
+    _need(esc_idx, "esc_idx", (torch.int64,))
+    N = sblocks.shape[0]
+    pp = pt if pt.dim() == 2 else pt.reshape(1, -1)
+    C = pp.shape[0]
+    if K % 128 or pp.shape[1] != 144 * (K // 128) or sblocks.numel() != N * -(-K // 1024) * 216:
+        raise ValueError("shape mismatch")
+    n_code, n_esc = codebook.numel() // 8, esc_idx.numel()
+    if codebook.numel() % 8 or esc_patt.numel() != 8 * n_esc:
+        raise ValueError("codebook and escape patterns hold 8 exponents each")
+    if out is None:
+        out = torch.empty((C, N), dtype=torch.float32, device=pt.device)
+    _need(out, "out", (torch.float32,))
+    if out.numel() != C * N:
+        raise ValueError("out must hold C*N elements")
+    st = _lib.load().mmvq_ptq1_1(sblocks.data_ptr(), codebook.data_ptr() if n_code else None, n_code,
+                                 esc_idx.data_ptr() if n_esc else None, esc_patt.data_ptr() if n_esc else None, n_esc,
+                                 pp.data_ptr(), out.data_ptr(), N, K, C, _stream(stream))
+    _lib.check("mmvq_ptq1_1", st)
     return out
 
 

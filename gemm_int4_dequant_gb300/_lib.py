@@ -63,6 +63,8 @@ def load():
     lib.gemv_w4a8.restype = I
     lib.mmvq_ptq1_0.argtypes = [P, P, P, I64, I64, I64, P]
     lib.mmvq_ptq1_0.restype = I
+    lib.mmvq_ptq1_1.argtypes = [P, P, I64, P, P, I64, P, P, I64, I64, I64, P]
+    lib.mmvq_ptq1_1.restype = I
     _lib = lib
     return lib
 

@@ -22,6 +22,7 @@
 #include <cuda_fp16.h>
 
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace w4 {
 
@@ -120,19 +121,23 @@ __device__ void stage_x(const uint8_t* __restrict__ pt, uint32_t* xs, float* dx,
     }
 }
 
-// One item: block i of rows row0 .. row0 + R - 1; writes R*C partial sums.
+// Digit p (0..4) of a byte b (0..242) for a p known only at run time:
+// floor(b / 3^p) = (b * ceil(2^15 / 3^p)) >> 15 (exact for b <= 242), then
+// mod 3 by the same rule for 3.
+__device__ __forceinline__ uint32_t digit_of(uint32_t b, uint32_t p) {
+    constexpr uint64_t kRecip = 10923ull | (3641ull << 16) | (1214ull << 32) | (405ull << 48);
+    const uint32_t m = p == 0 ? 32768u : static_cast<uint32_t>(kRecip >> (16 * (p - 1))) & 0xFFFFu;
+    const uint32_t q = (b * m) >> 15;
+    return q - 3u * ((q * 10923u) >> 15);
+}
+
+// One item of R rows of the same block i: qs[r] are the block's six qs
+// words of row r, tail[r] the digits (0..2) of weights 120 .. 127 as two
+// words, dw[r] the block's scale.  Writes the R*C partial sums.
 template <int C, int R>
-__device__ __forceinline__ void ptq1_0_item(const uint8_t* __restrict__ blocks, const uint32_t* xs,
-                                             const float* dx, const int* sq, int64_t N, int64_t bpr, int64_t row0,
-                                             int64_t i, float* out) {
-    uint32_t w[R][7];
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-        const int64_t row = row0 + r;
-        const uint32_t* src = reinterpret_cast<const uint32_t*>(blocks + (row * bpr + i) * PQ_BLOCK_BYTES);
-#pragma unroll
-        for (int q = 0; q < 7; ++q) w[r][q] = row < N ? __ldg(src + q) : 0u;   // a missing row has d = 0
-    }
+__device__ __forceinline__ void mmvq_item(const uint32_t (&qs)[R][6], const uint32_t (&tail)[R][2],
+                                          const float (&dw)[R], const uint32_t* xs, const float* dx, const int* sq,
+                                          int64_t bpr, int64_t i, float* out) {
     int dot[R][C][4];
 #pragma unroll
     for (int r = 0; r < R; ++r)
@@ -146,7 +151,7 @@ __device__ __forceinline__ void ptq1_0_item(const uint8_t* __restrict__ blocks, 
     for (int m = 0; m < 4; ++m) {
         uint32_t u[R][5];
 #pragma unroll
-        for (int r = 0; r < R; ++r) trit_digits(w[r][m], u[r]);
+        for (int r = 0; r < R; ++r) trit_digits(qs[r][m], u[r]);
 #pragma unroll
         for (int c = 0; c < C; ++c) {
             uint32_t xw[5];
@@ -164,7 +169,7 @@ __device__ __forceinline__ void ptq1_0_item(const uint8_t* __restrict__ blocks, 
     for (int m2 = 0; m2 < 2; ++m2) {
         uint32_t u[R][5];
 #pragma unroll
-        for (int r = 0; r < R; ++r) trit_digits(w[r][4 + m2], u[r]);
+        for (int r = 0; r < R; ++r) trit_digits(qs[r][4 + m2], u[r]);
 #pragma unroll
         for (int c = 0; c < C; ++c) {
             uint32_t xw[5];
@@ -176,14 +181,14 @@ __device__ __forceinline__ void ptq1_0_item(const uint8_t* __restrict__ blocks, 
                 for (int p = 0; p < 5; ++p) dot[r][c][p < 2 ? 2 : 3] = dp4(u[r][p], xw[p], dot[r][c][p < 2 ? 2 : 3]);
         }
     }
-    // tail: qh's eight 2-bit digits are elements 120 .. 127 = plane 7, words 2 and 3
+    // tail: weights 120 .. 127 are plane 7, words 2 and 3
 #pragma unroll
     for (int c = 0; c < C; ++c) {
         const uint32_t x2 = xs[((c * 8 + 7) * 4 + 2) * bpr + i], x3 = xs[((c * 8 + 7) * 4 + 3) * bpr + i];
 #pragma unroll
         for (int r = 0; r < R; ++r) {
-            dot[r][c][3] = dp4(spread2(w[r][6] & 0xFFu), x2, dot[r][c][3]);
-            dot[r][c][3] = dp4(spread2((w[r][6] >> 8) & 0xFFu), x3, dot[r][c][3]);
+            dot[r][c][3] = dp4(tail[r][0], x2, dot[r][c][3]);
+            dot[r][c][3] = dp4(tail[r][1], x3, dot[r][c][3]);
         }
     }
 #pragma unroll
@@ -197,23 +202,119 @@ __device__ __forceinline__ void ptq1_0_item(const uint8_t* __restrict__ blocks, 
         }
 #pragma unroll
         for (int r = 0; r < R; ++r) {
-            const float dw = __half2float(__ushort_as_half(static_cast<unsigned short>(w[r][6] >> 16)));
             float a = 0.f;
 #pragma unroll
             for (int j = 0; j < 4; ++j) a = fmaf(dxj[j], static_cast<float>(dot[r][c][j] - sqj[j]), a);
-            out[r * C + c] = dw * a;
+            out[r * C + c] = dw[r] * a;
         }
     }
+}
+
+// PTQ1_0: the block's seven words are qs (0..5), then qh | d << 16.
+template <int C, int R>
+__device__ __forceinline__ void ptq1_0_item(const uint8_t* __restrict__ blocks, const uint32_t* xs,
+                                             const float* dx, const int* sq, int64_t N, int64_t bpr, int64_t row0,
+                                             int64_t i, float* out) {
+    uint32_t qs[R][6], tail[R][2];
+    float dw[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const int64_t row = row0 + r;
+        const uint32_t* src = reinterpret_cast<const uint32_t*>(blocks + (row * bpr + i) * PQ_BLOCK_BYTES);
+#pragma unroll
+        for (int q = 0; q < 6; ++q) qs[r][q] = row < N ? __ldg(src + q) : 0u;
+        const uint32_t w6 = row < N ? __ldg(src + 6) : 0u;   // a missing row has d = 0
+        tail[r][0] = spread2(w6 & 0xFFu);
+        tail[r][1] = spread2((w6 >> 8) & 0xFFu);
+        dw[r] = __half2float(__ushort_as_half(static_cast<unsigned short>(w6 >> 16)));
+    }
+    mmvq_item<C, R>(qs, tail, dw, xs, dx, sq, bpr, i, out);
+}
+
+// PTQ1_1 superblock (216 bytes): qs[192] (block s at 24 s), qh[13] at 192,
+// eight 10-bit mantissas at 205, the exponents byte at 215.  Block s's tail
+// trit j is digit (8 s + j) mod 5 of qh byte (8 s + j) / 5; digit 4 of qh
+// byte 12 is the free trit f; the pattern index exponents + 256 f names a
+// codebook entry (< 767) or, at 767, the escape table entry of the
+// superblock's index.  A pattern that cannot be found records ERR_PATTERN
+// and gives d = 0.
+constexpr int ERR_PATTERN = 2;
+constexpr int PTQ1_1_BYTES = 216;
+
+__device__ __forceinline__ const uint8_t* find_escape(const int64_t* __restrict__ esc_idx,
+                                                      const uint8_t* __restrict__ esc_patt, int64_t n_esc,
+                                                      int64_t g) {
+    int64_t lo = 0, hi = n_esc;   // esc_idx ascending
+    while (lo < hi) {
+        const int64_t mid = (lo + hi) / 2;
+        if (esc_idx[mid] < g) lo = mid + 1;
+        else hi = mid;
+    }
+    return (lo < n_esc && esc_idx[lo] == g) ? esc_patt + 8 * lo : nullptr;
+}
+
+template <int C, int R>
+__device__ __forceinline__ void ptq1_1_item(const uint8_t* __restrict__ sblocks, const uint8_t* code,
+                                             int64_t n_code, const int64_t* __restrict__ esc_idx,
+                                             const uint8_t* __restrict__ esc_patt, int64_t n_esc,
+                                             const uint32_t* xs, const float* dx, const int* sq, int64_t N,
+                                             int64_t bpr, int64_t row0, int64_t i, float* out) {
+    const int64_t sbpr = (bpr + 7) / 8, sb = i / 8;
+    const uint32_t s = static_cast<uint32_t>(i % 8);
+    uint32_t qs[R][6], tail[R][2];
+    float dw[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const int64_t row = row0 + r;
+        const int64_t g = row * sbpr + sb;
+        const uint32_t* base = reinterpret_cast<const uint32_t*>(sblocks + g * PTQ1_1_BYTES);
+        uint32_t h[6];
+#pragma unroll
+        for (int q = 0; q < 6; ++q) qs[r][q] = row < N ? __ldg(base + 6 * s + q) : 0u;
+#pragma unroll
+        for (int q = 0; q < 6; ++q) h[q] = row < N ? __ldg(base + 48 + q) : 0u;   // bytes 192 .. 215
+        // tail digits: trit u = 8 s + j is digit u % 5 of qh byte u / 5
+        uint32_t t0 = 0, t1 = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const uint32_t u = 8 * s + j, n = (u * 205u) >> 10, p = u - 5 * n;
+            const uint32_t hw = n < 4 ? h[0] : n < 8 ? h[1] : n < 12 ? h[2] : h[3];
+            const uint32_t dg = digit_of((hw >> (8 * (n & 3))) & 0xFFu, p);
+            if (j < 4) t0 |= dg << (8 * j);
+            else t1 |= dg << (8 * (j - 4));
+        }
+        tail[r][0] = t0;
+        tail[r][1] = t1;
+        // mantissa s: bits 10 s .. 10 s + 9 of bytes 205 .. 214
+        const uint64_t lo64 = uint64_t(h[3] >> 8) | (uint64_t(h[4]) << 24) | (uint64_t(h[5] & 0xFFu) << 56);
+        const uint64_t hi16 = (h[5] >> 8) & 0xFFFFu;
+        const uint32_t o = 10 * s;
+        const uint64_t v = o < 64 ? ((lo64 >> o) | (o > 54 ? (hi16 << (64 - o)) : 0ull)) : (hi16 >> (o - 64));
+        const uint32_t mant = static_cast<uint32_t>(v) & 0x3FFu;
+        // exponent from the pattern
+        const uint32_t idx = (h[5] >> 24) + 256u * digit_of(h[3] & 0xFFu, 4);
+        const uint8_t* pat = nullptr;
+        if (row < N) {
+            if (idx < 767u) pat = int64_t(idx) < n_code ? code + 8 * idx : nullptr;
+            else pat = find_escape(esc_idx, esc_patt, n_esc, g);
+            if (!pat) atomicCAS(&g_device_error, 0, ERR_PATTERN);
+        }
+        const uint32_t e = pat ? pat[s] : 0u;
+        dw[r] = pat ? __half2float(__ushort_as_half(static_cast<unsigned short>((e << 10) | mant))) : 0.f;
+    }
+    mmvq_item<C, R>(qs, tail, dw, xs, dx, sq, bpr, i, out);
 }
 
 // CTA b takes the row groups [b G, b G + G) (R rows each): its items are
 // (row group, block) pairs, spread over the threads; the R*C partial sums
 // of each item go to shared memory and are added over the blocks of a row
-// in block order.  d is fp32 [C][N].
-template <int C, int R>
+// in block order.  d is fp32 [C][N].  PTQ1_1 also copies the codebook into
+// shared memory.
+template <int C, int R, bool SUPER>
 __global__ void __launch_bounds__(PQ_THREADS)
-mmvq_ptq1_0_kernel(const uint8_t* __restrict__ blocks, const uint8_t* __restrict__ pt, float* __restrict__ d,
-                   int64_t N, int64_t K, int64_t G) {
+mmvq_ptq1_kernel(const uint8_t* __restrict__ w, const uint8_t* __restrict__ codebook, int64_t n_code,
+                 const int64_t* __restrict__ esc_idx, const uint8_t* __restrict__ esc_patt, int64_t n_esc,
+                 const uint8_t* __restrict__ pt, float* __restrict__ d, int64_t N, int64_t K, int64_t G) {
     extern __shared__ __align__(16) uint8_t smem[];
     const int64_t bpr = K / 128, items = G * bpr;
     const PqLayout L = pq_layout(C, K, items, R);
@@ -221,12 +322,19 @@ mmvq_ptq1_0_kernel(const uint8_t* __restrict__ blocks, const uint8_t* __restrict
     float* dx = reinterpret_cast<float*>(smem + L.dx);
     int* sq = reinterpret_cast<int*>(smem + L.sq);
     float* part = reinterpret_cast<float*>(smem + L.part);
+    uint8_t* code = smem + L.total;
+    if (SUPER)
+        for (int64_t t = threadIdx.x; t < 8 * n_code; t += PQ_THREADS) code[t] = codebook[t];
     stage_x<C>(pt, xs, dx, sq, bpr);
     __syncthreads();
     const int64_t rg0 = int64_t(blockIdx.x) * G;
     for (int64_t t = threadIdx.x; t < items; t += PQ_THREADS) {
         const int64_t g = t / bpr, i = t % bpr;
-        ptq1_0_item<C, R>(blocks, xs, dx, sq, N, bpr, (rg0 + g) * R, i, part + t * R * C);
+        if (SUPER)
+            ptq1_1_item<C, R>(w, code, n_code, esc_idx, esc_patt, n_esc, xs, dx, sq, N, bpr, (rg0 + g) * R, i,
+                              part + t * R * C);
+        else
+            ptq1_0_item<C, R>(w, xs, dx, sq, N, bpr, (rg0 + g) * R, i, part + t * R * C);
     }
     __syncthreads();
     for (int64_t o = threadIdx.x; o < G * R * C; o += PQ_THREADS) {
@@ -239,49 +347,67 @@ mmvq_ptq1_0_kernel(const uint8_t* __restrict__ blocks, const uint8_t* __restrict
     }
 }
 
-template <int C>
-w4_status launch_ptq1_0(const void* blocks, const void* pt, float* d, int64_t N, int64_t K, cudaStream_t stream) {
+constexpr size_t kCodebookBytes = 767 * 8;
+
+template <int C, bool SUPER>
+w4_status launch_ptq1(const void* w, const void* codebook, int64_t n_code, const void* esc_idx,
+                      const void* esc_patt, int64_t n_esc, const void* pt, float* d, int64_t N, int64_t K,
+                      cudaStream_t stream) {
     constexpr int R = C <= 4 ? 4 : 2;
     static int smem_set[64];
     const int64_t bpr = K / 128, groups = (N + R - 1) / R;
+    const size_t extra = SUPER ? kCodebookBytes : 0;
     const int sms = sm_count();
     if (sms <= 0) return W4_ERR_CUDA;
     // about two CTAs per SM, at most 1024 items per CTA, within shared memory
     int64_t G = (groups + 2 * sms - 1) / (2 * sms);
     G = G < 1 ? 1 : G;
     if (G * bpr > 1024) G = 1024 / bpr > 0 ? 1024 / bpr : 1;
-    while (G > 1 && pq_layout(C, K, G * bpr, R).total > size_t(W4_W4A8_MAX_SMEM)) --G;
-    const size_t smem = pq_layout(C, K, G * bpr, R).total;
+    while (G > 1 && pq_layout(C, K, G * bpr, R).total + extra > size_t(W4_W4A8_MAX_SMEM)) --G;
+    const size_t smem = pq_layout(C, K, G * bpr, R).total + extra;
     if (smem > size_t(W4_W4A8_MAX_SMEM)) return W4_ERR_SHAPE;
-    auto kern = mmvq_ptq1_0_kernel<C, R>;
+    auto kern = mmvq_ptq1_kernel<C, R, SUPER>;
     if (ensure_smem_limit(kern, static_cast<int>(smem), smem_set) != cudaSuccess) return W4_ERR_CUDA;
     const int64_t ctas = (groups + G - 1) / G;
     if (ctas > 0x7FFFFFFF) return W4_ERR_SHAPE;
-    kern<<<static_cast<unsigned>(ctas), PQ_THREADS, smem, stream>>>(static_cast<const uint8_t*>(blocks),
-                                                                     static_cast<const uint8_t*>(pt), d, N, K, G);
+    kern<<<static_cast<unsigned>(ctas), PQ_THREADS, smem, stream>>>(
+        static_cast<const uint8_t*>(w), static_cast<const uint8_t*>(codebook), n_code,
+        static_cast<const int64_t*>(esc_idx), static_cast<const uint8_t*>(esc_patt), n_esc,
+        static_cast<const uint8_t*>(pt), d, N, K, G);
     return launch_status(cudaGetLastError());
+}
+
+template <bool SUPER>
+w4_status run_ptq1(const void* w, const void* codebook, int64_t n_code, const void* esc_idx, const void* esc_patt,
+                   int64_t n_esc, const void* pt, float* d, int64_t N, int64_t K, int64_t C, cudaStream_t stream) {
+    switch (C) {
+#define W4_PTQ1_CASE(CC) \
+    case CC: return launch_ptq1<CC, SUPER>(w, codebook, n_code, esc_idx, esc_patt, n_esc, pt, d, N, K, stream);
+        W4_PTQ1_CASE(1) W4_PTQ1_CASE(2) W4_PTQ1_CASE(3) W4_PTQ1_CASE(4)
+        W4_PTQ1_CASE(5) W4_PTQ1_CASE(6) W4_PTQ1_CASE(7) W4_PTQ1_CASE(8)
+#undef W4_PTQ1_CASE
+        default: return W4_ERR_SHAPE;
+    }
 }
 
 }  // namespace
 
-bool ptq1_fits(int64_t C, int64_t K) {
+bool ptq1_fits(int64_t C, int64_t K, bool super) {
     const int R = C <= 4 ? 4 : 2;
-    return pq_layout(C, K, K / 128, R).total <= size_t(W4_W4A8_MAX_SMEM);
+    return pq_layout(C, K, K / 128, R).total + (super ? kCodebookBytes : 0) <= size_t(W4_W4A8_MAX_SMEM);
 }
 
 w4_status run_mmvq_ptq1_0(const void* blocks, const void* pt, float* d, int64_t N, int64_t K, int64_t C,
                           cudaStream_t stream) {
-    switch (C) {
-        case 1: return launch_ptq1_0<1>(blocks, pt, d, N, K, stream);
-        case 2: return launch_ptq1_0<2>(blocks, pt, d, N, K, stream);
-        case 3: return launch_ptq1_0<3>(blocks, pt, d, N, K, stream);
-        case 4: return launch_ptq1_0<4>(blocks, pt, d, N, K, stream);
-        case 5: return launch_ptq1_0<5>(blocks, pt, d, N, K, stream);
-        case 6: return launch_ptq1_0<6>(blocks, pt, d, N, K, stream);
-        case 7: return launch_ptq1_0<7>(blocks, pt, d, N, K, stream);
-        case 8: return launch_ptq1_0<8>(blocks, pt, d, N, K, stream);
-        default: return W4_ERR_SHAPE;
-    }
+    return run_ptq1<false>(blocks, nullptr, 0, nullptr, nullptr, 0, pt, d, N, K, C, stream);
 }
+
+w4_status run_mmvq_ptq1_1(const void* sblocks, const void* codebook, int64_t n_code, const void* esc_idx,
+                          const void* esc_patt, int64_t n_esc, const void* pt, float* d, int64_t N, int64_t K,
+                          int64_t C, cudaStream_t stream) {
+    return run_ptq1<true>(sblocks, codebook, n_code, esc_idx, esc_patt, n_esc, pt, d, N, K, C, stream);
+}
+
+int take_device_error_ptq1() { return take_unit_device_error(); }
 
 }  // namespace w4

@@ -27,7 +27,11 @@ w4_status run_gemv_w4a8(const void* qw, const void* scale, const void* zero, con
 bool w4a8_fits(int64_t C, int64_t K);
 w4_status run_mmvq_ptq1_0(const void* blocks, const void* pt, float* d, int64_t N, int64_t K, int64_t C,
                           cudaStream_t s);
-bool ptq1_fits(int64_t C, int64_t K);
+w4_status run_mmvq_ptq1_1(const void* sblocks, const void* codebook, int64_t n_code, const void* esc_idx,
+                          const void* esc_patt, int64_t n_esc, const void* pt, float* d, int64_t N, int64_t K,
+                          int64_t C, cudaStream_t s);
+bool ptq1_fits(int64_t C, int64_t K, bool super);
+int take_device_error_ptq1();
 int take_device_error_gemm();
 int take_device_error_gemv();
 int take_device_error_quant();
@@ -89,8 +93,9 @@ int w4_device_error(void* stream) {
     const int a = take_device_error_gemm();
     const int b = take_device_error_gemv();
     const int c = take_device_error_quant();
-    if (a < 0 || b < 0 || c < 0) return -1;
-    return a != 0 ? a : b != 0 ? b : c;
+    const int e = take_device_error_ptq1();
+    if (a < 0 || b < 0 || c < 0 || e < 0) return -1;
+    return a != 0 ? a : b != 0 ? b : c != 0 ? c : e;
 }
 
 const char* w4_status_string(w4_status status) {
@@ -217,13 +222,30 @@ w4_status gemv_w4a8(const void* qweight, const void* scale, const void* zero, co
 }
 
 w4_status mmvq_ptq1_0(const void* blocks, const void* pt, float* d, int64_t N, int64_t K, int64_t C, void* stream) {
-    if (N < 0 || K < 0 || (K % 128) != 0 || C < 1 || C > 8 || !ptq1_fits(C, K)) return W4_ERR_SHAPE;
+    if (N < 0 || K < 0 || (K % 128) != 0 || C < 1 || C > 8 || !ptq1_fits(C, K, false)) return W4_ERR_SHAPE;
     if (N == 0) return W4_OK;
     if (!d || (K > 0 && (!blocks || !pt))) return W4_ERR_NULL;
     if (!aligned16(d) || (K > 0 && (!aligned16(blocks) || !aligned16(pt)))) return W4_ERR_ALIGN;
     if (!device_is_sm103()) return W4_ERR_DEVICE;
     if (K == 0) return launch_status(cudaMemsetAsync(d, 0, C * N * sizeof(float), (cudaStream_t)stream));
     return run_mmvq_ptq1_0(blocks, pt, d, N, K, C, (cudaStream_t)stream);
+}
+
+w4_status mmvq_ptq1_1(const void* sblocks, const void* codebook, int64_t n_code, const void* esc_idx,
+                      const void* esc_patt, int64_t n_esc, const void* pt, float* d, int64_t N, int64_t K, int64_t C,
+                      void* stream) {
+    if (N < 0 || K < 0 || (K % 128) != 0 || C < 1 || C > 8 || n_code < 0 || n_code > 767 || n_esc < 0 ||
+        !ptq1_fits(C, K, true))
+        return W4_ERR_SHAPE;
+    if (N == 0) return W4_OK;
+    if (!d || (K > 0 && (!sblocks || !pt)) || (n_code > 0 && !codebook) || (n_esc > 0 && (!esc_idx || !esc_patt)))
+        return W4_ERR_NULL;
+    if (!aligned16(d) || (K > 0 && (!aligned16(sblocks) || !aligned16(pt))) || (n_code > 0 && !aligned16(codebook)) ||
+        (n_esc > 0 && (!aligned16(esc_idx) || !aligned16(esc_patt))))
+        return W4_ERR_ALIGN;
+    if (!device_is_sm103()) return W4_ERR_DEVICE;
+    if (K == 0) return launch_status(cudaMemsetAsync(d, 0, C * N * sizeof(float), (cudaStream_t)stream));
+    return run_mmvq_ptq1_1(sblocks, codebook, n_code, esc_idx, esc_patt, n_esc, pt, d, N, K, C, (cudaStream_t)stream);
 }
 
 w4_status gemm_w4(const void* A, const void* B, const void* scale, const void* zero, void* C, int64_t M, int64_t N,

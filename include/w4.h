@@ -26,8 +26,10 @@
  *                       x quantised to block_q8_1 in the "PT" planes, and
  *                       gemv_w4's int4 weights against it with integer dot
  *                       products ("三值量化模型的无损压缩", sections 3 and 3.1).
- *   mmvq_ptq1_0         ternary weights in PTQ1_0 blocks against x in that
- *                       form (same page, sections 2, 3 and 3.2).
+ *   mmvq_ptq1_0, mmvq_ptq1_1
+ *                       ternary weights in PTQ1_0 blocks, or in the PTQ1_1
+ *                       superblocks that pack eight of them, against x in
+ *                       that form (same page, sections 2, 3 and 3.2).
  *
  * Conventions shared by every entry point:
  *   - All data pointers are DEVICE pointers owned by the caller.  The library
@@ -83,8 +85,10 @@ const char* w4_status_string(w4_status status);
  * iteration/time limit (about two seconds) records a nonzero code here,
  * drains the work it already issued, frees its tensor memory and returns.
  * This call synchronises `stream`, then returns and clears the first code
- * recorded on the current device (0 = none, 1 = a pipeline wait timed out),
- * or -1 if the synchronisation or the read failed.
+ * recorded on the current device (0 = none, 1 = a pipeline wait timed out,
+ * 2 = a PTQ1_1 superblock's pattern index named no codebook entry or escape;
+ * its blocks then count as d = 0), or -1 if the synchronisation or the read
+ * failed.
  */
 int w4_device_error(void* stream);
 
@@ -345,6 +349,36 @@ w4_status gemv_w4a8(const void* qweight, const void* scale, const void* zero, co
  * sum_k |w x| (2e-5 is the tested bound).
  */
 w4_status mmvq_ptq1_0(const void* blocks, const void* pt, float* d, int64_t N, int64_t K, int64_t C, void* stream);
+
+/*
+ * mmvq_ptq1_1 -- mmvq_ptq1_0's product over the same weights packed as
+ * PTQ1_1 superblocks (same page, section 2): eight consecutive blocks of a
+ * row in 216 bytes,
+ *   qs[192]        the eight blocks' qs bytes, block s at 24 s;
+ *   qh[13]         the 64 tail trits, tail trit j of block s as base-3 digit
+ *                  (8 s + j) mod 5 of byte (8 s + j) / 5; digit 4 of byte 12
+ *                  is the free trit f;
+ *   mantissa[8]    ten bits each, block s at bits 10 s .. 10 s + 9 of the
+ *                  little-endian 80-bit string;
+ *   exponents      one byte; the pattern index exponents + 256 f < 767 names
+ *                  codebook entry [index], 767 the escape table entry of this
+ *                  superblock (index r * ceil(K/1024) + sb).
+ * Block s's d is the positive half with the pattern's exponent s and
+ * mantissa s.  A row of K/128 blocks takes ceil(K/1024) superblocks; the
+ * blocks past K (zero trits, d = 0) are not read.
+ *
+ * sblocks   N * ceil(K/1024) superblocks, row after row, 16-byte aligned.
+ * codebook  uint8 [n_code][8] exponents (0 <= n_code <= 767).
+ * esc_idx   int64 [n_esc] superblock indices, ascending; esc_patt uint8
+ *           [n_esc][8] their exponents.
+ * pt, d, C, K: as mmvq_ptq1_0 (the codebook takes 6136 bytes more shared
+ * memory).  All pointers 16-byte aligned; codebook / esc_* may be NULL when
+ * n_code / n_esc is 0.  An index that names no entry records device error 2
+ * (w4_device_error) and its blocks count as d = 0.
+ */
+w4_status mmvq_ptq1_1(const void* sblocks, const void* codebook, int64_t n_code, const void* esc_idx,
+                      const void* esc_patt, int64_t n_esc, const void* pt, float* d, int64_t N, int64_t K, int64_t C,
+                      void* stream);
 
 #ifdef __cplusplus
 }
