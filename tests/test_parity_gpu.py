@@ -403,8 +403,12 @@ def test_permute_int8_bit_exact(w4, K, N):
     assert _guards_intact(buf, pad, N * K, 0x5A)
 
 
-@pytest.mark.parametrize("N,K,C", [(1, 1, 1), (37, 100, 3), (300, 4096, 8), (1000, 5120, 1), (17280, 5120, 1),
-                                   (5120, 17280, 4)])
+@pytest.mark.parametrize("N,K,C", [
+    (1, 1, 1), (37, 100, 3), (300, 4096, 8), (1000, 5120, 1),     # N % 16 != 0: the plain kernel
+    (17280, 5120, 1), (5120, 17280, 4), (5120, 17280, 8),          # N % 16 == 0: 128-column strips, K split
+    (6144, 5120, 2), (16, 7, 3),                                   # a cluster rank with no rows of K
+    (272, 100, 5), (48, 8192, 6),                                  # a partial strip; eight columns a thread
+])
 def test_gemv_w8(w4, N, K, C):
     gi = synth.int8_gemv_inputs(N, K, C, seed=N + K + C)
     buf, out, pad = _guarded(C * N, torch.bfloat16, -7.0)
