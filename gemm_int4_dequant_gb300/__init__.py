@@ -19,6 +19,7 @@ in the library's CUDA kernels; there is no CPU or eager fallback.
     gemv_w4a8(qweight, scale, zero, pt) -> d [C, N] bf16 (int4 weights x int8 activations)
     mmvq_ptq1_0(blocks, pt)             -> d [C, N] fp32 (ternary PTQ1_0 weights x int8 activations)
     mmvq_ptq1_1(sblocks, codebook, esc_idx, esc_patt, pt, K) -> d [C, N] fp32 (PTQ1_1 superblocks)
+    ptq1_1_encode(blocks)               -> (sblocks, codebook, esc_idx, esc_patt): PTQ1_0 -> PTQ1_1 (host)
 """
 import torch
 
@@ -26,8 +27,8 @@ from . import _lib
 from ._lib import W4Error, W4_BF16, W4_F32
 
 __all__ = ["quantize_pack_int4", "permute_int4", "quantize_pack_permute_int4", "gemv_w4", "gemv_w4_permuted", "gemm_w4",
-           "quantize_int8", "permute_int8", "gemv_w8", "quantize_q8_1_pt", "gemv_w4a8", "mmvq_ptq1_0", "mmvq_ptq1_1", "device_error",
-           "W4Error"]
+           "quantize_int8", "permute_int8", "gemv_w8", "quantize_q8_1_pt", "gemv_w4a8", "mmvq_ptq1_0", "mmvq_ptq1_1",
+           "ptq1_1_encode", "device_error", "W4Error"]
 
 _lib.load()  # fail loudly at import if the CUDA library is missing
 
@@ -328,6 +329,37 @@ def mmvq_ptq1_1(sblocks, codebook, esc_idx, esc_patt, pt, K, out=None, stream=No
                                  pp.data_ptr(), out.data_ptr(), N, K, C, _stream(stream))
     _lib.check("mmvq_ptq1_1", st)
     return out
+
+
+def ptq1_1_encode(blocks):
+    """Convert ternary PTQ1_0 blocks (host uint8 [N, K/128, 28], numpy or a
+    CPU tensor) into PTQ1_1 superblocks with the tensor's own codebook.
+    Runs on the host.  Returns numpy (sblocks uint8 [N, ceil(K/1024), 216],
+    codebook uint8 [n_code, 8], esc_idx int64 [n_esc], esc_patt uint8
+    [n_esc, 8])."""
+    import ctypes
+    import numpy as np
+    b = blocks.numpy() if isinstance(blocks, torch.Tensor) else blocks
+    b = np.ascontiguousarray(b, dtype=np.uint8)
+    if b.ndim != 3 or b.shape[2] != 28:
+        raise ValueError("blocks must be [N, K/128, 28] bytes")
+    N, bpr = b.shape[:2]
+    K = 128 * bpr
+    sbpr = -(-bpr // 8)
+    lib = _lib.load()
+    ptr = lambda a: a.ctypes.data_as(ctypes.c_void_p)
+    code = np.zeros((767, 8), np.uint8)
+    n_code = ctypes.c_int64(0)
+    _lib.check("ptq1_1_codebook", lib.ptq1_1_codebook(ptr(b), N, K, ptr(code), ctypes.byref(n_code)))
+    sblocks = np.zeros((N, sbpr, 216), np.uint8)
+    cap = max(1, N * sbpr)
+    esc_idx = np.zeros(cap, np.int64)
+    esc_patt = np.zeros((cap, 8), np.uint8)
+    n_esc = ctypes.c_int64(0)
+    _lib.check("ptq1_1_encode", lib.ptq1_1_encode(ptr(b), N, K, ptr(code), n_code.value, ptr(sblocks), ptr(esc_idx),
+                                                  ptr(esc_patt), cap, ctypes.byref(n_esc)))
+    n = n_esc.value
+    return sblocks, code[:n_code.value].copy(), esc_idx[:n].copy(), esc_patt[:n].copy()
 
 
 def device_error(stream=None):

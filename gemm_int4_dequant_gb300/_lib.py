@@ -11,6 +11,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libw4.so")
 
 W4_OK, W4_ERR_NULL, W4_ERR_SHAPE, W4_ERR_ALIGN, W4_ERR_DTYPE, W4_ERR_CUDA, W4_ERR_DEVICE = 0, -1, -2, -3, -4, -5, -6
+W4_ERR_VALUE = -7
 W4_F32, W4_BF16 = 0, 1
 
 _lib = None
@@ -65,6 +66,10 @@ def load():
     lib.mmvq_ptq1_0.restype = I
     lib.mmvq_ptq1_1.argtypes = [P, P, I64, P, P, I64, P, P, I64, I64, I64, P]
     lib.mmvq_ptq1_1.restype = I
+    lib.ptq1_1_codebook.argtypes = [P, I64, I64, P, P]
+    lib.ptq1_1_codebook.restype = I
+    lib.ptq1_1_encode.argtypes = [P, I64, I64, P, I64, P, P, P, I64, P]
+    lib.ptq1_1_encode.restype = I
     _lib = lib
     return lib
 

@@ -107,6 +107,7 @@ const char* w4_status_string(w4_status status) {
         case W4_ERR_DTYPE: return "unsupported dtype";
         case W4_ERR_CUDA: return "CUDA launch error";
         case W4_ERR_DEVICE: return "current device is not an sm_103 (GB300) GPU";
+        case W4_ERR_VALUE: return "input value outside the format's range";
     }
     return "unknown status";
 }

@@ -30,6 +30,9 @@
  *                       ternary weights in PTQ1_0 blocks, or in the PTQ1_1
  *                       superblocks that pack eight of them, against x in
  *                       that form (same page, sections 2, 3 and 3.2).
+ *   ptq1_1_codebook, ptq1_1_encode
+ *                       host-side conversion of ternary PTQ1_0 blocks into
+ *                       PTQ1_1 superblocks ("三值量化模型的无损压缩", section 2).
  *
  * Conventions shared by every entry point:
  *   - All data pointers are DEVICE pointers owned by the caller.  The library
@@ -42,8 +45,9 @@
  *     that is not 16-byte aligned W4_ERR_ALIGN, an unknown dtype W4_ERR_DTYPE;
  *     in all those cases nothing is launched and no output is touched.  A
  *     CUDA error while launching gives W4_ERR_CUDA (the CUDA error itself is
- *     left for cudaGetLastError of the caller's runtime to report) and
- *     W4_ERR_DEVICE means the current device is not an sm_103 GPU.
+ *     left for cudaGetLastError of the caller's runtime to report),
+ *     W4_ERR_DEVICE means the current device is not an sm_103 GPU, and
+ *     W4_ERR_VALUE an input value the format cannot hold (host conversions).
  *   - Sizes are int64_t; every size must be >= 0.  Outputs are fully
  *     overwritten (their prior contents never matter).  Inputs and outputs
  *     must not overlap.
@@ -65,7 +69,8 @@ typedef enum {
     W4_ERR_ALIGN = -3,
     W4_ERR_DTYPE = -4,
     W4_ERR_CUDA = -5,
-    W4_ERR_DEVICE = -6
+    W4_ERR_DEVICE = -6,
+    W4_ERR_VALUE = -7
 } w4_status;
 
 /* Largest K that gemv_w4 accepts. */
@@ -379,6 +384,46 @@ w4_status mmvq_ptq1_0(const void* blocks, const void* pt, float* d, int64_t N, i
 w4_status mmvq_ptq1_1(const void* sblocks, const void* codebook, int64_t n_code, const void* esc_idx,
                       const void* esc_patt, int64_t n_esc, const void* pt, float* d, int64_t N, int64_t K, int64_t C,
                       void* stream);
+/*
+ * PTQ1_1 conversion (page "三值量化模型的无损压缩", section 2 "权重的无损压缩").
+ * HOST functions: every pointer is host memory; nothing touches a GPU.
+ *
+ * A PTQ1_0 block (28 bytes) holds 128 trits: qs[24] five trits a byte
+ * (byte = sum_p (t_p + 1) 3^p; weight e < 80 at trit e >> 4 of byte e & 15,
+ * weight 80 + e at trit e >> 3 of byte 16 + (e & 7)), qh[2] a little-endian
+ * word whose 2-bit field j is t + 1 of weight 120 + j, and the half d.
+ * A PTQ1_1 superblock (216 bytes) holds eight consecutive blocks of a row:
+ * qs[192] (block s at 24 s), qh[13] (tail trit j of block s as base-3
+ * digit (8 s + j) mod 5 of byte (8 s + j) / 5; digit 4 of byte 12 is the
+ * free trit f), eight 10-bit mantissas (block s at bits 10 s .. 10 s + 9 of
+ * the little-endian 80-bit string at byte 205) and one exponents byte: the
+ * pattern index exponents + 256 f names codebook entry [index] (< 767) or,
+ * at 767, the escape-table entry of the superblock.  A row of K/128 blocks
+ * takes ceil(K/1024) superblocks, the missing blocks of the last one being
+ * zero trits with d = +0; superblock (r, sb) has index r * ceil(K/1024) + sb.
+ *
+ * ptq1_1_codebook -- the tensor's exponent patterns (eight 5-bit exponents of
+ * a superblock's blocks) by descending count, ties in ascending order of the
+ * pattern read as a 40-bit number with block 0's exponent most significant;
+ * the first min(767, distinct) go to codebook (uint8 [767][8]) and their
+ * number to *n_code.
+ * blocks  N * K/128 PTQ1_0 blocks, row after row.  K % 128 == 0, else
+ * W4_ERR_SHAPE.
+ */
+w4_status ptq1_1_codebook(const void* blocks, int64_t N, int64_t K, void* codebook, int64_t* n_code);
+
+/*
+ * ptq1_1_encode -- PTQ1_0 blocks -> PTQ1_1 superblocks (N * ceil(K/1024) *
+ * 216 bytes) with the given codebook (uint8 [n_code][8], 0 <= n_code <=
+ * 767; a repeated pattern resolves to its first entry).  A superblock whose
+ * pattern is not in the codebook gets index 767 and an escape entry:
+ * esc_idx (int64, ascending superblock indices) and esc_patt (uint8
+ * [.][8]), at most max_esc of them (more: W4_ERR_SHAPE); *n_esc receives
+ * their number.  W4_ERR_VALUE if a block has a negative d (PTQ1_1 keeps no
+ * sign), a qs byte above 242 or a qh field of 3.
+ */
+w4_status ptq1_1_encode(const void* blocks, int64_t N, int64_t K, const void* codebook, int64_t n_code,
+                        void* sblocks, void* esc_idx, void* esc_patt, int64_t max_esc, int64_t* n_esc);
 
 #ifdef __cplusplus
 }

@@ -27,7 +27,8 @@ def _declared_functions():
 def test_header_declares_the_hot_path():
     names = _declared_functions()
     for fn in ("quantize_pack_int4", "permute_int4", "quantize_pack_permute_int4", "gemv_w4", "gemv_w4_permuted",
-               "gemm_w4", "quantize_int8", "permute_int8", "gemv_w8", "quantize_q8_1_pt", "gemv_w4a8", "mmvq_ptq1_0", "mmvq_ptq1_1",
+               "gemm_w4", "quantize_int8", "permute_int8", "gemv_w8", "quantize_q8_1_pt", "gemv_w4a8", "mmvq_ptq1_0",
+               "mmvq_ptq1_1", "ptq1_1_codebook", "ptq1_1_encode",
                "w4_status_string", "w4_abi_version", "w4_device_error"):
         assert fn in names
 
@@ -38,6 +39,7 @@ def test_library_exports_every_declared_symbol():
         assert hasattr(lib, fn), "libw4.so does not export %s" % fn
     assert lib.w4_abi_version() == 4
     assert lib.w4_status_string(-2) == b"illegal size or shape"
+    assert lib.w4_status_string(-7) == b"input value outside the format's range"
 
 
 def test_library_has_no_oracle_dependency():
@@ -47,7 +49,7 @@ def test_library_has_no_oracle_dependency():
     pkg = os.path.join(ROOT, "gemm_int4_dequant_gb300")
     for dirpath, _, files in os.walk(pkg):
         for f in files:
-            if f.endswith((".py", ".cu", ".cuh", ".h")):
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
                 text = open(os.path.join(dirpath, f), errors="ignore").read()
                 assert "import oracle" not in text and "from oracle" not in text and "w4_oracle" not in text, f
 
