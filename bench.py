@@ -72,10 +72,12 @@ WORKLOADS = {
     # ternary PTQ1_0 weights: x quantised to block_q8_1 / PT, then the MMVQ
     "ptq1_decode": dict(kind="ptq1", N=17280, K=5120, C=1),
     "ptq1_c8": dict(kind="ptq1", N=5120, K=17280, C=8),
+    # the same weights as PTQ1_1 superblocks (the library's host conversion)
+    "ptq1_1_decode": dict(kind="ptq1", N=17280, K=5120, C=1, superblocks=True),
 }
 COMPONENTS = ["c4", "c8", "c4s", "c8s", "c4_perm", "c8_perm", "c4s_perm", "c8s_perm", "quant", "quant_2call", "gemm",
               "w8_decode", "w8_quant", "w4a8_decode", "w4a8_c8",
-              "ptq1_decode", "ptq1_c8"]
+              "ptq1_decode", "ptq1_c8", "ptq1_1_decode"]
 
 
 def load_peaks():
@@ -119,10 +121,11 @@ def w4a8_bytes(N, K, C):
     return N * K // 2 + 4 * N + 2 * C * K + 2 * C * 144 * (K // 128) + 2 * C * N
 
 
-def ptq1_bytes(N, K, C):
-    # PTQ1_0 blocks + x read by the quantiser + the PT activations written
-    # and read back + d (fp32)
-    return N * (K // 128) * 28 + 2 * C * K + 2 * C * 144 * (K // 128) + 4 * C * N
+def ptq1_bytes(N, K, C, superblocks=False):
+    # PTQ1_0 blocks (or PTQ1_1 superblocks) + x read by the quantiser + the
+    # PT activations written and read back + d (fp32)
+    w = N * -(-K // 1024) * 216 if superblocks else N * (K // 128) * 28
+    return w + 2 * C * K + 2 * C * 144 * (K // 128) + 4 * C * N
 
 
 def gemm_bytes(M, N, K):
@@ -407,9 +410,14 @@ class Ptq1Work:
     """quantize_q8_1_pt of x, then mmvq_ptq1_0 over rotating copies of a
     PTQ1_0 tensor."""
 
-    def __init__(self, w4, N, K, C, seed=0):
+    def __init__(self, w4, N, K, C, seed=0, superblocks=False):
         dev = torch.device("cuda")
         blocks = synth.ptq1_0_blocks(N, K, seed=seed)
+        self.superblocks = superblocks
+        if superblocks:
+            sb, code, ei, ep = w4.ptq1_1_encode(blocks)   # host conversion, untimed
+            blocks = sb
+            self.tables = [torch.from_numpy(a).to(dev) for a in (code, ei, ep)]
         self.R = copies_for(blocks.nbytes)
         self.q = [torch.from_numpy(blocks).to(dev) for _ in range(self.R)]
         self.x_cpu = synth.gemv_inputs(1, K, C, act="bf16", seed=seed).x
@@ -419,20 +427,26 @@ class Ptq1Work:
         self.w4 = w4
         self.i = 0
         self.N, self.K, self.C = N, K, C
-        self.bytes = ptq1_bytes(N, K, C)
+        self.bytes = ptq1_bytes(N, K, C, superblocks)
         self.flops = 2 * N * K * C
         self.launches_per_step = 2
 
     def run(self, x, i):
         self.w4.quantize_q8_1_pt(x, out=self.pt)
-        self.w4.mmvq_ptq1_0(self.q[i % self.R], self.pt, out=self.d)
+        if self.superblocks:
+            code, ei, ep = self.tables
+            self.w4.mmvq_ptq1_1(self.q[i % self.R], code, ei, ep, self.pt, self.K, out=self.d)
+        else:
+            self.w4.mmvq_ptq1_0(self.q[i % self.R], self.pt, out=self.d)
 
     def step(self):
         self.run(self.x, self.i)
         self.i += 1
 
     def l2_note(self):
-        return "rotating %d PTQ1_0 copies (%.0f MB > 2x L2)" % (self.R, self.R * self.N * self.K / 128 * 28 / 1e6)
+        per = self.q[0].numel()
+        return "rotating %d %s copies (%.0f MB > 2x L2)" % (self.R, "PTQ1_1" if self.superblocks else "PTQ1_0",
+                                                          self.R * per / 1e6)
 
 
 class Quant8Work:
@@ -742,7 +756,9 @@ def cpu_baseline(name, budget_s=10.0):
                           "thread), %.1f s" % (done, N, K, cfg["C"], t_total)}
     if cfg["kind"] == "ptq1":
         N, K = cfg["N"], cfg["K"]
+        sup = cfg.get("superblocks", False)
         blocks = synth.ptq1_0_blocks(N, K, seed=0)
+        wsb = oracle.ptq1_1_encode(blocks) if sup else None
         xb = np_bits(synth.gemv_inputs(1, K, cfg["C"], act="bf16", seed=0).x)
         done, t_total, r0 = 0, 0.0, 0
         rows = 256
@@ -750,11 +766,14 @@ def cpu_baseline(name, budget_s=10.0):
             r1 = min(N, r0 + rows)
             t0 = time.perf_counter()
             pt = oracle.quantize_q8_1_pt(xb)
-            oracle.mmvq_ptq1_0(blocks, pt, rows=(r0, r1))
+            if sup:
+                oracle.mmvq_ptq1_1(wsb, pt, rows=(r0, r1))
+            else:
+                oracle.mmvq_ptq1_0(blocks, pt, rows=(r0, r1))
             t_total += time.perf_counter() - t0
             done += r1 - r0
             r0 = 0 if r1 >= N else r1
-        return {"value": ptq1_bytes(N, K, cfg["C"]) * done / N / t_total / 1e9, "unit": "GB/s", "cores": 1,
+        return {"value": ptq1_bytes(N, K, cfg["C"], sup) * done / N / t_total / 1e9, "unit": "GB/s", "cores": 1,
                 "kind": "oracle",
                 "sample": "%d rows of the %dx%d C=%d ternary MMVQ, x quantised each time (fp64 C oracle, single "
                           "thread), %.1f s" % (done, N, K, cfg["C"], t_total)}
@@ -808,7 +827,8 @@ def dtype_of(name):
     if cfg["kind"] == "w4a8":
         return "x quantised to int8 (block_q8_1) / uint4 weights, int32 dp4a dots, fp32 accumulate"
     if cfg["kind"] == "ptq1":
-        return "x quantised to int8 (block_q8_1) / ternary PTQ1_0 weights, int32 dp4a dots, fp32 accumulate"
+        fmt = "PTQ1_1" if cfg.get("superblocks") else "PTQ1_0"
+        return "x quantised to int8 (block_q8_1) / ternary %s weights, int32 dp4a dots, fp32 accumulate" % fmt
     return "bf16 in, int4 out (fp32 arithmetic)"
 
 
