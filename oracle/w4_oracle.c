@@ -360,6 +360,32 @@ void w4o_gemv_int8(const int8_t* q, const float* scale, const uint16_t* x, long 
     }
 }
 
+/*
+ * Large-M GEMM over the int8 quantised matrix (the int8 counterpart of
+ * w4o_gemm_at; [P3]'s C = A B with B the symmetric int8 weights):
+ *   C[m][n] = sum_k A[m][k] * q[k][n] * scale[n],  A bf16 [M][K], q int8
+ *   [K][N] row-major, scale fp32 [N],
+ * evaluated at the coordinates (m_idx[t], n_idx[t]); ref_abs (may be NULL)
+ * receives sum_k |A * w|.
+ */
+void w4o_gemm_int8_at(const uint16_t* A, const int8_t* q, const float* scale, long M, long N, long K,
+                      const long* m_idx, const long* n_idx, long count, double* c, double* ref_abs) {
+    (void)M;
+    for (long t = 0; t < count; ++t) {
+        long m = m_idx[t], n = n_idx[t];
+        double s = (double)scale[n];
+        double acc = 0.0, abs_acc = 0.0;
+        for (long k = 0; k < K; ++k) {
+            double a = (double)bf16_bits_to_float(A[m * K + k]);
+            double w = (double)q[k * N + n] * s;
+            acc += a * w;
+            abs_acc += fabs(a * w);
+        }
+        c[t] = acc;
+        if (ref_abs) ref_abs[t] = abs_acc;
+    }
+}
+
 /* ------------------------------------------------------------------------
  * W4A8: int4 weights with activations quantised to block_q8_1 in the PT
  * plane layout ([P4] sections 3 and 3.1).

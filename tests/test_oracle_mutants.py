@@ -77,7 +77,12 @@ MUTANTS = [
     ("int8_permute_table", [("{0, 2, 4, 6, 8, 10, 12, 14, 1, 3, 5, 7, 9, 11, 13, 15}",
                              "{0, 2, 4, 6, 8, 10, 12, 14, 3, 1, 5, 7, 9, 11, 13, 15}")]),
     ("int8_column_order", [("64 * (n_id % 2) +", "64 * (1 - n_id % 2) +")]),
-    ("int8_gemv_scale_dropped", [("double w = (double)q[k * N + n] * s;", "double w = (double)q[k * N + n];")]),
+    ("int8_gemv_scale_dropped", [("double w = (double)q[k * N + n] * s;\n                double xv",
+                                  "double w = (double)q[k * N + n];\n                double xv")]),
+    ("int8_gemm_transposed_q", [("double w = (double)q[k * N + n] * s;\n            acc",
+                                 "double w = (double)q[n * K + k] * s;\n            acc")]),
+    ("int8_gemm_a_column", [("double a = (double)bf16_bits_to_float(A[m * K + k]);",
+                             "double a = (double)bf16_bits_to_float(A[k * M + m]);")]),
     # fp32 -> half conversion used by block_q8_1
     ("half_ties_down", [("if (rest > 0x1000u || (rest == 0x1000u && (half & 1u))) ++half;",
                          "if (rest > 0x1000u) ++half;")]),

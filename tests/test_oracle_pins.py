@@ -499,6 +499,29 @@ def test_gemv_int8_matches_dense_matmul_and_one_hot():
     assert np.array_equal(d1[0], q[17].astype(np.float64) * s.astype(np.float64))
 
 
+def test_gemm_int8_matches_dense_matmul_identity_and_gemv():
+    """The int8 GEMM: a numpy matmul of A and the dequantised weights; A = I
+    returns q * scale exactly; a single row of A is the int8 GEMV of that
+    row; sampled coordinates equal the full product."""
+    rng = np.random.default_rng(4)
+    M, K, N = 24, 64, 40
+    q = rng.integers(-128, 128, (K, N), dtype=np.int64).astype(np.int8)
+    s = rng.uniform(1e-3, 1e-2, N).astype(np.float32)
+    A = bf16_bits(rng.standard_normal((M, K)))
+    c, ref = oracle.gemm_int8_full(A, q, s)
+    Wd = q.astype(np.float64) * s.astype(np.float64)[None, :]
+    Ad = bf16_values(A)
+    assert np.allclose(c, Ad @ Wd, rtol=1e-12, atol=1e-12)
+    assert np.allclose(ref, np.abs(Ad) @ np.abs(Wd), rtol=1e-12, atol=1e-12)
+    eye, _ = oracle.gemm_int8_full(bf16_bits(np.eye(K)), q, s)
+    assert np.array_equal(eye, Wd)
+    g, _ = oracle.gemv_int8(q, s, A[5:6])
+    assert np.allclose(c[5], g[0], rtol=1e-13, atol=0)
+    mi, ni = rng.integers(0, M, 50), rng.integers(0, N, 50)
+    part, _ = oracle.gemm_int8_at(A, q, s, mi, ni)
+    assert np.array_equal(part, c[mi, ni])
+
+
 # ---------------------------------------------------------------------------
 # W4A8: block_q8_1 activations in the PT plane layout
 # ---------------------------------------------------------------------------
