@@ -65,6 +65,7 @@ WORKLOADS = {
     # quantize_int8 + permute_int8 of one 8192x8192 weight
     "w8_decode": dict(kind="gemv8", N=17280, K=5120, C=1),
     "w8_quant": dict(kind="quant8", K=8192, N=8192),
+    "w8_gemm": dict(kind="gemm8", M=8192, N=8192, K=8192),
     # W4A8: x quantised to block_q8_1 in the PT planes, then the int4 GEMV
     # with integer dots (two kernels per step)
     "w4a8_decode": dict(kind="w4a8", N=17280, K=5120, C=1),
@@ -76,7 +77,7 @@ WORKLOADS = {
     "ptq1_1_decode": dict(kind="ptq1", N=17280, K=5120, C=1, superblocks=True),
 }
 COMPONENTS = ["c4", "c8", "c4s", "c8s", "c4_perm", "c8_perm", "c4s_perm", "c8s_perm", "quant", "quant_2call", "gemm",
-              "w8_decode", "w8_quant", "w4a8_decode", "w4a8_c8",
+              "w8_decode", "w8_quant", "w8_gemm", "w4a8_decode", "w4a8_c8",
               "ptq1_decode", "ptq1_c8", "ptq1_1_decode"]
 
 
@@ -518,6 +519,25 @@ class GemmWork:
         return "A+C are %.0f MB > L2" % ((self.M * self.K + self.M * self.N) * 2 / 1e6)
 
 
+class Gemm8Work(GemmWork):
+    """gemm_w8: bf16 A times quantize_int8's matrix."""
+
+    def __init__(self, w4, M, N, K, seed=0):
+        dev = torch.device("cuda")
+        gi = synth.int8_gemv_inputs(N, K, 1, seed=seed)
+        self.A = synth.gemm_inputs(M, 16, K, seed=seed + 1).A.to(dev)
+        self.B, self.s = gi.q.to(dev), gi.scale.to(dev)
+        self.C = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        self.w4 = w4
+        self.M, self.N, self.K = M, N, K
+        self.bytes = M * K * 2 + K * N + M * N * 2 + 4 * N
+        self.flops = gemm_flops(M, N, K)
+        self.launches_per_step = 1
+
+    def step(self):
+        self.w4.gemm_w8(self.A, self.B, self.s, out=self.C)
+
+
 def make_work(w4, name):
     cfg = dict(WORKLOADS[name])
     kind = cfg.pop("kind")
@@ -533,6 +553,8 @@ def make_work(w4, name):
         return Quant8Work(w4, **cfg)
     if kind == "w4a8":
         return W4a8Work(w4, **cfg)
+    if kind == "gemm8":
+        return Gemm8Work(w4, **cfg)
     if kind == "ptq1":
         return Ptq1Work(w4, **cfg)
     return GemmWork(w4, **cfg)
@@ -719,6 +741,22 @@ def cpu_baseline(name, budget_s=10.0):
         return {"value": flops / t_total / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
                 "sample": "%d sampled outputs of the 8192^3 GEMM (fp64 C oracle, single thread), %.1f s" %
                           (n_out, t_total)}
+    if cfg["kind"] == "gemm8":
+        M, N, K = cfg["M"], cfg["N"], cfg["K"]
+        gi = synth.int8_gemv_inputs(N, K, 1, seed=0)
+        A = np_bits(synth.gemm_inputs(M, 16, K, seed=1).A)
+        rng = np.random.default_rng(0)
+        n_out, t_total = 0, 0.0
+        while t_total < budget_s:
+            mi, ni = rng.integers(0, M, 256), rng.integers(0, N, 256)
+            t0 = time.perf_counter()
+            oracle.gemm_int8_at(A, gi.q.numpy(), gi.scale.numpy(), mi, ni)
+            t_total += time.perf_counter() - t0
+            n_out += 256
+        flops = 2.0 * K * n_out
+        return {"value": flops / t_total / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+                "sample": "%d sampled outputs of the 8192^3 int8 GEMM (fp64 C oracle, single thread), %.1f s" %
+                          (n_out, t_total)}
     if cfg["kind"] == "gemv8":
         g = synth.int8_gemv_inputs(cfg["N"], cfg["K"], cfg["C"], seed=0)
         q, scale, xb = g.q.numpy(), g.scale.numpy(), np_bits(g.x)
@@ -820,6 +858,8 @@ def dtype_of(name):
         return "bf16 x / uint4 weights (bf16 MMA), fp32 accumulate"
     if cfg["kind"] == "gemm":
         return "bf16 A / uint4 B (bf16 tcgen05 MMA), fp32 accumulate"
+    if cfg["kind"] == "gemm8":
+        return "bf16 A / int8 B (bf16 tcgen05 MMA), fp32 accumulate"
     if cfg["kind"] == "gemv8":
         return "bf16 x / int8 weights (fp32 FMA)"
     if cfg["kind"] == "quant8":

@@ -19,7 +19,7 @@
  *                       int4 -> 16-bit dequant), symmetric per-column scale.
  *   gemm_w4             large-M bf16 x int4 dequant GEMM
  *                       ("int4 gemm kernel", the matmul_bf16_int4 example).
- *   quantize_int8, permute_int8, gemv_w8
+ *   quantize_int8, permute_int8, gemv_w8, gemm_w8
  *                       the int8 weight-only counterparts (the first page's
  *                       int8 permute, from which its int4 permute derives).
  *   quantize_q8_1_pt, gemv_w4a8
@@ -280,6 +280,23 @@ w4_status permute_int8(const void* q, void* out, int64_t K, int64_t N, void* str
  * one bf16 rounding; the tolerance is gemv_w4's (2e-3 * sum_k |w*x|).
  */
 w4_status gemv_w8(const void* q, const float* scale, const void* x, void* d, int64_t N, int64_t K, int64_t C,
+                  void* stream);
+
+/*
+ * gemm_w8 -- large-M bf16 x int8 GEMM over quantize_int8's matrix (the int8
+ * counterpart of gemm_w4):
+ *
+ *   C[m][n] = scale[n] * sum_k A[m][k] * q[k][n]
+ *
+ * A      bf16 [M][K] row-major, 16-byte aligned.
+ * q      int8 [K][N] row-major, 16-byte aligned.
+ * scale  fp32 [N], 16-byte aligned.
+ * C      bf16 [M][N] row-major (output), 16-byte aligned.
+ * Requires K % 64 == 0 and N % 16 == 0 (else W4_ERR_SHAPE); K == 0 gives
+ * C = 0.  bf16 tensor-core products (int8 is exact in bf16), fp32
+ * accumulation, one bf16 rounding; the tolerance is gemm_w4's.
+ */
+w4_status gemm_w8(const void* A, const void* q, const float* scale, void* C, int64_t M, int64_t N, int64_t K,
                   void* stream);
 
 /* Shared memory available to one CTA on sm_103 (227 KB); gemv_w4a8 keeps all

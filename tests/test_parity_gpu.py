@@ -433,3 +433,60 @@ def test_int8_quantise_permute_gemv_chain(w4):
     d = w4.gemv_w8(q, scale, x.to(_dev()))
     ref, ref_abs = oracle.gemv_int8(q_ref, s_ref, np_bits(x))
     assert not parity_violations(d.float().cpu().numpy(), ref, ref_abs, BF16_TOL, bf16_out=True).any()
+
+
+# ---------------------------------------------------------------------------
+# gemm_w8: bf16 x int8 on the tensor cores
+# ---------------------------------------------------------------------------
+
+def _w8_gemm_case(M, N, K, seed):
+    gi = synth.int8_gemv_inputs(N, K, 1, seed=seed)
+    A = synth.gemm_inputs(M, 16, K, seed=seed + 1).A
+    return A, gi.q, gi.scale
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 256, 64), (300, 528, 192), (1, 16, 64), (777, 1040, 640), (512, 1024, 1024)])
+def test_gemm_w8_small(w4, M, N, K):
+    A, q, s = _w8_gemm_case(M, N, K, seed=M + N + K)
+    buf, out, pad = _guarded(M * N, torch.bfloat16, -3.0)
+    w4.gemm_w8(A.to(_dev()), q.to(_dev()), s.to(_dev()), out=out.view(M, N))
+    assert w4.device_error() == 0
+    ref, ref_abs = oracle.gemm_int8_full(np_bits(A), q.numpy(), s.numpy())
+    got = out.float().cpu().numpy().astype(np.float64).reshape(M, N)
+    bad = parity_violations(got, ref, ref_abs, BF16_TOL, bf16_out=True)
+    assert not bad.any(), "max err/ref_abs %g" % (np.abs(got - ref) / ref_abs).max()
+    assert _guards_intact(buf, pad, M * N, -3.0)
+
+
+def test_gemm_w8_full_size_sampled(w4):
+    M = N = K = 8192
+    A, q, s = _w8_gemm_case(M, N, K, seed=3)
+    C = w4.gemm_w8(A.to(_dev()), q.to(_dev()), s.to(_dev()))
+    assert w4.device_error() == 0
+    Cn = C.float().cpu().numpy().astype(np.float64)
+    rng = np.random.default_rng(1)
+    mi = list(rng.integers(0, M, 32768))
+    ni = list(rng.integers(0, N, 32768))
+    for m in (0, 127, 128, M - 1):
+        mi += [m] * 1024
+        ni += list(rng.integers(0, N, 1024))
+    for n in (0, 255, 256, N - 1):
+        mi += list(rng.integers(0, M, 1024))
+        ni += [n] * 1024
+    mi, ni = np.array(mi), np.array(ni)
+    ref, ref_abs = oracle.gemm_int8_at(np_bits(A), q.numpy(), s.numpy(), mi, ni)
+    bad = parity_violations(Cn[mi, ni], ref, ref_abs, BF16_TOL, bf16_out=True)
+    assert not bad.any()
+
+
+def test_quantize_int8_then_gemm_w8(w4):
+    """quantize_int8 on the device, then gemm_w8, against the oracle's
+    quantisation and product."""
+    K, N, M = 1024, 512, 384
+    W = synth.quant_inputs(K, N, seed=31)
+    A = synth.gemm_inputs(M, 16, K, seed=32).A
+    q, scale = w4.quantize_int8(W.to(_dev()))
+    C = w4.gemm_w8(A.to(_dev()), q, scale)
+    s_ref, q_ref = oracle.quantize_int8(np_bits(W))
+    ref, ref_abs = oracle.gemm_int8_full(np_bits(A), q_ref, s_ref)
+    assert not parity_violations(C.float().cpu().numpy(), ref, ref_abs, BF16_TOL, bf16_out=True).any()
