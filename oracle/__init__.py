@@ -47,6 +47,8 @@ def _load():
         lib.w4o_gemv_int8.restype = None
         lib.w4o_gemm_int8_at.argtypes = [P, P, P, L, L, L, P, P, L, P, P]
         lib.w4o_gemm_int8_at.restype = None
+        lib.w4o_gemm_packed_at.argtypes = [P, P, P, L, L, L, P, P, L, P, P]
+        lib.w4o_gemm_packed_at.restype = None
         lib.w4o_quantize_q8_1_pt.argtypes = [P, L, L, P]
         lib.w4o_quantize_q8_1_pt.restype = None
         lib.w4o_gemv_w4a8.argtypes = [P, P, P, P, L, L, L, L, L, P, P]
@@ -186,6 +188,38 @@ def gemm_int8_full(A_bits, q, scale):
     M, N = np.shape(A_bits)[0], np.shape(q)[1]
     mm, nn = np.meshgrid(np.arange(M), np.arange(N), indexing="ij")
     return gemm_int8_at(A_bits, q, scale, mm, nn)
+
+
+def gemm_packed_at(A_bits, packed, scale, m_idx, n_idx):
+    """C[m, n] = sum_k A[m, k] * q[k, n] * scale[n] at the given coordinates,
+    in fp64, over the quantiser's packed matrix (uint8 [K/2, N], two's
+    complement nibbles, even k low) and fp32 scale [N]."""
+    lib = _load()
+    A = np.ascontiguousarray(A_bits, dtype=np.uint16)
+    P_ = np.ascontiguousarray(packed, dtype=np.uint8)
+    M, K = A.shape
+    if P_.shape[0] * 2 != K:
+        raise ValueError("packed must be [K/2, N]")
+    N = P_.shape[1]
+    s = np.ascontiguousarray(scale, dtype=np.float32)
+    mi = np.ascontiguousarray(m_idx, dtype=np.int64).ravel()
+    ni = np.ascontiguousarray(n_idx, dtype=np.int64).ravel()
+    if mi.shape != ni.shape:
+        raise ValueError("m_idx and n_idx differ in size")
+    if mi.size and (mi.min() < 0 or mi.max() >= M or ni.min() < 0 or ni.max() >= N):
+        raise IndexError("coordinate out of range")
+    c = np.empty(mi.shape, np.float64)
+    ref = np.empty(mi.shape, np.float64)
+    lib.w4o_gemm_packed_at(_ptr(A), _ptr(P_), _ptr(s), M, N, K, _ptr(mi), _ptr(ni), mi.size, _ptr(c), _ptr(ref))
+    shape = np.shape(m_idx)
+    return c.reshape(shape), ref.reshape(shape)
+
+
+def gemm_packed_full(A_bits, packed, scale):
+    """Every element of the GEMM over the packed matrix (small shapes only)."""
+    M, N = np.shape(A_bits)[0], np.shape(packed)[1]
+    mm, nn = np.meshgrid(np.arange(M), np.arange(N), indexing="ij")
+    return gemm_packed_at(A_bits, packed, scale, mm, nn)
 
 
 def quantize_pack(W_bits):

@@ -205,6 +205,35 @@ void w4o_gemv_packed(const uint8_t* packed, const float* scale, const uint16_t* 
 }
 
 /*
+ * Large-M GEMM over the quantiser's packed matrix (the operand the permute
+ * rearranges; [P3]'s C = A B with B the symmetric int4 weights):
+ *   C[m][n] = sum_k A[m][k] * q[k][n] * scale[n]
+ * with q[k][n] the two's complement nibble of byte (k/2, n) of packed[K/2][N]
+ * (even k low) and scale fp32 [N]; at the coordinates (m_idx[t], n_idx[t]),
+ * ref_abs (may be NULL) = sum_k |A * w|.
+ */
+void w4o_gemm_packed_at(const uint16_t* A, const uint8_t* packed, const float* scale, long M, long N, long K,
+                        const long* m_idx, const long* n_idx, long count, double* c, double* ref_abs) {
+    (void)M;
+    for (long t = 0; t < count; ++t) {
+        long m = m_idx[t], n = n_idx[t];
+        double s = (double)scale[n];
+        double acc = 0.0, abs_acc = 0.0;
+        for (long k = 0; k < K; ++k) {
+            unsigned byte = packed[(k / 2) * N + n];
+            unsigned nib = (k % 2 == 0) ? (byte & 0x0Fu) : (byte >> 4);
+            int q = (nib >= 8u) ? (int)nib - 16 : (int)nib;
+            double a = (double)bf16_bits_to_float(A[m * K + k]);
+            double w = (double)q * s;
+            acc += a * w;
+            abs_acc += fabs(a * w);
+        }
+        c[t] = acc;
+        if (ref_abs) ref_abs[t] = abs_acc;
+    }
+}
+
+/*
  * [P1 section "int4 permute kernel"]: destination of source byte t inside
  * each 16-byte group of a column's byte stream (the "coordinates" of the
  * mapping 0..15 -> 0 8 4 12 1 9 5 13 2 10 6 14 3 11 7 15).  Copied from the

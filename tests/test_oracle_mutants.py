@@ -61,7 +61,8 @@ MUTANTS = [
     ("pack_offset_binary", [("(uint8_t)(((unsigned)q[0] & 0x0Fu) | (((unsigned)q[1] & 0x0Fu) << 4));",
                              "(uint8_t)(((unsigned)(q[0] + 8) & 0x0Fu) | (((unsigned)(q[1] + 8) & 0x0Fu) << 4));")]),
     # GEMV over the quantiser's packed columns
-    ("packed_no_sign_extension", [("int q = (nib >= 8u) ? (int)nib - 16 : (int)nib;", "int q = (int)nib;")]),
+    ("packed_no_sign_extension", [("((byte >> 4) & 0x0Fu);\n                int q = (nib >= 8u) ? (int)nib - 16 : (int)nib;",
+                                   "((byte >> 4) & 0x0Fu);\n                int q = (int)nib;")]),
     ("packed_halves_swapped", [("(k % 2 == 0) ? (byte & 0x0Fu) : ((byte >> 4) & 0x0Fu)",
                                 "(k % 2 == 1) ? (byte & 0x0Fu) : ((byte >> 4) & 0x0Fu)")]),
     # int4 permute
@@ -81,8 +82,14 @@ MUTANTS = [
                                   "double w = (double)q[k * N + n];\n                double xv")]),
     ("int8_gemm_transposed_q", [("double w = (double)q[k * N + n] * s;\n            acc",
                                  "double w = (double)q[n * K + k] * s;\n            acc")]),
-    ("int8_gemm_a_column", [("double a = (double)bf16_bits_to_float(A[m * K + k]);",
-                             "double a = (double)bf16_bits_to_float(A[k * M + m]);")]),
+    ("packed_gemm_unsigned", [("unsigned nib = (k % 2 == 0) ? (byte & 0x0Fu) : (byte >> 4);\n            int q = (nib >= 8u) ? (int)nib - 16 : (int)nib;",
+                               "unsigned nib = (k % 2 == 0) ? (byte & 0x0Fu) : (byte >> 4);\n            int q = (int)nib;")]),
+    ("packed_gemm_halves", [("unsigned nib = (k % 2 == 0) ? (byte & 0x0Fu) : (byte >> 4);",
+                             "unsigned nib = (k % 2 == 1) ? (byte & 0x0Fu) : (byte >> 4);")]),
+    ("int8_gemm_a_column", [("double a = (double)bf16_bits_to_float(A[m * K + k]);\n            double w = (double)q[k * N + n] * s;",
+                             "double a = (double)bf16_bits_to_float(A[k * M + m]);\n            double w = (double)q[k * N + n] * s;")]),
+    ("packed_gemm_a_column", [("double a = (double)bf16_bits_to_float(A[m * K + k]);\n            double w = (double)q * s;",
+                               "double a = (double)bf16_bits_to_float(A[k * M + m]);\n            double w = (double)q * s;")]),
     # fp32 -> half conversion used by block_q8_1
     ("half_ties_down", [("if (rest > 0x1000u || (rest == 0x1000u && (half & 1u))) ++half;",
                          "if (rest > 0x1000u) ++half;")]),

@@ -320,6 +320,30 @@ def test_gemv_packed_matches_dense_matmul():
     np.testing.assert_allclose(ref, np.abs(xv) @ np.abs(W), rtol=1e-12, atol=1e-12)
 
 
+def test_gemm_packed_matches_dense_matmul_identity_and_gemv():
+    """The GEMM over the quantiser's packed matrix: a numpy matmul of A and
+    the signed weights, A = I returning q * scale exactly, a row of A equal
+    to the packed GEMV of that row, and the bf16 GEMM of the same weights
+    re-encoded as u = q + 8 with zero point 8 and a bf16 scale."""
+    rng = np.random.default_rng(25)
+    M, K, N = 20, 64, 24
+    Q = _signed_q(rng, K, N)
+    s = bf16_values(bf16_bits(rng.uniform(0.01, 0.2, N))).astype(np.float32)   # bf16-exact scales
+    A = bf16_bits(rng.normal(0, 1, (M, K)))
+    P = _pack_cols(Q)
+    c, ref = oracle.gemm_packed_full(A, P, s)
+    W = Q * s.astype(np.float64)[None, :]
+    Ad = bf16_values(A)
+    np.testing.assert_allclose(c, Ad @ W, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(ref, np.abs(Ad) @ np.abs(W), rtol=1e-12, atol=1e-12)
+    eye, _ = oracle.gemm_packed_full(bf16_bits(np.eye(K)), P, s)
+    assert np.array_equal(eye, W)
+    g, _ = oracle.gemv_packed(P, s, A[3:4])
+    np.testing.assert_allclose(c[3], g[0], rtol=1e-13, atol=0)
+    c8, _ = oracle.gemm_full(A, _pack_cols(Q + 8), bf16_bits(s), bf16_bits(np.full(N, 8.0)))
+    np.testing.assert_allclose(c, c8, rtol=1e-12, atol=1e-12)
+
+
 def test_gemv_packed_agrees_with_row_gemv_at_zero_point_8():
     """Two's complement q is the unsigned u = q + 8 with zero point 8: the
     row-layout GEMV over the re-encoded words must give the same products."""
