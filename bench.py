@@ -66,6 +66,8 @@ WORKLOADS = {
     "w8_decode": dict(kind="gemv8", N=17280, K=5120, C=1),
     "w8_quant": dict(kind="quant8", K=8192, N=8192),
     "w8_gemm": dict(kind="gemm8", M=8192, N=8192, K=8192),
+    # the GEMM over permute_int4's output (fp32 scale, no zero point)
+    "gemm_perm": dict(kind="gemmp", M=8192, N=8192, K=8192),
     # W4A8: x quantised to block_q8_1 in the PT planes, then the int4 GEMV
     # with integer dots (two kernels per step)
     "w4a8_decode": dict(kind="w4a8", N=17280, K=5120, C=1),
@@ -77,7 +79,7 @@ WORKLOADS = {
     "ptq1_1_decode": dict(kind="ptq1", N=17280, K=5120, C=1, superblocks=True),
 }
 COMPONENTS = ["c4", "c8", "c4s", "c8s", "c4_perm", "c8_perm", "c4s_perm", "c8s_perm", "quant", "quant_2call", "gemm",
-              "w8_decode", "w8_quant", "w8_gemm", "w4a8_decode", "w4a8_c8",
+              "w8_decode", "w8_quant", "w8_gemm", "gemm_perm", "w4a8_decode", "w4a8_c8",
               "ptq1_decode", "ptq1_c8", "ptq1_1_decode"]
 
 
@@ -538,6 +540,26 @@ class Gemm8Work(GemmWork):
         self.w4.gemm_w8(self.A, self.B, self.s, out=self.C)
 
 
+class GemmPermWork(GemmWork):
+    """gemm_w4_permuted over weights permuted once at setup (untimed)."""
+
+    def __init__(self, w4, M, N, K, seed=0):
+        dev = torch.device("cuda")
+        g = synth.packed_gemv_inputs(N, K, 1, seed=seed)
+        self.A = synth.gemm_inputs(M, 16, K, seed=seed + 1).A.to(dev)
+        self.B = w4.permute_int4(g.packed.to(dev))
+        self.s = g.scale.to(dev)
+        self.C = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        self.w4 = w4
+        self.M, self.N, self.K = M, N, K
+        self.bytes = gemm_bytes(M, N, K)
+        self.flops = gemm_flops(M, N, K)
+        self.launches_per_step = 1
+
+    def step(self):
+        self.w4.gemm_w4_permuted(self.A, self.B, self.s, out=self.C)
+
+
 def make_work(w4, name):
     cfg = dict(WORKLOADS[name])
     kind = cfg.pop("kind")
@@ -555,6 +577,8 @@ def make_work(w4, name):
         return W4a8Work(w4, **cfg)
     if kind == "gemm8":
         return Gemm8Work(w4, **cfg)
+    if kind == "gemmp":
+        return GemmPermWork(w4, **cfg)
     if kind == "ptq1":
         return Ptq1Work(w4, **cfg)
     return GemmWork(w4, **cfg)
@@ -741,6 +765,21 @@ def cpu_baseline(name, budget_s=10.0):
         return {"value": flops / t_total / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
                 "sample": "%d sampled outputs of the 8192^3 GEMM (fp64 C oracle, single thread), %.1f s" %
                           (n_out, t_total)}
+    if cfg["kind"] == "gemmp":
+        M, N, K = cfg["M"], cfg["N"], cfg["K"]
+        g = synth.packed_gemv_inputs(N, K, 1, seed=0)
+        A = np_bits(synth.gemm_inputs(M, 16, K, seed=1).A)
+        rng = np.random.default_rng(0)
+        n_out, t_total = 0, 0.0
+        while t_total < budget_s:
+            mi, ni = rng.integers(0, M, 256), rng.integers(0, N, 256)
+            t0 = time.perf_counter()
+            oracle.gemm_packed_at(A, g.packed.numpy(), g.scale.numpy(), mi, ni)
+            t_total += time.perf_counter() - t0
+            n_out += 256
+        return {"value": 2.0 * K * n_out / t_total / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+                "sample": "%d sampled outputs of the 8192^3 GEMM over the packed matrix (fp64 C oracle, single "
+                          "thread), %.1f s" % (n_out, t_total)}
     if cfg["kind"] == "gemm8":
         M, N, K = cfg["M"], cfg["N"], cfg["K"]
         gi = synth.int8_gemv_inputs(N, K, 1, seed=0)
@@ -860,6 +899,8 @@ def dtype_of(name):
         return "bf16 A / uint4 B (bf16 tcgen05 MMA), fp32 accumulate"
     if cfg["kind"] == "gemm8":
         return "bf16 A / int8 B (bf16 tcgen05 MMA), fp32 accumulate"
+    if cfg["kind"] == "gemmp":
+        return "bf16 A / permuted int4 B (bf16 tcgen05 MMA), fp32 accumulate"
     if cfg["kind"] == "gemv8":
         return "bf16 x / int8 weights (fp32 FMA)"
     if cfg["kind"] == "quant8":

@@ -16,6 +16,7 @@ in the library's CUDA kernels; there is no CPU or eager fallback.
     permute_int8(q)                     -> out [N*K] int8 (interleaved)
     gemv_w8(q, scale, x)                -> d [C, N] bf16
     gemm_w8(A, q, scale)                -> C [M, N] bf16 (bf16 x int8 on the tensor cores)
+    gemm_w4_permuted(A, permuted, scale) -> C [M, N] bf16 (over permute_int4's output)
     quantize_q8_1_pt(x)                 -> pt [C, 144*K/128] uint8 (block_q8_1 in PT planes)
     gemv_w4a8(qweight, scale, zero, pt) -> d [C, N] bf16 (int4 weights x int8 activations)
     mmvq_ptq1_0(blocks, pt)             -> d [C, N] fp32 (ternary PTQ1_0 weights x int8 activations)
@@ -28,7 +29,7 @@ from . import _lib
 from ._lib import W4Error, W4_BF16, W4_F32
 
 __all__ = ["quantize_pack_int4", "permute_int4", "quantize_pack_permute_int4", "gemv_w4", "gemv_w4_permuted", "gemm_w4",
-           "quantize_int8", "permute_int8", "gemv_w8", "gemm_w8", "quantize_q8_1_pt", "gemv_w4a8", "mmvq_ptq1_0", "mmvq_ptq1_1",
+           "quantize_int8", "permute_int8", "gemv_w8", "gemm_w8", "gemm_w4_permuted", "quantize_q8_1_pt", "gemv_w4a8", "mmvq_ptq1_0", "mmvq_ptq1_1",
            "ptq1_1_encode", "device_error", "W4Error"]
 
 _lib.load()  # fail loudly at import if the CUDA library is missing
@@ -256,6 +257,28 @@ def gemm_w8(A, q, scale, out=None, stream=None):
         raise ValueError("out must hold M*N elements")
     st = _lib.load().gemm_w8(A.data_ptr(), q.data_ptr(), scale.data_ptr(), out.data_ptr(), M, N, K, _stream(stream))
     _lib.check("gemm_w8", st)
+    return out
+
+
+def gemm_w4_permuted(A, permuted, scale, out=None, stream=None):
+    """C[m, n] = scale[n] * sum_k A[m, k] q[k, n] with the int4 weights read
+    straight from permute_int4's output (N*K/2 bytes): A bf16 [M, K]
+    (K % 64 == 0), scale fp32 [N] (N % 16 == 0).  Returns bf16 [M, N]."""
+    _need(A, "A", (torch.bfloat16,), 2)
+    _need(permuted, "permuted", (torch.int8, torch.uint8))
+    _need(scale, "scale", (torch.float32,), 1)
+    M, K = A.shape
+    N = scale.numel()
+    if permuted.numel() != N * (K // 2):
+        raise ValueError("permuted must hold N*K/2 bytes")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    _need(out, "out", (torch.bfloat16,))
+    if out.numel() != M * N:
+        raise ValueError("out must hold M*N elements")
+    st = _lib.load().gemm_w4_permuted(A.data_ptr(), permuted.data_ptr(), scale.data_ptr(), out.data_ptr(), M, N, K,
+                                      _stream(stream))
+    _lib.check("gemm_w4_permuted", st)
     return out
 
 

@@ -60,6 +60,8 @@ def load():
     lib.gemv_w8.restype = I
     lib.gemm_w8.argtypes = [P, P, P, P, I64, I64, I64, P]
     lib.gemm_w8.restype = I
+    lib.gemm_w4_permuted.argtypes = [P, P, P, P, I64, I64, I64, P]
+    lib.gemm_w4_permuted.restype = I
     lib.quantize_q8_1_pt.argtypes = [P, P, I64, I64, P]
     lib.quantize_q8_1_pt.restype = I
     lib.gemv_w4a8.argtypes = [P, P, P, P, P, I64, I64, I64, P]

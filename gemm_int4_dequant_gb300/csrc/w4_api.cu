@@ -34,6 +34,8 @@ bool ptq1_fits(int64_t C, int64_t K, bool super);
 int take_device_error_ptq1();
 w4_status run_gemm_w8(const void* A, const void* q, const float* scale, void* C, int64_t M, int64_t N, int64_t K,
                       cudaStream_t s);
+w4_status run_gemm_w4_permuted(const void* A, const void* permuted, const float* scale, void* C, int64_t M,
+                               int64_t N, int64_t K, cudaStream_t s);
 int take_device_error_gemm();
 int take_device_error_gemv();
 int take_device_error_quant();
@@ -260,6 +262,17 @@ w4_status gemm_w8(const void* A, const void* q, const float* scale, void* C, int
     if (!device_is_sm103()) return W4_ERR_DEVICE;
     if (K == 0) return launch_status(cudaMemsetAsync(C, 0, M * N * 2, (cudaStream_t)stream));
     return run_gemm_w8(A, q, scale, C, M, N, K, (cudaStream_t)stream);
+}
+
+w4_status gemm_w4_permuted(const void* A, const void* permuted, const float* scale, void* C, int64_t M, int64_t N,
+                           int64_t K, void* stream) {
+    if (M < 0 || N < 0 || K < 0 || (K % 64) != 0 || (N % 16) != 0) return W4_ERR_SHAPE;
+    if (M == 0 || N == 0) return W4_OK;
+    if (!C || !scale || (K > 0 && (!A || !permuted))) return W4_ERR_NULL;
+    if (!aligned16(C) || !aligned16(scale) || (K > 0 && (!aligned16(A) || !aligned16(permuted)))) return W4_ERR_ALIGN;
+    if (!device_is_sm103()) return W4_ERR_DEVICE;
+    if (K == 0) return launch_status(cudaMemsetAsync(C, 0, M * N * 2, (cudaStream_t)stream));
+    return run_gemm_w4_permuted(A, permuted, scale, C, M, N, K, (cudaStream_t)stream);
 }
 
 w4_status gemm_w4(const void* A, const void* B, const void* scale, const void* zero, void* C, int64_t M, int64_t N,

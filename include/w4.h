@@ -18,7 +18,8 @@
  *                       interleaved layout the page builds for the fast
  *                       int4 -> 16-bit dequant), symmetric per-column scale.
  *   gemm_w4             large-M bf16 x int4 dequant GEMM
- *                       ("int4 gemm kernel", the matmul_bf16_int4 example).
+ *                       ("int4 gemm kernel", the matmul_bf16_int4 example);
+ *                       gemm_w4_permuted, the same over permute_int4's output.
  *   quantize_int8, permute_int8, gemv_w8, gemm_w8
  *                       the int8 weight-only counterparts (the first page's
  *                       int8 permute, from which its int4 permute derives).
@@ -298,6 +299,25 @@ w4_status gemv_w8(const void* q, const float* scale, const void* x, void* d, int
  */
 w4_status gemm_w8(const void* A, const void* q, const float* scale, void* C, int64_t M, int64_t N, int64_t K,
                   void* stream);
+
+/*
+ * gemm_w4_permuted -- large-M bf16 x int4 GEMM that reads permute_int4's
+ * output directly (the layout that page builds for the fast int4 -> 16-bit
+ * dequant):
+ *
+ *   C[m][n] = scale[n] * sum_k A[m][k] * q[k][n]
+ *
+ * with q[k][n] the two's complement weights quantize_pack_int4 packed and
+ * permute_int4 rearranged.
+ * A         bf16 [M][K] row-major, 16-byte aligned.
+ * permuted  N*K/2 bytes (permute_int4's output), 16-byte aligned.
+ * scale     fp32 [N], 16-byte aligned.
+ * C         bf16 [M][N] row-major (output), 16-byte aligned.
+ * Requires K % 64 == 0 and N % 16 == 0 (else W4_ERR_SHAPE); K == 0 gives
+ * C = 0.  Tolerance as gemm_w4.
+ */
+w4_status gemm_w4_permuted(const void* A, const void* permuted, const float* scale, void* C, int64_t M, int64_t N,
+                           int64_t K, void* stream);
 
 /* Shared memory available to one CTA on sm_103 (227 KB); gemv_w4a8 keeps all
  * of x there. */

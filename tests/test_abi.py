@@ -27,7 +27,7 @@ def _declared_functions():
 def test_header_declares_the_hot_path():
     names = _declared_functions()
     for fn in ("quantize_pack_int4", "permute_int4", "quantize_pack_permute_int4", "gemv_w4", "gemv_w4_permuted",
-               "gemm_w4", "quantize_int8", "permute_int8", "gemv_w8", "gemm_w8", "quantize_q8_1_pt", "gemv_w4a8", "mmvq_ptq1_0",
+               "gemm_w4", "quantize_int8", "permute_int8", "gemv_w8", "gemm_w8", "gemm_w4_permuted", "quantize_q8_1_pt", "gemv_w4a8", "mmvq_ptq1_0",
                "mmvq_ptq1_1", "ptq1_1_codebook", "ptq1_1_encode",
                "w4_status_string", "w4_abi_version", "w4_device_error"):
         assert fn in names
@@ -148,6 +148,12 @@ def test_argument_validation_happens_on_host():
     assert lib.gemm_w8(A, None, A, A, 128, 256, 128, None) == L.W4_ERR_NULL
     assert lib.gemm_w8(A, A, odd, A, 128, 256, 128, None) == L.W4_ERR_ALIGN
     assert lib.gemm_w8(A, A, A, A, 0, 256, 128, None) == L.W4_OK
+    # gemm_w4_permuted: the GEMM's tile rules
+    assert lib.gemm_w4_permuted(A, A, A, A, 128, 256, 100, None) == L.W4_ERR_SHAPE
+    assert lib.gemm_w4_permuted(A, A, A, A, 128, 264, 128, None) == L.W4_ERR_SHAPE
+    assert lib.gemm_w4_permuted(A, None, A, A, 128, 256, 128, None) == L.W4_ERR_NULL
+    assert lib.gemm_w4_permuted(odd, A, A, A, 128, 256, 128, None) == L.W4_ERR_ALIGN
+    assert lib.gemm_w4_permuted(A, A, A, A, 0, 256, 128, None) == L.W4_OK
     # gemm_w4
     assert lib.gemm_w4(A, A, A, A, A, 128, 256, 100, None) == L.W4_ERR_SHAPE
     assert lib.gemm_w4(A, A, A, A, A, 128, 250, 128, None) == L.W4_ERR_SHAPE

@@ -29,7 +29,7 @@ def test_gemm_bytes_and_flops():
 
 def test_workloads_name_known_kinds():
     for name, cfg in bench.WORKLOADS.items():
-        assert cfg["kind"] in ("gemv", "quant", "gemm", "gemv8", "quant8", "w4a8", "ptq1", "gemm8"), name
+        assert cfg["kind"] in ("gemv", "quant", "gemm", "gemv8", "quant8", "w4a8", "ptq1", "gemm8", "gemmp"), name
     assert set(bench.COMPONENTS) <= set(bench.WORKLOADS)
     assert bench.WORKLOADS["quant"]["fused"] and not bench.WORKLOADS["quant_2call"]["fused"]
 

@@ -490,3 +490,57 @@ def test_quantize_int8_then_gemm_w8(w4):
     s_ref, q_ref = oracle.quantize_int8(np_bits(W))
     ref, ref_abs = oracle.gemm_int8_full(np_bits(A), q_ref, s_ref)
     assert not parity_violations(C.float().cpu().numpy(), ref, ref_abs, BF16_TOL, bf16_out=True).any()
+
+
+# ---------------------------------------------------------------------------
+# gemm_w4_permuted: the GEMM reading permute_int4's layout
+# ---------------------------------------------------------------------------
+
+def _perm_gemm_case(M, N, K, seed):
+    g = synth.packed_gemv_inputs(N, K, 1, seed=seed)
+    A = synth.gemm_inputs(M, 16, K, seed=seed + 1).A
+    permuted = oracle.permute(g.packed.numpy(), K, N)
+    return A, g.packed.numpy(), permuted, g.scale
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 256, 64), (300, 528, 192), (1, 16, 64), (777, 1040, 640), (512, 1024, 1024)])
+def test_gemm_w4_permuted_small(w4, M, N, K):
+    A, packed, permuted, s = _perm_gemm_case(M, N, K, seed=M + N + K)
+    buf, out, pad = _guarded(M * N, torch.bfloat16, -3.0)
+    w4.gemm_w4_permuted(A.to(_dev()), torch.from_numpy(permuted).to(_dev()), s.to(_dev()), out=out.view(M, N))
+    assert w4.device_error() == 0
+    ref, ref_abs = oracle.gemm_packed_full(np_bits(A), packed, s.numpy())
+    got = out.float().cpu().numpy().astype(np.float64).reshape(M, N)
+    bad = parity_violations(got, ref, ref_abs, BF16_TOL, bf16_out=True)
+    assert not bad.any(), "max err/ref_abs %g" % (np.abs(got - ref) / ref_abs).max()
+    assert _guards_intact(buf, pad, M * N, -3.0)
+
+
+def test_gemm_w4_permuted_full_size_sampled(w4):
+    M = N = K = 8192
+    A, packed, permuted, s = _perm_gemm_case(M, N, K, seed=5)
+    C = w4.gemm_w4_permuted(A.to(_dev()), torch.from_numpy(permuted).to(_dev()), s.to(_dev()))
+    assert w4.device_error() == 0
+    Cn = C.float().cpu().numpy().astype(np.float64)
+    rng = np.random.default_rng(2)
+    mi = list(rng.integers(0, M, 32768))
+    ni = list(rng.integers(0, N, 32768))
+    for n in (0, 3, 4, 127, 128, 255, 256, N - 1):      # group and tile edges
+        mi += list(rng.integers(0, M, 512))
+        ni += [n] * 512
+    mi, ni = np.array(mi), np.array(ni)
+    ref, ref_abs = oracle.gemm_packed_at(np_bits(A), packed, s.numpy(), mi, ni)
+    assert not parity_violations(Cn[mi, ni], ref, ref_abs, BF16_TOL, bf16_out=True).any()
+
+
+def test_quantise_permute_then_gemm(w4):
+    """quantize_pack_permute_int4 on the device, then gemm_w4_permuted,
+    against the oracle's quantisation and product."""
+    K, N, M = 1024, 512, 384
+    W = synth.quant_inputs(K, N, seed=41)
+    A = synth.gemm_inputs(M, 16, K, seed=42).A
+    permuted, scale = w4.quantize_pack_permute_int4(W.to(_dev()))
+    C = w4.gemm_w4_permuted(A.to(_dev()), permuted, scale)
+    s_ref, p_ref = oracle.quantize_pack(np_bits(W))
+    ref, ref_abs = oracle.gemm_packed_full(np_bits(A), p_ref, s_ref)
+    assert not parity_violations(C.float().cpu().numpy(), ref, ref_abs, BF16_TOL, bf16_out=True).any()
