@@ -43,6 +43,8 @@ import synth  # noqa: E402
 
 METRIC = "int4 W-only GEMV HBM GB/s (% of GB300 peak); dequant-GEMM TFLOP/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# GB300's nominal figures (HBM3e 7.9 TB/s; 2.25 PFLOP/s dense bf16), reported beside the measured peaks
+NOMINAL_PEAKS = {"hbm_gbs": 7900.0, "bf16_tflops": 2250.0}
 
 WORKLOADS = {
     "decode": dict(kind="gemv", N=17280, K=5120, C=1),
@@ -929,12 +931,15 @@ def roofline(work, sec_per_launch, peaks, peak_src, kind_name, workload):
         peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
         return {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "peak_source": "%s bf16 burst" % peak_src,
+                "peak_nominal": NOMINAL_PEAKS["bf16_tflops"], "frac_nominal": achieved / NOMINAL_PEAKS["bf16_tflops"],
                 "traffic": recorded_traffic("gemm", workload)}
     # quant: the two kernels of a step together (bytes of the step / time of the step)
     achieved = work.bytes / work.launches_per_step / sec_per_launch / 1e9
     peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     return {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-            "peak_source": "%s HBM copy" % peak_src, "traffic": recorded_traffic(kind_name, workload)}
+            "peak_source": "%s HBM copy" % peak_src,
+            "peak_nominal": NOMINAL_PEAKS["hbm_gbs"], "frac_nominal": achieved / NOMINAL_PEAKS["hbm_gbs"],
+            "traffic": recorded_traffic(kind_name, workload)}
 
 
 def run_ours(args, world, rank):

@@ -45,6 +45,7 @@ def test_roofline_record_hbm():
     assert r["bound"] == "hbm" and r["unit"] == "GB/s"
     assert r["achieved"] == pytest.approx(4435.072)
     assert r["frac"] == pytest.approx(4435.072 / 6772.5)
+    assert r["peak_nominal"] == 7900.0 and r["frac_nominal"] == pytest.approx(4435.072 / 7900.0)
 
 
 def test_source_hash_ignores_comments_but_not_code(tmp_path, monkeypatch):
