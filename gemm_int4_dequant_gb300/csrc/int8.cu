@@ -320,9 +320,147 @@ w4_status launch_w8_fast(const void* q, const float* scale, const void* x, void*
                                             K, static_cast<int>(S)));
 }
 
+// ---------------------------------------------------------------------------
+// Single-read quantiser (N % 8 == 0, K <= Q8C_MAX_K): a cluster of
+// Q8C_CTAS CTAs takes a strip of 64 columns -- one 128-byte line of every
+// row of W -- and splits K; each CTA keeps its rows in shared memory, so W
+// is read once.  The column maxima of the CTAs meet through distributed
+// shared memory between two cluster barriers; every CTA then quantises its
+// own rows from shared memory (IEEE division, half-away rounding, as the
+// two-pass kernel) and rank 0 writes the scales.  2KN read + KN + 4N written.
+// ---------------------------------------------------------------------------
+
+constexpr int Q8C_CTAS = 8;
+constexpr int Q8C_THREADS = 256;
+constexpr int Q8C_COLS = 64;                       // bf16 columns of a strip (128 bytes)
+constexpr int Q8C_ROWS_MAX = 1600;                 // rows a CTA can hold (200 KB)
+constexpr int64_t Q8C_MAX_K = int64_t(Q8C_CTAS) * Q8C_ROWS_MAX;
+
+__host__ __device__ inline size_t q8c_smem_bytes(int64_t rows) {
+    return size_t(rows) * Q8C_COLS * 2 + Q8C_COLS * 4 * 2 + (Q8C_THREADS / 32) * Q8C_COLS * 4;
+}
+
+__global__ void __launch_bounds__(Q8C_THREADS, 1)
+quantize_int8_cluster_kernel(const uint16_t* __restrict__ W, int8_t* __restrict__ q, float* __restrict__ scale,
+                             int64_t K, int64_t N) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    const int rank = static_cast<int>(blockIdx.x % Q8C_CTAS);
+    const int64_t strip = blockIdx.x / Q8C_CTAS;
+    const int64_t Kr = (K + Q8C_CTAS - 1) / Q8C_CTAS, k0 = rank * Kr, k1 = (k0 + Kr < K) ? k0 + Kr : K;
+    const int64_t rows = k1 > k0 ? k1 - k0 : 0;
+    uint16_t* tile = reinterpret_cast<uint16_t*>(smem);                                // [Kr][64]
+    uint32_t* cmax = reinterpret_cast<uint32_t*>(smem + size_t(Kr) * Q8C_COLS * 2);    // [64] this CTA's max
+    float* s_col = reinterpret_cast<float*>(cmax + Q8C_COLS);                          // [64] the scales
+    uint32_t* red = reinterpret_cast<uint32_t*>(s_col + Q8C_COLS);                     // [warp][64]
+
+    const int cq = threadIdx.x % 8, rl = threadIdx.x / 8;   // 8 columns, one of 32 row lanes
+    const int64_t n0 = strip * Q8C_COLS + cq * 8;
+    const bool live = n0 < N;                                // N % 8 == 0: all 8 columns exist
+    uint32_t m[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    constexpr int U = 8;
+    for (int64_t r0 = rl; r0 < rows; r0 += 32 * U) {
+        uint4 v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t r = r0 + 32 * u;
+            v[u] = (live && r < rows) ? ldg_stream_u4(W + (k0 + r) * N + n0) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t r = r0 + 32 * u;
+            if (r >= rows) break;
+            *reinterpret_cast<uint4*>(tile + r * Q8C_COLS + cq * 8) = v[u];
+            const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                m[2 * j] = max(m[2 * j], w[j] & 0x7FFFu);          // |w| as a bf16 bit pattern
+                m[2 * j + 1] = max(m[2 * j + 1], (w[j] >> 16) & 0x7FFFu);
+            }
+        }
+    }
+    // the CTA's column maxima: the warp's four row lanes by shuffles, then the warps
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        uint32_t x = m[j];
+        x = max(x, __shfl_xor_sync(0xFFFFFFFFu, x, 8));
+        x = max(x, __shfl_xor_sync(0xFFFFFFFFu, x, 16));
+        if (lane < 8) red[warp * Q8C_COLS + cq * 8 + j] = x;
+    }
+    __syncthreads();
+    if (threadIdx.x < Q8C_COLS) {
+        uint32_t x = 0;
+        for (int wi = 0; wi < Q8C_THREADS / 32; ++wi) x = max(x, red[wi * Q8C_COLS + threadIdx.x]);
+        cmax[threadIdx.x] = x;
+    }
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+    if (threadIdx.x < Q8C_COLS) {
+        uint32_t x = 0;
+        const uint32_t local = static_cast<uint32_t>(__cvta_generic_to_shared(cmax + threadIdx.x));
+        for (int r = 0; r < Q8C_CTAS; ++r) {
+            uint32_t v;
+            asm volatile("{\n\t.reg .b32 a;\n\tmapa.shared::cluster.u32 a, %1, %2;\n\tld.shared::cluster.u32 %0, [a];\n\t}"
+                         : "=r"(v) : "r"(local), "r"(r) : "memory");
+            x = max(x, v);
+        }
+        const float sc = __fdiv_rn(bf16_bits_to_f32(x), 127.0f);
+        s_col[threadIdx.x] = sc;
+        const int64_t n = strip * Q8C_COLS + threadIdx.x;
+        if (rank == 0 && n < N) scale[n] = sc;
+    }
+    __syncthreads();
+    if (live) {
+        float sc[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) sc[j] = s_col[cq * 8 + j];
+        for (int64_t r = rl; r < rows; r += 32) {
+            const uint4 v = *reinterpret_cast<const uint4*>(tile + r * Q8C_COLS + cq * 8);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+            uint32_t out[2] = {0, 0};
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const uint32_t bits = (j % 2 == 0) ? (w[j / 2] & 0xFFFFu) : (w[j / 2] >> 16);
+                const int8_t qq = quant8(bf16_bits_to_f32(bits), sc[j]);
+                out[j / 4] |= (static_cast<uint32_t>(static_cast<uint8_t>(qq))) << (8 * (j % 4));
+            }
+            *reinterpret_cast<uint2*>(q + (k0 + r) * N + n0) = make_uint2(out[0], out[1]);
+        }
+    }
+    // keep this CTA's maxima readable until every peer has read them
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+w4_status launch_quantize_int8_cluster(const void* W, void* q, float* scale, int64_t K, int64_t N,
+                                       cudaStream_t stream) {
+    const int64_t strips = (N + Q8C_COLS - 1) / Q8C_COLS;
+    const int64_t Kr = (K + Q8C_CTAS - 1) / Q8C_CTAS;
+    const size_t smem = q8c_smem_bytes(Kr);
+    if (strips * Q8C_CTAS > 0x7FFFFFFF) return W4_ERR_SHAPE;
+    static int smem_set[64];
+    if (ensure_smem_limit(quantize_int8_cluster_kernel, static_cast<int>(smem), smem_set) != cudaSuccess)
+        return W4_ERR_CUDA;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(strips * Q8C_CTAS), 1, 1);
+    cfg.blockDim = dim3(Q8C_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = Q8C_CTAS;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return launch_status(cudaLaunchKernelEx(&cfg, quantize_int8_cluster_kernel, static_cast<const uint16_t*>(W),
+                                            static_cast<int8_t*>(q), scale, K, N));
+}
+
 }  // namespace
 
 w4_status run_quantize_int8(const void* W, void* q, float* scale, int64_t K, int64_t N, cudaStream_t stream) {
+    if (N % 8 == 0 && K <= Q8C_MAX_K) return launch_quantize_int8_cluster(W, q, scale, K, N, stream);
     const int64_t strips = (N + Q8_COLS - 1) / Q8_COLS;
     if (strips > 0x7FFFFFFF) return W4_ERR_SHAPE;
     quantize_int8_kernel<<<static_cast<unsigned>(strips), Q8_COLS * Q8_LANES, 0, stream>>>(

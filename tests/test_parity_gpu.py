@@ -375,7 +375,12 @@ def test_gemm_k_zero(w4):
 # int8 weight-only variant: quantize_int8, permute_int8 (bit-exact), gemv_w8
 # ---------------------------------------------------------------------------
 
-@pytest.mark.parametrize("K,N", [(1, 8), (64, 2), (130, 37), (1024, 1000), (8192, 8192)])
+@pytest.mark.parametrize("K,N", [
+    (64, 2), (130, 37),                       # N % 8 != 0: the two-pass kernel
+    (1, 8), (7, 120),                         # single-read clusters: ranks without rows; a partial strip
+    (1024, 1000), (8192, 8192), (12800, 72),  # ... up to the longest K a cluster holds
+    (12808, 16),                              # one step past it: the two-pass kernel again
+])
 def test_quantize_int8_bit_exact(w4, K, N):
     W = synth.quant_inputs(K, N, seed=K + 5 * N)
     if N > 3:
