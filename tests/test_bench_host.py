@@ -90,3 +90,23 @@ def test_ptq1_bytes():
     # 28-byte blocks + x + PT written and read + fp32 d
     N, K, C = 17280, 5120, 1
     assert bench.ptq1_bytes(N, K, C) == N * 40 * 28 + 2 * K + 2 * 144 * 40 + 4 * N
+
+
+def test_reference_arm_runs_on_the_host_and_prints_the_contract_line():
+    """`bench.py --impl reference` times the oracle on the host cores alone
+    (no GPU) and prints one JSON line with the contract's keys."""
+    import json
+    import subprocess
+    import sys
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "1", "--warmup", "1",
+                        "--cpu-seconds", "1"], cwd=bench.ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    for key in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e", "gpu_launches"):
+        assert key in line, key
+    assert line["impl"] == "reference" and line["gpu_launches"] == 0 and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["config"]["workload"] == "decode"

@@ -57,3 +57,19 @@ def test_single_rank_is_unchanged():
     import bench
     assert bench.max_over_ranks(0.5, 1) == 0.5
     assert bench.job_rate(3.0, 1) == 3.0
+
+
+def test_reference_arm_under_torchrun_prints_once():
+    """Launched as the driver launches it for N > 1, the reference arm runs
+    on rank 0 alone: one JSON line, every rank exits 0."""
+    import json
+    import subprocess
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(_free_port()), "bench.py", "--impl", "reference",
+           "--gpus", "2", "--steps", "1", "--warmup", "1", "--cpu-seconds", "1"]
+    r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.strip().startswith("{")]
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["n_gpus"] == 2
