@@ -884,6 +884,55 @@ def cpu_baseline(name, budget_s=10.0):
                       (n_done, K, N, t_total)}
 
 
+def host_threads():
+    """The host cores this process may run on."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline_all_cores(name, budget_s=10.0):
+    """The same oracle on every host core: threads take disjoint 64-row
+    chunks of the row-layout GEMV (the C oracle runs outside the Python
+    lock), until the budget; None for the other workloads."""
+    cfg = WORKLOADS[name]
+    if cfg["kind"] != "gemv" or cfg.get("perm"):
+        return None
+    import threading
+    from concurrent.futures import ThreadPoolExecutor
+
+    import oracle
+    from synth import np_bits
+    g = synth.gemv_inputs(cfg["N"], cfg["K"], cfg["C"], act="bf16", seed=0)
+    args = (np_bits(g.qweight), np_bits(g.scale), np_bits(g.zero), np_bits(g.x), oracle.BF16)
+    N, chunk, threads = cfg["N"], 64, host_threads()
+    oracle.gemv(*args, rows=(0, 1))   # load the library before the clock starts
+    lock = threading.Lock()
+    state = {"next": 0}
+    deadline = time.perf_counter() + budget_s
+
+    def worker():
+        done = 0
+        while time.perf_counter() < deadline:
+            with lock:
+                r0 = state["next"]
+                state["next"] = (r0 + chunk) % N if r0 + chunk < N else 0
+            r1 = min(N, r0 + chunk)
+            oracle.gemv(*args, rows=(r0, r1))
+            done += r1 - r0
+        return done
+
+    t0 = time.perf_counter()
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        rows = sum(ex.map(lambda _: worker(), range(threads)))
+    wall = time.perf_counter() - t0
+    return {"value": gemv_bytes(N, cfg["K"], cfg["C"]) * rows / N / wall / 1e9, "unit": "GB/s", "cores": threads,
+            "kind": "oracle",
+            "sample": "%d rows of the %dx%d C=%d GEMV in 64-row chunks over %d threads (fp64 C oracle), %.1f s" %
+                      (rows, N, cfg["K"], cfg["C"], threads, wall)}
+
+
 # ---------------------------------------------------------------------------
 # main
 # ---------------------------------------------------------------------------
@@ -979,6 +1028,9 @@ def run_ours(args, world, rank):
                                     "step time")
     if rank == 0 and world == 1:
         line["cpu_baseline"] = cpu_baseline(args.workload, budget_s=args.cpu_seconds)
+        every_core = cpu_baseline_all_cores(args.workload, budget_s=args.cpu_seconds)
+        if every_core is not None:
+            line["cpu_baseline_all_cores"] = every_core
     if args.components and world == 1:
         comps = {}
         for name in [n for n in COMPONENTS if n != args.workload]:

@@ -110,3 +110,10 @@ def test_reference_arm_runs_on_the_host_and_prints_the_contract_line():
     assert line["impl"] == "reference" and line["gpu_launches"] == 0 and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["config"]["workload"] == "decode"
+
+
+def test_all_core_baseline_runs_the_oracle_in_threads():
+    r = bench.cpu_baseline_all_cores("decode", budget_s=1.0)
+    assert r["kind"] == "oracle" and r["unit"] == "GB/s" and r["value"] > 0
+    assert r["cores"] == bench.host_threads() >= 1
+    assert bench.cpu_baseline_all_cores("gemm", budget_s=0.1) is None
