@@ -560,6 +560,35 @@ class GemmPermWork(GemmWork):
 
     def step(self):
         self.w4.gemm_w4_permuted(self.A, self.B, self.s, out=self.C)
+def torch_matmul_context(work, steps):
+    """Context only, not a product path: the packed B dequantised to bf16 once
+    with torch ops (untimed), then torch.matmul (cuBLAS) timed with CUDA
+    events over `steps` calls.  Returns TFLOP/s, or an error note (this bar
+    never fails the benchmark)."""
+    try:
+        B = work.B
+        K2, N = B.shape
+        W = torch.empty((2 * K2, N), dtype=torch.bfloat16, device=B.device)
+        W[0::2] = (B & 0x0F).to(torch.bfloat16)   # even k in the low nibble
+        W[1::2] = (B >> 4).to(torch.bfloat16)
+        W = (W - work.z[None, :]) * work.s[None, :]
+        out = torch.empty((work.M, N), dtype=torch.bfloat16, device=B.device)
+        for _ in range(3):
+            torch.matmul(work.A, W, out=out)
+        torch.cuda.synchronize()
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record()
+        for _ in range(steps):
+            torch.matmul(work.A, W, out=out)
+        end.record()
+        torch.cuda.synchronize()
+        sec = start.elapsed_time(end) / 1e3 / steps
+        del W, out
+        torch.cuda.empty_cache()
+        return {"value": work.flops / sec / 1e12, "unit": "TFLOP/s",
+                "note": "context: B dequantised to bf16 once (untimed), then torch.matmul (cuBLAS)"}
+    except Exception as e:   # noqa: BLE001 -- a context bar must not fail the run
+        return {"value": None, "error": "%s: %s" % (type(e).__name__, str(e)[:200])}
 
 
 def make_work(w4, name):
@@ -1021,6 +1050,8 @@ def run_ours(args, world, rank):
         "clocks": clocks,
         "e2e": {"value": e2e_val, "unit": unit_of(work), "h2d_bytes_per_step": hb, "d2h_bytes_per_step": ob},
     }
+    if kind == "gemm":
+        line["context_torch_matmul"] = torch_matmul_context(work, max(3, min(args.steps, 20)))
     if kind == "quant8" or (kind == "quant" and not WORKLOADS[args.workload].get("fused", True)):
         line["roofline"]["note"] = "two kernels per step (quantise, then permute); achieved = step bytes / step time"
     if kind in ("w4a8", "ptq1"):
@@ -1042,6 +1073,8 @@ def run_ours(args, world, rank):
             comps[name] = {"value": rate(wk, per), "unit": unit_of(wk), "ms_per_step": per * 1e3,
                            "frac": rl["frac"], "bound": rl["bound"], "traffic": rl["traffic"],
                            "config": {k: v for k, v in cfg.items() if k != "kind"}}
+            if cfg["kind"] == "gemm":
+                comps[name]["context_torch_matmul"] = torch_matmul_context(wk, 10)
             del wk
             torch.cuda.empty_cache()
         line["components"] = comps

@@ -117,3 +117,19 @@ def test_all_core_baseline_runs_the_oracle_in_threads():
     assert r["kind"] == "oracle" and r["unit"] == "GB/s" and r["value"] > 0
     assert r["cores"] == bench.host_threads() >= 1
     assert bench.cpu_baseline_all_cores("gemm", budget_s=0.1) is None
+
+
+def test_matmul_context_bar_never_raises():
+    """The cuBLAS context bar reports an error note instead of failing the
+    run (here: no GPU for its CUDA events)."""
+    import types
+
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    work = types.SimpleNamespace(B=torch.randint(0, 256, (32, 16), dtype=torch.uint8),
+                                 A=torch.zeros((8, 64), dtype=torch.bfloat16),
+                                 s=torch.ones(16, dtype=torch.bfloat16), z=torch.full((16,), 8.0, dtype=torch.bfloat16),
+                                 M=8, flops=2 * 8 * 16 * 64)
+    r = bench.torch_matmul_context(work, 3)
+    assert r["value"] is None and "error" in r
