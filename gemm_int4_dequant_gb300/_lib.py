@@ -40,6 +40,8 @@ def load():
     lib.w4_status_string.restype = ctypes.c_char_p
     lib.w4_device_error.argtypes = [P]
     lib.w4_device_error.restype = I
+    lib.w4_selftest_wait_timeout.argtypes = [P, P]
+    lib.w4_selftest_wait_timeout.restype = I
     lib.quantize_pack_int4.argtypes = [P, P, P, I64, I64, P]
     lib.quantize_pack_int4.restype = I
     lib.permute_int4.argtypes = [P, P, I64, I64, P]

@@ -32,6 +32,8 @@ w4_status run_mmvq_ptq1_1(const void* sblocks, const void* codebook, int64_t n_c
                           int64_t C, cudaStream_t s);
 bool ptq1_fits(int64_t C, int64_t K, bool super);
 int take_device_error_ptq1();
+w4_status run_selftest_wait_timeout(int* waited, cudaStream_t s);
+int take_device_error_selftest();
 w4_status run_gemm_w8(const void* A, const void* q, const float* scale, void* C, int64_t M, int64_t N, int64_t K,
                       cudaStream_t s);
 w4_status run_gemm_w4_permuted(const void* A, const void* permuted, const float* scale, void* C, int64_t M,
@@ -98,8 +100,9 @@ int w4_device_error(void* stream) {
     const int b = take_device_error_gemv();
     const int c = take_device_error_quant();
     const int e = take_device_error_ptq1();
-    if (a < 0 || b < 0 || c < 0 || e < 0) return -1;
-    return a != 0 ? a : b != 0 ? b : c != 0 ? c : e;
+    const int f = take_device_error_selftest();
+    if (a < 0 || b < 0 || c < 0 || e < 0 || f < 0) return -1;
+    return a != 0 ? a : b != 0 ? b : c != 0 ? c : e != 0 ? e : f;
 }
 
 const char* w4_status_string(w4_status status) {
@@ -273,6 +276,12 @@ w4_status gemm_w4_permuted(const void* A, const void* permuted, const float* sca
     if (!device_is_sm103()) return W4_ERR_DEVICE;
     if (K == 0) return launch_status(cudaMemsetAsync(C, 0, M * N * 2, (cudaStream_t)stream));
     return run_gemm_w4_permuted(A, permuted, scale, C, M, N, K, (cudaStream_t)stream);
+}
+
+w4_status w4_selftest_wait_timeout(int* waited, void* stream) {
+    if (!waited) return W4_ERR_NULL;
+    if (!device_is_sm103()) return W4_ERR_DEVICE;
+    return run_selftest_wait_timeout(waited, (cudaStream_t)stream);
 }
 
 w4_status gemm_w4(const void* A, const void* B, const void* scale, const void* zero, void* C, int64_t M, int64_t N,

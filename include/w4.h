@@ -99,6 +99,15 @@ const char* w4_status_string(w4_status status);
 int w4_device_error(void* stream);
 
 /*
+ * w4_selftest_wait_timeout -- test of the device error path: one CTA runs the
+ * library's bounded mbarrier wait on a barrier that nothing completes.  The
+ * wait gives up after its limit (about two seconds), the kernel writes 0 to
+ * *waited (DEVICE int, 1 if the wait had completed) and records code 1 for
+ * w4_device_error; the context stays usable.  Nothing faults, traps or hangs.
+ */
+w4_status w4_selftest_wait_timeout(int* waited, void* stream);
+
+/*
  * quantize_pack_int4 -- symmetric per-column int4 quantisation + column pack.
  *
  *   scale[n]  = max_k |W[k][n]| / 7                (IEEE fp32 division)

@@ -29,7 +29,7 @@ def test_header_declares_the_hot_path():
     for fn in ("quantize_pack_int4", "permute_int4", "quantize_pack_permute_int4", "gemv_w4", "gemv_w4_permuted",
                "gemm_w4", "quantize_int8", "permute_int8", "gemv_w8", "gemm_w8", "gemm_w4_permuted", "quantize_q8_1_pt", "gemv_w4a8", "mmvq_ptq1_0",
                "mmvq_ptq1_1", "ptq1_1_codebook", "ptq1_1_encode",
-               "w4_status_string", "w4_abi_version", "w4_device_error"):
+               "w4_status_string", "w4_abi_version", "w4_device_error", "w4_selftest_wait_timeout"):
         assert fn in names
 
 

@@ -549,3 +549,22 @@ def test_quantise_permute_then_gemm(w4):
     s_ref, p_ref = oracle.quantize_pack(np_bits(W))
     ref, ref_abs = oracle.gemm_packed_full(np_bits(A), p_ref, s_ref)
     assert not parity_violations(C.float().cpu().numpy(), ref, ref_abs, BF16_TOL, bf16_out=True).any()
+
+
+
+# ---------------------------------------------------------------------------
+# the device error path
+# ---------------------------------------------------------------------------
+
+def test_bounded_wait_gives_up_reports_and_leaves_the_context_usable(w4):
+    """A wait on a barrier nothing completes ends after its limit with error
+    code 1 (read and cleared by w4_device_error); the next calls work."""
+    from gemm_int4_dequant_gb300 import _lib as L
+    waited = torch.full((1,), 7, dtype=torch.int32, device=_dev())
+    assert w4.device_error() == 0
+    st = L.load().w4_selftest_wait_timeout(waited.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    assert st == L.W4_OK
+    assert w4.device_error() == 1
+    assert int(waited.item()) == 0
+    assert w4.device_error() == 0
+    _check_gemv(w4, 300, 4096, 2, "bf16", seed=9)
