@@ -67,9 +67,22 @@ WORKLOADS = {
     # quantize_int8 + permute_int8 of one 8192x8192 weight
     "w8_decode": dict(kind="gemv8", N=17280, K=5120, C=1),
     "w8_quant": dict(kind="quant8", K=8192, N=8192),
+    "w8_gemm": dict(kind="gemm8", M=8192, N=8192, K=8192),
+    # the GEMM over permute_int4's output (fp32 scale, no zero point)
+    "gemm_perm": dict(kind="gemmp", M=8192, N=8192, K=8192),
+    # W4A8: x quantised to block_q8_1 in the PT planes, then the int4 GEMV
+    # with integer dots (two kernels per step)
+    "w4a8_decode": dict(kind="w4a8", N=17280, K=5120, C=1),
+    "w4a8_c8": dict(kind="w4a8", N=5120, K=17280, C=8),
+    # ternary PTQ1_0 weights: x quantised to block_q8_1 / PT, then the MMVQ
+    "ptq1_decode": dict(kind="ptq1", N=17280, K=5120, C=1),
+    "ptq1_c8": dict(kind="ptq1", N=5120, K=17280, C=8),
+    # the same weights as PTQ1_1 superblocks (the library's host conversion)
+    "ptq1_1_decode": dict(kind="ptq1", N=17280, K=5120, C=1, superblocks=True),
 }
 COMPONENTS = ["c4", "c8", "c4s", "c8s", "c4_perm", "c8_perm", "c4s_perm", "c8s_perm", "quant", "quant_2call", "gemm",
-              "w8_decode", "w8_quant"]
+              "w8_decode", "w8_quant", "w8_gemm", "gemm_perm", "w4a8_decode", "w4a8_c8",
+              "ptq1_decode", "ptq1_c8", "ptq1_1_decode"]
 
 
 def load_peaks():
@@ -105,6 +118,19 @@ def gemv8_bytes(N, K, C):
 def quant8_bytes(K, N):
     # quantize_int8: read W, write q + scale; permute_int8: read + write q
     return (2 * K * N + K * N + 4 * N) + 2 * K * N
+
+
+def w4a8_bytes(N, K, C):
+    # weights + bf16 scale and zero + x read by the quantiser + the PT
+    # activations written and read back + d
+    return N * K // 2 + 4 * N + 2 * C * K + 2 * C * 144 * (K // 128) + 2 * C * N
+
+
+def ptq1_bytes(N, K, C, superblocks=False):
+    # PTQ1_0 blocks (or PTQ1_1 superblocks) + x read by the quantiser + the
+    # PT activations written and read back + d (fp32)
+    w = N * -(-K // 1024) * 216 if superblocks else N * (K // 128) * 28
+    return w + 2 * C * K + 2 * C * 144 * (K // 128) + 4 * C * N
 
 
 def gemm_bytes(M, N, K):
@@ -354,6 +380,80 @@ class Gemv8Work:
         return "rotating %d int8 weight copies (%.0f MB > 2x L2)" % (self.R, self.R * self.N * self.K / 1e6)
 
 
+class W4a8Work:
+    """quantize_q8_1_pt of x, then gemv_w4a8 over rotating weight copies."""
+
+    def __init__(self, w4, N, K, C, seed=0):
+        g = synth.gemv_inputs(N, K, C, act="bf16", seed=seed)
+        self.g = g
+        dev = torch.device("cuda")
+        self.R = copies_for(N * K // 2)
+        self.q = [g.qweight.to(dev) for _ in range(self.R)]
+        self.s, self.z, self.x = g.scale.to(dev), g.zero.to(dev), g.x.to(dev)
+        self.pt = torch.empty((C, 144 * (K // 128)), dtype=torch.uint8, device=dev)
+        self.d = torch.empty((C, N), dtype=torch.bfloat16, device=dev)
+        self.w4 = w4
+        self.i = 0
+        self.N, self.K, self.C = N, K, C
+        self.bytes = w4a8_bytes(N, K, C)
+        self.flops = 2 * N * K * C
+        self.launches_per_step = 2
+
+    def run(self, x, i):
+        self.w4.quantize_q8_1_pt(x, out=self.pt)
+        self.w4.gemv_w4a8(self.q[i % self.R], self.s, self.z, self.pt, out=self.d)
+
+    def step(self):
+        self.run(self.x, self.i)
+        self.i += 1
+
+    def l2_note(self):
+        return "rotating %d weight copies (%.0f MB > 2x L2)" % (self.R, self.R * self.N * self.K / 2 / 1e6)
+
+
+class Ptq1Work:
+    """quantize_q8_1_pt of x, then mmvq_ptq1_0 over rotating copies of a
+    PTQ1_0 tensor."""
+
+    def __init__(self, w4, N, K, C, seed=0, superblocks=False):
+        dev = torch.device("cuda")
+        blocks = synth.ptq1_0_blocks(N, K, seed=seed)
+        self.superblocks = superblocks
+        if superblocks:
+            sb, code, ei, ep = w4.ptq1_1_encode(blocks)   # host conversion, untimed
+            blocks = sb
+            self.tables = [torch.from_numpy(a).to(dev) for a in (code, ei, ep)]
+        self.R = copies_for(blocks.nbytes)
+        self.q = [torch.from_numpy(blocks).to(dev) for _ in range(self.R)]
+        self.x_cpu = synth.gemv_inputs(1, K, C, act="bf16", seed=seed).x
+        self.x = self.x_cpu.to(dev)
+        self.pt = torch.empty((C, 144 * (K // 128)), dtype=torch.uint8, device=dev)
+        self.d = torch.empty((C, N), dtype=torch.float32, device=dev)
+        self.w4 = w4
+        self.i = 0
+        self.N, self.K, self.C = N, K, C
+        self.bytes = ptq1_bytes(N, K, C, superblocks)
+        self.flops = 2 * N * K * C
+        self.launches_per_step = 2
+
+    def run(self, x, i):
+        self.w4.quantize_q8_1_pt(x, out=self.pt)
+        if self.superblocks:
+            code, ei, ep = self.tables
+            self.w4.mmvq_ptq1_1(self.q[i % self.R], code, ei, ep, self.pt, self.K, out=self.d)
+        else:
+            self.w4.mmvq_ptq1_0(self.q[i % self.R], self.pt, out=self.d)
+
+    def step(self):
+        self.run(self.x, self.i)
+        self.i += 1
+
+    def l2_note(self):
+        per = self.q[0].numel()
+        return "rotating %d %s copies (%.0f MB > 2x L2)" % (self.R, "PTQ1_1" if self.superblocks else "PTQ1_0",
+                                                          self.R * per / 1e6)
+
+
 class Quant8Work:
     """quantize_int8 + permute_int8 of one weight."""
 
@@ -423,6 +523,43 @@ class GemmWork:
         return "A+C are %.0f MB > L2" % ((self.M * self.K + self.M * self.N) * 2 / 1e6)
 
 
+class Gemm8Work(GemmWork):
+    """gemm_w8: bf16 A times quantize_int8's matrix."""
+
+    def __init__(self, w4, M, N, K, seed=0):
+        dev = torch.device("cuda")
+        gi = synth.int8_gemv_inputs(N, K, 1, seed=seed)
+        self.A = synth.gemm_inputs(M, 16, K, seed=seed + 1).A.to(dev)
+        self.B, self.s = gi.q.to(dev), gi.scale.to(dev)
+        self.C = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        self.w4 = w4
+        self.M, self.N, self.K = M, N, K
+        self.bytes = M * K * 2 + K * N + M * N * 2 + 4 * N
+        self.flops = gemm_flops(M, N, K)
+        self.launches_per_step = 1
+
+    def step(self):
+        self.w4.gemm_w8(self.A, self.B, self.s, out=self.C)
+
+
+class GemmPermWork(GemmWork):
+    """gemm_w4_permuted over weights permuted once at setup (untimed)."""
+
+    def __init__(self, w4, M, N, K, seed=0):
+        dev = torch.device("cuda")
+        g = synth.packed_gemv_inputs(N, K, 1, seed=seed)
+        self.A = synth.gemm_inputs(M, 16, K, seed=seed + 1).A.to(dev)
+        self.B = w4.permute_int4(g.packed.to(dev))
+        self.s = g.scale.to(dev)
+        self.C = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        self.w4 = w4
+        self.M, self.N, self.K = M, N, K
+        self.bytes = gemm_bytes(M, N, K)
+        self.flops = gemm_flops(M, N, K)
+        self.launches_per_step = 1
+
+    def step(self):
+        self.w4.gemm_w4_permuted(self.A, self.B, self.s, out=self.C)
 def torch_matmul_context(work, steps):
     """Context only, not a product path: the packed B dequantised to bf16 once
     with torch ops (untimed), then torch.matmul (cuBLAS) timed with CUDA
@@ -467,6 +604,14 @@ def make_work(w4, name):
         return Gemv8Work(w4, **cfg)
     if kind == "quant8":
         return Quant8Work(w4, **cfg)
+    if kind == "w4a8":
+        return W4a8Work(w4, **cfg)
+    if kind == "gemm8":
+        return Gemm8Work(w4, **cfg)
+    if kind == "gemmp":
+        return GemmPermWork(w4, **cfg)
+    if kind == "ptq1":
+        return Ptq1Work(w4, **cfg)
     return GemmWork(w4, **cfg)
 
 
@@ -509,15 +654,18 @@ def soak(g, stream, seconds):
 
 def e2e_gemv(w4, work, steps, world):
     """Public API, host buffers: x from pinned host memory in, d back out."""
-    x_host = work.g.x.clone().pin_memory()
-    d_host = torch.empty((work.C, work.N), dtype=torch.bfloat16).pin_memory()
+    x_host = (work.x_cpu if isinstance(work, Ptq1Work) else work.g.x).clone().pin_memory()
+    d_host = torch.empty((work.C, work.N), dtype=work.d.dtype).pin_memory()
     x_dev = torch.empty_like(work.x)
     stream = torch.cuda.current_stream()
     perm = isinstance(work, GemvPermWork)
     w8 = isinstance(work, Gemv8Work)
+    w4a8 = isinstance(work, (W4a8Work, Ptq1Work))
 
     def call(i):
-        if perm:
+        if w4a8:
+            work.run(x_dev, i)
+        elif perm:
             w4.gemv_w4_permuted(work.q[i % work.R], work.s, x_dev, out=work.d)
         elif w8:
             w4.gemv_w8(work.q[i % work.R], work.s, x_dev, out=work.d)
@@ -541,7 +689,7 @@ def e2e_gemv(w4, work, steps, world):
     torch.cuda.synchronize()
     barrier(world)
     sec = max_over_ranks(start.elapsed_time(end) / 1e3, world)
-    return sec, x_host.numel() * 2, d_host.numel() * 2
+    return sec, x_host.numel() * 2, d_host.numel() * d_host.element_size()
 
 
 def e2e_generic(work, steps, world):
@@ -648,6 +796,37 @@ def cpu_baseline(name, budget_s=10.0):
         return {"value": flops / t_total / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
                 "sample": "%d sampled outputs of the 8192^3 GEMM (fp64 C oracle, single thread), %.1f s" %
                           (n_out, t_total)}
+    if cfg["kind"] == "gemmp":
+        M, N, K = cfg["M"], cfg["N"], cfg["K"]
+        g = synth.packed_gemv_inputs(N, K, 1, seed=0)
+        A = np_bits(synth.gemm_inputs(M, 16, K, seed=1).A)
+        rng = np.random.default_rng(0)
+        n_out, t_total = 0, 0.0
+        while t_total < budget_s:
+            mi, ni = rng.integers(0, M, 256), rng.integers(0, N, 256)
+            t0 = time.perf_counter()
+            oracle.gemm_packed_at(A, g.packed.numpy(), g.scale.numpy(), mi, ni)
+            t_total += time.perf_counter() - t0
+            n_out += 256
+        return {"value": 2.0 * K * n_out / t_total / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+                "sample": "%d sampled outputs of the 8192^3 GEMM over the packed matrix (fp64 C oracle, single "
+                          "thread), %.1f s" % (n_out, t_total)}
+    if cfg["kind"] == "gemm8":
+        M, N, K = cfg["M"], cfg["N"], cfg["K"]
+        gi = synth.int8_gemv_inputs(N, K, 1, seed=0)
+        A = np_bits(synth.gemm_inputs(M, 16, K, seed=1).A)
+        rng = np.random.default_rng(0)
+        n_out, t_total = 0, 0.0
+        while t_total < budget_s:
+            mi, ni = rng.integers(0, M, 256), rng.integers(0, N, 256)
+            t0 = time.perf_counter()
+            oracle.gemm_int8_at(A, gi.q.numpy(), gi.scale.numpy(), mi, ni)
+            t_total += time.perf_counter() - t0
+            n_out += 256
+        flops = 2.0 * K * n_out
+        return {"value": flops / t_total / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+                "sample": "%d sampled outputs of the 8192^3 int8 GEMM (fp64 C oracle, single thread), %.1f s" %
+                          (n_out, t_total)}
     if cfg["kind"] == "gemv8":
         g = synth.int8_gemv_inputs(cfg["N"], cfg["K"], cfg["C"], seed=0)
         q, scale, xb = g.q.numpy(), g.scale.numpy(), np_bits(g.x)
@@ -665,6 +844,47 @@ def cpu_baseline(name, budget_s=10.0):
                 "cores": 1, "kind": "oracle",
                 "sample": "%d columns of the %dx%d C=%d int8 GEMV (fp64 C oracle, single thread), %.1f s" %
                           (done, cfg["N"], cfg["K"], cfg["C"], t_total)}
+    if cfg["kind"] == "w4a8":
+        g = synth.gemv_inputs(cfg["N"], cfg["K"], cfg["C"], act="bf16", seed=0)
+        qw, s, z, xb = np_bits(g.qweight), np_bits(g.scale), np_bits(g.zero), np_bits(g.x)
+        N, K = cfg["N"], cfg["K"]
+        done, t_total, r0 = 0, 0.0, 0
+        rows = 256
+        while t_total < budget_s:
+            r1 = min(N, r0 + rows)
+            t0 = time.perf_counter()
+            pt = oracle.quantize_q8_1_pt(xb)
+            oracle.gemv_w4a8(qw, s, z, pt, K, rows=(r0, r1))
+            t_total += time.perf_counter() - t0
+            done += r1 - r0
+            r0 = 0 if r1 >= N else r1
+        return {"value": w4a8_bytes(N, K, cfg["C"]) * done / N / t_total / 1e9, "unit": "GB/s", "cores": 1,
+                "kind": "oracle",
+                "sample": "%d rows of the %dx%d C=%d W4A8 GEMV, x quantised each time (fp64 C oracle, single "
+                          "thread), %.1f s" % (done, N, K, cfg["C"], t_total)}
+    if cfg["kind"] == "ptq1":
+        N, K = cfg["N"], cfg["K"]
+        sup = cfg.get("superblocks", False)
+        blocks = synth.ptq1_0_blocks(N, K, seed=0)
+        wsb = oracle.ptq1_1_encode(blocks) if sup else None
+        xb = np_bits(synth.gemv_inputs(1, K, cfg["C"], act="bf16", seed=0).x)
+        done, t_total, r0 = 0, 0.0, 0
+        rows = 256
+        while t_total < budget_s:
+            r1 = min(N, r0 + rows)
+            t0 = time.perf_counter()
+            pt = oracle.quantize_q8_1_pt(xb)
+            if sup:
+                oracle.mmvq_ptq1_1(wsb, pt, rows=(r0, r1))
+            else:
+                oracle.mmvq_ptq1_0(blocks, pt, rows=(r0, r1))
+            t_total += time.perf_counter() - t0
+            done += r1 - r0
+            r0 = 0 if r1 >= N else r1
+        return {"value": ptq1_bytes(N, K, cfg["C"], sup) * done / N / t_total / 1e9, "unit": "GB/s", "cores": 1,
+                "kind": "oracle",
+                "sample": "%d rows of the %dx%d C=%d ternary MMVQ, x quantised each time (fp64 C oracle, single "
+                          "thread), %.1f s" % (done, N, K, cfg["C"], t_total)}
     if cfg["kind"] == "quant8":
         K, N = cfg["K"], cfg["N"]
         W = np_bits(synth.quant_inputs(K, N, seed=0))
@@ -757,10 +977,19 @@ def dtype_of(name):
         return "bf16 x / uint4 weights (bf16 MMA), fp32 accumulate"
     if cfg["kind"] == "gemm":
         return "bf16 A / uint4 B (bf16 tcgen05 MMA), fp32 accumulate"
+    if cfg["kind"] == "gemm8":
+        return "bf16 A / int8 B (bf16 tcgen05 MMA), fp32 accumulate"
+    if cfg["kind"] == "gemmp":
+        return "bf16 A / permuted int4 B (bf16 tcgen05 MMA), fp32 accumulate"
     if cfg["kind"] == "gemv8":
         return "bf16 x / int8 weights (fp32 FMA)"
     if cfg["kind"] == "quant8":
         return "bf16 in, int8 out (fp32 division)"
+    if cfg["kind"] == "w4a8":
+        return "x quantised to int8 (block_q8_1) / uint4 weights, int32 dp4a dots, fp32 accumulate"
+    if cfg["kind"] == "ptq1":
+        fmt = "PTQ1_1" if cfg.get("superblocks") else "PTQ1_0"
+        return "x quantised to int8 (block_q8_1) / ternary %s weights, int32 dp4a dots, fp32 accumulate" % fmt
     return "bf16 in, int4 out (fp32 arithmetic)"
 
 
@@ -803,7 +1032,7 @@ def run_ours(args, world, rank):
         soak(g, stream, 2.0)
         sec2, _, _ = time_graph(work, args.steps, 0, world)
     clocks = cs.summary()
-    if kind in ("gemv", "gemv8"):
+    if kind in ("gemv", "gemv8", "w4a8", "ptq1"):
         e2e_sec, hb, ob = e2e_gemv(w4, work, args.steps, world)
     else:
         e2e_sec, hb, ob = e2e_generic(work, max(2, min(args.steps, 10)), world)
@@ -825,6 +1054,9 @@ def run_ours(args, world, rank):
         line["context_torch_matmul"] = torch_matmul_context(work, max(3, min(args.steps, 20)))
     if kind == "quant8" or (kind == "quant" and not WORKLOADS[args.workload].get("fused", True)):
         line["roofline"]["note"] = "two kernels per step (quantise, then permute); achieved = step bytes / step time"
+    if kind in ("w4a8", "ptq1"):
+        line["roofline"]["note"] = ("two kernels per step (quantise x, then the GEMV); achieved = step bytes / "
+                                    "step time")
     if rank == 0 and world == 1:
         line["cpu_baseline"] = cpu_baseline(args.workload, budget_s=args.cpu_seconds)
         every_core = cpu_baseline_all_cores(args.workload, budget_s=args.cpu_seconds)

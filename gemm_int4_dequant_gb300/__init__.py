@@ -15,6 +15,12 @@ in the library's CUDA kernels; there is no CPU or eager fallback.
     quantize_int8(W)                    -> (q [K, N] int8, scale [N] fp32)
     permute_int8(q)                     -> out [N*K] int8 (interleaved)
     gemv_w8(q, scale, x)                -> d [C, N] bf16
+    gemm_w8(A, q, scale)                -> C [M, N] bf16 (bf16 x int8 on the tensor cores)
+    gemm_w4_permuted(A, permuted, scale) -> C [M, N] bf16 (over permute_int4's output)
+    quantize_q8_1_pt(x)                 -> pt [C, 144*K/128] uint8 (block_q8_1 in PT planes)
+    gemv_w4a8(qweight, scale, zero, pt) -> d [C, N] bf16 (int4 weights x int8 activations)
+    mmvq_ptq1_0(blocks, pt)             -> d [C, N] fp32 (ternary PTQ1_0 weights x int8 activations)
+    mmvq_ptq1_1(sblocks, codebook, esc_idx, esc_patt, pt, K) -> d [C, N] fp32 (PTQ1_1 superblocks)
     ptq1_1_encode(blocks)               -> (sblocks, codebook, esc_idx, esc_patt): PTQ1_0 -> PTQ1_1 (host)
 """
 import torch
@@ -23,7 +29,8 @@ from . import _lib
 from ._lib import W4Error, W4_BF16, W4_F32
 
 __all__ = ["quantize_pack_int4", "permute_int4", "quantize_pack_permute_int4", "gemv_w4", "gemv_w4_permuted", "gemm_w4",
-           "quantize_int8", "permute_int8", "gemv_w8", "ptq1_1_encode", "device_error", "W4Error"]
+           "quantize_int8", "permute_int8", "gemv_w8", "gemm_w8", "gemm_w4_permuted", "quantize_q8_1_pt", "gemv_w4a8", "mmvq_ptq1_0", "mmvq_ptq1_1",
+           "ptq1_1_encode", "device_error", "W4Error"]
 
 _lib.load()  # fail loudly at import if the CUDA library is missing
 
@@ -230,6 +237,141 @@ def gemv_w8(q, scale, x, out=None, stream=None):
     st = _lib.load().gemv_w8(q.data_ptr(), scale.data_ptr(), xx.data_ptr(), out.data_ptr(), N, K, C,
                              _stream(stream))
     _lib.check("gemv_w8", st)
+    return out
+
+
+def gemm_w8(A, q, scale, out=None, stream=None):
+    """C[m, n] = scale[n] * sum_k A[m, k] q[k, n]: A bf16 [M, K] (K % 64 == 0),
+    q int8 [K, N] (N % 16 == 0), scale fp32 [N].  Returns bf16 [M, N]."""
+    _need(A, "A", (torch.bfloat16,), 2)
+    _need(q, "q", (torch.int8,), 2)
+    _need(scale, "scale", (torch.float32,), 1)
+    M, K = A.shape
+    if q.shape[0] != K or scale.numel() != q.shape[1]:
+        raise ValueError("shape mismatch")
+    N = q.shape[1]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    _need(out, "out", (torch.bfloat16,))
+    if out.numel() != M * N:
+        raise ValueError("out must hold M*N elements")
+    st = _lib.load().gemm_w8(A.data_ptr(), q.data_ptr(), scale.data_ptr(), out.data_ptr(), M, N, K, _stream(stream))
+    _lib.check("gemm_w8", st)
+    return out
+
+
+def gemm_w4_permuted(A, permuted, scale, out=None, stream=None):
+    """C[m, n] = scale[n] * sum_k A[m, k] q[k, n] with the int4 weights read
+    straight from permute_int4's output (N*K/2 bytes): A bf16 [M, K]
+    (K % 64 == 0), scale fp32 [N] (N % 16 == 0).  Returns bf16 [M, N]."""
+    _need(A, "A", (torch.bfloat16,), 2)
+    _need(permuted, "permuted", (torch.int8, torch.uint8))
+    _need(scale, "scale", (torch.float32,), 1)
+    M, K = A.shape
+    N = scale.numel()
+    if permuted.numel() != N * (K // 2):
+        raise ValueError("permuted must hold N*K/2 bytes")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    _need(out, "out", (torch.bfloat16,))
+    if out.numel() != M * N:
+        raise ValueError("out must hold M*N elements")
+    st = _lib.load().gemm_w4_permuted(A.data_ptr(), permuted.data_ptr(), scale.data_ptr(), out.data_ptr(), M, N, K,
+                                      _stream(stream))
+    _lib.check("gemm_w4_permuted", st)
+    return out
+
+
+def quantize_q8_1_pt(x, out=None, stream=None):
+    """x bf16 [C, K] (K % 128 == 0) as block_q8_1 in the PT planes: uint8
+    [C, 144*K/128] per vector (qs planes 0..7, the (d, s) halves in plane 8)."""
+    _need(x, "x", (torch.bfloat16,))
+    xx = x if x.dim() == 2 else x.reshape(1, -1)
+    C, K = xx.shape
+    if out is None:
+        out = torch.empty((C, 144 * (K // 128)), dtype=torch.uint8, device=x.device)
+    _need(out, "out", (torch.uint8, torch.int8))
+    if out.numel() != C * 144 * (K // 128):
+        raise ValueError("out must hold C*144*K/128 bytes")
+    st = _lib.load().quantize_q8_1_pt(xx.data_ptr(), out.data_ptr(), C, K, _stream(stream))
+    _lib.check("quantize_q8_1_pt", st)
+    return out
+
+
+def gemv_w4a8(qweight, scale, zero, pt, out=None, stream=None):
+    """d[c, r] = scale[r] * sum_b (d_b * sum_{k in b} q[r, k] qs[c, k] - zero[r] s_b):
+    gemv_w4's packed words (int32 [N, K/8]), bf16 scale and zero [N], and x as
+    quantize_q8_1_pt's output (uint8 [C, 144*K/128], C <= 8).  Returns bf16 [C, N]."""
+    _need(qweight, "qweight", (torch.int32, torch.uint32) if hasattr(torch, "uint32") else (torch.int32,), 2)
+    _need(scale, "scale", (torch.bfloat16,), 1)
+    _need(zero, "zero", (torch.bfloat16,), 1)
+    _need(pt, "pt", (torch.uint8, torch.int8))
+    N, K = qweight.shape[0], qweight.shape[1] * 8
+    pp = pt if pt.dim() == 2 else pt.reshape(1, -1)
+    C = pp.shape[0]
+    if K % 128 or pp.shape[1] != 144 * (K // 128) or scale.numel() != N or zero.numel() != N:
+        raise ValueError("shape mismatch")
+    if out is None:
+        out = torch.empty((C, N), dtype=torch.bfloat16, device=qweight.device)
+    _need(out, "out", (torch.bfloat16,))
+    if out.numel() != C * N:
+        raise ValueError("out must hold C*N elements")
+    st = _lib.load().gemv_w4a8(qweight.data_ptr(), scale.data_ptr(), zero.data_ptr(), pp.data_ptr(), out.data_ptr(),
+                               N, K, C, _stream(stream))
+    _lib.check("gemv_w4a8", st)
+    return out
+
+
+def mmvq_ptq1_0(blocks, pt, out=None, stream=None):
+    """d[c, r] = sum_k W[r, k] x[c, k] for ternary W in PTQ1_0 blocks (uint8
+    [N, K/128, 28], or [N, 28*K/128]) and x as quantize_q8_1_pt's output
+    (uint8 [C, 144*K/128], C <= 8).  Returns fp32 [C, N]."""
+    _need(blocks, "blocks", (torch.uint8, torch.int8))
+    _need(pt, "pt", (torch.uint8, torch.int8))
+    N = blocks.shape[0]
+    pp = pt if pt.dim() == 2 else pt.reshape(1, -1)
+    C = pp.shape[0]
+    per_row = blocks.numel() // max(N, 1)
+    if N and (blocks.numel() % N or per_row % 28):
+        raise ValueError("blocks must hold N rows of 28-byte blocks")
+    K = 128 * (per_row // 28) if N else 128 * (pp.shape[1] // 144)
+    if pp.shape[1] != 144 * (K // 128):
+        raise ValueError("pt must hold 144*K/128 bytes per vector")
+    if out is None:
+        out = torch.empty((C, N), dtype=torch.float32, device=pt.device)
+    _need(out, "out", (torch.float32,))
+    if out.numel() != C * N:
+        raise ValueError("out must hold C*N elements")
+    st = _lib.load().mmvq_ptq1_0(blocks.data_ptr(), pp.data_ptr(), out.data_ptr(), N, K, C, _stream(stream))
+    _lib.check("mmvq_ptq1_0", st)
+    return out
+
+
+def mmvq_ptq1_1(sblocks, codebook, esc_idx, esc_patt, pt, K, out=None, stream=None):
+    """mmvq_ptq1_0's product over PTQ1_1 superblocks (uint8 [N, ceil(K/1024),
+    216]) with their codebook (uint8 [n_code, 8]) and escape table (int64
+    [n_esc] ascending superblock indices, uint8 [n_esc, 8]); x as
+    quantize_q8_1_pt's output.  Returns fp32 [C, N]."""
+    for t, name in ((sblocks, "sblocks"), (codebook, "codebook"), (esc_patt, "esc_patt"), (pt, "pt")):
+        _need(t, name, (torch.uint8, torch.int8))
+    _need(esc_idx, "esc_idx", (torch.int64,))
+    N = sblocks.shape[0]
+    pp = pt if pt.dim() == 2 else pt.reshape(1, -1)
+    C = pp.shape[0]
+    if K % 128 or pp.shape[1] != 144 * (K // 128) or sblocks.numel() != N * -(-K // 1024) * 216:
+        raise ValueError("shape mismatch")
+    n_code, n_esc = codebook.numel() // 8, esc_idx.numel()
+    if codebook.numel() % 8 or esc_patt.numel() != 8 * n_esc:
+        raise ValueError("codebook and escape patterns hold 8 exponents each")
+    if out is None:
+        out = torch.empty((C, N), dtype=torch.float32, device=pt.device)
+    _need(out, "out", (torch.float32,))
+    if out.numel() != C * N:
+        raise ValueError("out must hold C*N elements")
+    st = _lib.load().mmvq_ptq1_1(sblocks.data_ptr(), codebook.data_ptr() if n_code else None, n_code,
+                                 esc_idx.data_ptr() if n_esc else None, esc_patt.data_ptr() if n_esc else None, n_esc,
+                                 pp.data_ptr(), out.data_ptr(), N, K, C, _stream(stream))
+    _lib.check("mmvq_ptq1_1", st)
     return out
 
 

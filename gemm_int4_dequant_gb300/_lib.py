@@ -40,6 +40,8 @@ def load():
     lib.w4_status_string.restype = ctypes.c_char_p
     lib.w4_device_error.argtypes = [P]
     lib.w4_device_error.restype = I
+    lib.w4_selftest_wait_timeout.argtypes = [P, P]
+    lib.w4_selftest_wait_timeout.restype = I
     lib.quantize_pack_int4.argtypes = [P, P, P, I64, I64, P]
     lib.quantize_pack_int4.restype = I
     lib.permute_int4.argtypes = [P, P, I64, I64, P]
@@ -58,6 +60,18 @@ def load():
     lib.permute_int8.restype = I
     lib.gemv_w8.argtypes = [P, P, P, P, I64, I64, I64, P]
     lib.gemv_w8.restype = I
+    lib.gemm_w8.argtypes = [P, P, P, P, I64, I64, I64, P]
+    lib.gemm_w8.restype = I
+    lib.gemm_w4_permuted.argtypes = [P, P, P, P, I64, I64, I64, P]
+    lib.gemm_w4_permuted.restype = I
+    lib.quantize_q8_1_pt.argtypes = [P, P, I64, I64, P]
+    lib.quantize_q8_1_pt.restype = I
+    lib.gemv_w4a8.argtypes = [P, P, P, P, P, I64, I64, I64, P]
+    lib.gemv_w4a8.restype = I
+    lib.mmvq_ptq1_0.argtypes = [P, P, P, I64, I64, I64, P]
+    lib.mmvq_ptq1_0.restype = I
+    lib.mmvq_ptq1_1.argtypes = [P, P, I64, P, P, I64, P, P, I64, I64, I64, P]
+    lib.mmvq_ptq1_1.restype = I
     lib.ptq1_1_codebook.argtypes = [P, I64, I64, P, P]
     lib.ptq1_1_codebook.restype = I
     lib.ptq1_1_encode.argtypes = [P, I64, I64, P, I64, P, P, P, I64, P]

@@ -16,7 +16,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libw4.so")
-SOURCES = ["w4_api.cu", "quant_permute.cu", "gemv.cu", "gemv_tma.cu", "gemm_tc.cu", "int8.cu", "ptq1_encode.cpp"]
+SOURCES = ["w4_api.cu", "quant_permute.cu", "gemv.cu", "gemv_tma.cu", "gemm_tc.cu", "int8.cu", "w4a8.cu", "ptq1.cu",
+           "ptq1_encode.cpp", "selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
 

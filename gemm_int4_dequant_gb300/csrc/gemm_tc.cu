@@ -33,6 +33,23 @@
 // puts the columns back in order.
 // Every wait is bounded; on timeout the kernel records an error code in a
 // device word (w4_device_error), stops issuing work, drains and frees TMEM.
+//
+// The kernel is a template over the format of B:
+//   FMT_INT4  the packed uint4 [K/2][N] above, bf16 scale and zero point;
+//   FMT_INT8  the symmetric int8 matrix of quantize_int8 (q[K][N], fp32
+//             scale per column, no zero point): B tiles of 64 rows x 128
+//             bytes, five stages; each int8 becomes bf16 exactly through the
+//             float 2^23 + (q + 128) built by a byte permute (bf16's seven
+//             fraction bits cannot hold q + 128 at one exponent);
+//   FMT_PERM  permute_int4's output (page "[PHI] add int4 weight only quant
+//             kernel ...": two's complement nibbles, fp32 scale, no zero
+//             point).  A 64-k tile of a group of four columns is exactly one
+//             128-byte line of that layout (32 bytes a column), so the tile's
+//             32 groups arrive as one 3-D TMA box, 128B-swizzled.  In word q
+//             of a column's 32 bytes, byte b holds the nibbles of
+//             k = 32 (q / 4) + 2 (q % 4) + {0, 8} (b = 0), {16, 24} (b = 1),
+//             {1, 9} (b = 2), {17, 25} (b = 3), low nibble first (P1's byte
+//             permute and nibble swap).
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -56,20 +73,28 @@ constexpr int BM = 128;                      // A rows per CTA (the pair covers 
 constexpr int BN = 256;                      // tile columns (the pair's MMA N)
 constexpr int BNH = BN / 2;                  // B columns held by each CTA
 constexpr int BK = 64;
-constexpr int STAGES = 6;
 constexpr int THREADS = 448;
 constexpr int A_BYTES = BM * BK * 2;         // 16 KB
-constexpr int BP_BYTES = (BK / 2) * BNH;     // 4 KB packed
 constexpr int BD_BYTES = BK * BNH * 2;       // 16 KB dequantised
-constexpr int OFF_A = 0;
-constexpr int OFF_BD = OFF_A + STAGES * A_BYTES;
-constexpr int OFF_BP = OFF_BD + STAGES * BD_BYTES;
-constexpr int OFF_BAR = OFF_BP + STAGES * BP_BYTES;
-constexpr int NUM_BARS = 4 * STAGES + 4;
-constexpr int OFF_TMEM_SLOT = OFF_BAR + NUM_BARS * 8;
-constexpr int OFF_ABORT = OFF_TMEM_SLOT + 4;
-constexpr int SMEM_USED = OFF_ABORT + 4;
-constexpr int SMEM_BYTES = SMEM_USED + 1024;  // slack to align the base to 1 KB
+
+// Shared-memory layout per B format: packed int4 (4 KB a stage, six
+// stages) or int8 (8 KB a stage, five stages).
+constexpr int FMT_INT4 = 0, FMT_INT8 = 1, FMT_PERM = 2;
+
+template <int FMT>
+struct Lay {
+    static constexpr bool I8 = FMT == FMT_INT8;
+    static constexpr int STAGES = I8 ? 5 : 6;
+    static constexpr int BP_BYTES = I8 ? BK * BNH : (BK / 2) * BNH;
+    static constexpr int OFF_A = 0;
+    static constexpr int OFF_BD = OFF_A + STAGES * A_BYTES;
+    static constexpr int OFF_BP = OFF_BD + STAGES * BD_BYTES;
+    static constexpr int OFF_BAR = OFF_BP + STAGES * BP_BYTES;
+    static constexpr int NUM_BARS = 4 * STAGES + 4;
+    static constexpr int OFF_TMEM_SLOT = OFF_BAR + NUM_BARS * 8;
+    static constexpr int OFF_ABORT = OFF_TMEM_SLOT + 4;
+    static constexpr int SMEM_BYTES = OFF_ABORT + 4 + 1024;   // slack to align the base to 1 KB
+};
 constexpr uint32_t TMEM_COLS = 512;            // two accumulators of 256 columns
 constexpr int EPI_WARP0 = 10;                   // warps 10..13
 constexpr int DEQ_WARPS = 8;
@@ -106,10 +131,38 @@ __device__ __forceinline__ void unpack_word(uint32_t w, uint32_t& e0, uint32_t& 
     o1 = and_or(w >> 12, mask, magic);
 }
 
+// Four int8 (one word) -> bf16 pairs in shared-memory column order (c0, c2)
+// and (c1, c3), exact.
+__device__ __forceinline__ void i8_word_to_bf16(uint32_t w, uint32_t& p02, uint32_t& p13) {
+    const uint32_t wx = w ^ 0x80808080u;
+    float f[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) f[j] = __uint_as_float(__byte_perm(wx, 0x4B000000u, 0x7540u | j)) - 8388736.0f;
+    const __nv_bfloat162 a = __floats2bfloat162_rn(f[0], f[2]);
+    const __nv_bfloat162 b = __floats2bfloat162_rn(f[1], f[3]);
+    p02 = *reinterpret_cast<const uint32_t*>(&a);
+    p13 = *reinterpret_cast<const uint32_t*>(&b);
+}
+
+// 3-D tiled TMA load into this CTA's shared memory.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::
+            "r"(dst),
+        "l"(map), "r"(x), "r"(y), "r"(z), "r"(bar)
+        : "memory");
+}
+
+template <int FMT>
 __global__ void __launch_bounds__(THREADS, 1)
 gemm_w4_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-                  const __nv_bfloat16* __restrict__ scale, const __nv_bfloat16* __restrict__ zero,
+                  const void* __restrict__ scale_p, const __nv_bfloat16* __restrict__ zero,
                   __nv_bfloat16* __restrict__ C, int M, int N, int K, int tiles_n, int num_tiles) {
+    using L = Lay<FMT>;
+    constexpr bool I8 = FMT == FMT_INT8, PERM = FMT == FMT_PERM;
+    constexpr int STAGES = L::STAGES, BP_BYTES = L::BP_BYTES;
+    constexpr int OFF_A = L::OFF_A, OFF_BD = L::OFF_BD, OFF_BP = L::OFF_BP, OFF_BAR = L::OFF_BAR;
+    constexpr int OFF_TMEM_SLOT = L::OFF_TMEM_SLOT, OFF_ABORT = L::OFF_ABORT;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -175,7 +228,10 @@ gemm_w4_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
                     if (round > 0 && !mbar_wait_fast(empty(s), (round - 1) & 1, abort_flag)) { ok = false; break; }
                     mbar_arrive_expect_tx(full_tma(s), bytes);
                     if (load_a) tma_load_2d(base + OFF_A + s * A_BYTES, &tmap_a, kt * BK, mr, full_tma(s));
-                    if (load_b) tma_load_2d(base + OFF_BP + s * BP_BYTES, &tmap_b, nh, kt * (BK / 2), full_tma(s));
+                    if (load_b && PERM)
+                        tma_load_3d(base + OFF_BP + s * BP_BYTES, &tmap_b, 0, kt, nh / 4, full_tma(s));
+                    else if (load_b)
+                        tma_load_2d(base + OFF_BP + s * BP_BYTES, &tmap_b, nh, kt * (I8 ? BK : BK / 2), full_tma(s));
                     issued = g + 1;
                 }
             }
@@ -230,6 +286,75 @@ gemm_w4_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
                     umma_commit_pair(empty(s), 0x3);
                 }
                 if (ok) umma_commit_pair(acc_full(b), 0x3);
+            }
+        }
+    } else if (warp < EPI_WARP0 && I8) {
+        // ---------------- dequant, int8 (warps 2..9) ----------------
+        // thread: 8 of this CTA's 128 columns, every 16th of the tile's 64 rows
+        const int t = threadIdx.x - 64;          // 0..255
+        const int nl = (t & 15) * 8;
+        const int k_lane = t >> 4;               // 0..15
+        bool ok = true;
+        for (int it = 0; it < my_tiles && ok; ++it) {
+            for (int kt = 0; kt < num_kt; ++kt) {
+                const int g = it * num_kt + kt, s = g % STAGES, round = g / STAGES;
+                if (round > 0 && !mbar_wait_fast(empty(s), (round - 1) & 1, abort_flag)) { ok = false; break; }
+                if (!mbar_wait_fast(full_tma(s), round & 1, abort_flag)) { ok = false; break; }
+                const uint8_t* bp = sbase + OFF_BP + s * BP_BYTES;
+                uint8_t* bd = sbase + OFF_BD + s * BD_BYTES;
+#pragma unroll
+                for (int i = 0; i < BK / 16; ++i) {
+                    const int k = k_lane + 16 * i;
+                    const uint2 v = *reinterpret_cast<const uint2*>(bp + k * BNH + nl);
+                    uint32_t h[4];
+                    i8_word_to_bf16(v.x, h[0], h[1]);
+                    i8_word_to_bf16(v.y, h[2], h[3]);
+                    *reinterpret_cast<uint4*>(bd + bd_offset(k, nl)) = make_uint4(h[0], h[1], h[2], h[3]);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(full_deq(s));
+            }
+        }
+    } else if (warp < EPI_WARP0 && PERM) {
+        // ---------------- dequant, permuted layout (warps 2..9) ----------------
+        // warp w takes groups 8 (w % 4) .. + 7 and words 4 (w / 4) .. + 3 of
+        // their lines; with the 128B swizzle the 32 lanes read 32 different
+        // banks for each column
+        const int dw = warp - 2;
+        const int G = 8 * (dw & 3) + (lane & 7);   // column group (4 columns) of this CTA's 32
+        const int q = 4 * (dw >> 2) + (lane >> 3); // word of each column's 32 bytes
+        const uint32_t flip = 0x43084308u, pass = 0x43074307u;   // 136 + q, q two's complement
+        // k of the low / high nibble of byte b of word q
+        const int kb = 32 * (q >> 2) + 2 * (q & 3);
+        const int klo[4] = {kb, kb + 16, kb + 1, kb + 17};
+        bool ok = true;
+        for (int it = 0; it < my_tiles && ok; ++it) {
+            for (int kt = 0; kt < num_kt; ++kt) {
+                const int g = it * num_kt + kt, s = g % STAGES, round = g / STAGES;
+                if (round > 0 && !mbar_wait_fast(empty(s), (round - 1) & 1, abort_flag)) { ok = false; break; }
+                if (!mbar_wait_fast(full_tma(s), round & 1, abort_flag)) { ok = false; break; }
+                const uint8_t* row = sbase + OFF_BP + s * BP_BYTES + 128 * G;
+                uint8_t* bd = sbase + OFF_BD + s * BD_BYTES;
+                uint32_t w[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    w[c] = *reinterpret_cast<const uint32_t*>(row + 16 * ((2 * c + (q >> 2)) ^ (G & 7)) + 4 * (q & 3));
+#pragma unroll
+                for (int b = 0; b < 4; ++b) {
+                    const uint32_t sel = static_cast<uint32_t>(b) | (static_cast<uint32_t>(4 + b) << 8);
+                    const uint32_t z02 = __byte_perm(w[0], w[2], sel), z13 = __byte_perm(w[1], w[3], sel);
+                    const uint32_t lo02 = bsub2(pass_flip_or(z02, pass, flip), flip);
+                    const uint32_t lo13 = bsub2(pass_flip_or(z13, pass, flip), flip);
+                    const uint32_t hi02 = bsub2(pass_flip_or(z02 >> 4, pass, flip), flip);
+                    const uint32_t hi13 = bsub2(pass_flip_or(z13 >> 4, pass, flip), flip);
+                    const int k0 = klo[b], k1 = klo[b] + 8;
+                    *reinterpret_cast<uint2*>(bd + bd_offset(k0, 8 * (G >> 1)) + 8 * (G & 1)) = make_uint2(lo02, lo13);
+                    *reinterpret_cast<uint2*>(bd + bd_offset(k1, 8 * (G >> 1)) + 8 * (G & 1)) = make_uint2(hi02, hi13);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(full_deq(s));
             }
         }
     } else if (warp < EPI_WARP0) {
@@ -319,7 +444,10 @@ gemm_w4_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
                         const int na = nb + 4 * g4;
                         float sc[4];
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) sc[q] = na + q < N ? __bfloat162float(scale[na + q]) : 0.f;
+                        for (int q = 0; q < 4; ++q)
+                            sc[q] = na + q >= N ? 0.f
+                                    : (I8 || PERM) ? static_cast<const float*>(scale_p)[na + q]
+                                         : __bfloat162float(static_cast<const __nv_bfloat16*>(scale_p)[na + q]);
                         const float v0 = __uint_as_float(r[4 * g4 + 0]) * sc[0];
                         const float v1 = __uint_as_float(r[4 * g4 + 2]) * sc[1];
                         const float v2 = __uint_as_float(r[4 * g4 + 1]) * sc[2];
@@ -363,9 +491,14 @@ gemm_w4_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
 
 }  // namespace gemm
 
-w4_status run_gemm(const void* A, const void* B, const void* scale, const void* zero, void* C, int64_t M,
-                   int64_t N, int64_t K, cudaStream_t stream) {
-    using namespace gemm;
+namespace gemm {
+
+template <int FMT>
+w4_status run_gemm_t(const void* A, const void* B, const void* scale, const void* zero, void* C, int64_t M,
+                     int64_t N, int64_t K, cudaStream_t stream) {
+    constexpr bool I8 = FMT == FMT_INT8;
+    constexpr int SMEM_BYTES = Lay<FMT>::SMEM_BYTES;
+    auto kern = gemm_w4_tc_kernel<FMT>;
     if (M > 0x7FFFFFFF || N > 0x7FFFFFFF || K > 0x7FFFFFFF) return W4_ERR_SHAPE;
     const int64_t tiles_m = (M + 2 * BM - 1) / (2 * BM), tiles_n = (N + BN - 1) / BN;
     if (tiles_m * tiles_n > 0x7FFFFFFF) return W4_ERR_SHAPE;
@@ -383,10 +516,21 @@ w4_status run_gemm(const void* A, const void* B, const void* scale, const void* 
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return W4_ERR_CUDA;
     }
-    {
-        cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(K / 2)};
+    if (FMT == FMT_PERM) {
+        // permute_int4's output as [N/4 groups][K/64 lines][128 bytes]
+        cuuint64_t dims[3] = {128, static_cast<cuuint64_t>(K / 64), static_cast<cuuint64_t>(N / 4)};
+        cuuint64_t strides[2] = {128, static_cast<cuuint64_t>(K / 2) * 4};
+        cuuint32_t box[3] = {128, 1, BNH / 4};
+        cuuint32_t estr[3] = {1, 1, 1};
+        if (encode(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(B), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return W4_ERR_CUDA;
+    } else {
+        // int4: packed [K/2][N] bytes; int8: q [K][N]
+        cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(I8 ? K : K / 2)};
         cuuint64_t strides[1] = {static_cast<cuuint64_t>(N)};
-        cuuint32_t box[2] = {BNH, BK / 2};
+        cuuint32_t box[2] = {BNH, I8 ? BK : BK / 2};
         cuuint32_t estr[2] = {1, 1};
         if (encode(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(B), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -394,7 +538,7 @@ w4_status run_gemm(const void* A, const void* B, const void* scale, const void* 
             return W4_ERR_CUDA;
     }
     static int smem_set[64];
-    cudaError_t e = ensure_smem_limit(gemm_w4_tc_kernel, SMEM_BYTES, smem_set);
+    cudaError_t e = ensure_smem_limit(kern, SMEM_BYTES, smem_set);
     if (e != cudaSuccess) return W4_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3(THREADS, 1, 1);
@@ -414,16 +558,33 @@ w4_status run_gemm(const void* A, const void* B, const void* scale, const void* 
     if (max_pairs[dev] == 0) {
         cfg.gridDim = dim3(static_cast<unsigned>(2 * std::max(1, sm_count() / 2)), 1, 1);
         int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, gemm_w4_tc_kernel, &cfg) != cudaSuccess || n <= 0) return W4_ERR_CUDA;
+        if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) return W4_ERR_CUDA;
         max_pairs[dev] = n;
     }
     const int64_t num_tiles = tiles_m * tiles_n;
     const int pairs = static_cast<int>(std::min<int64_t>(num_tiles, max_pairs[dev]));
     cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs), 1, 1);
-    return launch_status(cudaLaunchKernelEx(&cfg, gemm_w4_tc_kernel, ta, tb, static_cast<const __nv_bfloat16*>(scale),
-                                            static_cast<const __nv_bfloat16*>(zero), static_cast<__nv_bfloat16*>(C),
+    return launch_status(cudaLaunchKernelEx(&cfg, kern, ta, tb, scale, static_cast<const __nv_bfloat16*>(zero),
+                                            static_cast<__nv_bfloat16*>(C),
                                             static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
                                             static_cast<int>(tiles_n), static_cast<int>(num_tiles)));
+}
+
+}  // namespace gemm
+
+w4_status run_gemm(const void* A, const void* B, const void* scale, const void* zero, void* C, int64_t M,
+                   int64_t N, int64_t K, cudaStream_t stream) {
+    return gemm::run_gemm_t<gemm::FMT_INT4>(A, B, scale, zero, C, M, N, K, stream);
+}
+
+w4_status run_gemm_w8(const void* A, const void* q, const float* scale, void* C, int64_t M, int64_t N, int64_t K,
+                      cudaStream_t stream) {
+    return gemm::run_gemm_t<gemm::FMT_INT8>(A, q, scale, nullptr, C, M, N, K, stream);
+}
+
+w4_status run_gemm_w4_permuted(const void* A, const void* permuted, const float* scale, void* C, int64_t M,
+                               int64_t N, int64_t K, cudaStream_t stream) {
+    return gemm::run_gemm_t<gemm::FMT_PERM>(A, permuted, scale, nullptr, C, M, N, K, stream);
 }
 
 int take_device_error_gemm() { return take_unit_device_error(); }

@@ -131,9 +131,336 @@ gemv_w8_kernel(const int8_t* __restrict__ q, const float* __restrict__ scale, co
     }
 }
 
+// ---------------------------------------------------------------------------
+// Fast GEMV over q[K][N] (N % 16 == 0): a CTA takes a strip of 128 columns
+// -- one 128-byte line of every row it reads -- and a K-slice; the S CTAs
+// of a cluster split K and the partial sums meet in the first CTA's shared
+// memory.  A thread loads COLS columns of a row at once (16 for C <= 4, 8
+// above, to bound the accumulators); int8 -> fp32 is exact through the
+// float 2^23 + (q + 128) built by a byte permute, minus 2^23 + 128.
+// ---------------------------------------------------------------------------
+
+constexpr int W8F_THREADS = 256;
+constexpr int W8F_STRIP = 128;
+constexpr int W8F_WARPS = W8F_THREADS / 32;
+
+__device__ __forceinline__ float i8_to_f32(uint32_t wx, uint32_t j) {   // wx = w ^ 0x80808080
+    return __uint_as_float(__byte_perm(wx, 0x4B000000u, 0x7540u | j)) - 8388736.0f;
+}
+
+__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ uint32_t map_cluster_u32(uint32_t local, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+    return r;
+}
+
+template <int COLS>
+struct W8Vec;
+template <>
+struct W8Vec<16> {
+    using T = uint4;
+    static __device__ __forceinline__ T load(const int8_t* p) { return ldg_stream_u4(p); }
+    static __device__ __forceinline__ T zero() { return make_uint4(0, 0, 0, 0); }
+    static __device__ __forceinline__ uint32_t word(const T& v, int i) {
+        return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+    }
+};
+template <>
+struct W8Vec<8> {
+    using T = uint2;
+    static __device__ __forceinline__ T load(const int8_t* p) {
+        return make_uint2(ldg_stream_u32(p), ldg_stream_u32(p + 4));
+    }
+    static __device__ __forceinline__ T zero() { return make_uint2(0, 0); }
+    static __device__ __forceinline__ uint32_t word(const T& v, int i) { return i == 0 ? v.x : v.y; }
+};
+
+__host__ __device__ inline size_t w8f_xs_bytes(int C, int64_t Ks) { return (size_t(C) * Ks * 2 + 15) / 16 * 16; }
+__host__ __device__ inline size_t w8f_smem_bytes(int C, int64_t Ks) {
+    return w8f_xs_bytes(C, Ks) + size_t(W8F_WARPS) * C * W8F_STRIP * 4 + size_t(C) * W8F_STRIP * 4;
+}
+
+template <int C, int COLS, int U>
+__global__ void __launch_bounds__(W8F_THREADS)
+gemv_w8_fast_kernel(const int8_t* __restrict__ q, const float* __restrict__ scale,
+                    const __nv_bfloat16* __restrict__ x, __nv_bfloat16* __restrict__ d, int64_t N, int64_t K,
+                    int S) {
+    constexpr int LPR = W8F_STRIP / COLS;   // lanes per row
+    constexpr int RL = W8F_THREADS / LPR;   // rows the CTA reads at once
+    using V = W8Vec<COLS>;
+    extern __shared__ __align__(16) uint8_t smem[];
+    const int rank = static_cast<int>(blockIdx.x % S);   // clusters are S consecutive CTAs
+    const int64_t strip = blockIdx.x / S;
+    const int64_t Ks = (K + S - 1) / S, k0 = rank * Ks, k1 = (k0 + Ks < K) ? k0 + Ks : K;
+    __nv_bfloat16* xs = reinterpret_cast<__nv_bfloat16*>(smem);                 // [C][Ks]
+    float* red = reinterpret_cast<float*>(smem + w8f_xs_bytes(C, Ks));          // [warp][C][128]
+    float* sum = red + W8F_WARPS * C * W8F_STRIP;                               // [C][128]
+
+    for (int64_t t = threadIdx.x; t < int64_t(C) * Ks; t += W8F_THREADS) {
+        const int64_t c = t / Ks, kk = t % Ks;
+        if (k0 + kk < k1) xs[t] = x[c * K + k0 + kk];
+    }
+    __syncthreads();
+
+    const int lc = threadIdx.x % LPR, rl = threadIdx.x / LPR;
+    const int64_t n0 = strip * W8F_STRIP + lc * COLS;
+    const bool live = n0 < N;   // N % 16 == 0: a live thread's COLS columns all exist
+    float acc[C][COLS];
+#pragma unroll
+    for (int c = 0; c < C; ++c)
+#pragma unroll
+        for (int j = 0; j < COLS; ++j) acc[c][j] = 0.f;
+
+    for (int64_t kb = k0 + rl; kb < k1; kb += int64_t(RL) * U) {
+        typename V::T w[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t k = kb + int64_t(u) * RL;
+            w[u] = (live && k < k1) ? V::load(q + k * N + n0) : V::zero();
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t k = kb + int64_t(u) * RL;
+            if (k >= k1) break;
+            float wf[COLS];
+#pragma unroll
+            for (int i = 0; i < COLS / 4; ++i) {
+                const uint32_t wx = V::word(w[u], i) ^ 0x80808080u;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) wf[4 * i + j] = i8_to_f32(wx, j);
+            }
+#pragma unroll
+            for (int c = 0; c < C; ++c) {
+                const float xv = __bfloat162float(xs[c * Ks + (k - k0)]);
+#pragma unroll
+                for (int j = 0; j < COLS; ++j) acc[c][j] = fmaf(wf[j], xv, acc[c][j]);
+            }
+        }
+    }
+    // the warp's rows, then the CTA's warps, in a fixed order
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+#pragma unroll
+    for (int c = 0; c < C; ++c)
+#pragma unroll
+        for (int j = 0; j < COLS; ++j) {
+            float v = acc[c][j];
+#pragma unroll
+            for (int o = LPR; o < 32; o <<= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+            if (lane < LPR) red[(warp * C + c) * W8F_STRIP + lc * COLS + j] = v;
+        }
+    __syncthreads();
+    for (int o = threadIdx.x; o < C * W8F_STRIP; o += W8F_THREADS) {
+        const int c = o / W8F_STRIP, col = o % W8F_STRIP;
+        float v = 0.f;
+#pragma unroll
+        for (int wi = 0; wi < W8F_WARPS; ++wi) v += red[(wi * C + c) * W8F_STRIP + col];
+        sum[o] = v;
+    }
+    // the cluster's K-slices meet in rank 0 (a hardware cluster barrier; the
+    // second keeps every CTA's shared memory alive until rank 0 has read it)
+    if (S > 1) {
+        asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+        asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+    } else {
+        __syncthreads();
+    }
+    if (rank == 0) {
+        for (int o = threadIdx.x; o < C * W8F_STRIP; o += W8F_THREADS) {
+            const int c = o / W8F_STRIP, col = o % W8F_STRIP;
+            float v = sum[o];
+            const uint32_t local = static_cast<uint32_t>(__cvta_generic_to_shared(sum + o));
+            for (int r = 1; r < S; ++r) v += ld_cluster_f32(map_cluster_u32(local, r));
+            const int64_t n = strip * W8F_STRIP + col;
+            if (n < N) d[c * N + n] = __float2bfloat16_rn(scale[n] * v);
+        }
+    }
+    if (S > 1) {
+        asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+        asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+    }
+}
+
+template <int C>
+w4_status launch_w8_fast(const void* q, const float* scale, const void* x, void* d, int64_t N, int64_t K,
+                         cudaStream_t stream) {
+    constexpr int COLS = C <= 4 ? 16 : 8;
+    constexpr int U = C <= 2 ? 8 : 4;
+    const int sms = sm_count();
+    if (sms <= 0) return W4_ERR_CUDA;
+    const int64_t strips = (N + W8F_STRIP - 1) / W8F_STRIP;
+    // about two CTAs per SM; more K-slices if x would not fit shared memory
+    int64_t S = (2 * int64_t(sms) + strips - 1) / strips;
+    S = S < 1 ? 1 : S > 8 ? 8 : S;
+    while (S < 8 && w8f_smem_bytes(C, (K + S - 1) / S) > size_t(W4_W4A8_MAX_SMEM)) ++S;
+    const size_t smem = w8f_smem_bytes(C, (K + S - 1) / S);
+    if (smem > size_t(W4_W4A8_MAX_SMEM) || strips * S > 0x7FFFFFFF) return W4_ERR_SHAPE;
+    auto kern = gemv_w8_fast_kernel<C, COLS, U>;
+    static int smem_set[64];
+    if (ensure_smem_limit(kern, static_cast<int>(smem), smem_set) != cudaSuccess) return W4_ERR_CUDA;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(strips * S), 1, 1);
+    cfg.blockDim = dim3(W8F_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(S);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return launch_status(cudaLaunchKernelEx(&cfg, kern, static_cast<const int8_t*>(q), scale,
+                                            static_cast<const __nv_bfloat16*>(x), static_cast<__nv_bfloat16*>(d), N,
+                                            K, static_cast<int>(S)));
+}
+
+// ---------------------------------------------------------------------------
+// Single-read quantiser (N % 8 == 0, K <= Q8C_MAX_K): a cluster of
+// Q8C_CTAS CTAs takes a strip of 64 columns -- one 128-byte line of every
+// row of W -- and splits K; each CTA keeps its rows in shared memory, so W
+// is read once.  The column maxima of the CTAs meet through distributed
+// shared memory between two cluster barriers; every CTA then quantises its
+// own rows from shared memory (IEEE division, half-away rounding, as the
+// two-pass kernel) and rank 0 writes the scales.  2KN read + KN + 4N written.
+// ---------------------------------------------------------------------------
+
+constexpr int Q8C_CTAS = 8;
+constexpr int Q8C_THREADS = 256;
+constexpr int Q8C_COLS = 64;                       // bf16 columns of a strip (128 bytes)
+constexpr int Q8C_ROWS_MAX = 1600;                 // rows a CTA can hold (200 KB)
+constexpr int64_t Q8C_MAX_K = int64_t(Q8C_CTAS) * Q8C_ROWS_MAX;
+
+__host__ __device__ inline size_t q8c_smem_bytes(int64_t rows) {
+    return size_t(rows) * Q8C_COLS * 2 + Q8C_COLS * 4 * 2 + (Q8C_THREADS / 32) * Q8C_COLS * 4;
+}
+
+__global__ void __launch_bounds__(Q8C_THREADS, 1)
+quantize_int8_cluster_kernel(const uint16_t* __restrict__ W, int8_t* __restrict__ q, float* __restrict__ scale,
+                             int64_t K, int64_t N) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    const int rank = static_cast<int>(blockIdx.x % Q8C_CTAS);
+    const int64_t strip = blockIdx.x / Q8C_CTAS;
+    const int64_t Kr = (K + Q8C_CTAS - 1) / Q8C_CTAS, k0 = rank * Kr, k1 = (k0 + Kr < K) ? k0 + Kr : K;
+    const int64_t rows = k1 > k0 ? k1 - k0 : 0;
+    uint16_t* tile = reinterpret_cast<uint16_t*>(smem);                                // [Kr][64]
+    uint32_t* cmax = reinterpret_cast<uint32_t*>(smem + size_t(Kr) * Q8C_COLS * 2);    // [64] this CTA's max
+    float* s_col = reinterpret_cast<float*>(cmax + Q8C_COLS);                          // [64] the scales
+    uint32_t* red = reinterpret_cast<uint32_t*>(s_col + Q8C_COLS);                     // [warp][64]
+
+    const int cq = threadIdx.x % 8, rl = threadIdx.x / 8;   // 8 columns, one of 32 row lanes
+    const int64_t n0 = strip * Q8C_COLS + cq * 8;
+    const bool live = n0 < N;                                // N % 8 == 0: all 8 columns exist
+    uint32_t m[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    constexpr int U = 8;
+    for (int64_t r0 = rl; r0 < rows; r0 += 32 * U) {
+        uint4 v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t r = r0 + 32 * u;
+            v[u] = (live && r < rows) ? ldg_stream_u4(W + (k0 + r) * N + n0) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t r = r0 + 32 * u;
+            if (r >= rows) break;
+            *reinterpret_cast<uint4*>(tile + r * Q8C_COLS + cq * 8) = v[u];
+            const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                m[2 * j] = max(m[2 * j], w[j] & 0x7FFFu);          // |w| as a bf16 bit pattern
+                m[2 * j + 1] = max(m[2 * j + 1], (w[j] >> 16) & 0x7FFFu);
+            }
+        }
+    }
+    // the CTA's column maxima: the warp's four row lanes by shuffles, then the warps
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        uint32_t x = m[j];
+        x = max(x, __shfl_xor_sync(0xFFFFFFFFu, x, 8));
+        x = max(x, __shfl_xor_sync(0xFFFFFFFFu, x, 16));
+        if (lane < 8) red[warp * Q8C_COLS + cq * 8 + j] = x;
+    }
+    __syncthreads();
+    if (threadIdx.x < Q8C_COLS) {
+        uint32_t x = 0;
+        for (int wi = 0; wi < Q8C_THREADS / 32; ++wi) x = max(x, red[wi * Q8C_COLS + threadIdx.x]);
+        cmax[threadIdx.x] = x;
+    }
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+    if (threadIdx.x < Q8C_COLS) {
+        uint32_t x = 0;
+        const uint32_t local = static_cast<uint32_t>(__cvta_generic_to_shared(cmax + threadIdx.x));
+        for (int r = 0; r < Q8C_CTAS; ++r) {
+            uint32_t v;
+            asm volatile("{\n\t.reg .b32 a;\n\tmapa.shared::cluster.u32 a, %1, %2;\n\tld.shared::cluster.u32 %0, [a];\n\t}"
+                         : "=r"(v) : "r"(local), "r"(r) : "memory");
+            x = max(x, v);
+        }
+        const float sc = __fdiv_rn(bf16_bits_to_f32(x), 127.0f);
+        s_col[threadIdx.x] = sc;
+        const int64_t n = strip * Q8C_COLS + threadIdx.x;
+        if (rank == 0 && n < N) scale[n] = sc;
+    }
+    __syncthreads();
+    if (live) {
+        float sc[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) sc[j] = s_col[cq * 8 + j];
+        for (int64_t r = rl; r < rows; r += 32) {
+            const uint4 v = *reinterpret_cast<const uint4*>(tile + r * Q8C_COLS + cq * 8);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+            uint32_t out[2] = {0, 0};
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const uint32_t bits = (j % 2 == 0) ? (w[j / 2] & 0xFFFFu) : (w[j / 2] >> 16);
+                const int8_t qq = quant8(bf16_bits_to_f32(bits), sc[j]);
+                out[j / 4] |= (static_cast<uint32_t>(static_cast<uint8_t>(qq))) << (8 * (j % 4));
+            }
+            *reinterpret_cast<uint2*>(q + (k0 + r) * N + n0) = make_uint2(out[0], out[1]);
+        }
+    }
+    // keep this CTA's maxima readable until every peer has read them
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+w4_status launch_quantize_int8_cluster(const void* W, void* q, float* scale, int64_t K, int64_t N,
+                                       cudaStream_t stream) {
+    const int64_t strips = (N + Q8C_COLS - 1) / Q8C_COLS;
+    const int64_t Kr = (K + Q8C_CTAS - 1) / Q8C_CTAS;
+    const size_t smem = q8c_smem_bytes(Kr);
+    if (strips * Q8C_CTAS > 0x7FFFFFFF) return W4_ERR_SHAPE;
+    static int smem_set[64];
+    if (ensure_smem_limit(quantize_int8_cluster_kernel, static_cast<int>(smem), smem_set) != cudaSuccess)
+        return W4_ERR_CUDA;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(strips * Q8C_CTAS), 1, 1);
+    cfg.blockDim = dim3(Q8C_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = Q8C_CTAS;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return launch_status(cudaLaunchKernelEx(&cfg, quantize_int8_cluster_kernel, static_cast<const uint16_t*>(W),
+                                            static_cast<int8_t*>(q), scale, K, N));
+}
+
 }  // namespace
 
 w4_status run_quantize_int8(const void* W, void* q, float* scale, int64_t K, int64_t N, cudaStream_t stream) {
+    if (N % 8 == 0 && K <= Q8C_MAX_K) return launch_quantize_int8_cluster(W, q, scale, K, N, stream);
     const int64_t strips = (N + Q8_COLS - 1) / Q8_COLS;
     if (strips > 0x7FFFFFFF) return W4_ERR_SHAPE;
     quantize_int8_kernel<<<static_cast<unsigned>(strips), Q8_COLS * Q8_LANES, 0, stream>>>(
@@ -152,6 +479,19 @@ w4_status run_permute_int8(const void* q, void* out, int64_t K, int64_t N, cudaS
 
 w4_status run_gemv_w8(const void* q, const float* scale, const void* x, void* d, int64_t N, int64_t K, int64_t C,
                       cudaStream_t stream) {
+    if (N % 16 == 0) {
+        switch (C) {
+            case 1: return launch_w8_fast<1>(q, scale, x, d, N, K, stream);
+            case 2: return launch_w8_fast<2>(q, scale, x, d, N, K, stream);
+            case 3: return launch_w8_fast<3>(q, scale, x, d, N, K, stream);
+            case 4: return launch_w8_fast<4>(q, scale, x, d, N, K, stream);
+            case 5: return launch_w8_fast<5>(q, scale, x, d, N, K, stream);
+            case 6: return launch_w8_fast<6>(q, scale, x, d, N, K, stream);
+            case 7: return launch_w8_fast<7>(q, scale, x, d, N, K, stream);
+            case 8: return launch_w8_fast<8>(q, scale, x, d, N, K, stream);
+            default: return W4_ERR_SHAPE;
+        }
+    }
     const int64_t blocks = (N + Q8_COLS - 1) / Q8_COLS;
     if (blocks > 0x7FFFFFFF) return W4_ERR_SHAPE;
     const dim3 grid(static_cast<unsigned>(blocks));

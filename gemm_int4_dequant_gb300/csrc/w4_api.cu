@@ -21,6 +21,23 @@ w4_status run_quantize_int8(const void* W, void* q, float* scale, int64_t K, int
 w4_status run_permute_int8(const void* q, void* out, int64_t K, int64_t N, cudaStream_t s);
 w4_status run_gemv_w8(const void* q, const float* scale, const void* x, void* d, int64_t N, int64_t K, int64_t C,
                       cudaStream_t s);
+w4_status run_quantize_q8_1_pt(const void* x, void* pt, int64_t C, int64_t K, cudaStream_t s);
+w4_status run_gemv_w4a8(const void* qw, const void* scale, const void* zero, const void* pt, void* d, int64_t N,
+                        int64_t K, int64_t C, cudaStream_t s);
+bool w4a8_fits(int64_t C, int64_t K);
+w4_status run_mmvq_ptq1_0(const void* blocks, const void* pt, float* d, int64_t N, int64_t K, int64_t C,
+                          cudaStream_t s);
+w4_status run_mmvq_ptq1_1(const void* sblocks, const void* codebook, int64_t n_code, const void* esc_idx,
+                          const void* esc_patt, int64_t n_esc, const void* pt, float* d, int64_t N, int64_t K,
+                          int64_t C, cudaStream_t s);
+bool ptq1_fits(int64_t C, int64_t K, bool super);
+int take_device_error_ptq1();
+w4_status run_selftest_wait_timeout(int* waited, cudaStream_t s);
+int take_device_error_selftest();
+w4_status run_gemm_w8(const void* A, const void* q, const float* scale, void* C, int64_t M, int64_t N, int64_t K,
+                      cudaStream_t s);
+w4_status run_gemm_w4_permuted(const void* A, const void* permuted, const float* scale, void* C, int64_t M,
+                               int64_t N, int64_t K, cudaStream_t s);
 int take_device_error_gemm();
 int take_device_error_gemv();
 int take_device_error_quant();
@@ -75,15 +92,17 @@ using namespace w4;
 
 extern "C" {
 
-int w4_abi_version(void) { return 3; }
+int w4_abi_version(void) { return 4; }
 
 int w4_device_error(void* stream) {
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return -1;
     const int a = take_device_error_gemm();
     const int b = take_device_error_gemv();
     const int c = take_device_error_quant();
-    if (a < 0 || b < 0 || c < 0) return -1;
-    return a != 0 ? a : b != 0 ? b : c;
+    const int e = take_device_error_ptq1();
+    const int f = take_device_error_selftest();
+    if (a < 0 || b < 0 || c < 0 || e < 0 || f < 0) return -1;
+    return a != 0 ? a : b != 0 ? b : c != 0 ? c : e != 0 ? e : f;
 }
 
 const char* w4_status_string(w4_status status) {
@@ -187,6 +206,82 @@ w4_status gemv_w8(const void* q, const float* scale, const void* x, void* d, int
     if (!device_is_sm103()) return W4_ERR_DEVICE;
     if (K == 0) return launch_status(cudaMemsetAsync(d, 0, C * N * 2, (cudaStream_t)stream));
     return run_gemv_w8(q, scale, x, d, N, K, C, (cudaStream_t)stream);
+}
+
+w4_status quantize_q8_1_pt(const void* x, void* pt, int64_t C, int64_t K, void* stream) {
+    if (C < 0 || K < 0 || (K % 128) != 0) return W4_ERR_SHAPE;
+    if (C == 0 || K == 0) return W4_OK;
+    if (!x || !pt) return W4_ERR_NULL;
+    if (!aligned16(x) || !aligned16(pt)) return W4_ERR_ALIGN;
+    if (!device_is_sm103()) return W4_ERR_DEVICE;
+    return run_quantize_q8_1_pt(x, pt, C, K, (cudaStream_t)stream);
+}
+
+w4_status gemv_w4a8(const void* qweight, const void* scale, const void* zero, const void* pt, void* d, int64_t N,
+                    int64_t K, int64_t C, void* stream) {
+    if (N < 0 || K < 0 || (K % 128) != 0 || C < 1 || C > 8 || !w4a8_fits(C, K)) return W4_ERR_SHAPE;
+    if (N == 0) return W4_OK;
+    if (!d || !scale || !zero || (K > 0 && (!qweight || !pt))) return W4_ERR_NULL;
+    if (!aligned16(d) || !aligned16(scale) || !aligned16(zero) || (K > 0 && (!aligned16(qweight) || !aligned16(pt))))
+        return W4_ERR_ALIGN;
+    if (!device_is_sm103()) return W4_ERR_DEVICE;
+    if (K == 0) return launch_status(cudaMemsetAsync(d, 0, C * N * 2, (cudaStream_t)stream));
+    return run_gemv_w4a8(qweight, scale, zero, pt, d, N, K, C, (cudaStream_t)stream);
+}
+
+w4_status mmvq_ptq1_0(const void* blocks, const void* pt, float* d, int64_t N, int64_t K, int64_t C, void* stream) {
+    if (N < 0 || K < 0 || (K % 128) != 0 || C < 1 || C > 8 || !ptq1_fits(C, K, false)) return W4_ERR_SHAPE;
+    if (N == 0) return W4_OK;
+    if (!d || (K > 0 && (!blocks || !pt))) return W4_ERR_NULL;
+    if (!aligned16(d) || (K > 0 && (!aligned16(blocks) || !aligned16(pt)))) return W4_ERR_ALIGN;
+    if (!device_is_sm103()) return W4_ERR_DEVICE;
+    if (K == 0) return launch_status(cudaMemsetAsync(d, 0, C * N * sizeof(float), (cudaStream_t)stream));
+    return run_mmvq_ptq1_0(blocks, pt, d, N, K, C, (cudaStream_t)stream);
+}
+
+w4_status mmvq_ptq1_1(const void* sblocks, const void* codebook, int64_t n_code, const void* esc_idx,
+                      const void* esc_patt, int64_t n_esc, const void* pt, float* d, int64_t N, int64_t K, int64_t C,
+                      void* stream) {
+    if (N < 0 || K < 0 || (K % 128) != 0 || C < 1 || C > 8 || n_code < 0 || n_code > 767 || n_esc < 0 ||
+        !ptq1_fits(C, K, true))
+        return W4_ERR_SHAPE;
+    if (N == 0) return W4_OK;
+    if (!d || (K > 0 && (!sblocks || !pt)) || (n_code > 0 && !codebook) || (n_esc > 0 && (!esc_idx || !esc_patt)))
+        return W4_ERR_NULL;
+    if (!aligned16(d) || (K > 0 && (!aligned16(sblocks) || !aligned16(pt))) || (n_code > 0 && !aligned16(codebook)) ||
+        (n_esc > 0 && (!aligned16(esc_idx) || !aligned16(esc_patt))))
+        return W4_ERR_ALIGN;
+    if (!device_is_sm103()) return W4_ERR_DEVICE;
+    if (K == 0) return launch_status(cudaMemsetAsync(d, 0, C * N * sizeof(float), (cudaStream_t)stream));
+    return run_mmvq_ptq1_1(sblocks, codebook, n_code, esc_idx, esc_patt, n_esc, pt, d, N, K, C, (cudaStream_t)stream);
+}
+
+w4_status gemm_w8(const void* A, const void* q, const float* scale, void* C, int64_t M, int64_t N, int64_t K,
+                  void* stream) {
+    if (M < 0 || N < 0 || K < 0 || (K % 64) != 0 || (N % 16) != 0) return W4_ERR_SHAPE;
+    if (M == 0 || N == 0) return W4_OK;
+    if (!C || !scale || (K > 0 && (!A || !q))) return W4_ERR_NULL;
+    if (!aligned16(C) || !aligned16(scale) || (K > 0 && (!aligned16(A) || !aligned16(q)))) return W4_ERR_ALIGN;
+    if (!device_is_sm103()) return W4_ERR_DEVICE;
+    if (K == 0) return launch_status(cudaMemsetAsync(C, 0, M * N * 2, (cudaStream_t)stream));
+    return run_gemm_w8(A, q, scale, C, M, N, K, (cudaStream_t)stream);
+}
+
+w4_status gemm_w4_permuted(const void* A, const void* permuted, const float* scale, void* C, int64_t M, int64_t N,
+                           int64_t K, void* stream) {
+    if (M < 0 || N < 0 || K < 0 || (K % 64) != 0 || (N % 16) != 0) return W4_ERR_SHAPE;
+    if (M == 0 || N == 0) return W4_OK;
+    if (!C || !scale || (K > 0 && (!A || !permuted))) return W4_ERR_NULL;
+    if (!aligned16(C) || !aligned16(scale) || (K > 0 && (!aligned16(A) || !aligned16(permuted)))) return W4_ERR_ALIGN;
+    if (!device_is_sm103()) return W4_ERR_DEVICE;
+    if (K == 0) return launch_status(cudaMemsetAsync(C, 0, M * N * 2, (cudaStream_t)stream));
+    return run_gemm_w4_permuted(A, permuted, scale, C, M, N, K, (cudaStream_t)stream);
+}
+
+w4_status w4_selftest_wait_timeout(int* waited, void* stream) {
+    if (!waited) return W4_ERR_NULL;
+    if (!device_is_sm103()) return W4_ERR_DEVICE;
+    return run_selftest_wait_timeout(waited, (cudaStream_t)stream);
 }
 
 w4_status gemm_w4(const void* A, const void* B, const void* scale, const void* zero, void* C, int64_t M, int64_t N,

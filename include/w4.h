@@ -18,10 +18,19 @@
  *                       interleaved layout the page builds for the fast
  *                       int4 -> 16-bit dequant), symmetric per-column scale.
  *   gemm_w4             large-M bf16 x int4 dequant GEMM
- *                       ("int4 gemm kernel", the matmul_bf16_int4 example).
- *   quantize_int8, permute_int8, gemv_w8
+ *                       ("int4 gemm kernel", the matmul_bf16_int4 example);
+ *                       gemm_w4_permuted, the same over permute_int4's output.
+ *   quantize_int8, permute_int8, gemv_w8, gemm_w8
  *                       the int8 weight-only counterparts (the first page's
  *                       int8 permute, from which its int4 permute derives).
+ *   quantize_q8_1_pt, gemv_w4a8
+ *                       x quantised to block_q8_1 in the "PT" planes, and
+ *                       gemv_w4's int4 weights against it with integer dot
+ *                       products ("三值量化模型的无损压缩", sections 3 and 3.1).
+ *   mmvq_ptq1_0, mmvq_ptq1_1
+ *                       ternary weights in PTQ1_0 blocks, or in the PTQ1_1
+ *                       superblocks that pack eight of them, against x in
+ *                       that form (same page, sections 2, 3 and 3.2).
  *   ptq1_1_codebook, ptq1_1_encode
  *                       host-side conversion of ternary PTQ1_0 blocks into
  *                       PTQ1_1 superblocks ("三值量化模型的无损压缩", section 2).
@@ -82,10 +91,21 @@ const char* w4_status_string(w4_status status);
  * iteration/time limit (about two seconds) records a nonzero code here,
  * drains the work it already issued, frees its tensor memory and returns.
  * This call synchronises `stream`, then returns and clears the first code
- * recorded on the current device (0 = none, 1 = a pipeline wait timed out),
- * or -1 if the synchronisation or the read failed.
+ * recorded on the current device (0 = none, 1 = a pipeline wait timed out,
+ * 2 = a PTQ1_1 superblock's pattern index named no codebook entry or escape;
+ * its blocks then count as d = 0), or -1 if the synchronisation or the read
+ * failed.
  */
 int w4_device_error(void* stream);
+
+/*
+ * w4_selftest_wait_timeout -- test of the device error path: one CTA runs the
+ * library's bounded mbarrier wait on a barrier that nothing completes.  The
+ * wait gives up after its limit (about two seconds), the kernel writes 0 to
+ * *waited (DEVICE int, 1 if the wait had completed) and records code 1 for
+ * w4_device_error; the context stays usable.  Nothing faults, traps or hangs.
+ */
+w4_status w4_selftest_wait_timeout(int* waited, void* stream);
 
 /*
  * quantize_pack_int4 -- symmetric per-column int4 quantisation + column pack.
@@ -272,6 +292,144 @@ w4_status permute_int8(const void* q, void* out, int64_t K, int64_t N, void* str
 w4_status gemv_w8(const void* q, const float* scale, const void* x, void* d, int64_t N, int64_t K, int64_t C,
                   void* stream);
 
+/*
+ * gemm_w8 -- large-M bf16 x int8 GEMM over quantize_int8's matrix (the int8
+ * counterpart of gemm_w4):
+ *
+ *   C[m][n] = scale[n] * sum_k A[m][k] * q[k][n]
+ *
+ * A      bf16 [M][K] row-major, 16-byte aligned.
+ * q      int8 [K][N] row-major, 16-byte aligned.
+ * scale  fp32 [N], 16-byte aligned.
+ * C      bf16 [M][N] row-major (output), 16-byte aligned.
+ * Requires K % 64 == 0 and N % 16 == 0 (else W4_ERR_SHAPE); K == 0 gives
+ * C = 0.  bf16 tensor-core products (int8 is exact in bf16), fp32
+ * accumulation, one bf16 rounding; the tolerance is gemm_w4's.
+ */
+w4_status gemm_w8(const void* A, const void* q, const float* scale, void* C, int64_t M, int64_t N, int64_t K,
+                  void* stream);
+
+/*
+ * gemm_w4_permuted -- large-M bf16 x int4 GEMM that reads permute_int4's
+ * output directly (the layout that page builds for the fast int4 -> 16-bit
+ * dequant):
+ *
+ *   C[m][n] = scale[n] * sum_k A[m][k] * q[k][n]
+ *
+ * with q[k][n] the two's complement weights quantize_pack_int4 packed and
+ * permute_int4 rearranged.
+ * A         bf16 [M][K] row-major, 16-byte aligned.
+ * permuted  N*K/2 bytes (permute_int4's output), 16-byte aligned.
+ * scale     fp32 [N], 16-byte aligned.
+ * C         bf16 [M][N] row-major (output), 16-byte aligned.
+ * Requires K % 64 == 0 and N % 16 == 0 (else W4_ERR_SHAPE); K == 0 gives
+ * C = 0.  Tolerance as gemm_w4.
+ */
+w4_status gemm_w4_permuted(const void* A, const void* permuted, const float* scale, void* C, int64_t M, int64_t N,
+                           int64_t K, void* stream);
+
+/* Shared memory available to one CTA on sm_103 (227 KB); gemv_w4a8 keeps all
+ * of x there. */
+#define W4_W4A8_MAX_SMEM 232448
+
+/*
+ * quantize_q8_1_pt -- x as block_q8_1 in the PT planes (page
+ * "三值量化模型的无损压缩", section 3.1 "数据格式": 32 int8 values qs and the
+ * halves (d, s) per block, s = d * sum qs).  For every 32-element block of
+ * every vector:
+ *   d  = max |x| / 127                            (IEEE fp32 division)
+ *   qs = clamp(round(x / d), -127, 127)           (IEEE fp32 division, round
+ *        half away from zero; a block whose maximum is 0 gets d = 0, qs = 0)
+ *   stored: qs as int8, and d and the fp32 product d * sum qs as IEEE halves
+ *   rounded to nearest even.
+ * Layout of one vector (144 * K/128 bytes): element e of 128-element block i
+ * is byte 16 * ((e / 16) * K/128 + i) + e % 16 (planes 0..7), and the four
+ * (d, s) pairs of block i are the 16 bytes at 16 * (8 * K/128 + i) (plane 8;
+ * pair j at +4j, d then s, little-endian).  Vectors follow each other.
+ *
+ * x   bf16 [C][K] row-major, 16-byte aligned.
+ * pt  uint8 [C][144*K/128] (output), 16-byte aligned.
+ * Requires K % 128 == 0 (else W4_ERR_SHAPE); C == 0 or K == 0 is a no-op.
+ * NaN or Inf in x is undefined.  Bit-exact with the definition above.
+ */
+w4_status quantize_q8_1_pt(const void* x, void* pt, int64_t C, int64_t K, void* stream);
+
+/*
+ * gemv_w4a8 -- gemv_w4's int4 weights against activations in block_q8_1 /
+ * PT form (same page, sections 3 and 3.1), with exact integer dot products
+ * per 32-element block b and the zero point corrected through s:
+ *
+ *   d[c][r] = scale[r] * sum_b ( d_b * sum_{k in b} q[r][k] * qs[c][k]
+ *                                - zero[r] * s_b )
+ *
+ * qweight  uint32 [N][K/8] as for gemv_w4 (nibble j of word i is k = 8i+j,
+ *          unsigned), 16-byte aligned.
+ * scale, zero  bf16 [N], 16-byte aligned.
+ * pt       quantize_q8_1_pt's output for the C vectors, 16-byte aligned.
+ * d        bf16 [C][N] row-major (output), 16-byte aligned.
+ * Requires K % 128 == 0, 1 <= C <= 8 and C * K * 5/4 + 32 <= W4_W4A8_MAX_SMEM
+ * (x is kept in shared memory; K <= 23168 at C = 8), else W4_ERR_SHAPE;
+ * K == 0 gives d = 0.  fp32 accumulation of the exact dots; the tolerance is
+ * 2e-3 * sum_k |(q - zero) * scale * d_b * qs| plus the bf16 rounding.
+ */
+w4_status gemv_w4a8(const void* qweight, const void* scale, const void* zero, const void* pt, void* d, int64_t N,
+                    int64_t K, int64_t C, void* stream);
+
+/*
+ * mmvq_ptq1_0 -- the MMVQ product of ternary weights stored as PTQ1_0 blocks
+ * with x in block_q8_1 / PT form (page "三值量化模型的无损压缩", section 2 for
+ * the block, 3 for the product, 3.2 for where each trit sits):
+ *
+ *   d[c][r] = sum_b d_w(r, b) * sum_{j<4} d_x(c, b, j)
+ *                             * sum_{e in q8_1 block j} t(r, 128 b + e) * qs(c, 128 b + e)
+ *
+ * A PTQ1_0 block (28 bytes) holds 128 trits and a half d_w: qs[24] with
+ * five trits a byte (byte = sum_p (t_p + 1) 3^p), weight e < 80 at trit
+ * e >> 4 of byte e & 15, weight 80 + e (e < 40) at trit e >> 3 of byte
+ * 16 + (e & 7); qh[2], a little-endian 16-bit word whose 2-bit field j is
+ * t + 1 of weight 120 + j; then d_w (little-endian half).
+ *
+ * blocks  N * K/128 blocks, row r's blocks back to back, rows back to back;
+ *         16-byte aligned.
+ * pt      quantize_q8_1_pt's output for the C vectors, 16-byte aligned.
+ * d       fp32 [C][N] row-major (output), 16-byte aligned.
+ * Requires K % 128 == 0, 1 <= C <= 8 and x within shared memory
+ * (C * K * 21/16 <= W4_W4A8_MAX_SMEM at C > 4, C * K * 11/8 at C <= 4;
+ * K <= 22016 at C = 8), else W4_ERR_SHAPE; K == 0 gives d = 0.  The integer
+ * dots are exact; fp32 products and sums, within (K/128 + 5) * 2^-24 of
+ * sum_k |w x| (2e-5 is the tested bound).
+ */
+w4_status mmvq_ptq1_0(const void* blocks, const void* pt, float* d, int64_t N, int64_t K, int64_t C, void* stream);
+
+/*
+ * mmvq_ptq1_1 -- mmvq_ptq1_0's product over the same weights packed as
+ * PTQ1_1 superblocks (same page, section 2): eight consecutive blocks of a
+ * row in 216 bytes,
+ *   qs[192]        the eight blocks' qs bytes, block s at 24 s;
+ *   qh[13]         the 64 tail trits, tail trit j of block s as base-3 digit
+ *                  (8 s + j) mod 5 of byte (8 s + j) / 5; digit 4 of byte 12
+ *                  is the free trit f;
+ *   mantissa[8]    ten bits each, block s at bits 10 s .. 10 s + 9 of the
+ *                  little-endian 80-bit string;
+ *   exponents      one byte; the pattern index exponents + 256 f < 767 names
+ *                  codebook entry [index], 767 the escape table entry of this
+ *                  superblock (index r * ceil(K/1024) + sb).
+ * Block s's d is the positive half with the pattern's exponent s and
+ * mantissa s.  A row of K/128 blocks takes ceil(K/1024) superblocks; the
+ * blocks past K (zero trits, d = 0) are not read.
+ *
+ * sblocks   N * ceil(K/1024) superblocks, row after row, 16-byte aligned.
+ * codebook  uint8 [n_code][8] exponents (0 <= n_code <= 767).
+ * esc_idx   int64 [n_esc] superblock indices, ascending; esc_patt uint8
+ *           [n_esc][8] their exponents.
+ * pt, d, C, K: as mmvq_ptq1_0 (the codebook takes 6136 bytes more shared
+ * memory).  All pointers 16-byte aligned; codebook / esc_* may be NULL when
+ * n_code / n_esc is 0.  An index that names no entry records device error 2
+ * (w4_device_error) and its blocks count as d = 0.
+ */
+w4_status mmvq_ptq1_1(const void* sblocks, const void* codebook, int64_t n_code, const void* esc_idx,
+                      const void* esc_patt, int64_t n_esc, const void* pt, float* d, int64_t N, int64_t K, int64_t C,
+                      void* stream);
 /*
  * PTQ1_1 conversion (page "三值量化模型的无损压缩", section 2 "权重的无损压缩").
  * HOST functions: every pointer is host memory; nothing touches a GPU.

@@ -153,6 +153,24 @@ def ternary_inputs(N, K, C, seed=0, outlier_fraction=0.0):
     return TernaryInputs(trits, d, x, N, K, C)
 
 
+def ptq1_0_blocks(N, K, seed=0):
+    """PTQ1_0 tensors drawn directly as bytes (uint8 [N, K/128, 28]): each qs
+    byte uniform over 0..242 (= five independent uniform trits), each 2-bit
+    field of qh uniform over 0..2 (one uniform trit), d as ternary_inputs
+    draws it.  The same distribution as packing ternary_inputs' trits, with
+    no packing code here."""
+    if K % 128:
+        raise ValueError("K must be a multiple of 128")
+    bpr = K // 128
+    g = _gen(seed)
+    qs = torch.randint(0, 243, (N, bpr, 24), dtype=torch.int16, generator=g).to(torch.uint8)
+    fields = torch.randint(0, 3, (N, bpr, 2, 4), dtype=torch.int16, generator=g)
+    qh = (fields[..., 0] | (fields[..., 1] << 2) | (fields[..., 2] << 4) | (fields[..., 3] << 6)).to(torch.uint8)
+    d = np_bits(ternary_inputs(N, 128 * bpr, 1, seed=seed + 1).d).reshape(N, bpr, 1).view(np.uint8)
+    out = np.concatenate([qs.numpy(), qh.numpy(), d], axis=2)
+    return np.ascontiguousarray(out)
+
+
 def quant_inputs(K, N, seed=0, std=0.02):
     """W bf16 [K, N] ~ N(0, std)."""
     g = _gen(seed)

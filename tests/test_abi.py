@@ -27,8 +27,9 @@ def _declared_functions():
 def test_header_declares_the_hot_path():
     names = _declared_functions()
     for fn in ("quantize_pack_int4", "permute_int4", "quantize_pack_permute_int4", "gemv_w4", "gemv_w4_permuted",
-               "gemm_w4", "quantize_int8", "permute_int8", "gemv_w8", "ptq1_1_codebook", "ptq1_1_encode",
-               "w4_status_string", "w4_abi_version", "w4_device_error"):
+               "gemm_w4", "quantize_int8", "permute_int8", "gemv_w8", "gemm_w8", "gemm_w4_permuted", "quantize_q8_1_pt", "gemv_w4a8", "mmvq_ptq1_0",
+               "mmvq_ptq1_1", "ptq1_1_codebook", "ptq1_1_encode",
+               "w4_status_string", "w4_abi_version", "w4_device_error", "w4_selftest_wait_timeout"):
         assert fn in names
 
 
@@ -36,7 +37,7 @@ def test_library_exports_every_declared_symbol():
     lib, _ = _lib()
     for fn in _declared_functions():
         assert hasattr(lib, fn), "libw4.so does not export %s" % fn
-    assert lib.w4_abi_version() == 3
+    assert lib.w4_abi_version() == 4
     assert lib.w4_status_string(-2) == b"illegal size or shape"
     assert lib.w4_status_string(-7) == b"input value outside the format's range"
 
@@ -109,6 +110,50 @@ def test_argument_validation_happens_on_host():
     assert lib.gemv_w8(A, A, A, A, 0, 64, 1, None) == L.W4_OK
     assert lib.gemv_w8(A, A, None, A, 16, 64, 1, None) == L.W4_ERR_NULL
     assert lib.gemv_w8(A, A, A, odd, 16, 64, 1, None) == L.W4_ERR_ALIGN
+    # W4A8: the PT layout needs K % 128; x lives in shared memory
+    assert lib.quantize_q8_1_pt(A, A, 1, 192, None) == L.W4_ERR_SHAPE
+    assert lib.quantize_q8_1_pt(A, A, -1, 128, None) == L.W4_ERR_SHAPE
+    assert lib.quantize_q8_1_pt(A, A, 0, 128, None) == L.W4_OK
+    assert lib.quantize_q8_1_pt(A, A, 2, 0, None) == L.W4_OK
+    assert lib.quantize_q8_1_pt(None, A, 1, 128, None) == L.W4_ERR_NULL
+    assert lib.quantize_q8_1_pt(A, odd, 1, 128, None) == L.W4_ERR_ALIGN
+    assert lib.gemv_w4a8(A, A, A, A, A, 16, 192, 1, None) == L.W4_ERR_SHAPE        # K % 128
+    assert lib.gemv_w4a8(A, A, A, A, A, 16, 128, 0, None) == L.W4_ERR_SHAPE
+    assert lib.gemv_w4a8(A, A, A, A, A, 16, 128, 9, None) == L.W4_ERR_SHAPE
+    assert lib.gemv_w4a8(A, A, A, A, A, 16, 23168 + 128, 8, None) == L.W4_ERR_SHAPE  # x exceeds shared memory
+    assert lib.gemv_w4a8(A, A, A, A, A, 0, 128, 1, None) == L.W4_OK
+    assert lib.gemv_w4a8(A, A, None, A, A, 16, 128, 1, None) == L.W4_ERR_NULL
+    assert lib.gemv_w4a8(A, A, A, odd, A, 16, 128, 1, None) == L.W4_ERR_ALIGN
+    # mmvq_ptq1_0: whole 128-weight blocks; x in shared memory
+    assert lib.mmvq_ptq1_0(A, A, A, 16, 192, 1, None) == L.W4_ERR_SHAPE
+    assert lib.mmvq_ptq1_0(A, A, A, 16, 128, 0, None) == L.W4_ERR_SHAPE
+    assert lib.mmvq_ptq1_0(A, A, A, 16, 128, 9, None) == L.W4_ERR_SHAPE
+    assert lib.mmvq_ptq1_0(A, A, A, 16, 22016 + 128, 8, None) == L.W4_ERR_SHAPE
+    assert lib.mmvq_ptq1_0(A, A, A, 0, 128, 1, None) == L.W4_OK
+    assert lib.mmvq_ptq1_0(None, A, A, 16, 128, 1, None) == L.W4_ERR_NULL
+    assert lib.mmvq_ptq1_0(A, A, odd, 16, 128, 1, None) == L.W4_ERR_ALIGN
+    # mmvq_ptq1_1: codebook size, escape table, the codebook's share of shared memory
+    assert lib.mmvq_ptq1_1(A, A, 768, A, A, 1, A, A, 16, 1024, 1, None) == L.W4_ERR_SHAPE
+    assert lib.mmvq_ptq1_1(A, A, -1, A, A, 1, A, A, 16, 1024, 1, None) == L.W4_ERR_SHAPE
+    assert lib.mmvq_ptq1_1(A, A, 10, A, A, -1, A, A, 16, 1024, 1, None) == L.W4_ERR_SHAPE
+    assert lib.mmvq_ptq1_1(A, A, 10, A, A, 1, A, A, 16, 1000, 1, None) == L.W4_ERR_SHAPE
+    assert lib.mmvq_ptq1_1(A, A, 10, A, A, 1, A, A, 16, 22016, 8, None) == L.W4_ERR_SHAPE
+    assert lib.mmvq_ptq1_1(A, None, 10, A, A, 1, A, A, 16, 1024, 1, None) == L.W4_ERR_NULL
+    assert lib.mmvq_ptq1_1(A, A, 10, None, A, 1, A, A, 16, 1024, 1, None) == L.W4_ERR_NULL
+    assert lib.mmvq_ptq1_1(A, A, 10, odd, A, 1, A, A, 16, 1024, 1, None) == L.W4_ERR_ALIGN
+    assert lib.mmvq_ptq1_1(A, A, 10, A, A, 1, A, A, 0, 1024, 1, None) == L.W4_OK
+    # gemm_w8: the GEMM's tile rules
+    assert lib.gemm_w8(A, A, A, A, 128, 256, 100, None) == L.W4_ERR_SHAPE
+    assert lib.gemm_w8(A, A, A, A, 128, 250, 128, None) == L.W4_ERR_SHAPE
+    assert lib.gemm_w8(A, None, A, A, 128, 256, 128, None) == L.W4_ERR_NULL
+    assert lib.gemm_w8(A, A, odd, A, 128, 256, 128, None) == L.W4_ERR_ALIGN
+    assert lib.gemm_w8(A, A, A, A, 0, 256, 128, None) == L.W4_OK
+    # gemm_w4_permuted: the GEMM's tile rules
+    assert lib.gemm_w4_permuted(A, A, A, A, 128, 256, 100, None) == L.W4_ERR_SHAPE
+    assert lib.gemm_w4_permuted(A, A, A, A, 128, 264, 128, None) == L.W4_ERR_SHAPE
+    assert lib.gemm_w4_permuted(A, None, A, A, 128, 256, 128, None) == L.W4_ERR_NULL
+    assert lib.gemm_w4_permuted(odd, A, A, A, 128, 256, 128, None) == L.W4_ERR_ALIGN
+    assert lib.gemm_w4_permuted(A, A, A, A, 0, 256, 128, None) == L.W4_OK
     # gemm_w4
     assert lib.gemm_w4(A, A, A, A, A, 128, 256, 100, None) == L.W4_ERR_SHAPE
     assert lib.gemm_w4(A, A, A, A, A, 128, 250, 128, None) == L.W4_ERR_SHAPE

@@ -29,7 +29,7 @@ def test_gemm_bytes_and_flops():
 
 def test_workloads_name_known_kinds():
     for name, cfg in bench.WORKLOADS.items():
-        assert cfg["kind"] in ("gemv", "quant", "gemm", "gemv8", "quant8"), name
+        assert cfg["kind"] in ("gemv", "quant", "gemm", "gemv8", "quant8", "w4a8", "ptq1", "gemm8", "gemmp"), name
     assert set(bench.COMPONENTS) <= set(bench.WORKLOADS)
     assert bench.WORKLOADS["quant"]["fused"] and not bench.WORKLOADS["quant_2call"]["fused"]
 
@@ -78,6 +78,18 @@ def test_recorded_traffic_drops_on_code_change(tmp_path, monkeypatch):
     f = root / bench.KERNEL_SOURCES["gemv"][0]
     f.write_text(f.read_text() + "\nstatic int changed_code = 1;\n")
     assert bench.recorded_traffic("gemv", "decode") is None
+
+
+def test_w4a8_bytes():
+    # weights + scale/zero + x + PT written and read + d
+    N, K, C = 17280, 5120, 1
+    assert bench.w4a8_bytes(N, K, C) == N * K // 2 + 4 * N + 2 * K + 2 * 144 * 40 + 2 * N
+
+
+def test_ptq1_bytes():
+    # 28-byte blocks + x + PT written and read + fp32 d
+    N, K, C = 17280, 5120, 1
+    assert bench.ptq1_bytes(N, K, C) == N * 40 * 28 + 2 * K + 2 * 144 * 40 + 4 * N
 
 
 def test_reference_arm_runs_on_the_host_and_prints_the_contract_line():

@@ -375,7 +375,12 @@ def test_gemm_k_zero(w4):
 # int8 weight-only variant: quantize_int8, permute_int8 (bit-exact), gemv_w8
 # ---------------------------------------------------------------------------
 
-@pytest.mark.parametrize("K,N", [(1, 8), (64, 2), (130, 37), (1024, 1000), (8192, 8192)])
+@pytest.mark.parametrize("K,N", [
+    (64, 2), (130, 37),                       # N % 8 != 0: the two-pass kernel
+    (1, 8), (7, 120),                         # single-read clusters: ranks without rows; a partial strip
+    (1024, 1000), (8192, 8192), (12800, 72),  # ... up to the longest K a cluster holds
+    (12808, 16),                              # one step past it: the two-pass kernel again
+])
 def test_quantize_int8_bit_exact(w4, K, N):
     W = synth.quant_inputs(K, N, seed=K + 5 * N)
     if N > 3:
@@ -403,8 +408,12 @@ def test_permute_int8_bit_exact(w4, K, N):
     assert _guards_intact(buf, pad, N * K, 0x5A)
 
 
-@pytest.mark.parametrize("N,K,C", [(1, 1, 1), (37, 100, 3), (300, 4096, 8), (1000, 5120, 1), (17280, 5120, 1),
-                                   (5120, 17280, 4)])
+@pytest.mark.parametrize("N,K,C", [
+    (1, 1, 1), (37, 100, 3), (300, 4096, 8), (1000, 5120, 1),     # N % 16 != 0: the plain kernel
+    (17280, 5120, 1), (5120, 17280, 4), (5120, 17280, 8),          # N % 16 == 0: 128-column strips, K split
+    (6144, 5120, 2), (16, 7, 3),                                   # a cluster rank with no rows of K
+    (272, 100, 5), (48, 8192, 6),                                  # a partial strip; eight columns a thread
+])
 def test_gemv_w8(w4, N, K, C):
     gi = synth.int8_gemv_inputs(N, K, C, seed=N + K + C)
     buf, out, pad = _guarded(C * N, torch.bfloat16, -7.0)
@@ -429,3 +438,133 @@ def test_int8_quantise_permute_gemv_chain(w4):
     d = w4.gemv_w8(q, scale, x.to(_dev()))
     ref, ref_abs = oracle.gemv_int8(q_ref, s_ref, np_bits(x))
     assert not parity_violations(d.float().cpu().numpy(), ref, ref_abs, BF16_TOL, bf16_out=True).any()
+
+
+# ---------------------------------------------------------------------------
+# gemm_w8: bf16 x int8 on the tensor cores
+# ---------------------------------------------------------------------------
+
+def _w8_gemm_case(M, N, K, seed):
+    gi = synth.int8_gemv_inputs(N, K, 1, seed=seed)
+    A = synth.gemm_inputs(M, 16, K, seed=seed + 1).A
+    return A, gi.q, gi.scale
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 256, 64), (300, 528, 192), (1, 16, 64), (777, 1040, 640), (512, 1024, 1024)])
+def test_gemm_w8_small(w4, M, N, K):
+    A, q, s = _w8_gemm_case(M, N, K, seed=M + N + K)
+    buf, out, pad = _guarded(M * N, torch.bfloat16, -3.0)
+    w4.gemm_w8(A.to(_dev()), q.to(_dev()), s.to(_dev()), out=out.view(M, N))
+    assert w4.device_error() == 0
+    ref, ref_abs = oracle.gemm_int8_full(np_bits(A), q.numpy(), s.numpy())
+    got = out.float().cpu().numpy().astype(np.float64).reshape(M, N)
+    bad = parity_violations(got, ref, ref_abs, BF16_TOL, bf16_out=True)
+    assert not bad.any(), "max err/ref_abs %g" % (np.abs(got - ref) / ref_abs).max()
+    assert _guards_intact(buf, pad, M * N, -3.0)
+
+
+def test_gemm_w8_full_size_sampled(w4):
+    M = N = K = 8192
+    A, q, s = _w8_gemm_case(M, N, K, seed=3)
+    C = w4.gemm_w8(A.to(_dev()), q.to(_dev()), s.to(_dev()))
+    assert w4.device_error() == 0
+    Cn = C.float().cpu().numpy().astype(np.float64)
+    rng = np.random.default_rng(1)
+    mi = list(rng.integers(0, M, 32768))
+    ni = list(rng.integers(0, N, 32768))
+    for m in (0, 127, 128, M - 1):
+        mi += [m] * 1024
+        ni += list(rng.integers(0, N, 1024))
+    for n in (0, 255, 256, N - 1):
+        mi += list(rng.integers(0, M, 1024))
+        ni += [n] * 1024
+    mi, ni = np.array(mi), np.array(ni)
+    ref, ref_abs = oracle.gemm_int8_at(np_bits(A), q.numpy(), s.numpy(), mi, ni)
+    bad = parity_violations(Cn[mi, ni], ref, ref_abs, BF16_TOL, bf16_out=True)
+    assert not bad.any()
+
+
+def test_quantize_int8_then_gemm_w8(w4):
+    """quantize_int8 on the device, then gemm_w8, against the oracle's
+    quantisation and product."""
+    K, N, M = 1024, 512, 384
+    W = synth.quant_inputs(K, N, seed=31)
+    A = synth.gemm_inputs(M, 16, K, seed=32).A
+    q, scale = w4.quantize_int8(W.to(_dev()))
+    C = w4.gemm_w8(A.to(_dev()), q, scale)
+    s_ref, q_ref = oracle.quantize_int8(np_bits(W))
+    ref, ref_abs = oracle.gemm_int8_full(np_bits(A), q_ref, s_ref)
+    assert not parity_violations(C.float().cpu().numpy(), ref, ref_abs, BF16_TOL, bf16_out=True).any()
+
+
+# ---------------------------------------------------------------------------
+# gemm_w4_permuted: the GEMM reading permute_int4's layout
+# ---------------------------------------------------------------------------
+
+def _perm_gemm_case(M, N, K, seed):
+    g = synth.packed_gemv_inputs(N, K, 1, seed=seed)
+    A = synth.gemm_inputs(M, 16, K, seed=seed + 1).A
+    permuted = oracle.permute(g.packed.numpy(), K, N)
+    return A, g.packed.numpy(), permuted, g.scale
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 256, 64), (300, 528, 192), (1, 16, 64), (777, 1040, 640), (512, 1024, 1024)])
+def test_gemm_w4_permuted_small(w4, M, N, K):
+    A, packed, permuted, s = _perm_gemm_case(M, N, K, seed=M + N + K)
+    buf, out, pad = _guarded(M * N, torch.bfloat16, -3.0)
+    w4.gemm_w4_permuted(A.to(_dev()), torch.from_numpy(permuted).to(_dev()), s.to(_dev()), out=out.view(M, N))
+    assert w4.device_error() == 0
+    ref, ref_abs = oracle.gemm_packed_full(np_bits(A), packed, s.numpy())
+    got = out.float().cpu().numpy().astype(np.float64).reshape(M, N)
+    bad = parity_violations(got, ref, ref_abs, BF16_TOL, bf16_out=True)
+    assert not bad.any(), "max err/ref_abs %g" % (np.abs(got - ref) / ref_abs).max()
+    assert _guards_intact(buf, pad, M * N, -3.0)
+
+
+def test_gemm_w4_permuted_full_size_sampled(w4):
+    M = N = K = 8192
+    A, packed, permuted, s = _perm_gemm_case(M, N, K, seed=5)
+    C = w4.gemm_w4_permuted(A.to(_dev()), torch.from_numpy(permuted).to(_dev()), s.to(_dev()))
+    assert w4.device_error() == 0
+    Cn = C.float().cpu().numpy().astype(np.float64)
+    rng = np.random.default_rng(2)
+    mi = list(rng.integers(0, M, 32768))
+    ni = list(rng.integers(0, N, 32768))
+    for n in (0, 3, 4, 127, 128, 255, 256, N - 1):      # group and tile edges
+        mi += list(rng.integers(0, M, 512))
+        ni += [n] * 512
+    mi, ni = np.array(mi), np.array(ni)
+    ref, ref_abs = oracle.gemm_packed_at(np_bits(A), packed, s.numpy(), mi, ni)
+    assert not parity_violations(Cn[mi, ni], ref, ref_abs, BF16_TOL, bf16_out=True).any()
+
+
+def test_quantise_permute_then_gemm(w4):
+    """quantize_pack_permute_int4 on the device, then gemm_w4_permuted,
+    against the oracle's quantisation and product."""
+    K, N, M = 1024, 512, 384
+    W = synth.quant_inputs(K, N, seed=41)
+    A = synth.gemm_inputs(M, 16, K, seed=42).A
+    permuted, scale = w4.quantize_pack_permute_int4(W.to(_dev()))
+    C = w4.gemm_w4_permuted(A.to(_dev()), permuted, scale)
+    s_ref, p_ref = oracle.quantize_pack(np_bits(W))
+    ref, ref_abs = oracle.gemm_packed_full(np_bits(A), p_ref, s_ref)
+    assert not parity_violations(C.float().cpu().numpy(), ref, ref_abs, BF16_TOL, bf16_out=True).any()
+
+
+
+# ---------------------------------------------------------------------------
+# the device error path
+# ---------------------------------------------------------------------------
+
+def test_bounded_wait_gives_up_reports_and_leaves_the_context_usable(w4):
+    """A wait on a barrier nothing completes ends after its limit with error
+    code 1 (read and cleared by w4_device_error); the next calls work."""
+    from gemm_int4_dequant_gb300 import _lib as L
+    waited = torch.full((1,), 7, dtype=torch.int32, device=_dev())
+    assert w4.device_error() == 0
+    st = L.load().w4_selftest_wait_timeout(waited.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    assert st == L.W4_OK
+    assert w4.device_error() == 1
+    assert int(waited.item()) == 0
+    assert w4.device_error() == 0
+    _check_gemv(w4, 300, 4096, 2, "bf16", seed=9)

@@ -61,3 +61,20 @@ def test_ternary_inputs_deterministic_and_shaped():
     assert steps.max() <= 1 and 0.85 < (steps == 0).mean() < 0.99
     wild = synth.ternary_inputs(64, 1152, 1, seed=0, outlier_fraction=1.0)
     assert (np.abs(np.diff(((synth.np_bits(wild.d) >> 10) & 31).astype(int), axis=1)) > 1).any()
+
+
+def test_ptq1_0_blocks_are_valid_blocks():
+    """Every qs byte is a five-trit byte, every qh field a digit; the bytes
+    decode (through the oracle) to trits uniform over {-1, 0, 1}."""
+    import oracle
+    b = synth.ptq1_0_blocks(40, 1152, seed=0)
+    assert b.shape == (40, 9, 28) and b.dtype == np.uint8
+    assert np.array_equal(b, synth.ptq1_0_blocks(40, 1152, seed=0))
+    assert b[..., :24].max() <= 242
+    qh = b[..., 24:26]
+    for j in range(4):
+        assert ((qh >> (2 * j)) & 3).max() <= 2
+    t, d = oracle.ptq1_0_unpack(b)
+    counts = np.bincount(t.ravel() + 1, minlength=3)
+    assert counts.min() > 0.95 * counts.mean()
+    assert np.array_equal(oracle.ptq1_0_pack(t, d), b)
