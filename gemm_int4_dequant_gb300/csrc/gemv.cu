@@ -10,9 +10,11 @@
 // C = 1), so the kernel streams the packed words with 16-byte non-allocating
 // loads, stages x once per CTA in shared memory as fp32, converts nibbles to
 // exact fp32 with the IEEE "magic number" trick (OR the nibble into the
-// mantissa of 2^23, then one FMA by a power of two removes the offset and the
-// nibble's bit position) and accumulates in fp32.  The zero point is folded
-// out of the k-sum exactly:  sum_k (q - z) x = sum_k q x - z * sum_k x.
+// mantissa of 2^23, then one FMA by a power of two removes the offset, the
+// nibble's bit position and the zero point's integer part zi: q - zi comes
+// out exact) and accumulates in fp32.  A weight equal to an integer zero
+// point contributes exactly nothing; only a fractional rest is folded out
+// of the k-sum:  sum_k (q - z) x = sum_k (q - zi) x - (z - zi) sum_k x.
 // K is split across the CTAs of a thread-block cluster when x does not fit
 // in shared memory; the partial sums are reduced through distributed shared
 // memory, so no scratch buffer in global memory is needed.
@@ -20,6 +22,7 @@
 #include <cooperative_groups.h>
 
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -39,24 +42,45 @@ constexpr int GV_ROWS = GV_WARPS * GV_TILE;  // rows per CTA
 __device__ __forceinline__ int xpad(int i) { return i + (i >> 5) * 4; }
 __host__ __device__ constexpr int xpad_len(int n) { return n + ((n + 31) / 32) * 4 + 4; }
 
-// Eight nibbles of a word -> eight exact floats 0..15.
-__device__ __forceinline__ void nibbles_to_f32(uint32_t v, float (&q)[8]) {
+// The five offsets a row's nibbles are reduced by: -(2^(23-4j) + zi) for
+// j = 0..4, zi = zint(z) (every one exact in fp32).
+struct ZeroOffsets {
+    float o[5];
+};
+__device__ __forceinline__ ZeroOffsets zero_offsets(int zi) {
+    ZeroOffsets z;
+    const float zf = static_cast<float>(zi);
+    z.o[0] = -(8388608.0f + zf);
+    z.o[1] = -(524288.0f + zf);
+    z.o[2] = -(32768.0f + zf);
+    z.o[3] = -(2048.0f + zf);
+    z.o[4] = -(128.0f + zf);
+    return z;
+}
+
+// Eight nibbles of a word -> eight exact floats q - zi: nibble j ORed into
+// the mantissa of 2^23 is 2^23 + 2^(4j) q; scaled by 2^-4j (exact) it is
+// 2^(23-4j) + q, and the offset leaves q - zi (a single rounding of an
+// exactly representable result).  Nibbles 5..7 come from the word shifted
+// by 12, reusing the offsets of positions 2..4.
+__device__ __forceinline__ void nibbles_to_f32(uint32_t v, const ZeroOffsets& z, float (&q)[8]) {
     const uint32_t M = 0x4B000000u;  // 2^23
     const uint32_t h = v >> 12;
-    q[0] = __uint_as_float((v & 0x0000Fu) | M) - 8388608.0f;
-    q[1] = fmaf(__uint_as_float((v & 0x000F0u) | M), 0.0625f, -524288.0f);
-    q[2] = fmaf(__uint_as_float((v & 0x00F00u) | M), 0.00390625f, -32768.0f);
-    q[3] = fmaf(__uint_as_float((v & 0x0F000u) | M), 0.000244140625f, -2048.0f);
-    q[4] = fmaf(__uint_as_float((v & 0xF0000u) | M), 0.0000152587890625f, -128.0f);
-    q[5] = fmaf(__uint_as_float((h & 0x00F00u) | M), 0.00390625f, -32768.0f);
-    q[6] = fmaf(__uint_as_float((h & 0x0F000u) | M), 0.000244140625f, -2048.0f);
-    q[7] = fmaf(__uint_as_float((h & 0xF0000u) | M), 0.0000152587890625f, -128.0f);
+    q[0] = __uint_as_float((v & 0x0000Fu) | M) + z.o[0];
+    q[1] = fmaf(__uint_as_float((v & 0x000F0u) | M), 0.0625f, z.o[1]);
+    q[2] = fmaf(__uint_as_float((v & 0x00F00u) | M), 0.00390625f, z.o[2]);
+    q[3] = fmaf(__uint_as_float((v & 0x0F000u) | M), 0.000244140625f, z.o[3]);
+    q[4] = fmaf(__uint_as_float((v & 0xF0000u) | M), 0.0000152587890625f, z.o[4]);
+    q[5] = fmaf(__uint_as_float((h & 0x00F00u) | M), 0.00390625f, z.o[2]);
+    q[6] = fmaf(__uint_as_float((h & 0x0F000u) | M), 0.000244140625f, z.o[3]);
+    q[7] = fmaf(__uint_as_float((h & 0xF0000u) | M), 0.0000152587890625f, z.o[4]);
 }
 
 template <int C>
-__device__ __forceinline__ void word_dot(uint32_t v, const float (&xv)[C][8], float (&acc)[C]) {
+__device__ __forceinline__ void word_dot(uint32_t v, const ZeroOffsets& z, const float (&xv)[C][8],
+                                         float (&acc)[C]) {
     float q[8];
-    nibbles_to_f32(v, q);
+    nibbles_to_f32(v, z, q);
 #pragma unroll
     for (int c = 0; c < C; ++c)
 #pragma unroll
@@ -113,11 +137,15 @@ gemv_ffma_kernel(const uint32_t* __restrict__ qw, const T* __restrict__ scale, c
         int lrow[GV_RT];
         bool valid[GV_RT];
         const uint32_t* rp[GV_RT];
+        float zrow[GV_RT];
+        ZeroOffsets zo[GV_RT];
 #pragma unroll
         for (int t = 0; t < GV_RT; ++t) {
             lrow[t] = tile * GV_TILE + rl + GV_RL * t;
             valid[t] = lrow[t] < rows_here;
             rp[t] = qw + static_cast<int64_t>(row0 + (valid[t] ? lrow[t] : 0)) * (K / 8);
+            zrow[t] = valid[t] ? to_f32<T>(zero[row0 + lrow[t]]) : 0.0f;
+            zo[t] = zero_offsets(ptx::zint(zrow[t]));
         }
         float acc[GV_RT][C];
 #pragma unroll
@@ -146,7 +174,7 @@ gemv_ffma_kernel(const uint32_t* __restrict__ qw, const T* __restrict__ scale, c
 #pragma unroll
                     for (int t = 0; t < GV_RT; ++t) {
                         uint32_t v = w == 0 ? cur[t].x : w == 1 ? cur[t].y : w == 2 ? cur[t].z : cur[t].w;
-                        word_dot<C>(v, xv, acc[t]);
+                        word_dot<C>(v, zo[t], xv, acc[t]);
                     }
                 }
 #pragma unroll
@@ -161,7 +189,7 @@ gemv_ffma_kernel(const uint32_t* __restrict__ qw, const T* __restrict__ scale, c
                 float xv[C][8];
                 load_x8<C>(xs, xs_stride, xpad((wi - w0) * 8), xv);
 #pragma unroll
-                for (int t = 0; t < GV_RT; ++t) word_dot<C>(v[t], xv, acc[t]);
+                for (int t = 0; t < GV_RT; ++t) word_dot<C>(v[t], zo[t], xv, acc[t]);
             }
         }
         // reduce across the K lanes of each row
@@ -175,9 +203,9 @@ gemv_ffma_kernel(const uint32_t* __restrict__ qw, const T* __restrict__ scale, c
 #pragma unroll
             for (int t = 0; t < GV_RT; ++t) {
                 if (!valid[t]) continue;
-                const float z = to_f32<T>(zero[row0 + lrow[t]]);
+                const float zf = zrow[t] - static_cast<float>(ptx::zint(zrow[t]));   // fractional rest
 #pragma unroll
-                for (int c = 0; c < C; ++c) part[lrow[t] * C + c] = fmaf(-z, xsum[c], acc[t][c]);
+                for (int c = 0; c < C; ++c) part[lrow[t] * C + c] = fmaf(-zf, xsum[c], acc[t][c]);
             }
         }
     }

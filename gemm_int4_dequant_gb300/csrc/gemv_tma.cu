@@ -28,26 +28,29 @@
 //   * warps 0..NC-1 (consumers) share out the 128-k blocks of every stage
 //     round-robin (continuing across stages, so the split stays balanced):
 //     two 16-byte shared loads give a lane its rows g and g+8, each uint32
-//     word becomes four 16-bit pairs (nibbles j, j+4) and two
-//     mma.sync.m16n8k16 per word accumulate in fp32 against x, which was
-//     staged once per CTA in B-fragment order.  With several columns of x
-//     the pairs are bf16: one mask-and-OR per pair into the mantissa of
-//     128.0 (exactly 128 + q), after a shift by 4j.  With one column they
-//     are fp16, whose ten mantissa bits take a nibble at bits 0-3 or 4-7
-//     unshifted: one mask-and-OR gives 1024 + q (nibbles 0, 2; the second
-//     after a single shift by 8) or 1024 + 16q (nibbles 1, 3), five logic
-//     ops per word instead of seven; the two MMAs of a word then cover even
-//     and odd k, and the odd accumulator is scaled by 1/16.  x is scaled by
-//     a power of two (largest |x| in [2^14, 2^15)) before its fp16
-//     conversion, which is exact for every element within 2^32 of the
-//     largest, and the scaling is undone in fp32;
+//     word becomes four 16-bit pairs (nibbles j, j+4) of q - zi, zi the
+//     zero point's integer part, and two mma.sync.m16n8k16 per word
+//     accumulate in fp32 against x, which was staged once per CTA in
+//     B-fragment order.  The zero point leaves the weights before any
+//     product, exactly: a row whose nibbles all equal z gives exactly 0.
+//     In bf16 one mask-and-OR per pair puts the nibble into the mantissa of
+//     128.0 (exactly 128 + q, after a shift by 4j) and one packed subtract
+//     of 128 + zi leaves q - zi.  With one column of x the pairs are fp16,
+//     whose ten mantissa bits take a nibble at bits 0-3 or 4-7 unshifted:
+//     one mask-and-OR gives 1024 + q (nibbles 0, 2; the second after a
+//     single shift by 8), minus 1024 + zi, or 1024 + 16q (nibbles 1, 3),
+//     times 1/16 minus 64 + zi in one packed FMA; the two MMAs of a word
+//     cover even and odd k.  x is scaled by a power of two (largest |x| in
+//     [2^14, 2^15)) before its fp16 conversion, which is exact for every
+//     element within 2^30 of the largest; a CTA whose slice of x spans more
+//     (or whose largest |x| is below 2^-86) runs the bf16 loop instead, with
+//     x scaled up by a power of two when its largest |x| is below 2^14.
+//     The scaling is undone in fp32;
 //   * the NC warps' partial sums of a row are added in warp order (each warp
 //     keeps its own row partials, or per 16-row tile through a named
 //     barrier when those do not fit), so results never depend on timing;
-//   * the offset is folded out exactly at the end:
-//       sum_k (q - z) x = sum_k (128 + q) x - (128 + z) sum_k x
-//     (fp16: sum_k (q - z) x = S_even + S_odd / 16 - 1024 X_even - 64 X_odd
-//     - z X, with S the two accumulators and X the sums of x);
+//   * only a fractional zero point leaves a term for the end:
+//       sum_k (q - z) x = sum_k (q - zi) x - (z - zi) sum_k x;
 //   * K-slices of a cluster meet at the row's owner: every rank pushes its
 //     partials of the rows the others own into their shared memory
 //     (st.async), and owners add the slices in rank order.
@@ -60,6 +63,7 @@
 
 #include <algorithm>
 #include <cstring>
+#include <type_traits>
 
 #include "common.cuh"
 #include "ptx.cuh"
@@ -80,7 +84,16 @@ constexpr int THREADS = (NC + 1) * 32;        // + one producer warp
 constexpr int CT = NC * 32;                   // consumer threads
 constexpr int KB = 128;                       // k per unit (one consumer warp per unit)
 constexpr int MAX_NST = 8;                    // stages in the ring (at most)
-constexpr int KCHUNK_MAX = 8192;              // k per stage at most (4 KB per row)
+#ifndef W4_GEMV_KCHUNK
+#define W4_GEMV_KCHUNK 8192
+#endif
+constexpr int KCHUNK_MAX = W4_GEMV_KCHUNK;    // k per stage at most (4 KB per row)
+#ifndef W4_GEMV_MINB
+#define W4_GEMV_MINB 1
+#endif
+#ifndef W4_GEMV_SMEM
+#define W4_GEMV_SMEM (227 * 1024)
+#endif
 #ifndef W4_GEMV_PREFETCH_STAGES
 #define W4_GEMV_PREFETCH_STAGES 3               // stages warmed in L2 before the wait (one column of x)
 #endif
@@ -88,7 +101,7 @@ constexpr int KCHUNK_MAX = 8192;              // k per stage at most (4 KB per r
 // Nibble mask and bf16 magic passed at run time so they stay in registers and
 // each mask-and-OR is a single three-input logic op.
 struct MaskMagic {
-    uint32_t mask, magic;
+    uint32_t mask, magic, magic_bf16;   // magic: of the loop with one column of x (fp16); bf16 loop
 };
 
 // Run-time shape of the pipeline, identical for every CTA of a launch (peers
@@ -109,7 +122,7 @@ struct Plan {
 };
 
 struct Layout {
-    int stage_bytes, xf, xzero, red, part, partw, xsw, xsum, sz, rcv, rxs, bars, abort, total;
+    int stage_bytes, xf, xzero, red, part, partw, xsw, xsum, sz, zi, rcv, rxs, bars, abort, total;
 };
 
 __host__ __device__ inline Layout make_layout(int C, const Plan& P) {
@@ -124,11 +137,12 @@ __host__ __device__ inline Layout make_layout(int C, const Plan& P) {
     L.part = o;      o += P.rows_cap * C * 4;
     L.partw = o;     o += P.perwarp ? NC * ((P.rows_cap + 15) / 16 * 16) * C * 4 : 0;
     L.xsw = o;       o += NC * C * 2 * 4;
-    // per column: [0, 8) this CTA's sum of x (unscaled), [8, 16) cluster
-    // totals, [16, 24) the offset term to fold out, [24, 32) the factor that
-    // undoes the scaling of x
+    // per column: [0, 8) this CTA's sum of x (unscaled), [8] the smallest
+    // nonzero |x| (bf16 bits, one column), [16, 24) the largest |x| (bf16
+    // bits), later 0, [24, 32) the factor that undoes the scaling of x
     L.xsum = o;      o += 32 * 4;
-    L.sz = o;        o += P.rows_cap * 8;          // (scale, zero) per row as fp32
+    L.sz = o;        o += P.rows_cap * 8;          // (scale, z - zint(z)) per row as fp32
+    L.zi = o;        o += P.rows_cap * 4;          // zint(z) per row
     // K split: the other slices' partials of the rows this rank owns (rows
     // ks, ks+S, ...) and their sums of x, pushed in by the peers
     L.rcv = o;       o += P.S > 1 ? P.S * ((P.rows_cap + P.S - 1) / P.S) * C * 4 : 0;
@@ -145,7 +159,7 @@ __host__ __device__ inline Layout make_layout(int C, const Plan& P) {
 // of permute_int4 (column groups of 4, 128-byte lines of 64 k, two's
 // complement nibbles), fp32 scale per column and no zero point.
 template <int C, bool PERM>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(THREADS, W4_GEMV_MINB)
 gemv_tma_kernel(const uint8_t* __restrict__ qw, const void* __restrict__ scale,
                 const void* __restrict__ zero, const __nv_bfloat16* __restrict__ x,
                 __nv_bfloat16* __restrict__ d, int N, int K, Plan P, MaskMagic dq,
@@ -190,18 +204,20 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const void* __restrict__ scale,
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     // one column of the row layout runs on fp16 MMAs (x scaled by a power of
-    // two, weights unpacked with five logic ops per word); the others on bf16
-    constexpr bool F16 = !PERM && C == 1;
-    // (scale, zero) of output row r; the permuted operand is symmetric and
-    // its nibbles are read as 8 + q, which the fold treats as zero point 8
-    auto load_sz = [&](int r) -> float2 {
-        if constexpr (PERM) {
-            return make_float2(static_cast<const float*>(scale)[r], 8.0f);
-        } else {
-            return make_float2(__bfloat162float(static_cast<const __nv_bfloat16*>(scale)[r]),
-                               __bfloat162float(static_cast<const __nv_bfloat16*>(zero)[r]));
-        }
+    // two, weights unpacked with five logic ops per word) when the CTA's
+    // slice of x fits fp16's range; everything else on bf16
+    constexpr bool CAN_F16 = !PERM && C == 1;
+    // scale of output row r and its zero point split into the integer part
+    // taken out of the weights and the rest folded out at the end; the
+    // permuted operand is symmetric (zero point 0)
+    auto load_z = [&](int r) -> float {
+        return PERM ? 0.0f : __bfloat162float(static_cast<const __nv_bfloat16*>(zero)[r]);
     };
+    auto load_s = [&](int r) -> float {
+        return PERM ? static_cast<const float*>(scale)[r]
+                    : __bfloat162float(static_cast<const __nv_bfloat16*>(scale)[r]);
+    };
+    int* zi_s = reinterpret_cast<int*>(sm + L.zi);
 
     if (tid == 0) {
         for (int s = 0; s < NST; ++s) {
@@ -211,6 +227,7 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const void* __restrict__ scale,
         mbar_init(bar_x, 1);
         *abort_flag = 0;
         for (int c = 0; c < 8; ++c) reinterpret_cast<uint32_t*>(xsum)[16 + c] = 0;   // column maxima of |x|
+        reinterpret_cast<uint32_t*>(xsum)[8] = 0xFFFFu;                              // (smallest nonzero |x|) - 1
         if (S > 1) {
             // every peer pushes its partials of the rows this rank owns and its
             // C sums of x; they complete bytes on this barrier
@@ -326,15 +343,28 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const void* __restrict__ scale,
         if (lane == 0) mbar_drain(bar_x, 0);
     } else {
         // ------------------------------------------------------------ consumers
-        // scale / zero of this CTA's rows: the first two per thread are loaded
-        // now into registers (nothing waits on them) and stored after the
-        // main loop, so their latency never delays the start
-        float2 sz_pf[2];
+        // scale / zero point of this CTA's rows: the first two per thread are
+        // loaded now into registers (nothing waits on them); zint(z) goes to
+        // shared memory once x has arrived (the main loop subtracts it from
+        // the weights), the scale and z - zint(z) after the main loop
+        float sc_pf[2], z_pf[2];
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
             const int i = tid + j * CT;
-            if (i < nrows) sz_pf[j] = load_sz(r0 + i);
+            if (i < nrows) {
+                sc_pf[j] = load_s(r0 + i);
+                z_pf[j] = load_z(r0 + i);
+            }
         }
+        auto store_zint = [&]() {
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int i = tid + j * CT;
+                if (i < nrows) zi_s[i] = zint(z_pf[j]);
+            }
+            for (int i = tid + 2 * CT; i < nrows; i += CT) zi_s[i] = zint(load_z(r0 + i));
+        };
+        bool f16 = false;   // this CTA's main loop runs on fp16 MMAs
         // x as B fragments.  Row layout: entry (kb, word p, n, t4) holds, for
         // kk = kb*128 + 32*t4 + 8*p, the pairs (x[kk], x[kk+4]) (x[kk+1],
         // x[kk+5]) (x[kk+2], x[kk+6]) (x[kk+3], x[kk+7]) in bf16 -- the b0b1 /
@@ -370,24 +400,29 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const void* __restrict__ scale,
                         make_uint4(0, 0, 0, 0);
                 }
                 mbar_wait_fast(bar_x, 0, abort_flag);
+                store_zint();
             } else {
                 // x arrived by bulk copies as dense rows (row n at n*klen*2
                 // bytes) in the fragment buffer itself: every thread reads its
-                // entries' sources into registers (on fp16 noting the largest
-                // |x|: warp maxima meet in shared memory); after a barrier it
-                // writes them in fragment order (on fp16 scaled and
-                // converted).  At most XR entries per thread: the plan keeps
-                // the fragments within 80 KB = 10 entries per consumer thread.
+                // entries' sources into registers (with one column noting the
+                // largest and the smallest nonzero |x|: warp extremes meet in
+                // shared memory); after a barrier it writes them in fragment
+                // order (fp16: scaled and converted; bf16 with one column:
+                // scaled by a power of two when the largest |x| is below
+                // 2^14).  At most XR entries per thread: the plan keeps the
+                // fragments within 10 entries per consumer thread.
                 const int per_n = nkb * 16;
                 constexpr int XR = 10;
                 const int dn = per_n > 0 ? CT / per_n : 0, dj = CT - dn * per_n;
                 const int n_cur = per_n > 0 ? tid / per_n : C, j_cur = tid - n_cur * per_n;
                 const int mine = (C * per_n - tid + CT - 1) / CT;   // entries of this thread (<= XR)
                 const uint8_t* rows = reinterpret_cast<const uint8_t*>(xf);
-                uint32_t* xmax = reinterpret_cast<uint32_t*>(xsum) + 16;   // fp16: max |x| bits, zeroed at entry
+                uint32_t* xmax = reinterpret_cast<uint32_t*>(xsum) + 16;   // max |x| bits, zeroed at entry
+                uint32_t* xmin = reinterpret_cast<uint32_t*>(xsum) + 8;    // min nonzero |x| bits - 1
                 uint4 v[XR];
-                uint32_t mx = 0;
+                uint32_t mx = 0, mn = 0xFFFFu;
                 mbar_wait_fast(bar_x, 0, abort_flag);
+                store_zint();
                 int n = n_cur, j = j_cur;
 #pragma unroll
                 for (int b = 0; b < XR; ++b) {
@@ -396,27 +431,44 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const void* __restrict__ scale,
                     if (n < C) {
                         const int kk = (j >> 4) * KB + 32 * (j & 3) + 8 * ((j >> 2) & 3);
                         if (kk < klen) v[b] = *reinterpret_cast<const uint4*>(rows + (n * klen + kk) * 2);
-                        if constexpr (F16) {
-                            // |x| as bf16 bit patterns with the sign cleared (ordered as integers)
-                            const uint32_t m2 = __vmaxu2(__vmaxu2(v[b].x & 0x7FFF7FFFu, v[b].y & 0x7FFF7FFFu),
-                                                         __vmaxu2(v[b].z & 0x7FFF7FFFu, v[b].w & 0x7FFF7FFFu));
+                        if constexpr (CAN_F16) {
+                            // |x| as bf16 bit patterns with the sign cleared
+                            // (ordered as integers); |x| - 1 wraps 0 to 0xFFFF
+                            const uint32_t a0 = v[b].x & 0x7FFF7FFFu, a1 = v[b].y & 0x7FFF7FFFu;
+                            const uint32_t a2 = v[b].z & 0x7FFF7FFFu, a3 = v[b].w & 0x7FFF7FFFu;
+                            const uint32_t m2 = __vmaxu2(__vmaxu2(a0, a1), __vmaxu2(a2, a3));
                             mx = max(mx, max(m2 & 0xFFFFu, m2 >> 16));
+                            const uint32_t n2 = __vminu2(__vminu2(__vsub2(a0, 0x00010001u), __vsub2(a1, 0x00010001u)),
+                                                         __vminu2(__vsub2(a2, 0x00010001u), __vsub2(a3, 0x00010001u)));
+                            mn = min(mn, min(n2 & 0xFFFFu, n2 >> 16));
                         }
                     }
                     j += dj;
                     n += dn;
                     if (j >= per_n) { j -= per_n; ++n; }
                 }
-                if constexpr (F16) {
+                if constexpr (CAN_F16) {
                     const uint32_t wm = __reduce_max_sync(0xffffffffu, mx);
-                    if (lane == 0 && wm != 0) atomicMax(&xmax[0], wm);
+                    const uint32_t wn = __reduce_min_sync(0xffffffffu, mn);
+                    if (lane == 0) {
+                        if (wm != 0) atomicMax(&xmax[0], wm);
+                        if (wn != 0xFFFFu) atomicMin(&xmin[0], wn);
+                    }
                 }
-                named_barrier(1, CT);   // every source read (and the maximum of |x| final)
-                // fp16: x is scaled by 2^e, e = 141 - (biased bf16 exponent of
-                // max|x|), so that max|x| 2^e lies in [2^14, 2^15); at most 100
-                // (all-zero or tiny x).  se / so: sums of the converted x over
-                // even / odd k.
-                const float sc = F16 ? __int_as_float((127 + min(100, 141 - static_cast<int>(xmax[0] >> 7))) << 23) : 1.0f;
+                named_barrier(1, CT);   // every source read (and the extremes of |x| final)
+                // fp16 when every nonzero |x| lies within 2^30 of the largest
+                // and the largest is at least 2^-86: x is scaled by 2^e, e =
+                // 141 - (biased bf16 exponent of max|x|) <= 100, so that
+                // max|x| 2^e lies in [2^14, 2^15) and every element stays an
+                // exact fp16 (normal, or subnormal with 8 significant bits).
+                // Otherwise bf16, scaled by 2^min(126, e) only when e > 0
+                // (exact: bf16 has fp32's exponent range).  se / so: sums of
+                // the converted x over even / odd k (fp16).
+                const int emax = static_cast<int>(xmax[0] >> 7), emin = static_cast<int>((xmin[0] + 1) >> 7);
+                f16 = CAN_F16 && (xmax[0] == 0 || (emax >= 41 && emax - emin <= 30));
+                const float sc = f16 ? __int_as_float((127 + min(100, 141 - emax)) << 23)
+                                 : CAN_F16 ? __int_as_float((127 + min(126, max(0, 141 - emax))) << 23)
+                                           : 1.0f;
                 float se = 0.f, so = 0.f;
                 n = n_cur;
                 j = j_cur;
@@ -425,8 +477,17 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const void* __restrict__ scale,
                     if (b >= mine) break;
                     if (n < C) {
                         const int t = j & 3, p = (j >> 2) & 3, kb = j >> 4;
-                        const uint4 r = v[b];
-                        if constexpr (!F16) {
+                        uint4 r = v[b];
+                        if (!f16) {
+                            if (CAN_F16 && sc != 1.0f) {
+                                // times a power of two, exact in bf16
+                                auto up = [&](uint32_t w2) {
+                                    const uint32_t lo = __float_as_uint(bf16_bits_to_f32(w2 & 0xFFFFu) * sc) >> 16;
+                                    const uint32_t hi = __float_as_uint(bf16_bits_to_f32(w2 >> 16) * sc) >> 16;
+                                    return lo | (hi << 16);
+                                };
+                                r = make_uint4(up(r.x), up(r.y), up(r.z), up(r.w));
+                            }
                             xf[((kb * 4 + p) * C + n) * 4 + t] =
                                 make_uint4(__byte_perm(r.x, r.z, 0x5410), __byte_perm(r.x, r.z, 0x7632),
                                            __byte_perm(r.y, r.w, 0x5410), __byte_perm(r.y, r.w, 0x7632));
@@ -452,7 +513,7 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const void* __restrict__ scale,
                     n += dn;
                     if (j >= per_n) { j -= per_n; ++n; }
                 }
-                if constexpr (F16) {
+                if (f16) {
 #pragma unroll
                     for (int o = 16; o > 0; o >>= 1) {
                         se += __shfl_xor_sync(0xffffffffu, se, o);
@@ -471,7 +532,8 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const void* __restrict__ scale,
             // each MMA over a staged fragment into column sums (fp32
             // accumulation, as in the main product).  Warps take the (kb, word)
             // pairs round-robin, two at a time on independent accumulators.
-            if constexpr (!F16) {
+            // They are needed only to fold out a fractional zero point.
+            if (!f16) {
                 const uint32_t ones = 0x3F803F80u;   // bf16x2 (1.0, 1.0)
                 const uint32_t a1s[4] = {ones, ones, ones, ones};
                 float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
@@ -511,139 +573,165 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const void* __restrict__ scale,
                     se += xsw[(w * C + tid) * 2];
                     so += xsw[(w * C + tid) * 2 + 1];
                 }
-                if constexpr (!F16) {
-                    // nibbles read as 128 + q (row layout) or 128 + (q + 8)
-                    // (permuted layout, zero point 8): offset 128
-                    xsum[16 + tid] = 128.0f * se;
-                    xsum[24 + tid] = 1.0f;
-                    xsum[tid] = se;
-                } else {
-                    // even k read as 1024 + q, odd k as 1024 + 16q (the odd
-                    // accumulator is scaled by 1/16 before the fold)
-                    const int e = min(100, 141 - static_cast<int>(reinterpret_cast<const uint32_t*>(xsum)[16 + tid] >> 7));
-                    const float inv = __int_as_float((127 - e) << 23);   // 2^-e
-                    xsum[24 + tid] = inv;
-                    xsum[16 + tid] = fmaf(64.0f, so, 1024.0f * se);
-                    xsum[tid] = (se + so) * inv;
-                }
+                // the accumulators hold sum (q - zi) x in the units of the
+                // staged x: undo its scaling by 2^e (one column only)
+                const int emax = static_cast<int>(reinterpret_cast<const uint32_t*>(xsum)[16 + tid] >> 7);
+                const int e = f16 ? min(100, 141 - emax) : CAN_F16 ? min(126, max(0, 141 - emax)) : 0;
+                const float inv = __int_as_float((127 - e) << 23);   // 2^-e
+                xsum[24 + tid] = inv;
+                xsum[16 + tid] = 0.0f;
+                xsum[tid] = (se + so) * inv;
             }
         }
 
         // main loop: units of each stage go round-robin to the warps, the
         // rotation carrying over from stage to stage
         const int xkb_stride = bl ? 4 * xw_stride : 0;   // next unit
-        const uint32_t mask = dq.mask, magic = dq.magic, mask_hi = dq.mask << 4;
+        const uint32_t mask = dq.mask, mask_hi = dq.mask << 4;
         const int row_off_a = g * pitch + 16 * t4, row_off_b = (g + 8) * pitch + 16 * t4;
         // permuted operand: this lane's ldmatrix row -- column r + 8*(i & 1)
         // of matrix i = lane / 8 (r = lane % 8), 32-k group +(i >> 1); the
         // column groups sit 4*pitch apart, lines of 128 bytes, 32 bytes per column
         const int ldm_col = (lane & 7) + 8 * ((lane >> 3) & 1);
         const uint32_t ldm_off = (ldm_col >> 2) * 4 * pitch + (ldm_col & 3) * 32 + (lane >> 4) * 16;
-        // nibble -> bf16 (128 + q, or 136 + q for two's complement nibbles)
-        auto unpack = [&](uint32_t v) { return PERM ? pass_flip_or(v, mask, magic) : and_or(v, mask, magic); };
         int slot = 0, round = 0, first = warp;   // first unit of this warp in the current stage
         const int rows16 = (P.rows_cap + 15) / 16 * 16;
-        for (int tile = 0; tile < ntiles; ++tile) {
-            float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};
-            for (int ch = 0; ch < nch; ++ch) {
-                const int units = (min(P.kchunk, klen - ch * P.kchunk) + KB - 1) / KB;
-                const bool ok = mbar_wait_fast(bar_full + 8 * slot, round & 1, abort_flag);
-                if (ok) {
-                    const uint8_t* st = sm + slot * L.stage_bytes;
-                    for (int u = first; u < units; u += NC) {
-                        const uint4* xb = xlane + (ch * (P.kchunk / KB) + u) * xkb_stride;
-                        uint32_t wav[4], wbv[4];
-                        if constexpr (PERM) {
-                            // words of columns g and g+8 for the unit's four 32-k groups
-                            const uint32_t a = smem_u32(st) + ldm_off + u * 256;
-                            ldmatrix_x4(a, wav[0], wbv[0], wav[1], wbv[1]);
-                            ldmatrix_x4(a + 128, wav[2], wbv[2], wav[3], wbv[3]);
-                        } else {
-                            const uint4 wa = *reinterpret_cast<const uint4*>(st + row_off_a + u * 64);
-                            const uint4 wb = *reinterpret_cast<const uint4*>(st + row_off_b + u * 64);
-                            wav[0] = wa.x; wav[1] = wa.y; wav[2] = wa.z; wav[3] = wa.w;
-                            wbv[0] = wb.x; wbv[1] = wb.y; wbv[2] = wb.z; wbv[3] = wb.w;
-                        }
-#pragma unroll
-                        for (int w = 0; w < 4; ++w) {
-                            uint4 bx;
+        // H: fp16 MMAs (one column of x, within fp16's range), else bf16
+        auto main_loop = [&](auto mode) {
+            constexpr bool H = decltype(mode)::value;
+            const uint32_t magic = H ? dq.magic : dq.magic_bf16;
+            // nibble -> bf16 128 + q (row layout) or 136 + q (two's complement
+            // nibbles of the permuted layout, whose zero point is 0)
+            auto unpack = [&](uint32_t v) { return PERM ? pass_flip_or(v, mask, magic) : and_or(v, mask, magic); };
+            for (int tile = 0; tile < ntiles; ++tile) {
+                // what the unpack leaves above q - zi for rows g and g+8 of the
+                // tile: bf16 128 + zi (136 on the permuted layout); fp16 1024 +
+                // zi for even k, and -(64 + zi) after the scaling by 1/16 of
+                // 1024 + 16q for odd k
+                const int ra = tile * 16 + g, rb8 = ra + 8;
+                const uint32_t za = PERM || ra >= nrows ? 0u : static_cast<uint32_t>(zi_s[ra]);
+                const uint32_t zb = PERM || rb8 >= nrows ? 0u : static_cast<uint32_t>(zi_s[rb8]);
+                const uint32_t ze_a = (H ? 0x6400u + za : PERM ? 0x4308u : 0x4300u + za) * 0x10001u;
+                const uint32_t ze_b = (H ? 0x6400u + zb : PERM ? 0x4308u : 0x4300u + zb) * 0x10001u;
+                const uint32_t zo_a = (0xD400u + 16u * za) * 0x10001u, zo_b = (0xD400u + 16u * zb) * 0x10001u;
+                constexpr uint32_t kSixteenth = 0x2C002C00u;   // fp16x2 (1/16, 1/16)
+                float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};
+                for (int ch = 0; ch < nch; ++ch) {
+                    const int units = (min(P.kchunk, klen - ch * P.kchunk) + KB - 1) / KB;
+                    const bool ok = mbar_wait_fast(bar_full + 8 * slot, round & 1, abort_flag);
+                    if (ok) {
+                        const uint8_t* st = sm + slot * L.stage_bytes;
+                        for (int u = first; u < units; u += NC) {
+                            const uint4* xb = xlane + (ch * (P.kchunk / KB) + u) * xkb_stride;
+                            uint32_t wav[4], wbv[4];
                             if constexpr (PERM) {
-                                ldmatrix_x4(xa + ((ch * (P.kchunk / KB) + u) * 4 + w) * xs, bx.x, bx.y, bx.z, bx.w);
+                                // words of columns g and g+8 for the unit's four 32-k groups
+                                const uint32_t a = smem_u32(st) + ldm_off + u * 256;
+                                ldmatrix_x4(a, wav[0], wbv[0], wav[1], wbv[1]);
+                                ldmatrix_x4(a + 128, wav[2], wbv[2], wav[3], wbv[3]);
                             } else {
-                                bx = xb[w * xw_stride];
+                                const uint4 wa = *reinterpret_cast<const uint4*>(st + row_off_a + u * 64);
+                                const uint4 wb = *reinterpret_cast<const uint4*>(st + row_off_b + u * 64);
+                                wav[0] = wa.x; wav[1] = wa.y; wav[2] = wa.z; wav[3] = wa.w;
+                                wbv[0] = wb.x; wbv[1] = wb.y; wbv[2] = wb.z; wbv[3] = wb.w;
                             }
-                            const uint32_t va = wav[w], vb = wbv[w];
-                            if constexpr (!F16) {
-                                const uint32_t a0[4] = {unpack(va), unpack(vb), unpack(va >> 4), unpack(vb >> 4)};
-                                const uint32_t a1[4] = {unpack(va >> 8), unpack(vb >> 8), unpack(va >> 12),
-                                                        unpack(vb >> 12)};
-                                mma_bf16(acc, a0, bx.x, bx.y);
-                                mma_bf16(acc2, a1, bx.z, bx.w);
-                            } else {
-                                // fp16 1024 + q from nibbles 0 and 2 (bits 0-3 of each
-                                // half, after one shift by 8 for nibble 2), 1024 + 16q
-                                // from nibbles 1 and 3 (bits 4-7): five logic ops per word
-                                const uint32_t va8 = va >> 8, vb8 = vb >> 8;
-                                const uint32_t a0[4] = {and_or(va, mask, magic), and_or(vb, mask, magic),
-                                                        and_or(va8, mask, magic), and_or(vb8, mask, magic)};
-                                const uint32_t a1[4] = {and_or(va, mask_hi, magic), and_or(vb, mask_hi, magic),
-                                                        and_or(va8, mask_hi, magic), and_or(vb8, mask_hi, magic)};
-                                mma_f16(acc, a0, bx.x, bx.y);
-                                mma_f16(acc2, a1, bx.z, bx.w);
+#pragma unroll
+                            for (int w = 0; w < 4; ++w) {
+                                uint4 bx;
+                                if constexpr (PERM) {
+                                    ldmatrix_x4(xa + ((ch * (P.kchunk / KB) + u) * 4 + w) * xs, bx.x, bx.y, bx.z,
+                                                bx.w);
+                                } else {
+                                    bx = xb[w * xw_stride];
+                                }
+                                const uint32_t va = wav[w], vb = wbv[w];
+                                if constexpr (!H) {
+                                    const uint32_t a0[4] = {sub_bf16x2(unpack(va), ze_a), sub_bf16x2(unpack(vb), ze_b),
+                                                            sub_bf16x2(unpack(va >> 4), ze_a),
+                                                            sub_bf16x2(unpack(vb >> 4), ze_b)};
+                                    const uint32_t a1[4] = {sub_bf16x2(unpack(va >> 8), ze_a),
+                                                            sub_bf16x2(unpack(vb >> 8), ze_b),
+                                                            sub_bf16x2(unpack(va >> 12), ze_a),
+                                                            sub_bf16x2(unpack(vb >> 12), ze_b)};
+                                    mma_bf16(acc, a0, bx.x, bx.y);
+                                    mma_bf16(acc2, a1, bx.z, bx.w);
+                                } else {
+                                    // fp16 1024 + q from nibbles 0 and 2 (bits 0-3 of
+                                    // each half, after one shift by 8 for nibble 2),
+                                    // 1024 + 16q from nibbles 1 and 3 (bits 4-7)
+                                    const uint32_t va8 = va >> 8, vb8 = vb >> 8;
+                                    const uint32_t a0[4] = {
+                                        sub_f16x2(and_or(va, mask, magic), ze_a), sub_f16x2(and_or(vb, mask, magic), ze_b),
+                                        sub_f16x2(and_or(va8, mask, magic), ze_a),
+                                        sub_f16x2(and_or(vb8, mask, magic), ze_b)};
+                                    const uint32_t a1[4] = {fma_f16x2(and_or(va, mask_hi, magic), kSixteenth, zo_a),
+                                                            fma_f16x2(and_or(vb, mask_hi, magic), kSixteenth, zo_b),
+                                                            fma_f16x2(and_or(va8, mask_hi, magic), kSixteenth, zo_a),
+                                                            fma_f16x2(and_or(vb8, mask_hi, magic), kSixteenth, zo_b)};
+                                    mma_f16(acc, a0, bx.x, bx.y);
+                                    mma_f16(acc2, a1, bx.z, bx.w);
+                                }
                             }
                         }
                     }
+                    // rotate: this warp's first unit of the next stage
+                    first -= units % NC;
+                    if (first < 0) first += NC;
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
+                    if (++slot == NST) { slot = 0; ++round; }
                 }
-                // rotate: this warp's first unit of the next stage
-                first -= units % NC;
-                if (first < 0) first += NC;
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
-                if (++slot == NST) { slot = 0; ++round; }
-            }
-            const int c0 = 2 * t4, c1 = 2 * t4 + 1;
-            // the odd-k accumulator holds 16x its share on the row layout
-            constexpr float kOdd = F16 ? 0.0625f : 1.0f;
-            if (P.perwarp) {
-                // this warp's partial of the tile; warps are added at the end
-                float* pw = partw + (static_cast<size_t>(warp) * rows16 + tile * 16) * C;
-                if (c0 < C) {
-                    pw[g * C + c0] = fmaf(acc2[0], kOdd, acc[0]);
-                    pw[(g + 8) * C + c0] = fmaf(acc2[2], kOdd, acc[2]);
-                }
-                if (c1 < C) {
-                    pw[g * C + c1] = fmaf(acc2[1], kOdd, acc[1]);
-                    pw[(g + 8) * C + c1] = fmaf(acc2[3], kOdd, acc[3]);
-                }
-            } else {
-                // tile partials, added in warp order now (bounded shared memory)
-                float* rb = red + ((tile & 1) * NC + warp) * 16 * C;
-                if (c0 < C) {
-                    rb[g * C + c0] = fmaf(acc2[0], kOdd, acc[0]);
-                    rb[(g + 8) * C + c0] = fmaf(acc2[2], kOdd, acc[2]);
-                }
-                if (c1 < C) {
-                    rb[g * C + c1] = fmaf(acc2[1], kOdd, acc[1]);
-                    rb[(g + 8) * C + c1] = fmaf(acc2[3], kOdd, acc[3]);
-                }
-                named_barrier(1, CT);
-                for (int i = tid; i < 16 * C; i += CT) {
-                    const int r = i / C;
-                    if (tile * 16 + r < nrows) {
-                        float v = 0.f;
-                        for (int w = 0; w < NC; ++w) v += red[((tile & 1) * NC + w) * 16 * C + i];
-                        const int c = i - r * C;
-                        part[(tile * 16) * C + i] = (v - xsum[16 + c]) * xsum[24 + c];
+                const int c0 = 2 * t4, c1 = 2 * t4 + 1;
+                if (P.perwarp) {
+                    // this warp's partial of the tile; warps are added at the end
+                    float* pw = partw + (static_cast<size_t>(warp) * rows16 + tile * 16) * C;
+                    if (c0 < C) {
+                        pw[g * C + c0] = acc[0] + acc2[0];
+                        pw[(g + 8) * C + c0] = acc[2] + acc2[2];
+                    }
+                    if (c1 < C) {
+                        pw[g * C + c1] = acc[1] + acc2[1];
+                        pw[(g + 8) * C + c1] = acc[3] + acc2[3];
+                    }
+                } else {
+                    // tile partials, added in warp order now (bounded shared memory)
+                    float* rbuf = red + ((tile & 1) * NC + warp) * 16 * C;
+                    if (c0 < C) {
+                        rbuf[g * C + c0] = acc[0] + acc2[0];
+                        rbuf[(g + 8) * C + c0] = acc[2] + acc2[2];
+                    }
+                    if (c1 < C) {
+                        rbuf[g * C + c1] = acc[1] + acc2[1];
+                        rbuf[(g + 8) * C + c1] = acc[3] + acc2[3];
+                    }
+                    named_barrier(1, CT);
+                    for (int i = tid; i < 16 * C; i += CT) {
+                        const int r = i / C;
+                        if (tile * 16 + r < nrows) {
+                            float v = 0.f;
+                            for (int w = 0; w < NC; ++w) v += red[((tile & 1) * NC + w) * 16 * C + i];
+                            const int c = i - r * C;
+                            part[(tile * 16) * C + i] = v * xsum[24 + c];
+                        }
                     }
                 }
             }
+        };
+        if constexpr (CAN_F16) {
+            if (f16) main_loop(std::true_type{});
+            else main_loop(std::false_type{});
+        } else {
+            main_loop(std::false_type{});
         }
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
             const int i = tid + j * CT;
-            if (i < nrows) sz[i] = sz_pf[j];
+            if (i < nrows) sz[i] = make_float2(sc_pf[j], z_pf[j] - static_cast<float>(zint(z_pf[j])));
         }
-        for (int i = tid + 2 * CT; i < nrows; i += CT) sz[i] = load_sz(r0 + i);
+        for (int i = tid + 2 * CT; i < nrows; i += CT) {
+            const float z = load_z(r0 + i);
+            sz[i] = make_float2(load_s(r0 + i), z - static_cast<float>(zint(z)));
+        }
         if (S == 1) {
             // no K split: add the warps' partials (or take the tile sums),
             // fold the zero point, scale and store straight away
@@ -654,7 +742,7 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const void* __restrict__ scale,
                 if (P.perwarp) {
                     v = 0.f;
                     for (int w = 0; w < NC; ++w) v += partw[static_cast<size_t>(w) * rows16 * C + i];
-                    v = (v - xsum[16 + c]) * xsum[24 + c];
+                    v *= xsum[24 + c];
                 } else {
                     v = part[i];
                 }
@@ -667,7 +755,7 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const void* __restrict__ scale,
                 float v = 0.f;
                 for (int w = 0; w < NC; ++w) v += partw[static_cast<size_t>(w) * rows16 * C + i];
                 const int c = i % C;
-                part[i] = (v - xsum[16 + c]) * xsum[24 + c];
+                part[i] = v * xsum[24 + c];
             }
         }
     }
@@ -730,8 +818,10 @@ namespace {
 
 using namespace gtma;
 
-constexpr int kSmemMax = 227 * 1024;
-constexpr size_t kXfBudget = 80 * 1024;
+constexpr int kSmemMax = W4_GEMV_SMEM;
+// x fragments: at most 10 16-byte entries per consumer thread (the staging
+// pass keeps them in registers)
+constexpr size_t kXfBudget = static_cast<size_t>(10) * CT * 16;
 
 // Pipeline shape for (N, K, C) on `sms` SMs; nst == 0 if nothing fits.
 template <int C, bool PERM>
@@ -854,9 +944,9 @@ w4_status launch_gemv_tma_t(const void* qw, const void* scale, const void* zero,
     }
     // row layout: (v & 0x000F000F) | 0x43004300; permuted (two's complement):
     // pass bits 0-2, invert bit 3, set the exponent of 128.0
-    const MaskMagic dq = PERM      ? MaskMagic{0x43074307u, 0x43084308u}
-                         : C == 1 ? MaskMagic{0x000F000Fu, 0x64006400u}   // fp16 1024 + q
-                                  : MaskMagic{0x000F000Fu, 0x43004300u};  // bf16 128 + q
+    const MaskMagic dq = PERM      ? MaskMagic{0x43074307u, 0x43084308u, 0x43084308u}
+                         : C == 1 ? MaskMagic{0x000F000Fu, 0x64006400u, 0x43004300u}   // fp16 1024 + q
+                                  : MaskMagic{0x000F000Fu, 0x43004300u, 0x43004300u};  // bf16 128 + q
     e = cudaLaunchKernelEx(&cfg, kern, static_cast<const uint8_t*>(qw), scale, zero,
                            static_cast<const __nv_bfloat16*>(x), static_cast<__nv_bfloat16*>(d), N, K, P, dq, tm16,
                            tm4);

@@ -321,6 +321,32 @@ __device__ __forceinline__ uint32_t pass_flip_or(uint32_t a, uint32_t b, uint32_
     return d;
 }
 
+// Packed 16-bit arithmetic, round to nearest: a - b on bf16x2 and f16x2, and
+// a * b + c on f16x2 (one rounding).  The dequant uses them only where the
+// exact result is representable (small integers), so they are exact there.
+__device__ __forceinline__ uint32_t sub_bf16x2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+__device__ __forceinline__ uint32_t sub_f16x2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+__device__ __forceinline__ uint32_t fma_f16x2(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+// Integer part of a zero point taken out of the weights exactly before any
+// product: the nearest integer clamped to the nibble range 0..15 (what is
+// left, z - zint(z), is folded out after accumulation; |z - zint(z)| is at
+// most the distance from z to every nibble value, so that fold's rounding
+// stays within the bound relative to sum |(q - z) x|).
+__device__ __forceinline__ int zint(float z) { return static_cast<int>(fminf(fmaxf(rintf(z), 0.0f), 15.0f)); }
+
 // Four 8x8 b16 matrices from shared memory: lanes 8i..8i+7 give the row
 // addresses of matrix i; lane 4g+t receives row g, elements 2t and 2t+1 of
 // each matrix (one 32-bit word per matrix).

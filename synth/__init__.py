@@ -41,17 +41,45 @@ class GemvInputs:
     act: str
 
 
-def gemv_inputs(N, K, C, act="bf16", seed=0, scale_range=None, zero_value=8.0):
+def gemv_inputs(N, K, C, act="bf16", seed=0, scale_range=None, zero_value=8.0, q_dist="uniform", q_sigma=0.7,
+                zero_rows=0):
     """Packed uint4 weights uniform 0..15, per-row scale, constant zero, x ~ N(0,1).
 
     act="bf16": scale U[0.001, 0.01], zero 8, x N(0,1), all bf16.
     act="f32":  scale U[0.5, 2]/16, zero 8.0, x N(0,1), all fp32.
+
+    q_dist picks the nibble distribution (each nibble drawn independently, so
+    the two nibbles of a byte are interchangeable and no packing order is
+    involved):
+      "uniform"  0..15 (the workloads' draw: uniform random bytes);
+      "near"     round(zero_value + N(0, q_sigma)) clamped to 0..15, the
+                 shape of real asymmetric int4 weights clustered at their
+                 zero point (zero_value must be an integer);
+      "zero"     every nibble equal to zero_value (an integer 0..15).
+    zero_rows = m > 0 additionally sets every nibble of rows 0, m, 2m, ... to
+    zero_value.  The uniform draw leaves the bytes of the default call
+    unchanged.
     """
     if K % 8:
         raise ValueError("K must be a multiple of 8")
     g = _gen(seed)
-    qbytes = torch.randint(0, 256, (N, K // 2), dtype=torch.uint8, generator=g)
-    qweight = qbytes.view(torch.int32)
+    zi = int(round(float(zero_value)))
+    if q_dist != "uniform" or zero_rows:
+        if float(zero_value) != zi or not 0 <= zi <= 15:
+            raise ValueError("q_dist / zero_rows need an integer zero_value in 0..15")
+    if q_dist == "uniform":
+        qbytes = torch.randint(0, 256, (N, K // 2), dtype=torch.uint8, generator=g)
+    elif q_dist == "near":
+        nib = torch.round(torch.randn(N, K, generator=g, dtype=torch.float64) * q_sigma + zi).clamp(0, 15)
+        nib = nib.to(torch.uint8).view(N, K // 2, 2)
+        qbytes = nib[:, :, 0] + 16 * nib[:, :, 1]
+    elif q_dist == "zero":
+        qbytes = torch.full((N, K // 2), 17 * zi, dtype=torch.uint8)
+    else:
+        raise ValueError(q_dist)
+    if zero_rows:
+        qbytes[::zero_rows] = 17 * zi
+    qweight = qbytes.contiguous().view(torch.int32)
     if act == "f32":
         lo, hi = scale_range or (0.5 / 16, 2.0 / 16)
         dt = torch.float32
@@ -76,14 +104,31 @@ class PackedGemvInputs:
     C: int
 
 
-def packed_gemv_inputs(N, K, C, seed=0, scale_range=(0.005, 0.02)):
+def packed_gemv_inputs(N, K, C, seed=0, scale_range=(0.005, 0.02), q_dist="uniform", q_sigma=0.7, zero_cols=0):
     """The quantiser's operand layout: uniform random bytes (= independent
     uniform nibbles), fp32 per-column scale in the range the quantiser gives
-    for N(0, 0.02) weights, x ~ N(0,1) bf16."""
+    for N(0, 0.02) weights, x ~ N(0,1) bf16.
+
+    q_dist: "uniform" (uniform bytes), "near" (two's complement nibbles
+    round(N(0, q_sigma)) clamped to -8..7, each drawn independently) or
+    "zero" (every weight 0); zero_cols = m > 0 also zeroes columns 0, m, 2m,
+    ... (the operand is symmetric: a zero weight is the nibble 0)."""
     if K % 2:
         raise ValueError("K must be even")
     g = _gen(seed)
-    packed = torch.randint(0, 256, (K // 2, N), dtype=torch.uint8, generator=g)
+    if q_dist == "uniform":
+        packed = torch.randint(0, 256, (K // 2, N), dtype=torch.uint8, generator=g)
+    elif q_dist == "near":
+        nib = torch.round(torch.randn(K, N, generator=g, dtype=torch.float64) * q_sigma).clamp(-8, 7)
+        nib = nib.to(torch.int16).view(K // 2, 2, N) & 15
+        packed = (nib[:, 0, :] + 16 * nib[:, 1, :]).to(torch.uint8)
+    elif q_dist == "zero":
+        packed = torch.zeros((K // 2, N), dtype=torch.uint8)
+    else:
+        raise ValueError(q_dist)
+    if zero_cols:
+        packed[:, ::zero_cols] = 0
+    packed = packed.contiguous()
     lo, hi = scale_range
     scale = torch.rand(N, generator=g, dtype=torch.float32) * (hi - lo) + lo
     x = torch.randn(C, K, generator=g, dtype=torch.float32).to(torch.bfloat16)

@@ -37,7 +37,8 @@ def bf16_half_ulp(ref):
     to the bf16 output (bf16 carries 8 significant bits)."""
     ref = np.abs(np.asarray(ref, dtype=np.float64))
     _, e = np.frexp(ref)           # ref = m * 2**e, 0.5 <= m < 1
-    h = np.ldexp(1.0, e - 9)
+    # below 2^-126 bf16 is subnormal: its spacing stays 2^-133
+    h = np.maximum(np.ldexp(1.0, e - 9), 2.0 ** -134)
     return np.where(ref > 0, h, 0.0)
 
 

@@ -78,12 +78,16 @@ def test_recorded_traffic_is_well_formed():
 
 def test_recorded_traffic_drops_on_code_change(tmp_path, monkeypatch):
     root = tmp_path / "repo"
-    for rel in bench.KERNEL_SOURCES["gemv"] + ["profiles/" + bench.PROFILE_FILES["decode"]]:
+    for rel in bench.KERNEL_SOURCES["gemv"]:
         dst = root / rel
         dst.parent.mkdir(parents=True, exist_ok=True)
         shutil.copy(os.path.join(bench.ROOT, rel), dst)
     monkeypatch.setattr(bench, "ROOT", str(root))
-    assert bench.recorded_traffic("gemv", "decode") is not None
+    prof = root / "profiles" / bench.PROFILE_FILES["decode"]
+    prof.parent.mkdir(parents=True, exist_ok=True)
+    prof.write_text("traffic_bytes_per_launch: 44383232\nkernel_source_sha256_16: %s\n"
+                    % bench.source_hash(bench.KERNEL_SOURCES["gemv"]))
+    assert bench.recorded_traffic("gemv", "decode") == 44383232
     f = root / bench.KERNEL_SOURCES["gemv"][0]
     f.write_text(f.read_text() + "\nstatic int changed_code = 1;\n")
     assert bench.recorded_traffic("gemv", "decode") is None

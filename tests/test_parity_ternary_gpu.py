@@ -137,5 +137,5 @@ def test_mmvq_ptq1_1_unresolvable_pattern_reports_device_error(w4):
     w4.mmvq_ptq1_1(sb, code[:100].contiguous(), ei, ep, pt, K)
     assert w4.device_error() == 2
     assert w4.device_error() == 0          # read and cleared
-    w4.mmvq_ptq1_1(sb, code, ei[1:].contiguous(), ep[1:].contiguous(), pt, K)
+    w4.mmvq_ptq1_1(sb, code, ei[1:].clone(), ep[1:].clone(), pt, K)   # fresh, 16-byte aligned copies
     assert w4.device_error() == 2
