@@ -644,6 +644,30 @@ def time_graph(work, steps, warmup, world):
     return max_over_ranks(sec, world), g, stream
 
 
+def isolated_steps(work, n=50):
+    """Median time of one step launched alone: before each, a 256 MB write
+    evicts L2 (cold weights and x) and a short GPU spin keeps the device busy
+    while the host prepares the launch, so the event pair brackets the
+    step's kernels and not the host; a device synchronise follows every
+    step."""
+    stream = torch.cuda.Stream()
+    flush = torch.empty(256 * 2**20, dtype=torch.uint8, device="cuda")
+    times = []
+    with torch.cuda.stream(stream):
+        for i in range(n + 3):
+            flush.zero_()
+            torch.cuda._sleep(2000000)   # about 1 ms of GPU spin, so the launch is queued before e0 runs
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            work.step()
+            e1.record(stream)
+            e1.synchronize()
+            if i >= 3:
+                times.append(e0.elapsed_time(e1) / 1e3)
+    del flush
+    return statistics.median(times)
+
+
 def soak(g, stream, seconds):
     t0 = time.time()
     with torch.cuda.stream(stream):
@@ -1032,6 +1056,7 @@ def run_ours(args, world, rank):
         soak(g, stream, 2.0)
         sec2, _, _ = time_graph(work, args.steps, 0, world)
     clocks = cs.summary()
+    iso_sec = isolated_steps(work)
     if kind in ("gemv", "gemv8", "w4a8", "ptq1"):
         e2e_sec, hb, ob = e2e_gemv(w4, work, args.steps, world)
     else:
@@ -1046,10 +1071,18 @@ def run_ours(args, world, rank):
         "config": {"workload": args.workload, **{k: v for k, v in WORKLOADS[args.workload].items() if k != "kind"},
                    "l2": work.l2_note(), "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": roofline(work, sec_step / work.launches_per_step, peaks, peak_src, kind, args.workload),
+        "isolated": {"value": rate(work, iso_sec), "unit": unit_of(work), "ms_per_step": iso_sec * 1e3,
+                     "frac": roofline(work, iso_sec / work.launches_per_step, peaks, peak_src, kind,
+                                      args.workload)["frac"],
+                     "how": "one step alone after a 256 MB L2-evicting write, device synchronise after it; "
+                            "median of 50"},
         "gpu_launches": args.steps * work.launches_per_step,
         "clocks": clocks,
         "e2e": {"value": e2e_val, "unit": unit_of(work), "h2d_bytes_per_step": hb, "d2h_bytes_per_step": ob},
     }
+    line["roofline"]["timing"] = ("CUDA events around one graph replay of the timed steps, launched back to back: "
+                                  "a launch may start (programmatic dependent launch) while the previous one "
+                                  "finishes; `isolated` is one launch alone")
     if kind == "gemm":
         line["context_torch_matmul"] = torch_matmul_context(work, max(3, min(args.steps, 20)))
     if kind == "quant8" or (kind == "quant" and not WORKLOADS[args.workload].get("fused", True)):

@@ -42,6 +42,8 @@ def load():
     lib.w4_device_error.restype = I
     lib.w4_selftest_wait_timeout.argtypes = [P, P]
     lib.w4_selftest_wait_timeout.restype = I
+    lib.w4_selftest_configure.argtypes = [ctypes.c_longlong, I]
+    lib.w4_selftest_configure.restype = I
     lib.quantize_pack_int4.argtypes = [P, P, P, I64, I64, P]
     lib.quantize_pack_int4.restype = I
     lib.permute_int4.argtypes = [P, P, I64, I64, P]

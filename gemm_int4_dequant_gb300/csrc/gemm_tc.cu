@@ -69,6 +69,12 @@ namespace gemm {
 
 using namespace ptx;
 
+// Test switch (w4_selftest_configure): when set, the producer announces 16
+// bytes more than it copies for its first stage, so that stage's wait runs
+// out and the error path (error word, abort, drain, TMEM freed) runs
+// without any bad access.  Always 0 in normal use.
+static __device__ int g_short_first_stage;
+
 constexpr int BM = 128;                      // A rows per CTA (the pair covers 256)
 constexpr int BN = 256;                      // tile columns (the pair's MMA N)
 constexpr int BNH = BN / 2;                  // B columns held by each CTA
@@ -216,6 +222,7 @@ gemm_w4_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
             asm volatile("prefetch.tensormap [%0];" ::"l"(&tmap_b) : "memory");
             int issued = 0;
             bool ok = true;
+            const uint32_t short0 = g_short_first_stage ? 16u : 0u;
             for (int it = 0; it < my_tiles && ok; ++it) {
                 const int mr = tile_m(it) * (2 * BM) + rank * BM;   // this CTA's first A row
                 const int nh = tile_n(it) * BN + rank * BNH;        // this CTA's first B column
@@ -226,7 +233,8 @@ gemm_w4_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
                 for (int kt = 0; kt < num_kt; ++kt) {
                     const int g = it * num_kt + kt, s = g % STAGES, round = g / STAGES;
                     if (round > 0 && !mbar_wait_fast(empty(s), (round - 1) & 1, abort_flag)) { ok = false; break; }
-                    mbar_arrive_expect_tx(full_tma(s), bytes);
+                    if (*abort_flag) { ok = false; break; }
+                    mbar_arrive_expect_tx(full_tma(s), bytes + (g == 0 ? short0 : 0u));
                     if (load_a) tma_load_2d(base + OFF_A + s * A_BYTES, &tmap_a, kt * BK, mr, full_tma(s));
                     if (load_b && PERM)
                         tma_load_3d(base + OFF_BP + s * BP_BYTES, &tmap_b, 0, kt, nh / 4, full_tma(s));
@@ -588,5 +596,10 @@ w4_status run_gemm_w4_permuted(const void* A, const void* permuted, const float*
 }
 
 int take_device_error_gemm() { return take_unit_device_error(); }
+int set_wait_limit_gemm(long long clocks) { return set_unit_wait_limit(clocks); }
+int set_short_first_stage_gemm(int on) {
+    const int v = on ? 1 : 0;
+    return cudaMemcpyToSymbol(gemm::g_short_first_stage, &v, sizeof(v)) == cudaSuccess ? 0 : -1;
+}
 
 }  // namespace w4

@@ -76,6 +76,12 @@ namespace gtma {
 
 using namespace ptx;
 
+// Test switch (w4_selftest_configure): when set, the producer announces 16
+// bytes more than it copies for a CTA's first stage, so that stage's wait
+// cannot complete and runs out -- the error path (error word, abort, drain)
+// runs without any bad access.  Always 0 in normal use.
+static __device__ int g_short_first_stage;
+
 #ifndef W4_GEMV_NC
 #define W4_GEMV_NC 16
 #endif
@@ -122,7 +128,7 @@ struct Plan {
 };
 
 struct Layout {
-    int stage_bytes, xf, xzero, red, part, partw, xsw, xsum, sz, zi, rcv, rxs, bars, abort, total;
+    int stage_bytes, xf, xzero, red, part, partw, xsw, xsum, sz, zz, rcv, rxs, bars, abort, total;
 };
 
 __host__ __device__ inline Layout make_layout(int C, const Plan& P) {
@@ -142,7 +148,11 @@ __host__ __device__ inline Layout make_layout(int C, const Plan& P) {
     // bits), later 0, [24, 32) the factor that undoes the scaling of x
     L.xsum = o;      o += 32 * 4;
     L.sz = o;        o += P.rows_cap * 8;          // (scale, z - zint(z)) per row as fp32
-    L.zi = o;        o += P.rows_cap * 4;          // zint(z) per row
+    o = (o + 15) & ~15;
+    // per row, what the main loop subtracts after the unpack (zi = zint(z)):
+    // fp16 (1024 + zi, even k) and the addend -(64 + zi) of the odd-k FMA,
+    // bf16 128 + zi, each in both halves
+    L.zz = o;        o += P.rows_cap * 16;
     // K split: the other slices' partials of the rows this rank owns (rows
     // ks, ks+S, ...) and their sums of x, pushed in by the peers
     L.rcv = o;       o += P.S > 1 ? P.S * ((P.rows_cap + P.S - 1) / P.S) * C * 4 : 0;
@@ -217,7 +227,7 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const void* __restrict__ scale,
         return PERM ? static_cast<const float*>(scale)[r]
                     : __bfloat162float(static_cast<const __nv_bfloat16*>(scale)[r]);
     };
-    int* zi_s = reinterpret_cast<int*>(sm + L.zi);
+    uint4* zz_s = reinterpret_cast<uint4*>(sm + L.zz);
 
     if (tid == 0) {
         for (int s = 0; s < NST; ++s) {
@@ -293,9 +303,14 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const void* __restrict__ scale,
             const uint64_t policy = l2_evict_first_policy();
             const int64_t row_bytes = K / 2;
             const uint8_t* src0 = qw + static_cast<int64_t>(r0) * row_bytes + k0 / 2;
+            const uint32_t short0 = g_short_first_stage ? 16u : 0u;
             int tile = 0, ch = 0, issued = 0, slot = 0, round = 0;
             for (int s = 0; s < nstages; ++s) {
                 if (round > 0 && !mbar_wait_fast(bar_empty + 8 * slot, (round - 1) & 1, abort_flag)) break;
+                // after an abort the consumers still release their slots, but a
+                // stage whose copy never completed must not be armed again
+                if (*abort_flag) break;
+                const uint32_t extra = s == 0 ? short0 : 0u;
                 const int rows_here = min(16, nrows - tile * 16);
                 const int seg = min(P.kchunk, klen - ch * P.kchunk) / 2;   // bytes per row (multiple of 16)
                 const uint32_t dst = sm_addr + slot * L.stage_bytes;
@@ -309,27 +324,27 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const void* __restrict__ scale,
                     const int ng = rows_here / 4;
                     const uint8_t* g0 = qw + static_cast<int64_t>(r0 / 4 + tile * 4) * 2 * K +
                                         ((k0 + ch * P.kchunk) / 64) * 128;
-                    mbar_arrive_expect_tx(bar_full + 8 * slot, ng * gbytes);
+                    mbar_arrive_expect_tx(bar_full + 8 * slot, ng * gbytes + extra);
                     for (int gi = 0; gi < ng; ++gi)
                         bulk_load_hint(dst + gi * 4 * pitch, g0 + static_cast<int64_t>(gi) * 2 * K, gbytes,
                                        bar_full + 8 * slot, policy);
                 } else if (P.tmap) {
                     const int c0 = (k0 + ch * P.kchunk) / 128, row0 = r0 + tile * 16;
                     if (rows_here == 16) {
-                        mbar_arrive_expect_tx(bar_full + 8 * slot, 16 * pitch);
+                        mbar_arrive_expect_tx(bar_full + 8 * slot, 16 * pitch + extra);
                         tma_load_3d_hint(dst, &tm16, 0, c0, row0, bar_full + 8 * slot, policy);
                     } else {
                         const int nb = (rows_here + 3) / 4;
-                        mbar_arrive_expect_tx(bar_full + 8 * slot, nb * 4 * pitch);
+                        mbar_arrive_expect_tx(bar_full + 8 * slot, nb * 4 * pitch + extra);
                         for (int b = 0; b < nb; ++b)
                             tma_load_3d_hint(dst + b * 4 * pitch, &tm4, 0, c0, row0 + 4 * b, bar_full + 8 * slot,
                                              policy);
                     }
                 } else if (P.dense) {
-                    mbar_arrive_expect_tx(bar_full + 8 * slot, rows_here * seg);
+                    mbar_arrive_expect_tx(bar_full + 8 * slot, rows_here * seg + extra);
                     bulk_load_hint(dst, src, rows_here * seg, bar_full + 8 * slot, policy);
                 } else {
-                    mbar_arrive_expect_tx(bar_full + 8 * slot, rows_here * seg);
+                    mbar_arrive_expect_tx(bar_full + 8 * slot, rows_here * seg + extra);
                     for (int r = 0; r < rows_here; ++r)
                         bulk_load_hint(dst + r * pitch, src + r * row_bytes, seg, bar_full + 8 * slot, policy);
                 }
@@ -356,13 +371,19 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const void* __restrict__ scale,
                 z_pf[j] = load_z(r0 + i);
             }
         }
+        auto zconsts = [](int zi) {
+            const uint32_t u = static_cast<uint32_t>(zi);
+            return make_uint4((0x6400u + u) * 0x10001u, (0xD400u + 16u * u) * 0x10001u, (0x4300u + u) * 0x10001u, 0u);
+        };
         auto store_zint = [&]() {
+            if constexpr (!PERM) {
 #pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const int i = tid + j * CT;
-                if (i < nrows) zi_s[i] = zint(z_pf[j]);
+                for (int j = 0; j < 2; ++j) {
+                    const int i = tid + j * CT;
+                    if (i < nrows) zz_s[i] = zconsts(zint(z_pf[j]));
+                }
+                for (int i = tid + 2 * CT; i < nrows; i += CT) zz_s[i] = zconsts(zint(load_z(r0 + i)));
             }
-            for (int i = tid + 2 * CT; i < nrows; i += CT) zi_s[i] = zint(load_z(r0 + i));
         };
         bool f16 = false;   // this CTA's main loop runs on fp16 MMAs
         // x as B fragments.  Row layout: entry (kb, word p, n, t4) holds, for
@@ -596,6 +617,8 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const void* __restrict__ scale,
         const uint32_t ldm_off = (ldm_col >> 2) * 4 * pitch + (ldm_col & 3) * 32 + (lane >> 4) * 16;
         int slot = 0, round = 0, first = warp;   // first unit of this warp in the current stage
         const int rows16 = (P.rows_cap + 15) / 16 * 16;
+        // this lane's partial sums: warp's rows, row g, columns 2*t4, 2*t4 + 1
+        float* const pw_lane = partw + (warp * rows16 + g) * C + 2 * t4;
         // H: fp16 MMAs (one column of x, within fp16's range), else bf16
         auto main_loop = [&](auto mode) {
             constexpr bool H = decltype(mode)::value;
@@ -603,37 +626,77 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const void* __restrict__ scale,
             // nibble -> bf16 128 + q (row layout) or 136 + q (two's complement
             // nibbles of the permuted layout, whose zero point is 0)
             auto unpack = [&](uint32_t v) { return PERM ? pass_flip_or(v, mask, magic) : and_or(v, mask, magic); };
-            for (int tile = 0; tile < ntiles; ++tile) {
-                // what the unpack leaves above q - zi for rows g and g+8 of the
-                // tile: bf16 128 + zi (136 on the permuted layout); fp16 1024 +
-                // zi for even k, and -(64 + zi) after the scaling by 1/16 of
-                // 1024 + 16q for odd k
-                const int ra = tile * 16 + g, rb8 = ra + 8;
-                const uint32_t za = PERM || ra >= nrows ? 0u : static_cast<uint32_t>(zi_s[ra]);
-                const uint32_t zb = PERM || rb8 >= nrows ? 0u : static_cast<uint32_t>(zi_s[rb8]);
-                const uint32_t ze_a = (H ? 0x6400u + za : PERM ? 0x4308u : 0x4300u + za) * 0x10001u;
-                const uint32_t ze_b = (H ? 0x6400u + zb : PERM ? 0x4308u : 0x4300u + zb) * 0x10001u;
-                const uint32_t zo_a = (0xD400u + 16u * za) * 0x10001u, zo_b = (0xD400u + 16u * zb) * 0x10001u;
-                constexpr uint32_t kSixteenth = 0x2C002C00u;   // fp16x2 (1/16, 1/16)
-                float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};
+            // what is left above q - zi after the unpack, for local row r: bf16
+            // 128 + zi (136 on the permuted layout); fp16 1024 + zi (even k) and
+            // the addend -(64 + zi) of the odd-k FMA by 1/16
+            auto zconst = [&](int r, uint32_t& ze, uint32_t& zo) {
+                if constexpr (PERM) {
+                    ze = 0x43084308u;
+                    zo = 0u;
+                } else if (r >= nrows) {   // rows past the range: never stored
+                    ze = H ? 0x64006400u : 0x43004300u;
+                    zo = 0xD400D400u;
+                } else if constexpr (H) {
+                    const uint2 v = *reinterpret_cast<const uint2*>(&zz_s[r]);
+                    ze = v.x;
+                    zo = v.y;
+                } else {
+                    ze = zz_s[r].z;
+                    zo = 0u;
+                }
+            };
+            constexpr uint32_t kSixteenth = 0x2C002C00u;   // fp16x2 (1/16, 1/16)
+            // RT consecutive 16-row tiles at once (RT = 2 only when a tile is
+            // one stage): the warp's units of both stages share the x
+            // fragments and the per-stage bookkeeping
+            auto run = [&](auto rt_tag, int tile) {
+                constexpr int RT = decltype(rt_tag)::value;
+                uint32_t ze_a[RT], ze_b[RT], zo_a[RT], zo_b[RT];
+#pragma unroll
+                for (int t = 0; t < RT; ++t) {
+                    zconst((tile + t) * 16 + g, ze_a[t], zo_a[t]);
+                    zconst((tile + t) * 16 + g + 8, ze_b[t], zo_b[t]);
+                }
+                float acc[RT][4], acc2[RT][4];
+#pragma unroll
+                for (int t = 0; t < RT; ++t)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) acc[t][i] = acc2[t][i] = 0.f;
                 for (int ch = 0; ch < nch; ++ch) {
                     const int units = (min(P.kchunk, klen - ch * P.kchunk) + KB - 1) / KB;
-                    const bool ok = mbar_wait_fast(bar_full + 8 * slot, round & 1, abort_flag);
+                    int sl[RT], rd[RT];
+                    {
+                        int s2 = slot, r2 = round;
+#pragma unroll
+                        for (int t = 0; t < RT; ++t) {
+                            sl[t] = s2;
+                            rd[t] = r2;
+                            if (++s2 == NST) { s2 = 0; ++r2; }
+                        }
+                        slot = s2;
+                        round = r2;
+                    }
+                    bool ok = true;
+#pragma unroll
+                    for (int t = 0; t < RT; ++t) ok = ok && mbar_wait_fast(bar_full + 8 * sl[t], rd[t] & 1, abort_flag);
                     if (ok) {
-                        const uint8_t* st = sm + slot * L.stage_bytes;
                         for (int u = first; u < units; u += NC) {
                             const uint4* xb = xlane + (ch * (P.kchunk / KB) + u) * xkb_stride;
-                            uint32_t wav[4], wbv[4];
-                            if constexpr (PERM) {
-                                // words of columns g and g+8 for the unit's four 32-k groups
-                                const uint32_t a = smem_u32(st) + ldm_off + u * 256;
-                                ldmatrix_x4(a, wav[0], wbv[0], wav[1], wbv[1]);
-                                ldmatrix_x4(a + 128, wav[2], wbv[2], wav[3], wbv[3]);
-                            } else {
-                                const uint4 wa = *reinterpret_cast<const uint4*>(st + row_off_a + u * 64);
-                                const uint4 wb = *reinterpret_cast<const uint4*>(st + row_off_b + u * 64);
-                                wav[0] = wa.x; wav[1] = wa.y; wav[2] = wa.z; wav[3] = wa.w;
-                                wbv[0] = wb.x; wbv[1] = wb.y; wbv[2] = wb.z; wbv[3] = wb.w;
+                            uint32_t wav[RT][4], wbv[RT][4];
+#pragma unroll
+                            for (int t = 0; t < RT; ++t) {
+                                const uint8_t* st = sm + sl[t] * L.stage_bytes;
+                                if constexpr (PERM) {
+                                    // words of columns g and g+8 for the unit's four 32-k groups
+                                    const uint32_t a = smem_u32(st) + ldm_off + u * 256;
+                                    ldmatrix_x4(a, wav[t][0], wbv[t][0], wav[t][1], wbv[t][1]);
+                                    ldmatrix_x4(a + 128, wav[t][2], wbv[t][2], wav[t][3], wbv[t][3]);
+                                } else {
+                                    const uint4 wa = *reinterpret_cast<const uint4*>(st + row_off_a + u * 64);
+                                    const uint4 wb = *reinterpret_cast<const uint4*>(st + row_off_b + u * 64);
+                                    wav[t][0] = wa.x; wav[t][1] = wa.y; wav[t][2] = wa.z; wav[t][3] = wa.w;
+                                    wbv[t][0] = wb.x; wbv[t][1] = wb.y; wbv[t][2] = wb.z; wbv[t][3] = wb.w;
+                                }
                             }
 #pragma unroll
                             for (int w = 0; w < 4; ++w) {
@@ -644,76 +707,98 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const void* __restrict__ scale,
                                 } else {
                                     bx = xb[w * xw_stride];
                                 }
-                                const uint32_t va = wav[w], vb = wbv[w];
-                                if constexpr (!H) {
-                                    const uint32_t a0[4] = {sub_bf16x2(unpack(va), ze_a), sub_bf16x2(unpack(vb), ze_b),
-                                                            sub_bf16x2(unpack(va >> 4), ze_a),
-                                                            sub_bf16x2(unpack(vb >> 4), ze_b)};
-                                    const uint32_t a1[4] = {sub_bf16x2(unpack(va >> 8), ze_a),
-                                                            sub_bf16x2(unpack(vb >> 8), ze_b),
-                                                            sub_bf16x2(unpack(va >> 12), ze_a),
-                                                            sub_bf16x2(unpack(vb >> 12), ze_b)};
-                                    mma_bf16(acc, a0, bx.x, bx.y);
-                                    mma_bf16(acc2, a1, bx.z, bx.w);
-                                } else {
-                                    // fp16 1024 + q from nibbles 0 and 2 (bits 0-3 of
-                                    // each half, after one shift by 8 for nibble 2),
-                                    // 1024 + 16q from nibbles 1 and 3 (bits 4-7)
-                                    const uint32_t va8 = va >> 8, vb8 = vb >> 8;
-                                    const uint32_t a0[4] = {
-                                        sub_f16x2(and_or(va, mask, magic), ze_a), sub_f16x2(and_or(vb, mask, magic), ze_b),
-                                        sub_f16x2(and_or(va8, mask, magic), ze_a),
-                                        sub_f16x2(and_or(vb8, mask, magic), ze_b)};
-                                    const uint32_t a1[4] = {fma_f16x2(and_or(va, mask_hi, magic), kSixteenth, zo_a),
-                                                            fma_f16x2(and_or(vb, mask_hi, magic), kSixteenth, zo_b),
-                                                            fma_f16x2(and_or(va8, mask_hi, magic), kSixteenth, zo_a),
-                                                            fma_f16x2(and_or(vb8, mask_hi, magic), kSixteenth, zo_b)};
-                                    mma_f16(acc, a0, bx.x, bx.y);
-                                    mma_f16(acc2, a1, bx.z, bx.w);
+#pragma unroll
+                                for (int t = 0; t < RT; ++t) {
+                                    const uint32_t va = wav[t][w], vb = wbv[t][w];
+                                    if constexpr (!H) {
+                                        const uint32_t a0[4] = {sub_bf16x2(unpack(va), ze_a[t]),
+                                                                sub_bf16x2(unpack(vb), ze_b[t]),
+                                                                sub_bf16x2(unpack(va >> 4), ze_a[t]),
+                                                                sub_bf16x2(unpack(vb >> 4), ze_b[t])};
+                                        const uint32_t a1[4] = {sub_bf16x2(unpack(va >> 8), ze_a[t]),
+                                                                sub_bf16x2(unpack(vb >> 8), ze_b[t]),
+                                                                sub_bf16x2(unpack(va >> 12), ze_a[t]),
+                                                                sub_bf16x2(unpack(vb >> 12), ze_b[t])};
+                                        mma_bf16(acc[t], a0, bx.x, bx.y);
+                                        mma_bf16(acc2[t], a1, bx.z, bx.w);
+                                    } else {
+                                        // fp16 1024 + q from nibbles 0 and 2 (bits 0-3 of
+                                        // each half, after one shift by 8 for nibble 2),
+                                        // 1024 + 16q from nibbles 1 and 3 (bits 4-7)
+                                        const uint32_t va8 = va >> 8, vb8 = vb >> 8;
+                                        const uint32_t a0[4] = {sub_f16x2(and_or(va, mask, magic), ze_a[t]),
+                                                                sub_f16x2(and_or(vb, mask, magic), ze_b[t]),
+                                                                sub_f16x2(and_or(va8, mask, magic), ze_a[t]),
+                                                                sub_f16x2(and_or(vb8, mask, magic), ze_b[t])};
+                                        const uint32_t a1[4] = {
+                                            fma_f16x2(and_or(va, mask_hi, magic), kSixteenth, zo_a[t]),
+                                            fma_f16x2(and_or(vb, mask_hi, magic), kSixteenth, zo_b[t]),
+                                            fma_f16x2(and_or(va8, mask_hi, magic), kSixteenth, zo_a[t]),
+                                            fma_f16x2(and_or(vb8, mask_hi, magic), kSixteenth, zo_b[t])};
+                                        mma_f16(acc[t], a0, bx.x, bx.y);
+                                        mma_f16(acc2[t], a1, bx.z, bx.w);
+                                    }
                                 }
                             }
                         }
                     }
-                    // rotate: this warp's first unit of the next stage
+                    // rotate: this warp's first unit of the next stage (the RT
+                    // tiles of one step share the unit assignment)
                     first -= units % NC;
                     if (first < 0) first += NC;
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
-                    if (++slot == NST) { slot = 0; ++round; }
+                    if (lane == 0) {
+#pragma unroll
+                        for (int t = 0; t < RT; ++t) mbar_arrive(bar_empty + 8 * sl[t]);
+                    }
                 }
                 const int c0 = 2 * t4, c1 = 2 * t4 + 1;
-                if (P.perwarp) {
-                    // this warp's partial of the tile; warps are added at the end
-                    float* pw = partw + (static_cast<size_t>(warp) * rows16 + tile * 16) * C;
-                    if (c0 < C) {
-                        pw[g * C + c0] = acc[0] + acc2[0];
-                        pw[(g + 8) * C + c0] = acc[2] + acc2[2];
-                    }
-                    if (c1 < C) {
-                        pw[g * C + c1] = acc[1] + acc2[1];
-                        pw[(g + 8) * C + c1] = acc[3] + acc2[3];
-                    }
-                } else {
-                    // tile partials, added in warp order now (bounded shared memory)
-                    float* rbuf = red + ((tile & 1) * NC + warp) * 16 * C;
-                    if (c0 < C) {
-                        rbuf[g * C + c0] = acc[0] + acc2[0];
-                        rbuf[(g + 8) * C + c0] = acc[2] + acc2[2];
-                    }
-                    if (c1 < C) {
-                        rbuf[g * C + c1] = acc[1] + acc2[1];
-                        rbuf[(g + 8) * C + c1] = acc[3] + acc2[3];
-                    }
-                    named_barrier(1, CT);
-                    for (int i = tid; i < 16 * C; i += CT) {
-                        const int r = i / C;
-                        if (tile * 16 + r < nrows) {
-                            float v = 0.f;
-                            for (int w = 0; w < NC; ++w) v += red[((tile & 1) * NC + w) * 16 * C + i];
-                            const int c = i - r * C;
-                            part[(tile * 16) * C + i] = v * xsum[24 + c];
+#pragma unroll
+                for (int t = 0; t < RT; ++t) {
+                    if (P.perwarp) {
+                        // this warp's partial of the tile; warps are added at the end
+                        float* pw = pw_lane + (tile + t) * 16 * C;
+                        if (c0 < C) {
+                            pw[0] = acc[t][0] + acc2[t][0];
+                            pw[8 * C] = acc[t][2] + acc2[t][2];
+                        }
+                        if (c1 < C) {
+                            pw[1] = acc[t][1] + acc2[t][1];
+                            pw[8 * C + 1] = acc[t][3] + acc2[t][3];
+                        }
+                    } else {
+                        // tile partials, added in warp order now (bounded shared memory)
+                        const int tl = tile + t;
+                        float* rbuf = red + ((tl & 1) * NC + warp) * 16 * C;
+                        if (c0 < C) {
+                            rbuf[g * C + c0] = acc[t][0] + acc2[t][0];
+                            rbuf[(g + 8) * C + c0] = acc[t][2] + acc2[t][2];
+                        }
+                        if (c1 < C) {
+                            rbuf[g * C + c1] = acc[t][1] + acc2[t][1];
+                            rbuf[(g + 8) * C + c1] = acc[t][3] + acc2[t][3];
+                        }
+                        named_barrier(1, CT);
+                        for (int i = tid; i < 16 * C; i += CT) {
+                            const int r = i / C;
+                            if (tl * 16 + r < nrows) {
+                                float v = 0.f;
+                                for (int w = 0; w < NC; ++w) v += red[((tl & 1) * NC + w) * 16 * C + i];
+                                const int c = i - r * C;
+                                part[(tl * 16) * C + i] = v * xsum[24 + c];
+                            }
                         }
                     }
+                }
+            };
+            int tile = 0;
+            while (tile < ntiles) {
+                if (nch == 1 && P.perwarp && NST >= 2 && tile + 1 < ntiles) {
+                    run(std::integral_constant<int, 2>{}, tile);
+                    tile += 2;
+                } else {
+                    run(std::integral_constant<int, 1>{}, tile);
+                    tile += 1;
                 }
             }
         };
@@ -832,6 +917,9 @@ Plan make_plan(int N, int K, int sms, int max_clusters_for_S /* 0: unknown */, i
     auto slice_of = [&](int s) { return ((K + s - 1) / s + sgran - 1) / sgran * sgran; };
     auto xf_bytes = [&](int s) { return static_cast<size_t>((slice_of(s) + KB - 1) / KB) * 16 * C * 16; };
     int S = 1;
+#ifdef W4_GEMV_FORCE_S
+    if (!S_forced) S_forced = W4_GEMV_FORCE_S;
+#endif
     if (S_forced) S = S_forced;
     else while (S < 8 && xf_bytes(S) > kXfBudget) S *= 2;
     P.S = S;
@@ -845,7 +933,9 @@ Plan make_plan(int N, int K, int sms, int max_clusters_for_S /* 0: unknown */, i
     int groups = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(sms / S, tiles)));
     if (max_clusters_for_S > 0) groups = std::min(groups, max_clusters_for_S);
     const int64_t per = std::max<int64_t>(1, (tiles + groups - 1) / groups);
+#ifndef W4_GEMV_ALLSM
     groups = static_cast<int>(std::max<int64_t>(1, (tiles + per - 1) / per));
+#endif
     P.groups = groups;
     P.rows_cap = static_cast<int>(16 * std::max<int64_t>(1, per));
     // stage: one 16-row tile over a K-chunk
@@ -988,5 +1078,10 @@ w4_status run_gemv_permuted(const void* permuted, const float* scale, const void
 }
 
 int take_device_error_gemv() { return take_unit_device_error(); }
+int set_wait_limit_gemv(long long clocks) { return set_unit_wait_limit(clocks); }
+int set_short_first_stage_gemv(int on) {
+    const int v = on ? 1 : 0;
+    return cudaMemcpyToSymbol(gtma::g_short_first_stage, &v, sizeof(v)) == cudaSuccess ? 0 : -1;
+}
 
 }  // namespace w4

@@ -409,5 +409,6 @@ w4_status run_mmvq_ptq1_1(const void* sblocks, const void* codebook, int64_t n_c
 }
 
 int take_device_error_ptq1() { return take_unit_device_error(); }
+int set_wait_limit_ptq1(long long clocks) { return set_unit_wait_limit(clocks); }
 
 }  // namespace w4

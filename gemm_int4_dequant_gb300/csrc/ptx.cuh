@@ -16,6 +16,15 @@ namespace w4 {
 static __device__ int g_device_error;
 constexpr int ERR_TIMEOUT = 1;
 
+// SM clock cycles a bounded wait lasts before it gives up: 2^32, about two
+// seconds at GB300's clocks.  Per translation unit, like the error word; a
+// test hook (w4_selftest_configure) shortens it to make waits run out fast.
+static __device__ long long g_wait_limit = 1ll << 32;
+
+static inline int set_unit_wait_limit(long long clocks) {
+    return cudaMemcpyToSymbol(g_wait_limit, &clocks, sizeof(clocks)) == cudaSuccess ? 0 : -1;
+}
+
 // Host: synchronised read-and-clear of this unit's error word (-1 on failure).
 static inline int take_unit_device_error() {
     int v = 0;
@@ -78,7 +87,7 @@ static __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, vol
     while (true) {
         if (mbar_try_wait_sleep(bar, parity)) return true;
         if (*abort_flag) return false;
-        if (clock64() - t0 > (1ll << 32)) {
+        if (clock64() - t0 > g_wait_limit) {
             *abort_flag = 1;
             atomicCAS(&g_device_error, 0, ERR_TIMEOUT);
             return false;
@@ -91,7 +100,7 @@ static __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, vol
 static __device__ __noinline__ void mbar_drain(uint32_t bar, uint32_t parity) {
     const long long t0 = clock64();
     while (!mbar_try_wait_sleep(bar, parity)) {
-        if (clock64() - t0 > (1ll << 32)) {
+        if (clock64() - t0 > g_wait_limit) {
             atomicCAS(&g_device_error, 0, ERR_TIMEOUT);
             return;
         }
@@ -231,7 +240,7 @@ static __device__ __noinline__ bool mbar_wait_cluster_slow(uint32_t bar, uint32_
     while (true) {
         if (mbar_try_wait_cluster(bar, parity)) return true;
         if (*abort_flag) return false;
-        if (clock64() - t0 > (1ll << 32)) {
+        if (clock64() - t0 > g_wait_limit) {
             *abort_flag = 1;
             atomicCAS(&g_device_error, 0, ERR_TIMEOUT);
             return false;

@@ -732,5 +732,6 @@ w4_status run_quantize_pack_permute(const void* W, void* out, float* scale, int6
 }
 
 int take_device_error_quant() { return take_unit_device_error(); }
+int set_wait_limit_quant(long long clocks) { return set_unit_wait_limit(clocks); }
 
 }  // namespace w4

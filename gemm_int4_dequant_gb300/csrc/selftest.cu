@@ -35,5 +35,6 @@ w4_status run_selftest_wait_timeout(int* waited, cudaStream_t stream) {
 }
 
 int take_device_error_selftest() { return take_unit_device_error(); }
+int set_wait_limit_selftest(long long clocks) { return set_unit_wait_limit(clocks); }
 
 }  // namespace w4

@@ -41,6 +41,13 @@ w4_status run_gemm_w4_permuted(const void* A, const void* permuted, const float*
 int take_device_error_gemm();
 int take_device_error_gemv();
 int take_device_error_quant();
+int set_wait_limit_gemm(long long clocks);
+int set_wait_limit_gemv(long long clocks);
+int set_wait_limit_quant(long long clocks);
+int set_wait_limit_ptq1(long long clocks);
+int set_wait_limit_selftest(long long clocks);
+int set_short_first_stage_gemv(int on);
+int set_short_first_stage_gemm(int on);
 
 namespace {
 constexpr int kMaxDevices = 64;
@@ -276,6 +283,16 @@ w4_status gemm_w4_permuted(const void* A, const void* permuted, const float* sca
     if (!device_is_sm103()) return W4_ERR_DEVICE;
     if (K == 0) return launch_status(cudaMemsetAsync(C, 0, M * N * 2, (cudaStream_t)stream));
     return run_gemm_w4_permuted(A, permuted, scale, C, M, N, K, (cudaStream_t)stream);
+}
+
+w4_status w4_selftest_configure(long long wait_limit_clocks, int short_first_stage) {
+    const long long limit = wait_limit_clocks > 0 ? wait_limit_clocks : (1ll << 32);
+    if (cudaDeviceSynchronize() != cudaSuccess) return W4_ERR_CUDA;
+    if (set_wait_limit_gemm(limit) || set_wait_limit_gemv(limit) || set_wait_limit_quant(limit) ||
+        set_wait_limit_ptq1(limit) || set_wait_limit_selftest(limit) ||
+        set_short_first_stage_gemv(short_first_stage) || set_short_first_stage_gemm(short_first_stage))
+        return W4_ERR_CUDA;
+    return W4_OK;
 }
 
 w4_status w4_selftest_wait_timeout(int* waited, void* stream) {

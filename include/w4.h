@@ -108,6 +108,23 @@ int w4_device_error(void* stream);
 w4_status w4_selftest_wait_timeout(int* waited, void* stream);
 
 /*
+ * w4_selftest_configure -- test hook for the pipelined kernels' error path
+ * (no counterpart on the pages).  wait_limit_clocks > 0 sets how many SM
+ * clock cycles every bounded wait of the library lasts before it gives up
+ * (<= 0 restores the default 2^32, about two seconds); short_first_stage != 0
+ * makes the producers of gemv_w4 / gemv_w4_permuted (the tensor-core path)
+ * and of the gemm_w4 family announce 16 bytes more than they copy for their
+ * first stage, so that stage's wait can never complete: the kernel then runs
+ * out the limit, records code 1 for w4_device_error, stops issuing, drains
+ * the copies already issued, frees its tensor memory and returns, having
+ * stored (possibly meaningless) results only inside its output.  Nothing
+ * faults, traps or hangs.  Synchronises the device first; the settings hold
+ * for the whole process until changed.  Call (0, 0) to return to normal
+ * operation.  Never needed by a user of the library.
+ */
+w4_status w4_selftest_configure(long long wait_limit_clocks, int short_first_stage);
+
+/*
  * quantize_pack_int4 -- symmetric per-column int4 quantisation + column pack.
  *
  *   scale[n]  = max_k |W[k][n]| / 7                (IEEE fp32 division)

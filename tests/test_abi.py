@@ -29,7 +29,8 @@ def test_header_declares_the_hot_path():
     for fn in ("quantize_pack_int4", "permute_int4", "quantize_pack_permute_int4", "gemv_w4", "gemv_w4_permuted",
                "gemm_w4", "quantize_int8", "permute_int8", "gemv_w8", "gemm_w8", "gemm_w4_permuted", "quantize_q8_1_pt", "gemv_w4a8", "mmvq_ptq1_0",
                "mmvq_ptq1_1", "ptq1_1_codebook", "ptq1_1_encode",
-               "w4_status_string", "w4_abi_version", "w4_device_error", "w4_selftest_wait_timeout"):
+               "w4_status_string", "w4_abi_version", "w4_device_error", "w4_selftest_wait_timeout",
+               "w4_selftest_configure"):
         assert fn in names
 
 
@@ -43,9 +44,22 @@ def test_library_exports_every_declared_symbol():
 
 
 def test_library_has_no_oracle_dependency():
+    """The product library neither imports an oracle symbol nor needs the
+    oracle's shared object (its dynamic symbol table and NEEDED entries),
+    and no product source imports the oracle."""
+    import shutil
+    import subprocess
     from gemm_int4_dequant_gb300._lib import LIB_PATH
-    data = open(LIB_PATH, "rb").read()
-    assert b"w4o_" not in data, "product library references the oracle"
+    if not (shutil.which("nm") and shutil.which("readelf")):
+        pytest.skip("binutils not installed")
+    undefined = subprocess.run(["nm", "-D", "--undefined-only", LIB_PATH], capture_output=True, text=True,
+                               check=True).stdout
+    defined = subprocess.run(["nm", "-D", "--defined-only", LIB_PATH], capture_output=True, text=True,
+                             check=True).stdout
+    assert "w4o_" not in undefined and "w4o_" not in defined, "product library references the oracle"
+    dyn = subprocess.run(["readelf", "-d", LIB_PATH], capture_output=True, text=True, check=True).stdout
+    needed = [l for l in dyn.splitlines() if "(NEEDED)" in l]
+    assert needed and not any("oracle" in l for l in needed), needed
     pkg = os.path.join(ROOT, "gemm_int4_dequant_gb300")
     for dirpath, _, files in os.walk(pkg):
         for f in files:

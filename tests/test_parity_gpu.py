@@ -568,3 +568,72 @@ def test_bounded_wait_gives_up_reports_and_leaves_the_context_usable(w4):
     assert int(waited.item()) == 0
     assert w4.device_error() == 0
     _check_gemv(w4, 300, 4096, 2, "bf16", seed=9)
+
+
+def _selftest_configure(limit_clocks, short_first_stage):
+    from gemm_int4_dequant_gb300 import _lib as L
+    assert L.load().w4_selftest_configure(limit_clocks, short_first_stage) == L.W4_OK
+
+
+# about 2 ms of SM clock: every wait that cannot complete gives up quickly
+_SHORT_LIMIT = 1 << 22
+
+
+@pytest.mark.parametrize("N,K,C", [(1000, 5120, 1), (700, 4096, 4)])
+def test_gemv_stage_that_never_completes_runs_out_and_recovers(w4, N, K, C):
+    """The producer announces 16 bytes more than it copies for its first
+    stage (a test switch), so that stage's wait runs out its shortened
+    limit: the kernel records code 1, stops issuing, drains and returns with
+    the guard bands around its output intact; with the switch off again the
+    next call is within the bound and records nothing."""
+    g = synth.gemv_inputs(N, K, C, act="bf16", seed=21)
+    assert w4.device_error() == 0
+    buf, out, pad = _guarded(C * N, torch.bfloat16, -7.0)
+    try:
+        _selftest_configure(_SHORT_LIMIT, 1)
+        w4.gemv_w4(g.qweight.to(_dev()), g.scale.to(_dev()), g.zero.to(_dev()), g.x.to(_dev()), out=out)
+        assert w4.device_error() == 1
+    finally:
+        _selftest_configure(0, 0)
+    assert _guards_intact(buf, pad, C * N, -7.0)
+    assert w4.device_error() == 0
+    _check_gemv(w4, N, K, C, "bf16", seed=22)
+    assert w4.device_error() == 0
+
+
+def test_gemv_permuted_stage_that_never_completes_runs_out_and_recovers(w4):
+    N, K, C = 512, 5120, 4
+    g = synth.packed_gemv_inputs(N, K, C, seed=23)
+    perm = w4.permute_int4(g.packed.to(_dev()))
+    assert w4.device_error() == 0
+    buf, out, pad = _guarded(C * N, torch.bfloat16, -7.0)
+    try:
+        _selftest_configure(_SHORT_LIMIT, 1)
+        w4.gemv_w4_permuted(perm, g.scale.to(_dev()), g.x.to(_dev()), out=out)
+        assert w4.device_error() == 1
+    finally:
+        _selftest_configure(0, 0)
+    assert _guards_intact(buf, pad, C * N, -7.0)
+    assert w4.device_error() == 0
+    _check_gemv_permuted(w4, N, K, C, seed=24)
+    assert w4.device_error() == 0
+
+
+def test_gemm_stage_that_never_completes_runs_out_frees_tmem_and_recovers(w4):
+    """The same switch on the tensor-memory GEMM: every role of both CTAs
+    of a pair gives up, the pair frees its tensor memory (a later launch
+    allocates it again) and the next call is exact."""
+    M, N, K = 256, 512, 256
+    gi = synth.gemm_inputs(M, N, K, seed=25)
+    assert w4.device_error() == 0
+    buf, out, pad = _guarded(M * N, torch.bfloat16, -3.0)
+    try:
+        _selftest_configure(_SHORT_LIMIT, 1)
+        w4.gemm_w4(gi.A.to(_dev()), gi.B.to(_dev()), gi.scale.to(_dev()), gi.zero.to(_dev()), out=out)
+        assert w4.device_error() == 1
+    finally:
+        _selftest_configure(0, 0)
+    assert _guards_intact(buf, pad, M * N, -3.0)
+    assert w4.device_error() == 0
+    _check_gemm_full(w4, M, N, K, seed=26)
+    _check_gemm_full(w4, 2048, 4096, 64, seed=27)   # a multi-tile launch after the aborted one
