@@ -216,6 +216,11 @@ quantize_pack_cluster_kernel(const __grid_constant__ CUtensorMap tmap, uint8_t* 
         if (__all_sync(0xffffffffu, ok)) {
             const int cp = lane & 15, par = lane >> 4;
             const float inv0 = s_inv[2 * cp], inv1 = s_inv[2 * cp + 1];
+            // a scale below about 2^-128 (column maximum below about 7 * 2^-128)
+            // has no finite reciprocal: every weight of such a column takes the
+            // exact path below (its bracket test cannot pass by accident:
+            // |w| <= 7 s rules out the tie m s with the bogus m it reads)
+            const uint32_t force0 = isinf(inv0) ? ~0u : 0u, force1 = isinf(inv1) ? ~0u : 0u;
             const int mycol = 2 * cp + par;                       // the column this lane stores
             const bool col_ok = n0 + mycol < N;
             // output: 128-byte lines of the column's group of four, this
@@ -264,8 +269,8 @@ quantize_pack_cluster_kernel(const __grid_constant__ CUtensorMap tmap, uint8_t* 
                     // Exact ties (w = m s, the usual case: the FMA residual is
                     // then exactly 0) round away from zero; the rest take the
                     // exact IEEE division.  One weight per trip of a lane.
-                    uint32_t f0 = z[0][0] ^ zb[0][0], f1 = z[0][1] ^ zb[0][1];
-                    uint32_t f2 = z[1][0] ^ zb[1][0], f3 = z[1][1] ^ zb[1][1];
+                    uint32_t f0 = (z[0][0] ^ zb[0][0]) | force0, f1 = (z[0][1] ^ zb[0][1]) | force0;
+                    uint32_t f2 = (z[1][0] ^ zb[1][0]) | force1, f3 = (z[1][1] ^ zb[1][1]) | force1;
                     if (__any_sync(0xffffffffu, (f0 | f1 | f2 | f3) != 0)) {
                         while ((f0 | f1 | f2 | f3) != 0) {
                             const int wsel = f0 ? 0 : f1 ? 1 : f2 ? 2 : 3;   // word: col = wsel / 2, h = wsel % 2
@@ -318,8 +323,14 @@ quantize_pack_cluster_kernel(const __grid_constant__ CUtensorMap tmap, uint8_t* 
     if (__all_sync(0xffffffffu, ok)) {
         const bool col_ok = n0 + 8 * g < N;
         float inv[8];
+        // columns whose scale has no finite reciprocal (below about 2^-128):
+        // all their weights take the exact division of the fix-up
+        uint32_t tinymask = 0;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) inv[j] = s_inv[8 * g + j];
+        for (int j = 0; j < 8; ++j) {
+            inv[j] = s_inv[8 * g + j];
+            if (isinf(inv[j])) tinymask |= 3u << (2 * j);
+        }
         const int pairs = rows / 2;
         for (int p0 = rl & ~7; p0 < pairs; p0 += QC_RL) {   // rl & ~7: the warp's first row lane
             const int p = p0 + (rl & 7);
@@ -329,7 +340,7 @@ quantize_pack_cluster_kernel(const __grid_constant__ CUtensorMap tmap, uint8_t* 
             const uint4 c = *reinterpret_cast<const uint4*>(ra + QC_COLS * 2);
             const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, wb[4] = {c.x, c.y, c.z, c.w};
             // nibble of (row, column j) goes to bit 8*(j%4) + 4*row of word j/4
-            uint32_t out[2] = {0, 0}, nearmask = 0;
+            uint32_t out[2] = {0, 0}, nearmask = tinymask;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 const uint32_t ha = (j & 1) ? (wa[j / 2] & 0xFFFF0000u) : (wa[j / 2] << 16);

@@ -111,3 +111,41 @@ def test_every_bf16_weight_quantise_and_permute_in_one_pass(w4, weights):
     got = np_bits(out.cpu())
     bad = np.flatnonzero(got != ref)
     assert bad.size == 0, "%d bytes differ, first at %s" % (bad.size, bad[:8])
+
+
+# int8 variant (the int4 definition with the int8 range: s = max|W| / 127,
+# q = clamp(round(W / s), -128, 127)); its single-read kernel holds K <= 12800
+K8 = 12800
+
+
+def _int8_weights():
+    bits, vals = _all_finite_bf16()
+    cols = []
+    for m in MAXIMA:
+        mb = np_bits(torch.tensor([m], dtype=torch.bfloat16))[0]
+        mv = _bf16_from_bits(np.array([mb])).double().item()
+        sel = bits[np.abs(vals) <= mv]
+        for j in range(0, sel.size, K8 - 1):
+            col = np.zeros(K8, dtype=np.uint16)
+            chunk = sel[j:j + K8 - 1]
+            col[:chunk.size] = chunk
+            col[K8 - 1] = mb
+            cols.append(col)
+    n = (len(cols) + 7) // 8 * 8
+    W = np.zeros((K8, n), dtype=np.uint16)
+    for j, c in enumerate(cols):
+        W[:, j] = c
+    return W
+
+
+@pytest.mark.parametrize("extra_col", [False, True], ids=["single_read", "plain"])
+def test_every_bf16_weight_int8(w4, extra_col):
+    W = _int8_weights()
+    if extra_col:   # N % 8 != 0: the plain kernel
+        W = np.concatenate([W, np.zeros((K8, 1), dtype=np.uint16)], axis=1)
+    q, scale = w4.quantize_int8(_bf16_from_bits(W).to("cuda"))
+    s_ref, q_ref = oracle.quantize_int8(W)
+    assert np.array_equal(scale.cpu().numpy().view(np.uint32), s_ref.view(np.uint32))
+    got = q.cpu().numpy()
+    bad = np.argwhere(got != q_ref)
+    assert bad.size == 0, "%d weights differ, first (row, column) %s" % (len(bad), bad[:6].tolist())
