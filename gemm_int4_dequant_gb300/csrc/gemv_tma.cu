@@ -238,6 +238,7 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const void* __restrict__ scale,
         *abort_flag = 0;
         for (int c = 0; c < 8; ++c) reinterpret_cast<uint32_t*>(xsum)[16 + c] = 0;   // column maxima of |x|
         reinterpret_cast<uint32_t*>(xsum)[8] = 0xFFFFu;                              // (smallest nonzero |x|) - 1
+        reinterpret_cast<uint32_t*>(xsum)[9] = 0u;                                   // a fractional zero point seen
         if (S > 1) {
             // every peer pushes its partials of the rows this rank owns and its
             // C sums of x; they complete bytes on this barrier
@@ -375,14 +376,28 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const void* __restrict__ scale,
             const uint32_t u = static_cast<uint32_t>(zi);
             return make_uint4((0x6400u + u) * 0x10001u, (0xD400u + 16u * u) * 0x10001u, (0x4300u + u) * 0x10001u, 0u);
         };
+        // (also notes whether any row's zero point has a fractional part: only
+        // then do the sums of x enter the result)
+        volatile uint32_t* frac_seen = reinterpret_cast<volatile uint32_t*>(xsum) + 9;
         auto store_zint = [&]() {
             if constexpr (!PERM) {
+                bool frac = false;
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {
                     const int i = tid + j * CT;
-                    if (i < nrows) zz_s[i] = zconsts(zint(z_pf[j]));
+                    if (i < nrows) {
+                        const int zi = zint(z_pf[j]);
+                        zz_s[i] = zconsts(zi);
+                        frac |= static_cast<float>(zi) != z_pf[j];
+                    }
                 }
-                for (int i = tid + 2 * CT; i < nrows; i += CT) zz_s[i] = zconsts(zint(load_z(r0 + i)));
+                for (int i = tid + 2 * CT; i < nrows; i += CT) {
+                    const float z = load_z(r0 + i);
+                    const int zi = zint(z);
+                    zz_s[i] = zconsts(zi);
+                    frac |= static_cast<float>(zi) != z;
+                }
+                if (frac) *frac_seen = 1u;
             }
         };
         bool f16 = false;   // this CTA's main loop runs on fp16 MMAs
@@ -553,8 +568,10 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const void* __restrict__ scale,
             // each MMA over a staged fragment into column sums (fp32
             // accumulation, as in the main product).  Warps take the (kb, word)
             // pairs round-robin, two at a time on independent accumulators.
-            // They are needed only to fold out a fractional zero point.
-            if (!f16) {
+            // They are needed only to fold out a fractional zero point, so
+            // they are skipped when no row of this CTA has one.
+            const bool need_sums = *frac_seen != 0u;
+            if (!f16 && need_sums) {
                 const uint32_t ones = 0x3F803F80u;   // bf16x2 (1.0, 1.0)
                 const uint32_t a1s[4] = {ones, ones, ones, ones};
                 float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
@@ -590,9 +607,11 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const void* __restrict__ scale,
             }   // (fp16: the sums were stored before the last barrier)
             if (tid < C) {
                 float se = 0.f, so = 0.f;
-                for (int w = 0; w < NC; ++w) {
-                    se += xsw[(w * C + tid) * 2];
-                    so += xsw[(w * C + tid) * 2 + 1];
+                if (f16 || need_sums) {
+                    for (int w = 0; w < NC; ++w) {
+                        se += xsw[(w * C + tid) * 2];
+                        so += xsw[(w * C + tid) * 2 + 1];
+                    }
                 }
                 // the accumulators hold sum (q - zi) x in the units of the
                 // staged x: undo its scaling by 2^e (one column only)
@@ -681,7 +700,7 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const void* __restrict__ scale,
                     for (int t = 0; t < RT; ++t) ok = ok && mbar_wait_fast(bar_full + 8 * sl[t], rd[t] & 1, abort_flag);
                     if (ok) {
                         for (int u = first; u < units; u += NC) {
-                            const uint4* xb = xlane + (ch * (P.kchunk / KB) + u) * xkb_stride;
+                            [[maybe_unused]] const uint4* xb = xlane + (ch * (P.kchunk / KB) + u) * xkb_stride;
                             uint32_t wav[RT][4], wbv[RT][4];
 #pragma unroll
                             for (int t = 0; t < RT; ++t) {
@@ -925,15 +944,16 @@ Plan make_plan(int N, int K, int sms, int max_clusters_for_S /* 0: unknown */, i
     P.S = S;
     P.kslice = slice_of(S);
     // Row groups own whole 16-row tiles (a partial tile costs a full stage of
-    // consumer time, so a finer split would not shorten the busiest group).
-    // Of the row-group counts that give the busiest group the same number of
-    // tiles, take the smallest: the SMs left over hold the next launch's
-    // CTAs early (see the launch trigger in the kernel).
+    // consumer time, so a finer split would not shorten the busiest group),
+    // one group (or cluster) per SM: every SM streams, and the CTAs with one
+    // tile fewer finish early, letting the next launch's CTAs in (measured
+    // faster on every workload shape than the smallest grid with the same
+    // busiest group).
     const int64_t tiles = (static_cast<int64_t>(N) + 15) / 16;
     int groups = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(sms / S, tiles)));
     if (max_clusters_for_S > 0) groups = std::min(groups, max_clusters_for_S);
     const int64_t per = std::max<int64_t>(1, (tiles + groups - 1) / groups);
-#ifndef W4_GEMV_ALLSM
+#ifdef W4_GEMV_MINGRID
     groups = static_cast<int>(std::max<int64_t>(1, (tiles + per - 1) / per));
 #endif
     P.groups = groups;
