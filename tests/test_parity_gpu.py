@@ -196,6 +196,24 @@ def test_gemv_ragged_and_edge(w4, N, K, C, act):
     _check_gemv(w4, N, K, C, act, seed=N + K + C)
 
 
+@pytest.mark.parametrize("N,K", [
+    (50, 5120),      # fewer 16-row tiles than SMs, a short last tile
+    (1001, 4096),    # rows not a multiple of 16 or of the SM count
+    (153, 128),      # one 128-k unit per stage
+    (2000, 6144),    # 48 units per stage
+    (777, 1152),     # nine units per stage
+    (17296, 5120),   # the decode shape plus one tile
+])
+def test_gemv_one_column_shapes(w4, N, K):
+    """One column of bf16 x (the fp16 tensor-core loop): fewer 16-row tiles
+    than SMs, ragged row counts, a single 128-k unit, long and odd unit
+    counts, and rows at the zero point (exactly 0)."""
+    _check_gemv(w4, N, K, 1, "bf16", seed=N + K)
+    g = synth.gemv_inputs(N, K, 1, act="bf16", seed=N + 2 * K, zero_value=8, zero_rows=7)
+    got = w4.gemv_w4(g.qweight.to(_dev()), g.scale.to(_dev()), g.zero.to(_dev()), g.x.to(_dev()))
+    assert torch.all(got.float()[0, ::7] == 0)
+
+
 def test_gemv_non_integer_zero_and_wide_scales(w4):
     _check_gemv(w4, 500, 2048, 4, "bf16", seed=3, zero_value=7.3, scale_range=(0.5, 4.0))
     _check_gemv(w4, 500, 2048, 2, "f32", seed=4, zero_value=0.013, scale_range=(1e-3, 1.0))
