@@ -66,8 +66,7 @@ quantize_q8_1_pt_kernel(const __nv_bfloat16* __restrict__ x, uint8_t* __restrict
     }
 }
 
-constexpr int WA_THREADS = 512;   // 16 warps; a warp takes whole rows
-constexpr int WA_BATCH = 4;       // 16-byte weight loads a lane keeps in flight
+constexpr int WA_THREADS = 512;   // 16 warps; a warp takes groups of whole rows
 
 // Shared memory of gemv_w4a8_kernel for C vectors of K elements: qs in
 // word-matched order (C*K bytes), d_b and s_b as floats (2 * C*K/32 * 4
@@ -80,17 +79,22 @@ inline size_t w4a8_smem_bytes(int64_t C, int64_t K) { return size_t(C) * K + siz
 // the order in which a weight word's nibbles come out of w & 0x0F0F0F0F and
 // (w >> 4) & 0x0F0F0F0F.  Plane 8 gives d_b and s_b (b = 4 i + j).
 //
-// Main loop: warp w takes rows w, w + total warps, ...; lane l loads the
-// 16-byte chunks b = l, l + 32, ... of the row (one chunk = eight words = 32
-// weights = q8_1 block b) and for each vector c adds
+// Main loop (the MMVQ page's split, section 3: a few rows per worker, so the
+// activations read from shared memory serve all of them): warp w takes row
+// groups of R rows (R = 4 for C <= 4, else 2) w, w + total warps, ...;
+// lane l loads the 16-byte chunks b = l, l + 32, ... of the group's rows
+// (one chunk = eight words = 32 weights = q8_1 block b) and, for each vector
+// c, reads block b of x once and adds for each of the R rows
 //   d_b * (dp4a(w & 0x0F0F0F0F, even) + dp4a((w >> 4) & 0x0F0F0F0F, odd))
 // over its four words; the lanes' sums are added by a shuffle tree and
-// lane 0 stores bf16(scale * (sum - zero * S_c)).
+// lanes 0..R-1 store bf16(scale * (sum - zero * S_c)) for their row.
 template <int C>
 __global__ void __launch_bounds__(WA_THREADS)
 gemv_w4a8_kernel(const uint32_t* __restrict__ qw, const __nv_bfloat16* __restrict__ scale,
                  const __nv_bfloat16* __restrict__ zero, const uint8_t* __restrict__ pt,
                  __nv_bfloat16* __restrict__ d, int64_t N, int64_t K) {
+    constexpr int R = C <= 4 ? 4 : 2;
+    constexpr int BATCH = R == 4 ? 2 : 4;   // chunks of each row a lane keeps in flight
     extern __shared__ __align__(16) uint8_t smem[];
     const int64_t bpr = K / 128, nb = K / 32;
     uint8_t* xs = smem;
@@ -132,48 +136,68 @@ gemv_w4a8_kernel(const uint32_t* __restrict__ qw, const __nv_bfloat16* __restric
     __syncthreads();
 
     const int64_t warps = int64_t(gridDim.x) * (WA_THREADS / 32);
-    for (int64_t r = int64_t(blockIdx.x) * (WA_THREADS / 32) + warp_id; r < N; r += warps) {
-        const uint8_t* row = reinterpret_cast<const uint8_t*>(qw + r * (K / 8));
-        float acc[C];
+    const int64_t groups = (N + R - 1) / R;
+    for (int64_t rg = int64_t(blockIdx.x) * (WA_THREADS / 32) + warp_id; rg < groups; rg += warps) {
+        const int64_t r0 = rg * R;
+        const uint8_t* rows[R];
+        bool have[R];
 #pragma unroll
-        for (int c = 0; c < C; ++c) acc[c] = 0.f;
-        for (int64_t b0 = lane; b0 < nb; b0 += 32 * WA_BATCH) {
-            uint4 w[WA_BATCH];
+        for (int r = 0; r < R; ++r) {
+            have[r] = r0 + r < N;
+            rows[r] = reinterpret_cast<const uint8_t*>(qw + (have[r] ? r0 + r : r0) * (K / 8));
+        }
+        float acc[R][C];
 #pragma unroll
-            for (int u = 0; u < WA_BATCH; ++u) {
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int c = 0; c < C; ++c) acc[r][c] = 0.f;
+        for (int64_t b0 = lane; b0 < nb; b0 += 32 * BATCH) {
+            uint4 w[BATCH][R];
+#pragma unroll
+            for (int u = 0; u < BATCH; ++u) {
                 const int64_t b = b0 + 32 * u;
-                w[u] = b < nb ? ldg_stream_u4(row + 16 * b) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+                for (int r = 0; r < R; ++r)
+                    w[u][r] = (b < nb && have[r]) ? ldg_stream_u4(rows[r] + 16 * b) : make_uint4(0, 0, 0, 0);
             }
 #pragma unroll
-            for (int u = 0; u < WA_BATCH; ++u) {
+            for (int u = 0; u < BATCH; ++u) {
                 const int64_t b = b0 + 32 * u;
                 if (b >= nb) break;
-                const uint32_t ww[4] = {w[u].x, w[u].y, w[u].z, w[u].w};
 #pragma unroll
                 for (int c = 0; c < C; ++c) {
                     const uint4* xv = reinterpret_cast<const uint4*>(xs + c * K + 32 * b);
                     const uint4 x0 = xv[0], x1 = xv[1];
                     const uint32_t xe[4] = {x0.x, x0.z, x1.x, x1.z};
                     const uint32_t xo[4] = {x0.y, x0.w, x1.y, x1.w};
-                    int dot = 0;
+                    const float dbc = db[c * nb + b];
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        dot = __dp4a(static_cast<int>(ww[q] & 0x0F0F0F0Fu), static_cast<int>(xe[q]), dot);
-                        dot = __dp4a(static_cast<int>((ww[q] >> 4) & 0x0F0F0F0Fu), static_cast<int>(xo[q]), dot);
+                    for (int r = 0; r < R; ++r) {
+                        const uint32_t ww[4] = {w[u][r].x, w[u][r].y, w[u][r].z, w[u][r].w};
+                        int dot = 0;
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            dot = __dp4a(static_cast<int>(ww[q] & 0x0F0F0F0Fu), static_cast<int>(xe[q]), dot);
+                            dot = __dp4a(static_cast<int>((ww[q] >> 4) & 0x0F0F0F0Fu), static_cast<int>(xo[q]), dot);
+                        }
+                        acc[r][c] = fmaf(dbc, static_cast<float>(dot), acc[r][c]);
                     }
-                    acc[c] = fmaf(db[c * nb + b], static_cast<float>(dot), acc[c]);
                 }
             }
         }
 #pragma unroll
-        for (int c = 0; c < C; ++c) {
+        for (int r = 0; r < R; ++r)
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) acc[c] += __shfl_xor_sync(0xFFFFFFFFu, acc[c], o);
-        }
-        if (lane == 0) {
-            const float s = __bfloat162float(scale[r]), z = __bfloat162float(zero[r]);
+            for (int c = 0; c < C; ++c)
 #pragma unroll
-            for (int c = 0; c < C; ++c) d[c * N + r] = __float2bfloat16_rn(s * fmaf(-z, S[c], acc[c]));
+                for (int o = 16; o > 0; o >>= 1) acc[r][c] += __shfl_xor_sync(0xFFFFFFFFu, acc[r][c], o);
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            if (lane == r && have[r]) {
+                const float s = __bfloat162float(scale[r0 + r]), z = __bfloat162float(zero[r0 + r]);
+#pragma unroll
+                for (int c = 0; c < C; ++c) d[c * N + r0 + r] = __float2bfloat16_rn(s * fmaf(-z, S[c], acc[r][c]));
+            }
         }
     }
 }
@@ -188,7 +212,7 @@ w4_status launch_w4a8(const void* qw, const void* scale, const void* zero, const
     int per_sm = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, WA_THREADS, smem) != cudaSuccess || per_sm < 1)
         return W4_ERR_CUDA;
-    const int64_t warps_needed = N, warps_per_cta = WA_THREADS / 32;
+    const int64_t warps_needed = (N + (C <= 4 ? 4 : 2) - 1) / (C <= 4 ? 4 : 2), warps_per_cta = WA_THREADS / 32;
     int64_t blocks = int64_t(sm_count()) * per_sm;
     const int64_t max_useful = (warps_needed + warps_per_cta - 1) / warps_per_cta;
     if (blocks > max_useful) blocks = max_useful;
