@@ -263,11 +263,19 @@ KERNEL_SOURCES = {
              "gemm_int4_dequant_gb300/csrc/common.cuh"],
     "quant": ["gemm_int4_dequant_gb300/csrc/quant_permute.cu", "gemm_int4_dequant_gb300/csrc/ptx.cuh",
               "gemm_int4_dequant_gb300/csrc/common.cuh"],
+    "gemv8": ["gemm_int4_dequant_gb300/csrc/int8.cu", "gemm_int4_dequant_gb300/csrc/common.cuh"],
+    "w4a8": ["gemm_int4_dequant_gb300/csrc/w4a8.cu", "gemm_int4_dequant_gb300/csrc/common.cuh"],
+    "ptq1": ["gemm_int4_dequant_gb300/csrc/ptq1.cu", "gemm_int4_dequant_gb300/csrc/ptx.cuh",
+             "gemm_int4_dequant_gb300/csrc/common.cuh"],
 }
 
 
+# ncu summary per workload; for the two-kernel steps (w4a8, ptq1) the traffic
+# is that of the GEMV, the step's dominant kernel
 PROFILE_FILES = {"decode": "gemv_decode_ncu.md", "gemm": "gemm_8192_ncu.md", "quant": "quant_8192_ncu.md",
-                 "c8_perm": "gemv_perm_c8_ncu.md"}
+                 "c8_perm": "gemv_perm_c8_ncu.md", "c8": "gemv_c8_ncu.md", "c8s": "gemv_c8s_ncu.md",
+                 "w8_decode": "gemv_w8_decode_ncu.md", "w4a8_decode": "gemv_w4a8_decode_ncu.md",
+                 "ptq1_decode": "mmvq_ptq1_decode_ncu.md"}
 
 
 def recorded_traffic(kind, workload):
