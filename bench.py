@@ -653,11 +653,12 @@ def time_graph(work, steps, warmup, world):
 
 
 def isolated_steps(work, n=50):
-    """Median time of one step launched alone: before each, a 256 MB write
+    """Mean time of one step launched alone: before each, a 256 MB write
     evicts L2 (cold weights and x) and a short GPU spin keeps the device busy
     while the host prepares the launch, so the event pair brackets the
     step's kernels and not the host; a device synchronise follows every
-    step."""
+    step.  The mean, not the median: event timestamps here come in steps of
+    about 2 us, and averaging 50 samples resolves below that."""
     stream = torch.cuda.Stream()
     flush = torch.empty(256 * 2**20, dtype=torch.uint8, device="cuda")
     times = []
@@ -673,7 +674,7 @@ def isolated_steps(work, n=50):
             if i >= 3:
                 times.append(e0.elapsed_time(e1) / 1e3)
     del flush
-    return statistics.median(times)
+    return statistics.fmean(times)
 
 
 def soak(g, stream, seconds):
@@ -1083,7 +1084,7 @@ def run_ours(args, world, rank):
                      "frac": roofline(work, iso_sec / work.launches_per_step, peaks, peak_src, kind,
                                       args.workload)["frac"],
                      "how": "one step alone after a 256 MB L2-evicting write, device synchronise after it; "
-                            "median of 50"},
+                            "mean of 50"},
         "gpu_launches": args.steps * work.launches_per_step,
         "clocks": clocks,
         "e2e": {"value": e2e_val, "unit": unit_of(work), "h2d_bytes_per_step": hb, "d2h_bytes_per_step": ob},
