@@ -83,7 +83,7 @@ using namespace ptx;
 static __device__ int g_short_first_stage;
 
 #ifndef W4_GEMV_NC
-#define W4_GEMV_NC 16
+#define W4_GEMV_NC 12                           // three consumer warps per SM sub-partition
 #endif
 constexpr int NC = W4_GEMV_NC;                // consumer warps
 constexpr int THREADS = (NC + 1) * 32;        // + one producer warp
@@ -100,6 +100,10 @@ constexpr int KCHUNK_MAX = W4_GEMV_KCHUNK;    // k per stage at most (4 KB per r
 #ifndef W4_GEMV_SMEM
 #define W4_GEMV_SMEM (227 * 1024)
 #endif
+#ifndef W4_GEMV_XR
+#define W4_GEMV_XR 14                           // x fragments staged per consumer thread at most
+#endif
+constexpr int XR_MAX = W4_GEMV_XR;
 #ifndef W4_GEMV_PREFETCH_STAGES
 #define W4_GEMV_PREFETCH_STAGES 3               // stages warmed in L2 before the wait (one column of x)
 #endif
@@ -127,6 +131,10 @@ struct Plan {
     int xpitch;     // permuted layout: bytes per row of x in shared memory (16 mod 128); 0 otherwise
 };
 
+// Base alignment of the dynamic shared memory layout: tensor copies land at
+// 128-byte aligned addresses (every stage and box offset is a multiple of 256)
+constexpr int kSmemAlign = 128;
+
 struct Layout {
     int stage_bytes, xf, xzero, red, part, partw, xsw, xsum, sz, zz, rcv, rxs, bars, abort, total;
 };
@@ -147,7 +155,10 @@ __host__ __device__ inline Layout make_layout(int C, const Plan& P) {
     // nonzero |x| (bf16 bits, one column), [16, 24) the largest |x| (bf16
     // bits), later 0, [24, 32) the factor that undoes the scaling of x
     L.xsum = o;      o += 32 * 4;
-    L.sz = o;        o += P.rows_cap * 8;          // (scale, z - zint(z)) per row as fp32
+    // (scale, z - zint(z)) per row as fp32; with one column and no K split
+    // each thread finishes the rows whose scale and zero point it holds in
+    // registers, and the table is not needed
+    L.sz = o;        o += (C > 1 || P.S > 1) ? P.rows_cap * 8 : 0;
     o = (o + 15) & ~15;
     // per row, what the main loop subtracts after the unpack (zi = zint(z)):
     // fp16 (1024 + zi, even k) and the addend -(64 + zi) of the odd-k FMA,
@@ -176,7 +187,8 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const void* __restrict__ scale,
                 const __grid_constant__ CUtensorMap tm16, const __grid_constant__ CUtensorMap tm4) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
-    uint8_t* sm = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+    constexpr uint32_t kAl = kSmemAlign;
+    uint8_t* sm = smem_raw + (((raw_addr + (kAl - 1)) & ~(kAl - 1)) - raw_addr);
     const uint32_t sm_addr = smem_u32(sm);
     const Layout L = make_layout(C, P);
     const int S = P.S, NST = P.nst, pitch = P.pitch;
@@ -446,9 +458,9 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const void* __restrict__ scale,
                 // order (fp16: scaled and converted; bf16 with one column:
                 // scaled by a power of two when the largest |x| is below
                 // 2^14).  At most XR entries per thread: the plan keeps the
-                // fragments within 10 entries per consumer thread.
+                // fragments within XR entries per consumer thread.
                 const int per_n = nkb * 16;
-                constexpr int XR = 10;
+                constexpr int XR = XR_MAX;
                 const int dn = per_n > 0 ? CT / per_n : 0, dj = CT - dn * per_n;
                 const int n_cur = per_n > 0 ? tid / per_n : C, j_cur = tid - n_cur * per_n;
                 const int mine = (C * per_n - tid + CT - 1) / CT;   // entries of this thread (<= XR)
@@ -827,16 +839,39 @@ gemv_tma_kernel(const uint8_t* __restrict__ qw, const void* __restrict__ scale,
         } else {
             main_loop(std::false_type{});
         }
+        const bool row_regs = C == 1 && S == 1;   // rows finished by the threads holding their s, z
+        if (!row_regs) {
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            const int i = tid + j * CT;
-            if (i < nrows) sz[i] = make_float2(sc_pf[j], z_pf[j] - static_cast<float>(zint(z_pf[j])));
+            for (int j = 0; j < 2; ++j) {
+                const int i = tid + j * CT;
+                if (i < nrows) sz[i] = make_float2(sc_pf[j], z_pf[j] - static_cast<float>(zint(z_pf[j])));
+            }
+            for (int i = tid + 2 * CT; i < nrows; i += CT) {
+                const float z = load_z(r0 + i);
+                sz[i] = make_float2(load_s(r0 + i), z - static_cast<float>(zint(z)));
+            }
         }
-        for (int i = tid + 2 * CT; i < nrows; i += CT) {
-            const float z = load_z(r0 + i);
-            sz[i] = make_float2(load_s(r0 + i), z - static_cast<float>(zint(z)));
-        }
-        if (S == 1) {
+        if (row_regs) {
+            // one column, no K split: thread tid finishes rows tid, tid + CT
+            // (scale and zero point still in its registers), then every
+            // further CT-th row (loaded again)
+            named_barrier(1, CT);
+            auto finish = [&](int r, float sc, float z) {
+                float v;
+                if (P.perwarp) {
+                    v = 0.f;
+                    for (int w = 0; w < NC; ++w) v += partw[static_cast<size_t>(w) * rows16 + r];
+                    v *= xsum[24];
+                } else {
+                    v = part[r];
+                }
+                const float zf = z - static_cast<float>(zint(z));
+                d[r0 + r] = __float2bfloat16_rn(sc * fmaf(-zf, xsum[0], v));
+            };
+            if (tid < nrows) finish(tid, sc_pf[0], z_pf[0]);
+            if (tid + CT < nrows) finish(tid + CT, sc_pf[1], z_pf[1]);
+            for (int r = tid + 2 * CT; r < nrows; r += CT) finish(r, load_s(r0 + r), load_z(r0 + r));
+        } else if (S == 1) {
             // no K split: add the warps' partials (or take the tile sums),
             // fold the zero point, scale and store straight away
             named_barrier(1, CT);
@@ -923,9 +958,9 @@ namespace {
 using namespace gtma;
 
 constexpr int kSmemMax = W4_GEMV_SMEM;
-// x fragments: at most 10 16-byte entries per consumer thread (the staging
-// pass keeps them in registers)
-constexpr size_t kXfBudget = static_cast<size_t>(10) * CT * 16;
+// x fragments: at most XR_MAX 16-byte entries per consumer thread (the
+// staging pass keeps them in registers)
+constexpr size_t kXfBudget = static_cast<size_t>(XR_MAX) * CT * 16;
 
 // Pipeline shape for (N, K, C) on `sms` SMs; nst == 0 if nothing fits.
 template <int C, bool PERM>
@@ -984,7 +1019,7 @@ Plan make_plan(int N, int K, int sms, int max_clusters_for_S /* 0: unknown */, i
     for (int pw = 1; pw >= 0; --pw) {
         P.perwarp = pw;
         P.nst = MAX_NST;
-        while (P.nst >= 2 && make_layout(C, P).total + 1024 > kSmemMax) --P.nst;
+        while (P.nst >= 2 && make_layout(C, P).total + kSmemAlign > kSmemMax) --P.nst;
         if (P.nst >= (pw ? 3 : 2)) return P;
     }
     P.nst = 0;
@@ -1012,7 +1047,7 @@ w4_status launch_gemv_tma_t(const void* qw, const void* scale, const void* zero,
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    cudaError_t e = ensure_smem_limit(kern, make_layout(C, P).total + 1024, smem_set);
+    cudaError_t e = ensure_smem_limit(kern, make_layout(C, P).total + kSmemAlign, smem_set);
     if (e != cudaSuccess) return W4_ERR_CUDA;
     if (P.S > 1) {
         // every cluster must be resident at once: cap the row groups by the
@@ -1023,18 +1058,18 @@ w4_status launch_gemv_tma_t(const void* qw, const void* scale, const void* zero,
         const int si = P.S == 2 ? 0 : P.S == 4 ? 1 : 2;
         if (max_clusters[dev][si] == 0) {
             cfg.gridDim = dim3(P.S * P.groups, 1, 1);
-            cfg.dynamicSmemBytes = make_layout(C, P).total + 1024;
+            cfg.dynamicSmemBytes = make_layout(C, P).total + kSmemAlign;
             int n = 0;
             if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) return W4_ERR_CUDA;
             max_clusters[dev][si] = n;
         }
         P = make_plan<C, PERM>(N, K, sms, max_clusters[dev][si], P.S);
         if (P.nst == 0) return W4_ERR_SHAPE;
-        e = ensure_smem_limit(kern, make_layout(C, P).total + 1024, smem_set);
+        e = ensure_smem_limit(kern, make_layout(C, P).total + kSmemAlign, smem_set);
         if (e != cudaSuccess) return W4_ERR_CUDA;
     }
     cfg.gridDim = dim3(P.S * P.groups, 1, 1);
-    cfg.dynamicSmemBytes = make_layout(C, P).total + 1024;
+    cfg.dynamicSmemBytes = make_layout(C, P).total + kSmemAlign;
     CUtensorMap tm16, tm4;
     memset(&tm16, 0, sizeof(tm16));
     memset(&tm4, 0, sizeof(tm4));
