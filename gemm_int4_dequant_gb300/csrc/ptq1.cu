@@ -9,8 +9,12 @@
 // Encoding read where the page is silent: trit t is the digit u = t + 1 and
 // a byte is sum_p u_p 3^p; qh's 2-bit field j is tail trit j.
 //
-// Work split (the page's): a thread takes one 128-weight block i of R rows
-// (R = 4 for C <= 4, else 2), so the x of block i is read once for R rows.
+// Work split: as on the page, a thread's unit of work is one 128-weight
+// block i of R rows (R = 4 for C <= 4, else 2), so the x of block i is read
+// once for R rows.  GB300 layout of the work: one CTA per SM stages x once
+// and owns a contiguous range of row groups; its threads share the groups
+// out, a group's blocks split over T / G threads that each keep their R x C
+// sums in registers, added at the end in thread order.
 // Digit p of a qs byte lines up with PT plane p: for head word m (qs bytes
 // 4m .. 4m+3) digit p of its four bytes are elements 16p + 4m .. 16p + 4m + 3,
 // i.e. word m of plane p -- one dp4a each.  The integer dots are taken on
@@ -28,7 +32,7 @@ namespace w4 {
 
 namespace {
 
-constexpr int PQ_THREADS = 256;
+constexpr int PQ_THREADS = 512;
 constexpr int PQ_BLOCK_BYTES = 28;
 
 // Base-3 digits of two values 0..242 held in the 16-bit lanes of x: u[p] is
@@ -67,20 +71,24 @@ __device__ __forceinline__ int dp4(uint32_t a, uint32_t b, int c) {
 
 // Shared memory: x transposed so that lanes reading consecutive blocks read
 // consecutive words -- xs[c][plane][word][block] (C*K bytes) -- the q8_1
-// scales dx[c][block][j] and sums of qs sq[c][block][j], then the partial
-// sums of the items part[item][R][C].
+// scales dx[c][block][j] and sums of qs sq[c][block][j]; once every thread
+// is done with x, the threads' partial sums part[thread][R][C] take the same
+// space.  PTQ1_1's codebook follows both.
 struct PqLayout {
-    size_t xs, dx, sq, part, total;
+    size_t xs, dx, sq, part, code, total;
 };
 
-__host__ __device__ inline PqLayout pq_layout(int64_t C, int64_t K, int64_t items, int R) {
+__host__ __device__ inline PqLayout pq_layout(int64_t C, int64_t K, int R, bool super) {
     const int64_t bpr = K / 128;
     PqLayout L;
     L.xs = 0;
     L.dx = size_t(C) * K;
     L.sq = L.dx + size_t(C) * bpr * 4 * 4;
-    L.part = L.sq + size_t(C) * bpr * 4 * 4;
-    L.total = L.part + size_t(items) * R * C * 4;
+    L.part = 0;
+    const size_t x_end = L.sq + size_t(C) * bpr * 4 * 4;
+    const size_t part_end = size_t(PQ_THREADS) * R * C * 4;
+    L.code = ((x_end > part_end ? x_end : part_end) + 15) / 16 * 16;
+    L.total = L.code + (super ? size_t(767 * 8) : 0);
     return L;
 }
 
@@ -137,7 +145,7 @@ __device__ __forceinline__ uint32_t digit_of(uint32_t b, uint32_t p) {
 template <int C, int R>
 __device__ __forceinline__ void mmvq_item(const uint32_t (&qs)[R][6], const uint32_t (&tail)[R][2],
                                           const float (&dw)[R], const uint32_t* xs, const float* dx, const int* sq,
-                                          int64_t bpr, int64_t i, float* out) {
+                                          int64_t bpr, int64_t i, float (&acc)[R][C]) {
     int dot[R][C][4];
 #pragma unroll
     for (int r = 0; r < R; ++r)
@@ -205,7 +213,7 @@ __device__ __forceinline__ void mmvq_item(const uint32_t (&qs)[R][6], const uint
             float a = 0.f;
 #pragma unroll
             for (int j = 0; j < 4; ++j) a = fmaf(dxj[j], static_cast<float>(dot[r][c][j] - sqj[j]), a);
-            out[r * C + c] = dw[r] * a;
+            acc[r][c] = fmaf(dw[r], a, acc[r][c]);
         }
     }
 }
@@ -214,7 +222,7 @@ __device__ __forceinline__ void mmvq_item(const uint32_t (&qs)[R][6], const uint
 template <int C, int R>
 __device__ __forceinline__ void ptq1_0_item(const uint8_t* __restrict__ blocks, const uint32_t* xs,
                                              const float* dx, const int* sq, int64_t N, int64_t bpr, int64_t row0,
-                                             int64_t i, float* out) {
+                                             int64_t i, float (&acc)[R][C]) {
     uint32_t qs[R][6], tail[R][2];
     float dw[R];
 #pragma unroll
@@ -228,7 +236,7 @@ __device__ __forceinline__ void ptq1_0_item(const uint8_t* __restrict__ blocks, 
         tail[r][1] = spread2((w6 >> 8) & 0xFFu);
         dw[r] = __half2float(__ushort_as_half(static_cast<unsigned short>(w6 >> 16)));
     }
-    mmvq_item<C, R>(qs, tail, dw, xs, dx, sq, bpr, i, out);
+    mmvq_item<C, R>(qs, tail, dw, xs, dx, sq, bpr, i, acc);
 }
 
 // PTQ1_1 superblock (216 bytes): qs[192] (block s at 24 s), qh[13] at 192,
@@ -258,7 +266,7 @@ __device__ __forceinline__ void ptq1_1_item(const uint8_t* __restrict__ sblocks,
                                              int64_t n_code, const int64_t* __restrict__ esc_idx,
                                              const uint8_t* __restrict__ esc_patt, int64_t n_esc,
                                              const uint32_t* xs, const float* dx, const int* sq, int64_t N,
-                                             int64_t bpr, int64_t row0, int64_t i, float* out) {
+                                             int64_t bpr, int64_t row0, int64_t i, float (&acc)[R][C]) {
     const int64_t sbpr = (bpr + 7) / 8, sb = i / 8;
     const uint32_t s = static_cast<uint32_t>(i % 8);
     uint32_t qs[R][6], tail[R][2];
@@ -302,52 +310,77 @@ __device__ __forceinline__ void ptq1_1_item(const uint8_t* __restrict__ sblocks,
         const uint32_t e = pat ? pat[s] : 0u;
         dw[r] = pat ? __half2float(__ushort_as_half(static_cast<unsigned short>((e << 10) | mant))) : 0.f;
     }
-    mmvq_item<C, R>(qs, tail, dw, xs, dx, sq, bpr, i, out);
+    mmvq_item<C, R>(qs, tail, dw, xs, dx, sq, bpr, i, acc);
 }
 
-// CTA b takes the row groups [b G, b G + G) (R rows each): its items are
-// (row group, block) pairs, spread over the threads; the R*C partial sums
-// of each item go to shared memory and are added over the blocks of a row
-// in block order.  d is fp32 [C][N].  PTQ1_1 also copies the codebook into
-// shared memory.
+// CTA b takes the row groups [b G, b G + G) (R rows each).  With G <= T
+// threads, group g goes to threads [g tpg, g tpg + tpg), tpg = T / G: thread
+// j of them takes blocks j, j + tpg, ... in order and keeps R*C sums in
+// registers; after a barrier the sums go to shared memory (over the staged
+// x) and the group's first thread adds them in thread order.  With G > T
+// every thread takes whole groups (tpg = 1) and stores them itself.  d is
+// fp32 [C][N].  PTQ1_1 also copies the codebook into shared memory.
 template <int C, int R, bool SUPER>
 __global__ void __launch_bounds__(PQ_THREADS)
 mmvq_ptq1_kernel(const uint8_t* __restrict__ w, const uint8_t* __restrict__ codebook, int64_t n_code,
                  const int64_t* __restrict__ esc_idx, const uint8_t* __restrict__ esc_patt, int64_t n_esc,
                  const uint8_t* __restrict__ pt, float* __restrict__ d, int64_t N, int64_t K, int64_t G) {
     extern __shared__ __align__(16) uint8_t smem[];
-    const int64_t bpr = K / 128, items = G * bpr;
-    const PqLayout L = pq_layout(C, K, items, R);
+    const int64_t bpr = K / 128, groups = (N + R - 1) / R;
+    const PqLayout L = pq_layout(C, K, R, SUPER);
     uint32_t* xs = reinterpret_cast<uint32_t*>(smem + L.xs);
     float* dx = reinterpret_cast<float*>(smem + L.dx);
     int* sq = reinterpret_cast<int*>(smem + L.sq);
     float* part = reinterpret_cast<float*>(smem + L.part);
-    uint8_t* code = smem + L.total;
+    uint8_t* code = smem + L.code;
     if (SUPER)
         for (int64_t t = threadIdx.x; t < 8 * n_code; t += PQ_THREADS) code[t] = codebook[t];
     stage_x<C>(pt, xs, dx, sq, bpr);
     __syncthreads();
-    const int64_t rg0 = int64_t(blockIdx.x) * G;
-    for (int64_t t = threadIdx.x; t < items; t += PQ_THREADS) {
-        const int64_t g = t / bpr, i = t % bpr;
-        if (SUPER)
-            ptq1_1_item<C, R>(w, code, n_code, esc_idx, esc_patt, n_esc, xs, dx, sq, N, bpr, (rg0 + g) * R, i,
-                              part + t * R * C);
-        else
-            ptq1_0_item<C, R>(w, xs, dx, sq, N, bpr, (rg0 + g) * R, i, part + t * R * C);
+    const int64_t g0 = int64_t(blockIdx.x) * G;
+    const int64_t gn = groups - g0 < G ? groups - g0 : G;   // groups of this CTA
+    const int tpg = gn <= PQ_THREADS ? static_cast<int>(PQ_THREADS / gn) : 1;
+    const int j = static_cast<int>(threadIdx.x) % tpg;
+    const int gstep = PQ_THREADS / tpg;
+    float acc[R][C];
+    for (int64_t g = threadIdx.x / tpg; g < gn; g += gstep) {
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int c = 0; c < C; ++c) acc[r][c] = 0.f;
+        const int64_t row0 = (g0 + g) * R;
+        for (int64_t i = j; i < bpr; i += tpg) {
+            if (SUPER)
+                ptq1_1_item<C, R>(w, code, n_code, esc_idx, esc_patt, n_esc, xs, dx, sq, N, bpr, row0, i, acc);
+            else
+                ptq1_0_item<C, R>(w, xs, dx, sq, N, bpr, row0, i, acc);
+        }
+        if (tpg == 1) {
+#pragma unroll
+            for (int r = 0; r < R; ++r)
+#pragma unroll
+                for (int c = 0; c < C; ++c)
+                    if (row0 + r < N) d[c * N + row0 + r] = acc[r][c];
+        }
+    }
+    if (tpg == 1) return;
+    __syncthreads();   // every thread is done with x: its space takes the partial sums
+    if (threadIdx.x / tpg < gn) {
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int c = 0; c < C; ++c) part[(threadIdx.x * R + r) * C + c] = acc[r][c];
     }
     __syncthreads();
-    for (int64_t o = threadIdx.x; o < G * R * C; o += PQ_THREADS) {
+    for (int64_t o = threadIdx.x; o < gn * R * C; o += PQ_THREADS) {
         const int64_t g = o / (R * C), r = (o / C) % R, c = o % C;
-        const int64_t row = (rg0 + g) * R + r;
+        const int64_t row = (g0 + g) * R + r;
         if (row >= N) continue;
-        float s = 0.f;
-        for (int64_t i = 0; i < bpr; ++i) s += part[((g * bpr + i) * R + r) * C + c];
-        d[c * N + row] = s;
+        float sum = 0.f;
+        for (int t = 0; t < tpg; ++t) sum += part[((g * tpg + t) * R + r) * C + c];
+        d[c * N + row] = sum;
     }
 }
-
-constexpr size_t kCodebookBytes = 767 * 8;
 
 template <int C, bool SUPER>
 w4_status launch_ptq1(const void* w, const void* codebook, int64_t n_code, const void* esc_idx,
@@ -355,21 +388,17 @@ w4_status launch_ptq1(const void* w, const void* codebook, int64_t n_code, const
                       cudaStream_t stream) {
     constexpr int R = C <= 4 ? 4 : 2;
     static int smem_set[64];
-    const int64_t bpr = K / 128, groups = (N + R - 1) / R;
-    const size_t extra = SUPER ? kCodebookBytes : 0;
+    const int64_t groups = (N + R - 1) / R;
     const int sms = sm_count();
     if (sms <= 0) return W4_ERR_CUDA;
-    // about two CTAs per SM, at most 1024 items per CTA, within shared memory
-    int64_t G = (groups + 2 * sms - 1) / (2 * sms);
-    G = G < 1 ? 1 : G;
-    if (G * bpr > 1024) G = 1024 / bpr > 0 ? 1024 / bpr : 1;
-    while (G > 1 && pq_layout(C, K, G * bpr, R).total + extra > size_t(W4_W4A8_MAX_SMEM)) --G;
-    const size_t smem = pq_layout(C, K, G * bpr, R).total + extra;
+    // one CTA per SM, each a contiguous range of row groups
+    const int64_t ctas0 = groups < sms ? (groups > 0 ? groups : 1) : sms;
+    const int64_t G = (groups + ctas0 - 1) / ctas0 > 0 ? (groups + ctas0 - 1) / ctas0 : 1;
+    const int64_t ctas = groups > 0 ? (groups + G - 1) / G : 1;
+    const size_t smem = pq_layout(C, K, R, SUPER).total;
     if (smem > size_t(W4_W4A8_MAX_SMEM)) return W4_ERR_SHAPE;
     auto kern = mmvq_ptq1_kernel<C, R, SUPER>;
     if (ensure_smem_limit(kern, static_cast<int>(smem), smem_set) != cudaSuccess) return W4_ERR_CUDA;
-    const int64_t ctas = (groups + G - 1) / G;
-    if (ctas > 0x7FFFFFFF) return W4_ERR_SHAPE;
     kern<<<static_cast<unsigned>(ctas), PQ_THREADS, smem, stream>>>(
         static_cast<const uint8_t*>(w), static_cast<const uint8_t*>(codebook), n_code,
         static_cast<const int64_t*>(esc_idx), static_cast<const uint8_t*>(esc_patt), n_esc,
@@ -394,7 +423,7 @@ w4_status run_ptq1(const void* w, const void* codebook, int64_t n_code, const vo
 
 bool ptq1_fits(int64_t C, int64_t K, bool super) {
     const int R = C <= 4 ? 4 : 2;
-    return pq_layout(C, K, K / 128, R).total + (super ? kCodebookBytes : 0) <= size_t(W4_W4A8_MAX_SMEM);
+    return pq_layout(C, K, R, super).total <= size_t(W4_W4A8_MAX_SMEM);
 }
 
 w4_status run_mmvq_ptq1_0(const void* blocks, const void* pt, float* d, int64_t N, int64_t K, int64_t C,

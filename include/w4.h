@@ -411,8 +411,8 @@ w4_status gemv_w4a8(const void* qweight, const void* scale, const void* zero, co
  * pt      quantize_q8_1_pt's output for the C vectors, 16-byte aligned.
  * d       fp32 [C][N] row-major (output), 16-byte aligned.
  * Requires K % 128 == 0, 1 <= C <= 8 and x within shared memory
- * (C * K * 21/16 <= W4_W4A8_MAX_SMEM at C > 4, C * K * 11/8 at C <= 4;
- * K <= 22016 at C = 8), else W4_ERR_SHAPE; K == 0 gives d = 0.  The integer
+ * (C * K * 5/4 <= W4_W4A8_MAX_SMEM, so K <= 23168 at C = 8), else
+ * W4_ERR_SHAPE; K == 0 gives d = 0.  The integer
  * dots are exact; fp32 products and sums, within (K/128 + 5) * 2^-24 of
  * sum_k |w x| (2e-5 is the tested bound).
  */
@@ -440,7 +440,7 @@ w4_status mmvq_ptq1_0(const void* blocks, const void* pt, float* d, int64_t N, i
  * esc_idx   int64 [n_esc] superblock indices, ascending; esc_patt uint8
  *           [n_esc][8] their exponents.
  * pt, d, C, K: as mmvq_ptq1_0 (the codebook takes 6136 bytes more shared
- * memory).  All pointers 16-byte aligned; codebook / esc_* may be NULL when
+ * memory: K <= 22528 at C = 8).  All pointers 16-byte aligned; codebook / esc_* may be NULL when
  * n_code / n_esc is 0.  An index that names no entry records device error 2
  * (w4_device_error) and its blocks count as d = 0.
  */

@@ -142,7 +142,7 @@ def test_argument_validation_happens_on_host():
     assert lib.mmvq_ptq1_0(A, A, A, 16, 192, 1, None) == L.W4_ERR_SHAPE
     assert lib.mmvq_ptq1_0(A, A, A, 16, 128, 0, None) == L.W4_ERR_SHAPE
     assert lib.mmvq_ptq1_0(A, A, A, 16, 128, 9, None) == L.W4_ERR_SHAPE
-    assert lib.mmvq_ptq1_0(A, A, A, 16, 22016 + 128, 8, None) == L.W4_ERR_SHAPE
+    assert lib.mmvq_ptq1_0(A, A, A, 16, 23168 + 128, 8, None) == L.W4_ERR_SHAPE
     assert lib.mmvq_ptq1_0(A, A, A, 0, 128, 1, None) == L.W4_OK
     assert lib.mmvq_ptq1_0(None, A, A, 16, 128, 1, None) == L.W4_ERR_NULL
     assert lib.mmvq_ptq1_0(A, A, odd, 16, 128, 1, None) == L.W4_ERR_ALIGN
@@ -151,7 +151,7 @@ def test_argument_validation_happens_on_host():
     assert lib.mmvq_ptq1_1(A, A, -1, A, A, 1, A, A, 16, 1024, 1, None) == L.W4_ERR_SHAPE
     assert lib.mmvq_ptq1_1(A, A, 10, A, A, -1, A, A, 16, 1024, 1, None) == L.W4_ERR_SHAPE
     assert lib.mmvq_ptq1_1(A, A, 10, A, A, 1, A, A, 16, 1000, 1, None) == L.W4_ERR_SHAPE
-    assert lib.mmvq_ptq1_1(A, A, 10, A, A, 1, A, A, 16, 22016, 8, None) == L.W4_ERR_SHAPE
+    assert lib.mmvq_ptq1_1(A, A, 10, A, A, 1, A, A, 16, 22528 + 128, 8, None) == L.W4_ERR_SHAPE
     assert lib.mmvq_ptq1_1(A, None, 10, A, A, 1, A, A, 16, 1024, 1, None) == L.W4_ERR_NULL
     assert lib.mmvq_ptq1_1(A, A, 10, None, A, 1, A, A, 16, 1024, 1, None) == L.W4_ERR_NULL
     assert lib.mmvq_ptq1_1(A, A, 10, odd, A, 1, A, A, 16, 1024, 1, None) == L.W4_ERR_ALIGN

@@ -49,7 +49,7 @@ def _case(N, K, C, seed):
     (600, 1152, 3), (33, 640, 5),     # nine and five blocks a row; two rows a group at C > 4
     (17280, 5120, 1),                 # decode shape of the page's model
     (6144, 5120, 8), (5120, 17280, 4), (5120, 17280, 8),
-    (37, 22016, 8),                   # the largest K whose x fits shared memory at C = 8
+    (37, 23168, 8),                   # the largest K whose x fits shared memory at C = 8
 ])
 def test_mmvq_ptq1_0(w4, N, K, C):
     blocks, xb = _case(N, K, C, seed=N + K + C)
@@ -106,7 +106,7 @@ def _dev_tables(w):
     (1000, 1152, 2, 0.9),      # full codebook, free-trit indices and escapes; a padded last superblock
     (17280, 5120, 1, 0.002),   # decode shape
     (5120, 17280, 8, 0.0),     # 135 blocks a row: seventeen superblocks, the last holding seven blocks
-    (37, 21504, 8, 0.5),       # the largest K whose x and codebook fit shared memory at C = 8
+    (37, 22528, 8, 0.5),       # the largest K whose x and codebook fit shared memory at C = 8
 ])
 def test_mmvq_ptq1_1(w4, N, K, C, outliers):
     blocks, w, xb = _ptq1_1_case(N, K, C, N + K + C, outliers)
