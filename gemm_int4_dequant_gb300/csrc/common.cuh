@@ -44,6 +44,21 @@ inline cudaError_t ensure_smem_limit(Kernel k, int bytes, int (&flags)[64]) {
     return e;
 }
 
+// Threads given to each of a CTA's gn row groups when T threads split the
+// groups' nb blocks (a thread takes every tpg-th block of its group, thread
+// rounds go over the groups T / tpg at a time): T / gn, or one warp per
+// group when that is not slower (a warp's lanes then read consecutive
+// blocks of the same rows).  1 when there are more groups than threads.
+__host__ __device__ inline int threads_per_group(int T, int64_t gn, int64_t nb) {
+    if (gn >= T) return 1;
+    const int even = static_cast<int>(T / gn);
+    auto cost = [&](int tpg) {
+        const int64_t per_round = T / tpg;
+        return ((gn + per_round - 1) / per_round) * ((nb + tpg - 1) / tpg);
+    };
+    return (even < 32 && cost(32) <= cost(even)) ? 32 : even;
+}
+
 // ---------------------------------------------------------------------------
 // Device side
 // ---------------------------------------------------------------------------

@@ -11,10 +11,12 @@
 //
 // Work split: as on the page, a thread's unit of work is one 128-weight
 // block i of R rows (R = 4 for C <= 4, else 2), so the x of block i is read
-// once for R rows.  GB300 layout of the work: one CTA per SM stages x once
-// and owns a contiguous range of row groups; its threads share the groups
-// out, a group's blocks split over T / G threads that each keep their R x C
-// sums in registers, added at the end in thread order.
+// once for R rows.  GB300 layout of the work: each resident CTA (one of 512
+// threads per SM; two of 256 with one column) stages x once and owns a
+// contiguous range of row groups; its threads share the groups
+// out, a group's blocks split over T / G threads (or one warp) that each
+// keep their R x C sums in registers, added at the end in thread order (a
+// warp's by a shuffle tree).
 // Digit p of a qs byte lines up with PT plane p: for head word m (qs bytes
 // 4m .. 4m+3) digit p of its four bytes are elements 16p + 4m .. 16p + 4m + 3,
 // i.e. word m of plane p -- one dp4a each.  The integer dots are taken on
@@ -32,7 +34,8 @@ namespace w4 {
 
 namespace {
 
-constexpr int PQ_THREADS = 512;
+// threads per CTA: 512, or 256 with one column (two CTAs per SM)
+__host__ __device__ constexpr int pq_threads(int64_t C) { return C == 1 ? 256 : 512; }
 constexpr int PQ_BLOCK_BYTES = 28;
 
 // Base-3 digits of two values 0..242 held in the 16-bit lanes of x: u[p] is
@@ -86,7 +89,7 @@ __host__ __device__ inline PqLayout pq_layout(int64_t C, int64_t K, int R, bool 
     L.sq = L.dx + size_t(C) * bpr * 4 * 4;
     L.part = 0;
     const size_t x_end = L.sq + size_t(C) * bpr * 4 * 4;
-    const size_t part_end = size_t(PQ_THREADS) * R * C * 4;
+    const size_t part_end = size_t(pq_threads(C)) * R * C * 4;
     L.code = ((x_end > part_end ? x_end : part_end) + 15) / 16 * 16;
     L.total = L.code + (super ? size_t(767 * 8) : 0);
     return L;
@@ -97,7 +100,7 @@ __host__ __device__ inline PqLayout pq_layout(int64_t C, int64_t K, int R, bool 
 template <int C>
 __device__ void stage_x(const uint8_t* __restrict__ pt, uint32_t* xs, float* dx, int* sq, int64_t bpr) {
     const int64_t chunks = int64_t(C) * 8 * bpr;
-    for (int64_t t = threadIdx.x; t < chunks; t += PQ_THREADS) {
+    for (int64_t t = threadIdx.x; t < chunks; t += pq_threads(C)) {
         const int64_t c = t / (8 * bpr), rem = t % (8 * bpr), p = rem / bpr, i = rem % bpr;
         const uint4 v = *reinterpret_cast<const uint4*>(pt + c * 144 * bpr + 16 * (p * bpr + i));
         uint32_t* dst = xs + ((c * 8 + p) * 4) * bpr + i;
@@ -106,7 +109,7 @@ __device__ void stage_x(const uint8_t* __restrict__ pt, uint32_t* xs, float* dx,
         dst[2 * bpr] = v.z;
         dst[3 * bpr] = v.w;
     }
-    for (int64_t t = threadIdx.x; t < int64_t(C) * bpr; t += PQ_THREADS) {
+    for (int64_t t = threadIdx.x; t < int64_t(C) * bpr; t += pq_threads(C)) {
         const int64_t c = t / bpr, i = t % bpr;
         const uint4 v = *reinterpret_cast<const uint4*>(pt + c * 144 * bpr + 16 * (8 * bpr + i));
         const uint32_t pr[4] = {v.x, v.y, v.z, v.w};
@@ -115,7 +118,7 @@ __device__ void stage_x(const uint8_t* __restrict__ pt, uint32_t* xs, float* dx,
             dx[(c * bpr + i) * 4 + j] = __half2float(__ushort_as_half(static_cast<unsigned short>(pr[j] & 0xFFFFu)));
     }
     __syncthreads();
-    for (int64_t t = threadIdx.x; t < int64_t(C) * bpr; t += PQ_THREADS) {
+    for (int64_t t = threadIdx.x; t < int64_t(C) * bpr; t += pq_threads(C)) {
         const int64_t c = t / bpr, i = t % bpr;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -201,13 +204,11 @@ __device__ __forceinline__ void mmvq_item(const uint32_t (&qs)[R][6], const uint
     }
 #pragma unroll
     for (int c = 0; c < C; ++c) {
-        float dxj[4];
-        int sqj[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            dxj[j] = dx[(c * bpr + i) * 4 + j];
-            sqj[j] = sq[(c * bpr + i) * 4 + j];
-        }
+        // the block's four scales and sums of qs: one 16-byte load each
+        const float4 dx4 = *reinterpret_cast<const float4*>(dx + (c * bpr + i) * 4);
+        const int4 sq4 = *reinterpret_cast<const int4*>(sq + (c * bpr + i) * 4);
+        const float dxj[4] = {dx4.x, dx4.y, dx4.z, dx4.w};
+        const int sqj[4] = {sq4.x, sq4.y, sq4.z, sq4.w};
 #pragma unroll
         for (int r = 0; r < R; ++r) {
             float a = 0.f;
@@ -314,17 +315,20 @@ __device__ __forceinline__ void ptq1_1_item(const uint8_t* __restrict__ sblocks,
 }
 
 // CTA b takes the row groups [b G, b G + G) (R rows each).  With G <= T
-// threads, group g goes to threads [g tpg, g tpg + tpg), tpg = T / G: thread
+// threads, group g goes to threads [g tpg, g tpg + tpg), tpg = T / G (or 32,
+// a warp per group, when that is not slower; see threads_per_group): thread
 // j of them takes blocks j, j + tpg, ... in order and keeps R*C sums in
-// registers; after a barrier the sums go to shared memory (over the staged
-// x) and the group's first thread adds them in thread order.  With G > T
-// every thread takes whole groups (tpg = 1) and stores them itself.  d is
-// fp32 [C][N].  PTQ1_1 also copies the codebook into shared memory.
+// registers.  A warp's sums meet by a shuffle tree; otherwise, after a
+// barrier, the sums go to shared memory (over the staged x) and the group's
+// first thread adds them in thread order.  With G > T every thread takes
+// whole groups (tpg = 1) and stores them itself.  d is fp32 [C][N].
+// PTQ1_1 also copies the codebook into shared memory.
 template <int C, int R, bool SUPER>
-__global__ void __launch_bounds__(PQ_THREADS)
+__global__ void __launch_bounds__(pq_threads(C))
 mmvq_ptq1_kernel(const uint8_t* __restrict__ w, const uint8_t* __restrict__ codebook, int64_t n_code,
                  const int64_t* __restrict__ esc_idx, const uint8_t* __restrict__ esc_patt, int64_t n_esc,
                  const uint8_t* __restrict__ pt, float* __restrict__ d, int64_t N, int64_t K, int64_t G) {
+    constexpr int PQ_THREADS = pq_threads(C);
     extern __shared__ __align__(16) uint8_t smem[];
     const int64_t bpr = K / 128, groups = (N + R - 1) / R;
     const PqLayout L = pq_layout(C, K, R, SUPER);
@@ -339,7 +343,7 @@ mmvq_ptq1_kernel(const uint8_t* __restrict__ w, const uint8_t* __restrict__ code
     __syncthreads();
     const int64_t g0 = int64_t(blockIdx.x) * G;
     const int64_t gn = groups - g0 < G ? groups - g0 : G;   // groups of this CTA
-    const int tpg = gn <= PQ_THREADS ? static_cast<int>(PQ_THREADS / gn) : 1;
+    const int tpg = threads_per_group(PQ_THREADS, gn, bpr);
     const int j = static_cast<int>(threadIdx.x) % tpg;
     const int gstep = PQ_THREADS / tpg;
     float acc[R][C];
@@ -355,7 +359,16 @@ mmvq_ptq1_kernel(const uint8_t* __restrict__ w, const uint8_t* __restrict__ code
             else
                 ptq1_0_item<C, R>(w, xs, dx, sq, N, bpr, row0, i, acc);
         }
-        if (tpg == 1) {
+        if (tpg == 32) {
+            // a warp per group: its lanes' sums meet by a shuffle tree
+#pragma unroll
+            for (int r = 0; r < R; ++r)
+#pragma unroll
+                for (int c = 0; c < C; ++c)
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) acc[r][c] += __shfl_xor_sync(0xFFFFFFFFu, acc[r][c], o);
+        }
+        if (tpg == 1 || (tpg == 32 && j == 0)) {
 #pragma unroll
             for (int r = 0; r < R; ++r)
 #pragma unroll
@@ -363,7 +376,7 @@ mmvq_ptq1_kernel(const uint8_t* __restrict__ w, const uint8_t* __restrict__ code
                     if (row0 + r < N) d[c * N + row0 + r] = acc[r][c];
         }
     }
-    if (tpg == 1) return;
+    if (tpg == 1 || tpg == 32) return;   // (otherwise one round: T / tpg >= gn)
     __syncthreads();   // every thread is done with x: its space takes the partial sums
     if (threadIdx.x / tpg < gn) {
 #pragma unroll
@@ -391,15 +404,20 @@ w4_status launch_ptq1(const void* w, const void* codebook, int64_t n_code, const
     const int64_t groups = (N + R - 1) / R;
     const int sms = sm_count();
     if (sms <= 0) return W4_ERR_CUDA;
-    // one CTA per SM, each a contiguous range of row groups
-    const int64_t ctas0 = groups < sms ? (groups > 0 ? groups : 1) : sms;
-    const int64_t G = (groups + ctas0 - 1) / ctas0 > 0 ? (groups + ctas0 - 1) / ctas0 : 1;
-    const int64_t ctas = groups > 0 ? (groups + G - 1) / G : 1;
     const size_t smem = pq_layout(C, K, R, SUPER).total;
     if (smem > size_t(W4_W4A8_MAX_SMEM)) return W4_ERR_SHAPE;
     auto kern = mmvq_ptq1_kernel<C, R, SUPER>;
     if (ensure_smem_limit(kern, static_cast<int>(smem), smem_set) != cudaSuccess) return W4_ERR_CUDA;
-    kern<<<static_cast<unsigned>(ctas), PQ_THREADS, smem, stream>>>(
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, pq_threads(C), smem) != cudaSuccess || per_sm < 1)
+        return W4_ERR_CUDA;
+    // as many CTAs as are resident at once, each a contiguous range of row groups
+    int64_t ctas = int64_t(sms) * per_sm;
+    if (ctas > groups) ctas = groups;
+    if (ctas < 1) ctas = 1;
+    const int64_t G = groups > 0 ? (groups + ctas - 1) / ctas : 1;
+    ctas = groups > 0 ? (groups + G - 1) / G : 1;
+    kern<<<static_cast<unsigned>(ctas), pq_threads(C), smem, stream>>>(
         static_cast<const uint8_t*>(w), static_cast<const uint8_t*>(codebook), n_code,
         static_cast<const int64_t*>(esc_idx), static_cast<const uint8_t*>(esc_patt), n_esc,
         static_cast<const uint8_t*>(pt), d, N, K, G);

@@ -66,41 +66,57 @@ quantize_q8_1_pt_kernel(const __nv_bfloat16* __restrict__ x, uint8_t* __restrict
     }
 }
 
-constexpr int WA_THREADS = 512;   // 16 warps; a warp takes groups of whole rows
+constexpr int WA_THREADS = 512;
 
-// Shared memory of gemv_w4a8_kernel for C vectors of K elements: qs in
-// word-matched order (C*K bytes), d_b and s_b as floats (2 * C*K/32 * 4
-// bytes), and the C sums of s.
-inline size_t w4a8_smem_bytes(int64_t C, int64_t K) { return size_t(C) * K + size_t(C) * (K / 32) * 8 + 8 * 4; }
+__host__ __device__ constexpr int w4a8_rows(int64_t C) { return C <= 4 ? 4 : 2; }
+
+// Shared memory of gemv_w4a8_kernel for C vectors of K elements: the C sums
+// of s (32 bytes), then qs in word-matched order (C*K bytes) and d_b, s_b as
+// floats (2 * C*K/32 * 4 bytes); once x is no longer read, the threads'
+// partial sums [thread][R][C] take the space after the sums of s.
+inline size_t w4a8_smem_bytes(int64_t C, int64_t K) {
+    const size_t x = size_t(C) * K + size_t(C) * (K / 32) * 8;
+    const size_t part = size_t(WA_THREADS) * w4a8_rows(C) * C * 4;
+    return 32 + (x > part ? x : part);
+}
 
 // The x staging: every 16-byte chunk of planes 0..7 (elements k0 .. k0+15 of
-// one vector) is stored at byte c*K + k0 of `xs` with each 8-element group
-// split into its even elements (k, k+2, k+4, k+6) and then its odd ones --
-// the order in which a weight word's nibbles come out of w & 0x0F0F0F0F and
-// (w >> 4) & 0x0F0F0F0F.  Plane 8 gives d_b and s_b (b = 4 i + j).
+// one vector) is stored with each 8-element group split into its even
+// elements (k, k+2, k+4, k+6) and then its odd ones -- the order in which a
+// weight word's nibbles come out of w & 0x0F0F0F0F and (w >> 4) &
+// 0x0F0F0F0F.  The two 16-element halves of q8_1 block b (k0 = 32 b and
+// 32 b + 16) go to c*K + 16 b and c*K + K/2 + 16 b, so that threads reading
+// consecutive blocks read consecutive 16-byte words.  Plane 8 gives d_b and
+// s_b (b = 4 i + j).
 //
 // Main loop (the MMVQ page's split, section 3: a few rows per worker, so the
-// activations read from shared memory serve all of them): warp w takes row
-// groups of R rows (R = 4 for C <= 4, else 2) w, w + total warps, ...;
-// lane l loads the 16-byte chunks b = l, l + 32, ... of the group's rows
-// (one chunk = eight words = 32 weights = q8_1 block b) and, for each vector
-// c, reads block b of x once and adds for each of the R rows
+// activations read from shared memory serve all of them): CTA b owns row
+// groups [b G, b G + G) of R rows (R = 4 for C <= 4, else 2).  With G <= T
+// threads, a group's 16-byte chunks (one chunk = eight words = 32 weights =
+// q8_1 block) go to tpg = T / G threads: thread j loads chunks j, j + tpg,
+// ... of the group's rows and, for each vector c, reads block b of x once
+// and adds for each of the R rows
 //   d_b * (dp4a(w & 0x0F0F0F0F, even) + dp4a((w >> 4) & 0x0F0F0F0F, odd))
-// over its four words; the lanes' sums are added by a shuffle tree and
-// lanes 0..R-1 store bf16(scale * (sum - zero * S_c)) for their row.
+// over its four words, in registers; the tpg partial sums of a group are
+// added in thread order through shared memory (one warp per group: by a
+// shuffle tree) and one thread stores bf16(scale * (sum - zero * S_c)) per
+// row and vector.  With G > T every thread takes whole groups and stores
+// them itself.
+// (one column fits 64 registers: two CTAs per SM)
 template <int C>
-__global__ void __launch_bounds__(WA_THREADS)
+__global__ void __launch_bounds__(WA_THREADS, C == 1 ? 2 : 1)
 gemv_w4a8_kernel(const uint32_t* __restrict__ qw, const __nv_bfloat16* __restrict__ scale,
                  const __nv_bfloat16* __restrict__ zero, const uint8_t* __restrict__ pt,
-                 __nv_bfloat16* __restrict__ d, int64_t N, int64_t K) {
-    constexpr int R = C <= 4 ? 4 : 2;
-    constexpr int BATCH = R == 4 ? 2 : 4;   // chunks of each row a lane keeps in flight
+                 __nv_bfloat16* __restrict__ d, int64_t N, int64_t K, int64_t G) {
+    constexpr int R = w4a8_rows(C);
+    constexpr int BATCH = C == 1 ? 1 : R == 4 ? 2 : 4;   // chunks of each row a thread keeps in flight (64 registers at C = 1)
     extern __shared__ __align__(16) uint8_t smem[];
     const int64_t bpr = K / 128, nb = K / 32;
-    uint8_t* xs = smem;
-    float* db = reinterpret_cast<float*>(smem + size_t(C) * K);
+    float* S = reinterpret_cast<float*>(smem);
+    uint8_t* xs = smem + 32;
+    float* db = reinterpret_cast<float*>(xs + size_t(C) * K);
     float* sb = db + C * nb;
-    float* S = sb + C * nb;
+    float* part = reinterpret_cast<float*>(smem + 32);
 
     // stage planes 0..7
     const int64_t chunks = int64_t(C) * 8 * bpr;
@@ -110,7 +126,7 @@ gemv_w4a8_kernel(const uint32_t* __restrict__ qw, const __nv_bfloat16* __restric
         const uint4 v = *reinterpret_cast<const uint4*>(pt + c * 144 * bpr + 16 * (p * bpr + i));
         const uint4 w = make_uint4(__byte_perm(v.x, v.y, 0x6420), __byte_perm(v.x, v.y, 0x7531),
                                    __byte_perm(v.z, v.w, 0x6420), __byte_perm(v.z, v.w, 0x7531));
-        *reinterpret_cast<uint4*>(xs + c * K + 128 * i + 16 * p) = w;
+        *reinterpret_cast<uint4*>(xs + c * K + (p & 1) * (K / 2) + 16 * (4 * i + p / 2)) = w;
     }
     // plane 8
     for (int64_t t = threadIdx.x; t < int64_t(C) * bpr; t += WA_THREADS) {
@@ -135,42 +151,43 @@ gemv_w4a8_kernel(const uint32_t* __restrict__ qw, const __nv_bfloat16* __restric
     }
     __syncthreads();
 
-    const int64_t warps = int64_t(gridDim.x) * (WA_THREADS / 32);
+    const int xstride = static_cast<int>(K), xhalf = static_cast<int>(K / 2);
     const int64_t groups = (N + R - 1) / R;
-    for (int64_t rg = int64_t(blockIdx.x) * (WA_THREADS / 32) + warp_id; rg < groups; rg += warps) {
-        const int64_t r0 = rg * R;
-        const uint8_t* rows[R];
-        bool have[R];
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            have[r] = r0 + r < N;
-            rows[r] = reinterpret_cast<const uint8_t*>(qw + (have[r] ? r0 + r : r0) * (K / 8));
-        }
-        float acc[R][C];
+    const int64_t g0 = int64_t(blockIdx.x) * G;
+    const int64_t gn = groups - g0 < G ? groups - g0 : G;   // groups of this CTA
+    const int tpg = threads_per_group(WA_THREADS, gn, nb);
+    const int j = static_cast<int>(threadIdx.x) % tpg;
+    const int gstep = WA_THREADS / tpg;
+    float acc[R][C];
+    for (int64_t g = threadIdx.x / tpg; g < gn; g += gstep) {
+        const int64_t r0 = (g0 + g) * R;
+        const uint8_t* row0 = reinterpret_cast<const uint8_t*>(qw + r0 * (K / 8));   // row r at + r * K/2
+        const int nrow = N - r0 < R ? static_cast<int>(N - r0) : R;               // rows of this group
 #pragma unroll
         for (int r = 0; r < R; ++r)
 #pragma unroll
             for (int c = 0; c < C; ++c) acc[r][c] = 0.f;
-        for (int64_t b0 = lane; b0 < nb; b0 += 32 * BATCH) {
+        const int nbi = static_cast<int>(nb);
+        for (int b0 = j; b0 < nbi; b0 += tpg * BATCH) {
             uint4 w[BATCH][R];
 #pragma unroll
             for (int u = 0; u < BATCH; ++u) {
-                const int64_t b = b0 + 32 * u;
+                const int b = b0 + tpg * u;
 #pragma unroll
                 for (int r = 0; r < R; ++r)
-                    w[u][r] = (b < nb && have[r]) ? ldg_stream_u4(rows[r] + 16 * b) : make_uint4(0, 0, 0, 0);
+                    w[u][r] = (b < nbi && r < nrow) ? ldg_stream_u4(row0 + r * (K / 2) + 16 * b) : make_uint4(0, 0, 0, 0);
             }
 #pragma unroll
             for (int u = 0; u < BATCH; ++u) {
-                const int64_t b = b0 + 32 * u;
-                if (b >= nb) break;
+                const int b = b0 + tpg * u;
+                if (b >= nbi) break;
 #pragma unroll
                 for (int c = 0; c < C; ++c) {
-                    const uint4* xv = reinterpret_cast<const uint4*>(xs + c * K + 32 * b);
-                    const uint4 x0 = xv[0], x1 = xv[1];
+                    const uint4 x0 = *reinterpret_cast<const uint4*>(xs + c * xstride + 16 * b);
+                    const uint4 x1 = *reinterpret_cast<const uint4*>(xs + c * xstride + xhalf + 16 * b);
                     const uint32_t xe[4] = {x0.x, x0.z, x1.x, x1.z};
                     const uint32_t xo[4] = {x0.y, x0.w, x1.y, x1.w};
-                    const float dbc = db[c * nb + b];
+                    const float dbc = db[c * nbi + b];
 #pragma unroll
                     for (int r = 0; r < R; ++r) {
                         const uint32_t ww[4] = {w[u][r].x, w[u][r].y, w[u][r].z, w[u][r].w};
@@ -185,20 +202,42 @@ gemv_w4a8_kernel(const uint32_t* __restrict__ qw, const __nv_bfloat16* __restric
                 }
             }
         }
+        if (tpg == 32) {
+            // a warp per group: its lanes' sums meet by a shuffle tree
 #pragma unroll
-        for (int r = 0; r < R; ++r)
+            for (int r = 0; r < R; ++r)
 #pragma unroll
-            for (int c = 0; c < C; ++c)
+                for (int c = 0; c < C; ++c)
 #pragma unroll
-                for (int o = 16; o > 0; o >>= 1) acc[r][c] += __shfl_xor_sync(0xFFFFFFFFu, acc[r][c], o);
+                    for (int o = 16; o > 0; o >>= 1) acc[r][c] += __shfl_xor_sync(0xFFFFFFFFu, acc[r][c], o);
+        }
+        if (tpg == 1 || tpg == 32) {
 #pragma unroll
-        for (int r = 0; r < R; ++r) {
-            if (lane == r && have[r]) {
+            for (int r = 0; r < R; ++r) {
+                if (r >= nrow || (tpg == 32 && lane != r)) continue;
                 const float s = __bfloat162float(scale[r0 + r]), z = __bfloat162float(zero[r0 + r]);
 #pragma unroll
                 for (int c = 0; c < C; ++c) d[c * N + r0 + r] = __float2bfloat16_rn(s * fmaf(-z, S[c], acc[r][c]));
             }
         }
+    }
+    if (tpg == 1 || tpg == 32) return;   // (otherwise one round: T / tpg >= gn)
+    __syncthreads();   // x is no longer read: its space takes the partial sums
+    if (threadIdx.x / tpg < gn) {
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int c = 0; c < C; ++c) part[(threadIdx.x * R + r) * C + c] = acc[r][c];
+    }
+    __syncthreads();
+    for (int64_t o = threadIdx.x; o < gn * R * C; o += WA_THREADS) {
+        const int64_t g = o / (R * C), r = (o / C) % R, c = o % C;
+        const int64_t row = (g0 + g) * R + r;
+        if (row >= N) continue;
+        float sum = 0.f;
+        for (int t = 0; t < tpg; ++t) sum += part[((g * tpg + t) * R + r) * C + c];
+        const float s = __bfloat162float(scale[row]), z = __bfloat162float(zero[row]);
+        d[c * N + row] = __float2bfloat16_rn(s * fmaf(-z, S[c], sum));
     }
 }
 
@@ -212,15 +251,17 @@ w4_status launch_w4a8(const void* qw, const void* scale, const void* zero, const
     int per_sm = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, WA_THREADS, smem) != cudaSuccess || per_sm < 1)
         return W4_ERR_CUDA;
-    const int64_t warps_needed = (N + (C <= 4 ? 4 : 2) - 1) / (C <= 4 ? 4 : 2), warps_per_cta = WA_THREADS / 32;
-    int64_t blocks = int64_t(sm_count()) * per_sm;
-    const int64_t max_useful = (warps_needed + warps_per_cta - 1) / warps_per_cta;
-    if (blocks > max_useful) blocks = max_useful;
-    if (blocks < 1) blocks = 1;
-    kern<<<static_cast<unsigned>(blocks), WA_THREADS, smem, stream>>>(
+    // as many CTAs as are resident at once, each a contiguous range of row groups
+    const int64_t groups = (N + w4a8_rows(C) - 1) / w4a8_rows(C);
+    int64_t ctas = int64_t(sm_count()) * per_sm;
+    if (ctas > groups) ctas = groups;
+    if (ctas < 1) ctas = 1;
+    const int64_t G = groups > 0 ? (groups + ctas - 1) / ctas : 1;
+    ctas = groups > 0 ? (groups + G - 1) / G : 1;
+    kern<<<static_cast<unsigned>(ctas), WA_THREADS, smem, stream>>>(
         static_cast<const uint32_t*>(qw), static_cast<const __nv_bfloat16*>(scale),
         static_cast<const __nv_bfloat16*>(zero), static_cast<const uint8_t*>(pt), static_cast<__nv_bfloat16*>(d), N,
-        K);
+        K, G);
     return launch_status(cudaGetLastError());
 }
 
