@@ -94,6 +94,60 @@ permute_int8_kernel(const uint8_t* __restrict__ q, uint8_t* __restrict__ out, in
     for (int i = 0; i < 8; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
 }
 
+// Tiled variant (N % 16 == 0): a CTA of 128 threads takes 64 rows x 128
+// columns.  The tile comes in by coalesced 16-byte loads (row-major, 16-byte
+// chunks of row r at chunk c ^ 2((r / 16) % 4), so that the reads below hit
+// 32 different banks).  Thread (q, m) -- column quad q, 16-row group m --
+// then builds, for each of its four columns, the 16 bytes of the column's
+// group m in the line: output word w holds rows 2w, 2w+8, 2w+1, 2w+9 (the
+// permute_kk order), so four 32-bit reads of those rows and a 4 x 4 byte
+// transpose (eight byte permutes) give word w of all four columns.  The
+// four adjacent m of a warp write 64 contiguous bytes of each line.
+constexpr int P8_ROWS = 64, P8_COLS = 128, P8_THREADS = 128;
+
+__global__ void __launch_bounds__(P8_THREADS)
+permute_int8_tiled_kernel(const uint8_t* __restrict__ q, uint8_t* __restrict__ out, int64_t K, int64_t N) {
+    __shared__ __align__(16) uint8_t tile[P8_ROWS * P8_COLS];
+    const int64_t n_tiles = (N + P8_COLS - 1) / P8_COLS;
+    const int64_t tn = blockIdx.x % n_tiles, j = blockIdx.x / n_tiles;   // column tile, 64-row line
+    const int64_t c0 = tn * P8_COLS;
+    const int valid = static_cast<int>(N - c0 < P8_COLS ? N - c0 : P8_COLS);   // multiple of 16
+#pragma unroll
+    for (int i = 0; i < P8_ROWS * P8_COLS / 16 / P8_THREADS; ++i) {
+        const int t = threadIdx.x + i * P8_THREADS;
+        const int r = t >> 3, c = t & 7;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (16 * c < valid) v = ldg_stream_u4(q + (64 * j + r) * N + c0 + 16 * c);
+        *reinterpret_cast<uint4*>(tile + r * P8_COLS + 16 * (c ^ (2 * ((r >> 4) & 3)))) = v;
+    }
+    __syncthreads();
+    const int lane = threadIdx.x & 31;
+    const int m = lane & 3, qd = (threadIdx.x >> 5) * 8 + (lane >> 2);   // 16-row group, column quad
+    const int sw = 8 * m;                                                  // word swizzle of rows 16m..
+    uint32_t col[4][4];   // [column of the quad][output word]
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        const int rbase = 16 * m + 2 * w;
+        const uint32_t* rw = reinterpret_cast<const uint32_t*>(tile);
+        const uint32_t a = rw[(rbase) * 32 + (qd ^ sw)], b = rw[(rbase + 8) * 32 + (qd ^ sw)];
+        const uint32_t c = rw[(rbase + 1) * 32 + (qd ^ sw)], d = rw[(rbase + 9) * 32 + (qd ^ sw)];
+        const uint32_t t0 = __byte_perm(a, b, 0x5140), t1 = __byte_perm(a, b, 0x7362);
+        const uint32_t t2 = __byte_perm(c, d, 0x5140), t3 = __byte_perm(c, d, 0x7362);
+        col[0][w] = __byte_perm(t0, t2, 0x5410);
+        col[1][w] = __byte_perm(t0, t2, 0x7632);
+        col[2][w] = __byte_perm(t1, t3, 0x5410);
+        col[3][w] = __byte_perm(t1, t3, 0x7632);
+    }
+#pragma unroll
+    for (int cc = 0; cc < 4; ++cc) {
+        const int nl = 4 * qd + cc;   // column within the tile
+        if (nl >= valid) break;
+        const int64_t n = c0 + nl;
+        uint8_t* dst = out + K * 2 * (n / 2) + 128 * j + 64 * (n % 2) + 16 * m;
+        *reinterpret_cast<uint4*>(dst) = make_uint4(col[cc][0], col[cc][1], col[cc][2], col[cc][3]);
+    }
+}
+
 // d[c][n] = bf16(scale[n] * sum_k q[k][n] * x[c][k]), fp32 accumulation.
 // A CTA takes 32 columns; its 8 warps take every 8th row of K, so each warp
 // reads 32 contiguous bytes of q per row and one broadcast x value per
@@ -320,147 +374,15 @@ w4_status launch_w8_fast(const void* q, const float* scale, const void* x, void*
                                             K, static_cast<int>(S)));
 }
 
-// ---------------------------------------------------------------------------
-// Single-read quantiser (N % 8 == 0, K <= Q8C_MAX_K): a cluster of
-// Q8C_CTAS CTAs takes a strip of 64 columns -- one 128-byte line of every
-// row of W -- and splits K; each CTA keeps its rows in shared memory, so W
-// is read once.  The column maxima of the CTAs meet through distributed
-// shared memory between two cluster barriers; every CTA then quantises its
-// own rows from shared memory (IEEE division, half-away rounding, as the
-// two-pass kernel) and rank 0 writes the scales.  2KN read + KN + 4N written.
-// ---------------------------------------------------------------------------
-
-constexpr int Q8C_CTAS = 8;
-constexpr int Q8C_THREADS = 256;
-constexpr int Q8C_COLS = 64;                       // bf16 columns of a strip (128 bytes)
-constexpr int Q8C_ROWS_MAX = 1600;                 // rows a CTA can hold (200 KB)
-constexpr int64_t Q8C_MAX_K = int64_t(Q8C_CTAS) * Q8C_ROWS_MAX;
-
-__host__ __device__ inline size_t q8c_smem_bytes(int64_t rows) {
-    return size_t(rows) * Q8C_COLS * 2 + Q8C_COLS * 4 * 2 + (Q8C_THREADS / 32) * Q8C_COLS * 4;
-}
-
-__global__ void __launch_bounds__(Q8C_THREADS, 1)
-quantize_int8_cluster_kernel(const uint16_t* __restrict__ W, int8_t* __restrict__ q, float* __restrict__ scale,
-                             int64_t K, int64_t N) {
-    extern __shared__ __align__(16) uint8_t smem[];
-    const int rank = static_cast<int>(blockIdx.x % Q8C_CTAS);
-    const int64_t strip = blockIdx.x / Q8C_CTAS;
-    const int64_t Kr = (K + Q8C_CTAS - 1) / Q8C_CTAS, k0 = rank * Kr, k1 = (k0 + Kr < K) ? k0 + Kr : K;
-    const int64_t rows = k1 > k0 ? k1 - k0 : 0;
-    uint16_t* tile = reinterpret_cast<uint16_t*>(smem);                                // [Kr][64]
-    uint32_t* cmax = reinterpret_cast<uint32_t*>(smem + size_t(Kr) * Q8C_COLS * 2);    // [64] this CTA's max
-    float* s_col = reinterpret_cast<float*>(cmax + Q8C_COLS);                          // [64] the scales
-    uint32_t* red = reinterpret_cast<uint32_t*>(s_col + Q8C_COLS);                     // [warp][64]
-
-    const int cq = threadIdx.x % 8, rl = threadIdx.x / 8;   // 8 columns, one of 32 row lanes
-    const int64_t n0 = strip * Q8C_COLS + cq * 8;
-    const bool live = n0 < N;                                // N % 8 == 0: all 8 columns exist
-    uint32_t m[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    constexpr int U = 8;
-    for (int64_t r0 = rl; r0 < rows; r0 += 32 * U) {
-        uint4 v[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int64_t r = r0 + 32 * u;
-            v[u] = (live && r < rows) ? ldg_stream_u4(W + (k0 + r) * N + n0) : make_uint4(0, 0, 0, 0);
-        }
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int64_t r = r0 + 32 * u;
-            if (r >= rows) break;
-            *reinterpret_cast<uint4*>(tile + r * Q8C_COLS + cq * 8) = v[u];
-            const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                m[2 * j] = max(m[2 * j], w[j] & 0x7FFFu);          // |w| as a bf16 bit pattern
-                m[2 * j + 1] = max(m[2 * j + 1], (w[j] >> 16) & 0x7FFFu);
-            }
-        }
-    }
-    // the CTA's column maxima: the warp's four row lanes by shuffles, then the warps
-    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        uint32_t x = m[j];
-        x = max(x, __shfl_xor_sync(0xFFFFFFFFu, x, 8));
-        x = max(x, __shfl_xor_sync(0xFFFFFFFFu, x, 16));
-        if (lane < 8) red[warp * Q8C_COLS + cq * 8 + j] = x;
-    }
-    __syncthreads();
-    if (threadIdx.x < Q8C_COLS) {
-        uint32_t x = 0;
-        for (int wi = 0; wi < Q8C_THREADS / 32; ++wi) x = max(x, red[wi * Q8C_COLS + threadIdx.x]);
-        cmax[threadIdx.x] = x;
-    }
-    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-    if (threadIdx.x < Q8C_COLS) {
-        uint32_t x = 0;
-        const uint32_t local = static_cast<uint32_t>(__cvta_generic_to_shared(cmax + threadIdx.x));
-        for (int r = 0; r < Q8C_CTAS; ++r) {
-            uint32_t v;
-            asm volatile("{\n\t.reg .b32 a;\n\tmapa.shared::cluster.u32 a, %1, %2;\n\tld.shared::cluster.u32 %0, [a];\n\t}"
-                         : "=r"(v) : "r"(local), "r"(r) : "memory");
-            x = max(x, v);
-        }
-        const float sc = __fdiv_rn(bf16_bits_to_f32(x), 127.0f);
-        s_col[threadIdx.x] = sc;
-        const int64_t n = strip * Q8C_COLS + threadIdx.x;
-        if (rank == 0 && n < N) scale[n] = sc;
-    }
-    __syncthreads();
-    if (live) {
-        float sc[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) sc[j] = s_col[cq * 8 + j];
-        for (int64_t r = rl; r < rows; r += 32) {
-            const uint4 v = *reinterpret_cast<const uint4*>(tile + r * Q8C_COLS + cq * 8);
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-            uint32_t out[2] = {0, 0};
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const uint32_t bits = (j % 2 == 0) ? (w[j / 2] & 0xFFFFu) : (w[j / 2] >> 16);
-                const int8_t qq = quant8(bf16_bits_to_f32(bits), sc[j]);
-                out[j / 4] |= (static_cast<uint32_t>(static_cast<uint8_t>(qq))) << (8 * (j % 4));
-            }
-            *reinterpret_cast<uint2*>(q + (k0 + r) * N + n0) = make_uint2(out[0], out[1]);
-        }
-    }
-    // keep this CTA's maxima readable until every peer has read them
-    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-w4_status launch_quantize_int8_cluster(const void* W, void* q, float* scale, int64_t K, int64_t N,
-                                       cudaStream_t stream) {
-    const int64_t strips = (N + Q8C_COLS - 1) / Q8C_COLS;
-    const int64_t Kr = (K + Q8C_CTAS - 1) / Q8C_CTAS;
-    const size_t smem = q8c_smem_bytes(Kr);
-    if (strips * Q8C_CTAS > 0x7FFFFFFF) return W4_ERR_SHAPE;
-    static int smem_set[64];
-    if (ensure_smem_limit(quantize_int8_cluster_kernel, static_cast<int>(smem), smem_set) != cudaSuccess)
-        return W4_ERR_CUDA;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(strips * Q8C_CTAS), 1, 1);
-    cfg.blockDim = dim3(Q8C_THREADS, 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = Q8C_CTAS;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return launch_status(cudaLaunchKernelEx(&cfg, quantize_int8_cluster_kernel, static_cast<const uint16_t*>(W),
-                                            static_cast<int8_t*>(q), scale, K, N));
-}
-
 }  // namespace
 
+// the single-read quantiser shared with quantize_pack_int4 (quant_permute.cu)
+w4_status run_quantize_int8_single_read(const void* W, void* q, float* scale, int64_t K, int64_t N,
+                                        cudaStream_t stream);
+
 w4_status run_quantize_int8(const void* W, void* q, float* scale, int64_t K, int64_t N, cudaStream_t stream) {
-    if (N % 8 == 0 && K <= Q8C_MAX_K) return launch_quantize_int8_cluster(W, q, scale, K, N, stream);
+    const w4_status st = run_quantize_int8_single_read(W, q, scale, K, N, stream);
+    if (st != W4_ERR_SHAPE) return st;
     const int64_t strips = (N + Q8_COLS - 1) / Q8_COLS;
     if (strips > 0x7FFFFFFF) return W4_ERR_SHAPE;
     quantize_int8_kernel<<<static_cast<unsigned>(strips), Q8_COLS * Q8_LANES, 0, stream>>>(
@@ -469,6 +391,14 @@ w4_status run_quantize_int8(const void* W, void* q, float* scale, int64_t K, int
 }
 
 w4_status run_permute_int8(const void* q, void* out, int64_t K, int64_t N, cudaStream_t stream) {
+    if (N % 16 == 0) {
+        const int64_t tiles = (N + P8_COLS - 1) / P8_COLS * (K / 64);
+        if (tiles > 0x7FFFFFFF) return W4_ERR_SHAPE;
+        if (tiles == 0) return W4_OK;
+        permute_int8_tiled_kernel<<<static_cast<unsigned>(tiles), P8_THREADS, 0, stream>>>(
+            static_cast<const uint8_t*>(q), static_cast<uint8_t*>(out), K, N);
+        return launch_status(cudaGetLastError());
+    }
     const int64_t work = (N / 2) * (K / 64);
     const int64_t blocks = (work + 127) / 128;
     if (blocks > 0x7FFFFFFF) return W4_ERR_SHAPE;

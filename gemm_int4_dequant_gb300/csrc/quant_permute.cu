@@ -81,6 +81,27 @@ __device__ __forceinline__ bool quant_near(uint32_t u) { return (u & 0xFFFCu) ==
 constexpr float QB_HI = 192.50003051757812f;   // 192.5 + 2^-15
 constexpr float QB_LO = 192.49996948242188f;   // 192.5 - 2^-15
 
+// int8 (quantize_int8: s = max|w| / 127, q = clamp(round_half_away(w / s),
+// -128, 127)) with the same bracket one binade higher:
+//   u_hi / u_lo = fl(w * inv + 384.5 +/- 2^-13),  inv = fl(1/s).
+// |w / s| <= 127 (1 + 2^-23), so u lies in [256, 512), ulp 2^-15, and the
+// integer part F of u sits in mantissa bits 15..22 (F - 256).  w * inv is
+// within 127 * 2^-24 of w / s and fl(w / s) within 2^-18 of it, and each FMA
+// rounds by at most 2^-16: if both brackets have the integer part F, then
+// fl(w / s) + 0.5 lies strictly inside (F - 384, F - 383), so
+// round_half_away(fl(w / s)) = F - 384 (never 128: |fl(w / s)| < 127.5), the
+// byte ((u >> 15) & 0xFF) ^ 0x80.  Otherwise the weight takes the exact
+// division.
+constexpr float QB8_HI = 384.50012207031250f;   // 384.5 + 2^-13
+constexpr float QB8_LO = 384.49987792968750f;   // 384.5 - 2^-13
+
+__device__ __forceinline__ uint32_t quant_byte_exact(uint32_t wbits, float s) {
+    const float w = bf16_bits_to_f32(wbits & 0xFFFFu);
+    float r = (s == 0.0f) ? 0.0f : roundf(__fdiv_rn(w, s));
+    r = fminf(fmaxf(r, -128.0f), 127.0f);
+    return static_cast<uint32_t>(static_cast<int>(r)) & 0xFFu;
+}
+
 // Byte 2 of a and byte 2 of b in bytes 0, 1 (sel 0x0062) or 2, 3 (sel 0x6200).
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) { return __byte_perm(a, b, sel); }
 
@@ -106,7 +127,8 @@ __device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
 // directly: for column n and 32-row group t the 16 bytes at
 // (K/2)*4*(n/4) + (t/2)*128 + 32*(n%4) + 16*(t%2), whose 32-bit word i holds
 // in nibble slots 0..7 the rows 32t + 2i + (0, 8, 16, 24, 1, 9, 17, 25).
-template <bool PERMUTED>
+// INT8 = true (quantize_int8): `out` is q int8 [K][N], scale = max / 127.
+template <bool PERMUTED, bool INT8 = false>
 __global__ void __launch_bounds__(QC_THREADS)
 quantize_pack_cluster_kernel(const __grid_constant__ CUtensorMap tmap, uint8_t* __restrict__ out,
                              float* __restrict__ scale, int K, int N, int R, int box) {
@@ -199,7 +221,7 @@ quantize_pack_cluster_kernel(const __grid_constant__ CUtensorMap tmap, uint8_t* 
     if (tid < QC_COLS) {
         uint32_t m = 0;
         for (int r = 0; r < cs; ++r) m = max(m, pm_all[r][tid]);
-        const float sc = __fdiv_rn(bf16_bits_to_f32(m), 7.0f);
+        const float sc = __fdiv_rn(bf16_bits_to_f32(m), INT8 ? 127.0f : 7.0f);
         s_scale[tid] = sc;
         s_inv[tid] = sc == 0.0f ? 0.0f : __frcp_rn(sc);
         if (rank == 0 && n0 + tid < N) scale[n0 + tid] = sc;
@@ -311,6 +333,52 @@ quantize_pack_cluster_kernel(const __grid_constant__ CUtensorMap tmap, uint8_t* 
                     d[0] = res[0];
                     d[1] = res[1];
                 }
+            }
+        }
+        return;
+    }
+
+    if constexpr (INT8) {
+        // int8: thread (g, rl) takes the 8 columns of group g on rows rl,
+        // rl + QC_RL, ... (a warp: 8 consecutive rows), brackets each weight
+        // with two FMAs and stores 8 bytes per row; near-ties and columns
+        // whose scale has no finite reciprocal take the exact division.
+        // Control flow is warp-uniform, as below.
+        if (__all_sync(0xffffffffu, ok)) {
+            const bool col_ok = n0 + 8 * g < N;
+            float inv[8];
+            uint32_t tinymask = 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                inv[j] = s_inv[8 * g + j];
+                if (isinf(inv[j])) tinymask |= 1u << j;
+            }
+            for (int r0 = rl & ~7; r0 < rows; r0 += QC_RL) {
+                const int r = r0 + (rl & 7);
+                const uint8_t* ra = qtile + min(r, rows - 1) * (QC_COLS * 2) + g * 16;
+                const uint4 a = *reinterpret_cast<const uint4*>(ra);
+                const uint32_t wa[4] = {a.x, a.y, a.z, a.w};
+                uint32_t res[2] = {0, 0}, nearmask = tinymask;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const float w = __uint_as_float((j & 1) ? (wa[j / 2] & 0xFFFF0000u) : (wa[j / 2] << 16));
+                    const uint32_t uh = __float_as_uint(__fmaf_rn(w, inv[j], QB8_HI));
+                    const uint32_t ul = __float_as_uint(__fmaf_rn(w, inv[j], QB8_LO));
+                    res[j / 4] |= (((uh >> 15) & 0xFFu) ^ 0x80u) << (8 * (j % 4));
+                    nearmask |= ((uh >> 15) != (ul >> 15) ? 1u : 0u) << j;
+                }
+                if (__any_sync(0xffffffffu, nearmask != 0)) {
+                    while (nearmask != 0) {
+                        const int j = __ffs(nearmask) - 1;
+                        nearmask &= nearmask - 1;
+                        const uint32_t e = reinterpret_cast<const uint16_t*>(ra)[j];
+                        const int pos = 8 * (j & 3);
+                        res[j / 4] = (res[j / 4] & ~(0xFFu << pos)) | (quant_byte_exact(e, s_scale[8 * g + j]) << pos);
+                    }
+                }
+                if (col_ok && r < rows)
+                    *reinterpret_cast<uint2*>(out + (static_cast<int64_t>(k0) + r) * N + n0 + 8 * g) =
+                        make_uint2(res[0], res[1]);
             }
         }
         return;
@@ -471,9 +539,10 @@ quantize_pack_kernel(const uint16_t* __restrict__ W, uint8_t* __restrict__ packe
 namespace {
 
 // Single-read path; W4_ERR_SHAPE means "use the two-pass kernel".
-// permuted = true writes permute_int4's layout (requires K % 64 == 0).
+// mode 0: packed int4; 1: permute_int4's layout (requires K % 64 == 0);
+// 2: int8 (quantize_int8).
 w4_status launch_quantize_cluster(const void* W, void* packed, float* scale, int64_t K, int64_t N,
-                                  cudaStream_t stream, bool permuted) {
+                                  cudaStream_t stream, int mode) {
     if ((N % 8) != 0 || K > QC_MAX_K || N > 0x7FFFFFFF) return W4_ERR_SHAPE;
     const int64_t strips = (N + QC_COLS - 1) / QC_COLS;
     // rows per CTA: whole TMA boxes, 1024 rows (64 KB) per CTA while the
@@ -503,9 +572,10 @@ w4_status launch_quantize_cluster(const void* W, void* packed, float* scale, int
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return W4_ERR_CUDA;
     const int smem = R * QC_COLS * 2;
-    static int smem_set[2][64];
-    auto kern = permuted ? quantize_pack_cluster_kernel<true> : quantize_pack_cluster_kernel<false>;
-    if (ensure_smem_limit(kern, smem, smem_set[permuted ? 1 : 0]) != cudaSuccess) return W4_ERR_CUDA;
+    static int smem_set[3][64];
+    auto kern = mode == 1 ? quantize_pack_cluster_kernel<true>
+                : mode == 2 ? quantize_pack_cluster_kernel<false, true> : quantize_pack_cluster_kernel<false>;
+    if (ensure_smem_limit(kern, smem, smem_set[mode]) != cudaSuccess) return W4_ERR_CUDA;
     if (cs > 8 && cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
         return W4_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
@@ -528,7 +598,7 @@ w4_status launch_quantize_cluster(const void* W, void* packed, float* scale, int
 
 w4_status run_quantize_pack(const void* W, void* packed, float* scale, int64_t K, int64_t N,
                             cudaStream_t stream) {
-    const w4_status st = launch_quantize_cluster(W, packed, scale, K, N, stream, false);
+    const w4_status st = launch_quantize_cluster(W, packed, scale, K, N, stream, 0);
     if (st != W4_ERR_SHAPE) return st;
     const int64_t strips = (N + QP_COLS - 1) / QP_COLS;
     if (strips > 0x7FFFFFFF) return W4_ERR_SHAPE;
@@ -739,7 +809,14 @@ w4_status run_permute(const void* packed, void* out, int64_t K, int64_t N, cudaS
 w4_status run_quantize_pack_permute(const void* W, void* out, float* scale, int64_t K, int64_t N,
                                     cudaStream_t stream) {
     if ((K % 64) != 0) return W4_ERR_SHAPE;
-    return launch_quantize_cluster(W, out, scale, K, N, stream, true);
+    return launch_quantize_cluster(W, out, scale, K, N, stream, 1);
+}
+
+// quantize_int8 through the single-read kernel; W4_ERR_SHAPE: the caller's
+// two-pass kernel (N % 8 != 0 or K > W4_QUANT_PERMUTE_MAX_K)
+w4_status run_quantize_int8_single_read(const void* W, void* q, float* scale, int64_t K, int64_t N,
+                                        cudaStream_t stream) {
+    return launch_quantize_cluster(W, q, scale, K, N, stream, 2);
 }
 
 int take_device_error_quant() { return take_unit_device_error(); }

@@ -396,8 +396,8 @@ def test_gemm_k_zero(w4):
 @pytest.mark.parametrize("K,N", [
     (64, 2), (130, 37),                       # N % 8 != 0: the two-pass kernel
     (1, 8), (7, 120),                         # single-read clusters: ranks without rows; a partial strip
-    (1024, 1000), (8192, 8192), (12800, 72),  # ... up to the longest K a cluster holds
-    (12808, 16),                              # one step past it: the two-pass kernel again
+    (1024, 1000), (8192, 8192), (26624, 72),  # ... up to the longest K a cluster holds
+    (26626, 16),                              # one step past it: the two-pass kernel again
 ])
 def test_quantize_int8_bit_exact(w4, K, N):
     W = synth.quant_inputs(K, N, seed=K + 5 * N)
@@ -416,7 +416,10 @@ def test_quantize_int8_bit_exact(w4, K, N):
     assert _guards_intact(buf, pad, K * N, 91)
 
 
-@pytest.mark.parametrize("K,N", [(64, 2), (128, 6), (1024, 1000), (4160, 1042)])
+@pytest.mark.parametrize("K,N", [
+    (64, 2), (128, 6), (1024, 1000), (4160, 1042),   # N % 16 != 0: one thread per line
+    (64, 16), (4160, 1040), (1024, 4096),            # tiles of 64 x 128 (a partial last tile)
+])
 def test_permute_int8_bit_exact(w4, K, N):
     g = torch.Generator().manual_seed(K * 3 + N)
     q = torch.randint(-128, 128, (K, N), dtype=torch.int16, generator=g).to(torch.int8)

@@ -114,7 +114,8 @@ def test_every_bf16_weight_quantise_and_permute_in_one_pass(w4, weights):
 
 
 # int8 variant (the int4 definition with the int8 range: s = max|W| / 127,
-# q = clamp(round(W / s), -128, 127)); its single-read kernel holds K <= 12800
+# q = clamp(round(W / s), -128, 127)); columns of 12800 rows stay within the
+# single-read kernel's K limit (26624)
 K8 = 12800
 
 
