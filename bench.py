@@ -267,6 +267,8 @@ KERNEL_SOURCES = {
     "w4a8": ["gemm_int4_dequant_gb300/csrc/w4a8.cu", "gemm_int4_dequant_gb300/csrc/common.cuh"],
     "ptq1": ["gemm_int4_dequant_gb300/csrc/ptq1.cu", "gemm_int4_dequant_gb300/csrc/ptx.cuh",
              "gemm_int4_dequant_gb300/csrc/common.cuh"],
+    "quant8": ["gemm_int4_dequant_gb300/csrc/quant_permute.cu", "gemm_int4_dequant_gb300/csrc/int8.cu",
+               "gemm_int4_dequant_gb300/csrc/ptx.cuh", "gemm_int4_dequant_gb300/csrc/common.cuh"],
 }
 
 
@@ -275,7 +277,8 @@ KERNEL_SOURCES = {
 PROFILE_FILES = {"decode": "gemv_decode_ncu.md", "gemm": "gemm_8192_ncu.md", "quant": "quant_8192_ncu.md",
                  "c8_perm": "gemv_perm_c8_ncu.md", "c8": "gemv_c8_ncu.md", "c8s": "gemv_c8s_ncu.md",
                  "w8_decode": "gemv_w8_decode_ncu.md", "w4a8_decode": "gemv_w4a8_decode_ncu.md",
-                 "ptq1_decode": "mmvq_ptq1_decode_ncu.md"}
+                 "ptq1_decode": "mmvq_ptq1_decode_ncu.md", "w4a8_c8": "gemv_w4a8_c8_ncu.md",
+                 "ptq1_c8": "mmvq_ptq1_c8_ncu.md", "w8_quant": "quant8_8192_ncu.md"}
 
 
 def recorded_traffic(kind, workload):
