@@ -168,37 +168,56 @@ gemv_w4a8_kernel(const uint32_t* __restrict__ qw, const __nv_bfloat16* __restric
 #pragma unroll
             for (int c = 0; c < C; ++c) acc[r][c] = 0.f;
         const int nbi = static_cast<int>(nb);
-        for (int b0 = j; b0 < nbi; b0 += tpg * BATCH) {
-            uint4 w[BATCH][R];
+        // BATCH chunks per row in flight; with several columns the chunk
+        // BATCH places ahead is requested as soon as a chunk's registers are
+        // free (one column: 64 registers, load then compute)
+        uint4 w[BATCH][R];
+        auto fetch = [&](int u, int b) {
 #pragma unroll
-            for (int u = 0; u < BATCH; ++u) {
-                const int b = b0 + tpg * u;
+            for (int r = 0; r < R; ++r)
+                w[u][r] = (b < nbi && r < nrow) ? ldg_stream_u4(row0 + r * (K / 2) + 16 * b) : make_uint4(0, 0, 0, 0);
+        };
+        auto chunk = [&](int u, int b) {
 #pragma unroll
-                for (int r = 0; r < R; ++r)
-                    w[u][r] = (b < nbi && r < nrow) ? ldg_stream_u4(row0 + r * (K / 2) + 16 * b) : make_uint4(0, 0, 0, 0);
-            }
+            for (int c = 0; c < C; ++c) {
+                const uint4 x0 = *reinterpret_cast<const uint4*>(xs + c * xstride + 16 * b);
+                const uint4 x1 = *reinterpret_cast<const uint4*>(xs + c * xstride + xhalf + 16 * b);
+                const uint32_t xe[4] = {x0.x, x0.z, x1.x, x1.z};
+                const uint32_t xo[4] = {x0.y, x0.w, x1.y, x1.w};
+                const float dbc = db[c * nbi + b];
 #pragma unroll
-            for (int u = 0; u < BATCH; ++u) {
-                const int b = b0 + tpg * u;
-                if (b >= nbi) break;
+                for (int r = 0; r < R; ++r) {
+                    const uint32_t ww[4] = {w[u][r].x, w[u][r].y, w[u][r].z, w[u][r].w};
+                    int dot = 0;
 #pragma unroll
-                for (int c = 0; c < C; ++c) {
-                    const uint4 x0 = *reinterpret_cast<const uint4*>(xs + c * xstride + 16 * b);
-                    const uint4 x1 = *reinterpret_cast<const uint4*>(xs + c * xstride + xhalf + 16 * b);
-                    const uint32_t xe[4] = {x0.x, x0.z, x1.x, x1.z};
-                    const uint32_t xo[4] = {x0.y, x0.w, x1.y, x1.w};
-                    const float dbc = db[c * nbi + b];
-#pragma unroll
-                    for (int r = 0; r < R; ++r) {
-                        const uint32_t ww[4] = {w[u][r].x, w[u][r].y, w[u][r].z, w[u][r].w};
-                        int dot = 0;
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            dot = __dp4a(static_cast<int>(ww[q] & 0x0F0F0F0Fu), static_cast<int>(xe[q]), dot);
-                            dot = __dp4a(static_cast<int>((ww[q] >> 4) & 0x0F0F0F0Fu), static_cast<int>(xo[q]), dot);
-                        }
-                        acc[r][c] = fmaf(dbc, static_cast<float>(dot), acc[r][c]);
+                    for (int q = 0; q < 4; ++q) {
+                        dot = __dp4a(static_cast<int>(ww[q] & 0x0F0F0F0Fu), static_cast<int>(xe[q]), dot);
+                        dot = __dp4a(static_cast<int>((ww[q] >> 4) & 0x0F0F0F0Fu), static_cast<int>(xo[q]), dot);
                     }
+                    acc[r][c] = fmaf(dbc, static_cast<float>(dot), acc[r][c]);
+                }
+            }
+        };
+        if constexpr (C == 1) {
+            for (int b0 = j; b0 < nbi; b0 += tpg * BATCH) {
+#pragma unroll
+                for (int u = 0; u < BATCH; ++u) fetch(u, b0 + tpg * u);
+#pragma unroll
+                for (int u = 0; u < BATCH; ++u) {
+                    if (b0 + tpg * u >= nbi) break;
+                    chunk(u, b0 + tpg * u);
+                }
+            }
+        } else {
+#pragma unroll
+            for (int u = 0; u < BATCH; ++u) fetch(u, j + tpg * u);
+            for (int b0 = j; b0 < nbi; b0 += tpg * BATCH) {
+#pragma unroll
+                for (int u = 0; u < BATCH; ++u) {
+                    const int b = b0 + tpg * u;
+                    if (b >= nbi) break;
+                    chunk(u, b);
+                    fetch(u, b + tpg * BATCH);
                 }
             }
         }
