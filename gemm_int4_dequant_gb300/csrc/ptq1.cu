@@ -53,13 +53,15 @@ __device__ __forceinline__ void digits16(uint32_t x, uint32_t (&u)[5]) {
     u[4] = q;
 }
 
-// Digit p of each byte of w (bytes 0..242), as the bytes of u[p].
+// Digit p of each byte of w (bytes 0..242), as the bytes of u[p]: bytes 0, 2
+// and 1, 3 go to the low bytes of two words' 16-bit lanes, and the digit
+// words are interleaved back, each by one byte permute.
 __device__ __forceinline__ void trit_digits(uint32_t w, uint32_t (&u)[5]) {
     uint32_t ue[5], uo[5];
-    digits16(w & 0x00FF00FFu, ue);
-    digits16((w >> 8) & 0x00FF00FFu, uo);
+    digits16(__byte_perm(w, 0u, 0x4240), ue);
+    digits16(__byte_perm(w, 0u, 0x4341), uo);
 #pragma unroll
-    for (int p = 0; p < 5; ++p) u[p] = ue[p] | (uo[p] << 8);
+    for (int p = 0; p < 5; ++p) u[p] = __byte_perm(ue[p], uo[p], 0x6240);
 }
 
 // The four 2-bit fields of b (bits 0..7) as the four bytes of a word.
