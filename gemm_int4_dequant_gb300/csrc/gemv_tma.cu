@@ -974,8 +974,17 @@ Plan make_plan(int N, int K, int sms, int max_clusters_for_S /* 0: unknown */, i
 #ifdef W4_GEMV_FORCE_S
     if (!S_forced) S_forced = W4_GEMV_FORCE_S;
 #endif
-    if (S_forced) S = S_forced;
-    else while (S < 8 && xf_bytes(S) > kXfBudget) S *= 2;
+    if (S_forced) {
+        S = S_forced;
+    } else {
+        while (S < 8 && xf_bytes(S) > kXfBudget) S *= 2;
+        // one more split halves every CTA's x staging; worth it when the staging
+        // holds more than 8 entries per consumer thread and a stage still gives
+        // every consumer warp 2.5 units or more (N=5120 K=17280 C=4: 15.2 ->
+        // 14.4 us; thinner stages cost more than the staging saved)
+        if (!PERM && S < 8 && xf_bytes(S) > static_cast<size_t>(8) * CT * 16 && 2 * (slice_of(2 * S) / KB) >= 5 * NC)
+            S *= 2;
+    }
     P.S = S;
     P.kslice = slice_of(S);
     // Row groups own whole 16-row tiles (a partial tile costs a full stage of
