@@ -50,6 +50,8 @@ def _case(N, K, C, seed):
     (17280, 5120, 1),                 # decode shape of the page's model
     (6144, 5120, 8), (5120, 17280, 4), (5120, 17280, 8),
     (37, 23168, 8),                   # the largest K whose x fits shared memory at C = 8
+    (10336, 4096, 2),                 # one warp per row group (partial sums by shuffles)
+    (320000, 128, 1),                 # more groups in a CTA than threads: threads take several groups
 ])
 def test_mmvq_ptq1_0(w4, N, K, C):
     blocks, xb = _case(N, K, C, seed=N + K + C)

@@ -71,6 +71,9 @@ def test_quantize_q8_1_pt_k_zero_is_a_no_op(w4):
     (17280, 5120, 1),     # decode shape
     (6144, 5120, 8), (5120, 17280, 4), (5120, 17280, 8),
     (37, 23168, 8),       # the largest K whose x fits shared memory at C = 8
+    (40000, 1024, 4),     # one warp per row group (partial sums by shuffles)
+    (200000, 256, 2),     # more groups in a CTA than half its threads: one thread per group
+    (700000, 128, 1),     # more groups in a CTA than threads: threads take several groups
 ])
 def test_gemv_w4a8(w4, N, K, C):
     g = synth.gemv_inputs(N, K, C, act="bf16", seed=N + K + C)
